@@ -1,0 +1,565 @@
+// ra_api.cpp -- the C ABI (include/ra.h): argument checks, plans, workspace
+// carving and the drivers of the simulated ring.  Host code only; every
+// step of the data path runs in the library's kernels.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "ra_internal.h"
+#include "ra_kernels.h"
+
+namespace ra {
+
+static thread_local std::string g_last_error;
+
+ra_status fail(ra_status s, const std::string &msg) {
+    g_last_error = msg;
+    return s;
+}
+
+static ra_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(RA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+#define RA_CUDA(call, what)                             \
+    do {                                                \
+        cudaError_t e_ = (call);                        \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static size_t esize(int dtype) { return dtype == RA_FP32 ? 4 : 2; }
+
+static ra_status check_common(int dtype, int Hq, int Hkv, int d) {
+    if (dtype != RA_BF16 && dtype != RA_FP32) return fail(RA_ERR_INVALID_ARG, "dtype must be RA_BF16 or RA_FP32");
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return fail(RA_ERR_INVALID_ARG, "Hq must be a positive multiple of Hkv");
+    if (d <= 0) return fail(RA_ERR_INVALID_ARG, "d must be positive");
+    if (d % 32 != 0 || d > 256) return fail(RA_ERR_UNSUPPORTED, "d must be a multiple of 32 and <= 256");
+    return RA_OK;
+}
+
+// Carves consecutive 256-byte aligned regions out of a workspace.
+struct Carver {
+    uint8_t *base;
+    size_t used = 0;
+    explicit Carver(void *b) : base(static_cast<uint8_t *>(b)) {}
+    void *take(size_t bytes) {
+        void *p = base ? base + used : nullptr;
+        used = align_up(used + bytes, 256);
+        return p;
+    }
+};
+
+}  // namespace ra
+
+using namespace ra;
+
+extern "C" {
+
+const char *ra_version(void) { return "libra 0.1 (sm_103a)"; }
+
+const char *ra_last_error(void) { return g_last_error.c_str(); }
+
+const char *ra_status_string(ra_status s) {
+    switch (s) {
+        case RA_OK: return "ok";
+        case RA_ERR_INVALID_ARG: return "invalid argument";
+        case RA_ERR_UNSUPPORTED: return "unsupported";
+        case RA_ERR_CUDA: return "CUDA error";
+        case RA_ERR_WORKSPACE: return "workspace too small";
+        case RA_ERR_TIMEOUT: return "device wait timed out";
+        case RA_ERR_DEVICE_BOUNDS: return "device index out of range";
+        default: return "unknown status";
+    }
+}
+
+ra_status ra_zigzag_plan(const int32_t *cu, int B, int cp, int mode, int32_t *perm, int32_t *off,
+                         int32_t *cu_local) {
+    if (!perm || !off || !cu_local) return fail(RA_ERR_INVALID_ARG, "output pointer is NULL");
+    ZigzagPlan zp;
+    ra_status st = build_zigzag(cu, B, cp, mode, zp);
+    if (st) return st;
+    std::memcpy(perm, zp.perm.data(), zp.perm.size() * 4);
+    std::memcpy(off, zp.off.data(), zp.off.size() * 4);
+    std::memcpy(cu_local, zp.cu_local.data(), zp.cu_local.size() * 4);
+    return RA_OK;
+}
+
+static ra_status permute_common(const void *src, void *dst, const int32_t *perm, int64_t T, int64_t row_bytes,
+                                void *stream, int inverse) {
+    if (T < 0 || row_bytes <= 0) return fail(RA_ERR_INVALID_ARG, "T must be >= 0 and row_bytes > 0");
+    if (T == 0) return RA_OK;
+    if (!src || !dst || !perm) return fail(RA_ERR_INVALID_ARG, "NULL pointer");
+    if (T > INT32_MAX) return fail(RA_ERR_UNSUPPORTED, "T must fit in int32");
+    PermJob job{src, dst, row_bytes};
+    RA_CUDA(launch_permute(&job, 1, perm, T, inverse, static_cast<cudaStream_t>(stream)), "permute launch");
+    return RA_OK;
+}
+
+ra_status ra_zigzag_permute(const void *x, void *y, const int32_t *perm, int64_t T, int64_t row_bytes,
+                            void *stream) {
+    return permute_common(x, y, perm, T, row_bytes, stream, 0);
+}
+
+ra_status ra_zigzag_unpermute(const void *y, void *x, const int32_t *perm, int64_t T, int64_t row_bytes,
+                              void *stream) {
+    return permute_common(y, x, perm, T, row_bytes, stream, 1);
+}
+
+ra_status ra_ring_rank_pairs(const int32_t *cu, int B, int cp, int mode, int causal, int64_t *counts) {
+    if (!counts) return fail(RA_ERR_INVALID_ARG, "counts is NULL");
+    ZigzagPlan zp;
+    ra_status st = build_zigzag(cu, B, cp, mode, zp);
+    if (st) return st;
+    for (int r = 0; r < cp; ++r) {
+        int64_t c = 0;
+        for (int b = 0; b < B; ++b) {
+            const int64_t lo = zp.off[r] + zp.cu_local[(size_t)r * (B + 1) + b];
+            const int64_t hi = zp.off[r] + zp.cu_local[(size_t)r * (B + 1) + b + 1];
+            const int64_t L = (int64_t)cu[b + 1] - cu[b];
+            for (int64_t i = lo; i < hi; ++i) c += causal ? (int64_t)zp.perm[i] - cu[b] + 1 : L;
+        }
+        counts[r] = c;
+    }
+    return RA_OK;
+}
+
+ra_status ra_get_device_status(void *stream) {
+    RA_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");
+    int *p = device_status_ptr();
+    if (!p) return fail(RA_ERR_CUDA, "status word unavailable");
+    int v = 0;
+    RA_CUDA(cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost), "status read");
+    if (v != 0) {
+        const int zero = 0;
+        RA_CUDA(cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice), "status clear");
+        return fail(v, std::string("device status: ") + ra_status_string(v));
+    }
+    return RA_OK;
+}
+
+ra_status ra_selftest_wait_timeout(int64_t budget_us, void *stream) {
+    if (budget_us < 1 || budget_us > 1000000) return fail(RA_ERR_INVALID_ARG, "budget_us must be in [1, 1e6]");
+    RA_CUDA(launch_wait_selftest((uint64_t)budget_us * 1000ull, static_cast<cudaStream_t>(stream)), "selftest launch");
+    return RA_OK;
+}
+
+// ---------------------------------------------------------------- merge
+ra_status ra_lse_merge(int n_parts, const float *const *outs, const float *const *lses, int64_t Tq, int Hq, int d,
+                       void *out, int out_dtype, float *lse_out, void *stream) {
+    if (n_parts < 1 || n_parts > kMaxMergeParts) return fail(RA_ERR_INVALID_ARG, "n_parts must be in [1, 64]");
+    if (!outs || !lses) return fail(RA_ERR_INVALID_ARG, "outs/lses is NULL");
+    if (Tq < 0 || Hq <= 0 || d <= 0) return fail(RA_ERR_INVALID_ARG, "bad shape");
+    if (d % 4 != 0 || d > 256) return fail(RA_ERR_UNSUPPORTED, "d must be a multiple of 4 and <= 256");
+    if (out_dtype != RA_BF16 && out_dtype != RA_FP32) return fail(RA_ERR_INVALID_ARG, "bad out_dtype");
+    if (Tq == 0) return RA_OK;
+    if (!out) return fail(RA_ERR_INVALID_ARG, "out is NULL");
+    for (int p = 0; p < n_parts; ++p) {
+        if (!outs[p] || !lses[p]) return fail(RA_ERR_INVALID_ARG, "NULL partial");
+        if (!aligned16(outs[p])) return fail(RA_ERR_UNSUPPORTED, "partial outputs must be 16-byte aligned");
+    }
+    if (!aligned16(out)) return fail(RA_ERR_UNSUPPORTED, "out must be 16-byte aligned");
+    RA_CUDA(launch_merge(n_parts, outs, lses, Tq, Hq, d, out, out_dtype, lse_out, static_cast<cudaStream_t>(stream)),
+            "merge launch");
+    return RA_OK;
+}
+
+// ---------------------------------------------------------------- partial
+size_t ra_partial_workspace_bytes(int64_t Tq, int64_t Tk, int nseg, int Hq, int Hkv, int d, int dtype) {
+    (void)d;
+    (void)dtype;
+    if (Tq < 0 || Tk < 0 || nseg < 1 || Hkv <= 0 || Hq <= 0) return 0;
+    // Upper bound over any positions: every tile holds at least one row.
+    const size_t qt = (size_t)Tq + nseg, kt = (size_t)Tk + nseg;
+    size_t s = 0;
+    s += align_up(qt * sizeof(Tile), 256) + align_up(kt * sizeof(Tile), 256);
+    s += 2 * align_up(((size_t)nseg + 2) * 4, 256);
+    s += align_up(((qt + 1) / 2 + nseg) * (size_t)Hkv * sizeof(WorkItem), 256);
+    s += align_up(((size_t)kt) * (size_t)Hkv * sizeof(WorkItem), 256);
+    // SIMT path: positions and offsets
+    s += align_up((size_t)Tq * 4, 256) + align_up((size_t)Tk * 4, 256) + 4 * align_up(((size_t)nseg + 2) * 4, 256);
+    return s + 4096;
+}
+
+ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, int dtype, int64_t Tq, int64_t Tk,
+                                 int Hq, int Hkv, int d, const int32_t *cu_q, const int32_t *cu_k, int nseg,
+                                 const int32_t *q_pos, const int32_t *k_pos, int causal, float scale, float *out,
+                                 float *lse, void *workspace, size_t ws_bytes, void *stream) {
+    ra_status st = check_common(dtype, Hq, Hkv, d);
+    if (st) return st;
+    if (Tq < 0 || Tk < 0 || Tq > INT32_MAX || Tk > INT32_MAX) return fail(RA_ERR_INVALID_ARG, "bad Tq/Tk");
+    if (nseg < 1) return fail(RA_ERR_INVALID_ARG, "nseg must be >= 1");
+    if ((st = validate_cu(cu_q, nseg, Tq))) return st;
+    if ((st = validate_cu(cu_k, nseg, Tk))) return st;
+    if (!std::isfinite(scale)) return fail(RA_ERR_INVALID_ARG, "scale must be finite");
+    if (Tq == 0) return RA_OK;
+    if (!q || !out || !lse || (Tk > 0 && (!k || !v))) return fail(RA_ERR_INVALID_ARG, "NULL tensor");
+    if (!aligned16(q) || !aligned16(out) || (Tk > 0 && (!aligned16(k) || !aligned16(v))))
+        return fail(RA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned");
+    const size_t need = ra_partial_workspace_bytes(Tq, Tk, nseg, Hq, Hkv, d, dtype);
+    if (!workspace || ws_bytes < need) return fail(RA_ERR_WORKSPACE, "workspace must be >= " + std::to_string(need));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int G = Hq / Hkv;
+    const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
+    Carver cv(workspace);
+    if (tc) {
+        TilePlan tp;
+        if ((st = build_partial_tiles(cu_q, cu_k, nseg, q_pos, k_pos, Tq, Tk, G, Hkv, causal, tp))) return st;
+        DeviceTables dt;
+        pack_tables(nullptr, &tp, dt);
+        void *tab = cv.take(dt.blob.size());
+        RA_CUDA(cudaMemcpyAsync(tab, dt.blob.data(), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
+        const uint8_t *tb = static_cast<const uint8_t *>(tab);
+        TcFwdArgs a{};
+        a.q = q;
+        a.k = k ? k : q;
+        a.v = v ? v : q;
+        a.Tq = Tq;
+        a.Tk = Tk;
+        a.Hq = Hq;
+        a.Hkv = Hkv;
+        a.G = G;
+        a.qtiles = tb + dt.o_qt;
+        a.kvtiles = tb + dt.o_kt;
+        a.kv_off = reinterpret_cast<const int32_t *>(tb + dt.o_kvoff);
+        a.items = tb + dt.o_items;
+        a.n_items = dt.n_items;
+        a.cp = 1;
+        a.B = nseg;
+        a.t0 = 0;
+        a.t1 = 1;
+        a.causal = causal;
+        a.scale = scale;
+        a.out_mode = kOutPartial;
+        a.out = out;
+        a.lse = lse;
+        a.lse_T = Tq;
+        RA_CUDA(launch_tc_fwd(a, s), "tensor-core partial launch");
+        return RA_OK;
+    }
+    // SIMT path: a one-rank ring with explicit position arrays.
+    std::vector<int32_t> qp((size_t)Tq), kp((size_t)Tk);
+    for (int64_t i = 0; i < Tq; ++i) qp[i] = q_pos ? q_pos[i] : (int32_t)i;
+    for (int64_t i = 0; i < Tk; ++i) kp[i] = k_pos ? k_pos[i] : (int32_t)i;
+    std::vector<int32_t> host;
+    const int32_t offq[2] = {0, (int32_t)Tq}, offk[2] = {0, (int32_t)Tk};
+    size_t o_qp = 0, o_kp, o_offq, o_offk, o_cuq, o_cuk;
+    auto put = [&](const int32_t *src, size_t n) {
+        size_t at = host.size();
+        host.insert(host.end(), src, src + n);
+        host.resize(align_up(host.size(), 64), 0);
+        return at;
+    };
+    o_qp = put(qp.data(), qp.size());
+    o_kp = put(kp.data(), kp.size());
+    o_offq = put(offq, 2);
+    o_offk = put(offk, 2);
+    o_cuq = put(cu_q, (size_t)nseg + 1);
+    o_cuk = put(cu_k, (size_t)nseg + 1);
+    int32_t *dh = static_cast<int32_t *>(cv.take(host.size() * 4));
+    RA_CUDA(cudaMemcpyAsync(dh, host.data(), host.size() * 4, cudaMemcpyHostToDevice, s), "table upload");
+    SimtArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.dtype = dtype;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.Tq = Tq;
+    a.Tk = Tk;
+    a.qoff = dh + o_offq;
+    a.qcul = dh + o_cuq;
+    a.qpos = dh + o_qp;
+    a.koff = dh + o_offk;
+    a.kcul = dh + o_cuk;
+    a.kpos = dh + o_kp;
+    a.cp = 1;
+    a.B = nseg;
+    a.t0 = 0;
+    a.t1 = 1;
+    a.causal = causal;
+    a.scale = scale;
+    a.out_mode = kOutPartial;
+    a.out = out;
+    a.lse = lse;
+    a.lse_T = Tq;
+    RA_CUDA(launch_simt_fwd(a, s), "SIMT partial launch");
+    return RA_OK;
+}
+
+// ---------------------------------------------------------------- ring
+namespace {
+
+struct RingLayout {
+    size_t total = 0;
+    size_t tables = 0, qp = 0, kp = 0, vp = 0;
+    // stepwise forward
+    size_t parts_o = 0, parts_l = 0, op = 0, lp = 0;
+    // backward
+    size_t dop = 0, Dv = 0, dq = 0, dk = 0, dv = 0;
+};
+
+RingLayout ring_layout(const RingPlan &plan, int64_t T, int Hq, int Hkv, int d, int dtype, int cp, int sched, int bwd) {
+    RingLayout L;
+    Carver c(nullptr);
+    auto at = [&](size_t bytes) {
+        size_t o = c.used;
+        c.take(bytes);
+        return o;
+    };
+    const size_t es = esize(dtype);
+    L.tables = at(plan.dev.blob.size());
+    L.qp = at((size_t)T * Hq * d * es);
+    L.kp = at((size_t)T * Hkv * d * es);
+    L.vp = at((size_t)T * Hkv * d * es);
+    if (!bwd && sched == RA_SCHED_STEPWISE) {
+        L.parts_o = at((size_t)cp * T * Hq * d * 4);
+        L.parts_l = at((size_t)cp * Hq * T * 4);
+        L.op = at((size_t)T * Hq * d * es);
+        L.lp = at((size_t)Hq * T * 4);
+    }
+    if (bwd) {
+        L.dop = at((size_t)T * Hq * d * es);
+        L.Dv = at((size_t)Hq * T * 4);
+        L.dq = at((size_t)T * Hq * d * 4);
+        L.dk = at((size_t)T * Hkv * d * 4);
+        L.dv = at((size_t)T * Hkv * d * 4);
+    }
+    L.total = c.used + 256;
+    return L;
+}
+
+ra_status ring_checks(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
+                      const int32_t *cu, int B, int cp, int mode, int sched, float scale) {
+    ra_status st = check_common(dtype, Hq, Hkv, d);
+    if (st) return st;
+    if (T < 0 || T > INT32_MAX) return fail(RA_ERR_INVALID_ARG, "T must be in [0, 2^31)");
+    if ((st = validate_cu(cu, B, T))) return st;
+    if (cp < 1 || cp > kMaxMergeParts) return fail(RA_ERR_INVALID_ARG, "cp must be in [1, 64]");
+    if (mode != RA_ZZ_GLOBAL && mode != RA_ZZ_PER_DOC) return fail(RA_ERR_INVALID_ARG, "unknown zigzag mode");
+    if (sched != RA_SCHED_FUSED && sched != RA_SCHED_STEPWISE) return fail(RA_ERR_INVALID_ARG, "unknown schedule");
+    if (!std::isfinite(scale)) return fail(RA_ERR_INVALID_ARG, "scale must be finite");
+    if (T > 0 && (!q || !k || !v)) return fail(RA_ERR_INVALID_ARG, "NULL tensor");
+    if (T > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v)))
+        return fail(RA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned");
+    return RA_OK;
+}
+
+}  // namespace
+
+size_t ra_ring_workspace_bytes(int64_t T, int Hq, int Hkv, int d, int dtype, const int32_t *cu, int B, int cp,
+                               int mode, int sched, int bwd) {
+    if (check_common(dtype, Hq, Hkv, d) != RA_OK || T < 0) return 0;
+    ra_status st;
+    const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
+    auto plan = get_ring_plan(cu, B, cp, mode, Hq / Hkv, Hkv, 1, tc, &st);
+    if (!plan) return 0;
+    return ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, bwd).total;
+}
+
+ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
+                           const int32_t *cu, int B, int cp, int mode, int causal, float scale, int sched, void *out,
+                           float *lse, void *workspace, size_t ws_bytes, void *stream) {
+    ra_status st = ring_checks(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, sched, scale);
+    if (st) return st;
+    if (T == 0) return RA_OK;
+    if (!out || !lse) return fail(RA_ERR_INVALID_ARG, "out/lse is NULL");
+    if (!aligned16(out)) return fail(RA_ERR_UNSUPPORTED, "out must be 16-byte aligned");
+    const int G = Hq / Hkv;
+    const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
+    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, 1, tc, &st);
+    if (!plan) return st;
+    const RingLayout L = ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, 0);
+    if (!workspace || ws_bytes < L.total)
+        return fail(RA_ERR_WORKSPACE, "workspace must be >= " + std::to_string(L.total) + " bytes");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const DeviceTables &dt = plan->dev;
+    uint8_t *tab = ws + L.tables;
+    RA_CUDA(cudaMemcpyAsync(tab, dt.blob.data(), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
+    const int32_t *perm = reinterpret_cast<const int32_t *>(tab + dt.o_perm);
+    const int32_t *off = reinterpret_cast<const int32_t *>(tab + dt.o_off);
+    const int32_t *cul = reinterpret_cast<const int32_t *>(tab + dt.o_cul);
+    const size_t es = esize(dtype);
+    void *Qp = ws + L.qp, *Kp = ws + L.kp, *Vp = ws + L.vp;
+    // a3: zigzag-permute Q, K, V into the ranks' shards (one launch)
+    PermJob jobs[3] = {{q, Qp, (int64_t)Hq * d * (int64_t)es},
+                       {k, Kp, (int64_t)Hkv * d * (int64_t)es},
+                       {v, Vp, (int64_t)Hkv * d * (int64_t)es}};
+    RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s), "permute launch");
+
+    auto run_partial = [&](int t0, int t1, int out_mode, void *o, float *l, int64_t lse_T) -> ra_status {
+        if (tc) {
+            TcFwdArgs a{};
+            a.q = Qp;
+            a.k = Kp;
+            a.v = Vp;
+            a.Tq = T;
+            a.Tk = T;
+            a.Hq = Hq;
+            a.Hkv = Hkv;
+            a.G = G;
+            a.qtiles = tab + dt.o_qt;
+            a.kvtiles = tab + dt.o_kt;
+            a.kv_off = reinterpret_cast<const int32_t *>(tab + dt.o_kvoff);
+            a.items = tab + dt.o_items;
+            a.n_items = dt.n_items;
+            a.cp = cp;
+            a.B = B;
+            a.t0 = t0;
+            a.t1 = t1;
+            a.causal = causal;
+            a.scale = scale;
+            a.out_mode = out_mode;
+            a.out = o;
+            a.lse = l;
+            a.lse_T = lse_T;
+            RA_CUDA(launch_tc_fwd(a, s), "tensor-core forward launch");
+        } else {
+            SimtArgs a{};
+            a.q = Qp;
+            a.k = Kp;
+            a.v = Vp;
+            a.dtype = dtype;
+            a.Hq = Hq;
+            a.Hkv = Hkv;
+            a.d = d;
+            a.Tq = T;
+            a.Tk = T;
+            a.qoff = off;
+            a.qcul = cul;
+            a.qpos = perm;
+            a.koff = off;
+            a.kcul = cul;
+            a.kpos = perm;
+            a.cp = cp;
+            a.B = B;
+            a.t0 = t0;
+            a.t1 = t1;
+            a.causal = causal;
+            a.scale = scale;
+            a.out_mode = out_mode;
+            a.out = o;
+            a.lse = l;
+            a.lse_T = lse_T;
+            RA_CUDA(launch_simt_fwd(a, s), "SIMT forward launch");
+        }
+        return RA_OK;
+    };
+
+    if (sched == RA_SCHED_FUSED) {
+        // a4+a5+a6 in one launch: ring order inside each tile, on-chip merge,
+        // rows written straight back to their original positions.
+        return run_partial(0, cp, kOutFinal, out, lse, T);
+    }
+    // STEPWISE: one launch per ring step into fp32 partials (local order),
+    // then the n-way LSE merge, then un-permute O and LSE.
+    std::vector<const float *> po((size_t)cp), pl((size_t)cp);
+    for (int t = 0; t < cp; ++t) {
+        float *o_t = reinterpret_cast<float *>(ws + L.parts_o) + (size_t)t * T * Hq * d;
+        float *l_t = reinterpret_cast<float *>(ws + L.parts_l) + (size_t)t * Hq * T;
+        if ((st = run_partial(t, t + 1, kOutPartial, o_t, l_t, T))) return st;
+        po[t] = o_t;
+        pl[t] = l_t;
+    }
+    void *Op = ws + L.op;
+    float *Lp = reinterpret_cast<float *>(ws + L.lp);
+    RA_CUDA(launch_merge(cp, po.data(), pl.data(), T, Hq, d, Op, dtype, Lp, s), "merge launch");
+    PermJob uj{Op, out, (int64_t)Hq * d * (int64_t)es};
+    RA_CUDA(launch_permute(&uj, 1, perm, T, 1, s), "unpermute launch");
+    RA_CUDA(launch_unpermute_cols(Lp, lse, perm, T, Hq, s), "lse unpermute launch");
+    return RA_OK;
+}
+
+ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
+                           const int32_t *cu, int B, int cp, int mode, int causal, float scale, int sched,
+                           const void *out, const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                           int grad_dtype, void *workspace, size_t ws_bytes, void *stream) {
+    ra_status st = ring_checks(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, sched, scale);
+    if (st) return st;
+    if (grad_dtype != RA_BF16 && grad_dtype != RA_FP32) return fail(RA_ERR_INVALID_ARG, "bad grad_dtype");
+    if (T == 0) return RA_OK;
+    if (!out || !lse || !dout || !dq || !dk || !dv) return fail(RA_ERR_INVALID_ARG, "NULL tensor");
+    if (!aligned16(out) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(RA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned");
+    const int G = Hq / Hkv;
+    const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
+    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, 1, tc, &st);
+    if (!plan) return st;
+    const RingLayout L = ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, 1);
+    if (!workspace || ws_bytes < L.total)
+        return fail(RA_ERR_WORKSPACE, "workspace must be >= " + std::to_string(L.total) + " bytes");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const DeviceTables &dt = plan->dev;
+    uint8_t *tab = ws + L.tables;
+    RA_CUDA(cudaMemcpyAsync(tab, dt.blob.data(), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
+    const int32_t *perm = reinterpret_cast<const int32_t *>(tab + dt.o_perm);
+    const int32_t *off = reinterpret_cast<const int32_t *>(tab + dt.o_off);
+    const int32_t *cul = reinterpret_cast<const int32_t *>(tab + dt.o_cul);
+    const size_t es = esize(dtype);
+    void *Qp = ws + L.qp, *Kp = ws + L.kp, *Vp = ws + L.vp, *dOp = ws + L.dop;
+    float *D = reinterpret_cast<float *>(ws + L.Dv);
+    float *dqa = reinterpret_cast<float *>(ws + L.dq);
+    float *dka = reinterpret_cast<float *>(ws + L.dk);
+    float *dva = reinterpret_cast<float *>(ws + L.dv);
+    // a7: permute Q, K, V, dO; D = rowsum(dO * O) in original order
+    PermJob jobs[4] = {{q, Qp, (int64_t)Hq * d * (int64_t)es},
+                       {k, Kp, (int64_t)Hkv * d * (int64_t)es},
+                       {v, Vp, (int64_t)Hkv * d * (int64_t)es},
+                       {dout, dOp, (int64_t)Hq * d * (int64_t)es}};
+    RA_CUDA(launch_permute(jobs, 4, perm, T, 0, s), "permute launch");
+    RA_CUDA(launch_rowdot(dout, out, dtype, T, Hq, d, D, s), "rowdot launch");
+    RA_CUDA(cudaMemsetAsync(dqa, 0, (size_t)T * Hq * d * 4, s), "memset dq");
+    RA_CUDA(cudaMemsetAsync(dka, 0, (size_t)T * Hkv * d * 4, s), "memset dk");
+    RA_CUDA(cudaMemsetAsync(dva, 0, (size_t)T * Hkv * d * 4, s), "memset dv");
+    // a8: per ring step (STEPWISE: one launch per step, fp32 dK/dV += per
+    // step) or all steps in one launch (FUSED)
+    SimtBwdArgs a{};
+    a.q = Qp;
+    a.k = Kp;
+    a.v = Vp;
+    a.dout = dOp;
+    a.dtype = dtype;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.T = T;
+    a.off = off;
+    a.cul = cul;
+    a.pos = perm;
+    a.cp = cp;
+    a.B = B;
+    a.causal = causal;
+    a.scale = scale;
+    a.lse = lse;
+    a.D = D;
+    a.lse_T = T;
+    a.dq = dqa;
+    a.dk = dka;
+    a.dv = dva;
+    if (sched == RA_SCHED_FUSED) {
+        a.t0 = 0;
+        a.t1 = cp;
+        RA_CUDA(launch_simt_bwd(a, s), "SIMT backward launch");
+    } else {
+        for (int t = 0; t < cp; ++t) {
+            a.t0 = t;
+            a.t1 = t + 1;
+            RA_CUDA(launch_simt_bwd(a, s), "SIMT backward launch");
+        }
+    }
+    // a9: cast to the gradient dtype (rows are already in original order)
+    RA_CUDA(launch_cast_f32(dqa, dq, grad_dtype, T * Hq * d, s), "cast dq");
+    RA_CUDA(launch_cast_f32(dka, dk, grad_dtype, T * Hkv * d, s), "cast dk");
+    RA_CUDA(launch_cast_f32(dva, dv, grad_dtype, T * Hkv * d, s), "cast dv");
+    return RA_OK;
+}
+
+}  // extern "C"

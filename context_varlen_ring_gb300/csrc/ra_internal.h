@@ -1,0 +1,113 @@
+// ra_internal.h -- host-side structures shared by the library's translation
+// units (planner, drivers, kernel launchers).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "../../include/ra.h"
+
+namespace ra {
+
+// Sets the thread-local detail message and returns the status.
+ra_status fail(ra_status s, const std::string &msg);
+
+// Tile geometry of the tensor-core kernels: 128 MMA rows (query tokens x
+// GQA heads packed together), 128-key KV tiles, head dim 128.
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kHeadDim = 128;
+
+// A tile is up to `rows` consecutive local rows of one segment whose
+// positions form at most two runs of consecutive integers:
+//   row c < split       -> pos0 + c
+//   split <= c < len    -> pos1 + (c - split)
+// Two int4 per tile on the device: {row0, len, split, pos0}, {pos1, pmin, pmax, seg}.
+struct Tile {
+    int32_t row0, len, split, pos0;
+    int32_t pos1, pmin, pmax, seg;
+};
+static_assert(sizeof(Tile) == 32, "tile record is two int4");
+
+// A work item of the tensor-core kernels.  Forward: two query tiles
+// (qt1 = -1 when absent) of one (rank r, segment b), one KV head g, and the
+// ring steps [t0, t1) whose KV tiles it visits.  Backward: qt0 is a KV
+// tile, qt1 unused, and the steps name the query ranks visited.
+struct WorkItem {
+    int32_t qt0, qt1, g, r;
+    int32_t b, t0, t1, cost;
+};
+static_assert(sizeof(WorkItem) == 32, "work item is two int4");
+
+// Zigzag plan (host): see ra_zigzag_plan in ra.h.
+struct ZigzagPlan {
+    int64_t T = 0;
+    int B = 0, cp = 0, mode = 0;
+    std::vector<int32_t> cu;        // [B+1]
+    std::vector<int32_t> perm;      // [T]
+    std::vector<int32_t> off;       // [cp+1]
+    std::vector<int32_t> cu_local;  // [cp*(B+1)]
+};
+
+ra_status validate_cu(const int32_t *cu, int B, int64_t T);
+ra_status build_zigzag(const int32_t *cu, int B, int cp, int mode, ZigzagPlan &zp);
+
+// Tile tables for one query side and one key side.  Tiles of segment b of
+// rank r are [q_off[r*(B+1)+b], q_off[r*(B+1)+b+1]) (same for kv_off).
+struct TilePlan {
+    int cp = 1, B = 0;
+    int q_tokens = 0;                    // tokens per query tile (128 / G)
+    std::vector<Tile> qtiles, kvtiles;
+    std::vector<int32_t> q_off, kv_off;  // [cp*(B+1)+1]
+    std::vector<WorkItem> items;         // forward items, LPT order
+    std::vector<WorkItem> bitems;        // backward items (one per KV tile x head)
+    int64_t fwd_tile_pairs = 0;          // non-skipped (query tile, KV tile) visits
+};
+
+// Builds tiles over rows [lo, hi) with positions pos[row] (at most two
+// consecutive-position runs per tile) and appends them.
+void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_t hi,
+                  int tile_rows, int seg);
+
+// Tile-pair class used by both the host cost model and the kernels.
+enum { kSkip = 0, kFull = 1, kPartial = 2 };
+inline int classify(const Tile &q, const Tile &k, int causal) {
+    if (q.len <= 0 || k.len <= 0) return kSkip;
+    if (causal && q.pmax < k.pmin) return kSkip;
+    if (k.len == kBN && (!causal || q.pmin >= k.pmax)) return kFull;
+    return kPartial;
+}
+
+// Ring tile plan: query side = key side = the permuted buffer.
+ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, TilePlan &tp);
+
+// Generic partial's tile plan: one "rank", separate Q and K sides.
+ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg,
+                              const int32_t *q_pos, const int32_t *k_pos, int64_t Tq, int64_t Tk,
+                              int G, int Hkv, int causal, TilePlan &tp);
+
+// Host image of the device tables, uploaded into the workspace each call.
+struct DeviceTables {
+    std::vector<uint8_t> blob;
+    size_t o_perm = 0, o_qt = 0, o_kt = 0, o_qoff = 0, o_kvoff = 0, o_items = 0,
+           o_bitems = 0, o_cul = 0, o_off = 0;
+    int n_items = 0, n_bitems = 0;
+};
+void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt);
+
+struct RingPlan {
+    ZigzagPlan zz;
+    TilePlan tiles;
+    bool has_tiles = false;
+    DeviceTables dev;
+};
+// Cached plans keyed by content (cu_seqlens, cp, mode, G, Hkv, causal).
+std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
+                                        int causal, bool want_tiles, ra_status *st);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace ra

@@ -1,0 +1,107 @@
+// ra_kernels.h -- launch interfaces of the library's kernels (host side).
+// Included by the C-ABI drivers and by the .cu files that implement them.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/ra.h"
+
+namespace ra {
+
+// ------------------------------------------------------------ status word
+int *device_status_ptr();          // device address of this device's status word
+uint64_t wait_budget_ns();         // budget of every device-side wait
+
+// ------------------------------------------------------------ permute
+struct PermJob {
+    const void *src;
+    void *dst;
+    int64_t row_bytes;
+};
+// inverse = 0: dst[i] = src[perm[i]];  inverse = 1: dst[perm[i]] = src[i].
+// Up to 4 jobs share one launch (same perm, same T).
+cudaError_t launch_permute(const PermJob *jobs, int njobs, const int32_t *perm, int64_t T, int inverse,
+                           cudaStream_t st);
+// [H, T] fp32: x[h, perm[i]] = y[h, i].
+cudaError_t launch_unpermute_cols(const float *y, float *x, const int32_t *perm, int64_t T, int H,
+                                  cudaStream_t st);
+
+// ------------------------------------------------------------ merge & misc
+constexpr int kMaxMergeParts = 64;
+cudaError_t launch_merge(int n, const float *const *outs, const float *const *lses, int64_t Tq, int Hq, int d,
+                         void *out, int out_dtype, float *lse_out, cudaStream_t st);
+// D[h, t] = sum_c a[t, h, c] * b[t, h, c]   (a, b of dtype; fp32 result)
+cudaError_t launch_rowdot(const void *a, const void *b, int dtype, int64_t T, int H, int d, float *D,
+                          cudaStream_t st);
+// dst (dtype) = src (fp32), n elements.
+cudaError_t launch_cast_f32(const float *src, void *dst, int dtype, int64_t n, cudaStream_t st);
+
+// ------------------------------------------------------------ attention
+// Where an attention kernel writes its rows.
+enum OutMode {
+    kOutFinal = 0,    // dtype output at row = position (original order), lse[h*lse_T + position]
+    kOutPartial = 1,  // fp32 output at the local row, lse[h*lse_T + local row]
+};
+
+// A ring over `cp` simulated ranks.  Query rows of rank r, segment b are
+// [qoff[r] + qcul[r*(B+1)+b], qoff[r] + qcul[r*(B+1)+b+1]); key rows of rank s
+// likewise with koff/kcul.  Positions (for the causal test and for kOutFinal
+// rows) come from qpos / kpos.
+struct SimtArgs {
+    const void *q, *k, *v;
+    int dtype, Hq, Hkv, d;
+    int64_t Tq, Tk;
+    const int32_t *qoff, *qcul, *qpos;
+    const int32_t *koff, *kcul, *kpos;
+    int cp, B, t0, t1;
+    int causal;
+    float scale;
+    int out_mode;
+    void *out;
+    float *lse;
+    int64_t lse_T;
+};
+cudaError_t launch_simt_fwd(const SimtArgs &a, cudaStream_t st);
+
+struct SimtBwdArgs {
+    const void *q, *k, *v, *dout;
+    int dtype, Hq, Hkv, d;
+    int64_t T;                         // rows of the permuted buffers
+    const int32_t *off, *cul, *pos;    // ring over cp ranks, q side = k side
+    int cp, B, t0, t1;
+    int causal;
+    float scale;
+    const float *lse, *D;              // [Hq, lse_T] indexed by position
+    int64_t lse_T;
+    float *dq;                         // fp32 [T_orig, Hq, d] at position rows (+=)
+    float *dk, *dv;                    // fp32 [T_orig, Hkv, d] at position rows (+=)
+};
+cudaError_t launch_simt_bwd(const SimtBwdArgs &a, cudaStream_t st);
+
+// Tensor-core forward (bf16, d = 128).
+struct TcFwdArgs {
+    const void *q, *k, *v;             // permuted buffers
+    int64_t Tq, Tk;
+    int Hq, Hkv, G;
+    const void *qtiles, *kvtiles;      // Tile records (two int4 each)
+    const int32_t *kv_off;             // [cp*(B+1)+1]
+    const void *items;                 // WorkItem records
+    int n_items;
+    int cp, B;
+    int t0, t1;                        // >= 0: override every item's step range
+    int causal;
+    float scale;
+    int out_mode;
+    void *out;
+    float *lse;
+    int64_t lse_T;
+};
+cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st);
+bool tc_fwd_supported(int dtype, int d, int Hq, int Hkv);
+
+// Device-wait self-test (see ra_selftest_wait_timeout).
+cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t st);
+
+}  // namespace ra

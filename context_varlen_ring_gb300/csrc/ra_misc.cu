@@ -1,0 +1,295 @@
+// ra_misc.cu -- bandwidth-bound kernels: zigzag permute / unpermute (the
+// reordering the maxtext PR #1133 review asks the framework to do around
+// load-balanced CP attention), the n-way LSE merge of ring partials, the
+// backward's row-dot preprocess and fp32 -> output casts; plus the device
+// status word and the wait-guard self-test.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "ra_dev.cuh"
+#include "ra_kernels.h"
+
+namespace ra {
+
+__device__ int g_ra_status;
+
+int *device_status_ptr() {
+    static int *ptrs[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ra_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int *>(p);
+    }
+    return ptrs[dev];
+}
+
+uint64_t wait_budget_ns() { return 2000000000ull; }
+
+static inline int num_sms() {
+    static int sms[128] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 128) return 148;
+    if (!sms[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        sms[dev] = v > 0 ? v : 148;
+    }
+    return sms[dev];
+}
+
+// ------------------------------------------------------------------ permute
+struct PermJobs {
+    PermJob j[4];
+    int n;
+};
+
+// One warp per row; each lane moves vectors of type V (16 B when every row
+// and pointer allows it), four in flight per lane before the stores.
+template <typename V>
+__global__ void __launch_bounds__(256) permute_kernel(PermJobs jobs, const int32_t *__restrict__ perm, int64_t T,
+                                                       int inverse, int *status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t i = warp; i < T; i += nwarps) {
+        const int32_t p = __ldg(perm + i);
+        if (p < 0 || (int64_t)p >= T) {
+            if (lane == 0) dev::record_status(status, RA_ERR_DEVICE_BOUNDS);
+            continue;
+        }
+        const int64_t srow = inverse ? i : (int64_t)p;
+        const int64_t drow = inverse ? (int64_t)p : i;
+        for (int jb = 0; jb < jobs.n; ++jb) {
+            const int64_t nvec = jobs.j[jb].row_bytes / (int64_t)sizeof(V);
+            const V *__restrict__ src = reinterpret_cast<const V *>(jobs.j[jb].src) + srow * nvec;
+            V *__restrict__ dst = reinterpret_cast<V *>(jobs.j[jb].dst) + drow * nvec;
+            for (int64_t c0 = lane; c0 < nvec; c0 += 128) {
+                V tmp[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t c = c0 + u * 32;
+                    if (c < nvec) tmp[u] = src[c];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t c = c0 + u * 32;
+                    if (c < nvec) dst[c] = tmp[u];
+                }
+            }
+        }
+    }
+}
+
+cudaError_t launch_permute(const PermJob *jobs, int njobs, const int32_t *perm, int64_t T, int inverse,
+                           cudaStream_t st) {
+    if (T <= 0 || njobs <= 0) return cudaSuccess;
+    PermJobs pj{};
+    pj.n = njobs;
+    int vec = 16;
+    for (int i = 0; i < njobs; ++i) {
+        pj.j[i] = jobs[i];
+        auto al = [](const void *p, int64_t rb, int a) {
+            return (reinterpret_cast<uintptr_t>(p) % a) == 0 && (rb % a) == 0;
+        };
+        while (vec > 1 && !(al(jobs[i].src, jobs[i].row_bytes, vec) && al(jobs[i].dst, jobs[i].row_bytes, vec)))
+            vec >>= 2;
+    }
+    const int64_t want = (T + 7) / 8;
+    const int blocks = (int)std::min<int64_t>(want, (int64_t)num_sms() * 8);
+    int *status = device_status_ptr();
+    if (vec == 16)
+        permute_kernel<uint4><<<blocks, 256, 0, st>>>(pj, perm, T, inverse, status);
+    else if (vec == 4)
+        permute_kernel<uint32_t><<<blocks, 256, 0, st>>>(pj, perm, T, inverse, status);
+    else
+        permute_kernel<uint8_t><<<blocks, 256, 0, st>>>(pj, perm, T, inverse, status);
+    return cudaGetLastError();
+}
+
+__global__ void unpermute_cols_kernel(const float *__restrict__ y, float *__restrict__ x,
+                                      const int32_t *__restrict__ perm, int64_t T, int H, int *status) {
+    const int64_t n = T * H;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < n; w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t h = w / T, i = w % T;
+        const int32_t p = __ldg(perm + i);
+        if (p < 0 || (int64_t)p >= T) {
+            dev::record_status(status, RA_ERR_DEVICE_BOUNDS);
+            continue;
+        }
+        x[h * T + p] = y[w];
+    }
+}
+
+cudaError_t launch_unpermute_cols(const float *y, float *x, const int32_t *perm, int64_t T, int H,
+                                  cudaStream_t st) {
+    if (T <= 0 || H <= 0) return cudaSuccess;
+    const int64_t n = T * H;
+    const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8);
+    unpermute_cols_kernel<<<blocks, 256, 0, st>>>(y, x, perm, T, H, device_status_ptr());
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ merge
+struct MergePtrs {
+    const float *o[kMaxMergeParts];
+    const float *l[kMaxMergeParts];
+};
+
+// One warp per (token, head) row.  M = max lse_p, L = M + log sum exp(lse_p - M),
+// out = sum_p exp(lse_p - L) out_p; lanes hold 4 consecutive elements of d.
+template <typename TOut>
+__global__ void __launch_bounds__(256) merge_kernel(MergePtrs P, int n, int64_t Tq, int Hq, int d, TOut *out,
+                                                     float *lse_out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = Tq * Hq;
+    const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows; w += nw) {
+        const int64_t t = w / Hq;
+        const int h = (int)(w % Hq);
+        const int64_t li = (int64_t)h * Tq + t;
+        float la = lane < n ? P.l[lane][li] : -INFINITY;
+        float lb = lane + 32 < n ? P.l[lane + 32][li] : -INFINITY;
+        float M = fmaxf(la, lb);
+#pragma unroll
+        for (int s = 16; s; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+        float L = -INFINITY;
+        if (M != -INFINITY) {
+            float sm = (la == -INFINITY ? 0.f : expf(la - M)) + (lb == -INFINITY ? 0.f : expf(lb - M));
+#pragma unroll
+            for (int s = 16; s; s >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, s);
+            L = M + logf(sm);
+        }
+        const float wa = (M == -INFINITY || la == -INFINITY) ? 0.f : expf(la - L);
+        const float wb = (M == -INFINITY || lb == -INFINITY) ? 0.f : expf(lb - L);
+        for (int c = lane * 4; c < d; c += 128) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int p = 0; p < n; ++p) {
+                const float wp = __shfl_sync(0xffffffffu, p < 32 ? wa : wb, p & 31);
+                if (wp == 0.f) continue;
+                const float4 x = *reinterpret_cast<const float4 *>(P.o[p] + w * d + c);
+                acc.x += wp * x.x;
+                acc.y += wp * x.y;
+                acc.z += wp * x.z;
+                acc.w += wp * x.w;
+            }
+            if constexpr (sizeof(TOut) == 4) {
+                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + w * d + c) = acc;
+            } else {
+                uint2 pk;
+                pk.x = dev::pack_bf16x2(acc.x, acc.y);
+                pk.y = dev::pack_bf16x2(acc.z, acc.w);
+                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + w * d + c) = pk;
+            }
+        }
+        if (lse_out && lane == 0) lse_out[li] = L;
+    }
+}
+
+cudaError_t launch_merge(int n, const float *const *outs, const float *const *lses, int64_t Tq, int Hq, int d,
+                         void *out, int out_dtype, float *lse_out, cudaStream_t st) {
+    if (Tq <= 0) return cudaSuccess;
+    MergePtrs P{};
+    for (int p = 0; p < n; ++p) {
+        P.o[p] = outs[p];
+        P.l[p] = lses[p];
+    }
+    const int64_t rows = Tq * Hq;
+    const int blocks = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 16);
+    if (out_dtype == RA_FP32)
+        merge_kernel<float><<<blocks, 256, 0, st>>>(P, n, Tq, Hq, d, static_cast<float *>(out), lse_out);
+    else
+        merge_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(P, n, Tq, Hq, d, static_cast<__nv_bfloat16 *>(out),
+                                                            lse_out);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ rowdot
+template <typename TIn>
+__global__ void __launch_bounds__(256) rowdot_kernel(const TIn *a, const TIn *b, int64_t T, int H, int d,
+                                                      float *D) {
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = T * H;
+    const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows; w += nw) {
+        float acc = 0.f;
+        for (int c = lane; c < d; c += 32) acc += (float)a[w * d + c] * (float)b[w * d + c];
+#pragma unroll
+        for (int s = 16; s; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+        if (lane == 0) {
+            const int64_t t = w / H;
+            const int h = (int)(w % H);
+            D[(int64_t)h * T + t] = acc;
+        }
+    }
+}
+
+cudaError_t launch_rowdot(const void *a, const void *b, int dtype, int64_t T, int H, int d, float *D,
+                          cudaStream_t st) {
+    if (T <= 0) return cudaSuccess;
+    const int64_t rows = T * H;
+    const int blocks = (int)std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 16);
+    if (dtype == RA_FP32)
+        rowdot_kernel<float><<<blocks, 256, 0, st>>>(static_cast<const float *>(a), static_cast<const float *>(b),
+                                                     T, H, d, D);
+    else
+        rowdot_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a),
+                                                             static_cast<const __nv_bfloat16 *>(b), T, H, d, D);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ cast
+__global__ void cast_bf16_kernel(const float *__restrict__ src, __nv_bfloat16 *__restrict__ dst, int64_t n) {
+    const int64_t n4 = n / 4;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 x = reinterpret_cast<const float4 *>(src)[i];
+        uint2 pk;
+        pk.x = dev::pack_bf16x2(x.x, x.y);
+        pk.y = dev::pack_bf16x2(x.z, x.w);
+        reinterpret_cast<uint2 *>(dst)[i] = pk;
+    }
+    for (int64_t i = n4 * 4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+cudaError_t launch_cast_f32(const float *src, void *dst, int dtype, int64_t n, cudaStream_t st) {
+    if (n <= 0) return cudaSuccess;
+    if (dtype == RA_FP32) {
+        if (src != dst) return cudaMemcpyAsync(dst, src, (size_t)n * 4, cudaMemcpyDeviceToDevice, st);
+        return cudaSuccess;
+    }
+    const int blocks = (int)std::min<int64_t>((n / 4 + 255) / 256 + 1, (int64_t)num_sms() * 8);
+    cast_bf16_kernel<<<blocks, 256, 0, st>>>(src, static_cast<__nv_bfloat16 *>(dst), n);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ self-test
+// Waits on a barrier nothing arrives at; the guard must give up after the
+// budget, record RA_ERR_TIMEOUT and let the kernel return.
+__global__ void wait_selftest_kernel(uint64_t budget_ns, int *status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        dev::mbar_init(&bar, 1);
+        dev::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        dev::WaitCtl w{&abort_flag, status, budget_ns};
+        (void)dev::mbar_wait(&bar, 0, w);
+    }
+    __syncthreads();
+}
+
+cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t st) {
+    wait_selftest_kernel<<<1, 32, 0, st>>>(budget_ns, device_status_ptr());
+    return cudaGetLastError();
+}
+
+}  // namespace ra

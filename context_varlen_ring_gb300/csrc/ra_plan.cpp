@@ -1,0 +1,298 @@
+// ra_plan.cpp -- host planner: zigzag plan, tile tables, work lists.
+//
+// Zigzag ("Zigzag attention support?", ring-attention-pytorch #20, the
+// extract_local snippet; maxtext PR #1133, review comment on reordering):
+// a stream of L tokens is cut into n = 2*cp chunks and rank r keeps chunks
+// r and n-1-r.  Here the chunk bounds are floor(c*L/n), which is the same
+// split as chunking into equal pieces when n divides L and stays defined
+// when it does not.  Per-document mode applies the rule to each document
+// ("Question about varlen ring attention", MiniMax-01 #6, on zigzag under
+// packing).
+//
+// The planner works on ranges: rank r's part of a stream is two ranges of
+// consecutive tokens, appended in increasing order.
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "ra_internal.h"
+
+namespace ra {
+
+ra_status validate_cu(const int32_t *cu, int B, int64_t T) {
+    if (!cu) return fail(RA_ERR_INVALID_ARG, "cu_seqlens is NULL");
+    if (B < 1) return fail(RA_ERR_INVALID_ARG, "B must be >= 1");
+    if (cu[0] != 0) return fail(RA_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
+    for (int b = 0; b < B; ++b)
+        if (cu[b + 1] < cu[b]) return fail(RA_ERR_INVALID_ARG, "cu_seqlens not non-decreasing at " + std::to_string(b));
+    if (T >= 0 && (int64_t)cu[B] != T)
+        return fail(RA_ERR_INVALID_ARG, "cu_seqlens[B] != T");
+    return RA_OK;
+}
+
+static inline int64_t bound(int64_t c, int64_t L, int64_t n) { return c * L / n; }
+
+ra_status build_zigzag(const int32_t *cu, int B, int cp, int mode, ZigzagPlan &zp) {
+    ra_status st = validate_cu(cu, B, -1);
+    if (st) return st;
+    if (cp < 1 || cp > 4096) return fail(RA_ERR_INVALID_ARG, "cp must be in [1, 4096]");
+    if (mode != RA_ZZ_GLOBAL && mode != RA_ZZ_PER_DOC) return fail(RA_ERR_INVALID_ARG, "unknown zigzag mode");
+    const int64_t T = cu[B];
+    const int64_t n = 2 * (int64_t)cp;
+    zp.T = T;
+    zp.B = B;
+    zp.cp = cp;
+    zp.mode = mode;
+    zp.cu.assign(cu, cu + B + 1);
+    zp.perm.resize((size_t)T);
+    zp.off.assign((size_t)cp + 1, 0);
+    zp.cu_local.assign((size_t)cp * (B + 1), 0);
+    int64_t p = 0;
+    for (int r = 0; r < cp; ++r) {
+        zp.off[r] = (int32_t)p;
+        int32_t *cl = zp.cu_local.data() + (size_t)r * (B + 1);
+        // the two ranges of rank r, per stream
+        auto emit = [&](int64_t a, int64_t e) {
+            for (int64_t i = a; i < e; ++i) zp.perm[(size_t)p++] = (int32_t)i;
+        };
+        if (mode == RA_ZZ_GLOBAL) {
+            const int64_t a0 = bound(r, T, n), e0 = bound(r + 1, T, n);
+            const int64_t a1 = bound(n - 1 - r, T, n), e1 = bound(n - r, T, n);
+            emit(a0, e0);
+            emit(a1, e1);
+            // local documents: intersect each document with the two ranges
+            for (int b = 0; b < B; ++b) {
+                auto inter = [&](int64_t a, int64_t e) {
+                    int64_t lo = std::max<int64_t>(a, cu[b]), hi = std::min<int64_t>(e, cu[b + 1]);
+                    return hi > lo ? hi - lo : 0;
+                };
+                cl[b + 1] = cl[b] + (int32_t)(inter(a0, e0) + inter(a1, e1));
+            }
+        } else {
+            for (int b = 0; b < B; ++b) {
+                const int64_t L = (int64_t)cu[b + 1] - cu[b], base = cu[b];
+                const int64_t a0 = base + bound(r, L, n), e0 = base + bound(r + 1, L, n);
+                const int64_t a1 = base + bound(n - 1 - r, L, n), e1 = base + bound(n - r, L, n);
+                emit(a0, e0);
+                emit(a1, e1);
+                cl[b + 1] = cl[b] + (int32_t)((e0 - a0) + (e1 - a1));
+            }
+        }
+    }
+    zp.off[cp] = (int32_t)p;
+    if (p != T) return fail(RA_ERR_INVALID_ARG, "internal: zigzag plan does not cover all tokens");
+    return RA_OK;
+}
+
+void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_t hi, int tile_rows, int seg) {
+    int64_t i = lo;
+    while (i < hi) {
+        const int64_t start = i;
+        const int32_t p0 = pos ? pos[i] : (int32_t)i;
+        auto P = [&](int64_t x) { return pos ? pos[x] : (int32_t)x; };
+        ++i;
+        while (i < hi && i - start < tile_rows && P(i) == P(i - 1) + 1) ++i;
+        const int32_t split = (int32_t)(i - start);
+        int32_t p1 = p0 + split;
+        bool two = false;
+        if (i < hi && i - start < tile_rows) {
+            p1 = P(i);
+            two = true;
+            ++i;
+            while (i < hi && i - start < tile_rows && P(i) == P(i - 1) + 1) ++i;
+        }
+        const int32_t len = (int32_t)(i - start);
+        Tile t;
+        t.row0 = (int32_t)start;
+        t.len = len;
+        t.split = split;
+        t.pos0 = p0;
+        t.pos1 = p1;
+        t.pmin = two ? std::min(p0, p1) : p0;
+        t.pmax = two ? std::max(p0 + split - 1, p1 + (len - split) - 1) : p0 + len - 1;
+        t.seg = seg;
+        out.push_back(t);
+    }
+}
+
+// Forward items: pairs of consecutive query tiles of one (rank, segment),
+// replicated over KV heads; backward items: one per KV tile and KV head.
+static void build_items(TilePlan &tp, int Hkv, int causal) {
+    const int cp = tp.cp, B = tp.B;
+    tp.items.clear();
+    tp.bitems.clear();
+    tp.fwd_tile_pairs = 0;
+    auto seg_idx = [&](int r, int b) { return r * (B + 1) + b; };
+    for (int r = 0; r < cp; ++r) {
+        for (int b = 0; b < B; ++b) {
+            const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
+            for (int i = qa; i < qe; i += 2) {
+                const int q1 = (i + 1 < qe) ? i + 1 : -1;
+                int64_t cost = 0;
+                for (int t = 0; t < cp; ++t) {
+                    const int s = ((r - t) % cp + cp) % cp;
+                    const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
+                    for (int j = ka; j < ke; ++j) {
+                        cost += classify(tp.qtiles[i], tp.kvtiles[j], causal) != kSkip;
+                        if (q1 >= 0) cost += classify(tp.qtiles[q1], tp.kvtiles[j], causal) != kSkip;
+                    }
+                }
+                for (int g = 0; g < Hkv; ++g) {
+                    WorkItem w{i, q1, g, r, b, 0, cp, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
+                    tp.items.push_back(w);
+                }
+                tp.fwd_tile_pairs += cost * Hkv;
+            }
+        }
+    }
+    for (int s = 0; s < cp; ++s) {
+        for (int b = 0; b < B; ++b) {
+            const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
+            for (int j = ka; j < ke; ++j) {
+                int64_t cost = 0;
+                for (int t = 0; t < cp; ++t) {
+                    const int r = (s + t) % cp;
+                    const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
+                    for (int i = qa; i < qe; ++i) cost += classify(tp.qtiles[i], tp.kvtiles[j], causal) != kSkip;
+                }
+                for (int g = 0; g < Hkv; ++g) {
+                    WorkItem w{j, -1, g, s, b, 0, cp, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
+                    tp.bitems.push_back(w);
+                }
+            }
+        }
+    }
+    // Longest-processing-time first: the grid's first CTAs take the longest
+    // items, so the tail of the launch is short ones.
+    auto by_cost = [](const WorkItem &a, const WorkItem &b) { return a.cost > b.cost; };
+    std::stable_sort(tp.items.begin(), tp.items.end(), by_cost);
+    std::stable_sort(tp.bitems.begin(), tp.bitems.end(), by_cost);
+}
+
+ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, TilePlan &tp) {
+    if (G < 1 || kBM % G != 0) return fail(RA_ERR_UNSUPPORTED, "GQA group must divide 128");
+    tp = TilePlan();
+    tp.cp = zp.cp;
+    tp.B = zp.B;
+    tp.q_tokens = kBM / G;
+    const int B = zp.B;
+    tp.q_off.assign((size_t)zp.cp * (B + 1) + 1, 0);
+    tp.kv_off.assign((size_t)zp.cp * (B + 1) + 1, 0);
+    for (int r = 0; r < zp.cp; ++r) {
+        for (int b = 0; b <= B; ++b) {
+            const size_t idx = (size_t)r * (B + 1) + b;
+            tp.q_off[idx] = (int32_t)tp.qtiles.size();
+            tp.kv_off[idx] = (int32_t)tp.kvtiles.size();
+            if (b == B) break;
+            const int64_t lo = zp.off[r] + zp.cu_local[idx], hi = zp.off[r] + zp.cu_local[idx + 1];
+            append_tiles(tp.qtiles, zp.perm.data(), lo, hi, tp.q_tokens, b);
+            append_tiles(tp.kvtiles, zp.perm.data(), lo, hi, kBN, b);
+        }
+    }
+    tp.q_off.back() = (int32_t)tp.qtiles.size();
+    tp.kv_off.back() = (int32_t)tp.kvtiles.size();
+    build_items(tp, Hkv, causal);
+    return RA_OK;
+}
+
+ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg,
+                              const int32_t *q_pos, const int32_t *k_pos, int64_t Tq, int64_t Tk,
+                              int G, int Hkv, int causal, TilePlan &tp) {
+    if (G < 1 || kBM % G != 0) return fail(RA_ERR_UNSUPPORTED, "GQA group must divide 128");
+    ra_status st = validate_cu(cu_q, nseg, Tq);
+    if (st) return st;
+    st = validate_cu(cu_k, nseg, Tk);
+    if (st) return st;
+    tp = TilePlan();
+    tp.cp = 1;
+    tp.B = nseg;
+    tp.q_tokens = kBM / G;
+    tp.q_off.assign((size_t)nseg + 2, 0);
+    tp.kv_off.assign((size_t)nseg + 2, 0);
+    for (int b = 0; b <= nseg; ++b) {
+        tp.q_off[b] = (int32_t)tp.qtiles.size();
+        tp.kv_off[b] = (int32_t)tp.kvtiles.size();
+        if (b == nseg) break;
+        append_tiles(tp.qtiles, q_pos, cu_q[b], cu_q[b + 1], tp.q_tokens, b);
+        append_tiles(tp.kvtiles, k_pos, cu_k[b], cu_k[b + 1], kBN, b);
+    }
+    tp.q_off.back() = (int32_t)tp.qtiles.size();
+    tp.kv_off.back() = (int32_t)tp.kvtiles.size();
+    build_items(tp, Hkv, causal);
+    return RA_OK;
+}
+
+void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    dt.o_perm = take(zp ? zp->perm.size() * 4 : 0);
+    dt.o_qt = take(tp ? tp->qtiles.size() * sizeof(Tile) : 0);
+    dt.o_kt = take(tp ? tp->kvtiles.size() * sizeof(Tile) : 0);
+    dt.o_qoff = take(tp ? tp->q_off.size() * 4 : 0);
+    dt.o_kvoff = take(tp ? tp->kv_off.size() * 4 : 0);
+    dt.o_items = take(tp ? tp->items.size() * sizeof(WorkItem) : 0);
+    dt.o_bitems = take(tp ? tp->bitems.size() * sizeof(WorkItem) : 0);
+    dt.o_cul = take(zp ? zp->cu_local.size() * 4 : 0);
+    dt.o_off = take(zp ? zp->off.size() * 4 : 0);
+    dt.blob.assign(o, 0);
+    auto put = [&](size_t at, const void *src, size_t bytes) {
+        if (bytes) std::memcpy(dt.blob.data() + at, src, bytes);
+    };
+    if (zp) {
+        put(dt.o_perm, zp->perm.data(), zp->perm.size() * 4);
+        put(dt.o_cul, zp->cu_local.data(), zp->cu_local.size() * 4);
+        put(dt.o_off, zp->off.data(), zp->off.size() * 4);
+    }
+    if (tp) {
+        put(dt.o_qt, tp->qtiles.data(), tp->qtiles.size() * sizeof(Tile));
+        put(dt.o_kt, tp->kvtiles.data(), tp->kvtiles.size() * sizeof(Tile));
+        put(dt.o_qoff, tp->q_off.data(), tp->q_off.size() * 4);
+        put(dt.o_kvoff, tp->kv_off.data(), tp->kv_off.size() * 4);
+        put(dt.o_items, tp->items.data(), tp->items.size() * sizeof(WorkItem));
+        put(dt.o_bitems, tp->bitems.data(), tp->bitems.size() * sizeof(WorkItem));
+        dt.n_items = (int)tp->items.size();
+        dt.n_bitems = (int)tp->bitems.size();
+    }
+}
+
+std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
+                                        int causal, bool want_tiles, ra_status *st) {
+    static std::mutex mu;
+    static std::map<std::string, std::shared_ptr<RingPlan>> cache;
+    static std::vector<std::string> order;
+    *st = validate_cu(cu, B, -1);
+    if (*st) return nullptr;
+    std::string key;
+    key.append(reinterpret_cast<const char *>(cu), sizeof(int32_t) * (size_t)(B + 1));
+    int32_t tail[7] = {B, cp, mode, G, Hkv, causal, want_tiles ? 1 : 0};
+    key.append(reinterpret_cast<const char *>(tail), sizeof(tail));
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    auto plan = std::make_shared<RingPlan>();
+    *st = build_zigzag(cu, B, cp, mode, plan->zz);
+    if (*st) return nullptr;
+    if (want_tiles) {
+        *st = build_ring_tiles(plan->zz, G, Hkv, causal, plan->tiles);
+        if (*st) return nullptr;
+        plan->has_tiles = true;
+    }
+    pack_tables(&plan->zz, want_tiles ? &plan->tiles : nullptr, plan->dev);
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = plan;
+    order.push_back(key);
+    if (order.size() > 16) {
+        cache.erase(order.front());
+        order.erase(order.begin());
+    }
+    return plan;
+}
+
+}  // namespace ra

@@ -1,0 +1,603 @@
+// ra_tc_fwd.cu -- tensor-core forward of packed causal varlen ring attention
+// (bf16 in, fp32 accumulation, head dim 128) for sm_103a.
+//
+// What it computes: for every query row of every simulated CP rank, the
+// softmax attention over the keys of its own document that pass the causal
+// test (k_pos <= q_pos), visiting the KV shards in ring order -- rank r at
+// step t reads the shard of rank s = (r - t) mod cp ("Question about varlen
+// ring attention", MiniMax-01 #6; zigzag shards per ring-attention-pytorch
+// #20 and maxtext PR #1133).  Partials of the steps are merged on chip by
+// the online softmax (equivalent to the LSE merge of per-step results);
+// with a one-step range the same kernel returns one ring step's partial
+// (out, lse).  Tiles whose pairs are all masked are never visited (the
+// pruning of FlagScale PR #910).
+//
+// GB300 design:
+//  * One CTA = one work item: two query tiles of 128 MMA rows each.  A row
+//    is (token, head) with the G query heads of one KV head packed together
+//    (128/G tokens x G heads), so a K/V tile loaded once serves all G heads.
+//  * TMA (3-D tensor maps over [T, H, 128], 128-byte swizzle) stages Q once
+//    and K/V tiles through a 3-slot ring; tcgen05.mma (kind::f16, M=128,
+//    N=128) computes S = Q K^T and O += P V into TMEM; the MMA is issued by
+//    one thread.
+//  * TMEM: S0, S1, O0, O1 (4 x 128 fp32 columns = all 512).
+//  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
+//    allocator, warps 4-7 softmax of query tile 0, warps 8-11 of tile 1.
+//    A softmax thread owns one TMEM lane (one row): it reads S, masks,
+//    takes exp2 in fp32, writes P (bf16) to shared memory in the MMA's
+//    swizzled layout, and rescales its O row in TMEM only when the running
+//    max grew by more than 2^8 (otherwise the stale max is kept; the final
+//    normalisation uses the same max, so the result is exact).
+//  * MMA issue order per KV tile j: PV0(j), S0(j+1), PV1(j), S1(j+1), so
+//    each softmax group has the other group's two MMAs to hide behind.
+//  * Every wait is bounded (2 s); a wait that runs out records
+//    RA_ERR_TIMEOUT and the CTA drains its copies and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "ra_dev.cuh"
+#include "ra_internal.h"
+#include "ra_kernels.h"
+
+namespace ra {
+
+namespace {
+
+using namespace dev;
+
+constexpr int kThreads = 384;
+constexpr int kSlots = 3;
+constexpr uint32_t kHalf = 16384;        // 128 rows x 128 B (64 bf16) swizzled half-tile
+constexpr uint32_t kTile = 2 * kHalf;    // 128 rows x 128 bf16
+constexpr uint32_t kOffQ0 = 0;
+constexpr uint32_t kOffQ1 = kTile;
+constexpr uint32_t kOffKV = 2 * kTile;
+constexpr uint32_t kOffP0 = kOffKV + kSlots * kTile;
+constexpr uint32_t kOffP1 = kOffP0 + kTile;
+constexpr uint32_t kOffBar = kOffP1 + kTile;
+constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+
+struct FwdParams {
+    CUtensorMap tmQ, tmK, tmV;
+    const int4 *qtiles, *kvtiles, *items;
+    const int *kv_off;
+    int n_items, cp, B, G, log2G, Hq;
+    int t0, t1, causal, out_mode;
+    float scale_log2;
+    void *out;
+    float *lse;
+    long long lse_T;
+    int *status;
+    unsigned long long budget_ns;
+};
+
+struct TileD {
+    int row0, len, split, pos0, pos1, pmin, pmax, seg;
+};
+
+__device__ __forceinline__ TileD load_tile(const int4 *tab, int idx) {
+    const int4 a = __ldg(tab + 2 * idx), b = __ldg(tab + 2 * idx + 1);
+    return TileD{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+}
+
+struct QInfo {
+    int len, pmin, pmax;
+};
+
+__device__ __forceinline__ int classify_q(const QInfo &q, int klen, int kpmin, int kpmax, int causal) {
+    if (q.len <= 0 || klen <= 0) return kSkip;
+    if (causal && q.pmax < kpmin) return kSkip;
+    if (klen == kBN && (!causal || q.pmin >= kpmax)) return kFull;
+    return kPartial;
+}
+
+// Walks the KV tiles a work item visits, in ring order, skipping tiles that
+// are fully masked for both query tiles.  Every role runs its own copy and
+// sees the same sequence; `next` returns the KV tile's index in the table.
+struct KvIter {
+    const FwdParams *p;
+    QInfo q0, q1;
+    int has1, r, b, t, t_end, j, j_end;
+
+    __device__ __forceinline__ bool next(int &idx, int &c0, int &c1) {
+        for (;;) {
+            while (j >= j_end) {
+                if (t >= t_end) return false;
+                int s = (r - t) % p->cp;
+                if (s < 0) s += p->cp;
+                const int o = s * (p->B + 1) + b;
+                j = __ldg(p->kv_off + o);
+                j_end = __ldg(p->kv_off + o + 1);
+                ++t;
+            }
+            idx = j++;
+            const int klen = __ldg(&p->kvtiles[2 * idx].y);
+            const int4 kb = __ldg(p->kvtiles + 2 * idx + 1);
+            c0 = classify_q(q0, klen, kb.y, kb.z, p->causal);
+            c1 = has1 ? classify_q(q1, klen, kb.y, kb.z, p->causal) : kSkip;
+            if (c0 != kSkip || c1 != kSkip) return true;
+        }
+    }
+};
+
+// Bits [a, b) of the 32 columns starting at `base`.
+__device__ __forceinline__ uint32_t range_bits(int a, int b, int base) {
+    const int lo = min(max(a - base, 0), 32), hi = min(max(b - base, 0), 32);
+    return (uint32_t)(((1ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
+}
+
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_s, uint32_t k_s, uint32_t idesc) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t off = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
+        tc_mma_ss(d_tmem, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k_s + off, 16, 1024), idesc, ks > 0);
+    }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_s, uint32_t v_s, uint32_t idesc,
+                                         uint32_t accumulate) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t aoff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
+        const uint32_t boff = (uint32_t)ks * 2048u;  // 16 key rows of 128 B
+        tc_mma_ss(d_tmem, sdesc_sw128(p_s + aoff, 16, 1024), sdesc_sw128(v_s + boff, kHalf, 1024), idesc,
+                  (accumulate || ks > 0) ? 1u : 0u);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
+    uint64_t *q_full = bars + 0;
+    uint64_t *kv_full = bars + 1;    // [3]
+    uint64_t *kv_empty = bars + 4;   // [3]
+    uint64_t *s_full = bars + 7;     // [2]
+    uint64_t *p_ready = bars + 9;    // [2]
+    uint64_t *o_done = bars + 11;    // [2]
+    uint64_t *mma_done = bars + 13;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 15);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int4 ia = __ldg(p.items + 2 * blockIdx.x), ib = __ldg(p.items + 2 * blockIdx.x + 1);
+    const int qt0 = ia.x, qt1 = ia.y, g = ia.z, r = ia.w, b = ib.x;
+    const int t0 = p.t0 >= 0 ? p.t0 : ib.y;
+    const int t1 = p.t0 >= 0 ? p.t1 : ib.z;
+
+    KvIter it;
+    it.p = &p;
+    it.has1 = qt1 >= 0;
+    {
+        const int4 a0 = __ldg(p.qtiles + 2 * qt0), b0 = __ldg(p.qtiles + 2 * qt0 + 1);
+        it.q0 = QInfo{a0.y, b0.y, b0.z};
+        if (it.has1) {
+            const int4 a1 = __ldg(p.qtiles + 2 * qt1), b1 = __ldg(p.qtiles + 2 * qt1 + 1);
+            it.q1 = QInfo{a1.y, b1.y, b1.z};
+        } else {
+            it.q1 = QInfo{0, 0, 0};
+        }
+    }
+    it.r = r;
+    it.b = b;
+    it.t = t0;
+    it.t_end = t1;
+    it.j = 0;
+    it.j_end = 0;
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(q_full, 1);
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(kv_full + i, 1);
+            mbar_init(kv_empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(s_full + i, 1);
+            mbar_init(p_ready + i, 128);
+            mbar_init(o_done + i, 1);
+        }
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl wc{abort_flag, p.status, p.budget_ns};
+    // Register split: 128 x 56 (producer/MMA group) + 256 x 224 (softmax
+    // groups) = 64512 = the 384 x 168 registers the CTA is launched with.
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmQ);
+            tma_prefetch_desc(&p.tmK);
+            tma_prefetch_desc(&p.tmV);
+            const int hq0 = g * p.G;
+            mbar_arrive_expect_tx(q_full, (it.has1 ? 2u : 1u) * kTile);
+            const int qrow0 = __ldg(&p.qtiles[2 * qt0].x);
+            tma_load_3d(base + kOffQ0, &p.tmQ, q_full, 0, hq0, qrow0);
+            tma_load_3d(base + kOffQ0 + kHalf, &p.tmQ, q_full, 64, hq0, qrow0);
+            if (it.has1) {
+                const int qrow1 = __ldg(&p.qtiles[2 * qt1].x);
+                tma_load_3d(base + kOffQ1, &p.tmQ, q_full, 0, hq0, qrow1);
+                tma_load_3d(base + kOffQ1 + kHalf, &p.tmQ, q_full, 64, hq0, qrow1);
+            }
+            uint32_t u = 0;
+            int kidx, c0, c1;
+            bool ok = true;
+            while (ok && it.next(kidx, c0, c1)) {
+                const int krow0 = __ldg(&p.kvtiles[2 * kidx].x);
+                for (int kv = 0; kv < 2; ++kv, ++u) {
+                    const uint32_t slot = u % kSlots, ph = (u / kSlots) & 1u;
+                    if (!mbar_wait(kv_empty + slot, ph ^ 1u, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *dst = base + kOffKV + slot * kTile;
+                    const CUtensorMap *m = kv ? &p.tmV : &p.tmK;
+                    mbar_arrive_expect_tx(kv_full + slot, kTile);
+                    tma_load_3d(dst, m, kv_full + slot, 0, g, krow0);
+                    tma_load_3d(dst + kHalf, m, kv_full + slot, 64, g, krow0);
+                }
+            }
+            // Drain: the last copy into each slot (and Q) must have landed
+            // before the CTA may exit.
+            volatile int local_abort = 0;
+            const WaitCtl drain{&local_abort, p.status, p.budget_ns};
+            (void)mbar_wait(q_full, 0, drain);
+            for (uint32_t x = (u > kSlots ? u - kSlots : 0); x < u; ++x)
+                (void)mbar_wait(kv_full + (x % kSlots), (x / kSlots) & 1u, drain);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+            const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);
+            const uint32_t q0s = base_s + kOffQ0, q1s = base_s + kOffQ1;
+            const uint32_t p0s = base_s + kOffP0, p1s = base_s + kOffP1;
+            const uint32_t kvs = base_s + kOffKV;
+            const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+            int kidx, c0, c1;
+            bool ok = mbar_wait(q_full, 0, wc);
+            tc_fence_after();
+            bool have = ok && it.next(kidx, c0, c1);
+            uint32_t np0 = 0, np1 = 0;  // PVs issued per query tile
+            if (have) {
+                if (!mbar_wait(kv_full + 0, 0, wc)) ok = false;
+                tc_fence_after();
+                if (ok) {
+                    if (c0 != kSkip) {
+                        issue_s(tS0, q0s, kvs, idesc_s);
+                        tc_commit(s_full + 0);
+                    }
+                    if (c1 != kSkip) {
+                        issue_s(tS1, q1s, kvs, idesc_s);
+                        tc_commit(s_full + 1);
+                    }
+                    tc_commit(kv_empty + 0);
+                }
+            }
+            uint32_t j = 0;
+            while (ok && have) {
+                const int cc0 = c0, cc1 = c1;
+                int nidx, nc0 = kSkip, nc1 = kSkip;
+                const bool have_next = it.next(nidx, nc0, nc1);
+                const uint32_t vidx = 2 * j + 1, vslot = vidx % kSlots;
+                if (!mbar_wait(kv_full + vslot, (vidx / kSlots) & 1u, wc)) break;
+                tc_fence_after();
+                const uint32_t vs = kvs + vslot * kTile;
+                const uint32_t kload = 2 * j + 2, kslot = kload % kSlots;
+                const uint32_t ks = kvs + kslot * kTile;
+                if (cc0 != kSkip) {
+                    if (!mbar_wait(p_ready + 0, np0 & 1u, wc)) break;
+                    tc_fence_after();
+                    issue_pv(tO0, p0s, vs, idesc_o, np0 > 0);
+                    tc_commit(o_done + 0);
+                    ++np0;
+                }
+                if (have_next) {
+                    if (!mbar_wait(kv_full + kslot, (kload / kSlots) & 1u, wc)) break;
+                    tc_fence_after();
+                    if (nc0 != kSkip) {
+                        issue_s(tS0, q0s, ks, idesc_s);
+                        tc_commit(s_full + 0);
+                    }
+                }
+                if (cc1 != kSkip) {
+                    if (!mbar_wait(p_ready + 1, np1 & 1u, wc)) break;
+                    tc_fence_after();
+                    issue_pv(tO1, p1s, vs, idesc_o, np1 > 0);
+                    tc_commit(o_done + 1);
+                    ++np1;
+                }
+                if (have_next) {
+                    if (nc1 != kSkip) {
+                        issue_s(tS1, q1s, ks, idesc_s);
+                        tc_commit(s_full + 1);
+                    }
+                    tc_commit(kv_empty + kslot);
+                }
+                tc_commit(kv_empty + vslot);
+                if (!have_next) break;
+                c0 = nc0;
+                c1 = nc1;
+                kidx = nidx;
+                ++j;
+            }
+            // every MMA issued must have completed before TMEM is released
+            tc_commit(mma_done);
+            volatile int local_abort = 0;
+            const WaitCtl drain{&local_abort, p.status, p.budget_ns};
+            (void)mbar_wait(mma_done, 0, drain);
+        }
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
+        // ------------------------------------------------ softmax / epilogue
+        const int k = (warp >= 8) ? 1 : 0;
+        const int m = threadIdx.x - 128 - 128 * k;  // TMEM lane = MMA row
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_base + 128u * k;
+        const uint32_t tO = tmem + lane_base + 256u + 128u * k;
+        uint8_t *P = base + (k ? kOffP1 : kOffP0);
+        if (k == 0 || it.has1) {
+            const TileD q = load_tile(p.qtiles, k ? qt1 : qt0);
+            const int tok = m >> p.log2G;
+            const int head = g * p.G + (m & (p.G - 1));
+            const bool valid = tok < q.len;
+            const int qpos = tok < q.split ? q.pos0 + tok : q.pos1 + (tok - q.split);
+            float m_run = -INFINITY, l_run = 0.f;
+            uint32_t nd = 0;
+            int kidx, c0, c1;
+            // swizzled P row: 16-byte chunk c of half h lives at
+            // h*16K + (m/8)*1024 + (m%8)*128 + ((c ^ (m%8)) * 16)
+            uint8_t *prow = P + (m >> 3) * 1024 + (m & 7) * 128;
+            const int sw = m & 7;
+            bool ok = true;
+            while (it.next(kidx, c0, c1)) {
+                const int cls = k ? c1 : c0;
+                if (cls == kSkip) continue;
+                if (!mbar_wait(s_full + k, nd & 1u, wc)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                float s[128];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(tS + 32u * ch, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[32 * ch + i] = __uint_as_float(v[i]);
+                }
+                if (cls == kPartial) {
+                    // allowed columns: [0, lim1) in the first position run and
+                    // [split, lim2) in the second, as one bit per column
+                    const int4 ka = __ldg(p.kvtiles + 2 * kidx);
+                    const int kt_len = ka.y, kt_split = ka.z, kt_pos0 = ka.w;
+                    const int kt_pos1 = __ldg(&p.kvtiles[2 * kidx + 1].x);
+                    int lim1, lim2;
+                    if (p.causal) {
+                        lim1 = min(max(qpos - kt_pos0 + 1, 0), kt_split);
+                        lim2 = min(max(qpos - kt_pos1 + kt_split + 1, kt_split), kt_len);
+                    } else {
+                        lim1 = kt_split;
+                        lim2 = kt_len;
+                    }
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const uint32_t w = range_bits(0, lim1, 32 * ch) | range_bits(kt_split, lim2, 32 * ch);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) s[32 * ch + i] = ((w >> i) & 1u) ? s[32 * ch + i] : -INFINITY;
+                    }
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+                const float m_new = fmaxf(m_run, mx * p.scale_log2);
+                const bool need = m_new > m_run + 8.0f;
+                float alpha = 1.f;
+                if (need) {
+                    alpha = ex2_approx(m_run - m_new);
+                    m_run = m_new;
+                    l_run *= alpha;
+                }
+                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                if (nd > 0) {
+                    // the previous PV must be done: it reads P and writes O
+                    if (!mbar_wait(o_done + k, (nd - 1) & 1u, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                float sum = 0.f;
+#pragma unroll
+                for (int c16 = 0; c16 < 16; ++c16) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float a0 = ex2_approx(fmaf(s[8 * c16 + 2 * e], p.scale_log2, -m_use));
+                        const float a1 = ex2_approx(fmaf(s[8 * c16 + 2 * e + 1], p.scale_log2, -m_use));
+                        sum += a0 + a1;
+                        pk[e] = pack_bf16x2(a0, a1);
+                    }
+                    const int h = c16 >> 3, c = c16 & 7;
+                    *reinterpret_cast<uint4 *>(prow + h * kHalf + ((c ^ sw) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                l_run += sum;
+                // rescale this row of O when the max moved (warp-uniform branch)
+                if (nd > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t v[32];
+                        tmem_ld32(tO + 32u * ch, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tmem_st32(tO + 32u * ch, v);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(p_ready + k);
+                ++nd;
+            }
+            // ---------------------------------------------- epilogue
+            if (ok && nd > 0) {
+                ok = mbar_wait(o_done + k, (nd - 1) & 1u, wc);
+                tc_fence_after();
+            }
+            const bool has_o = ok && nd > 0;
+            const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+            const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+            const long long orow = p.out_mode == kOutFinal ? (long long)qpos : (long long)(q.row0 + tok);
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t v[32];
+                if (has_o) {
+                    tmem_ld32(tO + 32u * ch, v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0u;
+                }
+                if (valid) {
+                    const long long e0 = (orow * p.Hq + head) * 128 + 32 * ch;
+                    if (p.out_mode == kOutFinal) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + e0);
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
+                            dst[q4] = w;
+                        }
+                    } else {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + e0);
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            dst[q4] = make_float4(__uint_as_float(v[4 * q4 + 0]) * inv, __uint_as_float(v[4 * q4 + 1]) * inv,
+                                                  __uint_as_float(v[4 * q4 + 2]) * inv, __uint_as_float(v[4 * q4 + 3]) * inv);
+                    }
+                }
+            }
+            if (valid) p.lse[(long long)head * p.lse_T + orow] = lse;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// 3-D map over a THD bf16 tensor [T, H, 128]: dims (d, H, T), box
+// (64, box_h, box_t), 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int box_h, int box_t) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_h, (cuuint32_t)box_t};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_fwd_supported(int dtype, int d, int Hq, int Hkv) {
+    if (dtype != RA_BF16 || d != 128 || Hkv <= 0 || Hq % Hkv) return false;
+    const int G = Hq / Hkv;
+    return G >= 1 && G <= 16 && (G & (G - 1)) == 0;
+}
+
+cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
+    if (a.n_items <= 0) return cudaSuccess;
+    FwdParams p;
+    memset(&p, 0, sizeof(p));
+    const int G = a.G;
+    if (!make_map(&p.tmQ, a.q, a.Tq, a.Hq, G, kBM / G) || !make_map(&p.tmK, a.k, a.Tk, a.Hkv, 1, kBN) ||
+        !make_map(&p.tmV, a.v, a.Tk, a.Hkv, 1, kBN))
+        return cudaErrorInvalidValue;
+    p.qtiles = static_cast<const int4 *>(a.qtiles);
+    p.kvtiles = static_cast<const int4 *>(a.kvtiles);
+    p.items = static_cast<const int4 *>(a.items);
+    p.kv_off = a.kv_off;
+    p.n_items = a.n_items;
+    p.cp = a.cp;
+    p.B = a.B;
+    p.G = G;
+    int lg = 0;
+    while ((1 << lg) < G) ++lg;
+    p.log2G = lg;
+    p.Hq = a.Hq;
+    p.t0 = a.t0;
+    p.t1 = a.t1;
+    p.causal = a.causal;
+    p.out_mode = a.out_mode;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.out = a.out;
+    p.lse = a.lse;
+    p.lse_T = a.lse_T;
+    p.status = device_status_ptr();
+    p.budget_ns = wait_budget_ns();
+    static bool attr_set[128] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 128 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        // The setmaxnreg split (128 x 56 + 256 x 224) needs the CTA to be
+        // launched with 168 registers per thread; with fewer, the increase
+        // could never be granted, so refuse to launch.
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, tc_fwd_kernel);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs < 168) return cudaErrorInvalidConfiguration;
+        attr_set[dev] = true;
+    }
+    tc_fwd_kernel<<<a.n_items, kThreads, kSmemBytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -1,0 +1,223 @@
+/*
+ * ra.h -- C ABI of libra: packed causal varlen ring attention with zigzag
+ * context-parallel (CP) load balancing, for NVIDIA GB300 (sm_103a).
+ *
+ * All CP ranks are simulated on one GPU: rank r's shard is the slice
+ * [off[r], off[r+1]) of one zigzag-permuted buffer, and a ring step that
+ * "receives" rank s's K/V reads that slice in place.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout "THD": a token-major tensor [T, H, d], row-major, d contiguous
+ *    (the packed layout of flash_attn_varlen_* named in "Attention Mask for
+ *    Packed Sequences (via Attention Bias)", EasyDeL #129).
+ *  - cu_seqlens: int32 cumulative document lengths, B+1 entries, cu[0] = 0,
+ *    non-decreasing, cu[B] = T.  Documents never attend to each other
+ *    (same page, opening request).
+ *  - GQA: Hq = G * Hkv; query head h reads KV head floor(h / G).
+ *  - LSE: natural-log log-sum-exp of the scaled scores, fp32, layout [Hq, T]
+ *    (row h holds all tokens of head h).  A row with no allowed key has
+ *    lse = -inf and output 0.
+ *  - Device pointers must be 16-byte aligned.  "HOST" marks host arrays.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) unless it says otherwise.  The caller owns and
+ *    allocates every device buffer, including the workspace; the library
+ *    allocates no device memory.
+ *  - Errors: argument checks happen on the host before any launch and
+ *    return RA_ERR_INVALID_ARG / RA_ERR_UNSUPPORTED / RA_ERR_WORKSPACE with
+ *    nothing launched; a failed launch returns RA_ERR_CUDA.  Device-side
+ *    faults the kernels detect themselves (a wait that gave up, an index
+ *    out of range) are recorded in a status word read by
+ *    ra_get_device_status().  ra_last_error() gives a one-line detail of the
+ *    last failure on the calling host thread.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int ra_status;
+enum {
+    RA_OK = 0,
+    RA_ERR_INVALID_ARG = 1,   /* bad shape, cu_seqlens, pointer, cp, mode   */
+    RA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (dtype, d, align) */
+    RA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed       */
+    RA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than required    */
+    RA_ERR_TIMEOUT = 5,       /* a device-side wait gave up (status word)   */
+    RA_ERR_DEVICE_BOUNDS = 6  /* a kernel caught an out-of-range index      */
+};
+
+enum { RA_ZZ_GLOBAL = 0, RA_ZZ_PER_DOC = 1 };        /* zigzag modes       */
+enum { RA_BF16 = 0, RA_FP32 = 1 };                   /* element types      */
+enum { RA_SCHED_FUSED = 0, RA_SCHED_STEPWISE = 1 };  /* ring schedules     */
+
+/* ------------------------------------------------------------------------
+ * ra_zigzag_plan  (HOST, synchronous, no GPU needed)
+ *
+ * The zigzag split of ring-attention-pytorch #20 ("Zigzag attention
+ * support?", the `extract_local` snippet) and maxtext PR #1133 (review
+ * comment on load-balanced reordering): a stream of L tokens is cut into
+ * n = 2*cp chunks, chunk c = [floor(c*L/n), floor((c+1)*L/n)), and rank r
+ * holds chunks r and n-1-r.  When n does not divide L this balanced split
+ * is used (chunks differ by at most one token; some may be empty).
+ *   mode RA_ZZ_GLOBAL : the stream is the whole packed batch (T tokens).
+ *   mode RA_ZZ_PER_DOC: every document is split on its own ("Question about
+ *                       varlen ring attention", MiniMax-01 #6, notes that
+ *                       zigzag under packing is the hard case).
+ * Local token order is increasing packed index in both modes.
+ *
+ *   cu_seqlens HOST [B+1]             in
+ *   perm       HOST [T]     int32     out: perm[i] = packed index of the
+ *                                     token in permuted slot i
+ *   off        HOST [cp+1]  int32     out: rank r owns slots [off[r], off[r+1])
+ *   cu_local   HOST [cp*(B+1)] int32  out: rank r's local cu_seqlens (entry
+ *                                     r*(B+1)+b); zero-length docs allowed
+ * ------------------------------------------------------------------------ */
+ra_status ra_zigzag_plan(const int32_t *cu_seqlens, int B, int cp, int mode,
+                         int32_t *perm, int32_t *off, int32_t *cu_local);
+
+/* ------------------------------------------------------------------------
+ * ra_zigzag_permute / ra_zigzag_unpermute  (DEVICE)
+ *
+ * Applies the reordering the maxtext PR #1133 review says the framework
+ * must perform before load-balanced CP attention (and undo afterwards):
+ *   permute:    y[i, :] = x[perm[i], :]      for i in [0, T)
+ *   unpermute:  x[perm[i], :] = y[i, :]
+ * Rows are `row_bytes` bytes (H*d*element size for THD tensors); the copy
+ * is bit-exact.  perm is a DEVICE int32 array [T] that must be a
+ * permutation of [0, T) (an entry outside [0, T) is skipped and recorded
+ * as RA_ERR_DEVICE_BOUNDS).  x and y must not overlap.
+ * ------------------------------------------------------------------------ */
+ra_status ra_zigzag_permute(const void *x, void *y, const int32_t *perm,
+                            int64_t T, int64_t row_bytes, void *stream);
+ra_status ra_zigzag_unpermute(const void *y, void *x, const int32_t *perm,
+                              int64_t T, int64_t row_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * ra_varlen_attn_partial  (DEVICE tensors, HOST segment/position arrays)
+ *
+ * One ring step's attention: local queries against one KV shard, returning
+ * the normalised output and its LSE so that partials can be merged
+ * ("[Train] Support custom attention with context parallel", FlagScale
+ * PR #910: RingAttention with a swappable forward_impl; this is that
+ * step).  Allowed pairs:
+ *   (i, j) with seg(i) == seg(j) and (causal == 0 or k_pos[j] <= q_pos[i]),
+ * where seg is given by cu_seqlens_q / cu_seqlens_k (segment b of Q pairs
+ * with segment b of K, nseg segments each).
+ *   q   DEVICE [Tq, Hq, d]      dtype RA_BF16 or RA_FP32
+ *   k,v DEVICE [Tk, Hkv, d]     same dtype
+ *   cu_seqlens_q, cu_seqlens_k  HOST [nseg+1]
+ *   q_pos HOST [Tq], k_pos HOST [Tk]  int32 positions used by the causal
+ *                               test (NULL = the local row index)
+ *   out DEVICE [Tq, Hq, d] fp32, lse DEVICE [Hq, Tq] fp32 (written in full)
+ *   workspace DEVICE, >= ra_partial_workspace_bytes(...) bytes
+ * bf16 with d = 128 and G a power of two <= 16 runs on the tensor cores
+ * (tcgen05, fp32 accumulation); other shapes and fp32 run a SIMT fp32 path.
+ * ------------------------------------------------------------------------ */
+size_t ra_partial_workspace_bytes(int64_t Tq, int64_t Tk, int nseg, int Hq, int Hkv, int d, int dtype);
+ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, int dtype,
+                                 int64_t Tq, int64_t Tk, int Hq, int Hkv, int d,
+                                 const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int nseg,
+                                 const int32_t *q_pos, const int32_t *k_pos,
+                                 int causal, float scale,
+                                 float *out, float *lse,
+                                 void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * ra_lse_merge  (DEVICE)
+ *
+ * Merges n_parts partial results of the same queries over disjoint key
+ * sets (the step that combines ring partials; the pages name the ring
+ * schedule, the merge is its textbook completion):
+ *   M = max_p lse_p;  lse = M + log(sum_p exp(lse_p - M));
+ *   out = sum_p exp(lse_p - lse) * out_p;   all -inf -> out 0, lse -inf.
+ *   outs  HOST array [n_parts] of DEVICE fp32 [Tq, Hq, d] pointers
+ *   lses  HOST array [n_parts] of DEVICE fp32 [Hq, Tq] pointers
+ *   out   DEVICE [Tq, Hq, d] of out_dtype (RA_BF16 or RA_FP32)
+ *   lse_out DEVICE [Hq, Tq] fp32 (may be NULL)
+ * 1 <= n_parts <= 64, d a multiple of 4 and <= 256.  out may alias
+ * outs[0] when out_dtype is RA_FP32 (each element is read before written).
+ * ------------------------------------------------------------------------ */
+ra_status ra_lse_merge(int n_parts, const float *const *outs, const float *const *lses,
+                       int64_t Tq, int Hq, int d, void *out, int out_dtype, float *lse_out,
+                       void *stream);
+
+/* ------------------------------------------------------------------------
+ * ra_ring_attn_fwd / ra_ring_attn_bwd  (DEVICE tensors, HOST cu_seqlens)
+ *
+ * The whole simulated ring: zigzag-permute Q/K/V, run the ring over cp
+ * simulated ranks (rank r at step t attends to the K/V of rank
+ * s = (r - t) mod cp), merge, and return results in the ORIGINAL token
+ * order.
+ *   sched RA_SCHED_FUSED    : one launch per direction; the ring steps are
+ *                             the order in which each query tile visits KV
+ *                             tiles and the merge is the on-chip online
+ *                             softmax.  Fully masked tiles are skipped
+ *                             (pruning, FlagScale PR #910).
+ *   sched RA_SCHED_STEPWISE : one partial launch per ring step into fp32
+ *                             buffers, then ra_lse_merge and unpermute
+ *                             (backward: fp32 dK/dV accumulated per step).
+ * Forward:
+ *   q DEVICE [T, Hq, d], k, v DEVICE [T, Hkv, d] (dtype), out DEVICE
+ *   [T, Hq, d] (dtype), lse DEVICE [Hq, T] fp32.
+ * Backward (from the saved lse, textbook gradient):
+ *   out, dout DEVICE [T, Hq, d] (dtype), lse DEVICE [Hq, T];
+ *   dq DEVICE [T, Hq, d], dk, dv DEVICE [T, Hkv, d] of grad_dtype
+ *   (RA_BF16 or RA_FP32; dK/dV are always accumulated in fp32).
+ * scale: softmax scale; pass 1/sqrt(d) for the usual attention (maxtext
+ * PR #1133, cudnn_flash_attention diff).  cp >= 1.
+ * workspace: DEVICE, >= ra_ring_workspace_bytes(...) for the same arguments.
+ * ------------------------------------------------------------------------ */
+size_t ra_ring_workspace_bytes(int64_t T, int Hq, int Hkv, int d, int dtype,
+                               const int32_t *cu_seqlens, int B, int cp, int zz_mode,
+                               int sched, int bwd);
+ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtype,
+                           int64_t T, int Hq, int Hkv, int d,
+                           const int32_t *cu_seqlens, int B, int cp, int zz_mode,
+                           int causal, float scale, int sched,
+                           void *out, float *lse,
+                           void *workspace, size_t ws_bytes, void *stream);
+ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtype,
+                           int64_t T, int Hq, int Hkv, int d,
+                           const int32_t *cu_seqlens, int B, int cp, int zz_mode,
+                           int causal, float scale, int sched,
+                           const void *out, const float *lse, const void *dout,
+                           void *dq, void *dk, void *dv, int grad_dtype,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * ra_ring_rank_pairs  (HOST, synchronous)
+ *
+ * Allowed (query, key) pairs each simulated rank computes over the whole
+ * ring: the causal load that zigzag balances ("Question about varlen ring
+ * attention", MiniMax-01 #6: causal imbalance; ring-attention-pytorch #20:
+ * zigzag spreads it).  counts HOST [cp] int64.
+ * ------------------------------------------------------------------------ */
+ra_status ra_ring_rank_pairs(const int32_t *cu_seqlens, int B, int cp, int zz_mode, int causal,
+                             int64_t *counts);
+
+/* Reads and clears the device status word of the current device (waits for
+ * `stream` first).  Returns RA_OK, RA_ERR_TIMEOUT or RA_ERR_DEVICE_BOUNDS. */
+ra_status ra_get_device_status(void *stream);
+
+/* Self-test of the device-wait guard: launches one CTA that waits on an
+ * mbarrier nothing ever arrives at, with a budget of `budget_us`
+ * microseconds (1..1000000).  The wait runs out, the kernel records
+ * RA_ERR_TIMEOUT in the status word and returns; no copy or MMA is in
+ * flight.  Read the result with ra_get_device_status().  Every real kernel
+ * uses the same guard (2 s budget) on each of its waits. */
+ra_status ra_selftest_wait_timeout(int64_t budget_us, void *stream);
+
+const char *ra_status_string(ra_status s);
+const char *ra_last_error(void);
+const char *ra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RA_H_ */

@@ -1,0 +1,123 @@
+"""C-ABI checks that need no GPU: the library loads and exports every
+symbol include/ra.h declares; the host planner matches the oracle bit for
+bit; argument checks return their status without launching anything."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def ra():
+    from context_varlen_ring_gb300 import build as b
+    b.build()
+    import context_varlen_ring_gb300 as m
+    m.lib()
+    return m
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "ra.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(ra):
+    from context_varlen_ring_gb300 import _lib
+    names = _declared_symbols()
+    assert len(names) >= 15
+    L = ra.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.EXPORTS)
+    assert b"sm_103a" in L.ra_version()
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_host_planner_matches_oracle(ra, orc, mode):
+    rng = np.random.default_rng(11)
+    cases = [W.C0.cu_seqlens(), W.C2.cu_seqlens(), np.array([0, 130]), np.array([0, 3, 4, 6])]
+    for _ in range(25):
+        cases.append(W.cu_seqlens(W.random_doc_lens(rng, 900, 1, 300)))
+    for cu in cases:
+        for cp in (1, 2, 3, 4, 8, 16):
+            p1, o1, c1 = ra.zigzag_plan(cu, cp, mode)
+            p2, o2, c2 = orc.zigzag_plan(cu, cp, mode)
+            assert np.array_equal(p1, p2) and np.array_equal(o1, o2) and np.array_equal(c1, c2)
+
+
+def test_rank_pairs_match_oracle(ra, orc):
+    rng = np.random.default_rng(12)
+    for _ in range(10):
+        cu = W.cu_seqlens(W.random_doc_lens(rng, 2000, 1, 600))
+        for cp in (1, 2, 4, 8):
+            for mode in (0, 1):
+                for causal in (True, False):
+                    assert np.array_equal(ra.ring_rank_pairs(cu, cp, mode, causal),
+                                          orc.rank_pairs(cu, cp, mode, causal))
+
+
+def test_c3_rank_pairs_closed_form(ra):
+    counts = ra.ring_rank_pairs(W.C3.cu_seqlens(), 16, W.ZZ_GLOBAL)
+    assert np.all(counts == 536_875_008) and counts.sum() == 8_590_000_128
+
+
+def _p(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def test_invalid_arguments_return_status(ra):
+    from context_varlen_ring_gb300 import _lib
+    L = ra.lib()
+    perm = np.zeros(8, np.int32)
+    off = np.zeros(3, np.int32)
+    cl = np.zeros(6, np.int32)
+    bad_cus = [np.array([1, 8], np.int32), np.array([0, 5, 3], np.int32)]
+    for cu in bad_cus:
+        assert L.ra_zigzag_plan(_p(cu), len(cu) - 1, 2, 0, _p(perm), _p(off), _p(cl)) == _lib.RA_ERR_INVALID_ARG
+        assert L.ra_last_error()
+    cu = np.array([0, 8], np.int32)
+    assert L.ra_zigzag_plan(_p(cu), 1, 0, 0, _p(perm), _p(off), _p(cl)) == _lib.RA_ERR_INVALID_ARG
+    assert L.ra_zigzag_plan(_p(cu), 1, 2, 7, _p(perm), _p(off), _p(cl)) == _lib.RA_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(256)  # never dereferenced: checks fail before any launch
+    ws = ctypes.c_void_p(4096)
+    args = dict(dt=_lib.RA_BF16, T=8, hq=4, hkv=2, d=128)
+
+    def fwd(cu, T=8, hq=4, hkv=2, d=128, cp=2, mode=0, sched=0, dt=_lib.RA_BF16, q=fake):
+        return L.ra_ring_attn_fwd(q, fake, fake, dt, T, hq, hkv, d, _p(cu), len(cu) - 1, cp, mode, 1, 0.1, sched,
+                                  fake, fake, ws, 1 << 40, None)
+    assert fwd(np.array([0, 7], np.int32)) == _lib.RA_ERR_INVALID_ARG          # cu[B] != T
+    assert fwd(np.array([0, 8], np.int32), hq=3) == _lib.RA_ERR_INVALID_ARG    # Hq % Hkv
+    assert fwd(np.array([0, 8], np.int32), cp=0) == _lib.RA_ERR_INVALID_ARG
+    assert fwd(np.array([0, 8], np.int32), mode=5) == _lib.RA_ERR_INVALID_ARG
+    assert fwd(np.array([0, 8], np.int32), sched=9) == _lib.RA_ERR_INVALID_ARG
+    assert fwd(np.array([0, 8], np.int32), d=100) == _lib.RA_ERR_UNSUPPORTED
+    assert fwd(np.array([0, 8], np.int32), dt=7) == _lib.RA_ERR_INVALID_ARG
+    assert fwd(np.array([0, 8], np.int32), q=ctypes.c_void_p(258)) == _lib.RA_ERR_UNSUPPORTED  # misaligned
+    # too-small workspace is caught before launching
+    cu = np.array([0, 8], np.int32)
+    rc = L.ra_ring_attn_fwd(fake, fake, fake, _lib.RA_BF16, 8, 4, 2, 128, _p(cu), 1, 2, 0, 1, 0.1, 0, fake, fake,
+                            ws, 16, None)
+    assert rc == _lib.RA_ERR_WORKSPACE
+    # merge argument checks
+    assert L.ra_lse_merge(0, None, None, 4, 2, 128, fake, 0, fake, None) == _lib.RA_ERR_INVALID_ARG
+    assert L.ra_lse_merge(65, None, None, 4, 2, 128, fake, 0, fake, None) == _lib.RA_ERR_INVALID_ARG
+    assert L.ra_selftest_wait_timeout(0, None) == _lib.RA_ERR_INVALID_ARG
+    assert L.ra_status_string(_lib.RA_ERR_TIMEOUT) == b"device wait timed out"
+
+
+def test_workspace_sizes(ra):
+    cu = W.C2.cu_seqlens()
+    f = ra.ring_workspace_bytes(32768, 32, 8, 128, 0, cu, 8, W.ZZ_PER_DOC, "fused")
+    s = ra.ring_workspace_bytes(32768, 32, 8, 128, 0, cu, 8, W.ZZ_PER_DOC, "stepwise")
+    b = ra.ring_workspace_bytes(32768, 32, 8, 128, 0, cu, 8, W.ZZ_PER_DOC, "fused", bwd=True)
+    qkv = 32768 * (32 + 16) * 128 * 2
+    assert qkv < f < qkv + (64 << 20)
+    assert s > f + 8 * 32768 * 32 * 128 * 4
+    assert b > f
