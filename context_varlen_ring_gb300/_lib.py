@@ -33,7 +33,7 @@ EXPORTS = (
     "ra_partial_workspace_bytes", "ra_varlen_attn_partial", "ra_lse_merge",
     "ra_ring_workspace_bytes", "ra_ring_attn_fwd", "ra_ring_attn_bwd",
     "ra_ring_rank_pairs", "ra_get_device_status", "ra_selftest_wait_timeout",
-    "ra_status_string", "ra_last_error", "ra_version",
+    "ra_status_string", "ra_last_error", "ra_version", "ra_profile_enable", "ra_profile_read",
 )
 
 _lib = None
@@ -66,6 +66,8 @@ def _declare(L):
         "ra_status_string": (ctypes.c_char_p, [i32]),
         "ra_last_error": (ctypes.c_char_p, []),
         "ra_version": (ctypes.c_char_p, []),
+        "ra_profile_enable": (i32, [i32]),
+        "ra_profile_read": (i32, [i32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)

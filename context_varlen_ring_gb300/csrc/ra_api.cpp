@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -30,6 +31,44 @@ static ra_status cuda_fail(cudaError_t e, const char *what) {
         cudaError_t e_ = (call);                        \
         if (e_ != cudaSuccess) return cuda_fail(e_, what); \
     } while (0)
+
+// ---------------------------------------------------------------- timing
+namespace {
+struct ProfRec {
+    std::string name;
+    cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+}  // namespace
+
+ProfScope::ProfScope(const char *name, cudaStream_t st) : st_(st) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return;
+    cudaEvent_t a = take_event(), b = take_event();
+    if (!a || !b) return;
+    if (cudaEventRecord(a, st) != cudaSuccess) return;
+    g_prof.push_back(ProfRec{name, a, b});
+    id_ = (int)g_prof.size() - 1;
+}
+
+ProfScope::~ProfScope() {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (id_ >= 0 && id_ < (int)g_prof.size()) cudaEventRecord(g_prof[id_].b, st_);
+}
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -62,6 +101,50 @@ using namespace ra;
 extern "C" {
 
 const char *ra_version(void) { return "libra 0.1 (sm_103a)"; }
+
+ra_status ra_profile_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (on) {
+        for (auto &r : g_prof) {
+            g_event_pool.push_back(r.a);
+            g_event_pool.push_back(r.b);
+        }
+        g_prof.clear();
+    }
+    g_prof_on = on != 0;
+    return RA_OK;
+}
+
+int ra_profile_read(int max_kernels, char *names, double *total_ms, int64_t *launches) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    std::vector<std::string> keys;
+    std::vector<double> ms;
+    std::vector<int64_t> cnt;
+    for (auto &r : g_prof) {
+        if (cudaEventSynchronize(r.b) != cudaSuccess) return -1;
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return -1;
+        size_t i = 0;
+        while (i < keys.size() && keys[i] != r.name) ++i;
+        if (i == keys.size()) {
+            keys.push_back(r.name);
+            ms.push_back(0.0);
+            cnt.push_back(0);
+        }
+        ms[i] += t;
+        cnt[i] += 1;
+    }
+    const int n = (int)std::min<size_t>(keys.size(), (size_t)std::max(max_kernels, 0));
+    for (int i = 0; i < n; ++i) {
+        if (names) {
+            std::strncpy(names + (size_t)i * 64, keys[i].c_str(), 63);
+            names[(size_t)i * 64 + 63] = 0;
+        }
+        if (total_ms) total_ms[i] = ms[i];
+        if (launches) launches[i] = cnt[i];
+    }
+    return n;
+}
 
 const char *ra_last_error(void) { return g_last_error.c_str(); }
 
@@ -97,7 +180,10 @@ static ra_status permute_common(const void *src, void *dst, const int32_t *perm,
     if (!src || !dst || !perm) return fail(RA_ERR_INVALID_ARG, "NULL pointer");
     if (T > INT32_MAX) return fail(RA_ERR_UNSUPPORTED, "T must fit in int32");
     PermJob job{src, dst, row_bytes};
-    RA_CUDA(launch_permute(&job, 1, perm, T, inverse, static_cast<cudaStream_t>(stream)), "permute launch");
+    {
+        ProfScope ps(inverse ? "ra_unpermute" : "ra_permute", static_cast<cudaStream_t>(stream));
+        RA_CUDA(launch_permute(&job, 1, perm, T, inverse, static_cast<cudaStream_t>(stream)), "permute launch");
+    }
     return RA_OK;
 }
 
@@ -164,6 +250,7 @@ ra_status ra_lse_merge(int n_parts, const float *const *outs, const float *const
         if (!aligned16(outs[p])) return fail(RA_ERR_UNSUPPORTED, "partial outputs must be 16-byte aligned");
     }
     if (!aligned16(out)) return fail(RA_ERR_UNSUPPORTED, "out must be 16-byte aligned");
+    ProfScope ps("ra_lse_merge", static_cast<cudaStream_t>(stream));
     RA_CUDA(launch_merge(n_parts, outs, lses, Tq, Hq, d, out, out_dtype, lse_out, static_cast<cudaStream_t>(stream)),
             "merge launch");
     return RA_OK;
@@ -239,6 +326,7 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
         a.out = out;
         a.lse = lse;
         a.lse_T = Tq;
+        ProfScope ps("ra_tc_fwd", s);
         RA_CUDA(launch_tc_fwd(a, s), "tensor-core partial launch");
         return RA_OK;
     }
@@ -289,6 +377,7 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
     a.out = out;
     a.lse = lse;
     a.lse_T = Tq;
+    ProfScope ps("ra_simt_fwd", s);
     RA_CUDA(launch_simt_fwd(a, s), "SIMT partial launch");
     return RA_OK;
 }
@@ -392,7 +481,10 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     PermJob jobs[3] = {{q, Qp, (int64_t)Hq * d * (int64_t)es},
                        {k, Kp, (int64_t)Hkv * d * (int64_t)es},
                        {v, Vp, (int64_t)Hkv * d * (int64_t)es}};
-    RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s), "permute launch");
+    {
+        ProfScope ps("ra_permute", s);
+        RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s), "permute launch");
+    }
 
     auto run_partial = [&](int t0, int t1, int out_mode, void *o, float *l, int64_t lse_T) -> ra_status {
         if (tc) {
@@ -420,6 +512,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
             a.out = o;
             a.lse = l;
             a.lse_T = lse_T;
+            ProfScope ps("ra_tc_fwd", s);
             RA_CUDA(launch_tc_fwd(a, s), "tensor-core forward launch");
         } else {
             SimtArgs a{};
@@ -448,6 +541,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
             a.out = o;
             a.lse = l;
             a.lse_T = lse_T;
+            ProfScope ps("ra_simt_fwd", s);
             RA_CUDA(launch_simt_fwd(a, s), "SIMT forward launch");
         }
         return RA_OK;
@@ -470,10 +564,19 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     }
     void *Op = ws + L.op;
     float *Lp = reinterpret_cast<float *>(ws + L.lp);
-    RA_CUDA(launch_merge(cp, po.data(), pl.data(), T, Hq, d, Op, dtype, Lp, s), "merge launch");
+    {
+        ProfScope ps("ra_lse_merge", s);
+        RA_CUDA(launch_merge(cp, po.data(), pl.data(), T, Hq, d, Op, dtype, Lp, s), "merge launch");
+    }
     PermJob uj{Op, out, (int64_t)Hq * d * (int64_t)es};
-    RA_CUDA(launch_permute(&uj, 1, perm, T, 1, s), "unpermute launch");
-    RA_CUDA(launch_unpermute_cols(Lp, lse, perm, T, Hq, s), "lse unpermute launch");
+    {
+        ProfScope ps("ra_unpermute", s);
+        RA_CUDA(launch_permute(&uj, 1, perm, T, 1, s), "unpermute launch");
+    }
+    {
+        ProfScope ps("ra_unpermute_lse", s);
+        RA_CUDA(launch_unpermute_cols(Lp, lse, perm, T, Hq, s), "lse unpermute launch");
+    }
     return RA_OK;
 }
 
@@ -514,8 +617,14 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
                        {k, Kp, (int64_t)Hkv * d * (int64_t)es},
                        {v, Vp, (int64_t)Hkv * d * (int64_t)es},
                        {dout, dOp, (int64_t)Hq * d * (int64_t)es}};
-    RA_CUDA(launch_permute(jobs, 4, perm, T, 0, s), "permute launch");
-    RA_CUDA(launch_rowdot(dout, out, dtype, T, Hq, d, D, s), "rowdot launch");
+    {
+        ProfScope ps("ra_permute", s);
+        RA_CUDA(launch_permute(jobs, 4, perm, T, 0, s), "permute launch");
+    }
+    {
+        ProfScope ps("ra_rowdot", s);
+        RA_CUDA(launch_rowdot(dout, out, dtype, T, Hq, d, D, s), "rowdot launch");
+    }
     RA_CUDA(cudaMemsetAsync(dqa, 0, (size_t)T * Hq * d * 4, s), "memset dq");
     RA_CUDA(cudaMemsetAsync(dka, 0, (size_t)T * Hkv * d * 4, s), "memset dk");
     RA_CUDA(cudaMemsetAsync(dva, 0, (size_t)T * Hkv * d * 4, s), "memset dv");
@@ -547,18 +656,23 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     if (sched == RA_SCHED_FUSED) {
         a.t0 = 0;
         a.t1 = cp;
+        ProfScope ps("ra_simt_bwd", s);
         RA_CUDA(launch_simt_bwd(a, s), "SIMT backward launch");
     } else {
         for (int t = 0; t < cp; ++t) {
             a.t0 = t;
             a.t1 = t + 1;
+            ProfScope ps("ra_simt_bwd", s);
             RA_CUDA(launch_simt_bwd(a, s), "SIMT backward launch");
         }
     }
     // a9: cast to the gradient dtype (rows are already in original order)
-    RA_CUDA(launch_cast_f32(dqa, dq, grad_dtype, T * Hq * d, s), "cast dq");
-    RA_CUDA(launch_cast_f32(dka, dk, grad_dtype, T * Hkv * d, s), "cast dk");
-    RA_CUDA(launch_cast_f32(dva, dv, grad_dtype, T * Hkv * d, s), "cast dv");
+    {
+        ProfScope ps("ra_cast", s);
+        RA_CUDA(launch_cast_f32(dqa, dq, grad_dtype, T * Hq * d, s), "cast dq");
+        RA_CUDA(launch_cast_f32(dka, dk, grad_dtype, T * Hkv * d, s), "cast dk");
+        RA_CUDA(launch_cast_f32(dva, dv, grad_dtype, T * Hkv * d, s), "cast dv");
+    }
     return RA_OK;
 }
 

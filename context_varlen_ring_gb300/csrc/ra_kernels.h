@@ -14,6 +14,18 @@ namespace ra {
 int *device_status_ptr();          // device address of this device's status word
 uint64_t wait_budget_ns();         // budget of every device-side wait
 
+// ------------------------------------------------------------ timing
+// Brackets one launch with CUDA events on `st` when profiling is enabled.
+class ProfScope {
+  public:
+    ProfScope(const char *name, cudaStream_t st);
+    ~ProfScope();
+
+  private:
+    int id_ = -1;
+    cudaStream_t st_;
+};
+
 // ------------------------------------------------------------ permute
 struct PermJob {
     const void *src;

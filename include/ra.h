@@ -213,6 +213,19 @@ ra_status ra_get_device_status(void *stream);
  * uses the same guard (2 s budget) on each of its waits. */
 ra_status ra_selftest_wait_timeout(int64_t budget_us, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Per-kernel timing (HOST).  While enabled, every kernel launch the library
+ * makes is bracketed by two CUDA events recorded on its launching stream.
+ * ra_profile_enable(1) clears earlier records; ra_profile_read waits for
+ * the recorded events and reports, per kernel name (at most max_kernels,
+ * names written as NUL-terminated strings of up to 64 bytes each into
+ * `names`), the summed device time in ms and the launch count.  Returns
+ * the number of kernels reported, or -1 on error.  Timing adds two event
+ * records per launch; keep it off for throughput runs.
+ * ------------------------------------------------------------------------ */
+ra_status ra_profile_enable(int on);
+int ra_profile_read(int max_kernels, char *names, double *total_ms, int64_t *launches);
+
 const char *ra_status_string(ra_status s);
 const char *ra_last_error(void);
 const char *ra_version(void);
