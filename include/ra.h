@@ -129,6 +129,37 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
                                  void *workspace, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * ra_varlen_attn_partial_noalloc  (DEVICE tensors, HOST segment/position
+ * arrays) -- the pages have no counterpart; this is a library convenience.
+ *
+ * The same computation, arguments and results as ra_varlen_attn_partial,
+ * for callers that cannot allocate device memory: a runtime whose memory
+ * pool already owns the GPU, a plugin that is handed only its input and
+ * output buffers, or code that must not risk the implicit device
+ * synchronisation cudaMalloc / cudaFree can cause.  Instead of a caller
+ * workspace it uses a static device array of RA_NOALLOC_SCRATCH_BYTES
+ * (8 MiB) that every GPU which loads the library holds until the process
+ * exits; this call allocates nothing.
+ *  - Size limit: a problem whose ra_partial_workspace_bytes(...) exceeds
+ *    RA_NOALLOC_SCRATCH_BYTES is rejected with RA_ERR_WORKSPACE (the detail
+ *    in ra_last_error() names both sizes); nothing is launched.
+ *  - Set-up: the first call on a device (with that device current) looks up
+ *    the array's device address and caches it.  Make that first call before
+ *    any stream capture.
+ *  - Sharing: all calls on a device share the one array, which keeps the
+ *    last call's contents.  Each call rewrites every table it reads, so no
+ *    state carries over, but calls that overlap on the GPU (different
+ *    streams, or host threads) race on the array: serialise them.
+ * ------------------------------------------------------------------------ */
+#define RA_NOALLOC_SCRATCH_BYTES (8u << 20)
+ra_status ra_varlen_attn_partial_noalloc(const void *q, const void *k, const void *v, int dtype,
+                                         int64_t Tq, int64_t Tk, int Hq, int Hkv, int d,
+                                         const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int nseg,
+                                         const int32_t *q_pos, const int32_t *k_pos,
+                                         int causal, float scale,
+                                         float *out, float *lse, void *stream);
+
+/* ------------------------------------------------------------------------
  * ra_lse_merge  (DEVICE)
  *
  * Merges n_parts partial results of the same queries over disjoint key
