@@ -163,9 +163,13 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
             }
         }
     }
-    // Longest-processing-time first: the grid's first CTAs take the longest
-    // items, so the tail of the launch is short ones.
-    auto by_cost = [](const WorkItem &a, const WorkItem &b) { return a.cost > b.cost; };
+    // KV head major, then longest-processing-time first within a head: the
+    // CTAs resident at any moment read the K/V of one or two heads (tens of
+    // MB), which stays in L2, and the launch ends on short items.
+    auto by_cost = [](const WorkItem &a, const WorkItem &b) {
+        if (a.g != b.g) return a.g < b.g;
+        return a.cost > b.cost;
+    };
     std::stable_sort(tp.items.begin(), tp.items.end(), by_cost);
     std::stable_sort(tp.bitems.begin(), tp.bitems.end(), by_cost);
 }

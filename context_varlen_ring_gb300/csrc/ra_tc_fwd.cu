@@ -17,7 +17,7 @@
 //    is (token, head) with the G query heads of one KV head packed together
 //    (128/G tokens x G heads), so a K/V tile loaded once serves all G heads.
 //  * TMA (3-D tensor maps over [T, H, 128], 128-byte swizzle) stages Q once
-//    and K/V tiles through a 3-slot ring; tcgen05.mma (kind::f16, M=128,
+//    and K/V tiles through a 4-slot ring; tcgen05.mma (kind::f16, M=128,
 //    N=128) computes S = Q K^T and O += P V into TMEM; the MMA is issued by
 //    one thread.
 //  * TMEM: S0, S1, O0, O1 (4 x 128 fp32 columns = all 512).
@@ -25,7 +25,9 @@
 //    allocator, warps 4-7 softmax of query tile 0, warps 8-11 of tile 1.
 //    A softmax thread owns one TMEM lane (one row): it reads S, masks,
 //    takes exp2 in fp32, writes P (bf16) to shared memory in the MMA's
-//    swizzled layout, and rescales its O row in TMEM only when the running
+//    swizzled layout (one P tile shared by the two groups, handed over in
+//    MMA order: a group writes P only after the previous PV read it), and
+//    rescales its O row in TMEM only when the running
 //    max grew by more than 2^8 (otherwise the stale max is kept; the final
 //    normalisation uses the same max, so the result is exact).
 //  * MMA issue order per KV tile j: PV0(j), S0(j+1), PV1(j), S1(j+1), so
@@ -52,15 +54,14 @@ namespace {
 using namespace dev;
 
 constexpr int kThreads = 384;
-constexpr int kSlots = 3;
+constexpr int kSlots = 4;
 constexpr uint32_t kHalf = 16384;        // 128 rows x 128 B (64 bf16) swizzled half-tile
 constexpr uint32_t kTile = 2 * kHalf;    // 128 rows x 128 bf16
 constexpr uint32_t kOffQ0 = 0;
 constexpr uint32_t kOffQ1 = kTile;
 constexpr uint32_t kOffKV = 2 * kTile;
-constexpr uint32_t kOffP0 = kOffKV + kSlots * kTile;
-constexpr uint32_t kOffP1 = kOffP0 + kTile;
-constexpr uint32_t kOffBar = kOffP1 + kTile;
+constexpr uint32_t kOffP = kOffKV + kSlots * kTile;   // one P tile shared by both softmax groups
+constexpr uint32_t kOffBar = kOffP + kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
 
 struct FwdParams {
@@ -159,14 +160,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
     uint64_t *q_full = bars + 0;
-    uint64_t *kv_full = bars + 1;    // [3]
-    uint64_t *kv_empty = bars + 4;   // [3]
-    uint64_t *s_full = bars + 7;     // [2]
-    uint64_t *p_ready = bars + 9;    // [2]
-    uint64_t *o_done = bars + 11;    // [2]
-    uint64_t *mma_done = bars + 13;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 15);
+    uint64_t *kv_full = bars + 1;    // [kSlots]
+    uint64_t *kv_empty = bars + 5;   // [kSlots]
+    uint64_t *s_full = bars + 9;     // [2]
+    uint64_t *p_full = bars + 11;    // P written (128 arrivals), one phase per P use
+    uint64_t *p_free = bars + 12;    // PV done reading P, one phase per P use
+    uint64_t *o_done = bars + 13;    // [2] PVs of each query tile done
+    uint64_t *mma_done = bars + 15;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -205,9 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full + i, 1);
-            mbar_init(p_ready + i, 128);
             mbar_init(o_done + i, 1);
         }
+        mbar_init(p_full, 128);
+        mbar_init(p_free, 1);
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
@@ -273,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);
             const uint32_t q0s = base_s + kOffQ0, q1s = base_s + kOffQ1;
-            const uint32_t p0s = base_s + kOffP0, p1s = base_s + kOffP1;
+            const uint32_t ps = base_s + kOffP;
             const uint32_t kvs = base_s + kOffKV;
             const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
             int kidx, c0, c1;
@@ -281,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             tc_fence_after();
             bool have = ok && it.next(kidx, c0, c1);
             uint32_t np0 = 0, np1 = 0;  // PVs issued per query tile
+            uint32_t npu = 0;           // P uses so far (both query tiles)
             if (have) {
                 if (!mbar_wait(kv_full + 0, 0, wc)) ok = false;
                 tc_fence_after();
@@ -308,11 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 const uint32_t kload = 2 * j + 2, kslot = kload % kSlots;
                 const uint32_t ks = kvs + kslot * kTile;
                 if (cc0 != kSkip) {
-                    if (!mbar_wait(p_ready + 0, np0 & 1u, wc)) break;
+                    if (!mbar_wait(p_full, npu & 1u, wc)) break;
                     tc_fence_after();
-                    issue_pv(tO0, p0s, vs, idesc_o, np0 > 0);
+                    issue_pv(tO0, ps, vs, idesc_o, np0 > 0);
+                    tc_commit(p_free);
                     tc_commit(o_done + 0);
                     ++np0;
+                    ++npu;
                 }
                 if (have_next) {
                     if (!mbar_wait(kv_full + kslot, (kload / kSlots) & 1u, wc)) break;
@@ -323,11 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     }
                 }
                 if (cc1 != kSkip) {
-                    if (!mbar_wait(p_ready + 1, np1 & 1u, wc)) break;
+                    if (!mbar_wait(p_full, npu & 1u, wc)) break;
                     tc_fence_after();
-                    issue_pv(tO1, p1s, vs, idesc_o, np1 > 0);
+                    issue_pv(tO1, ps, vs, idesc_o, np1 > 0);
+                    tc_commit(p_free);
                     tc_commit(o_done + 1);
                     ++np1;
+                    ++npu;
                 }
                 if (have_next) {
                     if (nc1 != kSkip) {
@@ -358,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + 128u * k;
         const uint32_t tO = tmem + lane_base + 256u + 128u * k;
-        uint8_t *P = base + (k ? kOffP1 : kOffP0);
+        uint8_t *P = base + kOffP;
         if (k == 0 || it.has1) {
             const TileD q = load_tile(p.qtiles, k ? qt1 : qt0);
             const int tok = m >> p.log2G;
@@ -373,7 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             uint8_t *prow = P + (m >> 3) * 1024 + (m & 7) * 128;
             const int sw = m & 7;
             bool ok = true;
+            uint32_t npu = 0;  // P uses before this tile (both query tiles, in MMA order)
             while (it.next(kidx, c0, c1)) {
+                const uint32_t u_mine = k ? npu + (c0 != kSkip) : npu;
+                npu += (c0 != kSkip) + (c1 != kSkip);
                 const int cls = k ? c1 : c0;
                 if (cls == kSkip) continue;
                 if (!mbar_wait(s_full + k, nd & 1u, wc)) {
@@ -382,12 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 }
                 tc_fence_after();
                 float s[128];
+                {
+                    uint32_t v[128];
+                    tmem_ld128(tS, v);
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t v[32];
-                    tmem_ld32(tS + 32u * ch, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[32 * ch + i] = __uint_as_float(v[i]);
+                    for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(v[i]);
                 }
                 if (cls == kPartial) {
                     // allowed columns: [0, lim1) in the first position run and
@@ -410,9 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         for (int i = 0; i < 32; ++i) s[32 * ch + i] = ((w >> i) & 1u) ? s[32 * ch + i] : -INFINITY;
                     }
                 }
-                float mx = s[0];
+                // row max as 8 independent chains, then a tree
+                float mx8[8];
 #pragma unroll
-                for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+                for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+                for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
                 const float m_new = fmaxf(m_run, mx * p.scale_log2);
                 const bool need = m_new > m_run + 8.0f;
                 float alpha = 1.f;
@@ -422,30 +437,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     l_run *= alpha;
                 }
                 const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-                if (nd > 0) {
-                    // the previous PV must be done: it reads P and writes O
-                    if (!mbar_wait(o_done + k, (nd - 1) & 1u, wc)) {
+                float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[64];
+#pragma unroll
+                for (int c2 = 0; c2 < 64; ++c2) {
+                    const float a0 = ex2_approx(fmaf(s[2 * c2], p.scale_log2, -m_use));
+                    const float a1 = ex2_approx(fmaf(s[2 * c2 + 1], p.scale_log2, -m_use));
+                    sum8[c2 & 7] += a0 + a1;
+                    pk[c2] = pack_bf16x2(a0, a1);
+                }
+                l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                if (u_mine > 0) {
+                    // the PV of the previous P use (and so every earlier PV,
+                    // including this tile's own O accumulation) is complete
+                    if (!mbar_wait(p_free, (u_mine - 1) & 1u, wc)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                 }
-                float sum = 0.f;
 #pragma unroll
                 for (int c16 = 0; c16 < 16; ++c16) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float a0 = ex2_approx(fmaf(s[8 * c16 + 2 * e], p.scale_log2, -m_use));
-                        const float a1 = ex2_approx(fmaf(s[8 * c16 + 2 * e + 1], p.scale_log2, -m_use));
-                        sum += a0 + a1;
-                        pk[e] = pack_bf16x2(a0, a1);
-                    }
                     const int h = c16 >> 3, c = c16 & 7;
                     *reinterpret_cast<uint4 *>(prow + h * kHalf + ((c ^ sw) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
                 }
-                l_run += sum;
                 // rescale this row of O when the max moved (warp-uniform branch)
                 if (nd > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
@@ -459,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(p_ready + k);
+                mbar_arrive(p_full);
                 ++nd;
             }
             // ---------------------------------------------- epilogue
