@@ -17,17 +17,18 @@
 //    is (token, head) with the G query heads of one KV head packed together
 //    (128/G tokens x G heads), so a K/V tile loaded once serves all G heads.
 //  * TMA (3-D tensor maps over [T, H, 128], 128-byte swizzle) stages Q once
-//    and K/V tiles through a 4-slot ring; tcgen05.mma (kind::f16, M=128,
-//    N=128) computes S = Q K^T and O += P V into TMEM; the MMA is issued by
-//    one thread.
-//  * TMEM: S0, S1, O0, O1 (4 x 128 fp32 columns = all 512).
+//    and K/V tiles through a 5-slot ring; tcgen05.mma (kind::f16, M=128,
+//    N=128) computes S = Q K^T (both operands in shared memory) and
+//    O += P V with P read from TMEM, so the PV product only streams V from
+//    shared memory (the N=128 SS product alone uses the whole shared-memory
+//    read port); the MMA is issued by one thread.
+//  * TMEM: S0, S1, O0, O1 (4 x 128 fp32 columns = all 512); P (bf16) is
+//    written over the first 64 columns of its S.
 //  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
 //    allocator, warps 4-7 softmax of query tile 0, warps 8-11 of tile 1.
 //    A softmax thread owns one TMEM lane (one row): it reads S, masks,
-//    takes exp2 in fp32, writes P (bf16) to shared memory in the MMA's
-//    swizzled layout (one P tile shared by the two groups, handed over in
-//    MMA order: a group writes P only after the previous PV read it), and
-//    rescales its O row in TMEM only when the running
+//    takes exp2 in fp32, writes P (bf16) back to TMEM, and rescales its O
+//    row in TMEM only when the running
 //    max grew by more than 2^8 (otherwise the stale max is kept; the final
 //    normalisation uses the same max, so the result is exact).
 //  * MMA issue order per KV tile j: PV0(j), S0(j+1), PV1(j), S1(j+1), so
@@ -54,14 +55,13 @@ namespace {
 using namespace dev;
 
 constexpr int kThreads = 384;
-constexpr int kSlots = 4;
+constexpr int kSlots = 5;
 constexpr uint32_t kHalf = 16384;        // 128 rows x 128 B (64 bf16) swizzled half-tile
 constexpr uint32_t kTile = 2 * kHalf;    // 128 rows x 128 bf16
 constexpr uint32_t kOffQ0 = 0;
 constexpr uint32_t kOffQ1 = kTile;
 constexpr uint32_t kOffKV = 2 * kTile;
-constexpr uint32_t kOffP = kOffKV + kSlots * kTile;   // one P tile shared by both softmax groups
-constexpr uint32_t kOffBar = kOffP + kTile;
+constexpr uint32_t kOffBar = kOffKV + kSlots * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
 
 struct FwdParams {
@@ -141,13 +141,14 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_s, uint32_t 
     }
 }
 
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_s, uint32_t v_s, uint32_t idesc,
+// O (+)= P V with P (bf16) in TMEM where S was (8 columns per 16 keys) and
+// V in shared memory read MN-major (d contiguous).
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_s, uint32_t idesc,
                                          uint32_t accumulate) {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t aoff = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
         const uint32_t boff = (uint32_t)ks * 2048u;  // 16 key rows of 128 B
-        tc_mma_ss(d_tmem, sdesc_sw128(p_s + aoff, 16, 1024), sdesc_sw128(v_s + boff, kHalf, 1024), idesc,
+        tc_mma_ts(d_tmem, p_tmem + 8u * ks, sdesc_sw128(v_s + boff, kHalf, 1024), idesc,
                   (accumulate || ks > 0) ? 1u : 0u);
     }
 }
@@ -161,14 +162,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
     uint64_t *q_full = bars + 0;
     uint64_t *kv_full = bars + 1;    // [kSlots]
-    uint64_t *kv_empty = bars + 5;   // [kSlots]
-    uint64_t *s_full = bars + 9;     // [2]
-    uint64_t *p_full = bars + 11;    // P written (128 arrivals), one phase per P use
-    uint64_t *p_free = bars + 12;    // PV done reading P, one phase per P use
-    uint64_t *o_done = bars + 13;    // [2] PVs of each query tile done
-    uint64_t *mma_done = bars + 15;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 17);
+    uint64_t *kv_empty = bars + 6;   // [kSlots]
+    uint64_t *s_full = bars + 11;    // [2] S of a query tile computed
+    uint64_t *p_ready = bars + 13;   // [2] P of a query tile written to TMEM (128 arrivals)
+    uint64_t *o_done = bars + 15;    // [2] PV of a query tile done
+    uint64_t *mma_done = bars + 17;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 19);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -207,10 +207,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(s_full + i, 1);
+            mbar_init(p_ready + i, 128);
             mbar_init(o_done + i, 1);
         }
-        mbar_init(p_full, 128);
-        mbar_init(p_free, 1);
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
@@ -276,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);
             const uint32_t q0s = base_s + kOffQ0, q1s = base_s + kOffQ1;
-            const uint32_t ps = base_s + kOffP;
             const uint32_t kvs = base_s + kOffKV;
             const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
             int kidx, c0, c1;
@@ -284,7 +282,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             tc_fence_after();
             bool have = ok && it.next(kidx, c0, c1);
             uint32_t np0 = 0, np1 = 0;  // PVs issued per query tile
-            uint32_t npu = 0;           // P uses so far (both query tiles)
             if (have) {
                 if (!mbar_wait(kv_full + 0, 0, wc)) ok = false;
                 tc_fence_after();
@@ -312,13 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 const uint32_t kload = 2 * j + 2, kslot = kload % kSlots;
                 const uint32_t ks = kvs + kslot * kTile;
                 if (cc0 != kSkip) {
-                    if (!mbar_wait(p_full, npu & 1u, wc)) break;
+                    if (!mbar_wait(p_ready + 0, np0 & 1u, wc)) break;
                     tc_fence_after();
-                    issue_pv(tO0, ps, vs, idesc_o, np0 > 0);
-                    tc_commit(p_free);
+                    issue_pv(tO0, tS0, vs, idesc_o, np0 > 0);
                     tc_commit(o_done + 0);
                     ++np0;
-                    ++npu;
                 }
                 if (have_next) {
                     if (!mbar_wait(kv_full + kslot, (kload / kSlots) & 1u, wc)) break;
@@ -329,13 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     }
                 }
                 if (cc1 != kSkip) {
-                    if (!mbar_wait(p_full, npu & 1u, wc)) break;
+                    if (!mbar_wait(p_ready + 1, np1 & 1u, wc)) break;
                     tc_fence_after();
-                    issue_pv(tO1, ps, vs, idesc_o, np1 > 0);
-                    tc_commit(p_free);
+                    issue_pv(tO1, tS1, vs, idesc_o, np1 > 0);
                     tc_commit(o_done + 1);
                     ++np1;
-                    ++npu;
                 }
                 if (have_next) {
                     if (nc1 != kSkip) {
@@ -366,7 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + 128u * k;
         const uint32_t tO = tmem + lane_base + 256u + 128u * k;
-        uint8_t *P = base + kOffP;
         if (k == 0 || it.has1) {
             const TileD q = load_tile(p.qtiles, k ? qt1 : qt0);
             const int tok = m >> p.log2G;
@@ -376,15 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             float m_run = -INFINITY, l_run = 0.f;
             uint32_t nd = 0;
             int kidx, c0, c1;
-            // swizzled P row: 16-byte chunk c of half h lives at
-            // h*16K + (m/8)*1024 + (m%8)*128 + ((c ^ (m%8)) * 16)
-            uint8_t *prow = P + (m >> 3) * 1024 + (m & 7) * 128;
-            const int sw = m & 7;
             bool ok = true;
-            uint32_t npu = 0;  // P uses before this tile (both query tiles, in MMA order)
             while (it.next(kidx, c0, c1)) {
-                const uint32_t u_mine = k ? npu + (c0 != kSkip) : npu;
-                npu += (c0 != kSkip) + (c1 != kSkip);
                 const int cls = k ? c1 : c0;
                 if (cls == kSkip) continue;
                 if (!mbar_wait(s_full + k, nd & 1u, wc)) {
@@ -447,21 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     pk[c2] = pack_bf16x2(a0, a1);
                 }
                 l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-                if (u_mine > 0) {
-                    // the PV of the previous P use (and so every earlier PV,
-                    // including this tile's own O accumulation) is complete
-                    if (!mbar_wait(p_free, (u_mine - 1) & 1u, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-#pragma unroll
-                for (int c16 = 0; c16 < 16; ++c16) {
-                    const int h = c16 >> 3, c = c16 & 7;
-                    *reinterpret_cast<uint4 *>(prow + h * kHalf + ((c ^ sw) << 4)) =
-                        make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
-                }
+                // P (bf16) replaces the first 64 columns of this row's S in
+                // TMEM; S of this tile completing implies the previous PV of
+                // this query tile (which read the old P) is done.
+                tmem_st64(tS, pk);
                 // rescale this row of O when the max moved (warp-uniform branch)
                 if (nd > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll 1
@@ -473,9 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         tmem_st32(tO + 32u * ch, v);
                     }
                 }
-                fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(p_full);
+                mbar_arrive(p_ready + k);
                 ++nd;
             }
             // ---------------------------------------------- epilogue
