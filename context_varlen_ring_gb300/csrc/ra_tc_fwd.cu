@@ -62,7 +62,8 @@ constexpr uint32_t kOffQ0 = 0;
 constexpr uint32_t kOffQ1 = kTile;
 constexpr uint32_t kOffKV = 2 * kTile;
 constexpr uint32_t kOffBar = kOffKV + kSlots * kTile;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
+constexpr int kRing = 8;                                 // visited-tile descriptors in flight
+constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + barriers/ring + alignment slack
 
 struct FwdParams {
     CUtensorMap tmQ, tmK, tmV;
@@ -98,35 +99,6 @@ __device__ __forceinline__ int classify_q(const QInfo &q, int klen, int kpmin, i
     return kPartial;
 }
 
-// Walks the KV tiles a work item visits, in ring order, skipping tiles that
-// are fully masked for both query tiles.  Every role runs its own copy and
-// sees the same sequence; `next` returns the KV tile's index in the table.
-struct KvIter {
-    const FwdParams *p;
-    QInfo q0, q1;
-    int has1, r, b, t, t_end, j, j_end;
-
-    __device__ __forceinline__ bool next(int &idx, int &c0, int &c1) {
-        for (;;) {
-            while (j >= j_end) {
-                if (t >= t_end) return false;
-                int s = (r - t) % p->cp;
-                if (s < 0) s += p->cp;
-                const int o = s * (p->B + 1) + b;
-                j = __ldg(p->kv_off + o);
-                j_end = __ldg(p->kv_off + o + 1);
-                ++t;
-            }
-            idx = j++;
-            const int klen = __ldg(&p->kvtiles[2 * idx].y);
-            const int4 kb = __ldg(p->kvtiles + 2 * idx + 1);
-            c0 = classify_q(q0, klen, kb.y, kb.z, p->causal);
-            c1 = has1 ? classify_q(q1, klen, kb.y, kb.z, p->causal) : kSkip;
-            if (c0 != kSkip || c1 != kSkip) return true;
-        }
-    }
-};
-
 // Bits [a, b) of the 32 columns starting at `base`.
 __device__ __forceinline__ uint32_t range_bits(int a, int b, int base) {
     const int lo = min(max(a - base, 0), 32), hi = min(max(b - base, 0), 32);
@@ -161,14 +133,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
     uint64_t *q_full = bars + 0;
-    uint64_t *kv_full = bars + 1;    // [kSlots]
-    uint64_t *kv_empty = bars + 6;   // [kSlots]
-    uint64_t *s_full = bars + 11;    // [2] S of a query tile computed
-    uint64_t *p_ready = bars + 13;   // [2] P of a query tile written to TMEM (128 arrivals)
-    uint64_t *o_done = bars + 15;    // [2] PV of a query tile done
+    uint64_t *kv_full = bars + 1;      // [kSlots]
+    uint64_t *kv_empty = bars + 6;     // [kSlots]
+    uint64_t *s_full = bars + 11;      // [2] S of a query tile computed
+    uint64_t *p_ready = bars + 13;     // [2] P of a query tile written to TMEM (128 arrivals)
+    uint64_t *o_done = bars + 15;      // [2] PV of a query tile done
     uint64_t *mma_done = bars + 17;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 19);
+    uint64_t *info_full = bars + 18;   // [kRing] descriptor published
+    uint64_t *info_empty = bars + 26;  // [kRing] descriptor read by every consumer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 34);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 35);
+    int4 *ring = reinterpret_cast<int4 *>(bars + 36);  // [kRing]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -177,26 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const int qt0 = ia.x, qt1 = ia.y, g = ia.z, r = ia.w, b = ib.x;
     const int t0 = p.t0 >= 0 ? p.t0 : ib.y;
     const int t1 = p.t0 >= 0 ? p.t1 : ib.z;
-
-    KvIter it;
-    it.p = &p;
-    it.has1 = qt1 >= 0;
-    {
-        const int4 a0 = __ldg(p.qtiles + 2 * qt0), b0 = __ldg(p.qtiles + 2 * qt0 + 1);
-        it.q0 = QInfo{a0.y, b0.y, b0.z};
-        if (it.has1) {
-            const int4 a1 = __ldg(p.qtiles + 2 * qt1), b1 = __ldg(p.qtiles + 2 * qt1 + 1);
-            it.q1 = QInfo{a1.y, b1.y, b1.z};
-        } else {
-            it.q1 = QInfo{0, 0, 0};
-        }
-    }
-    it.r = r;
-    it.b = b;
-    it.t = t0;
-    it.t_end = t1;
-    it.j = 0;
-    it.j_end = 0;
+    const bool has1 = qt1 >= 0;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -211,6 +167,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             mbar_init(o_done + i, 1);
         }
         mbar_init(mma_done, 1);
+        for (int i = 0; i < kRing; ++i) {
+            mbar_init(info_full + i, 1);
+            // consumers: the MMA thread and every softmax thread in use
+            mbar_init(info_empty + i, 1 + (has1 ? 256 : 128));
+        }
         fence_mbar_init();
     }
     if (warp == 2) {
@@ -222,135 +183,203 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{abort_flag, p.status, p.budget_ns};
+
+    // Visited-tile descriptor published by the producer, one per KV tile in
+    // ring order: x = class0 | class1 << 2 | end << 4, y = len | split << 16,
+    // z = pos0, w = pos1.
+    auto read_info = [&](uint32_t jt, int4 &e) -> bool {
+        const uint32_t slot = jt % kRing;
+        if (!mbar_wait(info_full + slot, (jt / kRing) & 1u, wc)) return false;
+        e = ring[slot];
+        mbar_arrive(info_empty + slot);
+        return true;
+    };
+
     // Register split: 128 x 56 (producer/MMA group) + 256 x 224 (softmax
     // groups) = 64512 = the 384 x 168 registers the CTA is launched with.
     if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
-
-    if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&p.tmQ);
-            tma_prefetch_desc(&p.tmK);
-            tma_prefetch_desc(&p.tmV);
+        if (warp == 0) {
+            // -------------------------------------------- TMA producer
+            // The whole warp walks the KV tile table of this item (32 records
+            // per load), classifies each tile against both query tiles, and
+            // lane 0 publishes the visited ones and loads their K and V.
+            const int4 qa0 = __ldg(p.qtiles + 2 * qt0), qb0 = __ldg(p.qtiles + 2 * qt0 + 1);
+            const QInfo q0{qa0.y, qb0.y, qb0.z};
+            QInfo q1{0, 0, 0};
+            int qrow1 = 0;
+            if (has1) {
+                const int4 qa1 = __ldg(p.qtiles + 2 * qt1), qb1 = __ldg(p.qtiles + 2 * qt1 + 1);
+                q1 = QInfo{qa1.y, qb1.y, qb1.z};
+                qrow1 = qa1.x;
+            }
             const int hq0 = g * p.G;
-            mbar_arrive_expect_tx(q_full, (it.has1 ? 2u : 1u) * kTile);
-            const int qrow0 = __ldg(&p.qtiles[2 * qt0].x);
-            tma_load_3d(base + kOffQ0, &p.tmQ, q_full, 0, hq0, qrow0);
-            tma_load_3d(base + kOffQ0 + kHalf, &p.tmQ, q_full, 64, hq0, qrow0);
-            if (it.has1) {
-                const int qrow1 = __ldg(&p.qtiles[2 * qt1].x);
-                tma_load_3d(base + kOffQ1, &p.tmQ, q_full, 0, hq0, qrow1);
-                tma_load_3d(base + kOffQ1 + kHalf, &p.tmQ, q_full, 64, hq0, qrow1);
-            }
-            uint32_t u = 0;
-            int kidx, c0, c1;
-            bool ok = true;
-            while (ok && it.next(kidx, c0, c1)) {
-                const int krow0 = __ldg(&p.kvtiles[2 * kidx].x);
-                for (int kv = 0; kv < 2; ++kv, ++u) {
-                    const uint32_t slot = u % kSlots, ph = (u / kSlots) & 1u;
-                    if (!mbar_wait(kv_empty + slot, ph ^ 1u, wc)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *dst = base + kOffKV + slot * kTile;
-                    const CUtensorMap *m = kv ? &p.tmV : &p.tmK;
-                    mbar_arrive_expect_tx(kv_full + slot, kTile);
-                    tma_load_3d(dst, m, kv_full + slot, 0, g, krow0);
-                    tma_load_3d(dst + kHalf, m, kv_full + slot, 64, g, krow0);
+            if (lane == 0) {
+                tma_prefetch_desc(&p.tmQ);
+                tma_prefetch_desc(&p.tmK);
+                tma_prefetch_desc(&p.tmV);
+                mbar_arrive_expect_tx(q_full, (has1 ? 2u : 1u) * kTile);
+                tma_load_3d(base + kOffQ0, &p.tmQ, q_full, 0, hq0, qa0.x);
+                tma_load_3d(base + kOffQ0 + kHalf, &p.tmQ, q_full, 64, hq0, qa0.x);
+                if (has1) {
+                    tma_load_3d(base + kOffQ1, &p.tmQ, q_full, 0, hq0, qrow1);
+                    tma_load_3d(base + kOffQ1 + kHalf, &p.tmQ, q_full, 64, hq0, qrow1);
                 }
             }
-            // Drain: the last copy into each slot (and Q) must have landed
-            // before the CTA may exit.
-            volatile int local_abort = 0;
-            const WaitCtl drain{&local_abort, p.status, p.budget_ns};
-            (void)mbar_wait(q_full, 0, drain);
-            for (uint32_t x = (u > kSlots ? u - kSlots : 0); x < u; ++x)
-                (void)mbar_wait(kv_full + (x % kSlots), (x / kSlots) & 1u, drain);
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-            const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);
-            const uint32_t q0s = base_s + kOffQ0, q1s = base_s + kOffQ1;
-            const uint32_t kvs = base_s + kOffKV;
-            const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-            int kidx, c0, c1;
-            bool ok = mbar_wait(q_full, 0, wc);
-            tc_fence_after();
-            bool have = ok && it.next(kidx, c0, c1);
-            uint32_t np0 = 0, np1 = 0;  // PVs issued per query tile
-            if (have) {
-                if (!mbar_wait(kv_full + 0, 0, wc)) ok = false;
-                tc_fence_after();
+            uint32_t u = 0, jt = 0;
+            int ok = 1;
+            for (int t = t0; t < t1 && ok; ++t) {
+                int s = (r - t) % p.cp;
+                if (s < 0) s += p.cp;
+                const int o = s * (p.B + 1) + b;
+                const int lo = __ldg(p.kv_off + o), hi = __ldg(p.kv_off + o + 1);
+                for (int base_idx = lo; base_idx < hi && ok; base_idx += 32) {
+                    const int idx = base_idx + lane;
+                    int4 ka = make_int4(0, 0, 0, 0), kb = make_int4(0, 0, 0, 0);
+                    int c0 = kSkip, c1 = kSkip;
+                    if (idx < hi) {
+                        ka = __ldg(p.kvtiles + 2 * idx);
+                        kb = __ldg(p.kvtiles + 2 * idx + 1);
+                        c0 = classify_q(q0, ka.y, kb.y, kb.z, p.causal);
+                        c1 = has1 ? classify_q(q1, ka.y, kb.y, kb.z, p.causal) : kSkip;
+                    }
+                    uint32_t vis = __ballot_sync(0xffffffffu, c0 != kSkip || c1 != kSkip);
+                    while (vis && ok) {
+                        const int src = __ffs(vis) - 1;
+                        vis &= vis - 1;
+                        const int row0 = __shfl_sync(0xffffffffu, ka.x, src);
+                        const int len = __shfl_sync(0xffffffffu, ka.y, src);
+                        const int split = __shfl_sync(0xffffffffu, ka.z, src);
+                        const int pos0 = __shfl_sync(0xffffffffu, ka.w, src);
+                        const int pos1 = __shfl_sync(0xffffffffu, kb.x, src);
+                        const int cc = __shfl_sync(0xffffffffu, c0 | (c1 << 2), src);
+                        if (lane == 0) {
+                            const uint32_t e = jt % kRing;
+                            if (!mbar_wait(info_empty + e, ((jt / kRing) & 1u) ^ 1u, wc)) ok = 0;
+                            if (ok) {
+                                ring[e] = make_int4(cc, len | (split << 16), pos0, pos1);
+                                mbar_arrive(info_full + e);
+                            }
+                            for (int kv = 0; kv < 2 && ok; ++kv, ++u) {
+                                const uint32_t slot = u % kSlots, ph = (u / kSlots) & 1u;
+                                if (!mbar_wait(kv_empty + slot, ph ^ 1u, wc)) {
+                                    ok = 0;
+                                    break;
+                                }
+                                uint8_t *dst = base + kOffKV + slot * kTile;
+                                const CUtensorMap *m = kv ? &p.tmV : &p.tmK;
+                                mbar_arrive_expect_tx(kv_full + slot, kTile);
+                                tma_load_3d(dst, m, kv_full + slot, 0, g, row0);
+                                tma_load_3d(dst + kHalf, m, kv_full + slot, 64, g, row0);
+                            }
+                        }
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        ++jt;
+                    }
+                }
+            }
+            if (lane == 0) {
                 if (ok) {
-                    if (c0 != kSkip) {
-                        issue_s(tS0, q0s, kvs, idesc_s);
-                        tc_commit(s_full + 0);
+                    // end marker
+                    const uint32_t e = jt % kRing;
+                    if (mbar_wait(info_empty + e, ((jt / kRing) & 1u) ^ 1u, wc)) {
+                        ring[e] = make_int4(1 << 4, 0, 0, 0);
+                        mbar_arrive(info_full + e);
                     }
-                    if (c1 != kSkip) {
-                        issue_s(tS1, q1s, kvs, idesc_s);
-                        tc_commit(s_full + 1);
-                    }
-                    tc_commit(kv_empty + 0);
                 }
+                // Drain: the last copy into each slot (and Q) must have landed
+                // before the CTA may exit.
+                volatile int local_abort = 0;
+                const WaitCtl drain{&local_abort, p.status, p.budget_ns};
+                (void)mbar_wait(q_full, 0, drain);
+                for (uint32_t x = (u > kSlots ? u - kSlots : 0); x < u; ++x)
+                    (void)mbar_wait(kv_full + (x % kSlots), (x / kSlots) & 1u, drain);
             }
-            uint32_t j = 0;
-            while (ok && have) {
-                const int cc0 = c0, cc1 = c1;
-                int nidx, nc0 = kSkip, nc1 = kSkip;
-                const bool have_next = it.next(nidx, nc0, nc1);
-                const uint32_t vidx = 2 * j + 1, vslot = vidx % kSlots;
-                if (!mbar_wait(kv_full + vslot, (vidx / kSlots) & 1u, wc)) break;
+        } else if (warp == 1) {
+            // -------------------------------------------- MMA issuer
+            if (lane == 0) {
+                const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+                const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);
+                const uint32_t q0s = base_s + kOffQ0, q1s = base_s + kOffQ1;
+                const uint32_t kvs = base_s + kOffKV;
+                const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+                bool ok = mbar_wait(q_full, 0, wc);
                 tc_fence_after();
-                const uint32_t vs = kvs + vslot * kTile;
-                const uint32_t kload = 2 * j + 2, kslot = kload % kSlots;
-                const uint32_t ks = kvs + kslot * kTile;
-                if (cc0 != kSkip) {
-                    if (!mbar_wait(p_ready + 0, np0 & 1u, wc)) break;
+                int4 e;
+                ok = ok && read_info(0, e);
+                bool have = ok && !(e.x & 16);
+                int c0 = e.x & 3, c1 = (e.x >> 2) & 3;
+                uint32_t np0 = 0, np1 = 0;  // PVs issued per query tile
+                if (have) {
+                    if (!mbar_wait(kv_full + 0, 0, wc)) ok = false;
                     tc_fence_after();
-                    issue_pv(tO0, tS0, vs, idesc_o, np0 > 0);
-                    tc_commit(o_done + 0);
-                    ++np0;
-                }
-                if (have_next) {
-                    if (!mbar_wait(kv_full + kslot, (kload / kSlots) & 1u, wc)) break;
-                    tc_fence_after();
-                    if (nc0 != kSkip) {
-                        issue_s(tS0, q0s, ks, idesc_s);
-                        tc_commit(s_full + 0);
+                    if (ok) {
+                        if (c0 != kSkip) {
+                            issue_s(tS0, q0s, kvs, idesc_s);
+                            tc_commit(s_full + 0);
+                        }
+                        if (c1 != kSkip) {
+                            issue_s(tS1, q1s, kvs, idesc_s);
+                            tc_commit(s_full + 1);
+                        }
+                        tc_commit(kv_empty + 0);
                     }
                 }
-                if (cc1 != kSkip) {
-                    if (!mbar_wait(p_ready + 1, np1 & 1u, wc)) break;
+                uint32_t j = 0;
+                while (ok && have) {
+                    const int cc0 = c0, cc1 = c1;
+                    int4 en;
+                    if (!read_info(j + 1, en)) break;
+                    const bool have_next = !(en.x & 16);
+                    const int nc0 = en.x & 3, nc1 = (en.x >> 2) & 3;
+                    const uint32_t vidx = 2 * j + 1, vslot = vidx % kSlots;
+                    if (!mbar_wait(kv_full + vslot, (vidx / kSlots) & 1u, wc)) break;
                     tc_fence_after();
-                    issue_pv(tO1, tS1, vs, idesc_o, np1 > 0);
-                    tc_commit(o_done + 1);
-                    ++np1;
-                }
-                if (have_next) {
-                    if (nc1 != kSkip) {
-                        issue_s(tS1, q1s, ks, idesc_s);
-                        tc_commit(s_full + 1);
+                    const uint32_t vs = kvs + vslot * kTile;
+                    const uint32_t kload = 2 * j + 2, kslot = kload % kSlots;
+                    const uint32_t ks = kvs + kslot * kTile;
+                    if (cc0 != kSkip) {
+                        if (!mbar_wait(p_ready + 0, np0 & 1u, wc)) break;
+                        tc_fence_after();
+                        issue_pv(tO0, tS0, vs, idesc_o, np0 > 0);
+                        tc_commit(o_done + 0);
+                        ++np0;
                     }
-                    tc_commit(kv_empty + kslot);
+                    if (have_next) {
+                        if (!mbar_wait(kv_full + kslot, (kload / kSlots) & 1u, wc)) break;
+                        tc_fence_after();
+                        if (nc0 != kSkip) {
+                            issue_s(tS0, q0s, ks, idesc_s);
+                            tc_commit(s_full + 0);
+                        }
+                    }
+                    if (cc1 != kSkip) {
+                        if (!mbar_wait(p_ready + 1, np1 & 1u, wc)) break;
+                        tc_fence_after();
+                        issue_pv(tO1, tS1, vs, idesc_o, np1 > 0);
+                        tc_commit(o_done + 1);
+                        ++np1;
+                    }
+                    if (have_next) {
+                        if (nc1 != kSkip) {
+                            issue_s(tS1, q1s, ks, idesc_s);
+                            tc_commit(s_full + 1);
+                        }
+                        tc_commit(kv_empty + kslot);
+                    }
+                    tc_commit(kv_empty + vslot);
+                    if (!have_next) break;
+                    c0 = nc0;
+                    c1 = nc1;
+                    ++j;
                 }
-                tc_commit(kv_empty + vslot);
-                if (!have_next) break;
-                c0 = nc0;
-                c1 = nc1;
-                kidx = nidx;
-                ++j;
+                // every MMA issued must have completed before TMEM is released
+                tc_commit(mma_done);
+                volatile int local_abort = 0;
+                const WaitCtl drain{&local_abort, p.status, p.budget_ns};
+                (void)mbar_wait(mma_done, 0, drain);
             }
-            // every MMA issued must have completed before TMEM is released
-            tc_commit(mma_done);
-            volatile int local_abort = 0;
-            const WaitCtl drain{&local_abort, p.status, p.budget_ns};
-            (void)mbar_wait(mma_done, 0, drain);
         }
-    }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
         // ------------------------------------------------ softmax / epilogue
@@ -359,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + 128u * k;
         const uint32_t tO = tmem + lane_base + 256u + 128u * k;
-        if (k == 0 || it.has1) {
+        if (k == 0 || has1) {
             const TileD q = load_tile(p.qtiles, k ? qt1 : qt0);
             const int tok = m >> p.log2G;
             const int head = g * p.G + (m & (p.G - 1));
@@ -367,10 +396,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             const int qpos = tok < q.split ? q.pos0 + tok : q.pos1 + (tok - q.split);
             float m_run = -INFINITY, l_run = 0.f;
             uint32_t nd = 0;
-            int kidx, c0, c1;
             bool ok = true;
-            while (it.next(kidx, c0, c1)) {
-                const int cls = k ? c1 : c0;
+            for (uint32_t jt = 0;; ++jt) {
+                int4 e;
+                if (!read_info(jt, e)) {
+                    ok = false;
+                    break;
+                }
+                if (e.x & 16) break;
+                const int cls = k ? ((e.x >> 2) & 3) : (e.x & 3);
                 if (cls == kSkip) continue;
                 if (!mbar_wait(s_full + k, nd & 1u, wc)) {
                     ok = false;
@@ -387,9 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 if (cls == kPartial) {
                     // allowed columns: [0, lim1) in the first position run and
                     // [split, lim2) in the second, as one bit per column
-                    const int4 ka = __ldg(p.kvtiles + 2 * kidx);
-                    const int kt_len = ka.y, kt_split = ka.z, kt_pos0 = ka.w;
-                    const int kt_pos1 = __ldg(&p.kvtiles[2 * kidx + 1].x);
+                    const int kt_len = e.y & 0xffff, kt_split = e.y >> 16, kt_pos0 = e.z, kt_pos1 = e.w;
                     int lim1, lim2;
                     if (p.causal) {
                         lim1 = min(max(qpos - kt_pos0 + 1, 0), kt_split);
