@@ -626,44 +626,88 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         RA_CUDA(launch_rowdot(dout, out, dtype, T, Hq, d, D, s), "rowdot launch");
     }
     RA_CUDA(cudaMemsetAsync(dqa, 0, (size_t)T * Hq * d * 4, s), "memset dq");
-    RA_CUDA(cudaMemsetAsync(dka, 0, (size_t)T * Hkv * d * 4, s), "memset dk");
-    RA_CUDA(cudaMemsetAsync(dva, 0, (size_t)T * Hkv * d * 4, s), "memset dv");
+    if (!(tc && sched == RA_SCHED_FUSED)) {
+        RA_CUDA(cudaMemsetAsync(dka, 0, (size_t)T * Hkv * d * 4, s), "memset dk");
+        RA_CUDA(cudaMemsetAsync(dva, 0, (size_t)T * Hkv * d * 4, s), "memset dv");
+    }
     // a8: per ring step (STEPWISE: one launch per step, fp32 dK/dV += per
-    // step) or all steps in one launch (FUSED)
-    SimtBwdArgs a{};
-    a.q = Qp;
-    a.k = Kp;
-    a.v = Vp;
-    a.dout = dOp;
-    a.dtype = dtype;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.d = d;
-    a.T = T;
-    a.off = off;
-    a.cul = cul;
-    a.pos = perm;
-    a.cp = cp;
-    a.B = B;
-    a.causal = causal;
-    a.scale = scale;
-    a.lse = lse;
-    a.D = D;
-    a.lse_T = T;
-    a.dq = dqa;
-    a.dk = dka;
-    a.dv = dva;
-    if (sched == RA_SCHED_FUSED) {
-        a.t0 = 0;
-        a.t1 = cp;
-        ProfScope ps("ra_simt_bwd", s);
-        RA_CUDA(launch_simt_bwd(a, s), "SIMT backward launch");
+    // step) or all steps in one launch (FUSED: dK/dV accumulate on chip)
+    if (tc) {
+        TcBwdArgs a{};
+        a.q = Qp;
+        a.k = Kp;
+        a.v = Vp;
+        a.dout = dOp;
+        a.T = T;
+        a.Hq = Hq;
+        a.Hkv = Hkv;
+        a.G = G;
+        a.qtiles = tab + dt.o_qt;
+        a.kvtiles = tab + dt.o_kt;
+        a.q_off = reinterpret_cast<const int32_t *>(tab + dt.o_qoff);
+        a.items = tab + dt.o_bitems;
+        a.n_items = dt.n_bitems;
+        a.cp = cp;
+        a.B = B;
+        a.causal = causal;
+        a.scale = scale;
+        a.lse = lse;
+        a.D = D;
+        a.lse_T = T;
+        a.dq = dqa;
+        a.dk = dka;
+        a.dv = dva;
+        if (sched == RA_SCHED_FUSED) {
+            a.t0 = 0;
+            a.t1 = cp;
+            a.kv_accumulate = 0;
+            ProfScope ps("ra_tc_bwd", s);
+            RA_CUDA(launch_tc_bwd(a, s), "tensor-core backward launch");
+        } else {
+            a.kv_accumulate = 1;
+            for (int t = 0; t < cp; ++t) {
+                a.t0 = t;
+                a.t1 = t + 1;
+                ProfScope ps("ra_tc_bwd", s);
+                RA_CUDA(launch_tc_bwd(a, s), "tensor-core backward launch");
+            }
+        }
     } else {
-        for (int t = 0; t < cp; ++t) {
-            a.t0 = t;
-            a.t1 = t + 1;
+        SimtBwdArgs a{};
+        a.q = Qp;
+        a.k = Kp;
+        a.v = Vp;
+        a.dout = dOp;
+        a.dtype = dtype;
+        a.Hq = Hq;
+        a.Hkv = Hkv;
+        a.d = d;
+        a.T = T;
+        a.off = off;
+        a.cul = cul;
+        a.pos = perm;
+        a.cp = cp;
+        a.B = B;
+        a.causal = causal;
+        a.scale = scale;
+        a.lse = lse;
+        a.D = D;
+        a.lse_T = T;
+        a.dq = dqa;
+        a.dk = dka;
+        a.dv = dva;
+        if (sched == RA_SCHED_FUSED) {
+            a.t0 = 0;
+            a.t1 = cp;
             ProfScope ps("ra_simt_bwd", s);
             RA_CUDA(launch_simt_bwd(a, s), "SIMT backward launch");
+        } else {
+            for (int t = 0; t < cp; ++t) {
+                a.t0 = t;
+                a.t1 = t + 1;
+                ProfScope ps("ra_simt_bwd", s);
+                RA_CUDA(launch_simt_bwd(a, s), "SIMT backward launch");
+            }
         }
     }
     // a9: cast to the gradient dtype (rows are already in original order)

@@ -113,6 +113,27 @@ struct TcFwdArgs {
 cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st);
 bool tc_fwd_supported(int dtype, int d, int Hq, int Hkv);
 
+// Tensor-core backward (bf16, d = 128): one CTA per KV tile and KV head.
+struct TcBwdArgs {
+    const void *q, *k, *v, *dout;      // permuted buffers
+    int64_t T;
+    int Hq, Hkv, G;
+    const void *qtiles, *kvtiles;      // Tile records
+    const int32_t *q_off;              // [cp*(B+1)+1]
+    const void *items;                 // backward WorkItem records (qt0 = KV tile)
+    int n_items;
+    int cp, B;
+    int t0, t1;                        // >= 0: override every item's step range
+    int causal;
+    float scale;
+    const float *lse, *D;              // [Hq, lse_T] at original positions
+    int64_t lse_T;
+    float *dq;                         // fp32 [T, Hq, d] at original positions, atomically added
+    float *dk, *dv;                    // fp32 [T, Hkv, d] at original positions
+    int kv_accumulate;                 // 1: dk/dv += (ring steps in separate launches)
+};
+cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st);
+
 // Device-wait self-test (see ra_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t st);
 

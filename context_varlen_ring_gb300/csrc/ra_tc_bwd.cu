@@ -1,0 +1,588 @@
+// ra_tc_bwd.cu -- tensor-core backward of packed causal varlen ring
+// attention (bf16 in, fp32 accumulation, head dim 128) for sm_103a.
+//
+// What it computes: the textbook gradient of softmax attention from the
+// saved log-sum-exp (the backward half of the RingAttention interface of
+// "[Train] Support custom attention with context parallel", FlagScale PR
+// #910, backward_impl):
+//   P  = exp(scale * Q K^T - lse)        over allowed pairs
+//   dV = P^T dO,   dP = dO V^T,   dS = P o (dP - D),  D = rowsum(dO o O)
+//   dQ = scale * dS K,            dK = scale * dS^T Q
+// with GQA sums over the query heads of each KV head.  In the ring, the K/V
+// shard of rank s meets the queries of rank r = (s + t) mod cp at step t;
+// one CTA owns one KV tile and walks the query tiles of its document over
+// the ring steps, so dK and dV accumulate in fp32 (TMEM) across all steps
+// and are written once; dQ rows receive fp32 atomic adds.
+//
+// GB300 design:
+//  * CTA = one KV tile (128 keys of one KV head).  K and V stay in shared
+//    memory; query tiles (128 MMA rows = 128/G tokens x G heads, as in the
+//    forward) and dO tiles stream through two TMA stages together with the
+//    tile's 128 LSE and D values.
+//  * TMEM (512 columns): dK [0,128), dV [128,256), S^T then P^T (bf16, first
+//    64 columns) [256,384), dP^T then dQ [384,512).
+//  * Per query tile the MMA thread issues, in order:
+//      S^T = K Q^T, dP^T = V dO^T, dV += P^T dO (P from TMEM), next S^T,
+//      dK += dS^T Q, dQ = dS K (dS^T in shared memory read MN-major),
+//    and the compute warpgroup (one thread per key row) turns S^T into P^T
+//    while dP^T runs, builds dS^T while dV runs, and drains dQ with
+//    vector atomics while the next tile's S^T/dP^T run.
+//  * Every wait is bounded (2 s); a wait that runs out records
+//    RA_ERR_TIMEOUT and the CTA drains its copies and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "ra_dev.cuh"
+#include "ra_internal.h"
+#include "ra_kernels.h"
+
+namespace ra {
+
+namespace {
+
+using namespace dev;
+
+constexpr int kThreads = 256;
+constexpr uint32_t kHalf = 16384;
+constexpr uint32_t kTile = 2 * kHalf;
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV = kTile;
+constexpr uint32_t kOffQ = 2 * kTile;             // [2] stages
+constexpr uint32_t kOffDO = 4 * kTile;            // [2] stages
+constexpr uint32_t kOffDS = 6 * kTile;            // dS^T, K-major swizzled
+constexpr uint32_t kOffLse = 7 * kTile;           // [2][128] fp32, scaled to log2
+constexpr uint32_t kOffD = kOffLse + 2 * 512;     // [2][128] fp32
+constexpr uint32_t kOffDesc = kOffD + 2 * 512;    // [2] x 2 int4
+constexpr uint32_t kOffBar = kOffDesc + 64;
+constexpr uint32_t kSmemBytes = kOffBar + 128;    // base must be 1024-aligned (checked)
+
+struct BwdParams {
+    CUtensorMap tmQ, tmK, tmV, tmDO;
+    const int4 *qtiles, *kvtiles, *items;
+    const int *q_off;
+    int n_items, cp, B, G, log2G, Hq, Hkv;
+    int t0, t1, causal, kv_accumulate;
+    float scale, scale_log2;
+    const float *lse, *D;
+    long long lse_T;
+    float *dq, *dk, *dv;
+    int *status;
+    unsigned long long budget_ns;
+};
+
+struct QInfo {
+    int len, pmin, pmax;
+};
+
+__device__ __forceinline__ int classify_pair(const QInfo &q, int klen, int kpmin, int kpmax, int causal) {
+    if (q.len <= 0 || klen <= 0) return kSkip;
+    if (causal && q.pmax < kpmin) return kSkip;
+    if (klen == kBN && (!causal || q.pmin >= kpmax)) return kFull;
+    return kPartial;
+}
+
+__device__ __forceinline__ uint32_t range_bits(int a, int b, int base) {
+    const int lo = min(max(a - base, 0), 32), hi = min(max(b - base, 0), 32);
+    return (uint32_t)(((1ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
+}
+
+// D[tmem] = A B^T, both K-major (d contiguous) in shared memory.
+__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_s, uint32_t b_s, uint32_t idesc) {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t off = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
+        tc_mma_ss(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024), idesc, ks > 0);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t base_s = smem_u32(smem);
+    if (base_s & 1023u) {  // the layout has no slack for realignment
+        if (threadIdx.x == 0) record_status(p.status, RA_ERR_DEVICE_BOUNDS);
+        return;
+    }
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *kv_full = bars + 0;
+    uint64_t *st_full = bars + 1;    // [2] Q, dO, lse, D and descriptor of a stage (32 arrivals)
+    uint64_t *st_empty = bars + 3;   // [2]
+    uint64_t *s_full = bars + 5;     // S^T done
+    uint64_t *dp_full = bars + 6;    // dP^T done
+    uint64_t *p_ready = bars + 7;    // P^T in TMEM (128 arrivals)
+    uint64_t *ds_ready = bars + 8;   // dS^T in shared memory (128 arrivals)
+    uint64_t *dq_full = bars + 9;    // dQ done (and dK, so dS^T is free)
+    uint64_t *dq_empty = bars + 10;  // dQ read out (128 arrivals)
+    uint64_t *mma_done = bars + 11;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 13);
+    float *lse_st = reinterpret_cast<float *>(smem + kOffLse);
+    float *d_st = reinterpret_cast<float *>(smem + kOffD);
+    int4 *desc = reinterpret_cast<int4 *>(smem + kOffDesc);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int4 ia = __ldg(p.items + 2 * blockIdx.x), ib = __ldg(p.items + 2 * blockIdx.x + 1);
+    const int kt = ia.x, g = ia.z, s = ia.w, b = ib.x;
+    const int t0 = p.t0 >= 0 ? p.t0 : ib.y;
+    const int t1 = p.t0 >= 0 ? p.t1 : ib.z;
+    const int4 ka = __ldg(p.kvtiles + 2 * kt), kb = __ldg(p.kvtiles + 2 * kt + 1);
+    // KV tile: row0 ka.x, len ka.y, split ka.z, pos0 ka.w, pos1 kb.x, pmin kb.y, pmax kb.z
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(kv_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(st_full + i, 32);
+            mbar_init(st_empty + i, 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(dp_full, 1);
+        mbar_init(p_ready, 128);
+        mbar_init(ds_ready, 128);
+        mbar_init(dq_full, 1);
+        mbar_init(dq_empty, 128);
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtl wc{abort_flag, p.status, p.budget_ns};
+    const uint32_t tDK = tmem, tDV = tmem + 128, tS = tmem + 256, tDP = tmem + 384;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        const int G = p.G;
+        if (lane == 0) {
+            tma_prefetch_desc(&p.tmQ);
+            tma_prefetch_desc(&p.tmK);
+            tma_prefetch_desc(&p.tmV);
+            tma_prefetch_desc(&p.tmDO);
+            mbar_arrive_expect_tx(kv_full, 2 * kTile);
+            tma_load_3d(smem + kOffK, &p.tmK, kv_full, 0, g, ka.x);
+            tma_load_3d(smem + kOffK + kHalf, &p.tmK, kv_full, 64, g, ka.x);
+            tma_load_3d(smem + kOffV, &p.tmV, kv_full, 0, g, ka.x);
+            tma_load_3d(smem + kOffV + kHalf, &p.tmV, kv_full, 64, g, ka.x);
+        }
+        uint32_t n = 0;
+        int ok = 1;
+        const float log2e = 1.4426950408889634f;
+        auto publish = [&](int4 d0, int4 d1, bool end) {
+            const uint32_t st = n & 1u;
+            if (lane == 0 && !mbar_wait(st_empty + st, ((n >> 1) & 1u) ^ 1u, wc)) ok = 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) return;
+            if (!end) {
+                // 128 columns (token, head) of this query tile: LSE (log2) and D
+                const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = lane + 32 * e;
+                    const int tok = c >> p.log2G, head = g * G + (c & (G - 1));
+                    float l2 = INFINITY, dd = 0.f;
+                    if (tok < qlen) {
+                        const int pos = tok < split ? pos0 + tok : pos1 + (tok - split);
+                        const float l = __ldg(p.lse + (long long)head * p.lse_T + pos);
+                        l2 = (l == -INFINITY) ? INFINITY : l * log2e;
+                        dd = __ldg(p.D + (long long)head * p.lse_T + pos);
+                    }
+                    lse_st[st * 128 + c] = l2;
+                    d_st[st * 128 + c] = dd;
+                }
+            }
+            if (lane == 0) {
+                desc[2 * st] = d0;
+                desc[2 * st + 1] = end ? make_int4(0, 1, 0, 0) : d1;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (!end) {
+                    mbar_arrive_expect_tx(st_full + st, 2 * kTile);
+                    const int hq0 = g * G;
+                    tma_load_3d(smem + kOffQ + st * kTile, &p.tmQ, st_full + st, 0, hq0, d0.x);
+                    tma_load_3d(smem + kOffQ + st * kTile + kHalf, &p.tmQ, st_full + st, 64, hq0, d0.x);
+                    tma_load_3d(smem + kOffDO + st * kTile, &p.tmDO, st_full + st, 0, hq0, d0.x);
+                    tma_load_3d(smem + kOffDO + st * kTile + kHalf, &p.tmDO, st_full + st, 64, hq0, d0.x);
+                } else {
+                    mbar_arrive(st_full + st);
+                }
+            } else {
+                mbar_arrive(st_full + st);
+            }
+            ++n;
+        };
+        for (int t = t0; t < t1 && ok; ++t) {
+            const int r = (s + t) % p.cp;
+            const int o = r * (p.B + 1) + b;
+            const int lo = __ldg(p.q_off + o), hi = __ldg(p.q_off + o + 1);
+            for (int bi = lo; bi < hi && ok; bi += 32) {
+                const int idx = bi + lane;
+                int4 qa = make_int4(0, 0, 0, 0), qb = make_int4(0, 0, 0, 0);
+                int cls = kSkip;
+                if (idx < hi) {
+                    qa = __ldg(p.qtiles + 2 * idx);
+                    qb = __ldg(p.qtiles + 2 * idx + 1);
+                    cls = classify_pair(QInfo{qa.y, qb.y, qb.z}, ka.y, kb.y, kb.z, p.causal);
+                }
+                uint32_t vis = __ballot_sync(0xffffffffu, cls != kSkip);
+                while (vis && ok) {
+                    const int src = __ffs(vis) - 1;
+                    vis &= vis - 1;
+                    int4 d0, d1;
+                    d0.x = __shfl_sync(0xffffffffu, qa.x, src);
+                    d0.y = __shfl_sync(0xffffffffu, qa.y, src);
+                    d0.z = __shfl_sync(0xffffffffu, qa.z, src);
+                    d0.w = __shfl_sync(0xffffffffu, qa.w, src);
+                    d1.x = __shfl_sync(0xffffffffu, qb.x, src);
+                    d1.y = __shfl_sync(0xffffffffu, cls, src) << 1;  // flags: class << 1, bit 0 = end
+                    d1.z = 0;
+                    d1.w = 0;
+                    publish(d0, d1, false);
+                }
+            }
+        }
+        if (ok) publish(make_int4(0, 0, 0, 0), make_int4(0, 1, 0, 0), true);
+        if (lane == 0) {
+            volatile int local_abort = 0;
+            const WaitCtl drain{&local_abort, p.status, p.budget_ns};
+            (void)mbar_wait(kv_full, 0, drain);
+            for (uint32_t x = (n > 2 ? n - 2 : 0); x < n; ++x)
+                (void)mbar_wait(st_full + (x & 1u), (x >> 1) & 1u, drain);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);   // A, B K-major
+            const uint32_t id_kmn = idesc_bf16_f32(128, 128, 0, 1);  // A K-major (smem/TMEM), B MN-major
+            const uint32_t id_mnmn = idesc_bf16_f32(128, 128, 1, 1); // A MN-major, B MN-major
+            const uint32_t ks_ = base_s + kOffK, vs_ = base_s + kOffV, dss = base_s + kOffDS;
+            bool ok = mbar_wait(kv_full, 0, wc) && mbar_wait(st_full + 0, 0, wc);
+            tc_fence_after();
+            bool have = ok && !(desc[1].y & 1);
+            uint32_t i = 0;
+            if (have) {
+                mma_kk(tS, ks_, base_s + kOffQ, id_kk);
+                tc_commit(s_full);
+                mma_kk(tDP, vs_, base_s + kOffDO, id_kk);
+                tc_commit(dp_full);
+            }
+            while (ok && have) {
+                const uint32_t st = i & 1u;
+                const uint32_t qs = base_s + kOffQ + st * kTile, dos = base_s + kOffDO + st * kTile;
+                // dV += P^T dO: P^T from TMEM, dO read MN-major (d contiguous)
+                if (!mbar_wait(p_ready, i & 1u, wc)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    tc_mma_ts(tDV, tS + 8u * k, sdesc_sw128(dos + k * 2048u, kHalf, 1024), id_kmn, (i > 0 || k > 0));
+                // next tile's S^T (the dV above read P^T first: in-order)
+                const uint32_t nst = (i + 1) & 1u;
+                if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
+                tc_fence_after();
+                const bool have_next = !(desc[2 * nst + 1].y & 1);
+                if (have_next) {
+                    mma_kk(tS, ks_, base_s + kOffQ + nst * kTile, id_kk);
+                    tc_commit(s_full);
+                }
+                // dK += dS^T Q (dS^T K-major in shared memory, Q read MN-major)
+                if (!mbar_wait(ds_ready, i & 1u, wc)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t aoff = (uint32_t)(k >> 2) * kHalf + (uint32_t)(k & 3) * 32u;
+                    tc_mma_ss(tDK, sdesc_sw128(dss + aoff, 16, 1024), sdesc_sw128(qs + k * 2048u, kHalf, 1024),
+                              id_kmn, (i > 0 || k > 0));
+                }
+                tc_commit(st_empty + st);  // Q and dO of this stage are no longer read
+                // dQ = dS K: dS^T read MN-major (query rows contiguous), K read MN-major
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    tc_mma_ss(tDP, sdesc_sw128(dss + k * 2048u, kHalf, 1024), sdesc_sw128(ks_ + k * 2048u, kHalf, 1024),
+                              id_mnmn, k > 0);
+                tc_commit(dq_full);
+                if (!have_next) break;
+                // next tile's dP^T overwrites dQ once it has been read out
+                if (!mbar_wait(dq_empty, i & 1u, wc)) break;
+                tc_fence_after();
+                mma_kk(tDP, vs_, base_s + kOffDO + nst * kTile, id_kk);
+                tc_commit(dp_full);
+                ++i;
+            }
+            tc_commit(mma_done);
+            volatile int local_abort = 0;
+            const WaitCtl drain{&local_abort, p.status, p.budget_ns};
+            (void)mbar_wait(mma_done, 0, drain);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ compute warpgroup
+        const int j = threadIdx.x - 128;  // TMEM lane: key row (S^T, dP^T, dK, dV) / query row (dQ)
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const bool kvalid = j < ka.y;
+        const int kpos = j < ka.z ? ka.w + j : kb.x + (j - ka.z);
+        const int G = p.G;
+        const int tok_m = j >> p.log2G, head_m = g * G + (j & (G - 1));
+        uint8_t *dsrow = smem + kOffDS + (j >> 3) * 1024 + (j & 7) * 128;
+        const int sw = j & 7;
+        float P[128];
+        bool ok = mbar_wait(st_full + 0, 0, wc);
+        int4 dc0 = desc[0], dc1 = desc[1];
+        bool have = ok && !(dc1.y & 1);
+        uint32_t i = 0;
+
+        // S^T -> P^T (kept in registers as fp32, written to TMEM as bf16)
+        auto step_p = [&](uint32_t it, const int4 &d0, const int4 &d1) -> bool {
+            if (!mbar_wait(s_full, it & 1u, wc)) return false;
+            tc_fence_after();
+            uint32_t v[128];
+            tmem_ld128(tS + lane_base, v);
+            const float *l2 = lse_st + (it & 1u) * 128;
+            const int cls = d1.y >> 1;
+            uint32_t wmask[4] = {~0u, ~0u, ~0u, ~0u};
+            if (cls == kPartial) {
+                int a1 = 0, e1 = 0, a2 = 0, e2 = 0;
+                if (kvalid) {
+                    const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
+                    if (p.causal) {
+                        a1 = min(max(kpos - pos0, 0), split);
+                        a2 = min(max(kpos - pos1 + split, split), qlen);
+                    } else {
+                        a1 = 0;
+                        a2 = split;
+                    }
+                    e1 = split;
+                    e2 = qlen;
+                }
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch)
+                    wmask[ch] = range_bits(a1 * G, e1 * G, 32 * ch) | range_bits(a2 * G, e2 * G, 32 * ch);
+            }
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                const float x = ex2_approx(fmaf(__uint_as_float(v[c]), p.scale_log2, -l2[c]));
+                P[c] = ((wmask[c >> 5] >> (c & 31)) & 1u) ? x : 0.f;
+            }
+#pragma unroll
+            for (int c2 = 0; c2 < 64; ++c2) pk[c2] = pack_bf16x2(P[2 * c2], P[2 * c2 + 1]);
+            tmem_st64(tS + lane_base, pk);
+            tc_fence_before();
+            mbar_arrive(p_ready);
+            return true;
+        };
+        // dP^T -> dS^T = P^T o (dP^T - D) * scale, bf16 into shared memory
+        auto step_ds = [&](uint32_t it) -> bool {
+            if (!mbar_wait(dp_full, it & 1u, wc)) return false;
+            tc_fence_after();
+            const float *dd = d_st + (it & 1u) * 128;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(tDP + lane_base + 32u * ch, v);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int c = 32 * ch + 2 * e;
+                    const float d0v = P[c] * (__uint_as_float(v[2 * e]) - dd[c]) * p.scale;
+                    const float d1v = P[c + 1] * (__uint_as_float(v[2 * e + 1]) - dd[c + 1]) * p.scale;
+                    pk[e] = pack_bf16x2(d0v, d1v);
+                }
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int c16 = ch * 4 + q4;  // 16-byte chunk index along the row (0..15)
+                    const int h = c16 >> 3, c = c16 & 7;
+                    *reinterpret_cast<uint4 *>(dsrow + h * kHalf + ((c ^ sw) << 4)) =
+                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(ds_ready);
+            return true;
+        };
+        // dQ (thread = query row): fp32 vector atomics into dq at the row's position
+        auto step_dq = [&](uint32_t it, const int4 &d0, const int4 &d1) -> bool {
+            if (!mbar_wait(dq_full, it & 1u, wc)) return false;
+            tc_fence_after();
+            const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
+            const bool qvalid = tok_m < qlen;
+            const int qpos = tok_m < split ? pos0 + tok_m : pos1 + (tok_m - split);
+            float4 *dst = reinterpret_cast<float4 *>(p.dq + ((long long)qpos * p.Hq + head_m) * 128);
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t v[32];
+                tmem_ld32(tDP + lane_base + 32u * ch, v);
+                if (ch == 3) {
+                    tc_fence_before();
+                    mbar_arrive(dq_empty);
+                }
+                if (qvalid) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        atomicAdd(dst + ch * 8 + q4,
+                                  make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
+                                              __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])));
+                }
+            }
+            return true;
+        };
+
+        if (have) {
+            ok = step_p(0, dc0, dc1) && step_ds(0);
+        }
+        while (ok && have) {
+            const uint32_t nst = (i + 1) & 1u;
+            if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) {
+                ok = false;
+                break;
+            }
+            const int4 nd0 = desc[2 * nst], nd1 = desc[2 * nst + 1];
+            const bool have_next = !(nd1.y & 1);
+            if (have_next && !step_p(i + 1, nd0, nd1)) {
+                ok = false;
+                break;
+            }
+            if (!step_dq(i, dc0, dc1)) {
+                ok = false;
+                break;
+            }
+            if (!have_next) break;
+            if (!step_ds(i + 1)) {
+                ok = false;
+                break;
+            }
+            dc0 = nd0;
+            dc1 = nd1;
+            ++i;
+        }
+        // ---------------------------------------------- epilogue: dK, dV rows
+        const bool has_acc = ok && have;
+        if (has_acc) tc_fence_after();  // dq_full of the last tile covers every MMA
+        const long long rowoff = ((long long)kpos * p.Hkv + g) * 128;
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+            float *dst = (which ? p.dv : p.dk) + rowoff;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t v[32];
+                if (has_acc) {
+                    tmem_ld32((which ? tDV : tDK) + lane_base + 32u * ch, v);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                if (kvalid) {
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * ch);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4) {
+                        float4 x = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
+                                               __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
+                        if (p.kv_accumulate) {
+                            const float4 o = d4[q4];
+                            x.x += o.x;
+                            x.y += o.y;
+                            x.z += o.z;
+                            x.w += o.w;
+                        }
+                        d4[q4] = x;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+bool make_map(CUtensorMap *m, const void *ptr, int64_t T, int H, int box_h, int box_t) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+    cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_h, (cuuint32_t)box_t};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult rc = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return rc == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
+    if (a.n_items <= 0) return cudaSuccess;
+    BwdParams p;
+    memset(&p, 0, sizeof(p));
+    const int G = a.G;
+    if (!make_map(&p.tmQ, a.q, a.T, a.Hq, G, kBM / G) || !make_map(&p.tmDO, a.dout, a.T, a.Hq, G, kBM / G) ||
+        !make_map(&p.tmK, a.k, a.T, a.Hkv, 1, kBN) || !make_map(&p.tmV, a.v, a.T, a.Hkv, 1, kBN))
+        return cudaErrorInvalidValue;
+    p.qtiles = static_cast<const int4 *>(a.qtiles);
+    p.kvtiles = static_cast<const int4 *>(a.kvtiles);
+    p.items = static_cast<const int4 *>(a.items);
+    p.q_off = a.q_off;
+    p.n_items = a.n_items;
+    p.cp = a.cp;
+    p.B = a.B;
+    p.G = G;
+    int lg = 0;
+    while ((1 << lg) < G) ++lg;
+    p.log2G = lg;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.t0 = a.t0;
+    p.t1 = a.t1;
+    p.causal = a.causal;
+    p.kv_accumulate = a.kv_accumulate;
+    p.scale = a.scale;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.lse = a.lse;
+    p.D = a.D;
+    p.lse_T = a.lse_T;
+    p.dq = a.dq;
+    p.dk = a.dk;
+    p.dv = a.dv;
+    p.status = device_status_ptr();
+    p.budget_ns = wait_budget_ns();
+    static bool attr_set[128] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 128 && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    tc_bwd_kernel<<<a.n_items, kThreads, kSmemBytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ra

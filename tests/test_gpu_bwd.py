@@ -1,0 +1,133 @@
+"""GPU parity of the ring backward (dQ, dK, dV from the saved LSE) against the
+fp64 oracle.  bf16 inputs: max-abs error <= 2e-2 * max(1, max|ref|) per
+gradient; fp32 inputs: 1e-5 * max(1, max|ref|)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ra():
+    assert torch.cuda.is_available()
+    from context_varlen_ring_gb300 import build as b
+    b.build()
+    import context_varlen_ring_gb300 as m
+    m.lib()
+    torch.cuda.set_device(0)
+    return m
+
+
+def _err(got, ref):
+    return float(np.abs(np.asarray(got, dtype=np.float64) - ref).max()) / max(1.0, float(np.abs(ref).max()))
+
+
+def _run(ra, q, k, v, do, cu, cp, mode, causal, sched, grad_dtype=torch.float32):
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    out, lse = ra.ring_attn_fwd(qd, kd, vd, cu, cp, mode, causal, None, sched)
+    dq, dk, dv = ra.ring_attn_bwd(qd, kd, vd, out, lse, dod, cu, cp, mode, causal, None, sched, grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    assert ra.device_status() == 0
+    return out, lse, dq.float().cpu().numpy(), dk.float().cpu().numpy(), dv.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("sched", ["fused", "stepwise"])
+def test_bwd_c0_fp32(ra, orc, sched):
+    wl = W.C0
+    cu = wl.cu_seqlens()
+    q, k, v = W.make_qkv(wl.T, wl.hq, wl.hkv, wl.d, wl.dtype)
+    do = W.make_dout(wl.T, wl.hq, wl.d, wl.dtype)
+    _, _, dq, dk, dv = _run(ra, q, k, v, do, cu, wl.cp, wl.zz_mode, True, sched)
+    ro, rl = orc.attn_fwd(q, k, v, cu, True, wl.scale)
+    rdq, rdk, rdv = orc.attn_bwd(q, k, v, ro, rl, do, cu, True, wl.scale)
+    for g, r in ((dq, rdq), (dk, rdk), (dv, rdv)):
+        assert _err(g, r) <= 1e-5
+
+
+@pytest.mark.parametrize("sched", ["fused", "stepwise"])
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_bwd_small_bf16(ra, orc, sched, mode, G):
+    rng = np.random.default_rng(300 + 10 * G + mode)
+    for trial in range(2):
+        docs = W.random_doc_lens(rng, 1400, 1, 600)
+        cu = W.cu_seqlens(docs)
+        T = int(cu[-1])
+        cp = [2, 3, 4, 8, 1][(trial + G) % 5]
+        hkv = 2
+        causal = trial == 0 or G != 2
+        q, k, v = W.make_qkv(T, hkv * G, hkv, 128, torch.bfloat16, seed_offset=trial)
+        do = W.make_dout(T, hkv * G, 128, torch.bfloat16, seed_offset=trial)
+        _, _, dq, dk, dv = _run(ra, q, k, v, do, cu, cp, mode, causal, sched)
+        scale = 1 / math.sqrt(128)
+        ro, rl = orc.attn_fwd(q, k, v, cu, causal, scale)
+        rdq, rdk, rdv = orc.attn_bwd(q, k, v, ro, rl, do, cu, causal, scale)
+        for name, g, r in (("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv)):
+            e = _err(g, r)
+            assert e <= 2e-2, (name, docs, cp, e)
+
+
+def test_bwd_bf16_grad_output(ra, orc):
+    """Gradients returned in bf16 (accumulated in fp32, cast at the end)."""
+    cu = W.cu_seqlens((300, 41, 500))
+    T = int(cu[-1])
+    q, k, v = W.make_qkv(T, 16, 4, 128, torch.bfloat16)
+    do = W.make_dout(T, 16, 128, torch.bfloat16)
+    _, _, dq, dk, dv = _run(ra, q, k, v, do, cu, 4, 1, True, "fused", grad_dtype=torch.bfloat16)
+    ro, rl = orc.attn_fwd(q, k, v, cu, True, 1 / math.sqrt(128))
+    rdq, rdk, rdv = orc.attn_bwd(q, k, v, ro, rl, do, cu, True, 1 / math.sqrt(128))
+    for g, r in ((dq, rdq), (dk, rdk), (dv, rdv)):
+        assert _err(g, r) <= 2e-2
+
+
+def test_bwd_c4_full_size(ra, orc):
+    """The packed 32768-token workload at full size: every gradient row of
+    the documents up to 1300 tokens against the oracle (documents are
+    independent), sampled dQ rows of the long documents, and the two sum
+    identities over all keys."""
+    wl = W.C4
+    cu = wl.cu_seqlens()
+    T = wl.T
+    q, k, v = W.make_qkv(T, wl.hq, wl.hkv, wl.d, wl.dtype)
+    do = W.make_dout(T, wl.hq, wl.d, wl.dtype)
+    out, lse, dq, dk, dv = _run(ra, q, k, v, do, cu, wl.cp, wl.zz_mode, True, "fused")
+    lens = np.diff(cu)
+    for bdoc in np.nonzero(lens <= 1300)[0]:
+        a, e = int(cu[bdoc]), int(cu[bdoc + 1])
+        sub = np.array([0, e - a])
+        qs, ks, vs, ds = q[a:e], k[a:e], v[a:e], do[a:e]
+        ro, rl = orc.attn_fwd(qs, ks, vs, sub, True, wl.scale)
+        rdq, rdk, rdv = orc.attn_bwd(qs, ks, vs, ro, rl, ds, sub, True, wl.scale)
+        for name, g, r in (("dq", dq[a:e], rdq), ("dk", dk[a:e], rdk), ("dv", dv[a:e], rdv)):
+            err = _err(g, r)
+            assert err <= 2e-2, (name, bdoc, err)
+    # sampled dQ rows in the long documents
+    long_docs = np.nonzero(lens > 1300)[0]
+    rows = []
+    rng = np.random.default_rng(7)
+    for bdoc in long_docs:
+        a, e = int(cu[bdoc]), int(cu[bdoc + 1])
+        rows += [a, e - 1] + list(rng.integers(a, e, size=3))
+    rows = np.array(sorted(set(rows)), dtype=np.int64)
+    seg = orc.doc_ids(cu)
+    pos = np.arange(T)
+    ro, rl = orc.partial_fwd(q[torch.from_numpy(rows)], k, v, seg[rows], seg, rows, pos, True, wl.scale)
+    o_full = np.zeros((T, wl.hq, wl.d))
+    l_full = np.zeros((T, wl.hq))
+    o_full[rows] = ro
+    l_full[rows] = rl
+    rdq, _, _ = orc.attn_bwd(q, k, v, o_full, l_full, do, cu, True, wl.scale, dq_rows=rows, dk_rows=np.array([0]))
+    assert _err(dq[rows], rdq) <= 2e-2
+    # sum identities: sum_j dV_j = sum over the group's heads of sum_i dO_i; sum_j dK_j = 0
+    G = wl.hq // wl.hkv
+    dof = do.double().numpy()
+    for g in range(wl.hkv):
+        ref = dof[:, g * G:(g + 1) * G].sum((0, 1))
+        assert np.abs(dv[:, g].astype(np.float64).sum(0) - ref).max() <= 1e-2 * max(1.0, np.abs(ref).max())
+        scale_k = np.abs(dk[:, g]).sum(0).max()
+        assert np.abs(dk[:, g].astype(np.float64).sum(0)).max() <= 1e-3 * scale_k
