@@ -657,6 +657,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         a.dq = dqa;
         a.dk = dka;
         a.dv = dva;
+        a.with_dq = 1;
         if (sched == RA_SCHED_FUSED) {
             a.t0 = 0;
             a.t1 = cp;

@@ -131,6 +131,7 @@ struct TcBwdArgs {
     float *dq;                         // fp32 [T, Hq, d] at original positions, atomically added
     float *dk, *dv;                    // fp32 [T, Hkv, d] at original positions
     int kv_accumulate;                 // 1: dk/dv += (ring steps in separate launches)
+    int with_dq;                       // 1: also dQ (atomics); 0: dK/dV only
 };
 cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st);
 

@@ -19,8 +19,9 @@
 //    memory; query tiles (128 MMA rows = 128/G tokens x G heads, as in the
 //    forward) and dO tiles stream through two TMA stages together with the
 //    tile's 128 LSE and D values.
-//  * TMEM (512 columns): dK [0,128), dV [128,256), S^T then P^T (bf16, first
-//    64 columns) [256,384), dP^T then dQ [384,512).
+//  * TMEM (512 columns): dK [0,128), dV [128,256), S^T then P^T [256,384)
+//    (bf16, each half of P^T packed into the first 32 columns of the S^T
+//    half it came from), dP^T then dQ [384,512).
 //  * Per query tile the MMA thread issues, in order:
 //      S^T = K Q^T, dP^T = V dO^T, dV += P^T dO (P from TMEM), next S^T,
 //      dK += dS^T Q, dQ = dS K (dS^T in shared memory read MN-major),
@@ -48,7 +49,7 @@ namespace {
 
 using namespace dev;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr uint32_t kHalf = 16384;
 constexpr uint32_t kTile = 2 * kHalf;
 constexpr uint32_t kOffK = 0;
@@ -67,7 +68,7 @@ struct BwdParams {
     const int4 *qtiles, *kvtiles, *items;
     const int *q_off;
     int n_items, cp, B, G, log2G, Hq, Hkv;
-    int t0, t1, causal, kv_accumulate;
+    int t0, t1, causal, kv_accumulate, with_dq;
     float scale, scale_log2;
     const float *lse, *D;
     long long lse_T;
@@ -114,10 +115,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     uint64_t *st_empty = bars + 3;   // [2]
     uint64_t *s_full = bars + 5;     // S^T done
     uint64_t *dp_full = bars + 6;    // dP^T done
-    uint64_t *p_ready = bars + 7;    // P^T in TMEM (128 arrivals)
-    uint64_t *ds_ready = bars + 8;   // dS^T in shared memory (128 arrivals)
-    uint64_t *dq_full = bars + 9;    // dQ done (and dK, so dS^T is free)
-    uint64_t *dq_empty = bars + 10;  // dQ read out (128 arrivals)
+    uint64_t *p_ready = bars + 7;    // P^T in TMEM (256 arrivals)
+    uint64_t *ds_ready = bars + 8;   // dS^T in shared memory (256 arrivals)
+    uint64_t *dq_full = bars + 9;    // dK (and dQ) done: dS^T and dQ may be reused
+    uint64_t *dq_empty = bars + 10;  // dQ read out (256 arrivals)
     uint64_t *mma_done = bars + 11;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 13);
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     const int t1 = p.t0 >= 0 ? p.t1 : ib.z;
     const int4 ka = __ldg(p.kvtiles + 2 * kt), kb = __ldg(p.kvtiles + 2 * kt + 1);
     // KV tile: row0 ka.x, len ka.y, split ka.z, pos0 ka.w, pos1 kb.x, pmin kb.y, pmax kb.z
+    const bool with_dq = p.with_dq != 0;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -143,10 +145,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
-        mbar_init(p_ready, 128);
-        mbar_init(ds_ready, 128);
+        mbar_init(p_ready, 256);
+        mbar_init(ds_ready, 256);
         mbar_init(dq_full, 1);
-        mbar_init(dq_empty, 128);
+        mbar_init(dq_empty, 256);
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
@@ -178,42 +180,56 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         uint32_t n = 0;
         int ok = 1;
         const float log2e = 1.4426950408889634f;
-        auto publish = [&](int4 d0, int4 d1, bool end) {
+        // A visited query tile waits in registers (descriptor, its 128 LSE and
+        // D values already loaded) while the previous one is published, so
+        // the global-load latency overlaps the wait for a free stage.
+        bool pend = false;
+        int4 pd0 = make_int4(0, 0, 0, 0), pd1 = make_int4(0, 0, 0, 0);
+        float pl[4], pD[4];
+        auto fetch = [&](const int4 &d0, const int4 &d1) {
+            const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int c = lane + 32 * e;
+                const int tok = c >> p.log2G, head = g * G + (c & (G - 1));
+                pl[e] = INFINITY;
+                pD[e] = 0.f;
+                if (tok < qlen) {
+                    const int pos = tok < split ? pos0 + tok : pos1 + (tok - split);
+                    pl[e] = __ldg(p.lse + (long long)head * p.lse_T + pos);
+                    pD[e] = __ldg(p.D + (long long)head * p.lse_T + pos);
+                }
+            }
+            pd0 = d0;
+            pd1 = d1;
+            pend = true;
+        };
+        auto publish = [&](bool end) {
             const uint32_t st = n & 1u;
             if (lane == 0 && !mbar_wait(st_empty + st, ((n >> 1) & 1u) ^ 1u, wc)) ok = 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) return;
             if (!end) {
-                // 128 columns (token, head) of this query tile: LSE (log2) and D
-                const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int c = lane + 32 * e;
-                    const int tok = c >> p.log2G, head = g * G + (c & (G - 1));
-                    float l2 = INFINITY, dd = 0.f;
-                    if (tok < qlen) {
-                        const int pos = tok < split ? pos0 + tok : pos1 + (tok - split);
-                        const float l = __ldg(p.lse + (long long)head * p.lse_T + pos);
-                        l2 = (l == -INFINITY) ? INFINITY : l * log2e;
-                        dd = __ldg(p.D + (long long)head * p.lse_T + pos);
-                    }
-                    lse_st[st * 128 + c] = l2;
-                    d_st[st * 128 + c] = dd;
+                    lse_st[st * 128 + c] = (pl[e] == -INFINITY) ? INFINITY : pl[e] * log2e;
+                    d_st[st * 128 + c] = pD[e];
                 }
             }
             if (lane == 0) {
-                desc[2 * st] = d0;
-                desc[2 * st + 1] = end ? make_int4(0, 1, 0, 0) : d1;
+                desc[2 * st] = end ? make_int4(0, 0, 0, 0) : pd0;
+                desc[2 * st + 1] = end ? make_int4(0, 1, 0, 0) : pd1;
             }
             __syncwarp();
             if (lane == 0) {
                 if (!end) {
                     mbar_arrive_expect_tx(st_full + st, 2 * kTile);
                     const int hq0 = g * G;
-                    tma_load_3d(smem + kOffQ + st * kTile, &p.tmQ, st_full + st, 0, hq0, d0.x);
-                    tma_load_3d(smem + kOffQ + st * kTile + kHalf, &p.tmQ, st_full + st, 64, hq0, d0.x);
-                    tma_load_3d(smem + kOffDO + st * kTile, &p.tmDO, st_full + st, 0, hq0, d0.x);
-                    tma_load_3d(smem + kOffDO + st * kTile + kHalf, &p.tmDO, st_full + st, 64, hq0, d0.x);
+                    tma_load_3d(smem + kOffQ + st * kTile, &p.tmQ, st_full + st, 0, hq0, pd0.x);
+                    tma_load_3d(smem + kOffQ + st * kTile + kHalf, &p.tmQ, st_full + st, 64, hq0, pd0.x);
+                    tma_load_3d(smem + kOffDO + st * kTile, &p.tmDO, st_full + st, 0, hq0, pd0.x);
+                    tma_load_3d(smem + kOffDO + st * kTile + kHalf, &p.tmDO, st_full + st, 64, hq0, pd0.x);
                 } else {
                     mbar_arrive(st_full + st);
                 }
@@ -221,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                 mbar_arrive(st_full + st);
             }
             ++n;
+            pend = false;
         };
         for (int t = t0; t < t1 && ok; ++t) {
             const int r = (s + t) % p.cp;
@@ -248,11 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     d1.y = __shfl_sync(0xffffffffu, cls, src) << 1;  // flags: class << 1, bit 0 = end
                     d1.z = 0;
                     d1.w = 0;
-                    publish(d0, d1, false);
+                    if (pend) publish(false);
+                    if (ok) fetch(d0, d1);
                 }
             }
         }
-        if (ok) publish(make_int4(0, 0, 0, 0), make_int4(0, 1, 0, 0), true);
+        if (ok && pend) publish(false);
+        if (ok) publish(true);
         if (lane == 0) {
             volatile int local_abort = 0;
             const WaitCtl drain{&local_abort, p.status, p.budget_ns};
@@ -283,9 +302,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                 // dV += P^T dO: P^T from TMEM, dO read MN-major (d contiguous)
                 if (!mbar_wait(p_ready, i & 1u, wc)) break;
                 tc_fence_after();
+                // P^T columns 0-63 are packed at TMEM columns [0,32) and
+                // columns 64-127 at [64,96) (each warpgroup writes inside its
+                // own S^T columns)
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    tc_mma_ts(tDV, tS + 8u * k, sdesc_sw128(dos + k * 2048u, kHalf, 1024), id_kmn, (i > 0 || k > 0));
+                    tc_mma_ts(tDV, tS + 8u * k + (k >= 4 ? 32u : 0u), sdesc_sw128(dos + k * 2048u, kHalf, 1024), id_kmn,
+                              (i > 0 || k > 0));
                 // next tile's S^T (the dV above read P^T first: in-order)
                 const uint32_t nst = (i + 1) & 1u;
                 if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
@@ -305,16 +328,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                               id_kmn, (i > 0 || k > 0));
                 }
                 tc_commit(st_empty + st);  // Q and dO of this stage are no longer read
-                // dQ = dS K: dS^T read MN-major (query rows contiguous), K read MN-major
+                if (with_dq) {
+                    // dQ = dS K: dS^T read MN-major (query rows contiguous), K read MN-major
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    tc_mma_ss(tDP, sdesc_sw128(dss + k * 2048u, kHalf, 1024), sdesc_sw128(ks_ + k * 2048u, kHalf, 1024),
-                              id_mnmn, k > 0);
+                    for (int k = 0; k < 8; ++k)
+                        tc_mma_ss(tDP, sdesc_sw128(dss + k * 2048u, kHalf, 1024),
+                                  sdesc_sw128(ks_ + k * 2048u, kHalf, 1024), id_mnmn, k > 0);
+                }
                 tc_commit(dq_full);
                 if (!have_next) break;
-                // next tile's dP^T overwrites dQ once it has been read out
-                if (!mbar_wait(dq_empty, i & 1u, wc)) break;
-                tc_fence_after();
+                if (with_dq) {
+                    // next tile's dP^T overwrites dQ once it has been read out
+                    if (!mbar_wait(dq_empty, i & 1u, wc)) break;
+                    tc_fence_after();
+                }
                 mma_kk(tDP, vs_, base_s + kOffDO + nst * kTile, id_kk);
                 tc_commit(dp_full);
                 ++i;
@@ -325,30 +352,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             (void)mbar_wait(mma_done, 0, drain);
         }
     } else if (warp >= 4) {
-        // ------------------------------------------------ compute warpgroup
-        const int j = threadIdx.x - 128;  // TMEM lane: key row (S^T, dP^T, dK, dV) / query row (dQ)
+        // ------------------------------------------------ compute warpgroups
+        // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) owns columns
+        // [64h, 64h + 64) of S^T, dP^T, dQ, dK and dV; thread j owns TMEM lane j.
+        const int h = (warp >= 8) ? 1 : 0;
+        const int j = (threadIdx.x - 128) & 127;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const bool kvalid = j < ka.y;
         const int kpos = j < ka.z ? ka.w + j : kb.x + (j - ka.z);
         const int G = p.G;
         const int tok_m = j >> p.log2G, head_m = g * G + (j & (G - 1));
-        uint8_t *dsrow = smem + kOffDS + (j >> 3) * 1024 + (j & 7) * 128;
+        uint8_t *dsrow = smem + kOffDS + h * kHalf + (j >> 3) * 1024 + (j & 7) * 128;
         const int sw = j & 7;
-        float P[128];
+        float P[64];
         bool ok = mbar_wait(st_full + 0, 0, wc);
         int4 dc0 = desc[0], dc1 = desc[1];
         bool have = ok && !(dc1.y & 1);
         uint32_t i = 0;
 
-        // S^T -> P^T (kept in registers as fp32, written to TMEM as bf16)
+        // S^T -> P^T (fp32 in registers; bf16 into TMEM over the first 32 of
+        // this warpgroup's own 64 S^T columns, which it has already read)
         auto step_p = [&](uint32_t it, const int4 &d0, const int4 &d1) -> bool {
             if (!mbar_wait(s_full, it & 1u, wc)) return false;
             tc_fence_after();
-            uint32_t v[128];
-            tmem_ld128(tS + lane_base, v);
-            const float *l2 = lse_st + (it & 1u) * 128;
+            uint32_t v[64];
+            tmem_ld64(tS + lane_base + 64u * h, v);
+            const float4 *l4 = reinterpret_cast<const float4 *>(lse_st + (it & 1u) * 128 + 64 * h);
             const int cls = d1.y >> 1;
-            uint32_t wmask[4] = {~0u, ~0u, ~0u, ~0u};
+            uint32_t wm[2] = {~0u, ~0u};
             if (cls == kPartial) {
                 int a1 = 0, e1 = 0, a2 = 0, e2 = 0;
                 if (kvalid) {
@@ -364,18 +395,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     e2 = qlen;
                 }
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    wmask[ch] = range_bits(a1 * G, e1 * G, 32 * ch) | range_bits(a2 * G, e2 * G, 32 * ch);
-            }
-            uint32_t pk[64];
-#pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float x = ex2_approx(fmaf(__uint_as_float(v[c]), p.scale_log2, -l2[c]));
-                P[c] = ((wmask[c >> 5] >> (c & 31)) & 1u) ? x : 0.f;
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int cb = 64 * h + 32 * ch;
+                    wm[ch] = range_bits(a1 * G, e1 * G, cb) | range_bits(a2 * G, e2 * G, cb);
+                }
             }
 #pragma unroll
-            for (int c2 = 0; c2 < 64; ++c2) pk[c2] = pack_bf16x2(P[2 * c2], P[2 * c2 + 1]);
-            tmem_st64(tS + lane_base, pk);
+            for (int c4 = 0; c4 < 16; ++c4) {
+                const float4 l = l4[c4];
+                const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = 4 * c4 + e;
+                    const float x = ex2_approx(fmaf(__uint_as_float(v[c]), p.scale_log2, -lv[e]));
+                    P[c] = ((wm[c >> 5] >> (c & 31)) & 1u) ? x : 0.f;
+                }
+            }
+            uint32_t pk[32];
+#pragma unroll
+            for (int c2 = 0; c2 < 32; ++c2) pk[c2] = pack_bf16x2(P[2 * c2], P[2 * c2 + 1]);
+            tmem_st32(tS + lane_base + 64u * h, pk);
             tc_fence_before();
             mbar_arrive(p_ready);
             return true;
@@ -384,62 +423,52 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         auto step_ds = [&](uint32_t it) -> bool {
             if (!mbar_wait(dp_full, it & 1u, wc)) return false;
             tc_fence_after();
-            const float *dd = d_st + (it & 1u) * 128;
+            uint32_t v[64];
+            tmem_ld64(tDP + lane_base + 64u * h, v);
+            const float4 *d4 = reinterpret_cast<const float4 *>(d_st + (it & 1u) * 128 + 64 * h);
+            uint32_t pk[32];
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t v[32];
-                tmem_ld32(tDP + lane_base + 32u * ch, v);
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c = 32 * ch + 2 * e;
-                    const float d0v = P[c] * (__uint_as_float(v[2 * e]) - dd[c]) * p.scale;
-                    const float d1v = P[c + 1] * (__uint_as_float(v[2 * e + 1]) - dd[c + 1]) * p.scale;
-                    pk[e] = pack_bf16x2(d0v, d1v);
-                }
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int c16 = ch * 4 + q4;  // 16-byte chunk index along the row (0..15)
-                    const int h = c16 >> 3, c = c16 & 7;
-                    *reinterpret_cast<uint4 *>(dsrow + h * kHalf + ((c ^ sw) << 4)) =
-                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-                }
+            for (int c4 = 0; c4 < 16; ++c4) {
+                const float4 dd = d4[c4];
+                const int c = 4 * c4;
+                pk[2 * c4] = pack_bf16x2(P[c] * (__uint_as_float(v[c]) - dd.x) * p.scale,
+                                         P[c + 1] * (__uint_as_float(v[c + 1]) - dd.y) * p.scale);
+                pk[2 * c4 + 1] = pack_bf16x2(P[c + 2] * (__uint_as_float(v[c + 2]) - dd.z) * p.scale,
+                                             P[c + 3] * (__uint_as_float(v[c + 3]) - dd.w) * p.scale);
             }
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4 *>(dsrow + ((c ^ sw) << 4)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(ds_ready);
             return true;
         };
-        // dQ (thread = query row): fp32 vector atomics into dq at the row's position
+        // dK (and dQ) of tile `it` done; with dQ: read it out (thread = query
+        // row) and add it into dq at the row's position with fp32 vector atomics
         auto step_dq = [&](uint32_t it, const int4 &d0, const int4 &d1) -> bool {
             if (!mbar_wait(dq_full, it & 1u, wc)) return false;
             tc_fence_after();
+            if (!with_dq) return true;
             const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
             const bool qvalid = tok_m < qlen;
             const int qpos = tok_m < split ? pos0 + tok_m : pos1 + (tok_m - split);
-            float4 *dst = reinterpret_cast<float4 *>(p.dq + ((long long)qpos * p.Hq + head_m) * 128);
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t v[32];
-                tmem_ld32(tDP + lane_base + 32u * ch, v);
-                if (ch == 3) {
-                    tc_fence_before();
-                    mbar_arrive(dq_empty);
-                }
-                if (qvalid) {
+            uint32_t v[64];
+            tmem_ld64(tDP + lane_base + 64u * h, v);
+            tc_fence_before();
+            mbar_arrive(dq_empty);
+            if (qvalid) {
+                float4 *dst = reinterpret_cast<float4 *>(p.dq + ((long long)qpos * p.Hq + head_m) * 128 + 64 * h);
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        atomicAdd(dst + ch * 8 + q4,
-                                  make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
-                                              __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])));
-                }
+                for (int q4 = 0; q4 < 16; ++q4)
+                    atomicAdd(dst + q4, make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
+                                                    __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])));
             }
             return true;
         };
 
-        if (have) {
-            ok = step_p(0, dc0, dc1) && step_ds(0);
-        }
+        if (have) ok = step_p(0, dc0, dc1) && step_ds(0);
         while (ok && have) {
             const uint32_t nst = (i + 1) & 1u;
             if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) {
@@ -467,35 +496,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         }
         // ---------------------------------------------- epilogue: dK, dV rows
         const bool has_acc = ok && have;
-        if (has_acc) tc_fence_after();  // dq_full of the last tile covers every MMA
-        const long long rowoff = ((long long)kpos * p.Hkv + g) * 128;
+        const long long rowoff = ((long long)kpos * p.Hkv + g) * 128 + 64 * h;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
-            float *dst = (which ? p.dv : p.dk) + rowoff;
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t v[32];
-                if (has_acc) {
-                    tmem_ld32((which ? tDV : tDK) + lane_base + 32u * ch, v);
-                } else {
+            uint32_t v[64];
+            if (has_acc) {
+                tmem_ld64((which ? tDV : tDK) + lane_base + 64u * h, v);
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
-                }
-                if (kvalid) {
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + 32 * ch);
+                for (int e = 0; e < 64; ++e) v[e] = 0u;
+            }
+            if (kvalid) {
+                float4 *d4 = reinterpret_cast<float4 *>((which ? p.dv : p.dk) + rowoff);
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        float4 x = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
-                                               __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
-                        if (p.kv_accumulate) {
-                            const float4 o = d4[q4];
-                            x.x += o.x;
-                            x.y += o.y;
-                            x.z += o.z;
-                            x.w += o.w;
-                        }
-                        d4[q4] = x;
+                for (int q4 = 0; q4 < 16; ++q4) {
+                    float4 x = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
+                                           __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
+                    if (p.kv_accumulate) {
+                        const float4 o = d4[q4];
+                        x.x += o.x;
+                        x.y += o.y;
+                        x.z += o.z;
+                        x.w += o.w;
                     }
+                    d4[q4] = x;
                 }
             }
         }
@@ -563,6 +587,7 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
     p.t1 = a.t1;
     p.causal = a.causal;
     p.kv_accumulate = a.kv_accumulate;
+    p.with_dq = a.with_dq;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.lse = a.lse;
