@@ -625,13 +625,15 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         ProfScope ps("ra_rowdot", s);
         RA_CUDA(launch_rowdot(dout, out, dtype, T, Hq, d, D, s), "rowdot launch");
     }
-    RA_CUDA(cudaMemsetAsync(dqa, 0, (size_t)T * Hq * d * 4, s), "memset dq");
-    if (!(tc && sched == RA_SCHED_FUSED)) {
+    const bool fused_tc = tc && sched == RA_SCHED_FUSED;
+    if (!fused_tc) {
+        RA_CUDA(cudaMemsetAsync(dqa, 0, (size_t)T * Hq * d * 4, s), "memset dq");
         RA_CUDA(cudaMemsetAsync(dka, 0, (size_t)T * Hkv * d * 4, s), "memset dk");
         RA_CUDA(cudaMemsetAsync(dva, 0, (size_t)T * Hkv * d * 4, s), "memset dv");
     }
-    // a8: per ring step (STEPWISE: one launch per step, fp32 dK/dV += per
-    // step) or all steps in one launch (FUSED: dK/dV accumulate on chip)
+    // a8: the ring backward.  Tensor cores: a key-side pass (dK, dV in TMEM
+    // across ring steps) and a query-side pass (dQ in TMEM, no atomics).
+    // STEPWISE: one launch of each per ring step, accumulating in fp32.
     if (tc) {
         TcBwdArgs a{};
         a.q = Qp;
@@ -657,20 +659,59 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         a.dq = dqa;
         a.dk = dka;
         a.dv = dva;
-        a.with_dq = 1;
-        if (sched == RA_SCHED_FUSED) {
+        a.with_dq = 0;
+        TcDqArgs qa{};
+        qa.q = Qp;
+        qa.k = Kp;
+        qa.v = Vp;
+        qa.dout = dOp;
+        qa.T = T;
+        qa.Hq = Hq;
+        qa.Hkv = Hkv;
+        qa.G = G;
+        qa.qtiles = tab + dt.o_qt;
+        qa.kvtiles = tab + dt.o_kt;
+        qa.kv_off = reinterpret_cast<const int32_t *>(tab + dt.o_kvoff);
+        qa.items = tab + dt.o_qitems;
+        qa.n_items = dt.n_qitems;
+        qa.cp = cp;
+        qa.B = B;
+        qa.causal = causal;
+        qa.scale = scale;
+        qa.lse = lse;
+        qa.D = D;
+        qa.lse_T = T;
+        if (fused_tc) {
             a.t0 = 0;
             a.t1 = cp;
             a.kv_accumulate = 0;
-            ProfScope ps("ra_tc_bwd", s);
-            RA_CUDA(launch_tc_bwd(a, s), "tensor-core backward launch");
+            {
+                ProfScope ps("ra_tc_bwd_dkdv", s);
+                RA_CUDA(launch_tc_bwd(a, s), "tensor-core dK/dV launch");
+            }
+            qa.t0 = 0;
+            qa.t1 = cp;
+            qa.dq = dq;  // complete per query tile: written once in the gradient dtype
+            qa.out_mode = grad_dtype == RA_BF16 ? 0 : 1;
+            {
+                ProfScope ps("ra_tc_bwd_dq", s);
+                RA_CUDA(launch_tc_dq(qa, s), "tensor-core dQ launch");
+            }
         } else {
             a.kv_accumulate = 1;
+            qa.dq = dqa;
+            qa.out_mode = 2;
             for (int t = 0; t < cp; ++t) {
-                a.t0 = t;
-                a.t1 = t + 1;
-                ProfScope ps("ra_tc_bwd", s);
-                RA_CUDA(launch_tc_bwd(a, s), "tensor-core backward launch");
+                a.t0 = qa.t0 = t;
+                a.t1 = qa.t1 = t + 1;
+                {
+                    ProfScope ps("ra_tc_bwd_dkdv", s);
+                    RA_CUDA(launch_tc_bwd(a, s), "tensor-core dK/dV launch");
+                }
+                {
+                    ProfScope ps("ra_tc_bwd_dq", s);
+                    RA_CUDA(launch_tc_dq(qa, s), "tensor-core dQ launch");
+                }
             }
         }
     } else {
@@ -714,7 +755,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     // a9: cast to the gradient dtype (rows are already in original order)
     {
         ProfScope ps("ra_cast", s);
-        RA_CUDA(launch_cast_f32(dqa, dq, grad_dtype, T * Hq * d, s), "cast dq");
+        if (!fused_tc) RA_CUDA(launch_cast_f32(dqa, dq, grad_dtype, T * Hq * d, s), "cast dq");
         RA_CUDA(launch_cast_f32(dka, dk, grad_dtype, T * Hkv * d, s), "cast dk");
         RA_CUDA(launch_cast_f32(dva, dv, grad_dtype, T * Hkv * d, s), "cast dv");
     }

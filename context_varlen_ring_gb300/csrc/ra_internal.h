@@ -63,7 +63,8 @@ struct TilePlan {
     std::vector<Tile> qtiles, kvtiles;
     std::vector<int32_t> q_off, kv_off;  // [cp*(B+1)+1]
     std::vector<WorkItem> items;         // forward items, LPT order
-    std::vector<WorkItem> bitems;        // backward items (one per KV tile x head)
+    std::vector<WorkItem> bitems;        // backward dK/dV items (one per KV tile x head)
+    std::vector<WorkItem> qitems;        // backward dQ items (one per query tile x head)
     int64_t fwd_tile_pairs = 0;          // non-skipped (query tile, KV tile) visits
 };
 
@@ -93,8 +94,8 @@ ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg
 struct DeviceTables {
     std::vector<uint8_t> blob;
     size_t o_perm = 0, o_qt = 0, o_kt = 0, o_qoff = 0, o_kvoff = 0, o_items = 0,
-           o_bitems = 0, o_cul = 0, o_off = 0;
-    int n_items = 0, n_bitems = 0;
+           o_bitems = 0, o_qitems = 0, o_cul = 0, o_off = 0;
+    int n_items = 0, n_bitems = 0, n_qitems = 0;
 };
 void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt);
 

@@ -135,6 +135,27 @@ struct TcBwdArgs {
 };
 cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st);
 
+// Tensor-core dQ pass (bf16, d = 128): one CTA per query tile and KV head;
+// no atomics.  out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 +=.
+struct TcDqArgs {
+    const void *q, *k, *v, *dout;      // permuted buffers
+    int64_t T;
+    int Hq, Hkv, G;
+    const void *qtiles, *kvtiles;
+    const int32_t *kv_off;
+    const void *items;                 // dQ WorkItem records (qt0 = query tile)
+    int n_items;
+    int cp, B;
+    int t0, t1;
+    int causal;
+    float scale;
+    const float *lse, *D;              // [Hq, lse_T] at original positions
+    int64_t lse_T;
+    void *dq;                          // [T, Hq, d] at original positions
+    int out_mode;
+};
+cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st);
+
 // Device-wait self-test (see ra_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t st);
 

@@ -122,6 +122,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
     const int cp = tp.cp, B = tp.B;
     tp.items.clear();
     tp.bitems.clear();
+    tp.qitems.clear();
     tp.fwd_tile_pairs = 0;
     auto seg_idx = [&](int r, int b) { return r * (B + 1) + b; };
     for (int r = 0; r < cp; ++r) {
@@ -141,6 +142,19 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
                 for (int g = 0; g < Hkv; ++g) {
                     WorkItem w{i, q1, g, r, b, 0, cp, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
                     tp.items.push_back(w);
+                }
+                // per-query-tile items of the dQ pass
+                for (int qi = i; qi <= (q1 >= 0 ? q1 : i); ++qi) {
+                    int64_t qc = 0;
+                    for (int t = 0; t < cp; ++t) {
+                        const int s2 = ((r - t) % cp + cp) % cp;
+                        const int ka = tp.kv_off[seg_idx(s2, b)], ke = tp.kv_off[seg_idx(s2, b) + 1];
+                        for (int j = ka; j < ke; ++j) qc += classify(tp.qtiles[qi], tp.kvtiles[j], causal) != kSkip;
+                    }
+                    for (int g = 0; g < Hkv; ++g) {
+                        WorkItem w{qi, -1, g, r, b, 0, cp, (int32_t)std::min<int64_t>(qc, INT32_MAX)};
+                        tp.qitems.push_back(w);
+                    }
                 }
                 tp.fwd_tile_pairs += cost * Hkv;
             }
@@ -172,6 +186,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
     };
     std::stable_sort(tp.items.begin(), tp.items.end(), by_cost);
     std::stable_sort(tp.bitems.begin(), tp.bitems.end(), by_cost);
+    std::stable_sort(tp.qitems.begin(), tp.qitems.end(), by_cost);
 }
 
 ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, TilePlan &tp) {
@@ -241,6 +256,7 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
     dt.o_kvoff = take(tp ? tp->kv_off.size() * 4 : 0);
     dt.o_items = take(tp ? tp->items.size() * sizeof(WorkItem) : 0);
     dt.o_bitems = take(tp ? tp->bitems.size() * sizeof(WorkItem) : 0);
+    dt.o_qitems = take(tp ? tp->qitems.size() * sizeof(WorkItem) : 0);
     dt.o_cul = take(zp ? zp->cu_local.size() * 4 : 0);
     dt.o_off = take(zp ? zp->off.size() * 4 : 0);
     dt.blob.assign(o, 0);
@@ -259,8 +275,10 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
         put(dt.o_kvoff, tp->kv_off.data(), tp->kv_off.size() * 4);
         put(dt.o_items, tp->items.data(), tp->items.size() * sizeof(WorkItem));
         put(dt.o_bitems, tp->bitems.data(), tp->bitems.size() * sizeof(WorkItem));
+        put(dt.o_qitems, tp->qitems.data(), tp->qitems.size() * sizeof(WorkItem));
         dt.n_items = (int)tp->items.size();
         dt.n_bitems = (int)tp->bitems.size();
+        dt.n_qitems = (int)tp->qitems.size();
     }
 }
 
