@@ -168,6 +168,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sched", default="fused", choices=["fused", "stepwise"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--probe", action="store_true",
+                    help="only W+K plain steps (for profilers): no e2e, per-kernel or CPU passes")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)
@@ -221,6 +223,16 @@ def main():
         step()
     barrier()
     assert ra.device_status() == 0
+    if args.probe:
+        for _ in range(args.steps):
+            step()
+        barrier()
+        assert ra.device_status() == 0
+        if rank == 0:
+            print(json.dumps({"probe": wl.name, "steps": args.steps, "warmup": args.warmup}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
 
     # ---- timed region: K steps, device events on the launching stream
     clocks = Clocks(local)
