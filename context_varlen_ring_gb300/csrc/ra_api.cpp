@@ -391,7 +391,7 @@ struct RingLayout {
     // stepwise forward
     size_t parts_o = 0, parts_l = 0, op = 0, lp = 0;
     // backward
-    size_t dop = 0, Dv = 0, dq = 0, dk = 0, dv = 0;
+    size_t dop = 0, Dv = 0, dq = 0, dk = 0, dv = 0, tile_ld = 0;
 };
 
 RingLayout ring_layout(const RingPlan &plan, int64_t T, int Hq, int Hkv, int d, int dtype, int cp, int sched, int bwd) {
@@ -419,6 +419,7 @@ RingLayout ring_layout(const RingPlan &plan, int64_t T, int Hq, int Hkv, int d, 
         L.dq = at((size_t)T * Hq * d * 4);
         L.dk = at((size_t)T * Hkv * d * 4);
         L.dv = at((size_t)T * Hkv * d * 4);
+        L.tile_ld = at(plan.tiles.qtiles.size() * (size_t)Hkv * 1024);
     }
     L.total = c.used + 256;
     return L;
@@ -635,6 +636,12 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     // across ring steps) and a query-side pass (dQ in TMEM, no atomics).
     // STEPWISE: one launch of each per ring step, accumulating in fp32.
     if (tc) {
+        float *tld = reinterpret_cast<float *>(ws + L.tile_ld);
+        {
+            ProfScope ps("ra_tile_lse_d", s);
+            RA_CUDA(launch_tile_lse_d(tab + dt.o_qt, (int)plan->tiles.qtiles.size(), Hkv, G, lse, D, T, tld, s),
+                    "tile lse/D launch");
+        }
         TcBwdArgs a{};
         a.q = Qp;
         a.k = Kp;
@@ -653,13 +660,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         a.B = B;
         a.causal = causal;
         a.scale = scale;
-        a.lse = lse;
-        a.D = D;
-        a.lse_T = T;
-        a.dq = dqa;
-        a.dk = dka;
-        a.dv = dva;
-        a.with_dq = 0;
+        a.tile_ld = tld;
         TcDqArgs qa{};
         qa.q = Qp;
         qa.k = Kp;
@@ -684,7 +685,10 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         if (fused_tc) {
             a.t0 = 0;
             a.t1 = cp;
-            a.kv_accumulate = 0;
+            // complete per KV tile: written once in the gradient dtype
+            a.dk = dk;
+            a.dv = dv;
+            a.out_mode = grad_dtype == RA_BF16 ? 0 : 1;
             {
                 ProfScope ps("ra_tc_bwd_dkdv", s);
                 RA_CUDA(launch_tc_bwd(a, s), "tensor-core dK/dV launch");
@@ -698,7 +702,9 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
                 RA_CUDA(launch_tc_dq(qa, s), "tensor-core dQ launch");
             }
         } else {
-            a.kv_accumulate = 1;
+            a.dk = dka;
+            a.dv = dva;
+            a.out_mode = 2;
             qa.dq = dqa;
             qa.out_mode = 2;
             for (int t = 0; t < cp; ++t) {
@@ -756,8 +762,10 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     {
         ProfScope ps("ra_cast", s);
         if (!fused_tc) RA_CUDA(launch_cast_f32(dqa, dq, grad_dtype, T * Hq * d, s), "cast dq");
-        RA_CUDA(launch_cast_f32(dka, dk, grad_dtype, T * Hkv * d, s), "cast dk");
-        RA_CUDA(launch_cast_f32(dva, dv, grad_dtype, T * Hkv * d, s), "cast dv");
+        if (!fused_tc) {
+            RA_CUDA(launch_cast_f32(dka, dk, grad_dtype, T * Hkv * d, s), "cast dk");
+            RA_CUDA(launch_cast_f32(dva, dv, grad_dtype, T * Hkv * d, s), "cast dv");
+        }
     }
     return RA_OK;
 }

@@ -47,6 +47,10 @@ cudaError_t launch_merge(int n, const float *const *outs, const float *const *ls
 // D[h, t] = sum_c a[t, h, c] * b[t, h, c]   (a, b of dtype; fp32 result)
 cudaError_t launch_rowdot(const void *a, const void *b, int dtype, int64_t T, int H, int d, float *D,
                           cudaStream_t st);
+// Per (query tile, KV head): 128 columns of lse*log2(e) then 128 of D,
+// contiguous (1 KB per tile and head), for the backward's bulk copies.
+cudaError_t launch_tile_lse_d(const void *qtiles, int n_qtiles, int Hkv, int G, const float *lse, const float *D,
+                              int64_t lse_T, float *out, cudaStream_t st);
 // dst (dtype) = src (fp32), n elements.
 cudaError_t launch_cast_f32(const float *src, void *dst, int dtype, int64_t n, cudaStream_t st);
 
@@ -113,25 +117,23 @@ struct TcFwdArgs {
 cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st);
 bool tc_fwd_supported(int dtype, int d, int Hq, int Hkv);
 
-// Tensor-core backward (bf16, d = 128): one CTA per KV tile and KV head.
+// Tensor-core key-side backward (bf16, d = 128): dK and dV, one CTA per KV
+// tile and KV head.  out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 +=.
 struct TcBwdArgs {
     const void *q, *k, *v, *dout;      // permuted buffers
     int64_t T;
     int Hq, Hkv, G;
     const void *qtiles, *kvtiles;      // Tile records
     const int32_t *q_off;              // [cp*(B+1)+1]
-    const void *items;                 // backward WorkItem records (qt0 = KV tile)
+    const void *items;                 // key-side WorkItem records (qt0 = KV tile)
     int n_items;
     int cp, B;
     int t0, t1;                        // >= 0: override every item's step range
     int causal;
     float scale;
-    const float *lse, *D;              // [Hq, lse_T] at original positions
-    int64_t lse_T;
-    float *dq;                         // fp32 [T, Hq, d] at original positions, atomically added
-    float *dk, *dv;                    // fp32 [T, Hkv, d] at original positions
-    int kv_accumulate;                 // 1: dk/dv += (ring steps in separate launches)
-    int with_dq;                       // 1: also dQ (atomics); 0: dK/dV only
+    const float *tile_ld;              // launch_tile_lse_d output for these tiles
+    void *dk, *dv;                     // [T, Hkv, d] at original positions
+    int out_mode;
 };
 cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st);
 

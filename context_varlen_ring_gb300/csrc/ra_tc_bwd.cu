@@ -1,33 +1,29 @@
-// ra_tc_bwd.cu -- tensor-core backward of packed causal varlen ring
-// attention (bf16 in, fp32 accumulation, head dim 128) for sm_103a.
+// ra_tc_bwd.cu -- tensor-core key-side backward (dK, dV) of packed causal
+// varlen ring attention (bf16 in, fp32 accumulation, head dim 128) for
+// sm_103a.
 //
-// What it computes: the textbook gradient of softmax attention from the
-// saved log-sum-exp (the backward half of the RingAttention interface of
-// "[Train] Support custom attention with context parallel", FlagScale PR
-// #910, backward_impl):
-//   P  = exp(scale * Q K^T - lse)        over allowed pairs
-//   dV = P^T dO,   dP = dO V^T,   dS = P o (dP - D),  D = rowsum(dO o O)
-//   dQ = scale * dS K,            dK = scale * dS^T Q
-// with GQA sums over the query heads of each KV head.  In the ring, the K/V
-// shard of rank s meets the queries of rank r = (s + t) mod cp at step t;
-// one CTA owns one KV tile and walks the query tiles of its document over
-// the ring steps, so dK and dV accumulate in fp32 (TMEM) across all steps
-// and are written once; dQ rows receive fp32 atomic adds.
+// What it computes: from the saved log-sum-exp and D = rowsum(dO o O),
+//   P  = exp(scale * Q K^T - lse)   over allowed pairs
+//   dV = P^T dO,   dS = P o (dO V^T - D),   dK = scale * dS^T Q
+// with GQA sums over the query heads of each KV head (the key side of the
+// backward_impl of FlagScale PR #910's RingAttention; the query side, dQ, is
+// ra_tc_dq.cu).  In the ring the K/V shard of rank s meets the queries of
+// rank r = (s + t) mod cp at step t; one CTA owns one KV tile and walks the
+// query tiles of its document over the ring steps, so dK and dV accumulate
+// in fp32 in TMEM across all steps and are written once.
 //
 // GB300 design:
-//  * CTA = one KV tile (128 keys of one KV head).  K and V stay in shared
-//    memory; query tiles (128 MMA rows = 128/G tokens x G heads, as in the
-//    forward) and dO tiles stream through two TMA stages together with the
-//    tile's 128 LSE and D values.
-//  * TMEM (512 columns): dK [0,128), dV [128,256), S^T then P^T [256,384)
-//    (bf16, each half of P^T packed into the first 32 columns of the S^T
-//    half it came from), dP^T then dQ [384,512).
-//  * Per query tile the MMA thread issues, in order:
-//      S^T = K Q^T, dP^T = V dO^T, dV += P^T dO (P from TMEM), next S^T,
-//      dK += dS^T Q, dQ = dS K (dS^T in shared memory read MN-major),
-//    and the compute warpgroup (one thread per key row) turns S^T into P^T
-//    while dP^T runs, builds dS^T while dV runs, and drains dQ with
-//    vector atomics while the next tile's S^T/dP^T run.
+//  * CTA = one KV tile (128 keys of one KV head); K and V stay in shared
+//    memory.  Visited query tiles (128 rows = 128/G tokens x G heads) and
+//    their dO tiles stream through two TMA stages together with the tile's
+//    128 LSE and D values (pre-gathered per tile, one bulk copy).
+//  * Per tile the MMA thread issues S^T = K Q^T and dP^T = V dO^T (SS), then
+//    dV += P^T dO and dK += dS^T Q as TS-MMAs with P^T and dS^T read from
+//    TMEM, so shared memory only streams Q and dO (the SS products at
+//    N = 128 already use most of the shared-memory read port).
+//  * TMEM: dK [0,128), dV [128,256), S^T then P^T [256,384), dP^T then dS^T
+//    [384,512).  Two compute warpgroups split the 128 query columns; each
+//    packs its P^T / dS^T (bf16) over the first 32 of its own 64 columns.
 //  * Every wait is bounded (2 s); a wait that runs out records
 //    RA_ERR_TIMEOUT and the CTA drains its copies and returns.
 #include <cuda.h>
@@ -50,17 +46,15 @@ namespace {
 using namespace dev;
 
 constexpr int kThreads = 384;
-constexpr uint32_t kHalf = 16384;
+constexpr uint32_t kHalf = 16384;                 // 128 rows x 128 B
 constexpr uint32_t kTile = 2 * kHalf;
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kTile;
 constexpr uint32_t kOffQ = 2 * kTile;             // [2] stages
 constexpr uint32_t kOffDO = 4 * kTile;            // [2] stages
-constexpr uint32_t kOffDS = 6 * kTile;            // dS^T, K-major swizzled
-constexpr uint32_t kOffLse = 7 * kTile;           // [2][128] fp32, scaled to log2
-constexpr uint32_t kOffD = kOffLse + 2 * 512;     // [2][128] fp32
-constexpr uint32_t kOffDesc = kOffD + 2 * 512;    // [2] x 2 int4
-constexpr uint32_t kOffBar = kOffDesc + 64;
+constexpr uint32_t kOffInfo = 6 * kTile;          // [2] x {lse[128], D[128], descriptor}
+constexpr uint32_t kInfoBytes = 1024 + 64;
+constexpr uint32_t kOffBar = kOffInfo + 2 * kInfoBytes;
 constexpr uint32_t kSmemBytes = kOffBar + 128;    // base must be 1024-aligned (checked)
 
 struct BwdParams {
@@ -68,11 +62,10 @@ struct BwdParams {
     const int4 *qtiles, *kvtiles, *items;
     const int *q_off;
     int n_items, cp, B, G, log2G, Hq, Hkv;
-    int t0, t1, causal, kv_accumulate, with_dq;
+    int t0, t1, causal, out_mode;                  // 0 bf16 store, 1 fp32 store, 2 fp32 +=
     float scale, scale_log2;
-    const float *lse, *D;
-    long long lse_T;
-    float *dq, *dk, *dv;
+    const float *tile_ld;
+    void *dk, *dv;
     int *status;
     unsigned long long budget_ns;
 };
@@ -102,7 +95,17 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_s, uint32_t b
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ BwdParams p) {
+// D[tmem] (+)= A[tmem] B: A = 128 x 128 bf16 packed by the two compute
+// groups at TMEM columns [0,32) and [64,96); B (128 rows x 128) read
+// MN-major from shared memory.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_s, uint32_t idesc, bool acc) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        tc_mma_ts(d_tmem, a_tmem + 8u * k + (k >= 4 ? 32u : 0u), sdesc_sw128(b_s + k * 2048u, kHalf, 1024), idesc,
+                  (acc || k > 0) ? 1u : 0u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base_s = smem_u32(smem);
     if (base_s & 1023u) {  // the layout has no slack for realignment
@@ -111,20 +114,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *kv_full = bars + 0;
-    uint64_t *st_full = bars + 1;    // [2] Q, dO, lse, D and descriptor of a stage (32 arrivals)
+    uint64_t *st_full = bars + 1;    // [2] Q, dO, lse, D of a stage (TMA + bulk copies)
     uint64_t *st_empty = bars + 3;   // [2]
     uint64_t *s_full = bars + 5;     // S^T done
     uint64_t *dp_full = bars + 6;    // dP^T done
     uint64_t *p_ready = bars + 7;    // P^T in TMEM (256 arrivals)
-    uint64_t *ds_ready = bars + 8;   // dS^T in shared memory (256 arrivals)
-    uint64_t *dq_full = bars + 9;    // dK (and dQ) done: dS^T and dQ may be reused
-    uint64_t *dq_empty = bars + 10;  // dQ read out (256 arrivals)
-    uint64_t *mma_done = bars + 11;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 12);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 13);
-    float *lse_st = reinterpret_cast<float *>(smem + kOffLse);
-    float *d_st = reinterpret_cast<float *>(smem + kOffD);
-    int4 *desc = reinterpret_cast<int4 *>(smem + kOffDesc);
+    uint64_t *ds_ready = bars + 8;   // dS^T in TMEM (256 arrivals)
+    uint64_t *mma_done = bars + 9;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 11);
+    auto info = [&](uint32_t st) -> uint8_t * { return smem + kOffInfo + st * kInfoBytes; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -134,21 +133,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     const int t1 = p.t0 >= 0 ? p.t1 : ib.z;
     const int4 ka = __ldg(p.kvtiles + 2 * kt), kb = __ldg(p.kvtiles + 2 * kt + 1);
     // KV tile: row0 ka.x, len ka.y, split ka.z, pos0 ka.w, pos1 kb.x, pmin kb.y, pmax kb.z
-    const bool with_dq = p.with_dq != 0;
+    const int G = p.G;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(kv_full, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(st_full + i, 32);
+            mbar_init(st_full + i, 1);
             mbar_init(st_empty + i, 1);
         }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
         mbar_init(p_ready, 256);
         mbar_init(ds_ready, 256);
-        mbar_init(dq_full, 1);
-        mbar_init(dq_empty, 256);
         mbar_init(mma_done, 1);
         fence_mbar_init();
     }
@@ -165,7 +162,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 
     if (warp == 0) {
         // ------------------------------------------------ producer
-        const int G = p.G;
         if (lane == 0) {
             tma_prefetch_desc(&p.tmQ);
             tma_prefetch_desc(&p.tmK);
@@ -177,67 +173,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             tma_load_3d(smem + kOffV, &p.tmV, kv_full, 0, g, ka.x);
             tma_load_3d(smem + kOffV + kHalf, &p.tmV, kv_full, 64, g, ka.x);
         }
-        uint32_t n = 0;
+        uint32_t n = 0;  // tiles published
         int ok = 1;
-        const float log2e = 1.4426950408889634f;
-        // A visited query tile waits in registers (descriptor, its 128 LSE and
-        // D values already loaded) while the previous one is published, so
-        // the global-load latency overlaps the wait for a free stage.
-        bool pend = false;
-        int4 pd0 = make_int4(0, 0, 0, 0), pd1 = make_int4(0, 0, 0, 0);
-        float pl[4], pD[4];
-        auto fetch = [&](const int4 &d0, const int4 &d1) {
-            const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int c = lane + 32 * e;
-                const int tok = c >> p.log2G, head = g * G + (c & (G - 1));
-                pl[e] = INFINITY;
-                pD[e] = 0.f;
-                if (tok < qlen) {
-                    const int pos = tok < split ? pos0 + tok : pos1 + (tok - split);
-                    pl[e] = __ldg(p.lse + (long long)head * p.lse_T + pos);
-                    pD[e] = __ldg(p.D + (long long)head * p.lse_T + pos);
-                }
-            }
-            pd0 = d0;
-            pd1 = d1;
-            pend = true;
-        };
-        auto publish = [&](bool end) {
+        // lane 0 publishes a query tile: descriptor, Q and dO by TMA, its 128
+        // LSE and D values (pre-gathered per tile) by bulk copy, one barrier
+        auto publish = [&](const int4 &d0, const int4 &d1, int qt, bool end) {
             const uint32_t st = n & 1u;
-            if (lane == 0 && !mbar_wait(st_empty + st, ((n >> 1) & 1u) ^ 1u, wc)) ok = 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) return;
-            if (!end) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = lane + 32 * e;
-                    lse_st[st * 128 + c] = (pl[e] == -INFINITY) ? INFINITY : pl[e] * log2e;
-                    d_st[st * 128 + c] = pD[e];
-                }
-            }
             if (lane == 0) {
-                desc[2 * st] = end ? make_int4(0, 0, 0, 0) : pd0;
-                desc[2 * st + 1] = end ? make_int4(0, 1, 0, 0) : pd1;
-            }
-            __syncwarp();
-            if (lane == 0) {
-                if (!end) {
-                    mbar_arrive_expect_tx(st_full + st, 2 * kTile);
-                    const int hq0 = g * G;
-                    tma_load_3d(smem + kOffQ + st * kTile, &p.tmQ, st_full + st, 0, hq0, pd0.x);
-                    tma_load_3d(smem + kOffQ + st * kTile + kHalf, &p.tmQ, st_full + st, 64, hq0, pd0.x);
-                    tma_load_3d(smem + kOffDO + st * kTile, &p.tmDO, st_full + st, 0, hq0, pd0.x);
-                    tma_load_3d(smem + kOffDO + st * kTile + kHalf, &p.tmDO, st_full + st, 64, hq0, pd0.x);
+                if (!mbar_wait(st_empty + st, ((n >> 1) & 1u) ^ 1u, wc)) {
+                    ok = 0;
                 } else {
-                    mbar_arrive(st_full + st);
+                    int4 *desc = reinterpret_cast<int4 *>(info(st) + 1024);
+                    desc[0] = d0;
+                    desc[1] = end ? make_int4(0, 1, 0, 0) : d1;
+                    if (!end) {
+                        mbar_arrive_expect_tx(st_full + st, 2 * kTile + 1024);
+                        const int hq0 = g * G;
+                        tma_load_3d(smem + kOffQ + st * kTile, &p.tmQ, st_full + st, 0, hq0, d0.x);
+                        tma_load_3d(smem + kOffQ + st * kTile + kHalf, &p.tmQ, st_full + st, 64, hq0, d0.x);
+                        tma_load_3d(smem + kOffDO + st * kTile, &p.tmDO, st_full + st, 0, hq0, d0.x);
+                        tma_load_3d(smem + kOffDO + st * kTile + kHalf, &p.tmDO, st_full + st, 64, hq0, d0.x);
+                        bulk_load(info(st), p.tile_ld + ((long long)qt * p.Hkv + g) * 256, 1024, st_full + st);
+                    } else {
+                        mbar_arrive(st_full + st);
+                    }
                 }
-            } else {
-                mbar_arrive(st_full + st);
             }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
             ++n;
-            pend = false;
         };
         for (int t = t0; t < t1 && ok; ++t) {
             const int r = (s + t) % p.cp;
@@ -265,13 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     d1.y = __shfl_sync(0xffffffffu, cls, src) << 1;  // flags: class << 1, bit 0 = end
                     d1.z = 0;
                     d1.w = 0;
-                    if (pend) publish(false);
-                    if (ok) fetch(d0, d1);
+                    publish(d0, d1, bi + src, false);
                 }
             }
         }
-        if (ok && pend) publish(false);
-        if (ok) publish(true);
+        if (ok) publish(make_int4(0, 0, 0, 0), make_int4(0, 1, 0, 0), 0, true);
         if (lane == 0) {
             volatile int local_abort = 0;
             const WaitCtl drain{&local_abort, p.status, p.budget_ns};
@@ -283,12 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);   // A, B K-major
-            const uint32_t id_kmn = idesc_bf16_f32(128, 128, 0, 1);  // A K-major (smem/TMEM), B MN-major
-            const uint32_t id_mnmn = idesc_bf16_f32(128, 128, 1, 1); // A MN-major, B MN-major
-            const uint32_t ks_ = base_s + kOffK, vs_ = base_s + kOffV, dss = base_s + kOffDS;
+            const uint32_t id_ts = idesc_bf16_f32(128, 128, 0, 1);   // A in TMEM, B MN-major
+            const uint32_t ks_ = base_s + kOffK, vs_ = base_s + kOffV;
+            auto is_end = [&](uint32_t st) {
+                return (reinterpret_cast<const int4 *>(info(st) + 1024)[1].y & 1) != 0;
+            };
             bool ok = mbar_wait(kv_full, 0, wc) && mbar_wait(st_full + 0, 0, wc);
             tc_fence_after();
-            bool have = ok && !(desc[1].y & 1);
+            bool have = ok && !is_end(0);
             uint32_t i = 0;
             if (have) {
                 mma_kk(tS, ks_, base_s + kOffQ, id_kk);
@@ -297,51 +260,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                 tc_commit(dp_full);
             }
             while (ok && have) {
-                const uint32_t st = i & 1u;
+                const uint32_t st = i & 1u, nst = (i + 1) & 1u;
                 const uint32_t qs = base_s + kOffQ + st * kTile, dos = base_s + kOffDO + st * kTile;
-                // dV += P^T dO: P^T from TMEM, dO read MN-major (d contiguous)
+                // dV += P^T dO
                 if (!mbar_wait(p_ready, i & 1u, wc)) break;
                 tc_fence_after();
-                // P^T columns 0-63 are packed at TMEM columns [0,32) and
-                // columns 64-127 at [64,96) (each warpgroup writes inside its
-                // own S^T columns)
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    tc_mma_ts(tDV, tS + 8u * k + (k >= 4 ? 32u : 0u), sdesc_sw128(dos + k * 2048u, kHalf, 1024), id_kmn,
-                              (i > 0 || k > 0));
-                // next tile's S^T (the dV above read P^T first: in-order)
-                const uint32_t nst = (i + 1) & 1u;
+                mma_ts(tDV, tS, dos, id_ts, i > 0);
+                // next tile's S^T (the dV above reads P^T first: in order)
                 if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
                 tc_fence_after();
-                const bool have_next = !(desc[2 * nst + 1].y & 1);
+                const bool have_next = !is_end(nst);
                 if (have_next) {
                     mma_kk(tS, ks_, base_s + kOffQ + nst * kTile, id_kk);
                     tc_commit(s_full);
                 }
-                // dK += dS^T Q (dS^T K-major in shared memory, Q read MN-major)
+                // dK += dS^T Q
                 if (!mbar_wait(ds_ready, i & 1u, wc)) break;
                 tc_fence_after();
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t aoff = (uint32_t)(k >> 2) * kHalf + (uint32_t)(k & 3) * 32u;
-                    tc_mma_ss(tDK, sdesc_sw128(dss + aoff, 16, 1024), sdesc_sw128(qs + k * 2048u, kHalf, 1024),
-                              id_kmn, (i > 0 || k > 0));
-                }
+                mma_ts(tDK, tDP, qs, id_ts, i > 0);
                 tc_commit(st_empty + st);  // Q and dO of this stage are no longer read
-                if (with_dq) {
-                    // dQ = dS K: dS^T read MN-major (query rows contiguous), K read MN-major
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        tc_mma_ss(tDP, sdesc_sw128(dss + k * 2048u, kHalf, 1024),
-                                  sdesc_sw128(ks_ + k * 2048u, kHalf, 1024), id_mnmn, k > 0);
-                }
-                tc_commit(dq_full);
                 if (!have_next) break;
-                if (with_dq) {
-                    // next tile's dP^T overwrites dQ once it has been read out
-                    if (!mbar_wait(dq_empty, i & 1u, wc)) break;
-                    tc_fence_after();
-                }
+                // next tile's dP^T (the dK above reads dS^T first: in order)
                 mma_kk(tDP, vs_, base_s + kOffDO + nst * kTile, id_kk);
                 tc_commit(dp_full);
                 ++i;
@@ -353,32 +292,35 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         }
     } else if (warp >= 4) {
         // ------------------------------------------------ compute warpgroups
-        // Warpgroup h (warps 4-7: h = 0, warps 8-11: h = 1) owns columns
-        // [64h, 64h + 64) of S^T, dP^T, dQ, dK and dV; thread j owns TMEM lane j.
+        // Group h (warps 4-7: 0, warps 8-11: 1) owns columns [64h, 64h+64) of
+        // S^T and dP^T and d columns [64h, 64h+64) of dK and dV; thread j owns
+        // TMEM lane j (one key row).
         const int h = (warp >= 8) ? 1 : 0;
         const int j = (threadIdx.x - 128) & 127;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const bool kvalid = j < ka.y;
         const int kpos = j < ka.z ? ka.w + j : kb.x + (j - ka.z);
-        const int G = p.G;
-        const int tok_m = j >> p.log2G, head_m = g * G + (j & (G - 1));
-        uint8_t *dsrow = smem + kOffDS + h * kHalf + (j >> 3) * 1024 + (j & 7) * 128;
-        const int sw = j & 7;
-        float P[64];
-        bool ok = mbar_wait(st_full + 0, 0, wc);
-        int4 dc0 = desc[0], dc1 = desc[1];
-        bool have = ok && !(dc1.y & 1);
-        uint32_t i = 0;
-
-        // S^T -> P^T (fp32 in registers; bf16 into TMEM over the first 32 of
-        // this warpgroup's own 64 S^T columns, which it has already read)
-        auto step_p = [&](uint32_t it, const int4 &d0, const int4 &d1) -> bool {
-            if (!mbar_wait(s_full, it & 1u, wc)) return false;
+        bool ok = true;
+        uint32_t nt = 0;
+        for (uint32_t i = 0;; ++i) {
+            const uint32_t st = i & 1u;
+            if (!mbar_wait(st_full + st, (i >> 1) & 1u, wc)) {
+                ok = false;
+                break;
+            }
+            const uint8_t *I = info(st);
+            const int4 d0 = reinterpret_cast<const int4 *>(I + 1024)[0];
+            const int4 d1 = reinterpret_cast<const int4 *>(I + 1024)[1];
+            if (d1.y & 1) break;
+            const int cls = d1.y >> 1;
+            // ---- P^T = exp2(S^T * scale * log2e - lse * log2e), masked
+            if (!mbar_wait(s_full, i & 1u, wc)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             uint32_t v[64];
             tmem_ld64(tS + lane_base + 64u * h, v);
-            const float4 *l4 = reinterpret_cast<const float4 *>(lse_st + (it & 1u) * 128 + 64 * h);
-            const int cls = d1.y >> 1;
             uint32_t wm[2] = {~0u, ~0u};
             if (cls == kPartial) {
                 int a1 = 0, e1 = 0, a2 = 0, e2 = 0;
@@ -400,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     wm[ch] = range_bits(a1 * G, e1 * G, cb) | range_bits(a2 * G, e2 * G, cb);
                 }
             }
+            const float4 *l4 = reinterpret_cast<const float4 *>(I) + 16 * h;
+            float P[64];
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
                 const float4 l = l4[c4];
@@ -411,21 +355,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                     P[c] = ((wm[c >> 5] >> (c & 31)) & 1u) ? x : 0.f;
                 }
             }
-            uint32_t pk[32];
+            {
+                uint32_t pk[32];
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2) pk[c2] = pack_bf16x2(P[2 * c2], P[2 * c2 + 1]);
-            tmem_st32(tS + lane_base + 64u * h, pk);
+                for (int c2 = 0; c2 < 32; ++c2) pk[c2] = pack_bf16x2(P[2 * c2], P[2 * c2 + 1]);
+                tmem_st32(tS + lane_base + 64u * h, pk);
+            }
             tc_fence_before();
             mbar_arrive(p_ready);
-            return true;
-        };
-        // dP^T -> dS^T = P^T o (dP^T - D) * scale, bf16 into shared memory
-        auto step_ds = [&](uint32_t it) -> bool {
-            if (!mbar_wait(dp_full, it & 1u, wc)) return false;
+            // ---- dS^T = P^T o (dP^T - D) * scale, bf16 over this group's dP^T columns
+            if (!mbar_wait(dp_full, i & 1u, wc)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            uint32_t v[64];
             tmem_ld64(tDP + lane_base + 64u * h, v);
-            const float4 *d4 = reinterpret_cast<const float4 *>(d_st + (it & 1u) * 128 + 64 * h);
+            const float4 *d4 = reinterpret_cast<const float4 *>(I + 512) + 16 * h;
             uint32_t pk[32];
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
@@ -436,66 +381,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
                 pk[2 * c4 + 1] = pack_bf16x2(P[c + 2] * (__uint_as_float(v[c + 2]) - dd.z) * p.scale,
                                              P[c + 3] * (__uint_as_float(v[c + 3]) - dd.w) * p.scale);
             }
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<uint4 *>(dsrow + ((c ^ sw) << 4)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            fence_proxy_async_smem();
+            tmem_st32(tDP + lane_base + 64u * h, pk);
             tc_fence_before();
             mbar_arrive(ds_ready);
-            return true;
-        };
-        // dK (and dQ) of tile `it` done; with dQ: read it out (thread = query
-        // row) and add it into dq at the row's position with fp32 vector atomics
-        auto step_dq = [&](uint32_t it, const int4 &d0, const int4 &d1) -> bool {
-            if (!mbar_wait(dq_full, it & 1u, wc)) return false;
-            tc_fence_after();
-            if (!with_dq) return true;
-            const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
-            const bool qvalid = tok_m < qlen;
-            const int qpos = tok_m < split ? pos0 + tok_m : pos1 + (tok_m - split);
-            uint32_t v[64];
-            tmem_ld64(tDP + lane_base + 64u * h, v);
-            tc_fence_before();
-            mbar_arrive(dq_empty);
-            if (qvalid) {
-                float4 *dst = reinterpret_cast<float4 *>(p.dq + ((long long)qpos * p.Hq + head_m) * 128 + 64 * h);
-#pragma unroll
-                for (int q4 = 0; q4 < 16; ++q4)
-                    atomicAdd(dst + q4, make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
-                                                    __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3])));
-            }
-            return true;
-        };
-
-        if (have) ok = step_p(0, dc0, dc1) && step_ds(0);
-        while (ok && have) {
-            const uint32_t nst = (i + 1) & 1u;
-            if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) {
-                ok = false;
-                break;
-            }
-            const int4 nd0 = desc[2 * nst], nd1 = desc[2 * nst + 1];
-            const bool have_next = !(nd1.y & 1);
-            if (have_next && !step_p(i + 1, nd0, nd1)) {
-                ok = false;
-                break;
-            }
-            if (!step_dq(i, dc0, dc1)) {
-                ok = false;
-                break;
-            }
-            if (!have_next) break;
-            if (!step_ds(i + 1)) {
-                ok = false;
-                break;
-            }
-            dc0 = nd0;
-            dc1 = nd1;
-            ++i;
+            ++nt;
         }
         // ---------------------------------------------- epilogue: dK, dV rows
-        const bool has_acc = ok && have;
+        if (ok && nt > 0) {
+            ok = mbar_wait(mma_done, 0, wc);
+            tc_fence_after();
+        }
+        const bool has_acc = ok && nt > 0;
         const long long rowoff = ((long long)kpos * p.Hkv + g) * 128 + 64 * h;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
@@ -506,13 +402,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll
                 for (int e = 0; e < 64; ++e) v[e] = 0u;
             }
-            if (kvalid) {
-                float4 *d4 = reinterpret_cast<float4 *>((which ? p.dv : p.dk) + rowoff);
+            if (!kvalid) continue;
+            void *outp = which ? p.dv : p.dk;
+            if (p.out_mode == 0) {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(outp) + rowoff);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1]));
+                    w.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3]));
+                    w.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5]));
+                    w.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7]));
+                    dst[q4] = w;
+                }
+            } else {
+                float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(outp) + rowoff);
 #pragma unroll
                 for (int q4 = 0; q4 < 16; ++q4) {
                     float4 x = make_float4(__uint_as_float(v[4 * q4]), __uint_as_float(v[4 * q4 + 1]),
                                            __uint_as_float(v[4 * q4 + 2]), __uint_as_float(v[4 * q4 + 3]));
-                    if (p.kv_accumulate) {
+                    if (p.out_mode == 2) {
                         const float4 o = d4[q4];
                         x.x += o.x;
                         x.y += o.y;
@@ -586,14 +495,10 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
     p.t0 = a.t0;
     p.t1 = a.t1;
     p.causal = a.causal;
-    p.kv_accumulate = a.kv_accumulate;
-    p.with_dq = a.with_dq;
+    p.out_mode = a.out_mode;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    p.lse = a.lse;
-    p.D = a.D;
-    p.lse_T = a.lse_T;
-    p.dq = a.dq;
+    p.tile_ld = a.tile_ld;
     p.dk = a.dk;
     p.dv = a.dv;
     p.status = device_status_ptr();
@@ -602,11 +507,11 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(tc_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_bwd_kernel<<<a.n_items, kThreads, kSmemBytes, st>>>(p);
+    tc_dkdv_kernel<<<a.n_items, kThreads, kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 
