@@ -55,6 +55,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe of the same condition (mbarrier.test_wait): lets a
+// thread that feeds the tensor pipe check its next dependency while the
+// queued products still run, instead of after they drain.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Shared abort state of a CTA: set by the first wait that runs out of
 // budget; every other wait of the CTA then gives up at once.
 struct WaitCtl {

@@ -14,12 +14,21 @@
 // backward.
 //
 // GB300 design: one CTA per query tile (128 MMA rows = 128/G tokens x G
-// heads of one KV head); Q and dO stay in shared memory; K/V tiles stream
-// through a 5-slot TMA ring fed by a producer warp that publishes each
-// visited KV tile (class and positions) through a shared-memory ring.
-// TMEM: dQ [0,128), S double-buffered [128,256) and [256,384), dP [384,512)
-// with dS (bf16) written over each warpgroup's own dP columns and fed to
-// the dQ TS-MMA.  Two compute warpgroups split the 128 key columns.
+// heads of one KV head).  Q and dO arrive by TMA once; Q is copied into
+// TMEM by the compute warpgroups (S = Q K^T is a TS-MMA) and its staging
+// area becomes a sixth slot of the K/V ring, while dO stays in shared
+// memory as the A operand of dP = dO V^T.  K/V tiles are fed by a producer
+// warp that publishes each visited KV tile (class and positions) through a
+// shared-memory ring.  TMEM: dQ [0,128), S [128,256), dP [256,384), Q
+// (bf16) [384,448), dS (bf16) [448,512).  Two compute warpgroups split the
+// 128 key columns.
+//
+// dS has its own TMEM buffer, so dP(j+1) may start as soon as the compute
+// groups have loaded dP(j), and the only loop left between products is
+// dQ(j) -> (dS buffer free) -> store dS(j+1) -> dQ(j+1).  One thread issues
+// a tcgen05.mma only about every 45-60 cycles, close to the 64 cycles an
+// M=128 N=128 K=16 product runs, so two warps issue: warp 1 the S
+// products and warp 3 dP(j+1) then dQ(j).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -40,14 +49,14 @@ namespace {
 using namespace dev;
 
 constexpr int kThreads = 384;
-constexpr int kSlots = 5;
+constexpr int kSlots = 6;  // slots 0-4 after the Q/dO staging, slot 5 reuses the Q staging
 constexpr int kRing = 8;
 constexpr uint32_t kHalf = 16384;
 constexpr uint32_t kTile = 2 * kHalf;
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffDO = kTile;
 constexpr uint32_t kOffKV = 2 * kTile;
-constexpr uint32_t kOffBar = kOffKV + kSlots * kTile;
+constexpr uint32_t kOffBar = kOffKV + 5 * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 
 struct DqParams {
@@ -56,7 +65,7 @@ struct DqParams {
     const int *kv_off;
     int n_items, cp, B, G, log2G, Hq;
     int t0, t1, causal, out_mode;  // out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 +=
-    float scale, scale_log2;
+    float scale, scale_log2, log2_scale;
     const float *lse, *D;
     long long lse_T;
     void *dq;
@@ -80,13 +89,7 @@ __device__ __forceinline__ uint32_t range_bits(int a, int b, int base) {
     return (uint32_t)(((1ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
 }
 
-__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_s, uint32_t b_s, uint32_t idesc) {
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-        tc_mma_ss(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024), idesc, ks > 0);
-    }
-}
+__device__ __forceinline__ uint32_t slot_off(uint32_t s) { return s < 5 ? kOffKV + s * kTile : kOffQ; }
 
 __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constant__ DqParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -97,16 +100,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
     uint64_t *q_full = bars + 0;
     uint64_t *kv_full = bars + 1;      // [kSlots]
-    uint64_t *kv_empty = bars + 6;     // [kSlots]
-    uint64_t *s_full = bars + 11;      // [2] S buffer b done (one phase per use)
-    uint64_t *dp_full = bars + 13;     // dP done
-    uint64_t *ds_ready = bars + 14;    // dS in TMEM (256 arrivals)
-    uint64_t *mma_done = bars + 15;
-    uint64_t *info_full = bars + 16;   // [kRing]
-    uint64_t *info_empty = bars + 24;  // [kRing]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 32);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 33);
-    int4 *ring = reinterpret_cast<int4 *>(bars + 34);  // [kRing]
+    uint64_t *kv_empty = bars + 7;     // [kSlots]
+    uint64_t *s_full = bars + 13;      // S done
+    uint64_t *s_free = bars + 14;      // S read by both compute groups (256 arrivals)
+    uint64_t *dp_full = bars + 15;     // dP done
+    uint64_t *dp_free = bars + 16;     // dP read by both compute groups (256 arrivals)
+    uint64_t *ds_ready = bars + 17;    // [2] dS half h in TMEM (128 arrivals each)
+    uint64_t *dq_done = bars + 19;     // dQ(j) done: dS buffer free
+    uint64_t *qc_ready = bars + 20;    // Q copied into TMEM (256 arrivals)
+    uint64_t *mma_done = bars + 21;    // all dQ products done
+    uint64_t *a_done = bars + 22;      // S issuer drained
+    uint64_t *info_full = bars + 23;   // [kRing]
+    uint64_t *info_empty = bars + 31;  // [kRing]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 39);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 40);
+    int4 *ring = reinterpret_cast<int4 *>(bars + 42);  // [kRing]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -124,14 +132,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
             mbar_init(kv_full + i, 1);
             mbar_init(kv_empty + i, 1);
         }
-        mbar_init(s_full + 0, 1);
-        mbar_init(s_full + 1, 1);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 256);
         mbar_init(dp_full, 1);
-        mbar_init(ds_ready, 256);
+        mbar_init(dp_free, 256);
+        mbar_init(ds_ready + 0, 128);
+        mbar_init(ds_ready + 1, 128);
+        mbar_init(dq_done, 1);
+        mbar_init(qc_ready, 256);
         mbar_init(mma_done, 1);
+        mbar_init(a_done, 1);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(info_full + i, 1);
-            mbar_init(info_empty + i, 1 + 256);
+            mbar_init(info_empty + i, 2 + 256);
         }
         fence_mbar_init();
     }
@@ -144,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{abort_flag, p.status, p.budget_ns};
-    const uint32_t tDQ = tmem, tS0 = tmem + 128, tDP = tmem + 384;
+    const uint32_t tDQ = tmem, tS = tmem + 128, tDP = tmem + 256, tQ = tmem + 384, tDS = tmem + 448;
 
     auto read_info = [&](uint32_t jt, int4 &e) -> bool {
         const uint32_t slot = jt % kRing;
@@ -210,7 +223,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                                     ok = 0;
                                     break;
                                 }
-                                uint8_t *dst = base + kOffKV + slot * kTile;
+                                // slot 5 is the Q staging: free once Q is copied into TMEM
+                                if (u == 5 && !mbar_wait(qc_ready, 0, wc)) {
+                                    ok = 0;
+                                    break;
+                                }
+                                uint8_t *dst = base + slot_off(slot);
                                 const CUtensorMap *m = kv ? &p.tmV : &p.tmK;
                                 mbar_arrive_expect_tx(kv_full + slot, kTile);
                                 tma_load_3d(dst, m, kv_full + slot, 0, g, row0);
@@ -236,72 +254,86 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 for (uint32_t x = (u > kSlots ? u - kSlots : 0); x < u; ++x)
                     (void)mbar_wait(kv_full + (x % kSlots), (x / kSlots) & 1u, drain);
             }
-        } else if (warp == 1) {
-            // -------------------------------------------- MMA issuer
-            if (lane == 0) {
-                const uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);
-                const uint32_t id_kmn = idesc_bf16_f32(128, 128, 0, 1);
-                const uint32_t qs = base_s + kOffQ, dos = base_s + kOffDO, kvs = base_s + kOffKV;
-                bool ok = mbar_wait(q_full, 0, wc);
+        } else if (lane == 0 && warp != 2) {
+            // -------------------------------------------- MMA issuers (warps 1 and 3)
+            constexpr uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: A and B K-major
+            constexpr uint32_t id_q = idesc_bf16_f32(128, 128, 0, 1);  // dQ: B MN-major
+            // K-major SW128 operand: 16-element k-step ks at (ks / 4) * kHalf + (ks % 4) * 32
+            auto kstep = [](int ks) -> uint32_t { return (((ks >> 2) * kHalf + (ks & 3) * 32u) >> 4); };
+            auto kv_par = [](uint32_t u) { return (u / kSlots) & 1u; };
+            auto wait = [&](uint64_t *bar, uint32_t par) -> bool {
+                const bool r = mbar_wait(bar, par, wc);
                 tc_fence_after();
-                int4 e;
-                ok = ok && read_info(0, e);
-                bool have = ok && !(e.x & 16);
-                uint32_t j = 0;
-                if (have) {
-                    // S(0), dP(0)
-                    if (!mbar_wait(kv_full + 0, 0, wc)) ok = false;
-                    tc_fence_after();
-                    if (ok) {
-                        mma_kk(tS0, qs, kvs, id_kk);
-                        tc_commit(s_full + 0);
-                    }
-                    if (ok && !mbar_wait(kv_full + 1, 0, wc)) ok = false;
-                    tc_fence_after();
-                    if (ok) {
-                        mma_kk(tDP, dos, kvs + kTile, id_kk);
-                        tc_commit(dp_full);
-                        tc_commit(kv_empty + 1);  // V(0) only feeds dP(0)
-                    }
+                return r;
+            };
+            uint64_t *drain_bar = warp == 1 ? a_done : mma_done;
+            if (warp == 1) {
+                // S(j) = Q K(j)^T (Q from TMEM) once both groups have read S(j-1)
+                bool ok = wait(qc_ready, 0);
+                for (uint32_t j = 0; ok; ++j) {
+                    int4 e;
+                    if (!read_info(j, e) || (e.x & 16)) break;
+                    if (j > 0 && !wait(s_free, (j - 1) & 1u)) break;
+                    const uint32_t ku = 2 * j;
+                    if (!wait(kv_full + ku % kSlots, kv_par(ku))) break;
+                    const uint64_t d0 = sdesc_sw128(base_s + slot_off(ku % kSlots), 16, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) tc_mma_ts(tS, tQ + 8u * ks, d0 + kstep(ks), id_s, ks > 0);
+                    tc_commit(s_full);
                 }
-                while (ok && have) {
+            } else {
+                // dP(j+1) = dO V(j+1)^T (dO from shared memory) once dP(j) was read,
+                // then dQ += dS(j) K(j)
+                const uint64_t a0 = sdesc_sw128(base_s + kOffDO, 16, 1024);
+                auto mma_dp = [&](uint32_t vu) {
+                    const uint64_t d0 = sdesc_sw128(base_s + slot_off(vu % kSlots), 16, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) tc_mma_ss(tDP, a0 + kstep(ks), d0 + kstep(ks), id_s, ks > 0);
+                    tc_commit(dp_full);
+                    tc_commit(kv_empty + vu % kSlots);  // V only feeds dP
+                };
+                int4 e;
+                bool have = wait(q_full, 0) && read_info(0, e) && !(e.x & 16);
+                if (have && wait(kv_full + 1, kv_par(1)))
+                    mma_dp(1);
+                else
+                    have = false;
+                for (uint32_t j = 0; have; ++j) {
                     int4 en;
                     if (!read_info(j + 1, en)) break;
                     const bool have_next = !(en.x & 16);
-                    const uint32_t kload = 2 * j, kslot = kload % kSlots;
-                    const uint32_t nk = 2 * j + 2, nkslot = nk % kSlots;
-                    const uint32_t nv = 2 * j + 3, nvslot = nv % kSlots;
                     if (have_next) {
-                        // S(j+1) into the other S buffer while the compute groups work on j
-                        if (!mbar_wait(kv_full + nkslot, (nk / kSlots) & 1u, wc)) break;
-                        tc_fence_after();
-                        mma_kk(tS0 + 128u * ((j + 1) & 1u), qs, kvs + nkslot * kTile, id_kk);
-                        tc_commit(s_full + ((j + 1) & 1u));
+                        const uint32_t vu = 2 * j + 3;
+                        if (!wait(dp_free, j & 1u)) break;
+                        if (!wait(kv_full + vu % kSlots, kv_par(vu))) break;
+                        mma_dp(vu);
                     }
-                    // dQ += dS(j) K(j): dS from TMEM (halves at dP columns [0,32) and
-                    // [64,96)), K read MN-major (d contiguous)
-                    if (!mbar_wait(ds_ready, j & 1u, wc)) break;
-                    tc_fence_after();
-                    const uint32_t ks_ = kvs + kslot * kTile;
+                    // dQ += dS_h(j) K(j)_h: keys [64h, 64h + 64) = K rows (MN-major: d
+                    // contiguous), A = group h's dS at dS columns [32h, 32h + 32)
+                    const uint32_t kslot = (2 * j) % kSlots;
+                    const uint64_t d0 = sdesc_sw128(base_s + slot_off(kslot), kHalf, 1024);
+                    bool okh = true;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        tc_mma_ts(tDQ, tDP + 8u * k + (k >= 4 ? 32u : 0u), sdesc_sw128(ks_ + k * 2048u, kHalf, 1024),
-                                  id_kmn, (j > 0 || k > 0));
-                    tc_commit(kv_empty + kslot);  // K(j) done
+                    for (int h = 0; h < 2; ++h) {
+                        if (!wait(ds_ready + h, j & 1u)) {
+                            okh = false;
+                            break;
+                        }
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma_ts(tDQ, tDS + 32u * h + 8u * k, d0 + ((8192u * h + 2048u * k) >> 4), id_q,
+                                      (j > 0 || h > 0 || k > 0));
+                    }
+                    if (!okh) break;
+                    tc_commit(dq_done);
+                    tc_commit(kv_empty + kslot);  // K(j) done (S(j) finished before dS(j))
                     if (!have_next) break;
-                    // dP(j+1) overwrites dS(j) after the dQ MMA above (in order)
-                    if (!mbar_wait(kv_full + nvslot, (nv / kSlots) & 1u, wc)) break;
-                    tc_fence_after();
-                    mma_kk(tDP, dos, kvs + nvslot * kTile, id_kk);
-                    tc_commit(dp_full);
-                    tc_commit(kv_empty + nvslot);  // V(j+1) done
-                    ++j;
                 }
-                tc_commit(mma_done);
-                volatile int local_abort = 0;
-                const WaitCtl drain{&local_abort, p.status, p.budget_ns};
-                (void)mbar_wait(mma_done, 0, drain);
             }
+            tc_commit(drain_bar);
+            volatile int local_abort = 0;
+            const WaitCtl drain{&local_abort, p.status, p.budget_ns};
+            (void)mbar_wait(drain_bar, 0, drain);
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
@@ -315,15 +347,37 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
         const int tok = m >> p.log2G, head = g * G + (m & (G - 1));
         const bool valid = tok < qa.y;
         const int qpos = tok < qa.z ? qa.w + tok : qb.x + (tok - qa.z);
-        float l2 = INFINITY, Dm = 0.f;
+        // P' = scale * P = exp2(s * scale * log2(e) + bias), bias = log2(scale) - lse * log2(e)
+        float bias = -INFINITY, Dm = 0.f;
         if (valid) {
             const float l = __ldg(p.lse + (long long)head * p.lse_T + qpos);
-            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+            bias = (l == -INFINITY) ? -INFINITY : p.log2_scale - l * 1.4426950408889634f;
             Dm = __ldg(p.D + (long long)head * p.lse_T + qpos);
         }
-        bool ok = true;
+        bool ok = mbar_wait(q_full, 0, wc);
+        if (ok) {
+            // copy this group's d half of the Q row into TMEM (bf16 pairs);
+            // swizzled 128-byte rows: chunk c of row m at (c ^ (m & 7)) * 16
+            const uint8_t *qrow = base + kOffQ + h * kHalf + (m >> 3) * 1024 + (m & 7) * 128;
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                uint32_t w[16];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int ch = 4 * part + c;
+                    const uint4 x = *reinterpret_cast<const uint4 *>(qrow + ((ch ^ (m & 7)) << 4));
+                    w[4 * c] = x.x;
+                    w[4 * c + 1] = x.y;
+                    w[4 * c + 2] = x.z;
+                    w[4 * c + 3] = x.w;
+                }
+                tmem_st16(tQ + lane_base + 32u * h + 16u * part, w);
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(qc_ready);
         uint32_t nd = 0;
-        for (uint32_t jt = 0;; ++jt) {
+        for (uint32_t jt = 0; ok; ++jt) {
             int4 e;
             if (!read_info(jt, e)) {
                 ok = false;
@@ -331,15 +385,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
             }
             if (e.x & 16) break;
             const int cls = e.x & 3;
-            const uint32_t sb = jt & 1u;
-            if (!mbar_wait(s_full + sb, (jt >> 1) & 1u, wc)) {
+            if (!mbar_wait(s_full, jt & 1u, wc)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             uint32_t v[64];
-            tmem_ld64(tS0 + 128u * sb + lane_base + 64u * h, v);
-            uint32_t wm[2] = {~0u, ~0u};
+            tmem_ld64(tS + lane_base + 64u * h, v);
+            tc_fence_before();
+            mbar_arrive(s_free);
+            float P[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) P[c] = ex2_approx(fmaf(__uint_as_float(v[c]), p.scale_log2, bias));
             if (cls == kPartial) {
                 const int kt_len = e.y & 0xffff, kt_split = e.y >> 16, kt_pos0 = e.z, kt_pos1 = e.w;
                 int lim1, lim2;
@@ -350,17 +407,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     lim1 = kt_split;
                     lim2 = kt_len;
                 }
+                uint32_t wm[2];
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
                     const int cb = 64 * h + 32 * ch;
                     wm[ch] = range_bits(0, lim1, cb) | range_bits(kt_split, lim2, cb);
                 }
-            }
-            float P[64];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float x = ex2_approx(fmaf(__uint_as_float(v[c]), p.scale_log2, -l2));
-                P[c] = ((wm[c >> 5] >> (c & 31)) & 1u) ? x : 0.f;
+                for (int c = 0; c < 64; ++c) P[c] = ((wm[c >> 5] >> (c & 31)) & 1u) ? P[c] : 0.f;
             }
             if (!mbar_wait(dp_full, jt & 1u, wc)) {
                 ok = false;
@@ -368,14 +422,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
             }
             tc_fence_after();
             tmem_ld64(tDP + lane_base + 64u * h, v);
+            tc_fence_before();
+            mbar_arrive(dp_free);
             uint32_t pk[32];
 #pragma unroll
             for (int c2 = 0; c2 < 32; ++c2)
-                pk[c2] = pack_bf16x2(P[2 * c2] * (__uint_as_float(v[2 * c2]) - Dm) * p.scale,
-                                     P[2 * c2 + 1] * (__uint_as_float(v[2 * c2 + 1]) - Dm) * p.scale);
-            tmem_st32(tDP + lane_base + 64u * h, pk);
+                pk[c2] = pack_bf16x2(P[2 * c2] * (__uint_as_float(v[2 * c2]) - Dm),
+                                     P[2 * c2 + 1] * (__uint_as_float(v[2 * c2 + 1]) - Dm));
+            // the dS buffer is free once dQ(jt - 1) has completed
+            if (jt > 0 && !mbar_wait(dq_done, (jt - 1) & 1u, wc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            tmem_st32(tDS + lane_base + 32u * h, pk);
             tc_fence_before();
-            mbar_arrive(ds_ready);
+            mbar_arrive(ds_ready + h);
             ++nd;
         }
         // ------------------------------------------------ epilogue
@@ -486,6 +548,7 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
     p.out_mode = a.out_mode;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.log2_scale = std::log2(a.scale);
     p.lse = a.lse;
     p.D = a.D;
     p.lse_T = a.lse_T;
