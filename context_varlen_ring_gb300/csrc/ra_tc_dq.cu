@@ -27,8 +27,8 @@
 // groups have loaded dP(j), and the only loop left between products is
 // dQ(j) -> (dS buffer free) -> store dS(j+1) -> dQ(j+1).  One thread issues
 // a tcgen05.mma only about every 45-60 cycles, close to the 64 cycles an
-// M=128 N=128 K=16 product runs, so two warps issue: warp 1 the S
-// products and warp 3 dP(j+1) then dQ(j).
+// M=128 N=128 K=16 product runs, so three warps issue: warp 1 the S
+// products, warp 2 dP and warp 3 dQ.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -110,11 +110,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
     uint64_t *qc_ready = bars + 20;    // Q copied into TMEM (256 arrivals)
     uint64_t *mma_done = bars + 21;    // all dQ products done
     uint64_t *a_done = bars + 22;      // S issuer drained
+    uint64_t *b_done = bars + 41;      // dP issuer drained
     uint64_t *info_full = bars + 23;   // [kRing]
     uint64_t *info_empty = bars + 31;  // [kRing]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 39);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 40);
-    int4 *ring = reinterpret_cast<int4 *>(bars + 42);  // [kRing]
+    int4 *ring = reinterpret_cast<int4 *>(bars + 42);  // [kRing] (bars 42-57)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -142,9 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
         mbar_init(qc_ready, 256);
         mbar_init(mma_done, 1);
         mbar_init(a_done, 1);
+        mbar_init(b_done, 1);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(info_full + i, 1);
-            mbar_init(info_empty + i, 2 + 256);
+            mbar_init(info_empty + i, 3 + 256);
         }
         fence_mbar_init();
     }
@@ -254,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 for (uint32_t x = (u > kSlots ? u - kSlots : 0); x < u; ++x)
                     (void)mbar_wait(kv_full + (x % kSlots), (x / kSlots) & 1u, drain);
             }
-        } else if (lane == 0 && warp != 2) {
-            // -------------------------------------------- MMA issuers (warps 1 and 3)
+        } else if (lane == 0) {
+            // -------------------------------------------- MMA issuers (warps 1-3)
             constexpr uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: A and B K-major
             constexpr uint32_t id_q = idesc_bf16_f32(128, 128, 0, 1);  // dQ: B MN-major
             // K-major SW128 operand: 16-element k-step ks at (ks / 4) * kHalf + (ks % 4) * 32
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 tc_fence_after();
                 return r;
             };
-            uint64_t *drain_bar = warp == 1 ? a_done : mma_done;
+            uint64_t *drain_bar = warp == 1 ? a_done : (warp == 2 ? b_done : mma_done);
             if (warp == 1) {
                 // S(j) = Q K(j)^T (Q from TMEM) once both groups have read S(j-1)
                 bool ok = wait(qc_ready, 0);
@@ -281,35 +283,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     for (int ks = 0; ks < 8; ++ks) tc_mma_ts(tS, tQ + 8u * ks, d0 + kstep(ks), id_s, ks > 0);
                     tc_commit(s_full);
                 }
-            } else {
-                // dP(j+1) = dO V(j+1)^T (dO from shared memory) once dP(j) was read,
-                // then dQ += dS(j) K(j)
+            } else if (warp == 2) {
+                // dP(j) = dO V(j)^T (dO from shared memory) once dP(j-1) was read
                 const uint64_t a0 = sdesc_sw128(base_s + kOffDO, 16, 1024);
-                auto mma_dp = [&](uint32_t vu) {
+                bool ok = wait(q_full, 0);
+                for (uint32_t j = 0; ok; ++j) {
+                    int4 e;
+                    if (!read_info(j, e) || (e.x & 16)) break;
+                    if (j > 0 && !wait(dp_free, (j - 1) & 1u)) break;
+                    const uint32_t vu = 2 * j + 1;
+                    if (!wait(kv_full + vu % kSlots, kv_par(vu))) break;
                     const uint64_t d0 = sdesc_sw128(base_s + slot_off(vu % kSlots), 16, 1024);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) tc_mma_ss(tDP, a0 + kstep(ks), d0 + kstep(ks), id_s, ks > 0);
                     tc_commit(dp_full);
                     tc_commit(kv_empty + vu % kSlots);  // V only feeds dP
-                };
-                int4 e;
-                bool have = wait(q_full, 0) && read_info(0, e) && !(e.x & 16);
-                if (have && wait(kv_full + 1, kv_par(1)))
-                    mma_dp(1);
-                else
-                    have = false;
-                for (uint32_t j = 0; have; ++j) {
-                    int4 en;
-                    if (!read_info(j + 1, en)) break;
-                    const bool have_next = !(en.x & 16);
-                    if (have_next) {
-                        const uint32_t vu = 2 * j + 3;
-                        if (!wait(dp_free, j & 1u)) break;
-                        if (!wait(kv_full + vu % kSlots, kv_par(vu))) break;
-                        mma_dp(vu);
-                    }
-                    // dQ += dS_h(j) K(j)_h: keys [64h, 64h + 64) = K rows (MN-major: d
-                    // contiguous), A = group h's dS at dS columns [32h, 32h + 32)
+                }
+            } else {
+                // dQ += dS_h(j) K(j)_h: keys [64h, 64h + 64) = K rows (MN-major: d
+                // contiguous), A = group h's dS at dS columns [32h, 32h + 32)
+                for (uint32_t j = 0;; ++j) {
+                    int4 e;
+                    if (!read_info(j, e) || (e.x & 16)) break;
                     const uint32_t kslot = (2 * j) % kSlots;
                     const uint64_t d0 = sdesc_sw128(base_s + slot_off(kslot), kHalf, 1024);
                     bool okh = true;
@@ -327,7 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     if (!okh) break;
                     tc_commit(dq_done);
                     tc_commit(kv_empty + kslot);  // K(j) done (S(j) finished before dS(j))
-                    if (!have_next) break;
                 }
             }
             tc_commit(drain_bar);
