@@ -277,5 +277,29 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Packed fp32 pair arithmetic (two lanes per instruction on sm_100-family
+// cores): d = a * b + c and d = (a - c) * b, element-wise on (x, y).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 sub_mul2(float2 a, float2 c, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rt;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rc, {%4, %5};\n\tmov.b64 rb, {%6, %7};\n\t"
+        "sub.rn.f32x2 rt, ra, rc;\n\t"
+        "mul.rn.f32x2 rt, rt, rb;\n\t"
+        "mov.b64 {%0, %1}, rt;\n\t}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(c.x), "f"(c.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 }  // namespace dev
 }  // namespace ra

@@ -390,7 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
             mbar_arrive(s_free);
             float P[64];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) P[c] = ex2_approx(fmaf(__uint_as_float(v[c]), p.scale_log2, bias));
+            for (int c = 0; c < 64; c += 2) {
+                const float2 x = fma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                      make_float2(p.scale_log2, p.scale_log2), make_float2(bias, bias));
+                P[c] = ex2_approx(x.x);
+                P[c + 1] = ex2_approx(x.y);
+            }
             if (cls == kPartial) {
                 const int kt_len = e.y & 0xffff, kt_split = e.y >> 16, kt_pos0 = e.z, kt_pos1 = e.w;
                 int lim1, lim2;
@@ -420,9 +425,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
             mbar_arrive(dp_free);
             uint32_t pk[32];
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2)
-                pk[c2] = pack_bf16x2(P[2 * c2] * (__uint_as_float(v[2 * c2]) - Dm),
-                                     P[2 * c2 + 1] * (__uint_as_float(v[2 * c2 + 1]) - Dm));
+            for (int c2 = 0; c2 < 32; ++c2) {
+                const float2 d = sub_mul2(make_float2(__uint_as_float(v[2 * c2]), __uint_as_float(v[2 * c2 + 1])),
+                                          make_float2(Dm, Dm), make_float2(P[2 * c2], P[2 * c2 + 1]));
+                pk[c2] = pack_bf16x2(d.x, d.y);
+            }
             // the dS buffer is free once dQ(jt - 1) has completed
             if (jt > 0 && !mbar_wait(dq_done, (jt - 1) & 1u, wc)) {
                 ok = false;
