@@ -639,7 +639,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         float *tld = reinterpret_cast<float *>(ws + L.tile_ld);
         {
             ProfScope ps("ra_tile_lse_d", s);
-            RA_CUDA(launch_tile_lse_d(tab + dt.o_qt, (int)plan->tiles.qtiles.size(), Hkv, G, lse, D, T, tld, s),
+            RA_CUDA(launch_tile_lse_d(tab + dt.o_qt, (int)plan->tiles.qtiles.size(), Hkv, G, lse, D, T, scale, tld, s),
                     "tile lse/D launch");
         }
         TcBwdArgs a{};

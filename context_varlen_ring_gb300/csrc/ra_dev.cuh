@@ -300,6 +300,18 @@ __device__ __forceinline__ float2 sub_mul2(float2 a, float2 c, float2 b) {
         : "f"(a.x), "f"(a.y), "f"(c.x), "f"(c.y), "f"(b.x), "f"(b.y));
     return d;
 }
+// d = (a * b + c) * m, element-wise on (x, y).
+__device__ __forceinline__ float2 fma_mul2(float2 a, float2 b, float2 c, float2 m) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rm, rt;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\tmov.b64 rm, {%8, %9};\n\t"
+        "fma.rn.f32x2 rt, ra, rb, rc;\n\t"
+        "mul.rn.f32x2 rt, rt, rm;\n\t"
+        "mov.b64 {%0, %1}, rt;\n\t}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y), "f"(m.x), "f"(m.y));
+    return d;
+}
 
 }  // namespace dev
 }  // namespace ra

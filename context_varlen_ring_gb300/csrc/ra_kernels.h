@@ -47,10 +47,11 @@ cudaError_t launch_merge(int n, const float *const *outs, const float *const *ls
 // D[h, t] = sum_c a[t, h, c] * b[t, h, c]   (a, b of dtype; fp32 result)
 cudaError_t launch_rowdot(const void *a, const void *b, int dtype, int64_t T, int H, int d, float *D,
                           cudaStream_t st);
-// Per (query tile, KV head): 128 columns of lse*log2(e) then 128 of D,
-// contiguous (1 KB per tile and head), for the backward's bulk copies.
+// Per (query tile, KV head): 128 columns of -lse*log2(e) (-inf for empty
+// rows) then 128 of -D*scale, contiguous (1 KB per tile and head), for the
+// key-side backward's bulk copies.
 cudaError_t launch_tile_lse_d(const void *qtiles, int n_qtiles, int Hkv, int G, const float *lse, const float *D,
-                              int64_t lse_T, float *out, cudaStream_t st);
+                              int64_t lse_T, float scale, float *out, cudaStream_t st);
 // dst (dtype) = src (fp32), n elements.
 cudaError_t launch_cast_f32(const float *src, void *dst, int dtype, int64_t n, cudaStream_t st);
 

@@ -249,7 +249,7 @@ cudaError_t launch_rowdot(const void *a, const void *b, int dtype, int64_t T, in
 // (0 where no token), stored contiguously: out[((tile * Hkv + g) * 2 + w) * 128 + c].
 __global__ void tile_lse_d_kernel(const int4 *__restrict__ qtiles, int n_qtiles, int Hkv, int G, int log2G,
                                   const float *__restrict__ lse, const float *__restrict__ D, long long lse_T,
-                                  float *__restrict__ out) {
+                                  float scale, float *__restrict__ out) {
     const long long total = (long long)n_qtiles * Hkv * 128;
     for (long long w = (long long)blockIdx.x * blockDim.x + threadIdx.x; w < total;
          w += (long long)gridDim.x * blockDim.x) {
@@ -260,27 +260,27 @@ __global__ void tile_lse_d_kernel(const int4 *__restrict__ qtiles, int n_qtiles,
         const int4 a = __ldg(qtiles + 2 * qt);
         const int pos1 = __ldg(&qtiles[2 * qt + 1].x);
         const int tok = c >> log2G, head = g * G + (c & (G - 1));
-        float l2 = INFINITY, dd = 0.f;
+        float nl2 = -INFINITY, nds = 0.f;
         if (tok < a.y) {
             const int pos = tok < a.z ? a.w + tok : pos1 + (tok - a.z);
             const float l = lse[(long long)head * lse_T + pos];
-            l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
-            dd = D[(long long)head * lse_T + pos];
+            nl2 = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+            nds = -D[(long long)head * lse_T + pos] * scale;
         }
-        out[(tg * 2 + 0) * 128 + c] = l2;
-        out[(tg * 2 + 1) * 128 + c] = dd;
+        out[(tg * 2 + 0) * 128 + c] = nl2;
+        out[(tg * 2 + 1) * 128 + c] = nds;
     }
 }
 
 cudaError_t launch_tile_lse_d(const void *qtiles, int n_qtiles, int Hkv, int G, const float *lse, const float *D,
-                              int64_t lse_T, float *out, cudaStream_t st) {
+                              int64_t lse_T, float scale, float *out, cudaStream_t st) {
     if (n_qtiles <= 0) return cudaSuccess;
     int lg = 0;
     while ((1 << lg) < G) ++lg;
     const long long total = (long long)n_qtiles * Hkv * 128;
     const int blocks = (int)std::min<long long>((total + 255) / 256, (long long)num_sms() * 8);
     tile_lse_d_kernel<<<blocks, 256, 0, st>>>(static_cast<const int4 *>(qtiles), n_qtiles, Hkv, G, lg, lse, D, lse_T,
-                                              out);
+                                              scale, out);
     return cudaGetLastError();
 }
 

@@ -17,10 +17,16 @@
 //    memory.  Visited query tiles (128 rows = 128/G tokens x G heads) and
 //    their dO tiles stream through two TMA stages together with the tile's
 //    128 LSE and D values (pre-gathered per tile, one bulk copy).
-//  * Per tile the MMA thread issues S^T = K Q^T and dP^T = V dO^T (SS), then
-//    dV += P^T dO and dK += dS^T Q as TS-MMAs with P^T and dS^T read from
-//    TMEM, so shared memory only streams Q and dO (the SS products at
-//    N = 128 already use most of the shared-memory read port).
+//  * Per tile S^T = K Q^T and dP^T = V dO^T are SS-MMAs, dV += P^T dO and
+//    dK += dS^T Q are TS-MMAs with P^T and dS^T read from TMEM, so shared
+//    memory only streams Q and dO (the SS products at N = 128 already use
+//    most of the shared-memory read port).
+//  * One thread issues a tcgen05.mma only about every 45-60 cycles, close to
+//    the 64 cycles one M=128 N=128 K=16 product runs, so two warps issue,
+//    one per TMEM reuse chain: warp 1 dV(i) then S^T(i+1) (which overwrites
+//    P^T(i)), warp 3 dK(i) then dP^T(i+1) (which overwrites dS^T(i)).  Each
+//    chain is ordered by the tensor pipe's in-order execution of one
+//    thread's products, and the two chains overlap.
 //  * TMEM: dK [0,128), dV [128,256), S^T then P^T [256,384), dP^T then dS^T
 //    [384,512).  Two compute warpgroups split the 128 query columns; each
 //    packs its P^T / dS^T (bf16) over the first 32 of its own 64 columns.
@@ -140,13 +146,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
         mbar_init(kv_full, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(st_full + i, 1);
-            mbar_init(st_empty + i, 1);
+            mbar_init(st_empty + i, 2);  // one commit from each issuer
         }
         mbar_init(s_full, 1);
         mbar_init(dp_full, 1);
         mbar_init(p_ready, 256);
         mbar_init(ds_ready, 256);
-        mbar_init(mma_done, 1);
+        mbar_init(mma_done, 2);  // one commit from each issuer
         fence_mbar_init();
     }
     if (warp == 2) {
@@ -240,56 +246,48 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             for (uint32_t x = (n > 2 ? n - 2 : 0); x < n; ++x)
                 (void)mbar_wait(st_full + (x & 1u), (x >> 1) & 1u, drain);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);   // A, B K-major
-            const uint32_t id_ts = idesc_bf16_f32(128, 128, 0, 1);   // A in TMEM, B MN-major
-            const uint32_t ks_ = base_s + kOffK, vs_ = base_s + kOffV;
-            auto is_end = [&](uint32_t st) {
-                return (reinterpret_cast<const int4 *>(info(st) + 1024)[1].y & 1) != 0;
-            };
-            bool ok = mbar_wait(kv_full, 0, wc) && mbar_wait(st_full + 0, 0, wc);
-            tc_fence_after();
-            bool have = ok && !is_end(0);
-            uint32_t i = 0;
-            if (have) {
-                mma_kk(tS, ks_, base_s + kOffQ, id_kk);
-                tc_commit(s_full);
-                mma_kk(tDP, vs_, base_s + kOffDO, id_kk);
-                tc_commit(dp_full);
-            }
-            while (ok && have) {
-                const uint32_t st = i & 1u, nst = (i + 1) & 1u;
-                const uint32_t qs = base_s + kOffQ + st * kTile, dos = base_s + kOffDO + st * kTile;
-                // dV += P^T dO
-                if (!mbar_wait(p_ready, i & 1u, wc)) break;
-                tc_fence_after();
-                mma_ts(tDV, tS, dos, id_ts, i > 0);
-                // next tile's S^T (the dV above reads P^T first: in order)
-                if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
-                tc_fence_after();
-                const bool have_next = !is_end(nst);
-                if (have_next) {
-                    mma_kk(tS, ks_, base_s + kOffQ + nst * kTile, id_kk);
-                    tc_commit(s_full);
-                }
-                // dK += dS^T Q
-                if (!mbar_wait(ds_ready, i & 1u, wc)) break;
-                tc_fence_after();
-                mma_ts(tDK, tDP, qs, id_ts, i > 0);
-                tc_commit(st_empty + st);  // Q and dO of this stage are no longer read
-                if (!have_next) break;
-                // next tile's dP^T (the dK above reads dS^T first: in order)
-                mma_kk(tDP, vs_, base_s + kOffDO + nst * kTile, id_kk);
-                tc_commit(dp_full);
-                ++i;
-            }
-            tc_commit(mma_done);
-            volatile int local_abort = 0;
-            const WaitCtl drain{&local_abort, p.status, p.budget_ns};
-            (void)mbar_wait(mma_done, 0, drain);
+    } else if ((warp == 1 || warp == 3) && lane == 0) {
+        // ------------------------------------------------ MMA issuers
+        const uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);   // A, B K-major
+        const uint32_t id_ts = idesc_bf16_f32(128, 128, 0, 1);   // A in TMEM, B MN-major
+        const uint32_t ks_ = base_s + kOffK, vs_ = base_s + kOffV;
+        auto is_end = [&](uint32_t st) {
+            return (reinterpret_cast<const int4 *>(info(st) + 1024)[1].y & 1) != 0;
+        };
+        // warp 1: S^T(0); dV(i), S^T(i+1).  warp 3: dP^T(0); dK(i), dP^T(i+1).
+        const bool pchain = warp == 1;
+        const uint32_t chain_d = pchain ? tS : tDP;          // S^T / dP^T accumulator
+        const uint32_t chain_a = pchain ? ks_ : vs_;         // K / V
+        const uint32_t chain_b = pchain ? kOffQ : kOffDO;    // Q / dO stage
+        const uint32_t grad_d = pchain ? tDV : tDK;          // dV / dK
+        const uint32_t grad_b = pchain ? kOffDO : kOffQ;     // dO / Q stage
+        uint64_t *chain_full = pchain ? s_full : dp_full;
+        uint64_t *ready = pchain ? p_ready : ds_ready;
+        bool ok = mbar_wait(kv_full, 0, wc) && mbar_wait(st_full + 0, 0, wc);
+        tc_fence_after();
+        bool have = ok && !is_end(0);
+        if (have) {
+            mma_kk(chain_d, chain_a, base_s + chain_b, id_kk);
+            tc_commit(chain_full);
         }
+        for (uint32_t i = 0; ok && have; ++i) {
+            const uint32_t st = i & 1u, nst = (i + 1) & 1u;
+            // dV += P^T dO  /  dK += dS^T Q
+            if (!mbar_wait(ready, i & 1u, wc)) break;
+            tc_fence_after();
+            mma_ts(grad_d, chain_d, base_s + grad_b + st * kTile, id_ts, i > 0);
+            tc_commit(st_empty + st);  // this issuer no longer reads the stage
+            // next tile's S^T / dP^T (the product above reads P^T / dS^T first: in order)
+            if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
+            tc_fence_after();
+            if (is_end(nst)) break;
+            mma_kk(chain_d, chain_a, base_s + chain_b + nst * kTile, id_kk);
+            tc_commit(chain_full);
+        }
+        tc_commit(mma_done);
+        volatile int local_abort = 0;
+        const WaitCtl drain{&local_abort, p.status, p.budget_ns};
+        (void)mbar_wait(mma_done, 0, drain);
     } else if (warp >= 4) {
         // ------------------------------------------------ compute warpgroups
         // Group h (warps 4-7: 0, warps 8-11: 1) owns columns [64h, 64h+64) of
@@ -342,18 +340,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                     wm[ch] = range_bits(a1 * G, e1 * G, cb) | range_bits(a2 * G, e2 * G, cb);
                 }
             }
+            // per query column: -lse * log2(e) at [0, 128), -D * scale at [128, 256)
             const float4 *l4 = reinterpret_cast<const float4 *>(I) + 16 * h;
+            const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
             float P[64];
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
                 const float4 l = l4[c4];
-                const float lv[4] = {l.x, l.y, l.z, l.w};
+                const int c = 4 * c4;
+                const float2 x0 = fma2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), sl2,
+                                       make_float2(l.x, l.y));
+                const float2 x1 = fma2(make_float2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), sl2,
+                                       make_float2(l.z, l.w));
+                P[c] = ex2_approx(x0.x);
+                P[c + 1] = ex2_approx(x0.y);
+                P[c + 2] = ex2_approx(x1.x);
+                P[c + 3] = ex2_approx(x1.y);
+            }
+            if (cls == kPartial) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int c = 4 * c4 + e;
-                    const float x = ex2_approx(fmaf(__uint_as_float(v[c]), p.scale_log2, -lv[e]));
-                    P[c] = ((wm[c >> 5] >> (c & 31)) & 1u) ? x : 0.f;
-                }
+                for (int c = 0; c < 64; ++c) P[c] = ((wm[c >> 5] >> (c & 31)) & 1u) ? P[c] : 0.f;
             }
             {
                 uint32_t pk[32];
@@ -363,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             }
             tc_fence_before();
             mbar_arrive(p_ready);
-            // ---- dS^T = P^T o (dP^T - D) * scale, bf16 over this group's dP^T columns
+            // ---- dS^T = (dP^T * scale - D * scale) o P^T, bf16 over this group's dP^T columns
             if (!mbar_wait(dp_full, i & 1u, wc)) {
                 ok = false;
                 break;
@@ -371,15 +377,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             tc_fence_after();
             tmem_ld64(tDP + lane_base + 64u * h, v);
             const float4 *d4 = reinterpret_cast<const float4 *>(I + 512) + 16 * h;
+            const float2 sc2 = make_float2(p.scale, p.scale);
             uint32_t pk[32];
 #pragma unroll
             for (int c4 = 0; c4 < 16; ++c4) {
                 const float4 dd = d4[c4];
                 const int c = 4 * c4;
-                pk[2 * c4] = pack_bf16x2(P[c] * (__uint_as_float(v[c]) - dd.x) * p.scale,
-                                         P[c + 1] * (__uint_as_float(v[c + 1]) - dd.y) * p.scale);
-                pk[2 * c4 + 1] = pack_bf16x2(P[c + 2] * (__uint_as_float(v[c + 2]) - dd.z) * p.scale,
-                                             P[c + 3] * (__uint_as_float(v[c + 3]) - dd.w) * p.scale);
+                const float2 s0 = fma_mul2(make_float2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), sc2,
+                                           make_float2(dd.x, dd.y), make_float2(P[c], P[c + 1]));
+                const float2 s1 = fma_mul2(make_float2(__uint_as_float(v[c + 2]), __uint_as_float(v[c + 3])), sc2,
+                                           make_float2(dd.z, dd.w), make_float2(P[c + 2], P[c + 3]));
+                pk[2 * c4] = pack_bf16x2(s0.x, s0.y);
+                pk[2 * c4 + 1] = pack_bf16x2(s1.x, s1.y);
             }
             tmem_st32(tDP + lane_base + 64u * h, pk);
             tc_fence_before();
