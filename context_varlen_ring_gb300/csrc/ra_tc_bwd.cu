@@ -21,12 +21,17 @@
 //    dK += dS^T Q are TS-MMAs with P^T and dS^T read from TMEM, so shared
 //    memory only streams Q and dO (the SS products at N = 128 already use
 //    most of the shared-memory read port).
-//  * One thread issues a tcgen05.mma only about every 45-60 cycles, close to
-//    the 64 cycles one M=128 N=128 K=16 product runs, so two warps issue,
-//    one per TMEM reuse chain: warp 1 dV(i) then S^T(i+1) (which overwrites
-//    P^T(i)), warp 3 dK(i) then dP^T(i+1) (which overwrites dS^T(i)).  Each
-//    chain is ordered by the tensor pipe's in-order execution of one
-//    thread's products, and the two chains overlap.
+//  * Each query tile is processed as two 64-column halves h (query rows
+//    [64h, 64h+64)), and compute group h owns half h: S^T_h, dP^T_h are
+//    N=64 products into that group's TMEM columns, and dV, dK take the
+//    matching 64-row slice of the contraction.  A group's chain
+//    S^T_h(i) -> P^T_h(i) -> dV_h(i) -> S^T_h(i+1) thus holds half a tile
+//    of products, and the two groups' chains interleave.
+//  * One thread issues a tcgen05.mma only about every 45-60 cycles, so two
+//    warps issue, one per TMEM reuse chain: warp 1 dV_h(i) then S^T_h(i+1)
+//    (which overwrites P^T_h(i)), warp 3 dK_h(i) then dP^T_h(i+1) (which
+//    overwrites dS^T_h(i)); each chain is ordered by the tensor pipe's
+//    in-order execution of one thread's products.
 //  * TMEM: dK [0,128), dV [128,256), S^T then P^T [256,384), dP^T then dS^T
 //    [384,512).  Two compute warpgroups split the 128 query columns; each
 //    packs its P^T / dS^T (bf16) over the first 32 of its own 64 columns.
@@ -61,7 +66,7 @@ constexpr uint32_t kOffDO = 4 * kTile;            // [2] stages
 constexpr uint32_t kOffInfo = 6 * kTile;          // [2] x {lse[128], D[128], descriptor}
 constexpr uint32_t kInfoBytes = 1024 + 64;
 constexpr uint32_t kOffBar = kOffInfo + 2 * kInfoBytes;
-constexpr uint32_t kSmemBytes = kOffBar + 128;    // base must be 1024-aligned (checked)
+constexpr uint32_t kSmemBytes = kOffBar + 128;    // 16 barrier words; base must be 1024-aligned (checked)
 
 struct BwdParams {
     CUtensorMap tmQ, tmK, tmV, tmDO;
@@ -92,25 +97,6 @@ __device__ __forceinline__ uint32_t range_bits(int a, int b, int base) {
     return (uint32_t)(((1ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
 }
 
-// D[tmem] = A B^T, both K-major (d contiguous) in shared memory.
-__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_s, uint32_t b_s, uint32_t idesc) {
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-        tc_mma_ss(d_tmem, sdesc_sw128(a_s + off, 16, 1024), sdesc_sw128(b_s + off, 16, 1024), idesc, ks > 0);
-    }
-}
-
-// D[tmem] (+)= A[tmem] B: A = 128 x 128 bf16 packed by the two compute
-// groups at TMEM columns [0,32) and [64,96); B (128 rows x 128) read
-// MN-major from shared memory.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_s, uint32_t idesc, bool acc) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        tc_mma_ts(d_tmem, a_tmem + 8u * k + (k >= 4 ? 32u : 0u), sdesc_sw128(b_s + k * 2048u, kHalf, 1024), idesc,
-                  (acc || k > 0) ? 1u : 0u);
-}
-
 __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base_s = smem_u32(smem);
@@ -122,13 +108,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
     uint64_t *kv_full = bars + 0;
     uint64_t *st_full = bars + 1;    // [2] Q, dO, lse, D of a stage (TMA + bulk copies)
     uint64_t *st_empty = bars + 3;   // [2]
-    uint64_t *s_full = bars + 5;     // S^T done
-    uint64_t *dp_full = bars + 6;    // dP^T done
-    uint64_t *p_ready = bars + 7;    // P^T in TMEM (256 arrivals)
-    uint64_t *ds_ready = bars + 8;   // dS^T in TMEM (256 arrivals)
-    uint64_t *mma_done = bars + 9;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 10);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 11);
+    uint64_t *s_full = bars + 5;     // [2] S^T half h done
+    uint64_t *dp_full = bars + 7;    // [2] dP^T half h done
+    uint64_t *p_ready = bars + 9;    // [2] P^T half h in TMEM (128 arrivals)
+    uint64_t *ds_ready = bars + 11;  // [2] dS^T half h in TMEM (128 arrivals)
+    uint64_t *mma_done = bars + 13;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 14);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 15);
     auto info = [&](uint32_t st) -> uint8_t * { return smem + kOffInfo + st * kInfoBytes; };
 
     const int warp = threadIdx.x >> 5;
@@ -148,10 +134,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             mbar_init(st_full + i, 1);
             mbar_init(st_empty + i, 2);  // one commit from each issuer
         }
-        mbar_init(s_full, 1);
-        mbar_init(dp_full, 1);
-        mbar_init(p_ready, 256);
-        mbar_init(ds_ready, 256);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(s_full + h, 1);
+            mbar_init(dp_full + h, 1);
+            mbar_init(p_ready + h, 128);
+            mbar_init(ds_ready + h, 128);
+        }
         mbar_init(mma_done, 2);  // one commit from each issuer
         fence_mbar_init();
     }
@@ -248,41 +236,60 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
         }
     } else if ((warp == 1 || warp == 3) && lane == 0) {
         // ------------------------------------------------ MMA issuers
-        const uint32_t id_kk = idesc_bf16_f32(128, 128, 0, 0);   // A, B K-major
-        const uint32_t id_ts = idesc_bf16_f32(128, 128, 0, 1);   // A in TMEM, B MN-major
-        const uint32_t ks_ = base_s + kOffK, vs_ = base_s + kOffV;
+        const uint32_t id_n64 = idesc_bf16_f32(128, 64, 0, 0);  // A, B K-major, N = 64 queries
+        const uint32_t id_ts = idesc_bf16_f32(128, 128, 0, 1);  // A in TMEM, B MN-major
         auto is_end = [&](uint32_t st) {
             return (reinterpret_cast<const int4 *>(info(st) + 1024)[1].y & 1) != 0;
         };
-        // warp 1: S^T(0); dV(i), S^T(i+1).  warp 3: dP^T(0); dK(i), dP^T(i+1).
+        auto kstep = [](int ks) -> uint32_t { return (((ks >> 2) * kHalf + (ks & 3) * 32u) >> 4); };
+        // warp 1: S^T_h and dV; warp 3: dP^T_h and dK
         const bool pchain = warp == 1;
-        const uint32_t chain_d = pchain ? tS : tDP;          // S^T / dP^T accumulator
-        const uint32_t chain_a = pchain ? ks_ : vs_;         // K / V
-        const uint32_t chain_b = pchain ? kOffQ : kOffDO;    // Q / dO stage
-        const uint32_t grad_d = pchain ? tDV : tDK;          // dV / dK
-        const uint32_t grad_b = pchain ? kOffDO : kOffQ;     // dO / Q stage
+        const uint32_t chain_d = pchain ? tS : tDP;                          // S^T / dP^T
+        const uint64_t chain_a = sdesc_sw128(base_s + (pchain ? kOffK : kOffV), 16, 1024);
+        const uint32_t chain_b = base_s + (pchain ? kOffQ : kOffDO);        // Q / dO stages
+        const uint32_t grad_d = pchain ? tDV : tDK;                          // dV / dK
+        const uint32_t grad_b = base_s + (pchain ? kOffDO : kOffQ);         // dO / Q stages
         uint64_t *chain_full = pchain ? s_full : dp_full;
         uint64_t *ready = pchain ? p_ready : ds_ready;
+        // S^T_h / dP^T_h of stage st: 128 keys x query rows [64h, 64h+64)
+        auto chain_mma = [&](int h, uint32_t st) {
+            const uint64_t b0 = sdesc_sw128(chain_b + st * kTile + 8192u * h, 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc_mma_ss(chain_d + 64u * h, chain_a + kstep(ks), b0 + kstep(ks), id_n64, ks > 0);
+            tc_commit(chain_full + h);
+        };
+        // dV / dK += P^T_h / dS^T_h (TMEM, group h's columns) x rows [64h, 64h+64)
+        // of dO / Q (MN-major: d contiguous)
+        auto grad_mma = [&](int h, uint32_t st, bool acc) {
+            const uint64_t b0 = sdesc_sw128(grad_b + st * kTile + 8192u * h, kHalf, 1024);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                tc_mma_ts(grad_d, chain_d + 64u * h + 8u * k, b0 + ((2048u * k) >> 4), id_ts, (acc || k > 0));
+        };
         bool ok = mbar_wait(kv_full, 0, wc) && mbar_wait(st_full + 0, 0, wc);
         tc_fence_after();
-        bool have = ok && !is_end(0);
+        const bool have = ok && !is_end(0);
         if (have) {
-            mma_kk(chain_d, chain_a, base_s + chain_b, id_kk);
-            tc_commit(chain_full);
+            chain_mma(0, 0);
+            chain_mma(1, 0);
         }
         for (uint32_t i = 0; ok && have; ++i) {
             const uint32_t st = i & 1u, nst = (i + 1) & 1u;
-            // dV += P^T dO  /  dK += dS^T Q
-            if (!mbar_wait(ready, i & 1u, wc)) break;
+            if (!mbar_wait(ready + 0, i & 1u, wc)) break;
             tc_fence_after();
-            mma_ts(grad_d, chain_d, base_s + grad_b + st * kTile, id_ts, i > 0);
-            tc_commit(st_empty + st);  // this issuer no longer reads the stage
-            // next tile's S^T / dP^T (the product above reads P^T / dS^T first: in order)
+            grad_mma(0, st, i > 0);
             if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
             tc_fence_after();
-            if (is_end(nst)) break;
-            mma_kk(chain_d, chain_a, base_s + chain_b + nst * kTile, id_kk);
-            tc_commit(chain_full);
+            const bool next_end = is_end(nst);
+            // half 0 of the next tile overwrites P^T_0 / dS^T_0 after the product above (in order)
+            if (!next_end) chain_mma(0, nst);
+            if (!mbar_wait(ready + 1, i & 1u, wc)) break;
+            tc_fence_after();
+            grad_mma(1, st, true);
+            tc_commit(st_empty + st);  // this issuer no longer reads the stage
+            if (next_end) break;
+            chain_mma(1, nst);
         }
         tc_commit(mma_done);
         volatile int local_abort = 0;
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             if (d1.y & 1) break;
             const int cls = d1.y >> 1;
             // ---- P^T = exp2(S^T * scale * log2e - lse * log2e), masked
-            if (!mbar_wait(s_full, i & 1u, wc)) {
+            if (!mbar_wait(s_full + h, i & 1u, wc)) {
                 ok = false;
                 break;
             }
@@ -368,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                 tmem_st32(tS + lane_base + 64u * h, pk);
             }
             tc_fence_before();
-            mbar_arrive(p_ready);
+            mbar_arrive(p_ready + h);
             // ---- dS^T = (dP^T * scale - D * scale) o P^T, bf16 over this group's dP^T columns
-            if (!mbar_wait(dp_full, i & 1u, wc)) {
+            if (!mbar_wait(dp_full + h, i & 1u, wc)) {
                 ok = false;
                 break;
             }
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             }
             tmem_st32(tDP + lane_base + 64u * h, pk);
             tc_fence_before();
-            mbar_arrive(ds_ready);
+            mbar_arrive(ds_ready + h);
             ++nt;
         }
         // ---------------------------------------------- epilogue: dK, dV rows
