@@ -300,6 +300,23 @@ __device__ __forceinline__ float2 sub_mul2(float2 a, float2 c, float2 b) {
         : "f"(a.x), "f"(a.y), "f"(c.x), "f"(c.y), "f"(b.x), "f"(b.y));
     return d;
 }
+// Three-input maximum (one instruction on sm_100-family cores).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// d = a + b, element-wise on (x, y).
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
 // d = (a * b + c) * m, element-wise on (x, y).
 __device__ __forceinline__ float2 fma_mul2(float2 a, float2 b, float2 c, float2 m) {
     float2 d;

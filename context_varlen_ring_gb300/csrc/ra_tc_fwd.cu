@@ -437,14 +437,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         for (int i = 0; i < 32; ++i) s[32 * ch + i] = ((w >> i) & 1u) ? s[32 * ch + i] : -INFINITY;
                     }
                 }
-                // row max as 8 independent chains, then a tree
+                // row max as 8 independent chains of three-input maxima, then a tree
                 float mx8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = s[i];
 #pragma unroll
-                for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int c = 8; c < 128; c += 16) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mx8[i] = max3f(mx8[i], s[c + i], s[c + 8 + i]);
+                }
+                const float mx = max3f(max3f(mx8[0], mx8[1], mx8[2]), max3f(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
                 const float m_new = fmaxf(m_run, mx * p.scale_log2);
                 const bool need = m_new > m_run + 8.0f;
                 float alpha = 1.f;
@@ -454,16 +456,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     l_run *= alpha;
                 }
                 const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-                float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                  make_float2(0.f, 0.f)};
+                const float2 sl2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m_use, -m_use);
                 uint32_t pk[64];
 #pragma unroll
                 for (int c2 = 0; c2 < 64; ++c2) {
-                    const float a0 = ex2_approx(fmaf(s[2 * c2], p.scale_log2, -m_use));
-                    const float a1 = ex2_approx(fmaf(s[2 * c2 + 1], p.scale_log2, -m_use));
-                    sum8[c2 & 7] += a0 + a1;
-                    pk[c2] = pack_bf16x2(a0, a1);
+                    const float2 x = fma2(make_float2(s[2 * c2], s[2 * c2 + 1]), sl2, nm2);
+                    const float2 e2 = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                    sum4[c2 & 3] = add2(sum4[c2 & 3], e2);
+                    pk[c2] = pack_bf16x2(e2.x, e2.y);
                 }
-                l_run += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+                const float2 sum2 = add2(add2(sum4[0], sum4[1]), add2(sum4[2], sum4[3]));
+                l_run += sum2.x + sum2.y;
                 // P (bf16) replaces the first 64 columns of this row's S in
                 // TMEM; S of this tile completing implies the previous PV of
                 // this query tile (which read the old P) is done.
