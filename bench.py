@@ -160,6 +160,28 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def kernel_traffic(name):
+    """DRAM bytes per launch of `name` from the committed ncu summary, or None
+    when there is none or the kernel's source changed since it was captured."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            tab = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = tab.get(name)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "context_varlen_ring_gb300", "csrc", ent["source"])
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return ent["dram_bytes_per_launch"] if digest == ent["source_sha256"] else None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -288,15 +310,31 @@ def main():
     roof = None
     if dominant:
         per_launch_s = kernels[dominant]["ms_per_launch"] / 1e3
-        if dominant.startswith("ra_tc_fwd") or dominant.startswith("ra_simt_fwd"):
-            flops = fwd_flops
+        # algorithmic work of what each kernel computes, per launch (fused schedule:
+        # one launch covers all ring steps): 2*d FLOPs per (query head, allowed pair)
+        # for each product it forms
+        products = {"ra_tc_fwd": 2, "ra_simt_fwd": 2,            # S, PV
+                    "ra_tc_bwd_dkdv": 4,                         # S^T, dP^T, dV, dK
+                    "ra_tc_bwd_dq": 3,                           # S, dP, dQ
+                    "ra_simt_bwd": 5}
+        n_prod = products.get(dominant)
+        if n_prod is not None:
+            flops = n_prod * 2 * d * hq * pairs
+            ach = flops / per_launch_s / 1e12
+            roof = {"kernel": dominant, "bound": "tensor", "achieved": ach, "peak": peak_sust, "unit": "TFLOP/s",
+                    "frac": ach / peak_sust, "traffic": kernel_traffic(dominant),
+                    "peak_kind": f"{peak_src} bf16 sustained (kernel timed inside a multi-step loop)",
+                    "algorithmic_per_launch": flops, "algorithmic_unit": "FLOP",
+                    "algorithmic_rule": f"{n_prod} products x 2*d FLOPs per (query head, allowed pair)"}
         else:
-            flops = bwd_flops
-        ach = flops / per_launch_s / 1e12
-        roof = {"kernel": dominant, "bound": "tensor", "achieved": ach, "peak": peak_sust, "unit": "TFLOP/s",
-                "frac": ach / peak_sust, "traffic": None,
-                "peak_kind": f"{peak_src} bf16 sustained (kernel timed inside a multi-step loop)",
-                "algorithmic_per_launch": flops}
+            roof = {"kernel": dominant, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s",
+                    "frac": None, "traffic": kernel_traffic(dominant)}
+    all_roof = {}
+    for nm, x in kernels.items():
+        n_prod = {"ra_tc_fwd": 2, "ra_tc_bwd_dkdv": 4, "ra_tc_bwd_dq": 3}.get(nm)
+        if n_prod:
+            tf = n_prod * 2 * d * hq * pairs / (x["ms_per_launch"] / 1e3) / 1e12
+            all_roof[nm] = {"tflops": tf, "frac_of_sustained": tf / peak_sust}
 
     # ---- end to end through the public API with host buffers
     hq_, hk_, hv_, hd_ = (x.cpu().pin_memory() for x in (q, k, v, do))
@@ -360,6 +398,7 @@ def main():
         "fwd_bwd_frac_of_peak": value / world / peak_burst,
         "peak_tflops": {"burst": peak_burst, "sustained": peak_sust, "source": peak_src},
         "roofline": roof,
+        "kernel_rooflines": all_roof,
         "kernels": kernels,
         "gpu_launches": gpu_launches,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
