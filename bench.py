@@ -160,6 +160,24 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's `x` (each rank's own timing); x itself when
+    world == 1.  Collective on the default process group."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_step, steps, max_ms):
+    """Whole-job throughput: every rank runs `steps` steps of `flops_per_step`
+    (replicas, weak scaling) within the slowest rank's `max_ms`."""
+    return world * flops_per_step * steps / (max_ms / 1e3) / 1e12
+
+
 def kernel_traffic(name):
     """DRAM bytes per launch of `name` from the committed ncu summary, or None
     when there is none or the kernel's source changed since it was captured."""
@@ -267,13 +285,9 @@ def main():
     e1.record(stream)
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = ms / args.steps
-    value = world * step_flops * args.steps / (ms / 1e3) / 1e12
+    value = job_tflops(world, step_flops, args.steps, ms)
 
     # ---- forward alone (same data), for the forward half of the metric
     barrier()
@@ -366,12 +380,8 @@ def main():
         e2e_step()
     g1.record(stream)
     barrier()
-    e2e_ms = g0.elapsed_time(g1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * step_flops * args.steps / (e2e_ms / 1e3) / 1e12
+    e2e_ms = max_over_ranks(g0.elapsed_time(g1), world, dev)
+    e2e_value = job_tflops(world, step_flops, args.steps, e2e_ms)
     assert ra.device_status() == 0
 
     if rank != 0:

@@ -758,14 +758,13 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
             }
         }
     }
-    // a9: cast to the gradient dtype (rows are already in original order)
-    {
+    // a9: cast to the gradient dtype (rows are already in original order); the
+    // fused tensor-core passes write the gradient dtype directly
+    if (!fused_tc) {
         ProfScope ps("ra_cast", s);
-        if (!fused_tc) RA_CUDA(launch_cast_f32(dqa, dq, grad_dtype, T * Hq * d, s), "cast dq");
-        if (!fused_tc) {
-            RA_CUDA(launch_cast_f32(dka, dk, grad_dtype, T * Hkv * d, s), "cast dk");
-            RA_CUDA(launch_cast_f32(dva, dv, grad_dtype, T * Hkv * d, s), "cast dv");
-        }
+        RA_CUDA(launch_cast_f32(dqa, dq, grad_dtype, T * Hq * d, s), "cast dq");
+        RA_CUDA(launch_cast_f32(dka, dk, grad_dtype, T * Hkv * d, s), "cast dk");
+        RA_CUDA(launch_cast_f32(dva, dv, grad_dtype, T * Hkv * d, s), "cast dv");
     }
     return RA_OK;
 }

@@ -1,0 +1,49 @@
+"""Multi-rank host logic of bench.py on CPU: two gloo ranks, each with its own
+timing, agree on the slowest rank's time and report whole-job throughput of
+the replicas (every rank runs the full workload)."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = 100.0 + 25.0 * rank          # rank 1 is the slow one
+        m = bench.max_over_ranks(ms, world, torch.device("cpu"))
+        out[rank] = m
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
+    assert out[0] == out[1] == 125.0
+
+
+def test_single_rank_passthrough():
+    assert bench.max_over_ranks(3.5, 1, torch.device("cpu")) == 3.5
+
+
+def test_job_tflops_is_whole_job():
+    # 2 replicas x 10 steps x 1e12 FLOP in 1 s (slowest rank) = 20 TFLOP/s
+    assert bench.job_tflops(2, 1e12, 10, 1000.0) == pytest.approx(20.0)
+    assert bench.job_tflops(1, 1e12, 10, 1000.0) == pytest.approx(10.0)
