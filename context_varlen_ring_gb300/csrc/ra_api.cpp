@@ -98,6 +98,32 @@ struct Carver {
 
 using namespace ra;
 
+namespace ra {
+
+RingPlan::~RingPlan() {
+    if (pinned) {
+        // an upload from this buffer may still be queued on some stream
+        (void)cudaDeviceSynchronize();
+        (void)cudaFreeHost(pinned);
+    }
+}
+
+const void *plan_upload_src(RingPlan &plan) {
+    std::lock_guard<std::mutex> lk(plan.pin_mu);
+    if (!plan.pinned && !plan.dev.blob.empty()) {
+        void *h = nullptr;
+        if (cudaMallocHost(&h, plan.dev.blob.size()) == cudaSuccess) {
+            std::memcpy(h, plan.dev.blob.data(), plan.dev.blob.size());
+            plan.pinned = h;
+        } else {
+            (void)cudaGetLastError();
+        }
+    }
+    return plan.pinned ? plan.pinned : static_cast<const void *>(plan.dev.blob.data());
+}
+
+}  // namespace ra
+
 extern "C" {
 
 const char *ra_version(void) { return "libra 0.1 (sm_103a)"; }
@@ -472,7 +498,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const DeviceTables &dt = plan->dev;
     uint8_t *tab = ws + L.tables;
-    RA_CUDA(cudaMemcpyAsync(tab, dt.blob.data(), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
+    RA_CUDA(cudaMemcpyAsync(tab, plan_upload_src(*plan), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
     const int32_t *perm = reinterpret_cast<const int32_t *>(tab + dt.o_perm);
     const int32_t *off = reinterpret_cast<const int32_t *>(tab + dt.o_off);
     const int32_t *cul = reinterpret_cast<const int32_t *>(tab + dt.o_cul);
@@ -603,7 +629,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const DeviceTables &dt = plan->dev;
     uint8_t *tab = ws + L.tables;
-    RA_CUDA(cudaMemcpyAsync(tab, dt.blob.data(), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
+    RA_CUDA(cudaMemcpyAsync(tab, plan_upload_src(*plan), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
     const int32_t *perm = reinterpret_cast<const int32_t *>(tab + dt.o_perm);
     const int32_t *off = reinterpret_cast<const int32_t *>(tab + dt.o_off);
     const int32_t *cul = reinterpret_cast<const int32_t *>(tab + dt.o_cul);

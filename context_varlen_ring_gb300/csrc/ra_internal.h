@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <memory>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -104,7 +105,16 @@ struct RingPlan {
     TilePlan tiles;
     bool has_tiles = false;
     DeviceTables dev;
+    // Page-locked copy of dev.blob, made on first upload, so that the
+    // per-call table upload is an asynchronous copy that never blocks the
+    // host (a pageable source is staged synchronously by the driver).
+    void *pinned = nullptr;
+    std::mutex pin_mu;
+    ~RingPlan();
 };
+// Host source for uploading plan.dev.blob: the pinned copy (made on first
+// use), or the pageable blob if page-locked memory is unavailable.
+const void *plan_upload_src(RingPlan &plan);
 // Cached plans keyed by content (cu_seqlens, cp, mode, G, Hkv, causal).
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
                                         int causal, bool want_tiles, ra_status *st);
