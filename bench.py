@@ -200,6 +200,47 @@ def kernel_traffic(name):
     return ent["dram_bytes_per_launch"] if digest == ent["source_sha256"] else None
 
 
+def fwd_configs(args, ra, torch):
+    """Forward-only TFLOP/s of the named workloads on one GPU (CUDA events on
+    the launching stream, W warm-up calls, K timed calls; every input is far
+    above L2 except C1's K/V)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak_burst, peak_sust, _, peak_src = peaks()
+    for name in [x.strip() for x in args.fwd_configs.split(",") if x.strip()]:
+        wl = W.ALL[name]
+        cu = wl.cu_seqlens()
+        T, hq, hkv, d = wl.T, wl.hq, wl.hkv, wl.d
+        pairs = pairs_of(cu)
+        flops = 4 * d * hq * pairs
+        q, k, v = (x.to(dev) for x in W.make_qkv(T, hq, hkv, d, wl.dtype))
+        out = torch.empty_like(q)
+        lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
+        ws = torch.empty(ra.ring_workspace_bytes(T, hq, hkv, d, 0 if wl.dtype == torch.bfloat16 else 1, cu, wl.cp,
+                                                 wl.zz_mode, "fused", bwd=False), dtype=torch.uint8, device=dev)
+        f = lambda: ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, "fused", out=out, lse=lse,
+                                     workspace=ws)
+        for _ in range(max(args.warmup, 3)):
+            f()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(args.steps):
+            f()
+        e1.record(st)
+        torch.cuda.synchronize()
+        assert ra.device_status() == 0
+        ms = e0.elapsed_time(e1) / args.steps
+        tf = flops / (ms / 1e3) / 1e12
+        print(json.dumps({"fwd_config": wl.name, "T": T, "Hq": hq, "Hkv": hkv, "d": d, "cp": wl.cp,
+                          "allowed_pairs_per_head": pairs, "ms": ms, "tflops": tf,
+                          "frac_of_peak": tf / peak_burst, "peak_tflops": peak_burst, "peak_source": peak_src,
+                          "steps": args.steps, "warmup": args.warmup}), flush=True)
+        del q, k, v, out, lse, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -210,6 +251,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--probe", action="store_true",
                     help="only W+K plain steps (for profilers): no e2e, per-kernel or CPU passes")
+    ap.add_argument("--fwd-configs", default="",
+                    help="comma list of forward-only workloads (e.g. C1,C2,C3) to time instead of the "
+                         "fwd+bwd step; one JSON line each (not the headline line)")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)
@@ -219,6 +263,10 @@ def main():
     import torch.distributed as dist
 
     import context_varlen_ring_gb300 as ra
+
+    if args.fwd_configs:
+        fwd_configs(args, ra, torch)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
