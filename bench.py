@@ -366,7 +366,8 @@ def main():
     total_kernel_ms = sum(x["ms_total"] for x in kernels.values()) or 1.0
     for x in kernels.values():
         x["share"] = x["ms_total"] / total_kernel_ms
-    gpu_launches = sum(x["launches"] for x in kernels.values())
+    # kernels only (the table upload is a copy, profiled alongside)
+    gpu_launches = sum(x["launches"] for nm, x in kernels.items() if not nm.endswith("_upload"))
     peak_burst, peak_sust, hbm, peak_src = peaks()
     dominant = max(kernels, key=lambda n: kernels[n]["ms_total"]) if kernels else None
     roof = None

@@ -498,7 +498,11 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const DeviceTables &dt = plan->dev;
     uint8_t *tab = ws + L.tables;
-    RA_CUDA(cudaMemcpyAsync(tab, plan_upload_src(*plan), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
+    {
+        ProfScope ps("ra_table_upload", s);
+        RA_CUDA(cudaMemcpyAsync(tab, plan_upload_src(*plan), dt.blob.size(), cudaMemcpyHostToDevice, s),
+                "table upload");
+    }
     const int32_t *perm = reinterpret_cast<const int32_t *>(tab + dt.o_perm);
     const int32_t *off = reinterpret_cast<const int32_t *>(tab + dt.o_off);
     const int32_t *cul = reinterpret_cast<const int32_t *>(tab + dt.o_cul);
@@ -509,7 +513,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
                        {k, Kp, (int64_t)Hkv * d * (int64_t)es},
                        {v, Vp, (int64_t)Hkv * d * (int64_t)es}};
     {
-        ProfScope ps("ra_permute", s);
+        ProfScope ps("ra_permute_fwd", s);
         RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s), "permute launch");
     }
 
@@ -629,7 +633,11 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const DeviceTables &dt = plan->dev;
     uint8_t *tab = ws + L.tables;
-    RA_CUDA(cudaMemcpyAsync(tab, plan_upload_src(*plan), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
+    {
+        ProfScope ps("ra_table_upload", s);
+        RA_CUDA(cudaMemcpyAsync(tab, plan_upload_src(*plan), dt.blob.size(), cudaMemcpyHostToDevice, s),
+                "table upload");
+    }
     const int32_t *perm = reinterpret_cast<const int32_t *>(tab + dt.o_perm);
     const int32_t *off = reinterpret_cast<const int32_t *>(tab + dt.o_off);
     const int32_t *cul = reinterpret_cast<const int32_t *>(tab + dt.o_cul);
@@ -644,11 +652,15 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
                        {k, Kp, (int64_t)Hkv * d * (int64_t)es},
                        {v, Vp, (int64_t)Hkv * d * (int64_t)es},
                        {dout, dOp, (int64_t)Hq * d * (int64_t)es}};
-    {
-        ProfScope ps("ra_permute", s);
-        RA_CUDA(launch_permute(jobs, 4, perm, T, 0, s), "permute launch");
-    }
-    {
+    if (dtype == RA_BF16 && d == 128 && aligned16(out) && aligned16(dout)) {
+        // one pass: the permutes and D from the same dO reads
+        ProfScope ps("ra_permute_rowdot", s);
+        RA_CUDA(launch_permute_rowdot(jobs, 3, dout, dOp, out, D, perm, T, Hq, s), "permute+rowdot launch");
+    } else {
+        {
+            ProfScope ps("ra_permute_bwd", s);
+            RA_CUDA(launch_permute(jobs, 4, perm, T, 0, s), "permute launch");
+        }
         ProfScope ps("ra_rowdot", s);
         RA_CUDA(launch_rowdot(dout, out, dtype, T, Hq, d, D, s), "rowdot launch");
     }

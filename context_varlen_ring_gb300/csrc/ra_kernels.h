@@ -45,6 +45,12 @@ constexpr int kMaxMergeParts = 64;
 cudaError_t launch_merge(int n, const float *const *outs, const float *const *lses, int64_t Tq, int Hq, int d,
                          void *out, int out_dtype, float *lse_out, cudaStream_t st);
 // D[h, t] = sum_c a[t, h, c] * b[t, h, c]   (a, b of dtype; fp32 result)
+// Backward preprocess of bf16 tensors with head dim 128, one pass: permute
+// the jobs (Q, K, V) and dO (dout -> dout_p, Hq heads) by perm, and
+// D[h, p] = sum_c dO[p, h, c] * O[p, h, c] in fp32 at original rows p.
+// All pointers and row sizes must be 16-byte aligned (else cudaErrorInvalidValue).
+cudaError_t launch_permute_rowdot(const PermJob *jobs, int njobs, const void *dout, void *dout_p, const void *out,
+                                  float *D, const int32_t *perm, int64_t T, int Hq, cudaStream_t st);
 cudaError_t launch_rowdot(const void *a, const void *b, int dtype, int64_t T, int H, int d, float *D,
                           cudaStream_t st);
 // Per (query tile, KV head): 128 columns of -lse*log2(e) (-inf for empty

@@ -209,6 +209,108 @@ cudaError_t launch_merge(int n, const float *const *outs, const float *const *ls
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ permute + rowdot
+// Backward preprocess in one pass over the rows (bf16, head dim 128): the
+// jobs (Q, K, V) are permuted as in permute_kernel, dO is permuted too, and
+// D[h, p] = sum_c dO[p, h, c] * O[p, h, c] (fp32, exact bf16 products) is
+// taken from the same dO reads at the original row p.  A head is 16 vectors
+// of 8 elements, so each 16-lane half-warp holds one head per step and the
+// dot product is a 4-step shuffle reduction inside the half.
+__device__ __forceinline__ float dot8_bf16(const uint4 &a, const uint4 &b) {
+    const __nv_bfloat162 *x = reinterpret_cast<const __nv_bfloat162 *>(&a);
+    const __nv_bfloat162 *y = reinterpret_cast<const __nv_bfloat162 *>(&b);
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 u = __bfloat1622float2(x[k]), v = __bfloat1622float2(y[k]);
+        s = fmaf(u.x, v.x, s);
+        s = fmaf(u.y, v.y, s);
+    }
+    return s;
+}
+
+__global__ void __launch_bounds__(256) permute_rowdot_kernel(PermJobs jobs, const uint4 *__restrict__ dout,
+                                                              uint4 *__restrict__ dout_p, const uint4 *__restrict__ out,
+                                                              float *__restrict__ D, const int32_t *__restrict__ perm,
+                                                              int64_t T, int Hq, int *status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t nvo = (int64_t)Hq * 16;  // 16-byte vectors per dO / O row
+    for (int64_t i = warp; i < T; i += nwarps) {
+        const int32_t p = __ldg(perm + i);
+        if (p < 0 || (int64_t)p >= T) {
+            if (lane == 0) dev::record_status(status, RA_ERR_DEVICE_BOUNDS);
+            continue;
+        }
+        for (int jb = 0; jb < jobs.n; ++jb) {
+            const int64_t nvec = jobs.j[jb].row_bytes / 16;
+            const uint4 *__restrict__ src = reinterpret_cast<const uint4 *>(jobs.j[jb].src) + (int64_t)p * nvec;
+            uint4 *__restrict__ dst = reinterpret_cast<uint4 *>(jobs.j[jb].dst) + i * nvec;
+            for (int64_t c0 = lane; c0 < nvec; c0 += 128) {
+                uint4 tmp[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t c = c0 + u * 32;
+                    if (c < nvec) tmp[u] = src[c];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int64_t c = c0 + u * 32;
+                    if (c < nvec) dst[c] = tmp[u];
+                }
+            }
+        }
+        const uint4 *__restrict__ a = dout + (int64_t)p * nvo;
+        const uint4 *__restrict__ b = out + (int64_t)p * nvo;
+        uint4 *__restrict__ dst = dout_p + i * nvo;
+        for (int64_t c0 = lane; c0 < nvo; c0 += 128) {
+            uint4 x[4], y[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + u * 32;
+                if (c < nvo) {
+                    x[u] = a[c];
+                    y[u] = b[c];
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + u * 32;
+                if (c < nvo) dst[c] = x[u];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t c = c0 + u * 32;  // nvo is a multiple of 16: a half-warp is all in or all out
+                float sum = c < nvo ? dot8_bf16(x[u], y[u]) : 0.f;
+#pragma unroll
+                for (int sh = 8; sh; sh >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, sh);
+                if (c < nvo && (lane & 15) == 0) D[(c >> 4) * T + p] = sum;
+            }
+        }
+    }
+}
+
+cudaError_t launch_permute_rowdot(const PermJob *jobs, int njobs, const void *dout, void *dout_p, const void *out,
+                                  float *D, const int32_t *perm, int64_t T, int Hq, cudaStream_t st) {
+    if (T <= 0) return cudaSuccess;
+    if (njobs < 0 || njobs > 4) return cudaErrorInvalidValue;
+    PermJobs pj{};
+    pj.n = njobs;
+    auto al = [](const void *q, int64_t rb) { return (reinterpret_cast<uintptr_t>(q) % 16) == 0 && (rb % 16) == 0; };
+    for (int i = 0; i < njobs; ++i) {
+        if (!al(jobs[i].src, jobs[i].row_bytes) || !al(jobs[i].dst, jobs[i].row_bytes)) return cudaErrorInvalidValue;
+        pj.j[i] = jobs[i];
+    }
+    if (!al(dout, 16) || !al(dout_p, 16) || !al(out, 16)) return cudaErrorInvalidValue;
+    const int64_t want = (T + 7) / 8;
+    const int blocks = (int)std::min<int64_t>(want, (int64_t)num_sms() * 8);
+    permute_rowdot_kernel<<<blocks, 256, 0, st>>>(pj, static_cast<const uint4 *>(dout), static_cast<uint4 *>(dout_p),
+                                                  static_cast<const uint4 *>(out), D, perm, T, Hq,
+                                                  device_status_ptr());
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ rowdot
 template <typename TIn>
 __global__ void __launch_bounds__(256) rowdot_kernel(const TIn *a, const TIn *b, int64_t T, int H, int d,
