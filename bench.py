@@ -2,10 +2,12 @@
 
 One step = the whole hot path on the packed 32768-token workload (GQA 32/8,
 d=128, bf16, per-document zigzag over 8 simulated CP ranks): zigzag
-permute, ring forward with on-chip merge, un-permute, backward
-preprocess, ring backward with fp32 dK/dV, casts.  FLOPs count allowed
-(causal, same-document) pairs only: 4*d*Hq per pair forward, 10*d*Hq
-backward.
+permute of Q, K, V, ring forward with on-chip merge (O and LSE written in
+the original order), backward preprocess (permute dO, D = rowsum(dO*O),
+per-tile LSE/D), ring backward with fp32 dK/dV (the backward reuses the
+forward's rank-ordered Q, K, V from the shared workspace, its saved
+activations).  FLOPs count allowed (causal, same-document) pairs only:
+4*d*Hq per pair forward, 10*d*Hq backward.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -301,7 +303,7 @@ def main():
     def step():
         ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, out=out, lse=lse, workspace=ws)
         ra.ring_attn_bwd(q, k, v, out, lse, do, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, dq=dq, dk=dk,
-                         dv=dv, workspace=ws)
+                         dv=dv, workspace=ws, reuse_fwd_workspace=True)
 
     def fwd_only():
         ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, out=out, lse=lse, workspace=ws)
@@ -414,7 +416,7 @@ def main():
         do_.copy_(hd_, non_blocking=True)
         o_, l_ = ra.ring_attn_fwd(q_, k_, v_, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, workspace=ws)
         g = ra.ring_attn_bwd(q_, k_, v_, o_, l_, do_, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, dq=dq_,
-                             dk=dk_, dv=dv_, workspace=ws)
+                             dk=dk_, dv=dv_, workspace=ws, reuse_fwd_workspace=True)
         ho.copy_(o_, non_blocking=True)
         hdq.copy_(g[0], non_blocking=True)
         hdk.copy_(g[1], non_blocking=True)
@@ -452,7 +454,9 @@ def main():
                    "cp": wl.cp, "zigzag": "per-doc", "sched": args.sched, "causal_pairs_per_head": pairs,
                    "l2": "no flush: each step streams ~2.6 GB (Q, dO, O 268 MB each, fp32 dQ 537 MB, permuted "
                          "copies), far above the 129 MB L2",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "bwd_reserve": "the backward reuses the forward's rank-ordered Q, K, V and tile tables from "
+                                  "the shared workspace (its saved activations); every step permutes once"},
         "fwd": {"tflops": fwd_tflops, "ms": fwd_ms, "frac_of_peak": fwd_tflops / peak_burst},
         "fwd_bwd_frac_of_peak": value / world / peak_burst,
         "peak_tflops": {"burst": peak_burst, "sustained": peak_sust, "source": peak_src},

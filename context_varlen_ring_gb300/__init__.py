@@ -13,8 +13,8 @@ import math
 import numpy as np
 import torch
 
-from ._lib import (RA_BF16, RA_FP32, RA_SCHED_FUSED, RA_SCHED_STEPWISE, RA_ZZ_GLOBAL, RA_ZZ_PER_DOC,
-                   RaError, check, lib)
+from ._lib import (RA_BF16, RA_BWD_FWD_RESERVE, RA_FP32, RA_SCHED_FUSED, RA_SCHED_STEPWISE, RA_ZZ_GLOBAL,
+                   RA_ZZ_PER_DOC, RaError, check, lib)
 
 __all__ = [
     "zigzag_plan", "zigzag_permute", "zigzag_unpermute", "varlen_attn_partial", "lse_merge",
@@ -200,8 +200,13 @@ def ring_attn_fwd(q, k, v, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal
 
 def ring_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool = True,
                   scale: float | None = None, sched: str = "fused", grad_dtype=None, dq=None, dk=None, dv=None,
-                  workspace=None):
-    """Gradients (dq, dk, dv) in the original token order."""
+                  workspace=None, reuse_fwd_workspace: bool = False):
+    """Gradients (dq, dk, dv) in the original token order.
+
+    reuse_fwd_workspace: `workspace` is the one the preceding ring_attn_fwd
+    used with these same q, k, v and arguments, untouched since; its
+    rank-ordered Q, K, V and tile tables are reused (RA_BWD_FWD_RESERVE).
+    """
     _check_cuda(q, k, v, out, lse, dout)
     T, Hq, d = q.shape
     Hkv = k.shape[1]
@@ -218,7 +223,8 @@ def ring_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, cp: int, mode: int = RA_Z
     ws = workspace if workspace is not None else _WS.get(q.device, int(need))
     check(L.ra_ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), dt, T, Hq, Hkv, d, _np_ptr(cu), B, cp, mode, int(causal),
                              scale, _SCHED[sched], _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
-                             _dtype_code(dq), _ptr(ws), ws.numel(), _stream(q.device)),
+                             _dtype_code(dq), RA_BWD_FWD_RESERVE if reuse_fwd_workspace else 0, _ptr(ws), ws.numel(),
+                             _stream(q.device)),
           "ra_ring_attn_bwd")
     return dq, dk, dv
 

@@ -22,6 +22,7 @@ RA_ERR_DEVICE_BOUNDS = 6
 
 RA_ZZ_GLOBAL = 0
 RA_ZZ_PER_DOC = 1
+RA_BWD_FWD_RESERVE = 1
 RA_BF16 = 0
 RA_FP32 = 1
 RA_SCHED_FUSED = 0
@@ -62,7 +63,7 @@ def _declare(L):
         "ra_ring_attn_fwd": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, i32, f32, i32,
                                    P, P, P, sz, P]),
         "ra_ring_attn_bwd": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, i32, f32, i32,
-                                   P, P, P, P, P, P, i32, P, sz, P]),
+                                   P, P, P, P, P, P, i32, i32, P, sz, P]),
         "ra_ring_rank_pairs": (i32, [P, i32, i32, i32, i32, P]),
         "ra_get_device_status": (i32, [P]),
         "ra_selftest_wait_timeout": (i32, [i64, P]),

@@ -122,6 +122,41 @@ const void *plan_upload_src(RingPlan &plan) {
     return plan.pinned ? plan.pinned : static_cast<const void *>(plan.dev.blob.data());
 }
 
+// Host record of what the last ring forward left in each workspace (the
+// reserve space a backward may reuse with RA_BWD_FWD_RESERVE).
+struct ReserveRec {
+    const void *plan, *q, *k, *v;
+    int dtype, Hq, Hkv, d, causal, sched;
+    int64_t T;
+};
+static std::mutex g_reserve_mu;
+static std::vector<std::pair<const void *, ReserveRec>> g_reserve;  // few workspaces, linear scan
+
+void reserve_record(const void *ws, const void *plan, const void *q, const void *k, const void *v, int dtype,
+                    int64_t T, int Hq, int Hkv, int d, int causal, int sched) {
+    std::lock_guard<std::mutex> lk(g_reserve_mu);
+    const ReserveRec r{plan, q, k, v, dtype, Hq, Hkv, d, causal, sched, T};
+    for (auto &e : g_reserve)
+        if (e.first == ws) {
+            e.second = r;
+            return;
+        }
+    if (g_reserve.size() >= 64) g_reserve.erase(g_reserve.begin());
+    g_reserve.emplace_back(ws, r);
+}
+
+bool reserve_matches(const void *ws, const void *plan, const void *q, const void *k, const void *v, int dtype,
+                     int64_t T, int Hq, int Hkv, int d, int causal, int sched) {
+    std::lock_guard<std::mutex> lk(g_reserve_mu);
+    for (const auto &e : g_reserve)
+        if (e.first == ws) {
+            const ReserveRec &r = e.second;
+            return r.plan == plan && r.q == q && r.k == k && r.v == v && r.dtype == dtype && r.T == T &&
+                   r.Hq == Hq && r.Hkv == Hkv && r.d == d && r.causal == causal && r.sched == sched;
+        }
+    return false;
+}
+
 }  // namespace ra
 
 extern "C" {
@@ -516,6 +551,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
         ProfScope ps("ra_permute_fwd", s);
         RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s), "permute launch");
     }
+    reserve_record(workspace, plan.get(), q, k, v, dtype, T, Hq, Hkv, d, causal, sched);
 
     auto run_partial = [&](int t0, int t1, int out_mode, void *o, float *l, int64_t lse_T) -> ra_status {
         if (tc) {
@@ -614,7 +650,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
 ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
                            const int32_t *cu, int B, int cp, int mode, int causal, float scale, int sched,
                            const void *out, const float *lse, const void *dout, void *dq, void *dk, void *dv,
-                           int grad_dtype, void *workspace, size_t ws_bytes, void *stream) {
+                           int grad_dtype, int flags, void *workspace, size_t ws_bytes, void *stream) {
     ra_status st = ring_checks(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, sched, scale);
     if (st) return st;
     if (grad_dtype != RA_BF16 && grad_dtype != RA_FP32) return fail(RA_ERR_INVALID_ARG, "bad grad_dtype");
@@ -633,7 +669,11 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     const DeviceTables &dt = plan->dev;
     uint8_t *tab = ws + L.tables;
-    {
+    // the forward's reserve space: tables and rank-ordered Q, K, V (same
+    // offsets in both layouts) when the caller asks and the host record agrees
+    const bool reserve = (flags & RA_BWD_FWD_RESERVE) &&
+                         reserve_matches(workspace, plan.get(), q, k, v, dtype, T, Hq, Hkv, d, causal, sched);
+    if (!reserve) {
         ProfScope ps("ra_table_upload", s);
         RA_CUDA(cudaMemcpyAsync(tab, plan_upload_src(*plan), dt.blob.size(), cudaMemcpyHostToDevice, s),
                 "table upload");
@@ -655,11 +695,15 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     if (dtype == RA_BF16 && d == 128 && aligned16(out) && aligned16(dout)) {
         // one pass: the permutes and D from the same dO reads
         ProfScope ps("ra_permute_rowdot", s);
-        RA_CUDA(launch_permute_rowdot(jobs, 3, dout, dOp, out, D, perm, T, Hq, s), "permute+rowdot launch");
+        RA_CUDA(launch_permute_rowdot(jobs, reserve ? 0 : 3, dout, dOp, out, D, perm, T, Hq, s),
+                "permute+rowdot launch");
     } else {
         {
             ProfScope ps("ra_permute_bwd", s);
-            RA_CUDA(launch_permute(jobs, 4, perm, T, 0, s), "permute launch");
+            if (reserve)
+                RA_CUDA(launch_permute(jobs + 3, 1, perm, T, 0, s), "permute launch");
+            else
+                RA_CUDA(launch_permute(jobs, 4, perm, T, 0, s), "permute launch");
         }
         ProfScope ps("ra_rowdot", s);
         RA_CUDA(launch_rowdot(dout, out, dtype, T, Hq, d, D, s), "rowdot launch");

@@ -213,12 +213,22 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
                            int causal, float scale, int sched,
                            void *out, float *lse,
                            void *workspace, size_t ws_bytes, void *stream);
+/* flags of ra_ring_attn_bwd.
+ * RA_BWD_FWD_RESERVE: the workspace is a reserve space left by the
+ * preceding ra_ring_attn_fwd on the same stream with the same q, k, v
+ * (unmodified), dtype, shapes, cu_seqlens, cp, zz_mode, causal and sched,
+ * and nothing has written into it since: the rank-ordered Q, K, V and the
+ * tile tables it holds are reused instead of rebuilt (they are the
+ * forward's saved activations).  The library checks on the host that the
+ * last forward on this workspace had the same pointers and plan and
+ * ignores the flag otherwise; it cannot see changes to the contents. */
+#define RA_BWD_FWD_RESERVE 1
 ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtype,
                            int64_t T, int Hq, int Hkv, int d,
                            const int32_t *cu_seqlens, int B, int cp, int zz_mode,
                            int causal, float scale, int sched,
                            const void *out, const float *lse, const void *dout,
-                           void *dq, void *dk, void *dv, int grad_dtype,
+                           void *dq, void *dk, void *dv, int grad_dtype, int flags,
                            void *workspace, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------

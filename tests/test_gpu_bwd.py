@@ -131,3 +131,37 @@ def test_bwd_c4_full_size(ra, orc):
         assert np.abs(dv[:, g].astype(np.float64).sum(0) - ref).max() <= 1e-2 * max(1.0, np.abs(ref).max())
         scale_k = np.abs(dk[:, g]).sum(0).max()
         assert np.abs(dk[:, g].astype(np.float64).sum(0)).max() <= 1e-3 * scale_k
+
+
+@pytest.mark.parametrize("sched", ["fused", "stepwise"])
+def test_bwd_reuse_forward_workspace(ra, sched):
+    """RA_BWD_FWD_RESERVE: reusing the forward's rank-ordered Q, K, V and
+    tables gives exactly the gradients of the full backward; with other
+    tensors than the forward's the library ignores the flag."""
+    cu = W.cu_seqlens((300, 41, 500, 77))
+    T = int(cu[-1])
+    q, k, v = (x.cuda() for x in W.make_qkv(T, 16, 4, 128, torch.bfloat16))
+    do = W.make_dout(T, 16, 128, torch.bfloat16).cuda()
+    nb = max(ra.ring_workspace_bytes(T, 16, 4, 128, 0, cu, 4, 1, sched, bwd=b) for b in (False, True))
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    out, lse = ra.ring_attn_fwd(q, k, v, cu, 4, 1, True, None, sched, workspace=ws)
+    ref = ra.ring_attn_bwd(q, k, v, out, lse, do, cu, 4, 1, True, None, sched, workspace=ws)
+    ref = [x.clone() for x in ref]
+    out, lse = ra.ring_attn_fwd(q, k, v, cu, 4, 1, True, None, sched, workspace=ws)
+    got = ra.ring_attn_bwd(q, k, v, out, lse, do, cu, 4, 1, True, None, sched, workspace=ws,
+                           reuse_fwd_workspace=True)
+    torch.cuda.synchronize()
+    assert ra.device_status() == 0
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+    # a different q than the forward saw: the flag must be ignored
+    q2 = q.flip(0).contiguous()
+    out2, lse2 = ra.ring_attn_fwd(q2, k, v, cu, 4, 1, True, None, sched)
+    ref2 = [x.clone() for x in ra.ring_attn_bwd(q2, k, v, out2, lse2, do, cu, 4, 1, True, None, sched)]
+    ra.ring_attn_fwd(q, k, v, cu, 4, 1, True, None, sched, workspace=ws)
+    got2 = ra.ring_attn_bwd(q2, k, v, out2, lse2, do, cu, 4, 1, True, None, sched, workspace=ws,
+                            reuse_fwd_workspace=True)
+    torch.cuda.synchronize()
+    assert ra.device_status() == 0
+    for a, b in zip(ref2, got2):
+        assert torch.equal(a, b)
