@@ -15,14 +15,15 @@
 //
 // GB300 design: a persistent CTA per SM walks work items (query tile of
 // 128 MMA rows = 128/G tokens x G heads of one KV head) in a fixed stride,
-// so there is no per-tile launch, TMEM allocation or cold start.  The
-// compute warpgroups load each item's Q rows from global memory (L2
-// prefetched one item ahead) straight into TMEM (S = Q K^T is a TS-MMA);
-// dO is staged by TMA in shared memory as the A operand of dP = dO V^T and
-// reloaded as soon as the previous item's last dP has read it.  K/V tiles
-// stream through a 6-slot TMA ring, the visited KV tiles (class and
-// positions) through a shared-memory ring, with an end marker after each
-// item.  TMEM: dQ [0,128), S [128,256), dP
+// so there is no per-tile launch, TMEM allocation or cold start.  Each
+// item's Q tile travels through the 6-slot TMA ring ahead of its K/V tiles
+// (ring order: Q(k), K(k,0), V(k,0), K(k,1), ...), so it lands while the
+// previous item still computes; the compute warpgroups copy it into TMEM
+// (S = Q K^T is a TS-MMA) and release the slot.  dO is staged by TMA in
+// shared memory as the A operand of dP = dO V^T; the dP issuer reloads it
+// as soon as its own last dP of an item has read it.  The visited KV tiles
+// (class and positions) go through a shared-memory ring, with an end marker
+// after each item.  TMEM: dQ [0,128), S [128,256), dP
 // [256,384), Q (bf16) [384,448), dS (bf16) [448,512).  Two compute
 // warpgroups split the 128 key columns.
 //
@@ -64,9 +65,7 @@ constexpr uint32_t kOffBar = kOffKV + kSlots * kTile;
 constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 
 struct DqParams {
-    CUtensorMap tmK, tmV, tmDO;
-    const void *q;  // permuted Q [T, Hq, 128] bf16 (read row-wise into TMEM)
-    long long T;
+    CUtensorMap tmQ, tmK, tmV, tmDO;
     const int4 *qtiles, *kvtiles, *items;
     const int *kv_off;
     int n_items, cp, B, G, log2G, Hq;
@@ -185,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
         if (warp == 0) {
             // -------------------------------------------- producer
             if (lane == 0) {
-                tma_prefetch_desc(&p.tmDO);
+                tma_prefetch_desc(&p.tmQ);
                 tma_prefetch_desc(&p.tmK);
                 tma_prefetch_desc(&p.tmV);
             }
@@ -200,13 +199,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 const int4 qa = __ldg(p.qtiles + 2 * qt), qb = __ldg(p.qtiles + 2 * qt + 1);
                 const QInfo q{qa.y, qb.y, qb.z};
                 if (lane == 0) {
-                    const int hq0 = g * p.G;
-                    // dO is free once the previous item's last dP has read it
-                    if (k > 0 && !mbar_wait(do_empty, (k - 1) & 1, wc)) ok = 0;
-                    if (ok) {
-                        mbar_arrive_expect_tx(do_full, kTile);
-                        tma_load_3d(base + kOffDO, &p.tmDO, do_full, 0, hq0, qa.x);
-                        tma_load_3d(base + kOffDO + kHalf, &p.tmDO, do_full, 64, hq0, qa.x);
+                    // Q(k) into the next ring slot, ahead of the item's K/V tiles
+                    const uint32_t slot = u % kSlots, ph = (u / kSlots) & 1u;
+                    if (!mbar_wait(kv_empty + slot, ph ^ 1u, wc)) {
+                        ok = 0;
+                    } else {
+                        uint8_t *dst = base + kOffKV + slot * kTile;
+                        mbar_arrive_expect_tx(kv_full + slot, kTile);
+                        tma_load_3d(dst, &p.tmQ, kv_full + slot, 0, g * p.G, qa.x);
+                        tma_load_3d(dst + kHalf, &p.tmQ, kv_full + slot, 64, g * p.G, qa.x);
+                        ++u;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -276,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 // the last copies into every buffer must have landed before exit
                 volatile int local_abort = 0;
                 const WaitCtl drain{&local_abort, p.status, p.budget_ns};
-                (void)mbar_wait(do_full, (n_my - 1) & 1, drain);
                 for (uint32_t x = (u > kSlots ? u - kSlots : 0); x < u; ++x)
                     (void)mbar_wait(kv_full + (x % kSlots), (x / kSlots) & 1u, drain);
             }
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                             ok = false;
                             break;
                         }
-                        const uint32_t ku = 2 * jg;
+                        const uint32_t ku = 2 * jg + k + 1;  // one Q slot per item before its tiles
                         if (!wait(kv_full + ku % kSlots, kv_par(ku))) {
                             ok = false;
                             break;
@@ -323,7 +324,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         ++jg;
                     }
                 } else if (warp == 2) {
-                    // dP(j) = dO V(j)^T (dO from shared memory) once dP(j-1) was read
+                    // dP(j) = dO V(j)^T (dO from shared memory) once dP(j-1) was read;
+                    // this thread also stages dO: item 0's here, item k+1's once
+                    // item k's last dP has read the buffer
+                    auto load_do = [&](int kk) {
+                        const int4 ia = __ldg(p.items + 2 * item_of(kk));
+                        const int row0 = __ldg(&p.qtiles[2 * ia.x].x);
+                        mbar_arrive_expect_tx(do_full, kTile);
+                        tma_load_3d(base + kOffDO, &p.tmDO, do_full, 0, ia.z * p.G, row0);
+                        tma_load_3d(base + kOffDO + kHalf, &p.tmDO, do_full, 64, ia.z * p.G, row0);
+                    };
+                    if (k == 0) load_do(0);
                     ok = wait(do_full, k & 1);
                     const uint64_t a0 = sdesc_sw128(base_s + kOffDO, 16, 1024);
                     for (; ok;) {
@@ -337,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                             ok = false;
                             break;
                         }
-                        const uint32_t vu = 2 * jg + 1;
+                        const uint32_t vu = 2 * jg + k + 2;
                         if (!wait(kv_full + vu % kSlots, kv_par(vu))) {
                             ok = false;
                             break;
@@ -350,6 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         ++jg;
                     }
                     if (ok) tc_commit(do_empty);  // this item's dO is no longer read
+                    if (ok && k + 1 < n_my) {
+                        ok = mbar_wait(do_empty, k & 1, wc);
+                        if (ok) load_do(k + 1);
+                    }
                 } else {
                     // dQ += dS_h(j) K(j)_h: keys [64h, 64h + 64) = K rows (MN-major: d
                     // contiguous), A = group h's dS at dS columns [32h, 32h + 32)
@@ -362,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                             break;
                         }
                         if (e.x & 16) break;
-                        const uint32_t kslot = (2 * jg) % kSlots;
+                        const uint32_t kslot = (2 * jg + k + 1) % kSlots;
                         const uint64_t d0 = sdesc_sw128(base_s + kOffKV + kslot * kTile, kHalf, 1024);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
@@ -399,30 +414,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const int G = p.G;
         uint32_t jg = 0, ri = 0;
-        // Row m of item k's Q tile: token m >> log2 G, head g G + (m mod G);
-        // this group's d half (64 bf16 = 128 bytes) at q_rowptr(k).
-        auto q_rowptr = [&](int k) -> const uint4 * {
-            const int4 ia = __ldg(p.items + 2 * item_of(k));
-            const int4 qa = __ldg(p.qtiles + 2 * ia.x);
-            const long long row = (long long)qa.x + (m >> p.log2G);
-            if (row >= p.T) return nullptr;  // beyond the buffer: padding row
-            const long long e0 = (row * p.Hq + ia.z * G + (m & (G - 1))) * 128 + 64 * h;
-            return reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.q) + e0);
-        };
-        // Q of item k into TMEM.  The S products of earlier items, which read
-        // tQ, are complete (their results were consumed), and the S issuer
-        // has taken item k-1's Q-ready phase, so the phases cannot run two
-        // ahead of it even across items without KV tiles.
+        // Q of item k into TMEM from its ring slot (u = 2 * tiles before item k
+        // + k), then the slot is released.  The S products of earlier items,
+        // which read tQ, are complete (their results were consumed), and the S
+        // issuer has taken item k-1's Q-ready phase, so the phases cannot run
+        // two ahead of it even across items without KV tiles.
         auto copy_q = [&](int k) -> bool {
-            bool okq = k == 0 || mbar_wait(x_ready, (k - 1) & 1, wc);
+            const uint32_t uq = 2 * jg + (uint32_t)k, slot = uq % kSlots;
+            bool okq = mbar_wait(kv_full + slot, (uq / kSlots) & 1u, wc) &&
+                       (k == 0 || mbar_wait(x_ready, (k - 1) & 1, wc));
             if (okq) {
-                const uint4 *src = q_rowptr(k);
+                // this group's d half of row m (bf16 pairs); swizzled 128-byte
+                // rows: chunk c of row m at (c ^ (m & 7)) * 16
+                const uint8_t *qrow = base + kOffKV + slot * kTile + h * kHalf + (m >> 3) * 1024 + (m & 7) * 128;
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
                     uint32_t w[16];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint4 x = src ? __ldg(src + 4 * part + c) : make_uint4(0, 0, 0, 0);
+                        const int ch = 4 * part + c;
+                        const uint4 x = *reinterpret_cast<const uint4 *>(qrow + ((ch ^ (m & 7)) << 4));
                         w[4 * c] = x.x;
                         w[4 * c + 1] = x.y;
                         w[4 * c + 2] = x.z;
@@ -431,6 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     tmem_st16(tQ + lane_base + 32u * h + 16u * part, w);
                 }
             }
+            // every compute thread has read the slot: release it to the producer
+            asm volatile("bar.sync 1, 256;\n" ::: "memory");
+            if (threadIdx.x == 128) mbar_arrive(kv_empty + slot);
             tc_fence_before();
             mbar_arrive(qc_ready);
             return okq;
@@ -440,10 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
             const int it = item_of(k);
             const int4 ia = __ldg(p.items + 2 * it);
             const int qt = ia.x, g = ia.z;
-            if (k + 1 < n_my) {
-                const uint4 *nx = q_rowptr(k + 1);
-                if (nx) asm volatile("prefetch.global.L2 [%0];" ::"l"(nx));
-            }
+
             const int4 qa = __ldg(p.qtiles + 2 * qt), qb = __ldg(p.qtiles + 2 * qt + 1);
             const int tok = m >> p.log2G, head = g * G + (m & (G - 1));
             const bool valid = tok < qa.y;
@@ -618,9 +629,7 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
     DqParams p;
     memset(&p, 0, sizeof(p));
     const int G = a.G;
-    p.q = a.q;
-    p.T = a.T;
-    if (!make_map(&p.tmDO, a.dout, a.T, a.Hq, G, kBM / G) ||
+    if (!make_map(&p.tmQ, a.q, a.T, a.Hq, G, kBM / G) || !make_map(&p.tmDO, a.dout, a.T, a.Hq, G, kBM / G) ||
         !make_map(&p.tmK, a.k, a.T, a.Hkv, 1, kBN) || !make_map(&p.tmV, a.v, a.T, a.Hkv, 1, kBN))
         return cudaErrorInvalidValue;
     p.qtiles = static_cast<const int4 *>(a.qtiles);
