@@ -300,6 +300,13 @@ __device__ __forceinline__ float2 sub_mul2(float2 a, float2 c, float2 b) {
         : "f"(a.x), "f"(a.y), "f"(c.x), "f"(c.y), "f"(b.x), "f"(b.y));
     return d;
 }
+// 32-byte global store (sm_100 family), dst 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *dst, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // Three-input maximum (one instruction on sm_100-family cores).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float d;

@@ -449,22 +449,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
             mbar_arrive(qc_ready);
             return okq;
         };
+        // row m of item k: validity, position, head, and its saved lse and D
+        // (issued one item ahead so their latency is off the first tile)
+        struct RowInfo {
+            bool valid;
+            int qpos, head;
+            float lse, D;
+        };
+        auto row_info = [&](int k) -> RowInfo {
+            const int4 ia = __ldg(p.items + 2 * item_of(k));
+            const int4 qa = __ldg(p.qtiles + 2 * ia.x), qb = __ldg(p.qtiles + 2 * ia.x + 1);
+            const int tok = m >> p.log2G;
+            RowInfo ri_{tok < qa.y, tok < qa.z ? qa.w + tok : qb.x + (tok - qa.z), ia.z * G + (m & (G - 1)), 0.f, 0.f};
+            if (ri_.valid) {
+                ri_.lse = __ldg(p.lse + (long long)ri_.head * p.lse_T + ri_.qpos);
+                ri_.D = __ldg(p.D + (long long)ri_.head * p.lse_T + ri_.qpos);
+            }
+            return ri_;
+        };
         bool ok = n_my > 0 ? copy_q(0) : true;
+        RowInfo nxt = n_my > 0 ? row_info(0) : RowInfo{false, 0, 0, 0.f, 0.f};
         for (int k = 0; k < n_my && ok; ++k) {
-            const int it = item_of(k);
-            const int4 ia = __ldg(p.items + 2 * it);
-            const int qt = ia.x, g = ia.z;
-
-            const int4 qa = __ldg(p.qtiles + 2 * qt), qb = __ldg(p.qtiles + 2 * qt + 1);
-            const int tok = m >> p.log2G, head = g * G + (m & (G - 1));
-            const bool valid = tok < qa.y;
-            const int qpos = tok < qa.z ? qa.w + tok : qb.x + (tok - qa.z);
+            const RowInfo cur = nxt;
+            if (k + 1 < n_my) nxt = row_info(k + 1);
+            const bool valid = cur.valid;
+            const int qpos = cur.qpos, head = cur.head;
             // P' = scale * P = exp2(s * scale * log2(e) + bias), bias = log2(scale) - lse * log2(e)
             float bias = -INFINITY, Dm = 0.f;
             if (valid) {
-                const float l = __ldg(p.lse + (long long)head * p.lse_T + qpos);
-                bias = (l == -INFINITY) ? -INFINITY : p.log2_scale - l * 1.4426950408889634f;
-                Dm = __ldg(p.D + (long long)head * p.lse_T + qpos);
+                bias = (cur.lse == -INFINITY) ? -INFINITY : p.log2_scale - cur.lse * 1.4426950408889634f;
+                Dm = cur.D;
             }
             uint32_t nd = 0;
             for (; ok;) {
@@ -557,15 +571,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
             if (ok && valid) {
                 const long long e0 = ((long long)qpos * p.Hq + head) * 128 + 64 * h;
                 if (p.out_mode == 0) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.dq) + e0);
+                    // 128 contiguous bytes per thread as four 32-byte stores
+                    __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.dq) + e0;
 #pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1]));
-                        w.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3]));
-                        w.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5]));
-                        w.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7]));
-                        dst[q4] = w;
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            w[e] = pack_bf16x2(__uint_as_float(v[16 * q8 + 2 * e]), __uint_as_float(v[16 * q8 + 2 * e + 1]));
+                        st_global_v8(dst + 16 * q8, w);
                     }
                 } else {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.dq) + e0);
