@@ -509,15 +509,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 if (valid) {
                     const long long e0 = (orow * p.Hq + head) * 128 + 32 * ch;
                     if (p.out_mode == kOutFinal) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) + e0);
+                        // 64 contiguous bytes per chunk as two 32-byte stores
+                        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(p.out) + e0;
 #pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
-                            w.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
-                            w.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
-                            w.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
-                            dst[q4] = w;
+                        for (int q8 = 0; q8 < 2; ++q8) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                w[e] = pack_bf16x2(__uint_as_float(v[16 * q8 + 2 * e]) * inv,
+                                                   __uint_as_float(v[16 * q8 + 2 * e + 1]) * inv);
+                            st_global_v8(dst + 16 * q8, w);
                         }
                     } else {
                         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + e0);
