@@ -421,15 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             if (!kvalid) continue;
             void *outp = which ? p.dv : p.dk;
             if (p.out_mode == 0) {
-                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(outp) + rowoff);
+                // 128 contiguous bytes per thread as four 32-byte stores
+                __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(outp) + rowoff;
 #pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]), __uint_as_float(v[8 * q4 + 1]));
-                    w.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]), __uint_as_float(v[8 * q4 + 3]));
-                    w.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]), __uint_as_float(v[8 * q4 + 5]));
-                    w.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]), __uint_as_float(v[8 * q4 + 7]));
-                    dst[q4] = w;
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w[e] = pack_bf16x2(__uint_as_float(v[16 * q8 + 2 * e]), __uint_as_float(v[16 * q8 + 2 * e + 1]));
+                    st_global_v8(dst + 16 * q8, w);
                 }
             } else {
                 float4 *d4 = reinterpret_cast<float4 *>(static_cast<float *>(outp) + rowoff);
