@@ -130,29 +130,47 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
             const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
             for (int i = qa; i < qe; i += 2) {
                 const int q1 = (i + 1 < qe) ? i + 1 : -1;
+                // the ring steps [tf, tl) span every visited KV tile: the
+                // kernels' producers scan no tile records outside them
                 int64_t cost = 0;
+                int tf = cp, tl = 0;
                 for (int t = 0; t < cp; ++t) {
                     const int s = ((r - t) % cp + cp) % cp;
                     const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
+                    int64_t c_t = 0;
                     for (int j = ka; j < ke; ++j) {
-                        cost += classify(tp.qtiles[i], tp.kvtiles[j], causal) != kSkip;
-                        if (q1 >= 0) cost += classify(tp.qtiles[q1], tp.kvtiles[j], causal) != kSkip;
+                        c_t += classify(tp.qtiles[i], tp.kvtiles[j], causal) != kSkip;
+                        if (q1 >= 0) c_t += classify(tp.qtiles[q1], tp.kvtiles[j], causal) != kSkip;
                     }
+                    if (c_t) {
+                        tf = std::min(tf, t);
+                        tl = t + 1;
+                    }
+                    cost += c_t;
                 }
+                if (tf > tl) tf = tl = 0;
                 for (int g = 0; g < Hkv; ++g) {
-                    WorkItem w{i, q1, g, r, b, 0, cp, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
+                    WorkItem w{i, q1, g, r, b, tf, tl, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
                     tp.items.push_back(w);
                 }
                 // per-query-tile items of the dQ pass
                 for (int qi = i; qi <= (q1 >= 0 ? q1 : i); ++qi) {
                     int64_t qc = 0;
+                    int qf = cp, ql = 0;
                     for (int t = 0; t < cp; ++t) {
                         const int s2 = ((r - t) % cp + cp) % cp;
                         const int ka = tp.kv_off[seg_idx(s2, b)], ke = tp.kv_off[seg_idx(s2, b) + 1];
-                        for (int j = ka; j < ke; ++j) qc += classify(tp.qtiles[qi], tp.kvtiles[j], causal) != kSkip;
+                        int64_t c_t = 0;
+                        for (int j = ka; j < ke; ++j) c_t += classify(tp.qtiles[qi], tp.kvtiles[j], causal) != kSkip;
+                        if (c_t) {
+                            qf = std::min(qf, t);
+                            ql = t + 1;
+                        }
+                        qc += c_t;
                     }
+                    if (qf > ql) qf = ql = 0;
                     for (int g = 0; g < Hkv; ++g) {
-                        WorkItem w{qi, -1, g, r, b, 0, cp, (int32_t)std::min<int64_t>(qc, INT32_MAX)};
+                        WorkItem w{qi, -1, g, r, b, qf, ql, (int32_t)std::min<int64_t>(qc, INT32_MAX)};
                         tp.qitems.push_back(w);
                     }
                 }
@@ -165,13 +183,21 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
             const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
             for (int j = ka; j < ke; ++j) {
                 int64_t cost = 0;
+                int tf = cp, tl = 0;
                 for (int t = 0; t < cp; ++t) {
                     const int r = (s + t) % cp;
                     const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
-                    for (int i = qa; i < qe; ++i) cost += classify(tp.qtiles[i], tp.kvtiles[j], causal) != kSkip;
+                    int64_t c_t = 0;
+                    for (int i = qa; i < qe; ++i) c_t += classify(tp.qtiles[i], tp.kvtiles[j], causal) != kSkip;
+                    if (c_t) {
+                        tf = std::min(tf, t);
+                        tl = t + 1;
+                    }
+                    cost += c_t;
                 }
+                if (tf > tl) tf = tl = 0;
                 for (int g = 0; g < Hkv; ++g) {
-                    WorkItem w{j, -1, g, s, b, 0, cp, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
+                    WorkItem w{j, -1, g, s, b, tf, tl, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
                     tp.bitems.push_back(w);
                 }
             }
