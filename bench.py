@@ -180,9 +180,24 @@ def job_tflops(world, flops_per_step, steps, max_ms):
     return world * flops_per_step * steps / (max_ms / 1e3) / 1e12
 
 
+# Algorithmic work of what each timed scope computes, per launch (fused
+# schedule: one launch covers all ring steps), in products of 2*d FLOPs per
+# (query head, allowed pair).  ra_tc_bwd is the fused backward: the key-side
+# kernel (S^T, dP^T, dV, dK) and the query-side kernel (S, dP, dQ) running
+# concurrently on two streams under one timing scope.
+PRODUCTS = {"ra_tc_fwd": 2, "ra_simt_fwd": 2,     # S, PV
+            "ra_tc_bwd": 7,                       # both backward kernels
+            "ra_tc_bwd_dkdv": 4,                  # S^T, dP^T, dV, dK
+            "ra_tc_bwd_dq": 3,                    # S, dP, dQ
+            "ra_simt_bwd": 5}
+KERNELS_PER_SCOPE = {"ra_tc_bwd": 2}
+
+
 def kernel_traffic(name):
     """DRAM bytes per launch of `name` from the committed ncu summary, or None
-    when there is none or the kernel's source changed since it was captured."""
+    when there is none or a source of the kernel changed since it was captured.
+    An entry lists every source file it depends on with its sha256 (the
+    concurrent backward pair lists both kernels' files and sums their bytes)."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -191,15 +206,16 @@ def kernel_traffic(name):
     except (OSError, ValueError):
         return None
     ent = tab.get(name)
-    if not ent:
+    if not ent or not ent.get("sources"):
         return None
-    src = os.path.join(ROOT, "context_varlen_ring_gb300", "csrc", ent["source"])
-    try:
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-    except OSError:
-        return None
-    return ent["dram_bytes_per_launch"] if digest == ent["source_sha256"] else None
+    for src, want in ent["sources"].items():
+        try:
+            with open(os.path.join(ROOT, "context_varlen_ring_gb300", "csrc", src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != want:
+                    return None
+        except OSError:
+            return None
+    return ent["dram_bytes_per_launch"]
 
 
 def fwd_configs(args, ra, torch):
@@ -369,7 +385,9 @@ def main():
     for x in kernels.values():
         x["share"] = x["ms_total"] / total_kernel_ms
     # kernels only (the table upload is a copy, profiled alongside)
-    gpu_launches = sum(x["launches"] for nm, x in kernels.items() if not nm.endswith("_upload"))
+    # (the fused backward's scope covers its two concurrent kernels)
+    gpu_launches = sum(x["launches"] * KERNELS_PER_SCOPE.get(nm, 1) for nm, x in kernels.items()
+                       if not nm.endswith("_upload"))
     peak_burst, peak_sust, hbm, peak_src = peaks()
     dominant = max(kernels, key=lambda n: kernels[n]["ms_total"]) if kernels else None
     roof = None
@@ -378,11 +396,7 @@ def main():
         # algorithmic work of what each kernel computes, per launch (fused schedule:
         # one launch covers all ring steps): 2*d FLOPs per (query head, allowed pair)
         # for each product it forms
-        products = {"ra_tc_fwd": 2, "ra_simt_fwd": 2,            # S, PV
-                    "ra_tc_bwd_dkdv": 4,                         # S^T, dP^T, dV, dK
-                    "ra_tc_bwd_dq": 3,                           # S, dP, dQ
-                    "ra_simt_bwd": 5}
-        n_prod = products.get(dominant)
+        n_prod = PRODUCTS.get(dominant)
         if n_prod is not None:
             flops = n_prod * 2 * d * hq * pairs
             ach = flops / per_launch_s / 1e12
@@ -396,8 +410,8 @@ def main():
                     "frac": None, "traffic": kernel_traffic(dominant)}
     all_roof = {}
     for nm, x in kernels.items():
-        n_prod = {"ra_tc_fwd": 2, "ra_tc_bwd_dkdv": 4, "ra_tc_bwd_dq": 3}.get(nm)
-        if n_prod:
+        n_prod = PRODUCTS.get(nm)
+        if n_prod and nm.startswith("ra_tc"):
             tf = n_prod * 2 * d * hq * pairs / (x["ms_per_launch"] / 1e3) / 1e12
             all_roof[nm] = {"tflops": tf, "frac_of_sustained": tf / peak_sust}
 

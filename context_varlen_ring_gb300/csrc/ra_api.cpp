@@ -122,6 +122,42 @@ const void *plan_upload_src(RingPlan &plan) {
     return plan.pinned ? plan.pinned : static_cast<const void *>(plan.dev.blob.data());
 }
 
+// A second stream per device, with a fork and a join event, for the query-side
+// backward pass to run beside the key-side pass: both read the same inputs and
+// write disjoint outputs.  The persistent dQ grid is issued first and holds one
+// CTA per SM; each key-side CTA takes an SM as soon as the dQ CTA there
+// retires, so the uneven ends of the dQ CTAs leave no SM idle.  The mutex is
+// held across a whole fork/join so that another thread cannot re-record the
+// events between a record and its wait.
+struct SideStream {
+    cudaStream_t st = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+
+SideStream *side_stream_locked() {
+    static SideStream ss[128];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    SideStream &s = ss[dev];
+    if (!s.st) {
+        cudaStream_t st = nullptr;
+        cudaEvent_t a = nullptr, b = nullptr;
+        if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&b, cudaEventDisableTiming) != cudaSuccess) {
+            (void)cudaGetLastError();
+            if (st) (void)cudaStreamDestroy(st);
+            if (a) (void)cudaEventDestroy(a);
+            return nullptr;
+        }
+        s.st = st;
+        s.fork = a;
+        s.join = b;
+    }
+    return &s;
+}
+
 // Host record of what the last ring forward left in each workspace (the
 // reserve space a backward may reuse with RA_BWD_FWD_RESERVE).
 struct ReserveRec {
@@ -771,17 +807,28 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
             a.dk = dk;
             a.dv = dv;
             a.out_mode = grad_dtype == RA_BF16 ? 0 : 1;
-            {
-                ProfScope ps("ra_tc_bwd_dkdv", s);
-                RA_CUDA(launch_tc_bwd(a, s), "tensor-core dK/dV launch");
-            }
             qa.t0 = 0;
             qa.t1 = cp;
             qa.dq = dq;  // complete per query tile: written once in the gradient dtype
             qa.out_mode = grad_dtype == RA_BF16 ? 0 : 1;
-            {
-                ProfScope ps("ra_tc_bwd_dq", s);
+            std::lock_guard<std::mutex> lk(g_side_mu);
+            SideStream *side = side_stream_locked();
+            if (side) {
+                // one timing scope over both kernels: they share the SMs
+                ProfScope ps("ra_tc_bwd", s);
+                RA_CUDA(cudaEventRecord(side->fork, s), "fork record");
                 RA_CUDA(launch_tc_dq(qa, s), "tensor-core dQ launch");
+                RA_CUDA(cudaStreamWaitEvent(side->st, side->fork, 0), "fork wait");
+                RA_CUDA(launch_tc_bwd(a, side->st), "tensor-core dK/dV launch");
+                RA_CUDA(cudaEventRecord(side->join, side->st), "join record");
+                RA_CUDA(cudaStreamWaitEvent(s, side->join, 0), "join wait");
+            } else {
+                {
+                    ProfScope ps("ra_tc_bwd_dq", s);
+                    RA_CUDA(launch_tc_dq(qa, s), "tensor-core dQ launch");
+                }
+                ProfScope ps("ra_tc_bwd_dkdv", s);
+                RA_CUDA(launch_tc_bwd(a, s), "tensor-core dK/dV launch");
             }
         } else {
             a.dk = dka;

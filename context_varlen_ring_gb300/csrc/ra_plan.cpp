@@ -211,8 +211,23 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
         return a.cost > b.cost;
     };
     std::stable_sort(tp.items.begin(), tp.items.end(), by_cost);
-    std::stable_sort(tp.bitems.begin(), tp.bitems.end(), by_cost);
     std::stable_sort(tp.qitems.begin(), tp.qitems.end(), by_cost);
+    // Key-side items: document major (heaviest document first), then KV
+    // head, then longest first.  A long document's first KV tile sees every
+    // query tile of the document, more work than one head's share of an SM,
+    // so under the head-major order the last head's heaviest items start
+    // late and leave the other SMs idle at the end; here they start in the
+    // first waves and the launch ends on the shortest documents.  The CTAs
+    // resident at once read the Q and dO of one or two (document, head)
+    // pairs, a smaller set than one head of every document.
+    std::vector<int32_t> doc_max(B, 0);
+    for (const WorkItem &w : tp.bitems) doc_max[w.b] = std::max(doc_max[w.b], w.cost);
+    std::stable_sort(tp.bitems.begin(), tp.bitems.end(), [&](const WorkItem &a, const WorkItem &b) {
+        if (doc_max[a.b] != doc_max[b.b]) return doc_max[a.b] > doc_max[b.b];
+        if (a.b != b.b) return a.b < b.b;
+        if (a.g != b.g) return a.g < b.g;
+        return a.cost > b.cost;
+    });
 }
 
 ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, TilePlan &tp) {
