@@ -21,7 +21,8 @@
 //    N=128) computes S = Q K^T (both operands in shared memory) and
 //    O += P V with P read from TMEM, so the PV product only streams V from
 //    shared memory (the N=128 SS product alone uses the whole shared-memory
-//    read port); the MMA is issued by one thread.
+//    read port).  The MMA warp runs converged and one elected lane issues
+//    each instruction, which keeps the issue cost under the tensor time.
 //  * TMEM: S0, S1, O0, O1 (4 x 128 fp32 columns = all 512); P (bf16) is
 //    written over the first 64 columns of its S.
 //  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
@@ -109,7 +110,7 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_s, uint32_t 
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (uint32_t)(ks >> 2) * kHalf + (uint32_t)(ks & 3) * 32u;
-        tc_mma_ss(d_tmem, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k_s + off, 16, 1024), idesc, ks > 0);
+        tc_mma_ss_w(d_tmem, sdesc_sw128(q_s + off, 16, 1024), sdesc_sw128(k_s + off, 16, 1024), idesc, ks > 0);
     }
 }
 
@@ -120,7 +121,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
         const uint32_t boff = (uint32_t)ks * 2048u;  // 16 key rows of 128 B
-        tc_mma_ts(d_tmem, p_tmem + 8u * ks, sdesc_sw128(v_s + boff, kHalf, 1024), idesc,
+        tc_mma_ts_w(d_tmem, p_tmem + 8u * ks, sdesc_sw128(v_s + boff, kHalf, 1024), idesc,
                   (accumulate || ks > 0) ? 1u : 0u);
     }
 }
@@ -297,88 +298,96 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             }
         } else if (warp == 1) {
             // -------------------------------------------- MMA issuer
-            if (lane == 0) {
-                const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-                const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);
-                const uint32_t q0s = base_s + kOffQ0, q1s = base_s + kOffQ1;
-                const uint32_t kvs = base_s + kOffKV;
-                const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-                bool ok = mbar_wait(q_full, 0, wc);
+            // The whole warp runs this loop converged and one elected lane
+            // issues each tcgen05 instruction (the _w helpers).
+            const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+            const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);
+            const uint32_t q0s = base_s + kOffQ0, q1s = base_s + kOffQ1;
+            const uint32_t kvs = base_s + kOffKV;
+            const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+            auto read_info_w = [&](uint32_t jt, int4 &e) -> bool {
+                const uint32_t slot = jt % kRing;
+                if (!mbar_wait_warp(info_full + slot, (jt / kRing) & 1u, wc)) return false;
+                e = ring[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(info_empty + slot);
+                return true;
+            };
+            bool ok = mbar_wait_warp(q_full, 0, wc);
+            tc_fence_after();
+            int4 e;
+            ok = ok && read_info_w(0, e);
+            bool have = ok && !(e.x & 16);
+            int c0 = e.x & 3, c1 = (e.x >> 2) & 3;
+            uint32_t np0 = 0, np1 = 0;  // PVs issued per query tile
+            if (have) {
+                if (!mbar_wait_warp(kv_full + 0, 0, wc)) ok = false;
                 tc_fence_after();
-                int4 e;
-                ok = ok && read_info(0, e);
-                bool have = ok && !(e.x & 16);
-                int c0 = e.x & 3, c1 = (e.x >> 2) & 3;
-                uint32_t np0 = 0, np1 = 0;  // PVs issued per query tile
-                if (have) {
-                    if (!mbar_wait(kv_full + 0, 0, wc)) ok = false;
-                    tc_fence_after();
-                    if (ok) {
-                        if (c0 != kSkip) {
-                            issue_s(tS0, q0s, kvs, idesc_s);
-                            tc_commit(s_full + 0);
-                        }
-                        if (c1 != kSkip) {
-                            issue_s(tS1, q1s, kvs, idesc_s);
-                            tc_commit(s_full + 1);
-                        }
-                        tc_commit(kv_empty + 0);
+                if (ok) {
+                    if (c0 != kSkip) {
+                        issue_s(tS0, q0s, kvs, idesc_s);
+                        tc_commit_w(s_full + 0);
                     }
+                    if (c1 != kSkip) {
+                        issue_s(tS1, q1s, kvs, idesc_s);
+                        tc_commit_w(s_full + 1);
+                    }
+                    tc_commit_w(kv_empty + 0);
                 }
-                uint32_t j = 0;
-                while (ok && have) {
-                    const int cc0 = c0, cc1 = c1;
-                    int4 en;
-                    if (!read_info(j + 1, en)) break;
-                    const bool have_next = !(en.x & 16);
-                    const int nc0 = en.x & 3, nc1 = (en.x >> 2) & 3;
-                    const uint32_t vidx = 2 * j + 1, vslot = vidx % kSlots;
-                    if (!mbar_wait(kv_full + vslot, (vidx / kSlots) & 1u, wc)) break;
-                    tc_fence_after();
-                    const uint32_t vs = kvs + vslot * kTile;
-                    const uint32_t kload = 2 * j + 2, kslot = kload % kSlots;
-                    const uint32_t ks = kvs + kslot * kTile;
-                    if (cc0 != kSkip) {
-                        if (!mbar_wait(p_ready + 0, np0 & 1u, wc)) break;
-                        tc_fence_after();
-                        issue_pv(tO0, tS0, vs, idesc_o, np0 > 0);
-                        tc_commit(o_done + 0);
-                        ++np0;
-                    }
-                    if (have_next) {
-                        if (!mbar_wait(kv_full + kslot, (kload / kSlots) & 1u, wc)) break;
-                        tc_fence_after();
-                        if (nc0 != kSkip) {
-                            issue_s(tS0, q0s, ks, idesc_s);
-                            tc_commit(s_full + 0);
-                        }
-                    }
-                    if (cc1 != kSkip) {
-                        if (!mbar_wait(p_ready + 1, np1 & 1u, wc)) break;
-                        tc_fence_after();
-                        issue_pv(tO1, tS1, vs, idesc_o, np1 > 0);
-                        tc_commit(o_done + 1);
-                        ++np1;
-                    }
-                    if (have_next) {
-                        if (nc1 != kSkip) {
-                            issue_s(tS1, q1s, ks, idesc_s);
-                            tc_commit(s_full + 1);
-                        }
-                        tc_commit(kv_empty + kslot);
-                    }
-                    tc_commit(kv_empty + vslot);
-                    if (!have_next) break;
-                    c0 = nc0;
-                    c1 = nc1;
-                    ++j;
-                }
-                // every MMA issued must have completed before TMEM is released
-                tc_commit(mma_done);
-                volatile int local_abort = 0;
-                const WaitCtl drain{&local_abort, p.status, p.budget_ns};
-                (void)mbar_wait(mma_done, 0, drain);
             }
+            uint32_t j = 0;
+            while (ok && have) {
+                const int cc0 = c0, cc1 = c1;
+                int4 en;
+                if (!read_info_w(j + 1, en)) break;
+                const bool have_next = !(en.x & 16);
+                const int nc0 = en.x & 3, nc1 = (en.x >> 2) & 3;
+                const uint32_t vidx = 2 * j + 1, vslot = vidx % kSlots;
+                if (!mbar_wait_warp(kv_full + vslot, (vidx / kSlots) & 1u, wc)) break;
+                tc_fence_after();
+                const uint32_t vs = kvs + vslot * kTile;
+                const uint32_t kload = 2 * j + 2, kslot = kload % kSlots;
+                const uint32_t ks = kvs + kslot * kTile;
+                if (cc0 != kSkip) {
+                    if (!mbar_wait_warp(p_ready + 0, np0 & 1u, wc)) break;
+                    tc_fence_after();
+                    issue_pv(tO0, tS0, vs, idesc_o, np0 > 0);
+                    tc_commit_w(o_done + 0);
+                    ++np0;
+                }
+                if (have_next) {
+                    if (!mbar_wait_warp(kv_full + kslot, (kload / kSlots) & 1u, wc)) break;
+                    tc_fence_after();
+                    if (nc0 != kSkip) {
+                        issue_s(tS0, q0s, ks, idesc_s);
+                        tc_commit_w(s_full + 0);
+                    }
+                }
+                if (cc1 != kSkip) {
+                    if (!mbar_wait_warp(p_ready + 1, np1 & 1u, wc)) break;
+                    tc_fence_after();
+                    issue_pv(tO1, tS1, vs, idesc_o, np1 > 0);
+                    tc_commit_w(o_done + 1);
+                    ++np1;
+                }
+                if (have_next) {
+                    if (nc1 != kSkip) {
+                        issue_s(tS1, q1s, ks, idesc_s);
+                        tc_commit_w(s_full + 1);
+                    }
+                    tc_commit_w(kv_empty + kslot);
+                }
+                tc_commit_w(kv_empty + vslot);
+                if (!have_next) break;
+                c0 = nc0;
+                c1 = nc1;
+                ++j;
+            }
+            // every MMA issued must have completed before TMEM is released
+            tc_commit_w(mma_done);
+            volatile int local_abort = 0;
+            const WaitCtl drain{&local_abort, p.status, p.budget_ns};
+            (void)mbar_wait_warp(mma_done, 0, drain);
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
