@@ -27,11 +27,13 @@
 //    matching 64-row slice of the contraction.  A group's chain
 //    S^T_h(i) -> P^T_h(i) -> dV_h(i) -> S^T_h(i+1) thus holds half a tile
 //    of products, and the two groups' chains interleave.
-//  * One thread issues a tcgen05.mma only about every 45-60 cycles, so two
-//    warps issue, one per TMEM reuse chain: warp 1 dV_h(i) then S^T_h(i+1)
-//    (which overwrites P^T_h(i)), warp 3 dK_h(i) then dP^T_h(i+1) (which
-//    overwrites dS^T_h(i)); each chain is ordered by the tensor pipe's
-//    in-order execution of one thread's products.
+//  * Two warps issue, one per TMEM reuse chain: warp 1 dV_h(i) then
+//    S^T_h(i+1) (which overwrites P^T_h(i)), warp 3 dK_h(i) then dP^T_h(i+1)
+//    (which overwrites dS^T_h(i)); each chain is ordered by the tensor
+//    pipe's in-order execution of one issuer's products.  Each issuer warp
+//    runs converged and one elected lane issues: from one lane of a
+//    divergent branch an MMA costs 45-60 cycles to issue, above the 32
+//    tensor cycles of an N=64 product.
 //  * TMEM: dK [0,128), dV [128,256), S^T then P^T [256,384), dP^T then dS^T
 //    [384,512).  Two compute warpgroups split the 128 query columns; each
 //    packs its P^T / dS^T (bf16) over the first 32 of its own 64 columns.
@@ -234,8 +236,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             for (uint32_t x = (n > 2 ? n - 2 : 0); x < n; ++x)
                 (void)mbar_wait(st_full + (x & 1u), (x >> 1) & 1u, drain);
         }
-    } else if ((warp == 1 || warp == 3) && lane == 0) {
+    } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------ MMA issuers
+        // Each issuer warp runs converged; one elected lane issues (_w helpers).
         const uint32_t id_n64 = idesc_bf16_f32(128, 64, 0, 0);  // A, B K-major, N = 64 queries
         const uint32_t id_ts = idesc_bf16_f32(128, 128, 0, 1);  // A in TMEM, B MN-major
         auto is_end = [&](uint32_t st) {
@@ -256,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             const uint64_t b0 = sdesc_sw128(chain_b + st * kTile + 8192u * h, 16, 1024);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                tc_mma_ss(chain_d + 64u * h, chain_a + kstep(ks), b0 + kstep(ks), id_n64, ks > 0);
-            tc_commit(chain_full + h);
+                tc_mma_ss_w(chain_d + 64u * h, chain_a + kstep(ks), b0 + kstep(ks), id_n64, ks > 0);
+            tc_commit_w(chain_full + h);
         };
         // dV / dK += P^T_h / dS^T_h (TMEM, group h's columns) x rows [64h, 64h+64)
         // of dO / Q (MN-major: d contiguous)
@@ -265,9 +268,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             const uint64_t b0 = sdesc_sw128(grad_b + st * kTile + 8192u * h, kHalf, 1024);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                tc_mma_ts(grad_d, chain_d + 64u * h + 8u * k, b0 + ((2048u * k) >> 4), id_ts, (acc || k > 0));
+                tc_mma_ts_w(grad_d, chain_d + 64u * h + 8u * k, b0 + ((2048u * k) >> 4), id_ts, (acc || k > 0));
         };
-        bool ok = mbar_wait(kv_full, 0, wc) && mbar_wait(st_full + 0, 0, wc);
+        bool ok = mbar_wait_warp(kv_full, 0, wc) && mbar_wait_warp(st_full + 0, 0, wc);
         tc_fence_after();
         const bool have = ok && !is_end(0);
         if (have) {
@@ -276,25 +279,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
         }
         for (uint32_t i = 0; ok && have; ++i) {
             const uint32_t st = i & 1u, nst = (i + 1) & 1u;
-            if (!mbar_wait(ready + 0, i & 1u, wc)) break;
+            if (!mbar_wait_warp(ready + 0, i & 1u, wc)) break;
             tc_fence_after();
             grad_mma(0, st, i > 0);
-            if (!mbar_wait(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
+            if (!mbar_wait_warp(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
             tc_fence_after();
             const bool next_end = is_end(nst);
             // half 0 of the next tile overwrites P^T_0 / dS^T_0 after the product above (in order)
             if (!next_end) chain_mma(0, nst);
-            if (!mbar_wait(ready + 1, i & 1u, wc)) break;
+            if (!mbar_wait_warp(ready + 1, i & 1u, wc)) break;
             tc_fence_after();
             grad_mma(1, st, true);
-            tc_commit(st_empty + st);  // this issuer no longer reads the stage
+            tc_commit_w(st_empty + st);  // this issuer no longer reads the stage
             if (next_end) break;
             chain_mma(1, nst);
         }
-        tc_commit(mma_done);
+        tc_commit_w(mma_done);
         volatile int local_abort = 0;
         const WaitCtl drain{&local_abort, p.status, p.budget_ns};
-        (void)mbar_wait(mma_done, 0, drain);
+        (void)mbar_wait_warp(mma_done, 0, drain);
     } else if (warp >= 4) {
         // ------------------------------------------------ compute warpgroups
         // Group h (warps 4-7: 0, warps 8-11: 1) owns columns [64h, 64h+64) of

@@ -29,10 +29,12 @@
 //
 // dS has its own TMEM buffer, so dP(j+1) may start as soon as the compute
 // groups have loaded dP(j), and the only loop left between products is
-// dQ(j) -> (dS buffer free) -> store dS(j+1) -> dQ(j+1).  One thread issues
-// a tcgen05.mma only about every 45-60 cycles, close to the 64 cycles an
-// M=128 N=128 K=16 product runs, so three warps issue: warp 1 the S
-// products, warp 2 dP and warp 3 dQ.  Barrier phases count KV tiles (and
+// dQ(j) -> (dS buffer free) -> store dS(j+1) -> dQ(j+1).  Three warps
+// issue, one per product chain: warp 1 the S products, warp 2 dP and warp 3
+// dQ, so no chain waits behind another's barrier.  Each issuer warp runs
+// converged and one elected lane issues (from one lane of a divergent
+// branch an MMA costs 45-60 cycles to issue, close to the 64 cycles an
+// M=128 N=128 K=16 product runs).  Barrier phases count KV tiles (and
 // items) across the whole walk.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -281,17 +283,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 for (uint32_t x = (u > kSlots ? u - kSlots : 0); x < u; ++x)
                     (void)mbar_wait(kv_full + (x % kSlots), (x / kSlots) & 1u, drain);
             }
-        } else if (lane == 0) {
+        } else {
             // -------------------------------------------- MMA issuers (warps 1-3)
+            // Each issuer warp runs converged; one elected lane issues each
+            // tcgen05 instruction (the _w helpers) and lane 0 arrives.
             constexpr uint32_t id_s = idesc_bf16_f32(128, 128, 0, 0);  // S, dP: A and B K-major
             constexpr uint32_t id_q = idesc_bf16_f32(128, 128, 0, 1);  // dQ: B MN-major
             // K-major SW128 operand: 16-element k-step ks at (ks / 4) * kHalf + (ks % 4) * 32
             auto kstep = [](int ks) -> uint32_t { return (((ks >> 2) * kHalf + (ks & 3) * 32u) >> 4); };
             auto kv_par = [](uint32_t u) { return (u / kSlots) & 1u; };
             auto wait = [&](uint64_t *bar, uint32_t par) -> bool {
-                const bool r = mbar_wait(bar, par, wc);
+                const bool r = mbar_wait_warp(bar, par, wc);
                 tc_fence_after();
                 return r;
+            };
+            auto read_info_w = [&](uint32_t ri_, int4 &e) -> bool {
+                const uint32_t slot = ri_ % kRing;
+                if (!mbar_wait_warp(info_full + slot, (ri_ / kRing) & 1u, wc)) return false;
+                e = ring[slot];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(info_empty + slot);
+                return true;
             };
             uint64_t *drain_bar = warp == 1 ? a_done : (warp == 2 ? b_done : z_done);
             uint32_t jg = 0, ri = 0;  // KV tiles and ring entries consumed so far
@@ -300,10 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 if (warp == 1) {
                     // S(j) = Q K(j)^T (Q from TMEM) once both groups have read S(j-1)
                     ok = wait(qc_ready, k & 1);
-                    mbar_arrive(x_ready);  // the next item's Q may now replace this one
+                    if (lane == 0) mbar_arrive(x_ready);  // the next item's Q may now replace this one
                     for (; ok;) {
                         int4 e;
-                        if (!read_info(ri++, e)) {
+                        if (!read_info_w(ri++, e)) {
                             ok = false;
                             break;
                         }
@@ -319,8 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         }
                         const uint64_t d0 = sdesc_sw128(base_s + kOffKV + (ku % kSlots) * kTile, 16, 1024);
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) tc_mma_ts(tS, tQ + 8u * ks, d0 + kstep(ks), id_s, ks > 0);
-                        tc_commit(s_full);
+                        for (int ks = 0; ks < 8; ++ks) tc_mma_ts_w(tS, tQ + 8u * ks, d0 + kstep(ks), id_s, ks > 0);
+                        tc_commit_w(s_full);
                         ++jg;
                     }
                 } else if (warp == 2) {
@@ -328,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     // this thread also stages dO: item 0's here, item k+1's once
                     // item k's last dP has read the buffer
                     auto load_do = [&](int kk) {
+                        if (lane != 0) return;
                         const int4 ia = __ldg(p.items + 2 * item_of(kk));
                         const int row0 = __ldg(&p.qtiles[2 * ia.x].x);
                         mbar_arrive_expect_tx(do_full, kTile);
@@ -339,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     const uint64_t a0 = sdesc_sw128(base_s + kOffDO, 16, 1024);
                     for (; ok;) {
                         int4 e;
-                        if (!read_info(ri++, e)) {
+                        if (!read_info_w(ri++, e)) {
                             ok = false;
                             break;
                         }
@@ -355,14 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         }
                         const uint64_t d0 = sdesc_sw128(base_s + kOffKV + (vu % kSlots) * kTile, 16, 1024);
 #pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) tc_mma_ss(tDP, a0 + kstep(ks), d0 + kstep(ks), id_s, ks > 0);
-                        tc_commit(dp_full);
-                        tc_commit(kv_empty + vu % kSlots);  // V only feeds dP
+                        for (int ks = 0; ks < 8; ++ks) tc_mma_ss_w(tDP, a0 + kstep(ks), d0 + kstep(ks), id_s, ks > 0);
+                        tc_commit_w(dp_full);
+                        tc_commit_w(kv_empty + vu % kSlots);  // V only feeds dP
                         ++jg;
                     }
-                    if (ok) tc_commit(do_empty);  // this item's dO is no longer read
+                    if (ok) tc_commit_w(do_empty);  // this item's dO is no longer read
                     if (ok && k + 1 < n_my) {
-                        ok = mbar_wait(do_empty, k & 1, wc);
+                        ok = mbar_wait_warp(do_empty, k & 1, wc);
                         if (ok) load_do(k + 1);
                     }
                 } else {
@@ -372,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     uint32_t jl = 0;
                     for (; ok;) {
                         int4 e;
-                        if (!read_info(ri++, e)) {
+                        if (!read_info_w(ri++, e)) {
                             ok = false;
                             break;
                         }
@@ -387,22 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                             }
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                tc_mma_ts(tDQ, tDS + 32u * h + 8u * kk, d0 + ((8192u * h + 2048u * kk) >> 4), id_q,
+                                tc_mma_ts_w(tDQ, tDS + 32u * h + 8u * kk, d0 + ((8192u * h + 2048u * kk) >> 4), id_q,
                                           (jl > 0 || h > 0 || kk > 0));
                         }
                         if (!ok) break;
-                        tc_commit(dq_done);
-                        tc_commit(kv_empty + kslot);  // K(j) done (S(j) finished before dS(j))
+                        tc_commit_w(dq_done);
+                        tc_commit_w(kv_empty + kslot);  // K(j) done (S(j) finished before dS(j))
                         ++jg;
                         ++jl;
                     }
-                    if (ok) tc_commit(mma_done);  // this item's dQ is complete
+                    if (ok) tc_commit_w(mma_done);  // this item's dQ is complete
                 }
             }
-            tc_commit(drain_bar);
+            tc_commit_w(drain_bar);
             volatile int local_abort = 0;
             const WaitCtl drain{&local_abort, p.status, p.budget_ns};
-            (void)mbar_wait(drain_bar, 0, drain);
+            (void)mbar_wait_warp(drain_bar, 0, drain);
         }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
