@@ -412,6 +412,7 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
         a.kvtiles = tb + dt.o_kt;
         a.kv_off = reinterpret_cast<const int32_t *>(tb + dt.o_kvoff);
         a.items = tb + dt.o_items;
+        a.sched = reinterpret_cast<int *>(const_cast<uint8_t *>(tb) + dt.o_sched);
         a.n_items = dt.n_items;
         a.cp = 1;
         a.B = nseg;
@@ -604,6 +605,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
             a.kvtiles = tab + dt.o_kt;
             a.kv_off = reinterpret_cast<const int32_t *>(tab + dt.o_kvoff);
             a.items = tab + dt.o_items;
+            a.sched = reinterpret_cast<int *>(tab + dt.o_sched);
             a.n_items = dt.n_items;
             a.cp = cp;
             a.B = B;

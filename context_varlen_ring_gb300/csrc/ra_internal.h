@@ -96,6 +96,9 @@ struct DeviceTables {
     std::vector<uint8_t> blob;
     size_t o_perm = 0, o_qt = 0, o_kt = 0, o_qoff = 0, o_kvoff = 0, o_items = 0,
            o_bitems = 0, o_qitems = 0, o_cul = 0, o_off = 0;
+    // Work counters of the persistent kernels (uploaded as zeros; a kernel
+    // returns its counter to zero when it finishes): [0, 2) forward.
+    size_t o_sched = 0;
     int n_items = 0, n_bitems = 0, n_qitems = 0;
 };
 void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt);

@@ -111,6 +111,7 @@ struct TcFwdArgs {
     const void *qtiles, *kvtiles;      // Tile records (two int4 each)
     const int32_t *kv_off;             // [cp*(B+1)+1]
     const void *items;                 // WorkItem records
+    int *sched;                        // [2] work counter, zero before the first launch
     int n_items;
     int cp, B;
     int t0, t1;                        // >= 0: override every item's step range

@@ -300,6 +300,7 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
     dt.o_qitems = take(tp ? tp->qitems.size() * sizeof(WorkItem) : 0);
     dt.o_cul = take(zp ? zp->cu_local.size() * 4 : 0);
     dt.o_off = take(zp ? zp->off.size() * 4 : 0);
+    dt.o_sched = take(64);
     dt.blob.assign(o, 0);
     auto put = [&](size_t at, const void *src, size_t bytes) {
         if (bytes) std::memcpy(dt.blob.data() + at, src, bytes);

@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -70,6 +71,7 @@ struct FwdParams {
     CUtensorMap tmQ, tmK, tmV;
     const int4 *qtiles, *kvtiles, *items;
     const int *kv_off;
+    int *sched;  // [2]: next item to claim, CTAs finished (zero between launches)
     int n_items, cp, B, G, log2G, Hq;
     int t0, t1, causal, out_mode;
     float scale_log2;
@@ -133,31 +135,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     uint8_t *base = smem_raw + (base_s - raw_s);
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + kOffBar);
-    uint64_t *q_full = bars + 0;
-    uint64_t *kv_full = bars + 1;      // [kSlots]
-    uint64_t *kv_empty = bars + 6;     // [kSlots]
-    uint64_t *s_full = bars + 11;      // [2] S of a query tile computed
-    uint64_t *p_ready = bars + 13;     // [2] P of a query tile written to TMEM (128 arrivals)
-    uint64_t *o_done = bars + 15;      // [2] PV of a query tile done
-    uint64_t *mma_done = bars + 17;
-    uint64_t *info_full = bars + 18;   // [kRing] descriptor published
-    uint64_t *info_empty = bars + 26;  // [kRing] descriptor read by every consumer
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 34);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 35);
-    int4 *ring = reinterpret_cast<int4 *>(bars + 36);  // [kRing]
+    uint64_t *q_full = bars + 0;       // Q tiles of an item landed (one phase per item)
+    uint64_t *q_empty = bars + 1;      // the item's last S products are done with the Q buffers
+    uint64_t *kv_full = bars + 2;      // [kSlots]
+    uint64_t *kv_empty = bars + 7;     // [kSlots]
+    uint64_t *s_full = bars + 12;      // [2] S of a query tile computed
+    uint64_t *p_ready = bars + 14;     // [2] P of a query tile written to TMEM (128 arrivals)
+    uint64_t *o_done = bars + 16;      // [2] PV of a query tile done
+    uint64_t *mma_done = bars + 18;
+    uint64_t *info_full = bars + 19;   // [kRing] descriptor published
+    uint64_t *info_empty = bars + 27;  // [kRing] descriptor read by every consumer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 35);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 36);
+    int4 *ring = reinterpret_cast<int4 *>(bars + 38);  // [kRing]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const int4 ia = __ldg(p.items + 2 * blockIdx.x), ib = __ldg(p.items + 2 * blockIdx.x + 1);
-    const int qt0 = ia.x, qt1 = ia.y, g = ia.z, r = ia.w, b = ib.x;
-    const int t0 = p.t0 >= 0 ? p.t0 : ib.y;
-    const int t1 = p.t0 >= 0 ? p.t1 : ib.z;
-    const bool has1 = qt1 >= 0;
-
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(kv_full + i, 1);
             mbar_init(kv_empty + i, 1);
@@ -170,8 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         mbar_init(mma_done, 1);
         for (int i = 0; i < kRing; ++i) {
             mbar_init(info_full + i, 1);
-            // consumers: the MMA thread and every softmax thread in use
-            mbar_init(info_empty + i, 1 + (has1 ? 256 : 128));
+            mbar_init(info_empty + i, 1 + 256);  // the MMA warp and every softmax thread
         }
         fence_mbar_init();
     }
@@ -185,9 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const uint32_t tmem = *tmem_slot;
     const WaitCtl wc{abort_flag, p.status, p.budget_ns};
 
-    // Visited-tile descriptor published by the producer, one per KV tile in
-    // ring order: x = class0 | class1 << 2 | end << 4, y = len | split << 16,
-    // z = pos0, w = pos1.
+    // Descriptor ring, one entry per step of the walk, in order: an item
+    // header (x = kHead, y = item index), one entry per visited KV tile
+    // (x = class0 | class1 << 2, y = len | split << 16, z = pos0, w = pos1),
+    // an item end (x = kEnd), and after the last item x = kDone.
+    constexpr int kEnd = 1 << 4, kHead = 1 << 5, kDone = 1 << 6;
     auto read_info = [&](uint32_t jt, int4 &e) -> bool {
         const uint32_t slot = jt % kRing;
         if (!mbar_wait(info_full + slot, (jt / kRing) & 1u, wc)) return false;
@@ -196,192 +195,272 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         return true;
     };
 
-    // Register split: 128 x 56 (producer/MMA group) + 256 x 224 (softmax
-    // groups) = 64512 = the 384 x 168 registers the CTA is launched with.
+    // Register split: 128 x 80 (producer/MMA group) + 256 x 200 (softmax
+    // groups) = 61440, within the 384 x 168 = 64512 registers the CTA is
+    // launched with.
     if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
         if (warp == 0) {
-            // -------------------------------------------- TMA producer
-            // The whole warp walks the KV tile table of this item (32 records
-            // per load), classifies each tile against both query tiles, and
-            // lane 0 publishes the visited ones and loads their K and V.
-            const int4 qa0 = __ldg(p.qtiles + 2 * qt0), qb0 = __ldg(p.qtiles + 2 * qt0 + 1);
-            const QInfo q0{qa0.y, qb0.y, qb0.z};
-            QInfo q1{0, 0, 0};
-            int qrow1 = 0;
-            if (has1) {
-                const int4 qa1 = __ldg(p.qtiles + 2 * qt1), qb1 = __ldg(p.qtiles + 2 * qt1 + 1);
-                q1 = QInfo{qa1.y, qb1.y, qb1.z};
-                qrow1 = qa1.x;
-            }
-            const int hq0 = g * p.G;
+            // -------------------------------------------- producer
+            // Claims items from the launch's work counter (the items are
+            // sorted longest first within a KV head, so the claims balance
+            // the SMs the way a hardware block scheduler would), loads each
+            // item's Q tiles once its predecessor's last S products are
+            // done, and walks the KV tile table of the item (32 records per
+            // load): the whole warp classifies each tile against both query
+            // tiles, and lane 0 publishes the visited ones and loads their
+            // K and V through the ring.
+            uint32_t u = 0, jt = 0;
+            int ok = 1, n_q = 0;
+            auto publish = [&](int4 v) -> int {  // lane 0
+                const uint32_t e = jt % kRing;
+                if (!mbar_wait(info_empty + e, ((jt / kRing) & 1u) ^ 1u, wc)) return 0;
+                ring[e] = v;
+                mbar_arrive(info_full + e);
+                return 1;
+            };
             if (lane == 0) {
                 tma_prefetch_desc(&p.tmQ);
                 tma_prefetch_desc(&p.tmK);
                 tma_prefetch_desc(&p.tmV);
-                mbar_arrive_expect_tx(q_full, (has1 ? 2u : 1u) * kTile);
-                tma_load_3d(base + kOffQ0, &p.tmQ, q_full, 0, hq0, qa0.x);
-                tma_load_3d(base + kOffQ0 + kHalf, &p.tmQ, q_full, 64, hq0, qa0.x);
-                if (has1) {
-                    tma_load_3d(base + kOffQ1, &p.tmQ, q_full, 0, hq0, qrow1);
-                    tma_load_3d(base + kOffQ1 + kHalf, &p.tmQ, q_full, 64, hq0, qrow1);
-                }
             }
-            uint32_t u = 0, jt = 0;
-            int ok = 1;
-            for (int t = t0; t < t1 && ok; ++t) {
-                int s = (r - t) % p.cp;
-                if (s < 0) s += p.cp;
-                const int o = s * (p.B + 1) + b;
-                const int lo = __ldg(p.kv_off + o), hi = __ldg(p.kv_off + o + 1);
-                for (int base_idx = lo; base_idx < hi && ok; base_idx += 32) {
-                    const int idx = base_idx + lane;
-                    int4 ka = make_int4(0, 0, 0, 0), kb = make_int4(0, 0, 0, 0);
-                    int c0 = kSkip, c1 = kSkip;
-                    if (idx < hi) {
-                        ka = __ldg(p.kvtiles + 2 * idx);
-                        kb = __ldg(p.kvtiles + 2 * idx + 1);
-                        c0 = classify_q(q0, ka.y, kb.y, kb.z, p.causal);
-                        c1 = has1 ? classify_q(q1, ka.y, kb.y, kb.z, p.causal) : kSkip;
+            for (int it = 0; ok; ++it) {
+                int item = 0;
+                if (lane == 0) item = atomicAdd(p.sched, 1);
+                item = __shfl_sync(0xffffffffu, item, 0);
+                if (item >= p.n_items) {
+                    if (lane == 0) ok = publish(make_int4(kDone, 0, 0, 0));
+                    ++jt;
+                    break;
+                }
+                const int4 ia = __ldg(p.items + 2 * item), ib = __ldg(p.items + 2 * item + 1);
+                const int qt0 = ia.x, qt1 = ia.y, g = ia.z, r = ia.w, b = ib.x;
+                const int t0 = p.t0 >= 0 ? p.t0 : ib.y;
+                const int t1 = p.t0 >= 0 ? p.t1 : ib.z;
+                const bool has1 = qt1 >= 0;
+                const int4 qa0 = __ldg(p.qtiles + 2 * qt0), qb0 = __ldg(p.qtiles + 2 * qt0 + 1);
+                const QInfo q0{qa0.y, qb0.y, qb0.z};
+                QInfo q1{0, 0, 0};
+                int qrow1 = 0;
+                if (has1) {
+                    const int4 qa1 = __ldg(p.qtiles + 2 * qt1), qb1 = __ldg(p.qtiles + 2 * qt1 + 1);
+                    q1 = QInfo{qa1.y, qb1.y, qb1.z};
+                    qrow1 = qa1.x;
+                }
+                const int hq0 = g * p.G;
+                // The Q buffers free up only when the previous item's last S
+                // products complete, so Q is staged in L2 now and copied
+                // after this item's first K and V loads (which need only
+                // ring slots) have been issued.
+                bool q_pending = true;
+                auto load_q = [&]() -> int {  // lane 0
+                    q_pending = false;
+                    if (it > 0 && !mbar_wait(q_empty, (it - 1) & 1u, wc)) return 0;
+                    mbar_arrive_expect_tx(q_full, (has1 ? 2u : 1u) * kTile);
+                    tma_load_3d(base + kOffQ0, &p.tmQ, q_full, 0, hq0, qa0.x);
+                    tma_load_3d(base + kOffQ0 + kHalf, &p.tmQ, q_full, 64, hq0, qa0.x);
+                    if (has1) {
+                        tma_load_3d(base + kOffQ1, &p.tmQ, q_full, 0, hq0, qrow1);
+                        tma_load_3d(base + kOffQ1 + kHalf, &p.tmQ, q_full, 64, hq0, qrow1);
                     }
-                    uint32_t vis = __ballot_sync(0xffffffffu, c0 != kSkip || c1 != kSkip);
-                    while (vis && ok) {
-                        const int src = __ffs(vis) - 1;
-                        vis &= vis - 1;
-                        const int row0 = __shfl_sync(0xffffffffu, ka.x, src);
-                        const int len = __shfl_sync(0xffffffffu, ka.y, src);
-                        const int split = __shfl_sync(0xffffffffu, ka.z, src);
-                        const int pos0 = __shfl_sync(0xffffffffu, ka.w, src);
-                        const int pos1 = __shfl_sync(0xffffffffu, kb.x, src);
-                        const int cc = __shfl_sync(0xffffffffu, c0 | (c1 << 2), src);
-                        if (lane == 0) {
-                            const uint32_t e = jt % kRing;
-                            if (!mbar_wait(info_empty + e, ((jt / kRing) & 1u) ^ 1u, wc)) ok = 0;
-                            if (ok) {
-                                ring[e] = make_int4(cc, len | (split << 16), pos0, pos1);
-                                mbar_arrive(info_full + e);
-                            }
-                            for (int kv = 0; kv < 2 && ok; ++kv, ++u) {
-                                const uint32_t slot = u % kSlots, ph = (u / kSlots) & 1u;
-                                if (!mbar_wait(kv_empty + slot, ph ^ 1u, wc)) {
-                                    ok = 0;
-                                    break;
-                                }
-                                uint8_t *dst = base + kOffKV + slot * kTile;
-                                const CUtensorMap *m = kv ? &p.tmV : &p.tmK;
-                                mbar_arrive_expect_tx(kv_full + slot, kTile);
-                                tma_load_3d(dst, m, kv_full + slot, 0, g, row0);
-                                tma_load_3d(dst + kHalf, m, kv_full + slot, 64, g, row0);
-                            }
+                    ++n_q;
+                    return 1;
+                };
+                if (lane == 0) {
+                    tma_prefetch_3d(&p.tmQ, 0, hq0, qa0.x);
+                    tma_prefetch_3d(&p.tmQ, 64, hq0, qa0.x);
+                    if (has1) {
+                        tma_prefetch_3d(&p.tmQ, 0, hq0, qrow1);
+                        tma_prefetch_3d(&p.tmQ, 64, hq0, qrow1);
+                    }
+                    ok = publish(make_int4(kHead, item, 0, 0));
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                ++jt;
+                for (int t = t0; t < t1 && ok; ++t) {
+                    int s = (r - t) % p.cp;
+                    if (s < 0) s += p.cp;
+                    const int o = s * (p.B + 1) + b;
+                    const int lo = __ldg(p.kv_off + o), hi = __ldg(p.kv_off + o + 1);
+                    for (int base_idx = lo; base_idx < hi && ok; base_idx += 32) {
+                        const int idx = base_idx + lane;
+                        int4 ka = make_int4(0, 0, 0, 0), kb = make_int4(0, 0, 0, 0);
+                        int c0 = kSkip, c1 = kSkip;
+                        if (idx < hi) {
+                            ka = __ldg(p.kvtiles + 2 * idx);
+                            kb = __ldg(p.kvtiles + 2 * idx + 1);
+                            c0 = classify_q(q0, ka.y, kb.y, kb.z, p.causal);
+                            c1 = has1 ? classify_q(q1, ka.y, kb.y, kb.z, p.causal) : kSkip;
                         }
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        ++jt;
+                        uint32_t vis = __ballot_sync(0xffffffffu, c0 != kSkip || c1 != kSkip);
+                        while (vis && ok) {
+                            const int src = __ffs(vis) - 1;
+                            vis &= vis - 1;
+                            const int row0 = __shfl_sync(0xffffffffu, ka.x, src);
+                            const int len = __shfl_sync(0xffffffffu, ka.y, src);
+                            const int split = __shfl_sync(0xffffffffu, ka.z, src);
+                            const int pos0 = __shfl_sync(0xffffffffu, ka.w, src);
+                            const int pos1 = __shfl_sync(0xffffffffu, kb.x, src);
+                            const int cc = __shfl_sync(0xffffffffu, c0 | (c1 << 2), src);
+                            if (lane == 0) {
+                                ok = publish(make_int4(cc, len | (split << 16), pos0, pos1));
+                                for (int kv = 0; kv < 2 && ok; ++kv, ++u) {
+                                    const uint32_t slot = u % kSlots, ph = (u / kSlots) & 1u;
+                                    if (!mbar_wait(kv_empty + slot, ph ^ 1u, wc)) {
+                                        ok = 0;
+                                        break;
+                                    }
+                                    uint8_t *dst = base + kOffKV + slot * kTile;
+                                    const CUtensorMap *m = kv ? &p.tmV : &p.tmK;
+                                    mbar_arrive_expect_tx(kv_full + slot, kTile);
+                                    tma_load_3d(dst, m, kv_full + slot, 0, g, row0);
+                                    tma_load_3d(dst + kHalf, m, kv_full + slot, 64, g, row0);
+                                }
+                                if (ok && q_pending) ok = load_q();
+                            }
+                            ok = __shfl_sync(0xffffffffu, ok, 0);
+                            ++jt;
+                        }
                     }
+                }
+                if (ok) {
+                    if (lane == 0) {
+                        if (q_pending) ok = load_q();  // an item without visited tiles
+                        if (ok) ok = publish(make_int4(kEnd, 0, 0, 0));
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    ++jt;
                 }
             }
             if (lane == 0) {
-                if (ok) {
-                    // end marker
-                    const uint32_t e = jt % kRing;
-                    if (mbar_wait(info_empty + e, ((jt / kRing) & 1u) ^ 1u, wc)) {
-                        ring[e] = make_int4(1 << 4, 0, 0, 0);
-                        mbar_arrive(info_full + e);
-                    }
-                }
-                // Drain: the last copy into each slot (and Q) must have landed
-                // before the CTA may exit.
+                // Drain: the last copy into each slot and the last Q must
+                // have landed before the CTA may exit.
                 volatile int local_abort = 0;
                 const WaitCtl drain{&local_abort, p.status, p.budget_ns};
-                (void)mbar_wait(q_full, 0, drain);
+                if (n_q > 0) (void)mbar_wait(q_full, (n_q - 1) & 1u, drain);
                 for (uint32_t x = (u > kSlots ? u - kSlots : 0); x < u; ++x)
                     (void)mbar_wait(kv_full + (x % kSlots), (x / kSlots) & 1u, drain);
             }
         } else if (warp == 1) {
             // -------------------------------------------- MMA issuer
             // The whole warp runs this loop converged and one elected lane
-            // issues each tcgen05 instruction (the _w helpers).
+            // issues each tcgen05 instruction (the _w helpers).  Per item:
+            // S0(0), S1(0), then per KV tile j: PV0(j), S0(j+1), PV1(j),
+            // S1(j+1).  K/V ring positions, barrier phases and PV counts run
+            // on across items.
             const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
             const uint32_t idesc_o = idesc_bf16_f32(128, 128, 0, 1);
             const uint32_t q0s = base_s + kOffQ0, q1s = base_s + kOffQ1;
             const uint32_t kvs = base_s + kOffKV;
             const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-            auto read_info_w = [&](uint32_t jt, int4 &e) -> bool {
-                const uint32_t slot = jt % kRing;
-                if (!mbar_wait_warp(info_full + slot, (jt / kRing) & 1u, wc)) return false;
+            auto read_info_w = [&](uint32_t jt_, int4 &e) -> bool {
+                const uint32_t slot = jt_ % kRing;
+                if (!mbar_wait_warp(info_full + slot, (jt_ / kRing) & 1u, wc)) return false;
                 e = ring[slot];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(info_empty + slot);
                 return true;
             };
-            bool ok = mbar_wait_warp(q_full, 0, wc);
-            tc_fence_after();
-            int4 e;
-            ok = ok && read_info_w(0, e);
-            bool have = ok && !(e.x & 16);
-            int c0 = e.x & 3, c1 = (e.x >> 2) & 3;
-            uint32_t np0 = 0, np1 = 0;  // PVs issued per query tile
-            if (have) {
-                if (!mbar_wait_warp(kv_full + 0, 0, wc)) ok = false;
+            uint32_t jt = 0, gt = 0;    // ring entries read, KV tiles consumed
+            uint32_t np0 = 0, np1 = 0;  // PVs issued per query tile (all items)
+            bool ok = true;
+            for (int it = 0; ok; ++it) {
+                int4 e;
+                if (!read_info_w(jt++, e) || (e.x & kDone)) break;
+                ok = mbar_wait_warp(q_full, it & 1u, wc);
                 tc_fence_after();
-                if (ok) {
+                if (!ok || !read_info_w(jt++, e)) break;
+                if (e.x & kEnd) {
+                    tc_commit_w(q_empty);  // no product reads this item's Q
+                    continue;
+                }
+                int c0 = e.x & 3, c1 = (e.x >> 2) & 3;
+                uint32_t n_pv0 = 0, n_pv1 = 0;  // this item's
+                {
+                    const uint32_t kslot = (2 * gt) % kSlots;
+                    if (!mbar_wait_warp(kv_full + kslot, ((2 * gt) / kSlots) & 1u, wc)) break;
+                    tc_fence_after();
+                    const uint32_t ks = kvs + kslot * kTile;
                     if (c0 != kSkip) {
-                        issue_s(tS0, q0s, kvs, idesc_s);
-                        tc_commit_w(s_full + 0);
-                    }
-                    if (c1 != kSkip) {
-                        issue_s(tS1, q1s, kvs, idesc_s);
-                        tc_commit_w(s_full + 1);
-                    }
-                    tc_commit_w(kv_empty + 0);
-                }
-            }
-            uint32_t j = 0;
-            while (ok && have) {
-                const int cc0 = c0, cc1 = c1;
-                int4 en;
-                if (!read_info_w(j + 1, en)) break;
-                const bool have_next = !(en.x & 16);
-                const int nc0 = en.x & 3, nc1 = (en.x >> 2) & 3;
-                const uint32_t vidx = 2 * j + 1, vslot = vidx % kSlots;
-                if (!mbar_wait_warp(kv_full + vslot, (vidx / kSlots) & 1u, wc)) break;
-                tc_fence_after();
-                const uint32_t vs = kvs + vslot * kTile;
-                const uint32_t kload = 2 * j + 2, kslot = kload % kSlots;
-                const uint32_t ks = kvs + kslot * kTile;
-                if (cc0 != kSkip) {
-                    if (!mbar_wait_warp(p_ready + 0, np0 & 1u, wc)) break;
-                    tc_fence_after();
-                    issue_pv(tO0, tS0, vs, idesc_o, np0 > 0);
-                    tc_commit_w(o_done + 0);
-                    ++np0;
-                }
-                if (have_next) {
-                    if (!mbar_wait_warp(kv_full + kslot, (kload / kSlots) & 1u, wc)) break;
-                    tc_fence_after();
-                    if (nc0 != kSkip) {
                         issue_s(tS0, q0s, ks, idesc_s);
                         tc_commit_w(s_full + 0);
                     }
-                }
-                if (cc1 != kSkip) {
-                    if (!mbar_wait_warp(p_ready + 1, np1 & 1u, wc)) break;
-                    tc_fence_after();
-                    issue_pv(tO1, tS1, vs, idesc_o, np1 > 0);
-                    tc_commit_w(o_done + 1);
-                    ++np1;
-                }
-                if (have_next) {
-                    if (nc1 != kSkip) {
+                    if (c1 != kSkip) {
                         issue_s(tS1, q1s, ks, idesc_s);
                         tc_commit_w(s_full + 1);
                     }
                     tc_commit_w(kv_empty + kslot);
                 }
-                tc_commit_w(kv_empty + vslot);
-                if (!have_next) break;
-                c0 = nc0;
-                c1 = nc1;
-                ++j;
+                for (;;) {
+                    const int cc0 = c0, cc1 = c1;
+                    int4 en;
+                    if (!read_info_w(jt++, en)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool have_next = !(en.x & kEnd);
+                    const int nc0 = en.x & 3, nc1 = (en.x >> 2) & 3;
+                    // this item's last S products are issued: the next item's
+                    // Q may replace this one once they complete
+                    if (!have_next) tc_commit_w(q_empty);
+                    const uint32_t vidx = 2 * gt + 1, vslot = vidx % kSlots;
+                    if (!mbar_wait_warp(kv_full + vslot, (vidx / kSlots) & 1u, wc)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vs = kvs + vslot * kTile;
+                    const uint32_t kload = 2 * gt + 2, kslot = kload % kSlots;
+                    const uint32_t ks = kvs + kslot * kTile;
+                    if (cc0 != kSkip) {
+                        // P0(j) written implies O0's readout of the previous
+                        // item is done (the softmax threads read O before
+                        // their next P)
+                        if (!mbar_wait_warp(p_ready + 0, np0 & 1u, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(tO0, tS0, vs, idesc_o, n_pv0 > 0);
+                        tc_commit_w(o_done + 0);
+                        ++np0;
+                        ++n_pv0;
+                    }
+                    if (have_next) {
+                        if (!mbar_wait_warp(kv_full + kslot, (kload / kSlots) & 1u, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (nc0 != kSkip) {
+                            issue_s(tS0, q0s, ks, idesc_s);
+                            tc_commit_w(s_full + 0);
+                        }
+                    }
+                    if (cc1 != kSkip) {
+                        if (!mbar_wait_warp(p_ready + 1, np1 & 1u, wc)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_pv(tO1, tS1, vs, idesc_o, n_pv1 > 0);
+                        tc_commit_w(o_done + 1);
+                        ++np1;
+                        ++n_pv1;
+                    }
+                    if (have_next) {
+                        if (nc1 != kSkip) {
+                            issue_s(tS1, q1s, ks, idesc_s);
+                            tc_commit_w(s_full + 1);
+                        }
+                        tc_commit_w(kv_empty + kslot);
+                    }
+                    tc_commit_w(kv_empty + vslot);
+                    ++gt;
+                    if (!have_next) break;
+                    c0 = nc0;
+                    c1 = nc1;
+                }
             }
             // every MMA issued must have completed before TMEM is released
             tc_commit_w(mma_done);
@@ -390,32 +469,39 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             (void)mbar_wait_warp(mma_done, 0, drain);
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n" ::: "memory");
         // ------------------------------------------------ softmax / epilogue
         const int k = (warp >= 8) ? 1 : 0;
         const int m = threadIdx.x - 128 - 128 * k;  // TMEM lane = MMA row
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + 128u * k;
         const uint32_t tO = tmem + lane_base + 256u + 128u * k;
-        if (k == 0 || has1) {
-            const TileD q = load_tile(p.qtiles, k ? qt1 : qt0);
-            const int tok = m >> p.log2G;
-            const int head = g * p.G + (m & (p.G - 1));
-            const bool valid = tok < q.len;
+        const int tok = m >> p.log2G;
+        uint32_t jt = 0, nd_all = 0;  // ring entries read; S tiles of this query tile (all items)
+        bool ok = true;
+        while (ok) {
+            int4 e;
+            if (!read_info(jt++, e)) break;
+            if (e.x & kDone) break;
+            const int item = e.y;
+            const int4 ia = __ldg(p.items + 2 * item);
+            const int qt = k ? ia.y : ia.x;
+            const int head = ia.z * p.G + (m & (p.G - 1));
+            TileD q{0, 0, 0, 0, 0, 0, 0, 0};
+            if (qt >= 0) q = load_tile(p.qtiles, qt);
+            const bool valid = qt >= 0 && tok < q.len;
             const int qpos = tok < q.split ? q.pos0 + tok : q.pos1 + (tok - q.split);
             float m_run = -INFINITY, l_run = 0.f;
-            uint32_t nd = 0;
-            bool ok = true;
-            for (uint32_t jt = 0;; ++jt) {
-                int4 e;
-                if (!read_info(jt, e)) {
+            uint32_t nd = 0;  // this item's
+            for (;;) {
+                if (!read_info(jt++, e)) {
                     ok = false;
                     break;
                 }
-                if (e.x & 16) break;
+                if (e.x & kEnd) break;
                 const int cls = k ? ((e.x >> 2) & 3) : (e.x & 3);
                 if (cls == kSkip) continue;
-                if (!mbar_wait(s_full + k, nd & 1u, wc)) {
+                if (!mbar_wait(s_full + k, nd_all & 1u, wc)) {
                     ok = false;
                     break;
                 }
@@ -496,12 +582,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 tc_fence_before();
                 mbar_arrive(p_ready + k);
                 ++nd;
+                ++nd_all;
             }
             // ---------------------------------------------- epilogue
+            // (O's columns are next overwritten by the first PV of a later
+            // item, which waits for this thread's next P: the readout below
+            // comes first in this thread's program order)
             if (ok && nd > 0) {
-                ok = mbar_wait(o_done + k, (nd - 1) & 1u, wc);
+                ok = mbar_wait(o_done + k, (nd_all - 1) & 1u, wc);
                 tc_fence_after();
             }
+            if (qt < 0) continue;
             const bool has_o = ok && nd > 0;
             const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
             const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
@@ -547,6 +638,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+    if (threadIdx.x == 0) {
+        // The last CTA to finish returns the work counter to zero for the
+        // next launch (every CTA has made its final claim by now).
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+            p.sched[0] = 0;
+            p.sched[1] = 0;
+            __threadfence();
+        }
     }
 }
 
@@ -599,6 +700,7 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
     p.kvtiles = static_cast<const int4 *>(a.kvtiles);
     p.items = static_cast<const int4 *>(a.items);
     p.kv_off = a.kv_off;
+    p.sched = a.sched;
     p.n_items = a.n_items;
     p.cp = a.cp;
     p.B = a.B;
@@ -623,7 +725,7 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
     if (dev >= 0 && dev < 128 && !attr_set[dev]) {
         cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        // The setmaxnreg split (128 x 56 + 256 x 224) needs the CTA to be
+        // The setmaxnreg split (128 x 80 + 256 x 200) needs the CTA to be
         // launched with 168 registers per thread; with fewer, the increase
         // could never be granted, so refuse to launch.
         cudaFuncAttributes fa;
@@ -632,7 +734,16 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
         if (fa.numRegs < 168) return cudaErrorInvalidConfiguration;
         attr_set[dev] = true;
     }
-    tc_fwd_kernel<<<a.n_items, kThreads, kSmemBytes, st>>>(p);
+    // persistent: one CTA per SM (shared memory allows no more), each
+    // claiming items until the counter runs past n_items
+    static int sm_count[128] = {};
+    if (dev >= 0 && dev < 128 && sm_count[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 1;
+        sm_count[dev] = n > 0 ? n : 1;
+    }
+    const int grid = std::min(a.n_items, (dev >= 0 && dev < 128) ? sm_count[dev] : 1);
+    tc_fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 
