@@ -100,26 +100,102 @@ using namespace ra;
 
 namespace ra {
 
+// Page-locked buffers of plans that left the cache, with the event of their
+// last upload; a new plan reuses one once that upload has finished reading
+// it.  Freeing page-locked memory would synchronise the device.
+struct PinnedBuf {
+    void *p;
+    size_t n;
+    void *ev;
+    bool multi;
+};
+std::mutex g_pool_mu;
+std::vector<PinnedBuf> g_pool;
+
+static void pinned_buf_settle(const PinnedBuf &b) {
+    if (b.multi) {
+        (void)cudaDeviceSynchronize();  // uploads on several streams: rare
+    } else if (b.ev) {
+        (void)cudaEventSynchronize(static_cast<cudaEvent_t>(b.ev));
+    }
+    if (b.ev) (void)cudaEventDestroy(static_cast<cudaEvent_t>(b.ev));
+}
+
+static void *take_pinned(size_t n, size_t *got) {
+    {
+        std::lock_guard<std::mutex> lk(g_pool_mu);
+        int best = -1;
+        for (int i = 0; i < (int)g_pool.size(); ++i)
+            if (g_pool[i].n >= n && (best < 0 || g_pool[i].n < g_pool[best].n)) best = i;
+        if (best >= 0) {
+            PinnedBuf b = g_pool[best];
+            g_pool.erase(g_pool.begin() + best);
+            pinned_buf_settle(b);
+            *got = b.n;
+            return b.p;
+        }
+    }
+    const size_t sz = align_up(n, (size_t)1 << 16);
+    void *h = nullptr;
+    if (cudaMallocHost(&h, sz) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    *got = sz;
+    return h;
+}
+
 RingPlan::~RingPlan() {
-    if (pinned) {
-        // an upload from this buffer may still be queued on some stream
-        (void)cudaDeviceSynchronize();
-        (void)cudaFreeHost(pinned);
+    if (!pinned) return;
+    if (in_graph) return;  // a captured graph may still copy from it
+    std::lock_guard<std::mutex> lk(g_pool_mu);
+    g_pool.push_back(PinnedBuf{pinned, pinned_bytes, uploaded, multi_stream});
+    if (g_pool.size() > 32) {  // bound the pool: release the oldest
+        PinnedBuf b = g_pool.front();
+        g_pool.erase(g_pool.begin());
+        pinned_buf_settle(b);
+        (void)cudaFreeHost(b.p);
     }
 }
 
-const void *plan_upload_src(RingPlan &plan) {
+ra_status upload_plan_tables(RingPlan &plan, void *dst, void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t n = plan.dev.blob.size();
+    if (n == 0) return RA_OK;
     std::lock_guard<std::mutex> lk(plan.pin_mu);
-    if (!plan.pinned && !plan.dev.blob.empty()) {
-        void *h = nullptr;
-        if (cudaMallocHost(&h, plan.dev.blob.size()) == cudaSuccess) {
-            std::memcpy(h, plan.dev.blob.data(), plan.dev.blob.size());
-            plan.pinned = h;
-        } else {
-            (void)cudaGetLastError();
-        }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cs = cudaStreamCaptureStatusNone;
     }
-    return plan.pinned ? plan.pinned : static_cast<const void *>(plan.dev.blob.data());
+    if (cs != cudaStreamCaptureStatusNone) {
+        if (!plan.pinned)
+            return fail(RA_ERR_UNSUPPORTED,
+                        "stream capture: call once outside capture with these sequence lengths first "
+                        "(the page-locked copy of the tables is made there)");
+        plan.in_graph = true;
+        RA_CUDA(cudaMemcpyAsync(dst, plan.pinned, n, cudaMemcpyHostToDevice, s), "table upload");
+        return RA_OK;
+    }
+    if (!plan.pinned) {
+        plan.pinned = take_pinned(n, &plan.pinned_bytes);
+        if (plan.pinned) std::memcpy(plan.pinned, plan.dev.blob.data(), n);
+    }
+    if (!plan.pinned) {  // no page-locked memory: pageable copy
+        RA_CUDA(cudaMemcpyAsync(dst, plan.dev.blob.data(), n, cudaMemcpyHostToDevice, s), "table upload");
+        return RA_OK;
+    }
+    RA_CUDA(cudaMemcpyAsync(dst, plan.pinned, n, cudaMemcpyHostToDevice, s), "table upload");
+    if (!plan.uploaded) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess) plan.uploaded = e;
+        else (void)cudaGetLastError();
+    }
+    if (plan.upload_stream && plan.upload_stream != stream) plan.multi_stream = true;
+    plan.upload_stream = stream;
+    if (plan.uploaded) RA_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(plan.uploaded), s), "upload event");
+    else plan.multi_stream = true;  // nothing to wait on: settle by a device sync
+    return RA_OK;
 }
 
 // A second stream per device, with a fork and a join event, for the query-side
@@ -135,12 +211,13 @@ struct SideStream {
 };
 std::mutex g_side_mu;
 
-SideStream *side_stream_locked() {
+SideStream *side_stream_locked(bool may_create) {
     static SideStream ss[128];
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
     SideStream &s = ss[dev];
     if (!s.st) {
+        if (!may_create) return nullptr;
         cudaStream_t st = nullptr;
         cudaEvent_t a = nullptr, b = nullptr;
         if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
@@ -572,8 +649,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     uint8_t *tab = ws + L.tables;
     {
         ProfScope ps("ra_table_upload", s);
-        RA_CUDA(cudaMemcpyAsync(tab, plan_upload_src(*plan), dt.blob.size(), cudaMemcpyHostToDevice, s),
-                "table upload");
+        if ((st = upload_plan_tables(*plan, tab, s))) return st;
     }
     const int32_t *perm = reinterpret_cast<const int32_t *>(tab + dt.o_perm);
     const int32_t *off = reinterpret_cast<const int32_t *>(tab + dt.o_off);
@@ -713,8 +789,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
                          reserve_matches(workspace, plan.get(), q, k, v, dtype, T, Hq, Hkv, d, causal, sched);
     if (!reserve) {
         ProfScope ps("ra_table_upload", s);
-        RA_CUDA(cudaMemcpyAsync(tab, plan_upload_src(*plan), dt.blob.size(), cudaMemcpyHostToDevice, s),
-                "table upload");
+        if ((st = upload_plan_tables(*plan, tab, s))) return st;
     }
     const int32_t *perm = reinterpret_cast<const int32_t *>(tab + dt.o_perm);
     const int32_t *off = reinterpret_cast<const int32_t *>(tab + dt.o_off);
@@ -814,7 +889,14 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
             qa.dq = dq;  // complete per query tile: written once in the gradient dtype
             qa.out_mode = grad_dtype == RA_BF16 ? 0 : 1;
             std::lock_guard<std::mutex> lk(g_side_mu);
-            SideStream *side = side_stream_locked();
+            // under stream capture the side stream is joined into the graph
+            // (fork/join through events); it is created outside capture only
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+                (void)cudaGetLastError();
+                cs = cudaStreamCaptureStatusActive;
+            }
+            SideStream *side = side_stream_locked(cs == cudaStreamCaptureStatusNone);
             if (side) {
                 // one timing scope over both kernels: they share the SMs
                 ProfScope ps("ra_tc_bwd", s);

@@ -108,16 +108,25 @@ struct RingPlan {
     TilePlan tiles;
     bool has_tiles = false;
     DeviceTables dev;
-    // Page-locked copy of dev.blob, made on first upload, so that the
-    // per-call table upload is an asynchronous copy that never blocks the
-    // host (a pageable source is staged synchronously by the driver).
+    // Page-locked copy of dev.blob, made on the first upload outside stream
+    // capture, so that the per-call table upload is an asynchronous copy that
+    // never blocks the host.  Page-locked buffers are recycled through a
+    // process-wide pool when plans leave the cache (no free, so no implicit
+    // device synchronisation); a buffer that a captured graph copies from is
+    // kept for the process lifetime.
     void *pinned = nullptr;
+    size_t pinned_bytes = 0;
+    void *uploaded = nullptr;          // cudaEvent_t of the last upload from `pinned`
+    void *upload_stream = nullptr;     // its stream
+    bool multi_stream = false;         // uploads went to more than one stream
+    bool in_graph = false;             // an upload was captured into a graph
     std::mutex pin_mu;
     ~RingPlan();
 };
-// Host source for uploading plan.dev.blob: the pinned copy (made on first
-// use), or the pageable blob if page-locked memory is unavailable.
-const void *plan_upload_src(RingPlan &plan);
+// Enqueues the copy of plan.dev.blob into the workspace tables at `dst` on
+// `stream` (a cudaStream_t).  Under stream capture the plan must already
+// have its page-locked copy (an earlier call outside capture made it).
+ra_status upload_plan_tables(RingPlan &plan, void *dst, void *stream);
 // Cached plans keyed by content (cu_seqlens, cp, mode, G, Hkv, causal).
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
                                         int causal, bool want_tiles, ra_status *st);
