@@ -203,6 +203,12 @@ ra_status ra_lse_merge(int n_parts, const float *const *outs, const float *const
  * scale: softmax scale; pass 1/sqrt(d) for the usual attention (maxtext
  * PR #1133, cudnn_flash_attention diff).  cp >= 1.
  * workspace: DEVICE, >= ra_ring_workspace_bytes(...) for the same arguments.
+ * Asynchronous on `stream`.  The backward's fused tensor-core path runs its
+ * key-side kernel on a second, library-owned stream forked from and joined
+ * back to `stream` through events.  Both calls may be captured into a CUDA
+ * graph once an uncaptured call with the same cu_seqlens, cp, zz_mode and
+ * heads has run (it makes the page-locked table copy and the second
+ * stream); otherwise a captured call returns RA_ERR_UNSUPPORTED.
  * ------------------------------------------------------------------------ */
 size_t ra_ring_workspace_bytes(int64_t T, int Hq, int Hkv, int d, int dtype,
                                const int32_t *cu_seqlens, int B, int cp, int zz_mode,
