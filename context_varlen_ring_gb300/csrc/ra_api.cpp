@@ -174,7 +174,7 @@ ra_status upload_plan_tables(RingPlan &plan, void *dst, void *stream) {
                         "stream capture: call once outside capture with these sequence lengths first "
                         "(the page-locked copy of the tables is made there)");
         plan.in_graph = true;
-        RA_CUDA(cudaMemcpyAsync(dst, plan.pinned, n, cudaMemcpyHostToDevice, s), "table upload");
+        RA_CUDA(launch_copy_from_host(plan.pinned, dst, n, s), "table upload");
         return RA_OK;
     }
     if (!plan.pinned) {
@@ -185,7 +185,9 @@ ra_status upload_plan_tables(RingPlan &plan, void *dst, void *stream) {
         RA_CUDA(cudaMemcpyAsync(dst, plan.dev.blob.data(), n, cudaMemcpyHostToDevice, s), "table upload");
         return RA_OK;
     }
-    RA_CUDA(cudaMemcpyAsync(dst, plan.pinned, n, cudaMemcpyHostToDevice, s), "table upload");
+    // a kernel reads the mapped page-locked copy: a copy engine could queue
+    // this small upload behind large transfers on other streams
+    RA_CUDA(launch_copy_from_host(plan.pinned, dst, n, s), "table upload");
     if (!plan.uploaded) {
         cudaEvent_t e = nullptr;
         if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess) plan.uploaded = e;

@@ -49,6 +49,11 @@ cudaError_t launch_merge(int n, const float *const *outs, const float *const *ls
 // the jobs (Q, K, V) and dO (dout -> dout_p, Hq heads) by perm, and
 // D[h, p] = sum_c dO[p, h, c] * O[p, h, c] in fp32 at original rows p.
 // All pointers and row sizes must be 16-byte aligned (else cudaErrorInvalidValue).
+// Copies n bytes from page-locked host memory (mapped into the device's
+// address space) to device memory with a kernel, so the copy never queues
+// behind other streams' transfers on a copy engine.  src and dst must be
+// 16-byte aligned (else cudaErrorInvalidValue).
+cudaError_t launch_copy_from_host(const void *src, void *dst, size_t n, cudaStream_t st);
 cudaError_t launch_permute_rowdot(const PermJob *jobs, int njobs, const void *dout, void *dout_p, const void *out,
                                   float *D, const int32_t *perm, int64_t T, int Hq, cudaStream_t st);
 cudaError_t launch_rowdot(const void *a, const void *b, int dtype, int64_t T, int H, int d, float *D,

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include <cmath>
 #include <cstdint>
 
@@ -387,6 +389,29 @@ cudaError_t launch_tile_lse_d(const void *qtiles, int n_qtiles, int Hkv, int G, 
 }
 
 // ------------------------------------------------------------------ cast
+__global__ void __launch_bounds__(256) copy_from_host_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                            int64_t n16, const uint8_t *__restrict__ src_tail,
+                                                            uint8_t *__restrict__ dst_tail, int tail) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) dst[i] = src[i];
+    if (blockIdx.x == 0 && (int)threadIdx.x < tail) dst_tail[threadIdx.x] = src_tail[threadIdx.x];
+}
+
+cudaError_t launch_copy_from_host(const void *src, void *dst, size_t n, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) return cudaErrorInvalidValue;
+    void *dsrc = nullptr;  // the device's address of the mapped host buffer
+    cudaError_t e = cudaHostGetDevicePointer(&dsrc, const_cast<void *>(src), 0);
+    if (e != cudaSuccess) return e;
+    const int64_t n16 = (int64_t)(n / 16);
+    const int tail = (int)(n % 16);
+    const int64_t blocks = std::min<int64_t>(std::max<int64_t>((n16 + 255) / 256, 1), 1024);
+    copy_from_host_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4 *>(dsrc), static_cast<uint4 *>(dst),
+                                                           n16, static_cast<const uint8_t *>(dsrc) + n16 * 16,
+                                                           static_cast<uint8_t *>(dst) + n16 * 16, tail);
+    return cudaGetLastError();
+}
+
 __global__ void cast_bf16_kernel(const float *__restrict__ src, __nv_bfloat16 *__restrict__ dst, int64_t n) {
     const int64_t n4 = n / 4;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
