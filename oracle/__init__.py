@@ -41,17 +41,17 @@ def lib():
         i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
         L.orc_set_threads.argtypes = [i32]
         L.orc_set_threads.restype = i32
-        L.orc_partial_fwd.argtypes = [P, P, P, i64, i64, i32, i32, i32, P, P, P, P, i32, dbl, P, i64, P, P]
+        L.orc_partial_fwd.argtypes = [P, P, P, i64, i64, i32, i32, i32, P, P, P, P, i32, i64, dbl, P, i64, P, P]
         L.orc_partial_fwd.restype = i32
         L.orc_lse_merge.argtypes = [i32, P, P, i64, i32, i32, P, P]
         L.orc_lse_merge.restype = i32
-        L.orc_attn_bwd.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, P, P, i32, dbl, P, i64, P, i64, P, P, P]
+        L.orc_attn_bwd.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, P, P, i32, i64, dbl, P, i64, P, i64, P, P, P]
         L.orc_attn_bwd.restype = i32
         L.orc_zigzag_owner.argtypes = [P, i32, i32, i32, P]
         L.orc_zigzag_owner.restype = i32
         L.orc_zigzag_plan.argtypes = [P, i32, i32, i32, P, P, P]
         L.orc_zigzag_plan.restype = i32
-        L.orc_rank_pairs.argtypes = [P, i32, i32, i32, i32, P]
+        L.orc_rank_pairs.argtypes = [P, i32, i32, i32, i32, i64, P]
         L.orc_rank_pairs.restype = i32
         _lib = L
     return _lib
@@ -93,9 +93,10 @@ def doc_ids(cu) -> np.ndarray:
     return ids
 
 
-def partial_fwd(q, k, v, seg_q, seg_k, q_pos, k_pos, causal: bool, scale: float, rows=None):
+def partial_fwd(q, k, v, seg_q, seg_k, q_pos, k_pos, causal: bool, scale: float, rows=None, window: int = -1):
     """Attention of queries against keys over the allowed pairs
-    {(i,j): seg_k[j]==seg_q[i] and (not causal or k_pos[j] <= q_pos[i])}.
+    {(i,j): seg_k[j]==seg_q[i] and (not causal or k_pos[j] <= q_pos[i])
+    and (window < 0 or k_pos[j] >= q_pos[i] - window)}.
 
     q [Tq,Hq,d], k/v [Tk,Hkv,d].  Returns (out [R,Hq,d], lse [R,Hq]) in fp64,
     R = len(rows) or Tq.  Empty rows give out = 0 and lse = -inf."""
@@ -113,18 +114,19 @@ def partial_fwd(q, k, v, seg_q, seg_k, q_pos, k_pos, causal: bool, scale: float,
     out = np.zeros((R, Hq, d), dtype=np.float64)
     lse = np.zeros((R, Hq), dtype=np.float64)
     rc = lib().orc_partial_fwd(_p(q), _p(k), _p(v), Tq, Tk, Hq, Hkv, d, _p(sq), _p(sk), _p(pq), _p(pk),
-                               int(bool(causal)), float(scale), rp, R, _p(out), _p(lse))
+                               int(bool(causal)), int(window), float(scale), rp, R, _p(out), _p(lse))
     if rc:
         raise ValueError(f"orc_partial_fwd failed ({rc})")
     return out, lse
 
 
-def attn_fwd(q, k, v, cu, causal: bool, scale: float, rows=None):
-    """Full packed (block-diagonal, optionally causal) attention."""
+def attn_fwd(q, k, v, cu, causal: bool, scale: float, rows=None, window: int = -1):
+    """Full packed (block-diagonal, optionally causal, optionally
+    sliding-window) attention."""
     T = int(np.asarray(cu)[-1])
     seg = doc_ids(cu)
     pos = np.arange(T, dtype=np.int64)
-    return partial_fwd(q, k, v, seg, seg, pos, pos, causal, scale, rows)
+    return partial_fwd(q, k, v, seg, seg, pos, pos, causal, scale, rows, window)
 
 
 def lse_merge(outs, lses):
@@ -143,7 +145,7 @@ def lse_merge(outs, lses):
     return out, lse
 
 
-def attn_bwd(q, k, v, o, lse, dout, cu, causal: bool, scale: float, dq_rows=None, dk_rows=None):
+def attn_bwd(q, k, v, o, lse, dout, cu, causal: bool, scale: float, dq_rows=None, dk_rows=None, window: int = -1):
     """Gradients (dq, dk, dv) in fp64 given the oracle's own forward (o, lse).
 
     o/lse/dout are [T,Hq,d]/[T,Hq]/[T,Hq,d]; rows that no requested output
@@ -167,7 +169,7 @@ def attn_bwd(q, k, v, o, lse, dout, cu, causal: bool, scale: float, dq_rows=None
     dk = np.zeros((nk, Hkv, d))
     dv = np.zeros((nk, Hkv, d))
     rc = lib().orc_attn_bwd(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(dout), T, Hq, Hkv, d,
-                            _p(seg), _p(pos), int(bool(causal)), float(scale), qp, nq, kp, nk,
+                            _p(seg), _p(pos), int(bool(causal)), int(window), float(scale), qp, nq, kp, nk,
                             _p(dq), _p(dk), _p(dv))
     if rc:
         raise ValueError("orc_attn_bwd failed")
@@ -198,16 +200,16 @@ def zigzag_plan(cu, cp: int, mode: int):
     return perm, off, cl
 
 
-def rank_pairs(cu, cp: int, mode: int, causal: bool = True) -> np.ndarray:
+def rank_pairs(cu, cp: int, mode: int, causal: bool = True, window: int = -1) -> np.ndarray:
     cu = _i32(cu)
     counts = np.zeros(cp, dtype=np.int64)
-    rc = lib().orc_rank_pairs(_p(cu), len(cu) - 1, cp, mode, int(bool(causal)), _p(counts))
+    rc = lib().orc_rank_pairs(_p(cu), len(cu) - 1, cp, mode, int(bool(causal)), int(window), _p(counts))
     if rc:
         raise ValueError("orc_rank_pairs failed")
     return counts
 
 
-def ring_fwd(q, k, v, cu, cp: int, mode: int, causal: bool, scale: float):
+def ring_fwd(q, k, v, cu, cp: int, mode: int, causal: bool, scale: float, window: int = -1):
     """The ring schedule written out step by step in fp64: zigzag-permute,
     for every rank r and step t take the partial of rank r's queries against
     rank s=(r-t) mod cp's keys, merge the cp partials, undo the permutation.
@@ -224,7 +226,7 @@ def ring_fwd(q, k, v, cu, cp: int, mode: int, causal: bool, scale: float):
         for t in range(cp):
             s = (r - t) % cp
             ki = perm[off[s]:off[s + 1]]
-            o_p, l_p = partial_fwd(q[qi], k[ki], v[ki], seg[qi], seg[ki], qi, ki, causal, scale)
+            o_p, l_p = partial_fwd(q[qi], k[ki], v[ki], seg[qi], seg[ki], qi, ki, causal, scale, window=window)
             parts_o.append(o_p)
             parts_l.append(l_p)
         o_r, l_r = lse_merge(parts_o, parts_l)

@@ -46,7 +46,12 @@ int orc_set_threads(int n) {
 /* ------------------------------------------------------------------------
  * Attention of a set of queries against a set of keys, restricted to the
  * allowed pairs
- *      A(i) = { j : seg_k[j] == seg_q[i]  and  (causal == 0  or  k_pos[j] <= q_pos[i]) }.
+ *      A(i) = { j : seg_k[j] == seg_q[i]  and  (causal == 0  or  k_pos[j] <= q_pos[i])
+ *                   and  (window < 0  or  k_pos[j] >= q_pos[i] - window) }.
+ * The window is the sliding-window mask named by the window_size argument of
+ * the cuDNN flash-attention call ("Add Context Parallelism support to cudnn
+ * Flash Attention #1133", maxtext, diff of cudnn_flash_attention), read as a
+ * key reaching back at most `window` positions from its query.
  * With seg = document id and pos = packed index this is the full
  * block-diagonal causal attention; with a subset of keys it is one ring
  * step's partial result.
@@ -63,7 +68,7 @@ int orc_partial_fwd(const double *q, const double *k, const double *v,
                     int64_t Tq, int64_t Tk, int Hq, int Hkv, int d,
                     const int32_t *seg_q, const int32_t *seg_k,
                     const int64_t *q_pos, const int64_t *k_pos,
-                    int causal, double scale,
+                    int causal, int64_t window, double scale,
                     const int64_t *rows, int64_t nrows,
                     double *out, double *lse)
 {
@@ -85,7 +90,8 @@ int orc_partial_fwd(const double *q, const double *k, const double *v,
             double m = -INFINITY;
             int any = 0;
             for (int64_t j = 0; j < Tk; ++j) {
-                int allowed = (seg_k[j] == seg_q[i]) && (!causal || k_pos[j] <= q_pos[i]);
+                int allowed = (seg_k[j] == seg_q[i]) && (!causal || k_pos[j] <= q_pos[i]) &&
+                              (window < 0 || k_pos[j] >= q_pos[i] - window);
                 ok[j] = (unsigned char)allowed;
                 if (!allowed) continue;
                 const double *kj = k + (j * Hkv + g) * (int64_t)d;
@@ -178,7 +184,7 @@ static double dot(const double *a, const double *b, int d)
 int orc_attn_bwd(const double *q, const double *k, const double *v,
                  const double *o, const double *lse, const double *dout,
                  int64_t T, int Hq, int Hkv, int d,
-                 const int32_t *seg, const int64_t *pos, int causal, double scale,
+                 const int32_t *seg, const int64_t *pos, int causal, int64_t window, double scale,
                  const int64_t *dq_rows, int64_t ndq,
                  const int64_t *dk_rows, int64_t ndk,
                  double *dq, double *dk, double *dv)
@@ -206,7 +212,8 @@ int orc_attn_bwd(const double *q, const double *k, const double *v,
         for (int c = 0; c < d; ++c) dqi[c] = 0.0;
         double li = lse[i * Hq + h];
         for (int64_t j = 0; j < T; ++j) {
-            if (!(seg[j] == seg[i] && (!causal || pos[j] <= pos[i]))) continue;
+            if (!(seg[j] == seg[i] && (!causal || pos[j] <= pos[i]) && (window < 0 || pos[j] >= pos[i] - window)))
+                continue;
             const double *kj = k + (j * Hkv + g) * (int64_t)d;
             const double *vj = v + (j * Hkv + g) * (int64_t)d;
             double p = exp(scale * dot(qi, kj, d) - li);
@@ -228,7 +235,9 @@ int orc_attn_bwd(const double *q, const double *k, const double *v,
         for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
         for (int h = g * G; h < (g + 1) * G; ++h) {
             for (int64_t i = 0; i < T; ++i) {
-                if (!(seg[j] == seg[i] && (!causal || pos[j] <= pos[i]))) continue;
+                if (!(seg[j] == seg[i] && (!causal || pos[j] <= pos[i]) &&
+                      (window < 0 || pos[j] >= pos[i] - window)))
+                    continue;
                 const double *qi = q + (i * Hq + h) * (int64_t)d;
                 const double *doi = dout + (i * Hq + h) * (int64_t)d;
                 double p = exp(scale * dot(qi, kj, d) - lse[i * Hq + h]);
@@ -308,7 +317,7 @@ int orc_zigzag_plan(const int32_t *cu, int B, int cp, int mode,
 
 /* Allowed (query, key) pairs per rank: a rank computes its own queries
  * against every key of the same document (the union of all ring steps). */
-int orc_rank_pairs(const int32_t *cu, int B, int cp, int mode, int causal, int64_t *counts)
+int orc_rank_pairs(const int32_t *cu, int B, int cp, int mode, int causal, int64_t window, int64_t *counts)
 {
     int64_t T = cu[B];
     int32_t *owner = (int32_t *)malloc(sizeof(int32_t) * (size_t)(T > 0 ? T : 1));
@@ -316,8 +325,12 @@ int orc_rank_pairs(const int32_t *cu, int B, int cp, int mode, int causal, int64
     if (rc) { free(owner); return rc; }
     for (int r = 0; r < cp; ++r) counts[r] = 0;
     for (int b = 0; b < B; ++b)
-        for (int64_t i = cu[b]; i < cu[b + 1]; ++i)
-            counts[owner[i]] += causal ? (i - cu[b] + 1) : ((int64_t)cu[b + 1] - cu[b]);
+        for (int64_t i = cu[b]; i < cu[b + 1]; ++i) {
+            /* keys of the document in [lo, hi] */
+            int64_t lo = cu[b], hi = causal ? i : (int64_t)cu[b + 1] - 1;
+            if (window >= 0 && i - window > lo) lo = i - window;
+            if (hi >= lo) counts[owner[i]] += hi - lo + 1;
+        }
     free(owner);
     return 0;
 }
