@@ -72,10 +72,11 @@ def zigzag_plan(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL):
     return perm[:T], off, cl
 
 
-def ring_rank_pairs(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool = True) -> np.ndarray:
+def ring_rank_pairs(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool = True,
+                    window: int = -1) -> np.ndarray:
     cu = _host_i32(cu_seqlens)
     counts = np.zeros(cp, dtype=np.int64)
-    check(lib().ra_ring_rank_pairs(_np_ptr(cu), len(cu) - 1, cp, mode, int(causal), _np_ptr(counts)),
+    check(lib().ra_ring_rank_pairs(_np_ptr(cu), len(cu) - 1, cp, mode, int(causal), int(window), _np_ptr(counts)),
           "ra_ring_rank_pairs")
     return counts
 
@@ -109,9 +110,10 @@ def zigzag_unpermute(y: torch.Tensor, perm) -> torch.Tensor:
 
 
 def varlen_attn_partial(q, k, v, cu_seqlens_q, cu_seqlens_k, q_pos=None, k_pos=None, causal: bool = True,
-                        scale: float | None = None, out=None, lse=None):
+                        scale: float | None = None, out=None, lse=None, window: int = -1):
     """One ring step: (out fp32 [Tq,Hq,d], lse fp32 [Hq,Tq]) of q against k/v
-    over pairs in the same segment with k_pos <= q_pos (when causal)."""
+    over pairs in the same segment with k_pos <= q_pos (when causal) and
+    k_pos >= q_pos - window (when window >= 0)."""
     _check_cuda(q, k, v)
     Tq, Hq, d = q.shape
     Tk, Hkv, _ = k.shape
@@ -130,7 +132,7 @@ def varlen_attn_partial(q, k, v, cu_seqlens_q, cu_seqlens_k, q_pos=None, k_pos=N
     ws = torch.empty(max(int(ws_bytes), 1), dtype=torch.uint8, device=q.device)
     check(L.ra_varlen_attn_partial(_ptr(q), _ptr(k), _ptr(v), dt, Tq, Tk, Hq, Hkv, d, _np_ptr(cuq), _np_ptr(cuk),
                                    nseg, _np_ptr(qp) if qp is not None else None,
-                                   _np_ptr(kp) if kp is not None else None, int(causal), scale, _ptr(out),
+                                   _np_ptr(kp) if kp is not None else None, int(causal), int(window), scale, _ptr(out),
                                    _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device)),
           "ra_varlen_attn_partial")
     return out, lse
@@ -175,9 +177,11 @@ def ring_workspace_bytes(T, Hq, Hkv, d, dtype, cu_seqlens, cp, mode, sched="fuse
 
 
 def ring_attn_fwd(q, k, v, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool = True,
-                  scale: float | None = None, sched: str = "fused", out=None, lse=None, workspace=None):
+                  scale: float | None = None, sched: str = "fused", out=None, lse=None, workspace=None,
+                  window: int = -1):
     """Simulated zigzag ring attention forward; returns (out [T,Hq,d] in q's
-    dtype, lse fp32 [Hq,T]) in the original token order."""
+    dtype, lse fp32 [Hq,T]) in the original token order.  window >= 0: a key
+    is visible only up to `window` positions behind its query."""
     _check_cuda(q, k, v)
     T, Hq, d = q.shape
     Hkv = k.shape[1]
@@ -193,15 +197,16 @@ def ring_attn_fwd(q, k, v, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal
     need = L.ra_ring_workspace_bytes(T, Hq, Hkv, d, dt, _np_ptr(cu), B, cp, mode, _SCHED[sched], 0)
     ws = workspace if workspace is not None else _WS.get(q.device, int(need))
     check(L.ra_ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, Hq, Hkv, d, _np_ptr(cu), B, cp, mode, int(causal),
-                             scale, _SCHED[sched], _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device)),
+                             int(window), scale, _SCHED[sched], _ptr(out), _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device)),
           "ra_ring_attn_fwd")
     return out, lse
 
 
 def ring_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool = True,
                   scale: float | None = None, sched: str = "fused", grad_dtype=None, dq=None, dk=None, dv=None,
-                  workspace=None, reuse_fwd_workspace: bool = False):
-    """Gradients (dq, dk, dv) in the original token order.
+                  workspace=None, reuse_fwd_workspace: bool = False, window: int = -1):
+    """Gradients (dq, dk, dv) in the original token order (window as in
+    ring_attn_fwd; pass the forward's).
 
     reuse_fwd_workspace: `workspace` is the one the preceding ring_attn_fwd
     used with these same q, k, v and arguments, untouched since; its
@@ -222,7 +227,7 @@ def ring_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, cp: int, mode: int = RA_Z
     need = L.ra_ring_workspace_bytes(T, Hq, Hkv, d, dt, _np_ptr(cu), B, cp, mode, _SCHED[sched], 1)
     ws = workspace if workspace is not None else _WS.get(q.device, int(need))
     check(L.ra_ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), dt, T, Hq, Hkv, d, _np_ptr(cu), B, cp, mode, int(causal),
-                             scale, _SCHED[sched], _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                             int(window), scale, _SCHED[sched], _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
                              _dtype_code(dq), RA_BWD_FWD_RESERVE if reuse_fwd_workspace else 0, _ptr(ws), ws.numel(),
                              _stream(q.device)),
           "ra_ring_attn_bwd")

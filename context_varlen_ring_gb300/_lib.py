@@ -54,17 +54,17 @@ def _declare(L):
         "ra_zigzag_permute": (i32, [P, P, P, i64, i64, P]),
         "ra_zigzag_unpermute": (i32, [P, P, P, i64, i64, P]),
         "ra_partial_workspace_bytes": (sz, [i64, i64, i32, i32, i32, i32, i32]),
-        "ra_varlen_attn_partial": (i32, [P, P, P, i32, i64, i64, i32, i32, i32, P, P, i32, P, P, i32, f32,
+        "ra_varlen_attn_partial": (i32, [P, P, P, i32, i64, i64, i32, i32, i32, P, P, i32, P, P, i32, i32, f32,
                                          P, P, P, sz, P]),
         "ra_varlen_attn_partial_noalloc": (i32, [P, P, P, i32, i64, i64, i32, i32, i32, P, P, i32, P, P, i32,
-                                                 f32, P, P, P]),
+                                                 i32, f32, P, P, P]),
         "ra_lse_merge": (i32, [i32, P, P, i64, i32, i32, P, i32, P, P]),
         "ra_ring_workspace_bytes": (sz, [i64, i32, i32, i32, i32, P, i32, i32, i32, i32, i32]),
-        "ra_ring_attn_fwd": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, i32, f32, i32,
+        "ra_ring_attn_fwd": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, i32, i32, f32, i32,
                                    P, P, P, sz, P]),
-        "ra_ring_attn_bwd": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, i32, f32, i32,
+        "ra_ring_attn_bwd": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, i32, i32, f32, i32,
                                    P, P, P, P, P, P, i32, i32, P, sz, P]),
-        "ra_ring_rank_pairs": (i32, [P, i32, i32, i32, i32, P]),
+        "ra_ring_rank_pairs": (i32, [P, i32, i32, i32, i32, i32, P]),
         "ra_get_device_status": (i32, [P]),
         "ra_selftest_wait_timeout": (i32, [i64, P]),
         "ra_status_string": (ctypes.c_char_p, [i32]),

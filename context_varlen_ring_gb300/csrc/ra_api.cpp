@@ -373,7 +373,7 @@ ra_status ra_zigzag_unpermute(const void *y, void *x, const int32_t *perm, int64
     return permute_common(y, x, perm, T, row_bytes, stream, 1);
 }
 
-ra_status ra_ring_rank_pairs(const int32_t *cu, int B, int cp, int mode, int causal, int64_t *counts) {
+ra_status ra_ring_rank_pairs(const int32_t *cu, int B, int cp, int mode, int causal, int window, int64_t *counts) {
     if (!counts) return fail(RA_ERR_INVALID_ARG, "counts is NULL");
     ZigzagPlan zp;
     ra_status st = build_zigzag(cu, B, cp, mode, zp);
@@ -384,7 +384,14 @@ ra_status ra_ring_rank_pairs(const int32_t *cu, int B, int cp, int mode, int cau
             const int64_t lo = zp.off[r] + zp.cu_local[(size_t)r * (B + 1) + b];
             const int64_t hi = zp.off[r] + zp.cu_local[(size_t)r * (B + 1) + b + 1];
             const int64_t L = (int64_t)cu[b + 1] - cu[b];
-            for (int64_t i = lo; i < hi; ++i) c += causal ? (int64_t)zp.perm[i] - cu[b] + 1 : L;
+            for (int64_t i = lo; i < hi; ++i) {
+                // keys of the document in [first, last]
+                const int64_t pos = zp.perm[i];
+                int64_t first = cu[b];
+                const int64_t last = causal ? pos : (int64_t)cu[b] + L - 1;
+                if (window >= 0 && pos - window > first) first = pos - window;
+                if (last >= first) c += last - first + 1;
+            }
         }
         counts[r] = c;
     }
@@ -451,10 +458,24 @@ size_t ra_partial_workspace_bytes(int64_t Tq, int64_t Tk, int nseg, int Hq, int 
 
 ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, int dtype, int64_t Tq, int64_t Tk,
                                  int Hq, int Hkv, int d, const int32_t *cu_q, const int32_t *cu_k, int nseg,
-                                 const int32_t *q_pos, const int32_t *k_pos, int causal, float scale, float *out,
-                                 float *lse, void *workspace, size_t ws_bytes, void *stream) {
+                                 const int32_t *q_pos, const int32_t *k_pos, int causal, int window, float scale,
+                                 float *out, float *lse, void *workspace, size_t ws_bytes, void *stream) {
     ra_status st = check_common(dtype, Hq, Hkv, d);
     if (st) return st;
+    if (window >= 0) {
+        // the kernels take position + window in 32-bit arithmetic
+        const int32_t lim = 1 << 30;
+        if (window >= lim) {
+            window = -1;  // reaches back further than any position
+        } else {
+            for (int64_t i = 0; i < Tq; ++i)
+                if ((q_pos ? q_pos[i] : i) >= lim || (q_pos && q_pos[i] < 0))
+                    return fail(RA_ERR_UNSUPPORTED, "with a window, positions must be in [0, 2^30)");
+            for (int64_t i = 0; i < Tk; ++i)
+                if ((k_pos ? k_pos[i] : i) >= lim || (k_pos && k_pos[i] < 0))
+                    return fail(RA_ERR_UNSUPPORTED, "with a window, positions must be in [0, 2^30)");
+        }
+    }
     if (Tq < 0 || Tk < 0 || Tq > INT32_MAX || Tk > INT32_MAX) return fail(RA_ERR_INVALID_ARG, "bad Tq/Tk");
     if (nseg < 1) return fail(RA_ERR_INVALID_ARG, "nseg must be >= 1");
     if ((st = validate_cu(cu_q, nseg, Tq))) return st;
@@ -472,7 +493,7 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
     Carver cv(workspace);
     if (tc) {
         TilePlan tp;
-        if ((st = build_partial_tiles(cu_q, cu_k, nseg, q_pos, k_pos, Tq, Tk, G, Hkv, causal, tp))) return st;
+        if ((st = build_partial_tiles(cu_q, cu_k, nseg, q_pos, k_pos, Tq, Tk, G, Hkv, causal, window, tp))) return st;
         DeviceTables dt;
         pack_tables(nullptr, &tp, dt);
         void *tab = cv.take(dt.blob.size());
@@ -498,6 +519,7 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
         a.t0 = 0;
         a.t1 = 1;
         a.causal = causal;
+        a.window = window;
         a.scale = scale;
         a.out_mode = kOutPartial;
         a.out = out;
@@ -549,6 +571,7 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
     a.t0 = 0;
     a.t1 = 1;
     a.causal = causal;
+    a.window = window;
     a.scale = scale;
     a.out_mode = kOutPartial;
     a.out = out;
@@ -602,6 +625,17 @@ RingLayout ring_layout(const RingPlan &plan, int64_t T, int Hq, int Hkv, int d, 
     return L;
 }
 
+// A window >= T reaches every earlier key of every document: no window.
+// Positions (< T) plus the window must fit the kernels' 32-bit arithmetic.
+static ra_status ring_window(int64_t T, int *window) {
+    if (*window < 0 || *window >= T) {
+        *window = -1;
+        return RA_OK;
+    }
+    if (T >= ((int64_t)1 << 30)) return fail(RA_ERR_UNSUPPORTED, "with a window, T must be < 2^30");
+    return RA_OK;
+}
+
 ra_status ring_checks(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
                       const int32_t *cu, int B, int cp, int mode, int sched, float scale) {
     ra_status st = check_common(dtype, Hq, Hkv, d);
@@ -625,14 +659,14 @@ size_t ra_ring_workspace_bytes(int64_t T, int Hq, int Hkv, int d, int dtype, con
     if (check_common(dtype, Hq, Hkv, d) != RA_OK || T < 0) return 0;
     ra_status st;
     const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
-    auto plan = get_ring_plan(cu, B, cp, mode, Hq / Hkv, Hkv, 1, tc, &st);
+    auto plan = get_ring_plan(cu, B, cp, mode, Hq / Hkv, Hkv, 1, -1, tc, &st);  // sizes: mask-independent
     if (!plan) return 0;
     return ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, bwd).total;
 }
 
 ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
-                           const int32_t *cu, int B, int cp, int mode, int causal, float scale, int sched, void *out,
-                           float *lse, void *workspace, size_t ws_bytes, void *stream) {
+                           const int32_t *cu, int B, int cp, int mode, int causal, int window, float scale, int sched,
+                           void *out, float *lse, void *workspace, size_t ws_bytes, void *stream) {
     ra_status st = ring_checks(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, sched, scale);
     if (st) return st;
     if (T == 0) return RA_OK;
@@ -640,7 +674,8 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     if (!aligned16(out)) return fail(RA_ERR_UNSUPPORTED, "out must be 16-byte aligned");
     const int G = Hq / Hkv;
     const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
-    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, 1, tc, &st);
+    if ((st = ring_window(T, &window))) return st;
+    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, &st);
     if (!plan) return st;
     const RingLayout L = ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, 0);
     if (!workspace || ws_bytes < L.total)
@@ -690,6 +725,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
             a.t0 = t0;
             a.t1 = t1;
             a.causal = causal;
+            a.window = window;
             a.scale = scale;
             a.out_mode = out_mode;
             a.out = o;
@@ -716,9 +752,10 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
             a.kpos = perm;
             a.cp = cp;
             a.B = B;
-            a.t0 = t0;
+            a.t0 = t0 < 0 ? 0 : t0;  // the SIMT kernel walks [t0, t1) for every row
             a.t1 = t1;
             a.causal = causal;
+            a.window = window;
             a.scale = scale;
             a.out_mode = out_mode;
             a.out = o;
@@ -732,8 +769,9 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
 
     if (sched == RA_SCHED_FUSED) {
         // a4+a5+a6 in one launch: ring order inside each tile, on-chip merge,
-        // rows written straight back to their original positions.
-        return run_partial(0, cp, kOutFinal, out, lse, T);
+        // rows written straight back to their original positions.  t0 = -1:
+        // each item walks only the ring steps that hold its visited KV tiles.
+        return run_partial(-1, cp, kOutFinal, out, lse, T);
     }
     // STEPWISE: one launch per ring step into fp32 partials (local order),
     // then the n-way LSE merge, then un-permute O and LSE.
@@ -764,7 +802,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
 }
 
 ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
-                           const int32_t *cu, int B, int cp, int mode, int causal, float scale, int sched,
+                           const int32_t *cu, int B, int cp, int mode, int causal, int window, float scale, int sched,
                            const void *out, const float *lse, const void *dout, void *dq, void *dk, void *dv,
                            int grad_dtype, int flags, void *workspace, size_t ws_bytes, void *stream) {
     ra_status st = ring_checks(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, sched, scale);
@@ -776,7 +814,8 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         return fail(RA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned");
     const int G = Hq / Hkv;
     const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
-    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, 1, tc, &st);
+    if ((st = ring_window(T, &window))) return st;
+    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, &st);
     if (!plan) return st;
     const RingLayout L = ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, 1);
     if (!workspace || ws_bytes < L.total)
@@ -856,6 +895,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         a.cp = cp;
         a.B = B;
         a.causal = causal;
+        a.window = window;
         a.scale = scale;
         a.tile_ld = tld;
         TcDqArgs qa{};
@@ -875,18 +915,19 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         qa.cp = cp;
         qa.B = B;
         qa.causal = causal;
+        qa.window = window;
         qa.scale = scale;
         qa.lse = lse;
         qa.D = D;
         qa.lse_T = T;
         if (fused_tc) {
-            a.t0 = 0;
+            a.t0 = -1;  // each item's own range of ring steps with visited tiles
             a.t1 = cp;
             // complete per KV tile: written once in the gradient dtype
             a.dk = dk;
             a.dv = dv;
             a.out_mode = grad_dtype == RA_BF16 ? 0 : 1;
-            qa.t0 = 0;
+            qa.t0 = -1;
             qa.t1 = cp;
             qa.dq = dq;  // complete per query tile: written once in the gradient dtype
             qa.out_mode = grad_dtype == RA_BF16 ? 0 : 1;
@@ -952,6 +993,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         a.cp = cp;
         a.B = B;
         a.causal = causal;
+        a.window = window;
         a.scale = scale;
         a.lse = lse;
         a.D = D;

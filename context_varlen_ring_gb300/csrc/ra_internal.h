@@ -74,22 +74,27 @@ struct TilePlan {
 void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_t hi,
                   int tile_rows, int seg);
 
-// Tile-pair class used by both the host cost model and the kernels.
+// Tile-pair class used by both the host cost model and the kernels: skip
+// when no pair is allowed (every key after every query under the causal
+// mask, or further behind every query than the window), full when every
+// pair of a 128-key tile is allowed.  window < 0: no window.
 enum { kSkip = 0, kFull = 1, kPartial = 2 };
-inline int classify(const Tile &q, const Tile &k, int causal) {
+inline int classify(const Tile &q, const Tile &k, int causal, int window) {
     if (q.len <= 0 || k.len <= 0) return kSkip;
     if (causal && q.pmax < k.pmin) return kSkip;
-    if (k.len == kBN && (!causal || q.pmin >= k.pmax)) return kFull;
+    if (window >= 0 && (int64_t)q.pmin - window > k.pmax) return kSkip;
+    if (k.len == kBN && (!causal || q.pmin >= k.pmax) && (window < 0 || (int64_t)q.pmax - window <= k.pmin))
+        return kFull;
     return kPartial;
 }
 
 // Ring tile plan: query side = key side = the permuted buffer.
-ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, TilePlan &tp);
+ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, TilePlan &tp);
 
 // Generic partial's tile plan: one "rank", separate Q and K sides.
 ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg,
                               const int32_t *q_pos, const int32_t *k_pos, int64_t Tq, int64_t Tk,
-                              int G, int Hkv, int causal, TilePlan &tp);
+                              int G, int Hkv, int causal, int window, TilePlan &tp);
 
 // Host image of the device tables, uploaded into the workspace each call.
 struct DeviceTables {
@@ -127,9 +132,9 @@ struct RingPlan {
 // `stream` (a cudaStream_t).  Under stream capture the plan must already
 // have its page-locked copy (an earlier call outside capture made it).
 ra_status upload_plan_tables(RingPlan &plan, void *dst, void *stream);
-// Cached plans keyed by content (cu_seqlens, cp, mode, G, Hkv, causal).
+// Cached plans keyed by content (cu_seqlens, cp, mode, G, Hkv, causal, window).
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
-                                        int causal, bool want_tiles, ra_status *st);
+                                        int causal, int window, bool want_tiles, ra_status *st);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -85,6 +85,7 @@ struct SimtArgs {
     const int32_t *koff, *kcul, *kpos;
     int cp, B, t0, t1;
     int causal;
+    int window;                        // sliding window (keys at most this far behind), < 0: none
     float scale;
     int out_mode;
     void *out;
@@ -100,6 +101,7 @@ struct SimtBwdArgs {
     const int32_t *off, *cul, *pos;    // ring over cp ranks, q side = k side
     int cp, B, t0, t1;
     int causal;
+    int window;                        // sliding window (keys at most this far behind), < 0: none
     float scale;
     const float *lse, *D;              // [Hq, lse_T] indexed by position
     int64_t lse_T;
@@ -121,6 +123,7 @@ struct TcFwdArgs {
     int cp, B;
     int t0, t1;                        // >= 0: override every item's step range
     int causal;
+    int window;                        // sliding window (keys at most this far behind), < 0: none
     float scale;
     int out_mode;
     void *out;
@@ -143,6 +146,7 @@ struct TcBwdArgs {
     int cp, B;
     int t0, t1;                        // >= 0: override every item's step range
     int causal;
+    int window;                        // sliding window (keys at most this far behind), < 0: none
     float scale;
     const float *tile_ld;              // launch_tile_lse_d output for these tiles
     void *dk, *dv;                     // [T, Hkv, d] at original positions
@@ -163,6 +167,7 @@ struct TcDqArgs {
     int cp, B;
     int t0, t1;
     int causal;
+    int window;                        // sliding window (keys at most this far behind), < 0: none
     float scale;
     const float *lse, *D;              // [Hq, lse_T] at original positions
     int64_t lse_T;

@@ -55,7 +55,7 @@ extern "C" ra_status ra_varlen_attn_partial_noalloc(const void *q, const void *k
                                                     int64_t Tq, int64_t Tk, int Hq, int Hkv, int d,
                                                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
                                                     int nseg, const int32_t *q_pos, const int32_t *k_pos,
-                                                    int causal, float scale, float *out, float *lse,
+                                                    int causal, int window, float scale, float *out, float *lse,
                                                     void *stream) {
     using namespace ra;
     const size_t need = ra_partial_workspace_bytes(Tq, Tk, nseg, Hq, Hkv, d, dtype);
@@ -71,5 +71,5 @@ extern "C" ra_status ra_varlen_attn_partial_noalloc(const void *q, const void *k
     // `stream` before the launch), so nothing in the shared array has to
     // start at zero.  Calls that overlap on the GPU share the array and race.
     return ra_varlen_attn_partial(q, k, v, dtype, Tq, Tk, Hq, Hkv, d, cu_seqlens_q, cu_seqlens_k, nseg, q_pos,
-                                  k_pos, causal, scale, out, lse, scratch, RA_NOALLOC_SCRATCH_BYTES, stream);
+                                  k_pos, causal, window, scale, out, lse, scratch, RA_NOALLOC_SCRATCH_BYTES, stream);
 }

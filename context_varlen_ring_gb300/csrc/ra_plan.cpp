@@ -118,7 +118,7 @@ void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_
 
 // Forward items: pairs of consecutive query tiles of one (rank, segment),
 // replicated over KV heads; backward items: one per KV tile and KV head.
-static void build_items(TilePlan &tp, int Hkv, int causal) {
+static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
     const int cp = tp.cp, B = tp.B;
     tp.items.clear();
     tp.bitems.clear();
@@ -139,8 +139,8 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
                     const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
                     int64_t c_t = 0;
                     for (int j = ka; j < ke; ++j) {
-                        c_t += classify(tp.qtiles[i], tp.kvtiles[j], causal) != kSkip;
-                        if (q1 >= 0) c_t += classify(tp.qtiles[q1], tp.kvtiles[j], causal) != kSkip;
+                        c_t += classify(tp.qtiles[i], tp.kvtiles[j], causal, window) != kSkip;
+                        if (q1 >= 0) c_t += classify(tp.qtiles[q1], tp.kvtiles[j], causal, window) != kSkip;
                     }
                     if (c_t) {
                         tf = std::min(tf, t);
@@ -161,7 +161,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
                         const int s2 = ((r - t) % cp + cp) % cp;
                         const int ka = tp.kv_off[seg_idx(s2, b)], ke = tp.kv_off[seg_idx(s2, b) + 1];
                         int64_t c_t = 0;
-                        for (int j = ka; j < ke; ++j) c_t += classify(tp.qtiles[qi], tp.kvtiles[j], causal) != kSkip;
+                        for (int j = ka; j < ke; ++j) c_t += classify(tp.qtiles[qi], tp.kvtiles[j], causal, window) != kSkip;
                         if (c_t) {
                             qf = std::min(qf, t);
                             ql = t + 1;
@@ -188,7 +188,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
                     const int r = (s + t) % cp;
                     const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
                     int64_t c_t = 0;
-                    for (int i = qa; i < qe; ++i) c_t += classify(tp.qtiles[i], tp.kvtiles[j], causal) != kSkip;
+                    for (int i = qa; i < qe; ++i) c_t += classify(tp.qtiles[i], tp.kvtiles[j], causal, window) != kSkip;
                     if (c_t) {
                         tf = std::min(tf, t);
                         tl = t + 1;
@@ -230,7 +230,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal) {
     });
 }
 
-ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, TilePlan &tp) {
+ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, TilePlan &tp) {
     if (G < 1 || kBM % G != 0) return fail(RA_ERR_UNSUPPORTED, "GQA group must divide 128");
     tp = TilePlan();
     tp.cp = zp.cp;
@@ -252,13 +252,13 @@ ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, Til
     }
     tp.q_off.back() = (int32_t)tp.qtiles.size();
     tp.kv_off.back() = (int32_t)tp.kvtiles.size();
-    build_items(tp, Hkv, causal);
+    build_items(tp, Hkv, causal, window);
     return RA_OK;
 }
 
 ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg,
                               const int32_t *q_pos, const int32_t *k_pos, int64_t Tq, int64_t Tk,
-                              int G, int Hkv, int causal, TilePlan &tp) {
+                              int G, int Hkv, int causal, int window, TilePlan &tp) {
     if (G < 1 || kBM % G != 0) return fail(RA_ERR_UNSUPPORTED, "GQA group must divide 128");
     ra_status st = validate_cu(cu_q, nseg, Tq);
     if (st) return st;
@@ -279,7 +279,7 @@ ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg
     }
     tp.q_off.back() = (int32_t)tp.qtiles.size();
     tp.kv_off.back() = (int32_t)tp.kvtiles.size();
-    build_items(tp, Hkv, causal);
+    build_items(tp, Hkv, causal, window);
     return RA_OK;
 }
 
@@ -325,7 +325,7 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
 }
 
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
-                                        int causal, bool want_tiles, ra_status *st) {
+                                        int causal, int window, bool want_tiles, ra_status *st) {
     static std::mutex mu;
     static std::map<std::string, std::shared_ptr<RingPlan>> cache;
     static std::vector<std::string> order;
@@ -333,7 +333,7 @@ std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mo
     if (*st) return nullptr;
     std::string key;
     key.append(reinterpret_cast<const char *>(cu), sizeof(int32_t) * (size_t)(B + 1));
-    int32_t tail[7] = {B, cp, mode, G, Hkv, causal, want_tiles ? 1 : 0};
+    int32_t tail[8] = {B, cp, mode, G, Hkv, causal, window, want_tiles ? 1 : 0};
     key.append(reinterpret_cast<const char *>(tail), sizeof(tail));
     {
         std::lock_guard<std::mutex> lk(mu);
@@ -344,7 +344,7 @@ std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mo
     *st = build_zigzag(cu, B, cp, mode, plan->zz);
     if (*st) return nullptr;
     if (want_tiles) {
-        *st = build_ring_tiles(plan->zz, G, Hkv, causal, plan->tiles);
+        *st = build_ring_tiles(plan->zz, G, Hkv, causal, window, plan->tiles);
         if (*st) return nullptr;
         plan->has_tiles = true;
     }

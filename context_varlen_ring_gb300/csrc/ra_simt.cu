@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(256) simt_fwd_kernel(SimtArgs a) {
             const int64_t j0 = a.koff[s] + kc[b], j1 = a.koff[s] + kc[b + 1];
             for (int64_t j = j0; j < j1; ++j) {
                 if (a.causal && a.kpos[j] > qp) continue;
+                if (a.window >= 0 && (int64_t)a.kpos[j] < (int64_t)qp - a.window) continue;
                 float part = 0.f;
 #pragma unroll
                 for (int e = 0; e < NV; ++e) part += qv[e] * ld_f(K + (j * a.Hkv + g) * a.d + lane + 32 * e);
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(256) simt_bwd_dq_kernel(SimtBwdArgs a) {
                 const int64_t j0 = a.off[s] + kc[b], j1 = a.off[s] + kc[b + 1];
                 for (int64_t j = j0; j < j1; ++j) {
                     if (a.causal && a.pos[j] > qp) continue;
+                    if (a.window >= 0 && (int64_t)a.pos[j] < (int64_t)qp - a.window) continue;
                     float ps = 0.f, pd = 0.f;
 #pragma unroll
                     for (int e = 0; e < NV; ++e) {
@@ -195,6 +197,7 @@ __global__ void __launch_bounds__(256) simt_bwd_dkv_kernel(SimtBwdArgs a) {
             for (int64_t i = i0; i < i1; ++i) {
                 const int32_t qp = a.pos[i];
                 if (a.causal && kp > qp) continue;
+                if (a.window >= 0 && (int64_t)kp < (int64_t)qp - a.window) continue;
                 for (int h = g * G; h < (g + 1) * G; ++h) {
                     const float lse = a.lse[(int64_t)h * a.lse_T + qp];
                     if (lse == -INFINITY) continue;

@@ -75,7 +75,7 @@ struct BwdParams {
     const int4 *qtiles, *kvtiles, *items;
     const int *q_off;
     int n_items, cp, B, G, log2G, Hq, Hkv;
-    int t0, t1, causal, out_mode;                  // 0 bf16 store, 1 fp32 store, 2 fp32 +=
+    int t0, t1, causal, window, out_mode;          // 0 bf16 store, 1 fp32 store, 2 fp32 +=
     float scale, scale_log2;
     const float *tile_ld;
     void *dk, *dv;
@@ -87,10 +87,12 @@ struct QInfo {
     int len, pmin, pmax;
 };
 
-__device__ __forceinline__ int classify_pair(const QInfo &q, int klen, int kpmin, int kpmax, int causal) {
+__device__ __forceinline__ int classify_pair(const QInfo &q, int klen, int kpmin, int kpmax, int causal,
+                                             int window) {
     if (q.len <= 0 || klen <= 0) return kSkip;
     if (causal && q.pmax < kpmin) return kSkip;
-    if (klen == kBN && (!causal || q.pmin >= kpmax)) return kFull;
+    if (window >= 0 && q.pmin - window > kpmax) return kSkip;
+    if (klen == kBN && (!causal || q.pmin >= kpmax) && (window < 0 || q.pmax - window <= kpmin)) return kFull;
     return kPartial;
 }
 
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                 if (idx < hi) {
                     qa = __ldg(p.qtiles + 2 * idx);
                     qb = __ldg(p.qtiles + 2 * idx + 1);
-                    cls = classify_pair(QInfo{qa.y, qb.y, qb.z}, ka.y, kb.y, kb.z, p.causal);
+                    cls = classify_pair(QInfo{qa.y, qb.y, qb.z}, ka.y, kb.y, kb.z, p.causal, p.window);
                 }
                 uint32_t vis = __ballot_sync(0xffffffffu, cls != kSkip);
                 while (vis && ok) {
@@ -343,6 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                     }
                     e1 = split;
                     e2 = qlen;
+                    if (p.window >= 0) {  // queries at most `window` ahead of this key
+                        e1 = min(max(kpos + p.window - pos0 + 1, 0), split);
+                        e2 = min(max(kpos + p.window - pos1 + split + 1, split), qlen);
+                    }
                 }
 #pragma unroll
                 for (int ch = 0; ch < 2; ++ch) {
@@ -514,6 +520,7 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
     p.t0 = a.t0;
     p.t1 = a.t1;
     p.causal = a.causal;
+    p.window = a.window;
     p.out_mode = a.out_mode;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;

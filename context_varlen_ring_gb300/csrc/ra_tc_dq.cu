@@ -71,7 +71,7 @@ struct DqParams {
     const int4 *qtiles, *kvtiles, *items;
     const int *kv_off;
     int n_items, cp, B, G, log2G, Hq;
-    int t0, t1, causal, out_mode;  // out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 +=
+    int t0, t1, causal, window, out_mode;  // out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 +=
     float scale, scale_log2, log2_scale;
     const float *lse, *D;
     long long lse_T;
@@ -84,10 +84,12 @@ struct QInfo {
     int len, pmin, pmax;
 };
 
-__device__ __forceinline__ int classify_q(const QInfo &q, int klen, int kpmin, int kpmax, int causal) {
+// The host classifier's rule (skip / full / partial), on device.
+__device__ __forceinline__ int classify_q(const QInfo &q, int klen, int kpmin, int kpmax, int causal, int window) {
     if (q.len <= 0 || klen <= 0) return kSkip;
     if (causal && q.pmax < kpmin) return kSkip;
-    if (klen == kBN && (!causal || q.pmin >= kpmax)) return kFull;
+    if (window >= 0 && q.pmin - window > kpmax) return kSkip;
+    if (klen == kBN && (!causal || q.pmin >= kpmax) && (window < 0 || q.pmax - window <= kpmin)) return kFull;
     return kPartial;
 }
 
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         if (idx < hi) {
                             ka = __ldg(p.kvtiles + 2 * idx);
                             kb = __ldg(p.kvtiles + 2 * idx + 1);
-                            c = classify_q(q, ka.y, kb.y, kb.z, p.causal);
+                            c = classify_q(q, ka.y, kb.y, kb.z, p.causal, p.window);
                         }
                         uint32_t vis = __ballot_sync(0xffffffffu, c != kSkip);
                         while (vis && ok) {
@@ -520,8 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     P[c + 1] = ex2_approx(x.y);
                 }
                 if (cls == kPartial) {
+                    // allowed key columns [lo1, lim1) and [lo2, lim2) (causal
+                    // upper limits, window lower limits)
                     const int kt_len = e.y & 0xffff, kt_split = e.y >> 16, kt_pos0 = e.z, kt_pos1 = e.w;
-                    int lim1, lim2;
+                    int lim1, lim2, lo1 = 0, lo2 = kt_split;
                     if (p.causal) {
                         lim1 = min(max(qpos - kt_pos0 + 1, 0), kt_split);
                         lim2 = min(max(qpos - kt_pos1 + kt_split + 1, kt_split), kt_len);
@@ -529,11 +533,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         lim1 = kt_split;
                         lim2 = kt_len;
                     }
+                    if (p.window >= 0) {
+                        lo1 = min(max(qpos - p.window - kt_pos0, 0), kt_split);
+                        lo2 = min(max(qpos - p.window - kt_pos1 + kt_split, kt_split), kt_len);
+                    }
                     uint32_t wm[2];
 #pragma unroll
                     for (int ch = 0; ch < 2; ++ch) {
                         const int cb = 64 * h + 32 * ch;
-                        wm[ch] = range_bits(0, lim1, cb) | range_bits(kt_split, lim2, cb);
+                        wm[ch] = range_bits(lo1, lim1, cb) | range_bits(lo2, lim2, cb);
                     }
 #pragma unroll
                     for (int c = 0; c < 64; ++c) P[c] = ((wm[c >> 5] >> (c & 31)) & 1u) ? P[c] : 0.f;
@@ -674,6 +682,7 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
     p.t0 = a.t0;
     p.t1 = a.t1;
     p.causal = a.causal;
+    p.window = a.window;
     p.out_mode = a.out_mode;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;

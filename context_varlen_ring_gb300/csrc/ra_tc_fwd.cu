@@ -73,7 +73,7 @@ struct FwdParams {
     const int *kv_off;
     int *sched;  // [2]: next item to claim, CTAs finished (zero between launches)
     int n_items, cp, B, G, log2G, Hq;
-    int t0, t1, causal, out_mode;
+    int t0, t1, causal, window, out_mode;
     float scale_log2;
     void *out;
     float *lse;
@@ -95,10 +95,12 @@ struct QInfo {
     int len, pmin, pmax;
 };
 
-__device__ __forceinline__ int classify_q(const QInfo &q, int klen, int kpmin, int kpmax, int causal) {
+// The host classifier's rule (skip / full / partial), on device.
+__device__ __forceinline__ int classify_q(const QInfo &q, int klen, int kpmin, int kpmax, int causal, int window) {
     if (q.len <= 0 || klen <= 0) return kSkip;
     if (causal && q.pmax < kpmin) return kSkip;
-    if (klen == kBN && (!causal || q.pmin >= kpmax)) return kFull;
+    if (window >= 0 && q.pmin - window > kpmax) return kSkip;
+    if (klen == kBN && (!causal || q.pmin >= kpmax) && (window < 0 || q.pmax - window <= kpmin)) return kFull;
     return kPartial;
 }
 
@@ -289,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         if (idx < hi) {
                             ka = __ldg(p.kvtiles + 2 * idx);
                             kb = __ldg(p.kvtiles + 2 * idx + 1);
-                            c0 = classify_q(q0, ka.y, kb.y, kb.z, p.causal);
-                            c1 = has1 ? classify_q(q1, ka.y, kb.y, kb.z, p.causal) : kSkip;
+                            c0 = classify_q(q0, ka.y, kb.y, kb.z, p.causal, p.window);
+                            c1 = has1 ? classify_q(q1, ka.y, kb.y, kb.z, p.causal, p.window) : kSkip;
                         }
                         uint32_t vis = __ballot_sync(0xffffffffu, c0 != kSkip || c1 != kSkip);
                         while (vis && ok) {
@@ -514,10 +516,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(v[i]);
                 }
                 if (cls == kPartial) {
-                    // allowed columns: [0, lim1) in the first position run and
-                    // [split, lim2) in the second, as one bit per column
+                    // allowed columns: [lo1, lim1) in the first position run
+                    // and [lo2, lim2) in the second, as one bit per column
+                    // (the upper limits from the causal mask, the lower ones
+                    // from the window)
                     const int kt_len = e.y & 0xffff, kt_split = e.y >> 16, kt_pos0 = e.z, kt_pos1 = e.w;
-                    int lim1, lim2;
+                    int lim1, lim2, lo1 = 0, lo2 = kt_split;
                     if (p.causal) {
                         lim1 = min(max(qpos - kt_pos0 + 1, 0), kt_split);
                         lim2 = min(max(qpos - kt_pos1 + kt_split + 1, kt_split), kt_len);
@@ -525,9 +529,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         lim1 = kt_split;
                         lim2 = kt_len;
                     }
+                    if (p.window >= 0) {
+                        lo1 = min(max(qpos - p.window - kt_pos0, 0), kt_split);
+                        lo2 = min(max(qpos - p.window - kt_pos1 + kt_split, kt_split), kt_len);
+                    }
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
-                        const uint32_t w = range_bits(0, lim1, 32 * ch) | range_bits(kt_split, lim2, 32 * ch);
+                        const uint32_t w = range_bits(lo1, lim1, 32 * ch) | range_bits(lo2, lim2, 32 * ch);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) s[32 * ch + i] = ((w >> i) & 1u) ? s[32 * ch + i] : -INFINITY;
                     }
@@ -712,6 +720,7 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
     p.t0 = a.t0;
     p.t1 = a.t1;
     p.causal = a.causal;
+    p.window = a.window;
     p.out_mode = a.out_mode;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.out = a.out;

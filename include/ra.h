@@ -106,9 +106,13 @@ ra_status ra_zigzag_unpermute(const void *y, void *x, const int32_t *perm,
  * ("[Train] Support custom attention with context parallel", FlagScale
  * PR #910: RingAttention with a swappable forward_impl; this is that
  * step).  Allowed pairs:
- *   (i, j) with seg(i) == seg(j) and (causal == 0 or k_pos[j] <= q_pos[i]),
+ *   (i, j) with seg(i) == seg(j) and (causal == 0 or k_pos[j] <= q_pos[i])
+ *          and (window < 0 or k_pos[j] >= q_pos[i] - window),
  * where seg is given by cu_seqlens_q / cu_seqlens_k (segment b of Q pairs
- * with segment b of K, nseg segments each).
+ * with segment b of K, nseg segments each).  window: the sliding window,
+ * the number of positions a key may lie behind its query (the window_size
+ * argument of the cuDNN flash-attention call in "Add Context Parallelism
+ * support to cudnn Flash Attention #1133", maxtext); -1 = no window.
  *   q   DEVICE [Tq, Hq, d]      dtype RA_BF16 or RA_FP32
  *   k,v DEVICE [Tk, Hkv, d]     same dtype
  *   cu_seqlens_q, cu_seqlens_k  HOST [nseg+1]
@@ -124,7 +128,7 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
                                  int64_t Tq, int64_t Tk, int Hq, int Hkv, int d,
                                  const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int nseg,
                                  const int32_t *q_pos, const int32_t *k_pos,
-                                 int causal, float scale,
+                                 int causal, int window, float scale,
                                  float *out, float *lse,
                                  void *workspace, size_t ws_bytes, void *stream);
 
@@ -156,7 +160,7 @@ ra_status ra_varlen_attn_partial_noalloc(const void *q, const void *k, const voi
                                          int64_t Tq, int64_t Tk, int Hq, int Hkv, int d,
                                          const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int nseg,
                                          const int32_t *q_pos, const int32_t *k_pos,
-                                         int causal, float scale,
+                                         int causal, int window, float scale,
                                          float *out, float *lse, void *stream);
 
 /* ------------------------------------------------------------------------
@@ -201,7 +205,9 @@ ra_status ra_lse_merge(int n_parts, const float *const *outs, const float *const
  *   dq DEVICE [T, Hq, d], dk, dv DEVICE [T, Hkv, d] of grad_dtype
  *   (RA_BF16 or RA_FP32; dK/dV are always accumulated in fp32).
  * scale: softmax scale; pass 1/sqrt(d) for the usual attention (maxtext
- * PR #1133, cudnn_flash_attention diff).  cp >= 1.
+ * PR #1133, cudnn_flash_attention diff).  cp >= 1.  window: sliding window
+ * as in ra_varlen_attn_partial (-1 = none); positions are the original
+ * (unpermuted) token indices, so the zigzag reorder leaves the mask intact.
  * workspace: DEVICE, >= ra_ring_workspace_bytes(...) for the same arguments.
  * Asynchronous on `stream`.  The backward's fused tensor-core path runs its
  * key-side kernel on a second, library-owned stream forked from and joined
@@ -216,7 +222,7 @@ size_t ra_ring_workspace_bytes(int64_t T, int Hq, int Hkv, int d, int dtype,
 ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtype,
                            int64_t T, int Hq, int Hkv, int d,
                            const int32_t *cu_seqlens, int B, int cp, int zz_mode,
-                           int causal, float scale, int sched,
+                           int causal, int window, float scale, int sched,
                            void *out, float *lse,
                            void *workspace, size_t ws_bytes, void *stream);
 /* flags of ra_ring_attn_bwd.
@@ -232,7 +238,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
 ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtype,
                            int64_t T, int Hq, int Hkv, int d,
                            const int32_t *cu_seqlens, int B, int cp, int zz_mode,
-                           int causal, float scale, int sched,
+                           int causal, int window, float scale, int sched,
                            const void *out, const float *lse, const void *dout,
                            void *dq, void *dk, void *dv, int grad_dtype, int flags,
                            void *workspace, size_t ws_bytes, void *stream);
@@ -243,9 +249,10 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
  * Allowed (query, key) pairs each simulated rank computes over the whole
  * ring: the causal load that zigzag balances ("Question about varlen ring
  * attention", MiniMax-01 #6: causal imbalance; ring-attention-pytorch #20:
- * zigzag spreads it).  counts HOST [cp] int64.
+ * zigzag spreads it).  window as in ra_varlen_attn_partial (-1 = none).
+ * counts HOST [cp] int64.
  * ------------------------------------------------------------------------ */
-ra_status ra_ring_rank_pairs(const int32_t *cu_seqlens, int B, int cp, int zz_mode, int causal,
+ra_status ra_ring_rank_pairs(const int32_t *cu_seqlens, int B, int cp, int zz_mode, int causal, int window,
                              int64_t *counts);
 
 /* Reads and clears the device status word of the current device (waits for

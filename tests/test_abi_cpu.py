@@ -90,7 +90,7 @@ def test_invalid_arguments_return_status(ra):
     args = dict(dt=_lib.RA_BF16, T=8, hq=4, hkv=2, d=128)
 
     def fwd(cu, T=8, hq=4, hkv=2, d=128, cp=2, mode=0, sched=0, dt=_lib.RA_BF16, q=fake):
-        return L.ra_ring_attn_fwd(q, fake, fake, dt, T, hq, hkv, d, _p(cu), len(cu) - 1, cp, mode, 1, 0.1, sched,
+        return L.ra_ring_attn_fwd(q, fake, fake, dt, T, hq, hkv, d, _p(cu), len(cu) - 1, cp, mode, 1, -1, 0.1, sched,
                                   fake, fake, ws, 1 << 40, None)
     assert fwd(np.array([0, 7], np.int32)) == _lib.RA_ERR_INVALID_ARG          # cu[B] != T
     assert fwd(np.array([0, 8], np.int32), hq=3) == _lib.RA_ERR_INVALID_ARG    # Hq % Hkv
@@ -102,7 +102,7 @@ def test_invalid_arguments_return_status(ra):
     assert fwd(np.array([0, 8], np.int32), q=ctypes.c_void_p(258)) == _lib.RA_ERR_UNSUPPORTED  # misaligned
     # too-small workspace is caught before launching
     cu = np.array([0, 8], np.int32)
-    rc = L.ra_ring_attn_fwd(fake, fake, fake, _lib.RA_BF16, 8, 4, 2, 128, _p(cu), 1, 2, 0, 1, 0.1, 0, fake, fake,
+    rc = L.ra_ring_attn_fwd(fake, fake, fake, _lib.RA_BF16, 8, 4, 2, 128, _p(cu), 1, 2, 0, 1, -1, 0.1, 0, fake, fake,
                             ws, 16, None)
     assert rc == _lib.RA_ERR_WORKSPACE
     # merge argument checks
@@ -121,3 +121,18 @@ def test_workspace_sizes(ra):
     assert qkv < f < qkv + (64 << 20)
     assert s > f + 8 * 32768 * 32 * 128 * 4
     assert b > f
+
+
+def test_ring_rank_pairs_window_matches_oracle(orc):
+    """The library's per-rank pair counts under a sliding window equal the
+    oracle's (host logic, no GPU)."""
+    import context_varlen_ring_gb300 as ra
+    rng = np.random.default_rng(21)
+    for _ in range(4):
+        cu = W.cu_seqlens(W.random_doc_lens(rng, 5000, 1, 900))
+        for cp in (1, 3, 8):
+            for mode in (0, 1):
+                for causal in (True, False):
+                    for window in (0, 13, 256, 10**6):
+                        assert np.array_equal(ra.ring_rank_pairs(cu, cp, mode, causal, window),
+                                              orc.rank_pairs(cu, cp, mode, causal, window))

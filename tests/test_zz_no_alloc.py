@@ -56,13 +56,13 @@ def _run_both(L, cuq, cuk, qpos, kpos, q, k, v):
     ref_l = torch.empty((hq, Tq), dtype=torch.float32, device="cuda")
     ws = torch.empty(L.ra_partial_workspace_bytes(Tq, Tk, nseg, hq, hkv, d, 0), dtype=torch.uint8, device="cuda")
     rc = L.ra_varlen_attn_partial(_p(q), _p(k), _p(v), 0, Tq, Tk, hq, hkv, d, _p(cuq), _p(cuk), nseg, _p(qpos),
-                                  _p(kpos), 1, scale, _p(ref_o), _p(ref_l), _p(ws), ws.numel(), stream)
+                                  _p(kpos), 1, -1, scale, _p(ref_o), _p(ref_l), _p(ws), ws.numel(), stream)
     assert rc == 0, L.ra_last_error()
     # fill the outputs with garbage first: the entry point must write them in full
     out = torch.full((Tq, hq, d), float("nan"), device="cuda")
     lse = torch.full((hq, Tq), float("nan"), device="cuda")
     rc = L.ra_varlen_attn_partial_noalloc(_p(q), _p(k), _p(v), 0, Tq, Tk, hq, hkv, d, _p(cuq), _p(cuk), nseg,
-                                          _p(qpos), _p(kpos), 1, scale, _p(out), _p(lse), stream)
+                                          _p(qpos), _p(kpos), 1, -1, scale, _p(out), _p(lse), stream)
     assert rc == 0, L.ra_last_error()
     torch.cuda.synchronize()
     assert L.ra_get_device_status(stream) == 0
@@ -90,6 +90,6 @@ def test_noalloc_rejects_oversize_problem(L):
     assert need > (8 << 20)
     fake = ctypes.c_void_p(256)  # never dereferenced: the size check comes first
     rc = L.ra_varlen_attn_partial_noalloc(fake, fake, fake, 0, big, big, 32, 8, 128, _p(cu), _p(cu), 1, None, None,
-                                          1, 0.1, fake, fake, None)
+                                          1, -1, 0.1, fake, fake, None)
     assert rc == 4  # RA_ERR_WORKSPACE
     assert b"static" in L.ra_last_error()
