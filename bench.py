@@ -47,9 +47,16 @@ def peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
-def pairs_of(cu) -> int:
+def pairs_of(cu, window: int = -1) -> int:
+    """Allowed causal (query, key) pairs of a packing; with a sliding window
+    a query sees at most window + 1 keys (itself included)."""
     L = np.diff(np.asarray(cu, dtype=np.int64))
-    return int((L * (L + 1) // 2).sum())
+    if window < 0:
+        return int((L * (L + 1) // 2).sum())
+    w1 = window + 1
+    short = L <= w1
+    return int((L[short] * (L[short] + 1) // 2).sum() +
+               (w1 * (w1 + 1) // 2 + (L[~short] - w1) * w1).sum())
 
 
 class Clocks:
@@ -117,7 +124,7 @@ def cpu_sample_docs(lens):
     return sorted(pick)
 
 
-def run_cpu_oracle(wl, steps=1):
+def run_cpu_oracle(wl, steps=1, window=-1):
     """fwd+bwd of the sampled documents with the fp64 oracle; returns
     (TFLOP/s, seconds per step, cores, sample description)."""
     import torch
@@ -134,13 +141,13 @@ def run_cpu_oracle(wl, steps=1):
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        o, l = oracle.attn_fwd(q, k, v, cu, True, wl.scale)
-        oracle.attn_bwd(q, k, v, o, l, do, cu, True, wl.scale)
+        o, l = oracle.attn_fwd(q, k, v, cu, True, wl.scale, window=window)
+        oracle.attn_bwd(q, k, v, o, l, do, cu, True, wl.scale, window=window)
         times.append(time.perf_counter() - t0)
     sec = statistics.median(times)
-    flops = 14 * wl.d * wl.hq * pairs_of(cu)
+    flops = 14 * wl.d * wl.hq * pairs_of(cu, window)
     sample = (f"fp64 fwd+bwd of {len(lens)} of the {wl.B} documents ({T} of {wl.T} tokens, "
-              f"{pairs_of(cu)} of {pairs_of(wl.cu_seqlens())} causal pairs), all {wl.hq} heads")
+              f"{pairs_of(cu, window)} of {pairs_of(wl.cu_seqlens(), window)} allowed pairs), all {wl.hq} heads")
     return flops / sec / 1e12, sec, cores, sample
 
 
@@ -229,7 +236,7 @@ def fwd_configs(args, ra, torch):
         wl = W.ALL[name]
         cu = wl.cu_seqlens()
         T, hq, hkv, d = wl.T, wl.hq, wl.hkv, wl.d
-        pairs = pairs_of(cu)
+        pairs = pairs_of(cu, args.window)
         flops = 4 * d * hq * pairs
         q, k, v = (x.to(dev) for x in W.make_qkv(T, hq, hkv, d, wl.dtype))
         out = torch.empty_like(q)
@@ -237,7 +244,7 @@ def fwd_configs(args, ra, torch):
         ws = torch.empty(ra.ring_workspace_bytes(T, hq, hkv, d, 0 if wl.dtype == torch.bfloat16 else 1, cu, wl.cp,
                                                  wl.zz_mode, "fused", bwd=False), dtype=torch.uint8, device=dev)
         f = lambda: ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, "fused", out=out, lse=lse,
-                                     workspace=ws)
+                                     workspace=ws, window=args.window)
         for _ in range(max(args.warmup, 3)):
             f()
         torch.cuda.synchronize()
@@ -252,6 +259,7 @@ def fwd_configs(args, ra, torch):
         ms = e0.elapsed_time(e1) / args.steps
         tf = flops / (ms / 1e3) / 1e12
         print(json.dumps({"fwd_config": wl.name, "T": T, "Hq": hq, "Hkv": hkv, "d": d, "cp": wl.cp,
+                          "window": args.window,
                           "allowed_pairs_per_head": pairs, "ms": ms, "tflops": tf,
                           "frac_of_peak": tf / peak_burst, "peak_tflops": peak_burst, "peak_source": peak_src,
                           "steps": args.steps, "warmup": args.warmup}), flush=True)
@@ -269,6 +277,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--probe", action="store_true",
                     help="only W+K plain steps (for profilers): no e2e, per-kernel or CPU passes")
+    ap.add_argument("--window", type=int, default=-1,
+                    help="sliding window (a key at most this many positions behind its query); -1: none")
     ap.add_argument("--fwd-configs", default="",
                     help="comma list of forward-only workloads (e.g. C1,C2,C3) to time instead of the "
                          "fwd+bwd step; one JSON line each (not the headline line)")
@@ -302,7 +312,8 @@ def main():
     wl = W.C4
     cu = wl.cu_seqlens()
     T, hq, hkv, d = wl.T, wl.hq, wl.hkv, wl.d
-    pairs = pairs_of(cu)
+    pairs = pairs_of(cu, args.window)
+    win = dict(window=args.window)
     fwd_flops = 4 * d * hq * pairs
     bwd_flops = 10 * d * hq * pairs
     step_flops = fwd_flops + bwd_flops
@@ -317,12 +328,14 @@ def main():
     ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
 
     def step():
-        ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, out=out, lse=lse, workspace=ws)
-        ra.ring_attn_bwd(q, k, v, out, lse, do, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, dq=dq, dk=dk,
+        ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, out=out, lse=lse, workspace=ws,
+                         **win)
+        ra.ring_attn_bwd(q, k, v, out, lse, do, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, dq=dq, dk=dk, **win,
                          dv=dv, workspace=ws, reuse_fwd_workspace=True)
 
     def fwd_only():
-        ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, out=out, lse=lse, workspace=ws)
+        ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, out=out, lse=lse, workspace=ws,
+                         **win)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(max(args.warmup, 3)):
@@ -444,9 +457,9 @@ def main():
         stream.wait_event(ev["out_free"][b])
         q_, k_, v_, do_ = dev_in[b]
         o_, dq_, dk_, dv_, l_ = dev_out[b]
-        ra.ring_attn_fwd(q_, k_, v_, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, out=o_, lse=l_,
+        ra.ring_attn_fwd(q_, k_, v_, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, out=o_, lse=l_, **win,
                          workspace=ws)
-        ra.ring_attn_bwd(q_, k_, v_, o_, l_, do_, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, dq=dq_,
+        ra.ring_attn_bwd(q_, k_, v_, o_, l_, do_, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, dq=dq_, **win,
                          dk=dk_, dv=dv_, workspace=ws, reuse_fwd_workspace=True)
         ev["in_free"][b].record(stream)
         ev["out_ready"][b].record(stream)
@@ -485,7 +498,7 @@ def main():
 
     cpu = None
     if world == 1 and not args.no_cpu:
-        tf, sec, cores, sample = run_cpu_oracle(wl, steps=1)
+        tf, sec, cores, sample = run_cpu_oracle(wl, steps=1, window=args.window)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
                "sec_per_sample": sec}
 
@@ -493,7 +506,8 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "T": T, "docs": list(wl.doc_lens), "Hq": hq, "Hkv": hkv, "d": d,
+        "config": {"workload": wl.name + (f", sliding window {args.window}" if args.window >= 0 else ""),
+                   "window": args.window, "T": T, "docs": list(wl.doc_lens), "Hq": hq, "Hkv": hkv, "d": d,
                    "cp": wl.cp, "zigzag": "per-doc", "sched": args.sched, "causal_pairs_per_head": pairs,
                    "l2": "no flush: each step streams ~2.6 GB (Q, dO, O 268 MB each, fp32 dQ 537 MB, permuted "
                          "copies), far above the 129 MB L2",
