@@ -101,6 +101,8 @@ __device__ __forceinline__ uint32_t range_bits(int a, int b, int base) {
     return (uint32_t)(((1ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
 }
 
+// kWindow: compiled with the sliding-window mask (p.window >= 0).
+template <bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_constant__ BwdParams p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base_s = smem_u32(smem);
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                 if (idx < hi) {
                     qa = __ldg(p.qtiles + 2 * idx);
                     qb = __ldg(p.qtiles + 2 * idx + 1);
-                    cls = classify_pair(QInfo{qa.y, qb.y, qb.z}, ka.y, kb.y, kb.z, p.causal, p.window);
+                    cls = classify_pair(QInfo{qa.y, qb.y, qb.z}, ka.y, kb.y, kb.z, p.causal, kWindow ? p.window : -1);
                 }
                 uint32_t vis = __ballot_sync(0xffffffffu, cls != kSkip);
                 while (vis && ok) {
@@ -345,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                     }
                     e1 = split;
                     e2 = qlen;
-                    if (p.window >= 0) {  // queries at most `window` ahead of this key
+                    if (kWindow) {  // queries at most `window` ahead of this key
                         e1 = min(max(kpos + p.window - pos0 + 1, 0), split);
                         e2 = min(max(kpos + p.window - pos1 + split + 1, split), qlen);
                     }
@@ -533,11 +535,16 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
+        for (const void *fn : {(const void *)tc_dkdv_kernel<false>, (const void *)tc_dkdv_kernel<true>}) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+        }
         attr_set[dev] = true;
     }
-    tc_dkdv_kernel<<<a.n_items, kThreads, kSmemBytes, st>>>(p);
+    if (p.window >= 0)
+        tc_dkdv_kernel<true><<<a.n_items, kThreads, kSmemBytes, st>>>(p);
+    else
+        tc_dkdv_kernel<false><<<a.n_items, kThreads, kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 

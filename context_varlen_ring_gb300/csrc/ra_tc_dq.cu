@@ -99,6 +99,8 @@ __device__ __forceinline__ uint32_t range_bits(int a, int b, int base) {
 }
 
 
+// kWindow: compiled with the sliding-window mask (p.window >= 0).
+template <bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constant__ DqParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         if (idx < hi) {
                             ka = __ldg(p.kvtiles + 2 * idx);
                             kb = __ldg(p.kvtiles + 2 * idx + 1);
-                            c = classify_q(q, ka.y, kb.y, kb.z, p.causal, p.window);
+                            c = classify_q(q, ka.y, kb.y, kb.z, p.causal, kWindow ? p.window : -1);
                         }
                         uint32_t vis = __ballot_sync(0xffffffffu, c != kSkip);
                         while (vis && ok) {
@@ -533,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         lim1 = kt_split;
                         lim2 = kt_len;
                     }
-                    if (p.window >= 0) {
+                    if (kWindow) {
                         lo1 = min(max(qpos - p.window - kt_pos0, 0), kt_split);
                         lo2 = min(max(qpos - p.window - kt_pos1 + kt_split, kt_split), kt_len);
                     }
@@ -697,12 +699,14 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, tc_dq_kernel);
-        if (e != cudaSuccess) return e;
-        if (fa.numRegs < 168) return cudaErrorInvalidConfiguration;  // setmaxnreg split needs 168
+        for (const void *fn : {(const void *)tc_dq_kernel<false>, (const void *)tc_dq_kernel<true>}) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, fn);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs < 168) return cudaErrorInvalidConfiguration;  // setmaxnreg split needs 168
+        }
         attr_set[dev] = true;
     }
     // persistent: at most one CTA per SM (the shared memory allows one)
@@ -714,7 +718,10 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
         sm_count[dev] = n > 0 ? n : 1;
     }
     const int grid = std::min(a.n_items, (dev >= 0 && dev < 128) ? sm_count[dev] : 1);
-    tc_dq_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
+    if (p.window >= 0)
+        tc_dq_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p);
+    else
+        tc_dq_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -130,6 +130,10 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     }
 }
 
+// kWindow: compiled with the sliding-window mask (p.window >= 0); the
+// instantiation without it keeps the partial-tile path as short as before
+// (this kernel is sensitive to its instruction footprint).
+template <bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
@@ -291,8 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         if (idx < hi) {
                             ka = __ldg(p.kvtiles + 2 * idx);
                             kb = __ldg(p.kvtiles + 2 * idx + 1);
-                            c0 = classify_q(q0, ka.y, kb.y, kb.z, p.causal, p.window);
-                            c1 = has1 ? classify_q(q1, ka.y, kb.y, kb.z, p.causal, p.window) : kSkip;
+                            const int win = kWindow ? p.window : -1;
+                            c0 = classify_q(q0, ka.y, kb.y, kb.z, p.causal, win);
+                            c1 = has1 ? classify_q(q1, ka.y, kb.y, kb.z, p.causal, win) : kSkip;
                         }
                         uint32_t vis = __ballot_sync(0xffffffffu, c0 != kSkip || c1 != kSkip);
                         while (vis && ok) {
@@ -529,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         lim1 = kt_split;
                         lim2 = kt_len;
                     }
-                    if (p.window >= 0) {
+                    if (kWindow) {
                         lo1 = min(max(qpos - p.window - kt_pos0, 0), kt_split);
                         lo2 = min(max(qpos - p.window - kt_pos1 + kt_split, kt_split), kt_len);
                     }
@@ -732,15 +737,17 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        // The setmaxnreg split (128 x 80 + 256 x 200) needs the CTA to be
-        // launched with 168 registers per thread; with fewer, the increase
-        // could never be granted, so refuse to launch.
-        cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, tc_fwd_kernel);
-        if (e != cudaSuccess) return e;
-        if (fa.numRegs < 168) return cudaErrorInvalidConfiguration;
+        for (const void *fn : {(const void *)tc_fwd_kernel<false>, (const void *)tc_fwd_kernel<true>}) {
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+            // The setmaxnreg split (128 x 80 + 256 x 200) needs the CTA to be
+            // launched with 168 registers per thread; with fewer, the increase
+            // could never be granted, so refuse to launch.
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, fn);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs < 168) return cudaErrorInvalidConfiguration;
+        }
         attr_set[dev] = true;
     }
     // persistent: one CTA per SM (shared memory allows no more), each
@@ -752,7 +759,10 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
         sm_count[dev] = n > 0 ? n : 1;
     }
     const int grid = std::min(a.n_items, (dev >= 0 && dev < 128) ? sm_count[dev] : 1);
-    tc_fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(p);
+    if (p.window >= 0)
+        tc_fwd_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p);
+    else
+        tc_fwd_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 
