@@ -3,7 +3,8 @@
 // sm_103a.
 //
 // What it computes: from the saved log-sum-exp and D = rowsum(dO o O),
-//   P  = exp(scale * Q K^T - lse)   over allowed pairs
+//   P  = exp(scale * Q K^T - lse)   over allowed pairs (same document,
+//                                    causal, and inside the sliding window)
 //   dV = P^T dO,   dS = P o (dO V^T - D),   dK = scale * dS^T Q
 // with GQA sums over the query heads of each KV head (the key side of the
 // backward_impl of FlagScale PR #910's RingAttention; the query side, dQ, is

@@ -3,35 +3,42 @@
 //
 // What it computes: for every query row of every simulated CP rank, the
 // softmax attention over the keys of its own document that pass the causal
-// test (k_pos <= q_pos), visiting the KV shards in ring order -- rank r at
-// step t reads the shard of rank s = (r - t) mod cp ("Question about varlen
-// ring attention", MiniMax-01 #6; zigzag shards per ring-attention-pytorch
-// #20 and maxtext PR #1133).  Partials of the steps are merged on chip by
-// the online softmax (equivalent to the LSE merge of per-step results);
-// with a one-step range the same kernel returns one ring step's partial
-// (out, lse).  Tiles whose pairs are all masked are never visited (the
-// pruning of FlagScale PR #910).
+// test (k_pos <= q_pos) and, with a sliding window w, k_pos >= q_pos - w
+// (the window_size argument in maxtext PR #1133's cudnn_flash_attention),
+// visiting the KV shards in ring order -- rank r at step t reads the shard
+// of rank s = (r - t) mod cp ("Question about varlen ring attention",
+// MiniMax-01 #6; zigzag shards per ring-attention-pytorch #20 and maxtext
+// PR #1133).  Partials of the steps are merged on chip by the online
+// softmax (equivalent to the LSE merge of per-step results); with a
+// one-step range the same kernel returns one ring step's partial (out,
+// lse).  Tiles whose pairs are all masked are never visited (the pruning of
+// FlagScale PR #910).
 //
 // GB300 design:
-//  * One CTA = one work item: two query tiles of 128 MMA rows each.  A row
-//    is (token, head) with the G query heads of one KV head packed together
-//    (128/G tokens x G heads), so a K/V tile loaded once serves all G heads.
-//  * TMA (3-D tensor maps over [T, H, 128], 128-byte swizzle) stages Q once
-//    and K/V tiles through a 5-slot ring; tcgen05.mma (kind::f16, M=128,
-//    N=128) computes S = Q K^T (both operands in shared memory) and
-//    O += P V with P read from TMEM, so the PV product only streams V from
-//    shared memory (the N=128 SS product alone uses the whole shared-memory
-//    read port).  The MMA warp runs converged and one elected lane issues
-//    each instruction, which keeps the issue cost under the tensor time.
+//  * Persistent: one CTA per SM claims work items from a counter; an item is
+//    two query tiles of 128 MMA rows.  A row is (token, head) with the G
+//    query heads of one KV head packed together (128/G tokens x G heads), so
+//    a K/V tile loaded once serves all G heads.
+//  * TMA (3-D tensor maps over [T, H, 128], 128-byte swizzle) stages an
+//    item's Q tiles (prefetched into L2 while the previous item runs, copied
+//    once its last S products are done) and K/V tiles through a 5-slot
+//    ring; tcgen05.mma (kind::f16, M=128, N=128) computes S = Q K^T (both
+//    operands in shared memory) and O += P V with P read from TMEM, so the
+//    PV product only streams V from shared memory (the N=128 SS product
+//    alone uses the whole shared-memory read port).  The MMA warp runs
+//    converged and one elected lane issues each instruction, which keeps the
+//    issue cost under the tensor time.
 //  * TMEM: S0, S1, O0, O1 (4 x 128 fp32 columns = all 512); P (bf16) is
 //    written over the first 64 columns of its S.
-//  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer, warp 2 TMEM
-//    allocator, warps 4-7 softmax of query tile 0, warps 8-11 of tile 1.
-//    A softmax thread owns one TMEM lane (one row): it reads S, masks,
-//    takes exp2 in fp32, writes P (bf16) back to TMEM, and rescales its O
-//    row in TMEM only when the running
-//    max grew by more than 2^8 (otherwise the stale max is kept; the final
-//    normalisation uses the same max, so the result is exact).
+//  * Warp roles: warp 0 producer (claims, loads, publishes the visited
+//    tiles through a shared-memory descriptor ring), warp 1 MMA issuer,
+//    warp 2 TMEM allocator, warps 4-7 softmax of query tile 0, warps 8-11
+//    of tile 1.  A softmax thread owns one TMEM lane (one row): it reads S,
+//    masks, takes exp2 in fp32, writes P (bf16) back to TMEM, and rescales
+//    its O row in TMEM only when the running max grew by more than 2^8
+//    (otherwise the stale max is kept; the final normalisation uses the
+//    same max, so the result is exact); at an item's end it writes O and
+//    the LSE of its row.
 //  * MMA issue order per KV tile j: PV0(j), S0(j+1), PV1(j), S1(j+1), so
 //    each softmax group has the other group's two MMAs to hide behind.
 //  * Every wait is bounded (2 s); a wait that runs out records
