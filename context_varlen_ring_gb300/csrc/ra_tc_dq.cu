@@ -5,8 +5,8 @@
 // D = rowsum(dO o O),
 //   P = exp(scale * q K^T - lse),  dS = P o (dO V^T - D),  dQ = scale * dS K
 // over the keys of its document that pass the causal test (and, with a
-// sliding window w, k_pos >= q_pos - w), visiting the KV shards in ring order (rank r at step t reads the shard of rank
-// s = (r - t) mod cp).  This is the query-side half of the backward of
+// sliding window w, k_pos >= q_pos - w), visiting the KV shards in ring
+// order (rank r at step t reads the shard of rank s = (r - t) mod cp).  This is the query-side half of the backward of
 // FlagScale PR #910's RingAttention (backward_impl); the key side (dK, dV)
 // is ra_tc_bwd.cu run without dQ.  Splitting the two sides costs one extra
 // S and dP product per tile pair but removes all fp32 atomics on dQ, whose
