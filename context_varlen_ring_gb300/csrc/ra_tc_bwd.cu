@@ -23,18 +23,19 @@
 //    memory only streams Q and dO (the SS products at N = 128 already use
 //    most of the shared-memory read port).
 //  * Each query tile is processed as two 64-column halves h (query rows
-//    [64h, 64h+64)), and compute group h owns half h: S^T_h, dP^T_h are
-//    N=64 products into that group's TMEM columns, and dV, dK take the
-//    matching 64-row slice of the contraction.  A group's chain
-//    S^T_h(i) -> P^T_h(i) -> dV_h(i) -> S^T_h(i+1) thus holds half a tile
-//    of products, and the two groups' chains interleave.
+//    [64h, 64h+64)), and compute group h owns half h: S^T_h is an N=64
+//    product into that group's TMEM columns, so group 0's exponentials
+//    start while S^T_1 is still in the pipe and the groups stay staggered;
+//    dP^T is one N=128 product (an SS product at N=64 reads 6 KB per 32
+//    tensor cycles, above the 128 B/cycle of the shared-memory port, so it
+//    runs at two thirds of the tensor rate); dV and dK take the matching
+//    64-row slice of the contraction per group.
 //  * Two warps issue, one per TMEM reuse chain: warp 1 dV_h(i) then
-//    S^T_h(i+1) (which overwrites P^T_h(i)), warp 3 dK_h(i) then dP^T_h(i+1)
-//    (which overwrites dS^T_h(i)); each chain is ordered by the tensor
-//    pipe's in-order execution of one issuer's products.  Each issuer warp
-//    runs converged and one elected lane issues: from one lane of a
-//    divergent branch an MMA costs 45-60 cycles to issue, above the 32
-//    tensor cycles of an N=64 product.
+//    S^T_h(i+1) (which overwrites P^T_h(i)), warp 3 dK_0(i), dK_1(i) then
+//    dP^T(i+1) (which overwrites both dS^T halves); each chain is ordered
+//    by the tensor pipe's in-order execution of one issuer's products.
+//    Each issuer warp runs converged and one elected lane issues: from one
+//    lane of a divergent branch an MMA costs 45-60 cycles to issue.
 //  * TMEM: dK [0,128), dV [128,256), S^T then P^T [256,384), dP^T then dS^T
 //    [384,512).  Two compute warpgroups split the 128 query columns; each
 //    packs its P^T / dS^T (bf16) over the first 32 of its own 64 columns.
@@ -245,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
         // ------------------------------------------------ MMA issuers
         // Each issuer warp runs converged; one elected lane issues (_w helpers).
         const uint32_t id_n64 = idesc_bf16_f32(128, 64, 0, 0);  // A, B K-major, N = 64 queries
+        const uint32_t id_n128 = idesc_bf16_f32(128, 128, 0, 0);
         const uint32_t id_ts = idesc_bf16_f32(128, 128, 0, 1);  // A in TMEM, B MN-major
         auto is_end = [&](uint32_t st) {
             return (reinterpret_cast<const int4 *>(info(st) + 1024)[1].y & 1) != 0;
@@ -267,6 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                 tc_mma_ss_w(chain_d + 64u * h, chain_a + kstep(ks), b0 + kstep(ks), id_n64, ks > 0);
             tc_commit_w(chain_full + h);
         };
+        // dP^T of stage st as one N=128 product (both groups' barriers)
+        auto chain_full_mma = [&](uint32_t st) {
+            const uint64_t b0 = sdesc_sw128(chain_b + st * kTile, 16, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                tc_mma_ss_w(chain_d, chain_a + kstep(ks), b0 + kstep(ks), id_n128, ks > 0);
+            tc_commit_w(chain_full + 0);
+            tc_commit_w(chain_full + 1);
+        };
         // dV / dK += P^T_h / dS^T_h (TMEM, group h's columns) x rows [64h, 64h+64)
         // of dO / Q (MN-major: d contiguous)
         auto grad_mma = [&](int h, uint32_t st, bool acc) {
@@ -278,26 +289,48 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
         bool ok = mbar_wait_warp(kv_full, 0, wc) && mbar_wait_warp(st_full + 0, 0, wc);
         tc_fence_after();
         const bool have = ok && !is_end(0);
-        if (have) {
+        if (have && pchain) {
+            // S^T as two N=64 halves, so group 0's exponentials start while
+            // half 1 is still in the pipe (the groups stay staggered)
             chain_mma(0, 0);
             chain_mma(1, 0);
-        }
-        for (uint32_t i = 0; ok && have; ++i) {
-            const uint32_t st = i & 1u, nst = (i + 1) & 1u;
-            if (!mbar_wait_warp(ready + 0, i & 1u, wc)) break;
-            tc_fence_after();
-            grad_mma(0, st, i > 0);
-            if (!mbar_wait_warp(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
-            tc_fence_after();
-            const bool next_end = is_end(nst);
-            // half 0 of the next tile overwrites P^T_0 / dS^T_0 after the product above (in order)
-            if (!next_end) chain_mma(0, nst);
-            if (!mbar_wait_warp(ready + 1, i & 1u, wc)) break;
-            tc_fence_after();
-            grad_mma(1, st, true);
-            tc_commit_w(st_empty + st);  // this issuer no longer reads the stage
-            if (next_end) break;
-            chain_mma(1, nst);
+            for (uint32_t i = 0; ok; ++i) {
+                const uint32_t st = i & 1u, nst = (i + 1) & 1u;
+                if (!mbar_wait_warp(ready + 0, i & 1u, wc)) break;
+                tc_fence_after();
+                grad_mma(0, st, i > 0);
+                if (!mbar_wait_warp(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
+                tc_fence_after();
+                const bool next_end = is_end(nst);
+                // half 0 of the next tile overwrites P^T_0 after the product above (in order)
+                if (!next_end) chain_mma(0, nst);
+                if (!mbar_wait_warp(ready + 1, i & 1u, wc)) break;
+                tc_fence_after();
+                grad_mma(1, st, true);
+                tc_commit_w(st_empty + st);  // this issuer no longer reads the stage
+                if (next_end) break;
+                chain_mma(1, nst);
+            }
+        } else if (have) {
+            // dP^T as one N=128 product: the N=64 halves of an SS product
+            // read 6 KB per 32 tensor cycles, above the 128 B/cycle of the
+            // shared-memory port, and the dS work needs no staggering
+            chain_full_mma(0);
+            for (uint32_t i = 0; ok; ++i) {
+                const uint32_t st = i & 1u, nst = (i + 1) & 1u;
+                if (!mbar_wait_warp(ready + 0, i & 1u, wc)) break;
+                tc_fence_after();
+                grad_mma(0, st, i > 0);
+                if (!mbar_wait_warp(ready + 1, i & 1u, wc)) break;
+                tc_fence_after();
+                grad_mma(1, st, true);
+                tc_commit_w(st_empty + st);  // this issuer no longer reads the stage
+                if (!mbar_wait_warp(st_full + nst, ((i + 1) >> 1) & 1u, wc)) break;
+                tc_fence_after();
+                if (is_end(nst)) break;
+                // the next dP^T overwrites both dS^T halves after the two products above
+                chain_full_mma(nst);
+            }
         }
         tc_commit_w(mma_done);
         volatile int local_abort = 0;
