@@ -267,6 +267,45 @@ def fwd_configs(args, ra, torch):
         torch.cuda.empty_cache()
 
 
+def balance_study(args):
+    """Per-rank causal load of CP sharding policies on synthetic packings
+    (the packing/balance question of "Question about varlen ring attention",
+    MiniMax-01 #6): allowed (query, key) pairs each simulated rank computes
+    over the whole ring, for per-document zigzag, whole-stream zigzag and
+    plain contiguous sharding, with documents in drawn order or sorted by
+    length.  The ring's step time follows the busiest rank, so the figure
+    of merit is max / mean.  Host only (the library's ra_ring_rank_pairs;
+    contiguous sharding is counted here)."""
+    import context_varlen_ring_gb300 as ra
+    cp = 8
+
+    def contiguous(cu, window):
+        T = int(cu[-1])
+        counts = np.zeros(cp, dtype=np.int64)
+        for b in range(len(cu) - 1):
+            i = np.arange(cu[b], cu[b + 1], dtype=np.int64)
+            keys = i - cu[b] + 1 if window < 0 else np.minimum(i - cu[b] + 1, window + 1)
+            owner = np.minimum(i * cp // T, cp - 1)
+            np.add.at(counts, owner, keys)
+        return counts
+
+    for seed in range(6):
+        lens = W.loguniform_doc_lens(32768, 128, 8192, seed)
+        for order in ("drawn", "sorted"):
+            ll = sorted(lens, reverse=True) if order == "sorted" else lens
+            cu = W.cu_seqlens(ll)
+            for window in (-1, 1024):
+                res = {}
+                for name, f in (("per_doc_zigzag", lambda c, w: ra.ring_rank_pairs(c, cp, W.ZZ_PER_DOC, True, w)),
+                                ("stream_zigzag", lambda c, w: ra.ring_rank_pairs(c, cp, W.ZZ_GLOBAL, True, w)),
+                                ("contiguous", contiguous)):
+                    c = np.asarray(f(cu, window), dtype=np.float64)
+                    res[name] = round(float(c.max() / c.mean()), 4)
+                print(json.dumps({"balance": "max/mean per-rank allowed pairs", "cp": cp, "T": 32768,
+                                  "docs_seed": seed, "doc_order": order, "n_docs": len(ll), "window": window,
+                                  **res}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -277,12 +316,17 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--probe", action="store_true",
                     help="only W+K plain steps (for profilers): no e2e, per-kernel or CPU passes")
+    ap.add_argument("--balance", action="store_true",
+                    help="host-only study of per-rank causal load under CP sharding policies (JSON lines)")
     ap.add_argument("--window", type=int, default=-1,
                     help="sliding window (a key at most this many positions behind its query); -1: none")
     ap.add_argument("--fwd-configs", default="",
                     help="comma list of forward-only workloads (e.g. C1,C2,C3) to time instead of the "
                          "fwd+bwd step; one JSON line each (not the headline line)")
     args = ap.parse_args()
+    if args.balance:
+        balance_study(args)
+        return
     if args.impl == "reference":
         reference_arm(args)
         return
