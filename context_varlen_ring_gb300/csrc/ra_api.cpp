@@ -2,6 +2,7 @@
 // carving and the drivers of the simulated ring.  Host code only; every
 // step of the data path runs in the library's kernels.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cmath>
 #include <cstdio>
@@ -55,7 +56,11 @@ cudaEvent_t take_event() {
 }
 }  // namespace
 
+// Every scope is also an NVTX range (host side), so a timeline tool shows
+// each phase and, in STEPWISE mode, each ring step by name; without a tool
+// attached the range calls return at once.
 ProfScope::ProfScope(const char *name, cudaStream_t st) : st_(st) {
+    nvtxRangePushA(name);
     std::lock_guard<std::mutex> lk(g_prof_mu);
     if (!g_prof_on) return;
     cudaEvent_t a = take_event(), b = take_event();
@@ -66,8 +71,11 @@ ProfScope::ProfScope(const char *name, cudaStream_t st) : st_(st) {
 }
 
 ProfScope::~ProfScope() {
-    std::lock_guard<std::mutex> lk(g_prof_mu);
-    if (id_ >= 0 && id_ < (int)g_prof.size()) cudaEventRecord(g_prof[id_].b, st_);
+    {
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        if (id_ >= 0 && id_ < (int)g_prof.size()) cudaEventRecord(g_prof[id_].b, st_);
+    }
+    nvtxRangePop();
 }
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

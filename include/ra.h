@@ -275,7 +275,12 @@ ra_status ra_selftest_wait_timeout(int64_t budget_us, void *stream);
  * names written as NUL-terminated strings of up to 64 bytes each into
  * `names`), the summed device time in ms and the launch count.  Returns
  * the number of kernels reported, or -1 on error.  Timing adds two event
- * records per launch; keep it off for throughput runs.
+ * records per launch; keep it off for throughput runs.  Independently of
+ * this switch, each timed unit (a kernel launch, or the concurrent backward
+ * pair "ra_tc_bwd") is also an NVTX range of the same name pushed on the
+ * calling host thread, so a timeline tool shows the phases of a step and,
+ * in STEPWISE mode, one range per ring step; with no tool attached the
+ * range calls do nothing.
  * ------------------------------------------------------------------------ */
 ra_status ra_profile_enable(int on);
 int ra_profile_read(int max_kernels, char *names, double *total_ms, int64_t *launches);
