@@ -701,13 +701,16 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     const int32_t *cul = reinterpret_cast<const int32_t *>(tab + dt.o_cul);
     const size_t es = esize(dtype);
     void *Qp = ws + L.qp, *Kp = ws + L.kp, *Vp = ws + L.vp;
-    // a3: zigzag-permute Q, K, V into the ranks' shards (one launch)
-    PermJob jobs[3] = {{q, Qp, (int64_t)Hq * d * (int64_t)es},
-                       {k, Kp, (int64_t)Hkv * d * (int64_t)es},
-                       {v, Vp, (int64_t)Hkv * d * (int64_t)es}};
+    // a3: zigzag-permute K, V and Q into the ranks' shards (one launch).  The
+    // tensor-core kernels read a query tile of one position run straight
+    // from q, so Q moves only for the rows of two-run tiles.
+    PermJob jobs[3] = {{k, Kp, (int64_t)Hkv * d * (int64_t)es},
+                       {v, Vp, (int64_t)Hkv * d * (int64_t)es},
+                       {q, Qp, (int64_t)Hq * d * (int64_t)es}};
+    const uint8_t *qmask = tc ? tab + dt.o_qmask : nullptr;
     {
         ProfScope ps("ra_permute_fwd", s);
-        RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s), "permute launch");
+        RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s, qmask, 2), "permute launch");
     }
     reserve_record(workspace, plan.get(), q, k, v, dtype, T, Hq, Hkv, d, causal, sched);
 
@@ -715,6 +718,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
         if (tc) {
             TcFwdArgs a{};
             a.q = Qp;
+            a.q_orig = q;
             a.k = Kp;
             a.v = Vp;
             a.Tq = T;
@@ -849,15 +853,19 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     float *dqa = reinterpret_cast<float *>(ws + L.dq);
     float *dka = reinterpret_cast<float *>(ws + L.dk);
     float *dva = reinterpret_cast<float *>(ws + L.dv);
-    // a7: permute Q, K, V, dO; D = rowsum(dO * O) in original order
-    PermJob jobs[4] = {{q, Qp, (int64_t)Hq * d * (int64_t)es},
-                       {k, Kp, (int64_t)Hkv * d * (int64_t)es},
+    // a7: permute K, V, Q, dO; D = rowsum(dO * O) in original order.  With
+    // the tensor cores, Q and dO move only for the rows of two-run query
+    // tiles (the kernels read the others straight from q and dout).
+    PermJob jobs[4] = {{k, Kp, (int64_t)Hkv * d * (int64_t)es},
                        {v, Vp, (int64_t)Hkv * d * (int64_t)es},
+                       {q, Qp, (int64_t)Hq * d * (int64_t)es},
                        {dout, dOp, (int64_t)Hq * d * (int64_t)es}};
+    const uint8_t *qmask = tc ? tab + dt.o_qmask : nullptr;
     if (dtype == RA_BF16 && d == 128 && aligned16(out) && aligned16(dout)) {
         // one pass: the permutes and D from the same dO reads
         ProfScope ps("ra_permute_rowdot", s);
-        RA_CUDA(launch_permute_rowdot(jobs, reserve ? 0 : 3, dout, dOp, out, D, perm, T, Hq, s),
+        RA_CUDA(launch_permute_rowdot(jobs, reserve ? 0 : 3, dout, dOp, out, D, perm, T, Hq, s, qmask,
+                                      reserve ? 0 : 2),
                 "permute+rowdot launch");
     } else {
         {
@@ -891,6 +899,8 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         a.k = Kp;
         a.v = Vp;
         a.dout = dOp;
+        a.q_orig = q;
+        a.dout_orig = dout;
         a.T = T;
         a.Hq = Hq;
         a.Hkv = Hkv;
@@ -911,6 +921,8 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         qa.k = Kp;
         qa.v = Vp;
         qa.dout = dOp;
+        qa.q_orig = q;
+        qa.dout_orig = dout;
         qa.T = T;
         qa.Hq = Hq;
         qa.Hkv = Hkv;

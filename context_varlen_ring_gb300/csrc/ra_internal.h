@@ -101,6 +101,10 @@ struct DeviceTables {
     std::vector<uint8_t> blob;
     size_t o_perm = 0, o_qt = 0, o_kt = 0, o_qoff = 0, o_kvoff = 0, o_items = 0,
            o_bitems = 0, o_qitems = 0, o_cul = 0, o_off = 0;
+    // One byte per rank-ordered row: 1 where the row belongs to a query tile
+    // of two position runs (the tensor-core kernels read such tiles from the
+    // rank-ordered copy; single-run tiles straight from the caller's tensor).
+    size_t o_qmask = 0;
     // Work counters of the persistent kernels (uploaded as zeros; a kernel
     // returns its counter to zero when it finishes): [0, 2) forward.
     size_t o_sched = 0;

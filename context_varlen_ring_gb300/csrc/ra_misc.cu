@@ -49,6 +49,9 @@ static inline int num_sms() {
 struct PermJobs {
     PermJob j[4];
     int n;
+    // jobs [only_from, n) copy just the rows i with only[i] != 0 (when set)
+    const uint8_t *only;
+    int only_from;
 };
 
 // One warp per row; each lane moves vectors of type V (16 B when every row
@@ -67,7 +70,8 @@ __global__ void __launch_bounds__(256) permute_kernel(PermJobs jobs, const int32
         }
         const int64_t srow = inverse ? i : (int64_t)p;
         const int64_t drow = inverse ? (int64_t)p : i;
-        for (int jb = 0; jb < jobs.n; ++jb) {
+        const int njobs = (jobs.only && !__ldg(jobs.only + i)) ? jobs.only_from : jobs.n;
+        for (int jb = 0; jb < njobs; ++jb) {
             const int64_t nvec = jobs.j[jb].row_bytes / (int64_t)sizeof(V);
             const V *__restrict__ src = reinterpret_cast<const V *>(jobs.j[jb].src) + srow * nvec;
             V *__restrict__ dst = reinterpret_cast<V *>(jobs.j[jb].dst) + drow * nvec;
@@ -89,10 +93,13 @@ __global__ void __launch_bounds__(256) permute_kernel(PermJobs jobs, const int32
 }
 
 cudaError_t launch_permute(const PermJob *jobs, int njobs, const int32_t *perm, int64_t T, int inverse,
-                           cudaStream_t st) {
+                           cudaStream_t st, const uint8_t *only, int only_from) {
     if (T <= 0 || njobs <= 0) return cudaSuccess;
+    if (njobs > 4 || only_from < 0 || only_from > njobs) return cudaErrorInvalidValue;
     PermJobs pj{};
     pj.n = njobs;
+    pj.only = only;
+    pj.only_from = only ? only_from : njobs;
     int vec = 16;
     for (int i = 0; i < njobs; ++i) {
         pj.j[i] = jobs[i];
@@ -245,7 +252,8 @@ __global__ void __launch_bounds__(256) permute_rowdot_kernel(PermJobs jobs, cons
             if (lane == 0) dev::record_status(status, RA_ERR_DEVICE_BOUNDS);
             continue;
         }
-        for (int jb = 0; jb < jobs.n; ++jb) {
+        const bool keep = !jobs.only || __ldg(jobs.only + i);
+        for (int jb = 0; jb < (keep ? jobs.n : jobs.only_from); ++jb) {
             const int64_t nvec = jobs.j[jb].row_bytes / 16;
             const uint4 *__restrict__ src = reinterpret_cast<const uint4 *>(jobs.j[jb].src) + (int64_t)p * nvec;
             uint4 *__restrict__ dst = reinterpret_cast<uint4 *>(jobs.j[jb].dst) + i * nvec;
@@ -279,7 +287,7 @@ __global__ void __launch_bounds__(256) permute_rowdot_kernel(PermJobs jobs, cons
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int64_t c = c0 + u * 32;
-                if (c < nvo) dst[c] = x[u];
+                if (c < nvo && keep) dst[c] = x[u];
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -294,11 +302,14 @@ __global__ void __launch_bounds__(256) permute_rowdot_kernel(PermJobs jobs, cons
 }
 
 cudaError_t launch_permute_rowdot(const PermJob *jobs, int njobs, const void *dout, void *dout_p, const void *out,
-                                  float *D, const int32_t *perm, int64_t T, int Hq, cudaStream_t st) {
+                                  float *D, const int32_t *perm, int64_t T, int Hq, cudaStream_t st,
+                                  const uint8_t *only, int only_from) {
     if (T <= 0) return cudaSuccess;
-    if (njobs < 0 || njobs > 4) return cudaErrorInvalidValue;
+    if (njobs < 0 || njobs > 4 || only_from < 0 || only_from > njobs) return cudaErrorInvalidValue;
     PermJobs pj{};
     pj.n = njobs;
+    pj.only = only;
+    pj.only_from = only ? only_from : njobs;
     auto al = [](const void *q, int64_t rb) { return (reinterpret_cast<uintptr_t>(q) % 16) == 0 && (rb % 16) == 0; };
     for (int i = 0; i < njobs; ++i) {
         if (!al(jobs[i].src, jobs[i].row_bytes) || !al(jobs[i].dst, jobs[i].row_bytes)) return cudaErrorInvalidValue;

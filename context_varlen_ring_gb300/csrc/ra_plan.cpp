@@ -301,6 +301,7 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
     dt.o_cul = take(zp ? zp->cu_local.size() * 4 : 0);
     dt.o_off = take(zp ? zp->off.size() * 4 : 0);
     dt.o_sched = take(64);
+    dt.o_qmask = take(zp && tp ? zp->perm.size() : 0);
     dt.blob.assign(o, 0);
     auto put = [&](size_t at, const void *src, size_t bytes) {
         if (bytes) std::memcpy(dt.blob.data() + at, src, bytes);
@@ -321,6 +322,17 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
         dt.n_items = (int)tp->items.size();
         dt.n_bitems = (int)tp->bitems.size();
         dt.n_qitems = (int)tp->qitems.size();
+    }
+    if (zp && tp) {
+        // the whole box a kernel copies for a two-run tile (q_tokens rows,
+        // padding included), so that its padding rows hold finite values
+        // like every other row a tile reads (the key-side backward sums
+        // over a tile's padded rows with zero weight)
+        const int64_t T = (int64_t)zp->perm.size();
+        uint8_t *mask = dt.blob.data() + dt.o_qmask;
+        for (const Tile &t : tp->qtiles)
+            if (t.split < t.len)
+                for (int64_t i = t.row0; i < (int64_t)t.row0 + tp->q_tokens && i < T; ++i) mask[i] = 1;
     }
 }
 

@@ -74,8 +74,10 @@ constexpr uint32_t kSmemBytes = kOffBar + 128;    // 16 barrier words; base must
 
 struct BwdParams {
     CUtensorMap tmQ, tmK, tmV, tmDO;
+    CUtensorMap tmQo, tmDOo;  // Q and dO in original order (valid when qdo_direct)
     const int4 *qtiles, *kvtiles, *items;
     const int *q_off;
+    int qdo_direct;  // single-run query tiles: Q and dO read at their first position
     int n_items, cp, B, G, log2G, Hq, Hkv;
     int t0, t1, causal, window, out_mode;          // 0 bf16 store, 1 fp32 store, 2 fp32 +=
     float scale, scale_log2;
@@ -169,6 +171,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             tma_prefetch_desc(&p.tmK);
             tma_prefetch_desc(&p.tmV);
             tma_prefetch_desc(&p.tmDO);
+            if (p.qdo_direct) {
+                tma_prefetch_desc(&p.tmQo);
+                tma_prefetch_desc(&p.tmDOo);
+            }
             mbar_arrive_expect_tx(kv_full, 2 * kTile);
             tma_load_3d(smem + kOffK, &p.tmK, kv_full, 0, g, ka.x);
             tma_load_3d(smem + kOffK + kHalf, &p.tmK, kv_full, 64, g, ka.x);
@@ -191,10 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                     if (!end) {
                         mbar_arrive_expect_tx(st_full + st, 2 * kTile + 1024);
                         const int hq0 = g * G;
-                        tma_load_3d(smem + kOffQ + st * kTile, &p.tmQ, st_full + st, 0, hq0, d0.x);
-                        tma_load_3d(smem + kOffQ + st * kTile + kHalf, &p.tmQ, st_full + st, 64, hq0, d0.x);
-                        tma_load_3d(smem + kOffDO + st * kTile, &p.tmDO, st_full + st, 0, hq0, d0.x);
-                        tma_load_3d(smem + kOffDO + st * kTile + kHalf, &p.tmDO, st_full + st, 64, hq0, d0.x);
+                        // one position run (split == len): the original rows
+                        const bool dir = p.qdo_direct && d0.z == d0.y;
+                        const CUtensorMap *mq = dir ? &p.tmQo : &p.tmQ, *mdo = dir ? &p.tmDOo : &p.tmDO;
+                        const int row = dir ? d0.w : d0.x;
+                        tma_load_3d(smem + kOffQ + st * kTile, mq, st_full + st, 0, hq0, row);
+                        tma_load_3d(smem + kOffQ + st * kTile + kHalf, mq, st_full + st, 64, hq0, row);
+                        tma_load_3d(smem + kOffDO + st * kTile, mdo, st_full + st, 0, hq0, row);
+                        tma_load_3d(smem + kOffDO + st * kTile + kHalf, mdo, st_full + st, 64, hq0, row);
                         bulk_load(info(st), p.tile_ld + ((long long)qt * p.Hkv + g) * 256, 1024, st_full + st);
                     } else {
                         mbar_arrive(st_full + st);
@@ -540,6 +550,12 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
     if (!make_map(&p.tmQ, a.q, a.T, a.Hq, G, kBM / G) || !make_map(&p.tmDO, a.dout, a.T, a.Hq, G, kBM / G) ||
         !make_map(&p.tmK, a.k, a.T, a.Hkv, 1, kBN) || !make_map(&p.tmV, a.v, a.T, a.Hkv, 1, kBN))
         return cudaErrorInvalidValue;
+    if ((a.q_orig != nullptr) != (a.dout_orig != nullptr)) return cudaErrorInvalidValue;
+    if (a.q_orig) {
+        if (!make_map(&p.tmQo, a.q_orig, a.T, a.Hq, G, kBM / G) || !make_map(&p.tmDOo, a.dout_orig, a.T, a.Hq, G, kBM / G))
+            return cudaErrorInvalidValue;
+        p.qdo_direct = 1;
+    }
     p.qtiles = static_cast<const int4 *>(a.qtiles);
     p.kvtiles = static_cast<const int4 *>(a.kvtiles);
     p.items = static_cast<const int4 *>(a.items);

@@ -68,8 +68,10 @@ constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 
 struct DqParams {
     CUtensorMap tmQ, tmK, tmV, tmDO;
+    CUtensorMap tmQo, tmDOo;  // Q and dO in original order (valid when qdo_direct)
     const int4 *qtiles, *kvtiles, *items;
     const int *kv_off;
+    int qdo_direct;  // single-run query tiles: Q and dO read at their first position
     int n_items, cp, B, G, log2G, Hq;
     int t0, t1, causal, window, out_mode;  // out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 +=
     float scale, scale_log2, log2_scale;
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 tma_prefetch_desc(&p.tmQ);
                 tma_prefetch_desc(&p.tmK);
                 tma_prefetch_desc(&p.tmV);
+                if (p.qdo_direct) tma_prefetch_desc(&p.tmQo);
             }
             uint32_t u = 0, ri = 0;
             int ok = 1;
@@ -211,9 +214,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         ok = 0;
                     } else {
                         uint8_t *dst = base + kOffKV + slot * kTile;
+                        // one position run (split == len): the original rows
+                        const bool dir = p.qdo_direct && qa.z == qa.y;
+                        const CUtensorMap *mq = dir ? &p.tmQo : &p.tmQ;
+                        const int row = dir ? qa.w : qa.x;
                         mbar_arrive_expect_tx(kv_full + slot, kTile);
-                        tma_load_3d(dst, &p.tmQ, kv_full + slot, 0, g * p.G, qa.x);
-                        tma_load_3d(dst + kHalf, &p.tmQ, kv_full + slot, 64, g * p.G, qa.x);
+                        tma_load_3d(dst, mq, kv_full + slot, 0, g * p.G, row);
+                        tma_load_3d(dst + kHalf, mq, kv_full + slot, 64, g * p.G, row);
                         ++u;
                     }
                 }
@@ -346,10 +353,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     auto load_do = [&](int kk) {
                         if (lane != 0) return;
                         const int4 ia = __ldg(p.items + 2 * item_of(kk));
-                        const int row0 = __ldg(&p.qtiles[2 * ia.x].x);
+                        const int4 qa = __ldg(p.qtiles + 2 * ia.x);
+                        const bool dir = p.qdo_direct && qa.z == qa.y;
+                        const CUtensorMap *mdo = dir ? &p.tmDOo : &p.tmDO;
+                        const int row = dir ? qa.w : qa.x;
                         mbar_arrive_expect_tx(do_full, kTile);
-                        tma_load_3d(base + kOffDO, &p.tmDO, do_full, 0, ia.z * p.G, row0);
-                        tma_load_3d(base + kOffDO + kHalf, &p.tmDO, do_full, 64, ia.z * p.G, row0);
+                        tma_load_3d(base + kOffDO, mdo, do_full, 0, ia.z * p.G, row);
+                        tma_load_3d(base + kOffDO + kHalf, mdo, do_full, 64, ia.z * p.G, row);
                     };
                     if (k == 0) load_do(0);
                     ok = wait(do_full, k & 1);
@@ -669,6 +679,12 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
     if (!make_map(&p.tmQ, a.q, a.T, a.Hq, G, kBM / G) || !make_map(&p.tmDO, a.dout, a.T, a.Hq, G, kBM / G) ||
         !make_map(&p.tmK, a.k, a.T, a.Hkv, 1, kBN) || !make_map(&p.tmV, a.v, a.T, a.Hkv, 1, kBN))
         return cudaErrorInvalidValue;
+    if ((a.q_orig != nullptr) != (a.dout_orig != nullptr)) return cudaErrorInvalidValue;
+    if (a.q_orig) {
+        if (!make_map(&p.tmQo, a.q_orig, a.T, a.Hq, G, kBM / G) || !make_map(&p.tmDOo, a.dout_orig, a.T, a.Hq, G, kBM / G))
+            return cudaErrorInvalidValue;
+        p.qdo_direct = 1;
+    }
     p.qtiles = static_cast<const int4 *>(a.qtiles);
     p.kvtiles = static_cast<const int4 *>(a.kvtiles);
     p.items = static_cast<const int4 *>(a.items);

@@ -76,9 +76,11 @@ constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + barriers/ring + alig
 
 struct FwdParams {
     CUtensorMap tmQ, tmK, tmV;
+    CUtensorMap tmQo;  // Q in original order (valid when q_direct)
     const int4 *qtiles, *kvtiles, *items;
     const int *kv_off;
     int *sched;  // [2]: next item to claim, CTAs finished (zero between launches)
+    int q_direct;  // single-run query tiles are read from tmQo at their first position
     int n_items, cp, B, G, log2G, Hq;
     int t0, t1, causal, window, out_mode;
     float scale_log2;
@@ -236,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 tma_prefetch_desc(&p.tmQ);
                 tma_prefetch_desc(&p.tmK);
                 tma_prefetch_desc(&p.tmV);
+                if (p.q_direct) tma_prefetch_desc(&p.tmQo);
             }
             for (int it = 0; ok; ++it) {
                 int item = 0;
@@ -253,12 +256,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 const bool has1 = qt1 >= 0;
                 const int4 qa0 = __ldg(p.qtiles + 2 * qt0), qb0 = __ldg(p.qtiles + 2 * qt0 + 1);
                 const QInfo q0{qa0.y, qb0.y, qb0.z};
+                // a tile of one position run (split == len) is the original
+                // rows [pos0, pos0 + len): read it there, not from the
+                // rank-ordered copy (which then holds only two-run tiles)
+                const bool dir0 = p.q_direct && qa0.z == qa0.y;
+                const CUtensorMap *mq0 = dir0 ? &p.tmQo : &p.tmQ;
+                const int qrow0 = dir0 ? qa0.w : qa0.x;
                 QInfo q1{0, 0, 0};
                 int qrow1 = 0;
+                const CUtensorMap *mq1 = &p.tmQ;
                 if (has1) {
                     const int4 qa1 = __ldg(p.qtiles + 2 * qt1), qb1 = __ldg(p.qtiles + 2 * qt1 + 1);
                     q1 = QInfo{qa1.y, qb1.y, qb1.z};
-                    qrow1 = qa1.x;
+                    const bool dir1 = p.q_direct && qa1.z == qa1.y;
+                    mq1 = dir1 ? &p.tmQo : &p.tmQ;
+                    qrow1 = dir1 ? qa1.w : qa1.x;
                 }
                 const int hq0 = g * p.G;
                 // The Q buffers free up only when the previous item's last S
@@ -270,21 +282,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     q_pending = false;
                     if (it > 0 && !mbar_wait(q_empty, (it - 1) & 1u, wc)) return 0;
                     mbar_arrive_expect_tx(q_full, (has1 ? 2u : 1u) * kTile);
-                    tma_load_3d(base + kOffQ0, &p.tmQ, q_full, 0, hq0, qa0.x);
-                    tma_load_3d(base + kOffQ0 + kHalf, &p.tmQ, q_full, 64, hq0, qa0.x);
+                    tma_load_3d(base + kOffQ0, mq0, q_full, 0, hq0, qrow0);
+                    tma_load_3d(base + kOffQ0 + kHalf, mq0, q_full, 64, hq0, qrow0);
                     if (has1) {
-                        tma_load_3d(base + kOffQ1, &p.tmQ, q_full, 0, hq0, qrow1);
-                        tma_load_3d(base + kOffQ1 + kHalf, &p.tmQ, q_full, 64, hq0, qrow1);
+                        tma_load_3d(base + kOffQ1, mq1, q_full, 0, hq0, qrow1);
+                        tma_load_3d(base + kOffQ1 + kHalf, mq1, q_full, 64, hq0, qrow1);
                     }
                     ++n_q;
                     return 1;
                 };
                 if (lane == 0) {
-                    tma_prefetch_3d(&p.tmQ, 0, hq0, qa0.x);
-                    tma_prefetch_3d(&p.tmQ, 64, hq0, qa0.x);
+                    tma_prefetch_3d(mq0, 0, hq0, qrow0);
+                    tma_prefetch_3d(mq0, 64, hq0, qrow0);
                     if (has1) {
-                        tma_prefetch_3d(&p.tmQ, 0, hq0, qrow1);
-                        tma_prefetch_3d(&p.tmQ, 64, hq0, qrow1);
+                        tma_prefetch_3d(mq1, 0, hq0, qrow1);
+                        tma_prefetch_3d(mq1, 64, hq0, qrow1);
                     }
                     ok = publish(make_int4(kHead, item, 0, 0));
                 }
@@ -716,6 +728,10 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
     if (!make_map(&p.tmQ, a.q, a.Tq, a.Hq, G, kBM / G) || !make_map(&p.tmK, a.k, a.Tk, a.Hkv, 1, kBN) ||
         !make_map(&p.tmV, a.v, a.Tk, a.Hkv, 1, kBN))
         return cudaErrorInvalidValue;
+    if (a.q_orig) {
+        if (!make_map(&p.tmQo, a.q_orig, a.Tq, a.Hq, G, kBM / G)) return cudaErrorInvalidValue;
+        p.q_direct = 1;
+    }
     p.qtiles = static_cast<const int4 *>(a.qtiles);
     p.kvtiles = static_cast<const int4 *>(a.kvtiles);
     p.items = static_cast<const int4 *>(a.items);
