@@ -701,16 +701,17 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     const int32_t *cul = reinterpret_cast<const int32_t *>(tab + dt.o_cul);
     const size_t es = esize(dtype);
     void *Qp = ws + L.qp, *Kp = ws + L.kp, *Vp = ws + L.vp;
-    // a3: zigzag-permute K, V and Q into the ranks' shards (one launch).  The
-    // tensor-core kernels read a query tile of one position run straight
-    // from q, so Q moves only for the rows of two-run tiles.
-    PermJob jobs[3] = {{k, Kp, (int64_t)Hkv * d * (int64_t)es},
-                       {v, Vp, (int64_t)Hkv * d * (int64_t)es},
-                       {q, Qp, (int64_t)Hq * d * (int64_t)es}};
+    // a3: zigzag-permute Q, K, V into the ranks' shards (one launch).  The
+    // tensor-core kernels read a tile of one position run straight from q, k
+    // and v, so the copies are made only for the rows of two-run tiles.
     const uint8_t *qmask = tc ? tab + dt.o_qmask : nullptr;
+    const uint8_t *kvmask = tc ? tab + dt.o_kvmask : nullptr;
+    PermJob jobs[3] = {{q, Qp, (int64_t)Hq * d * (int64_t)es, qmask},
+                       {k, Kp, (int64_t)Hkv * d * (int64_t)es, kvmask},
+                       {v, Vp, (int64_t)Hkv * d * (int64_t)es, kvmask}};
     {
         ProfScope ps("ra_permute_fwd", s);
-        RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s, qmask, 2), "permute launch");
+        RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s), "permute launch");
     }
     reserve_record(workspace, plan.get(), q, k, v, dtype, T, Hq, Hkv, d, causal, sched);
 
@@ -721,6 +722,8 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
             a.q_orig = q;
             a.k = Kp;
             a.v = Vp;
+            a.k_orig = k;
+            a.v_orig = v;
             a.Tq = T;
             a.Tk = T;
             a.Hq = Hq;
@@ -853,19 +856,19 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     float *dqa = reinterpret_cast<float *>(ws + L.dq);
     float *dka = reinterpret_cast<float *>(ws + L.dk);
     float *dva = reinterpret_cast<float *>(ws + L.dv);
-    // a7: permute K, V, Q, dO; D = rowsum(dO * O) in original order.  With
-    // the tensor cores, Q and dO move only for the rows of two-run query
-    // tiles (the kernels read the others straight from q and dout).
-    PermJob jobs[4] = {{k, Kp, (int64_t)Hkv * d * (int64_t)es},
-                       {v, Vp, (int64_t)Hkv * d * (int64_t)es},
-                       {q, Qp, (int64_t)Hq * d * (int64_t)es},
-                       {dout, dOp, (int64_t)Hq * d * (int64_t)es}};
+    // a7: permute Q, K, V, dO; D = rowsum(dO * O) in original order.  With
+    // the tensor cores the copies are made only for the rows of two-run
+    // tiles (the kernels read the others straight from q, k, v and dout).
     const uint8_t *qmask = tc ? tab + dt.o_qmask : nullptr;
+    const uint8_t *kvmask = tc ? tab + dt.o_kvmask : nullptr;
+    PermJob jobs[4] = {{q, Qp, (int64_t)Hq * d * (int64_t)es, qmask},
+                       {k, Kp, (int64_t)Hkv * d * (int64_t)es, kvmask},
+                       {v, Vp, (int64_t)Hkv * d * (int64_t)es, kvmask},
+                       {dout, dOp, (int64_t)Hq * d * (int64_t)es, qmask}};
     if (dtype == RA_BF16 && d == 128 && aligned16(out) && aligned16(dout)) {
         // one pass: the permutes and D from the same dO reads
         ProfScope ps("ra_permute_rowdot", s);
-        RA_CUDA(launch_permute_rowdot(jobs, reserve ? 0 : 3, dout, dOp, out, D, perm, T, Hq, s, qmask,
-                                      reserve ? 0 : 2),
+        RA_CUDA(launch_permute_rowdot(jobs, reserve ? 0 : 3, dout, dOp, out, D, perm, T, Hq, s, qmask),
                 "permute+rowdot launch");
     } else {
         {
@@ -901,6 +904,8 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         a.dout = dOp;
         a.q_orig = q;
         a.dout_orig = dout;
+        a.k_orig = k;
+        a.v_orig = v;
         a.T = T;
         a.Hq = Hq;
         a.Hkv = Hkv;
@@ -923,6 +928,8 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         qa.dout = dOp;
         qa.q_orig = q;
         qa.dout_orig = dout;
+        qa.k_orig = k;
+        qa.v_orig = v;
         qa.T = T;
         qa.Hq = Hq;
         qa.Hkv = Hkv;

@@ -105,6 +105,7 @@ struct DeviceTables {
     // of two position runs (the tensor-core kernels read such tiles from the
     // rank-ordered copy; single-run tiles straight from the caller's tensor).
     size_t o_qmask = 0;
+    size_t o_kvmask = 0;  // likewise for KV tiles (the K and V copies)
     // Work counters of the persistent kernels (uploaded as zeros; a kernel
     // returns its counter to zero when it finishes): [0, 2) forward.
     size_t o_sched = 0;

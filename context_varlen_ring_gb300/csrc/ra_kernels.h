@@ -31,13 +31,12 @@ struct PermJob {
     const void *src;
     void *dst;
     int64_t row_bytes;
+    const uint8_t *only = nullptr;  // T bytes: move just the rows i with only[i] != 0
 };
 // inverse = 0: dst[i] = src[perm[i]];  inverse = 1: dst[perm[i]] = src[i].
-// Up to 4 jobs share one launch (same perm, same T).  With `only` (T bytes)
-// given, the jobs from index only_from on move just the rows i with
-// only[i] != 0; the others move every row.
+// Up to 4 jobs share one launch (same perm, same T).
 cudaError_t launch_permute(const PermJob *jobs, int njobs, const int32_t *perm, int64_t T, int inverse,
-                           cudaStream_t st, const uint8_t *only = nullptr, int only_from = 0);
+                           cudaStream_t st);
 // [H, T] fp32: x[h, perm[i]] = y[h, i].
 cudaError_t launch_unpermute_cols(const float *y, float *x, const int32_t *perm, int64_t T, int H,
                                   cudaStream_t st);
@@ -51,8 +50,8 @@ cudaError_t launch_merge(int n, const float *const *outs, const float *const *ls
 // the jobs (Q, K, V) and dO (dout -> dout_p, Hq heads) by perm, and
 // D[h, p] = sum_c dO[p, h, c] * O[p, h, c] in fp32 at original rows p.
 // All pointers and row sizes must be 16-byte aligned (else cudaErrorInvalidValue).
-// With `only` (T bytes) given, the jobs from index only_from on and dout_p
-// receive just the rows i with only[i] != 0 (D is written for every row).
+// With dout_only (T bytes) given, dout_p receives just the rows i with
+// dout_only[i] != 0 (D is written for every row).
 // Copies n bytes from page-locked host memory (mapped into the device's
 // address space) to device memory with a kernel, so the copy never queues
 // behind other streams' transfers on a copy engine.  src and dst must be
@@ -60,7 +59,7 @@ cudaError_t launch_merge(int n, const float *const *outs, const float *const *ls
 cudaError_t launch_copy_from_host(const void *src, void *dst, size_t n, cudaStream_t st);
 cudaError_t launch_permute_rowdot(const PermJob *jobs, int njobs, const void *dout, void *dout_p, const void *out,
                                   float *D, const int32_t *perm, int64_t T, int Hq, cudaStream_t st,
-                                  const uint8_t *only = nullptr, int only_from = 0);
+                                  const uint8_t *dout_only = nullptr);
 cudaError_t launch_rowdot(const void *a, const void *b, int dtype, int64_t T, int H, int d, float *D,
                           cudaStream_t st);
 // Per (query tile, KV head): 128 columns of -lse*log2(e) (-inf for empty
@@ -118,8 +117,8 @@ cudaError_t launch_simt_bwd(const SimtBwdArgs &a, cudaStream_t st);
 // Tensor-core forward (bf16, d = 128).
 struct TcFwdArgs {
     const void *q, *k, *v;             // permuted buffers
-    const void *q_orig;                // nullable: Q in original order (rows = positions);
-                                       // single-run query tiles are read from it
+    const void *q_orig, *k_orig, *v_orig;  // nullable: Q / K and V in original order
+                                       // (rows = positions); single-run tiles are read from them
     int64_t Tq, Tk;
     int Hq, Hkv, G;
     const void *qtiles, *kvtiles;      // Tile records (two int4 each)
@@ -146,6 +145,7 @@ struct TcBwdArgs {
     const void *q, *k, *v, *dout;      // permuted buffers
     const void *q_orig, *dout_orig;    // nullable pair: Q and dO in original order, read for
                                        // single-run query tiles
+    const void *k_orig, *v_orig;       // nullable pair: K and V likewise for KV tiles
     int64_t T;
     int Hq, Hkv, G;
     const void *qtiles, *kvtiles;      // Tile records
@@ -167,7 +167,8 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st);
 // no atomics.  out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 +=.
 struct TcDqArgs {
     const void *q, *k, *v, *dout;      // permuted buffers
-    const void *q_orig, *dout_orig;    // nullable pair, as in TcBwdArgs
+    const void *q_orig, *dout_orig;    // nullable pairs, as in TcBwdArgs
+    const void *k_orig, *v_orig;
     int64_t T;
     int Hq, Hkv, G;
     const void *qtiles, *kvtiles;

@@ -49,9 +49,6 @@ static inline int num_sms() {
 struct PermJobs {
     PermJob j[4];
     int n;
-    // jobs [only_from, n) copy just the rows i with only[i] != 0 (when set)
-    const uint8_t *only;
-    int only_from;
 };
 
 // One warp per row; each lane moves vectors of type V (16 B when every row
@@ -70,8 +67,8 @@ __global__ void __launch_bounds__(256) permute_kernel(PermJobs jobs, const int32
         }
         const int64_t srow = inverse ? i : (int64_t)p;
         const int64_t drow = inverse ? (int64_t)p : i;
-        const int njobs = (jobs.only && !__ldg(jobs.only + i)) ? jobs.only_from : jobs.n;
-        for (int jb = 0; jb < njobs; ++jb) {
+        for (int jb = 0; jb < jobs.n; ++jb) {
+            if (jobs.j[jb].only && !__ldg(jobs.j[jb].only + i)) continue;
             const int64_t nvec = jobs.j[jb].row_bytes / (int64_t)sizeof(V);
             const V *__restrict__ src = reinterpret_cast<const V *>(jobs.j[jb].src) + srow * nvec;
             V *__restrict__ dst = reinterpret_cast<V *>(jobs.j[jb].dst) + drow * nvec;
@@ -93,13 +90,11 @@ __global__ void __launch_bounds__(256) permute_kernel(PermJobs jobs, const int32
 }
 
 cudaError_t launch_permute(const PermJob *jobs, int njobs, const int32_t *perm, int64_t T, int inverse,
-                           cudaStream_t st, const uint8_t *only, int only_from) {
+                           cudaStream_t st) {
     if (T <= 0 || njobs <= 0) return cudaSuccess;
-    if (njobs > 4 || only_from < 0 || only_from > njobs) return cudaErrorInvalidValue;
+    if (njobs > 4) return cudaErrorInvalidValue;
     PermJobs pj{};
     pj.n = njobs;
-    pj.only = only;
-    pj.only_from = only ? only_from : njobs;
     int vec = 16;
     for (int i = 0; i < njobs; ++i) {
         pj.j[i] = jobs[i];
@@ -241,7 +236,8 @@ __device__ __forceinline__ float dot8_bf16(const uint4 &a, const uint4 &b) {
 __global__ void __launch_bounds__(256) permute_rowdot_kernel(PermJobs jobs, const uint4 *__restrict__ dout,
                                                               uint4 *__restrict__ dout_p, const uint4 *__restrict__ out,
                                                               float *__restrict__ D, const int32_t *__restrict__ perm,
-                                                              int64_t T, int Hq, int *status) {
+                                                              int64_t T, int Hq, const uint8_t *__restrict__ dout_only,
+                                                              int *status) {
     const int lane = threadIdx.x & 31;
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -252,8 +248,8 @@ __global__ void __launch_bounds__(256) permute_rowdot_kernel(PermJobs jobs, cons
             if (lane == 0) dev::record_status(status, RA_ERR_DEVICE_BOUNDS);
             continue;
         }
-        const bool keep = !jobs.only || __ldg(jobs.only + i);
-        for (int jb = 0; jb < (keep ? jobs.n : jobs.only_from); ++jb) {
+        for (int jb = 0; jb < jobs.n; ++jb) {
+            if (jobs.j[jb].only && !__ldg(jobs.j[jb].only + i)) continue;
             const int64_t nvec = jobs.j[jb].row_bytes / 16;
             const uint4 *__restrict__ src = reinterpret_cast<const uint4 *>(jobs.j[jb].src) + (int64_t)p * nvec;
             uint4 *__restrict__ dst = reinterpret_cast<uint4 *>(jobs.j[jb].dst) + i * nvec;
@@ -274,6 +270,7 @@ __global__ void __launch_bounds__(256) permute_rowdot_kernel(PermJobs jobs, cons
         const uint4 *__restrict__ a = dout + (int64_t)p * nvo;
         const uint4 *__restrict__ b = out + (int64_t)p * nvo;
         uint4 *__restrict__ dst = dout_p + i * nvo;
+        const bool keep = !dout_only || __ldg(dout_only + i);
         for (int64_t c0 = lane; c0 < nvo; c0 += 128) {
             uint4 x[4], y[4];
 #pragma unroll
@@ -303,13 +300,11 @@ __global__ void __launch_bounds__(256) permute_rowdot_kernel(PermJobs jobs, cons
 
 cudaError_t launch_permute_rowdot(const PermJob *jobs, int njobs, const void *dout, void *dout_p, const void *out,
                                   float *D, const int32_t *perm, int64_t T, int Hq, cudaStream_t st,
-                                  const uint8_t *only, int only_from) {
+                                  const uint8_t *dout_only) {
     if (T <= 0) return cudaSuccess;
-    if (njobs < 0 || njobs > 4 || only_from < 0 || only_from > njobs) return cudaErrorInvalidValue;
+    if (njobs < 0 || njobs > 4) return cudaErrorInvalidValue;
     PermJobs pj{};
     pj.n = njobs;
-    pj.only = only;
-    pj.only_from = only ? only_from : njobs;
     auto al = [](const void *q, int64_t rb) { return (reinterpret_cast<uintptr_t>(q) % 16) == 0 && (rb % 16) == 0; };
     for (int i = 0; i < njobs; ++i) {
         if (!al(jobs[i].src, jobs[i].row_bytes) || !al(jobs[i].dst, jobs[i].row_bytes)) return cudaErrorInvalidValue;
@@ -319,7 +314,7 @@ cudaError_t launch_permute_rowdot(const PermJob *jobs, int njobs, const void *do
     const int64_t want = (T + 7) / 8;
     const int blocks = (int)std::min<int64_t>(want, (int64_t)num_sms() * 8);
     permute_rowdot_kernel<<<blocks, 256, 0, st>>>(pj, static_cast<const uint4 *>(dout), static_cast<uint4 *>(dout_p),
-                                                  static_cast<const uint4 *>(out), D, perm, T, Hq,
+                                                  static_cast<const uint4 *>(out), D, perm, T, Hq, dout_only,
                                                   device_status_ptr());
     return cudaGetLastError();
 }

@@ -302,6 +302,7 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
     dt.o_off = take(zp ? zp->off.size() * 4 : 0);
     dt.o_sched = take(64);
     dt.o_qmask = take(zp && tp ? zp->perm.size() : 0);
+    dt.o_kvmask = take(zp && tp ? zp->perm.size() : 0);
     dt.blob.assign(o, 0);
     auto put = [&](size_t at, const void *src, size_t bytes) {
         if (bytes) std::memcpy(dt.blob.data() + at, src, bytes);
@@ -329,10 +330,14 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
         // like every other row a tile reads (the key-side backward sums
         // over a tile's padded rows with zero weight)
         const int64_t T = (int64_t)zp->perm.size();
-        uint8_t *mask = dt.blob.data() + dt.o_qmask;
-        for (const Tile &t : tp->qtiles)
-            if (t.split < t.len)
-                for (int64_t i = t.row0; i < (int64_t)t.row0 + tp->q_tokens && i < T; ++i) mask[i] = 1;
+        auto mark = [&](size_t at, const std::vector<Tile> &tiles, int box) {
+            uint8_t *mask = dt.blob.data() + at;
+            for (const Tile &t : tiles)
+                if (t.split < t.len)
+                    for (int64_t i = t.row0; i < (int64_t)t.row0 + box && i < T; ++i) mask[i] = 1;
+        };
+        mark(dt.o_qmask, tp->qtiles, tp->q_tokens);
+        mark(dt.o_kvmask, tp->kvtiles, kBN);
     }
 }
 

@@ -75,9 +75,11 @@ constexpr uint32_t kSmemBytes = kOffBar + 128;    // 16 barrier words; base must
 struct BwdParams {
     CUtensorMap tmQ, tmK, tmV, tmDO;
     CUtensorMap tmQo, tmDOo;  // Q and dO in original order (valid when qdo_direct)
+    CUtensorMap tmKo, tmVo;   // K and V in original order (valid when kv_direct)
     const int4 *qtiles, *kvtiles, *items;
     const int *q_off;
     int qdo_direct;  // single-run query tiles: Q and dO read at their first position
+    int kv_direct;   // single-run KV tiles: K and V likewise
     int n_items, cp, B, G, log2G, Hq, Hkv;
     int t0, t1, causal, window, out_mode;          // 0 bf16 store, 1 fp32 store, 2 fp32 +=
     float scale, scale_log2;
@@ -175,11 +177,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                 tma_prefetch_desc(&p.tmQo);
                 tma_prefetch_desc(&p.tmDOo);
             }
+            // one position run (split == len): the original rows
+            const bool kdir = p.kv_direct && ka.z == ka.y;
+            const CUtensorMap *mk = kdir ? &p.tmKo : &p.tmK, *mv = kdir ? &p.tmVo : &p.tmV;
+            const int krow = kdir ? ka.w : ka.x;
             mbar_arrive_expect_tx(kv_full, 2 * kTile);
-            tma_load_3d(smem + kOffK, &p.tmK, kv_full, 0, g, ka.x);
-            tma_load_3d(smem + kOffK + kHalf, &p.tmK, kv_full, 64, g, ka.x);
-            tma_load_3d(smem + kOffV, &p.tmV, kv_full, 0, g, ka.x);
-            tma_load_3d(smem + kOffV + kHalf, &p.tmV, kv_full, 64, g, ka.x);
+            tma_load_3d(smem + kOffK, mk, kv_full, 0, g, krow);
+            tma_load_3d(smem + kOffK + kHalf, mk, kv_full, 64, g, krow);
+            tma_load_3d(smem + kOffV, mv, kv_full, 0, g, krow);
+            tma_load_3d(smem + kOffV + kHalf, mv, kv_full, 64, g, krow);
         }
         uint32_t n = 0;  // tiles published
         int ok = 1;
@@ -555,6 +561,12 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
         if (!make_map(&p.tmQo, a.q_orig, a.T, a.Hq, G, kBM / G) || !make_map(&p.tmDOo, a.dout_orig, a.T, a.Hq, G, kBM / G))
             return cudaErrorInvalidValue;
         p.qdo_direct = 1;
+    }
+    if ((a.k_orig != nullptr) != (a.v_orig != nullptr)) return cudaErrorInvalidValue;
+    if (a.k_orig) {
+        if (!make_map(&p.tmKo, a.k_orig, a.T, a.Hkv, 1, kBN) || !make_map(&p.tmVo, a.v_orig, a.T, a.Hkv, 1, kBN))
+            return cudaErrorInvalidValue;
+        p.kv_direct = 1;
     }
     p.qtiles = static_cast<const int4 *>(a.qtiles);
     p.kvtiles = static_cast<const int4 *>(a.kvtiles);

@@ -69,9 +69,11 @@ constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;
 struct DqParams {
     CUtensorMap tmQ, tmK, tmV, tmDO;
     CUtensorMap tmQo, tmDOo;  // Q and dO in original order (valid when qdo_direct)
+    CUtensorMap tmKo, tmVo;   // K and V in original order (valid when kv_direct)
     const int4 *qtiles, *kvtiles, *items;
     const int *kv_off;
     int qdo_direct;  // single-run query tiles: Q and dO read at their first position
+    int kv_direct;   // single-run KV tiles: K and V likewise
     int n_items, cp, B, G, log2G, Hq;
     int t0, t1, causal, window, out_mode;  // out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 +=
     float scale, scale_log2, log2_scale;
@@ -196,6 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 tma_prefetch_desc(&p.tmK);
                 tma_prefetch_desc(&p.tmV);
                 if (p.qdo_direct) tma_prefetch_desc(&p.tmQo);
+                if (p.kv_direct) {
+                    tma_prefetch_desc(&p.tmKo);
+                    tma_prefetch_desc(&p.tmVo);
+                }
             }
             uint32_t u = 0, ri = 0;
             int ok = 1;
@@ -256,6 +262,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                                     ring[e] = make_int4(cc, len | (split << 16), pos0, pos1);
                                     mbar_arrive(info_full + e);
                                 }
+                                // one position run: the original rows [pos0, pos0 + len)
+                                const bool kdir = p.kv_direct && split == len;
+                                const int krow = kdir ? pos0 : row0;
                                 for (int kv = 0; kv < 2 && ok; ++kv, ++u) {
                                     const uint32_t slot = u % kSlots, ph = (u / kSlots) & 1u;
                                     if (!mbar_wait(kv_empty + slot, ph ^ 1u, wc)) {
@@ -263,10 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                                         break;
                                     }
                                     uint8_t *dst = base + kOffKV + slot * kTile;
-                                    const CUtensorMap *m = kv ? &p.tmV : &p.tmK;
+                                    const CUtensorMap *m = kv ? (kdir ? &p.tmVo : &p.tmV) : (kdir ? &p.tmKo : &p.tmK);
                                     mbar_arrive_expect_tx(kv_full + slot, kTile);
-                                    tma_load_3d(dst, m, kv_full + slot, 0, g, row0);
-                                    tma_load_3d(dst + kHalf, m, kv_full + slot, 64, g, row0);
+                                    tma_load_3d(dst, m, kv_full + slot, 0, g, krow);
+                                    tma_load_3d(dst + kHalf, m, kv_full + slot, 64, g, krow);
                                 }
                             }
                             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -684,6 +693,12 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
         if (!make_map(&p.tmQo, a.q_orig, a.T, a.Hq, G, kBM / G) || !make_map(&p.tmDOo, a.dout_orig, a.T, a.Hq, G, kBM / G))
             return cudaErrorInvalidValue;
         p.qdo_direct = 1;
+    }
+    if ((a.k_orig != nullptr) != (a.v_orig != nullptr)) return cudaErrorInvalidValue;
+    if (a.k_orig) {
+        if (!make_map(&p.tmKo, a.k_orig, a.T, a.Hkv, 1, kBN) || !make_map(&p.tmVo, a.v_orig, a.T, a.Hkv, 1, kBN))
+            return cudaErrorInvalidValue;
+        p.kv_direct = 1;
     }
     p.qtiles = static_cast<const int4 *>(a.qtiles);
     p.kvtiles = static_cast<const int4 *>(a.kvtiles);

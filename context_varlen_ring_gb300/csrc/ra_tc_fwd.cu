@@ -76,11 +76,13 @@ constexpr uint32_t kSmemBytes = kOffBar + 512 + 1024;  // + barriers/ring + alig
 
 struct FwdParams {
     CUtensorMap tmQ, tmK, tmV;
-    CUtensorMap tmQo;  // Q in original order (valid when q_direct)
+    CUtensorMap tmQo;       // Q in original order (valid when q_direct)
+    CUtensorMap tmKo, tmVo;  // K, V in original order (valid when kv_direct)
     const int4 *qtiles, *kvtiles, *items;
     const int *kv_off;
     int *sched;  // [2]: next item to claim, CTAs finished (zero between launches)
-    int q_direct;  // single-run query tiles are read from tmQo at their first position
+    int q_direct;   // single-run query tiles are read from tmQo at their first position
+    int kv_direct;  // single-run KV tiles likewise from tmKo / tmVo
     int n_items, cp, B, G, log2G, Hq;
     int t0, t1, causal, window, out_mode;
     float scale_log2;
@@ -239,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 tma_prefetch_desc(&p.tmK);
                 tma_prefetch_desc(&p.tmV);
                 if (p.q_direct) tma_prefetch_desc(&p.tmQo);
+                if (p.kv_direct) {
+                    tma_prefetch_desc(&p.tmKo);
+                    tma_prefetch_desc(&p.tmVo);
+                }
             }
             for (int it = 0; ok; ++it) {
                 int item = 0;
@@ -330,6 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                             const int cc = __shfl_sync(0xffffffffu, c0 | (c1 << 2), src);
                             if (lane == 0) {
                                 ok = publish(make_int4(cc, len | (split << 16), pos0, pos1));
+                                // one position run: the original rows [pos0, pos0 + len)
+                                const bool dir = p.kv_direct && split == len;
+                                const int krow = dir ? pos0 : row0;
                                 for (int kv = 0; kv < 2 && ok; ++kv, ++u) {
                                     const uint32_t slot = u % kSlots, ph = (u / kSlots) & 1u;
                                     if (!mbar_wait(kv_empty + slot, ph ^ 1u, wc)) {
@@ -337,10 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                                         break;
                                     }
                                     uint8_t *dst = base + kOffKV + slot * kTile;
-                                    const CUtensorMap *m = kv ? &p.tmV : &p.tmK;
+                                    const CUtensorMap *m = kv ? (dir ? &p.tmVo : &p.tmV) : (dir ? &p.tmKo : &p.tmK);
                                     mbar_arrive_expect_tx(kv_full + slot, kTile);
-                                    tma_load_3d(dst, m, kv_full + slot, 0, g, row0);
-                                    tma_load_3d(dst + kHalf, m, kv_full + slot, 64, g, row0);
+                                    tma_load_3d(dst, m, kv_full + slot, 0, g, krow);
+                                    tma_load_3d(dst + kHalf, m, kv_full + slot, 64, g, krow);
                                 }
                                 if (ok && q_pending) ok = load_q();
                             }
@@ -731,6 +740,12 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
     if (a.q_orig) {
         if (!make_map(&p.tmQo, a.q_orig, a.Tq, a.Hq, G, kBM / G)) return cudaErrorInvalidValue;
         p.q_direct = 1;
+    }
+    if ((a.k_orig != nullptr) != (a.v_orig != nullptr)) return cudaErrorInvalidValue;
+    if (a.k_orig) {
+        if (!make_map(&p.tmKo, a.k_orig, a.Tk, a.Hkv, 1, kBN) || !make_map(&p.tmVo, a.v_orig, a.Tk, a.Hkv, 1, kBN))
+            return cudaErrorInvalidValue;
+        p.kv_direct = 1;
     }
     p.qtiles = static_cast<const int4 *>(a.qtiles);
     p.kvtiles = static_cast<const int4 *>(a.kvtiles);
