@@ -209,6 +209,11 @@ ra_status ra_lse_merge(int n_parts, const float *const *outs, const float *const
  * as in ra_varlen_attn_partial (-1 = none); positions are the original
  * (unpermuted) token indices, so the zigzag reorder leaves the mask intact.
  * workspace: DEVICE, >= ra_ring_workspace_bytes(...) for the same arguments.
+ * On the tensor-core path (bf16, d = 128) the kernels read every tile whose
+ * rows form one position run straight from q, k, v (and dout), and the
+ * workspace receives rank-ordered copies of the rows of the other tiles
+ * only (those that straddle two zigzag chunks); ra_zigzag_permute gives the
+ * whole rank-ordered tensor where a caller needs it.
  * Asynchronous on `stream`.  The backward's fused tensor-core path runs its
  * key-side kernel on a second, library-owned stream forked from and joined
  * back to `stream` through events.  Both calls may be captured into a CUDA
@@ -229,8 +234,8 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
  * RA_BWD_FWD_RESERVE: the workspace is a reserve space left by the
  * preceding ra_ring_attn_fwd on the same stream with the same q, k, v
  * (unmodified), dtype, shapes, cu_seqlens, cp, zz_mode, causal and sched,
- * and nothing has written into it since: the rank-ordered Q, K, V and the
- * tile tables it holds are reused instead of rebuilt (they are the
+ * and nothing has written into it since: the rank-ordered Q, K, V rows and
+ * the tile tables it holds are reused instead of rebuilt (they are the
  * forward's saved activations).  The library checks on the host that the
  * last forward on this workspace had the same pointers and plan and
  * ignores the flag otherwise; it cannot see changes to the contents. */
