@@ -2,11 +2,14 @@
 
 One step = the whole hot path on the packed 32768-token workload (GQA 32/8,
 d=128, bf16, per-document zigzag over 8 simulated CP ranks): zigzag
-permute of Q, K, V, ring forward with on-chip merge (O and LSE written in
-the original order), backward preprocess (permute dO, D = rowsum(dO*O),
-per-tile LSE/D), ring backward with fp32 dK/dV (the backward reuses the
-forward's rank-ordered Q, K, V from the shared workspace, its saved
-activations).  FLOPs count allowed (causal, same-document) pairs only:
+permute (rank-ordered copies of the rows of tiles that straddle two zigzag
+chunks; the kernels read every other tile in place), ring forward with
+on-chip merge (O and LSE written in the original order), backward
+preprocess (the same copies of dO, D = rowsum(dO*O), per-tile LSE/D), ring
+backward with fp32 dK/dV (the backward reuses the forward's copies and tile
+tables from the shared workspace, its saved activations).  --sched
+allgather times the all-gather form instead (each rank's queries against
+every rank's K/V, read in original order).  FLOPs count allowed (causal, same-document) pairs only:
 4*d*Hq per pair forward, 10*d*Hq backward.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -242,8 +245,8 @@ def fwd_configs(args, ra, torch):
         out = torch.empty_like(q)
         lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
         ws = torch.empty(ra.ring_workspace_bytes(T, hq, hkv, d, 0 if wl.dtype == torch.bfloat16 else 1, cu, wl.cp,
-                                                 wl.zz_mode, "fused", bwd=False), dtype=torch.uint8, device=dev)
-        f = lambda: ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, "fused", out=out, lse=lse,
+                                                 wl.zz_mode, args.sched, bwd=False), dtype=torch.uint8, device=dev)
+        f = lambda: ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, args.sched, out=out, lse=lse,
                                      workspace=ws, window=args.window)
         for _ in range(max(args.warmup, 3)):
             f()
@@ -259,7 +262,7 @@ def fwd_configs(args, ra, torch):
         ms = e0.elapsed_time(e1) / args.steps
         tf = flops / (ms / 1e3) / 1e12
         print(json.dumps({"fwd_config": wl.name, "T": T, "Hq": hq, "Hkv": hkv, "d": d, "cp": wl.cp,
-                          "window": args.window,
+                          "window": args.window, "sched": args.sched,
                           "allowed_pairs_per_head": pairs, "ms": ms, "tflops": tf,
                           "frac_of_peak": tf / peak_burst, "peak_tflops": peak_burst, "peak_source": peak_src,
                           "steps": args.steps, "warmup": args.warmup}), flush=True)
@@ -312,7 +315,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--sched", default="fused", choices=["fused", "stepwise"])
+    ap.add_argument("--sched", default="fused", choices=["fused", "stepwise", "allgather"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--probe", action="store_true",
                     help="only W+K plain steps (for profilers): no e2e, per-kernel or CPU passes")
@@ -563,14 +566,16 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name + (f", sliding window {args.window}" if args.window >= 0 else ""),
+        "config": {"workload": wl.name + (f", sliding window {args.window}" if args.window >= 0 else "")
+                               + (", all-gather KV schedule" if args.sched == "allgather" else ""),
                    "window": args.window, "T": T, "docs": list(wl.doc_lens), "Hq": hq, "Hkv": hkv, "d": d,
                    "cp": wl.cp, "zigzag": "per-doc", "sched": args.sched, "causal_pairs_per_head": pairs,
                    "l2": "no flush: each step streams ~2.6 GB (Q, dO, O 268 MB each, fp32 dQ 537 MB, permuted "
                          "copies), far above the 129 MB L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "bwd_reserve": "the backward reuses the forward's rank-ordered Q, K, V and tile tables from "
-                                  "the shared workspace (its saved activations); every step permutes once"},
+                   "bwd_reserve": "the backward reuses the forward's tile tables and rank-ordered copies (the rows "
+                                  "of tiles that straddle two zigzag chunks; the kernels read every other tile in "
+                                  "place) from the shared workspace; every step permutes once"},
         "fwd": {"tflops": fwd_tflops, "ms": fwd_ms, "frac_of_peak": fwd_tflops / peak_burst},
         "fwd_bwd_frac_of_peak": value / world / peak_burst,
         "peak_tflops": {"burst": peak_burst, "sustained": peak_sust, "source": peak_src},

@@ -13,16 +13,16 @@ import math
 import numpy as np
 import torch
 
-from ._lib import (RA_BF16, RA_BWD_FWD_RESERVE, RA_FP32, RA_SCHED_FUSED, RA_SCHED_STEPWISE, RA_ZZ_GLOBAL,
-                   RA_ZZ_PER_DOC, RaError, check, lib)
+from ._lib import (RA_BF16, RA_BWD_FWD_RESERVE, RA_FP32, RA_SCHED_ALLGATHER, RA_SCHED_FUSED, RA_SCHED_STEPWISE,
+                   RA_ZZ_GLOBAL, RA_ZZ_PER_DOC, RaError, check, lib)
 
 __all__ = [
     "zigzag_plan", "zigzag_permute", "zigzag_unpermute", "varlen_attn_partial", "lse_merge",
     "ring_attn_fwd", "ring_attn_bwd", "ring_rank_pairs", "device_status", "selftest_wait_timeout",
-    "RA_ZZ_GLOBAL", "RA_ZZ_PER_DOC", "RA_SCHED_FUSED", "RA_SCHED_STEPWISE", "RaError",
+    "RA_ZZ_GLOBAL", "RA_ZZ_PER_DOC", "RA_SCHED_FUSED", "RA_SCHED_STEPWISE", "RA_SCHED_ALLGATHER", "RaError",
 ]
 
-_SCHED = {"fused": RA_SCHED_FUSED, "stepwise": RA_SCHED_STEPWISE}
+_SCHED = {"fused": RA_SCHED_FUSED, "stepwise": RA_SCHED_STEPWISE, "allgather": RA_SCHED_ALLGATHER}
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -181,7 +181,10 @@ def ring_attn_fwd(q, k, v, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal
                   window: int = -1):
     """Simulated zigzag ring attention forward; returns (out [T,Hq,d] in q's
     dtype, lse fp32 [Hq,T]) in the original token order.  window >= 0: a key
-    is visible only up to `window` positions behind its query."""
+    is visible only up to `window` positions behind its query.  sched:
+    "fused" (ring steps in one launch), "stepwise" (a launch per ring step,
+    then the LSE merge) or "allgather" (each rank's queries over the gathered
+    K/V of all ranks)."""
     _check_cuda(q, k, v)
     T, Hq, d = q.shape
     Hkv = k.shape[1]

@@ -27,6 +27,7 @@ RA_BF16 = 0
 RA_FP32 = 1
 RA_SCHED_FUSED = 0
 RA_SCHED_STEPWISE = 1
+RA_SCHED_ALLGATHER = 2
 
 # every symbol include/ra.h declares
 EXPORTS = (

@@ -652,7 +652,8 @@ ra_status ring_checks(const void *q, const void *k, const void *v, int dtype, in
     if ((st = validate_cu(cu, B, T))) return st;
     if (cp < 1 || cp > kMaxMergeParts) return fail(RA_ERR_INVALID_ARG, "cp must be in [1, 64]");
     if (mode != RA_ZZ_GLOBAL && mode != RA_ZZ_PER_DOC) return fail(RA_ERR_INVALID_ARG, "unknown zigzag mode");
-    if (sched != RA_SCHED_FUSED && sched != RA_SCHED_STEPWISE) return fail(RA_ERR_INVALID_ARG, "unknown schedule");
+    if (sched != RA_SCHED_FUSED && sched != RA_SCHED_STEPWISE && sched != RA_SCHED_ALLGATHER)
+        return fail(RA_ERR_INVALID_ARG, "unknown schedule");
     if (!std::isfinite(scale)) return fail(RA_ERR_INVALID_ARG, "scale must be finite");
     if (T > 0 && (!q || !k || !v)) return fail(RA_ERR_INVALID_ARG, "NULL tensor");
     if (T > 0 && (!aligned16(q) || !aligned16(k) || !aligned16(v)))
@@ -667,7 +668,9 @@ size_t ra_ring_workspace_bytes(int64_t T, int Hq, int Hkv, int d, int dtype, con
     if (check_common(dtype, Hq, Hkv, d) != RA_OK || T < 0) return 0;
     ra_status st;
     const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
-    auto plan = get_ring_plan(cu, B, cp, mode, Hq / Hkv, Hkv, 1, -1, tc, &st);  // sizes: mask-independent
+    if (sched != RA_SCHED_FUSED && sched != RA_SCHED_STEPWISE && sched != RA_SCHED_ALLGATHER) return 0;
+    // sizes are mask-independent
+    auto plan = get_ring_plan(cu, B, cp, mode, Hq / Hkv, Hkv, 1, -1, tc, tc && sched == RA_SCHED_ALLGATHER, &st);
     if (!plan) return 0;
     return ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, bwd).total;
 }
@@ -682,8 +685,13 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     if (!aligned16(out)) return fail(RA_ERR_UNSUPPORTED, "out must be 16-byte aligned");
     const int G = Hq / Hkv;
     const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
+    // all-gather: one pass of each rank's queries over every document's K/V
+    // in original order (tensor cores); elsewhere the fused ring computes the
+    // same attention
+    const bool allgather = sched == RA_SCHED_ALLGATHER && tc;
+    if (sched == RA_SCHED_ALLGATHER && !tc) sched = RA_SCHED_FUSED;
     if ((st = ring_window(T, &window))) return st;
-    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, &st);
+    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, allgather, &st);
     if (!plan) return st;
     const RingLayout L = ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, 0);
     if (!workspace || ws_bytes < L.total)
@@ -710,8 +718,9 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
                        {k, Kp, (int64_t)Hkv * d * (int64_t)es, kvmask},
                        {v, Vp, (int64_t)Hkv * d * (int64_t)es, kvmask}};
     {
+        // all-gather: K and V are read in original order, never copied
         ProfScope ps("ra_permute_fwd", s);
-        RA_CUDA(launch_permute(jobs, 3, perm, T, 0, s), "permute launch");
+        RA_CUDA(launch_permute(jobs, allgather ? 1 : 3, perm, T, 0, s), "permute launch");
     }
     reserve_record(workspace, plan.get(), q, k, v, dtype, T, Hq, Hkv, d, causal, sched);
 
@@ -720,8 +729,8 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
             TcFwdArgs a{};
             a.q = Qp;
             a.q_orig = q;
-            a.k = Kp;
-            a.v = Vp;
+            a.k = allgather ? k : Kp;
+            a.v = allgather ? v : Vp;
             a.k_orig = k;
             a.v_orig = v;
             a.Tq = T;
@@ -782,7 +791,7 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
         return RA_OK;
     };
 
-    if (sched == RA_SCHED_FUSED) {
+    if (sched == RA_SCHED_FUSED || sched == RA_SCHED_ALLGATHER) {
         // a4+a5+a6 in one launch: ring order inside each tile, on-chip merge,
         // rows written straight back to their original positions.  t0 = -1:
         // each item walks only the ring steps that hold its visited KV tiles.
@@ -829,8 +838,10 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         return fail(RA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned");
     const int G = Hq / Hkv;
     const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
+    const bool allgather = sched == RA_SCHED_ALLGATHER && tc;
+    if (sched == RA_SCHED_ALLGATHER && !tc) sched = RA_SCHED_FUSED;
     if ((st = ring_window(T, &window))) return st;
-    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, &st);
+    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, allgather, &st);
     if (!plan) return st;
     const RingLayout L = ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, 1);
     if (!workspace || ws_bytes < L.total)
@@ -868,7 +879,9 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
     if (dtype == RA_BF16 && d == 128 && aligned16(out) && aligned16(dout)) {
         // one pass: the permutes and D from the same dO reads
         ProfScope ps("ra_permute_rowdot", s);
-        RA_CUDA(launch_permute_rowdot(jobs, reserve ? 0 : 3, dout, dOp, out, D, perm, T, Hq, s, qmask),
+        // (all-gather: K and V are read in original order, never copied)
+        RA_CUDA(launch_permute_rowdot(jobs, reserve ? 0 : (allgather ? 1 : 3), dout, dOp, out, D, perm, T, Hq, s,
+                                      qmask),
                 "permute+rowdot launch");
     } else {
         {
@@ -881,7 +894,7 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         ProfScope ps("ra_rowdot", s);
         RA_CUDA(launch_rowdot(dout, out, dtype, T, Hq, d, D, s), "rowdot launch");
     }
-    const bool fused_tc = tc && sched == RA_SCHED_FUSED;
+    const bool fused_tc = tc && (sched == RA_SCHED_FUSED || sched == RA_SCHED_ALLGATHER);
     if (!fused_tc) {
         RA_CUDA(cudaMemsetAsync(dqa, 0, (size_t)T * Hq * d * 4, s), "memset dq");
         RA_CUDA(cudaMemsetAsync(dka, 0, (size_t)T * Hkv * d * 4, s), "memset dk");
@@ -899,8 +912,8 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         }
         TcBwdArgs a{};
         a.q = Qp;
-        a.k = Kp;
-        a.v = Vp;
+        a.k = allgather ? k : Kp;
+        a.v = allgather ? v : Vp;
         a.dout = dOp;
         a.q_orig = q;
         a.dout_orig = dout;
@@ -923,8 +936,8 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         a.tile_ld = tld;
         TcDqArgs qa{};
         qa.q = Qp;
-        qa.k = Kp;
-        qa.v = Vp;
+        qa.k = allgather ? k : Kp;
+        qa.v = allgather ? v : Vp;
         qa.dout = dOp;
         qa.q_orig = q;
         qa.dout_orig = dout;

@@ -89,7 +89,11 @@ inline int classify(const Tile &q, const Tile &k, int causal, int window) {
 }
 
 // Ring tile plan: query side = key side = the permuted buffer.
-ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, TilePlan &tp);
+// allgather: the key side is every document's K/V in original order (the
+// all-gather schedule), held as the segments of rank 0; otherwise each
+// rank's zigzag shard, as the ring passes it.
+ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, bool allgather,
+                           TilePlan &tp);
 
 // Generic partial's tile plan: one "rank", separate Q and K sides.
 ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg,
@@ -139,7 +143,7 @@ struct RingPlan {
 ra_status upload_plan_tables(RingPlan &plan, void *dst, void *stream);
 // Cached plans keyed by content (cu_seqlens, cp, mode, G, Hkv, causal, window).
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
-                                        int causal, int window, bool want_tiles, ra_status *st);
+                                        int causal, int window, bool want_tiles, bool allgather, ra_status *st);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -230,7 +230,8 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
     });
 }
 
-ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, TilePlan &tp) {
+ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, bool allgather,
+                           TilePlan &tp) {
     if (G < 1 || kBM % G != 0) return fail(RA_ERR_UNSUPPORTED, "GQA group must divide 128");
     tp = TilePlan();
     tp.cp = zp.cp;
@@ -247,7 +248,10 @@ ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int
             if (b == B) break;
             const int64_t lo = zp.off[r] + zp.cu_local[idx], hi = zp.off[r] + zp.cu_local[idx + 1];
             append_tiles(tp.qtiles, zp.perm.data(), lo, hi, tp.q_tokens, b);
-            append_tiles(tp.kvtiles, zp.perm.data(), lo, hi, kBN, b);
+            if (!allgather)
+                append_tiles(tp.kvtiles, zp.perm.data(), lo, hi, kBN, b);
+            else if (r == 0)  // the whole document, original rows = positions
+                append_tiles(tp.kvtiles, nullptr, zp.cu[b], zp.cu[b + 1], kBN, b);
         }
     }
     tp.q_off.back() = (int32_t)tp.qtiles.size();
@@ -342,7 +346,7 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
 }
 
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
-                                        int causal, int window, bool want_tiles, ra_status *st) {
+                                        int causal, int window, bool want_tiles, bool allgather, ra_status *st) {
     static std::mutex mu;
     static std::map<std::string, std::shared_ptr<RingPlan>> cache;
     static std::vector<std::string> order;
@@ -350,7 +354,7 @@ std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mo
     if (*st) return nullptr;
     std::string key;
     key.append(reinterpret_cast<const char *>(cu), sizeof(int32_t) * (size_t)(B + 1));
-    int32_t tail[8] = {B, cp, mode, G, Hkv, causal, window, want_tiles ? 1 : 0};
+    int32_t tail[9] = {B, cp, mode, G, Hkv, causal, window, want_tiles ? 1 : 0, allgather ? 1 : 0};
     key.append(reinterpret_cast<const char *>(tail), sizeof(tail));
     {
         std::lock_guard<std::mutex> lk(mu);
@@ -361,7 +365,7 @@ std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mo
     *st = build_zigzag(cu, B, cp, mode, plan->zz);
     if (*st) return nullptr;
     if (want_tiles) {
-        *st = build_ring_tiles(plan->zz, G, Hkv, causal, window, plan->tiles);
+        *st = build_ring_tiles(plan->zz, G, Hkv, causal, window, allgather, plan->tiles);
         if (*st) return nullptr;
         plan->has_tiles = true;
     }

@@ -54,7 +54,7 @@ enum {
 
 enum { RA_ZZ_GLOBAL = 0, RA_ZZ_PER_DOC = 1 };        /* zigzag modes       */
 enum { RA_BF16 = 0, RA_FP32 = 1 };                   /* element types      */
-enum { RA_SCHED_FUSED = 0, RA_SCHED_STEPWISE = 1 };  /* ring schedules     */
+enum { RA_SCHED_FUSED = 0, RA_SCHED_STEPWISE = 1, RA_SCHED_ALLGATHER = 2 };  /* CP schedules */
 
 /* ------------------------------------------------------------------------
  * ra_zigzag_plan  (HOST, synchronous, no GPU needed)
@@ -197,6 +197,19 @@ ra_status ra_lse_merge(int n_parts, const float *const *outs, const float *const
  *   sched RA_SCHED_STEPWISE : one partial launch per ring step into fp32
  *                             buffers, then ra_lse_merge and unpermute
  *                             (backward: fp32 dK/dV accumulated per step).
+ *   sched RA_SCHED_ALLGATHER: the all-gather form of context parallelism
+ *                             (K/V of every rank gathered, then one pass of
+ *                             each rank's zigzag queries over them: the
+ *                             Llama 3 scheme discussed in "Zigzag attention
+ *                             support?", ring-attention-pytorch issue #20,
+ *                             and the Transformer-Engine path of maxtext PR
+ *                             #1133).  The gathered K/V are the documents in
+ *                             original order, tiled per document, so they
+ *                             are read in place and never permuted.  Same
+ *                             attention as the ring; only the tiling of
+ *                             the key side and the rounding order differ.
+ *                             Without tensor-core kernels (fp32, other
+ *                             shapes) it runs as RA_SCHED_FUSED.
  * Forward:
  *   q DEVICE [T, Hq, d], k, v DEVICE [T, Hkv, d] (dtype), out DEVICE
  *   [T, Hq, d] (dtype), lse DEVICE [Hq, T] fp32.

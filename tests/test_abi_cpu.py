@@ -121,6 +121,16 @@ def test_workspace_sizes(ra):
     assert qkv < f < qkv + (64 << 20)
     assert s > f + 8 * 32768 * 32 * 128 * 4
     assert b > f
+    # the all-gather schedule keeps the fused layout; its key side is tiled
+    # per document (fewer KV tiles and key-side items than the ring shards)
+    a = ra.ring_workspace_bytes(32768, 32, 8, 128, 0, cu, 8, W.ZZ_PER_DOC, "allgather")
+    ab = ra.ring_workspace_bytes(32768, 32, 8, 128, 0, cu, 8, W.ZZ_PER_DOC, "allgather", bwd=True)
+    assert qkv < a <= f and ab <= b and f - a < (1 << 20)
+    import ctypes
+    from context_varlen_ring_gb300 import _lib
+    c = np.ascontiguousarray(cu, dtype=np.int32)
+    assert _lib.lib().ra_ring_workspace_bytes(32768, 32, 8, 128, 0, c.ctypes.data_as(ctypes.c_void_p), len(c) - 1,
+                                              8, W.ZZ_PER_DOC, 3, 0) == 0  # unknown schedule
 
 
 def test_ring_rank_pairs_window_matches_oracle(orc):
