@@ -18,7 +18,7 @@ from ._lib import (RA_BF16, RA_BWD_FWD_RESERVE, RA_FP32, RA_SCHED_ALLGATHER, RA_
 
 __all__ = [
     "zigzag_plan", "zigzag_permute", "zigzag_unpermute", "varlen_attn_partial", "lse_merge",
-    "ring_attn_fwd", "ring_attn_bwd", "ring_rank_pairs", "device_status", "selftest_wait_timeout",
+    "ring_attn_fwd", "ring_attn_bwd", "ring_rank_pairs", "ring_plan_stats", "device_status", "selftest_wait_timeout",
     "RA_ZZ_GLOBAL", "RA_ZZ_PER_DOC", "RA_SCHED_FUSED", "RA_SCHED_STEPWISE", "RA_SCHED_ALLGATHER", "RaError",
 ]
 
@@ -79,6 +79,23 @@ def ring_rank_pairs(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool 
     check(lib().ra_ring_rank_pairs(_np_ptr(cu), len(cu) - 1, cp, mode, int(causal), int(window), _np_ptr(counts)),
           "ra_ring_rank_pairs")
     return counts
+
+
+PLAN_STATS = ("q_tiles", "kv_tiles", "fwd_items", "dkdv_items", "dq_items", "fwd_visited", "fwd_full",
+              "two_run_q_rows", "two_run_kv_rows", "fwd_capacity", "fwd_allowed", "full_disallowed",
+              "dkdv_allowed", "dq_allowed", "dkdv_visited", "dq_visited")
+
+
+def ring_plan_stats(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, G: int = 4, Hkv: int = 8, causal: bool = True,
+                    window: int = -1, sched: str = "fused", exact: bool = False) -> dict:
+    """Host-only counts of what the tensor-core passes visit (tiles, work
+    items, visited tile pairs, rows copied into rank order; with exact=True
+    also the allowed pairs inside the visited tile pairs of each pass)."""
+    cu = _host_i32(cu_seqlens)
+    out = np.zeros(len(PLAN_STATS), dtype=np.int64)
+    check(lib().ra_ring_plan_stats(_np_ptr(cu), len(cu) - 1, cp, mode, G, Hkv, int(causal), int(window),
+                                   _SCHED[sched], int(exact), _np_ptr(out)), "ra_ring_plan_stats")
+    return dict(zip(PLAN_STATS, (int(x) for x in out)))
 
 
 def _perm_dev(perm, device):

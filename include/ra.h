@@ -273,6 +273,35 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
 ra_status ra_ring_rank_pairs(const int32_t *cu_seqlens, int B, int cp, int zz_mode, int causal, int window,
                              int64_t *counts);
 
+/* ------------------------------------------------------------------------
+ * ra_ring_plan_stats  (HOST only; no GPU needed)
+ *
+ * What the tensor-core passes of ra_ring_attn_fwd / bwd visit for a packing
+ * (bf16, d = 128; G = Hq / Hkv a power of two dividing 128), found by
+ * walking every work item over its range of ring steps with the kernels'
+ * own step-to-rank rule and tile classifier (tile-level skipping of fully
+ * masked blocks, FlagScale PR #910).  stats HOST int64[RA_PLAN_STATS_N]:
+ *   [0] query tiles (128/G tokens x G heads)   [1] key tiles (128 keys)
+ *   [2] forward items  [3] dK/dV items  [4] dQ items (all KV heads)
+ *   [5] forward visited (query tile, key tile) pairs, one KV head
+ *   [6]   of which full (no mask inside)
+ *   [7] rows of two-run query tiles  [8] rows of two-run key tiles
+ *       (the rows the permutes copy into rank order)
+ *   [9] token-pair capacity of the forward's visited pairs
+ *       ([5] x 128/G x 128: the tensor work per head group / (2 d G))
+ *   exact != 0 (brute force over the visited pairs; else -1):
+ *   [10] allowed (query token, key) pairs inside the forward's visited pairs
+ *   [11] disallowed pairs among valid rows and keys of "full" pairs
+ *   [12] allowed pairs inside the dK/dV pass's visited pairs
+ *   [13] allowed pairs inside the dQ pass's visited pairs
+ *   [14] dK/dV visited pairs  [15] dQ visited pairs
+ * A correct plan covers each allowed pair once in every pass: [10], [12]
+ * and [13] equal the sum of ra_ring_rank_pairs, and [11] is 0.
+ * ------------------------------------------------------------------------ */
+#define RA_PLAN_STATS_N 16
+ra_status ra_ring_plan_stats(const int32_t *cu_seqlens, int B, int cp, int zz_mode, int G, int Hkv, int causal,
+                             int window, int sched, int exact, int64_t *stats);
+
 /* Reads and clears the device status word of the current device (waits for
  * `stream` first).  Returns RA_OK, RA_ERR_TIMEOUT or RA_ERR_DEVICE_BOUNDS. */
 ra_status ra_get_device_status(void *stream);
