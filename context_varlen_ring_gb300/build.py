@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libra.so")
-SOURCES = ["ra_api.cpp", "ra_plan.cpp", "ra_misc.cu", "ra_simt.cu", "ra_tc_fwd.cu", "ra_tc_bwd.cu", "ra_tc_dq.cu", "ra_noalloc.cu"]
+SOURCES = ["ra_api.cpp", "ra_plan.cpp", "ra_stats.cpp", "ra_misc.cu", "ra_simt.cu", "ra_tc_fwd.cu", "ra_tc_bwd.cu",
+           "ra_tc_dq.cu", "ra_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-I" + os.path.join(HERE, "..", "include")]

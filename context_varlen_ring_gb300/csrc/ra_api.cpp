@@ -406,101 +406,6 @@ ra_status ra_ring_rank_pairs(const int32_t *cu, int B, int cp, int mode, int cau
     return RA_OK;
 }
 
-// Walks each tensor-core pass's work items over their ring-step ranges the
-// way the kernels do (forward and dQ: rank r at step t reads the key tiles
-// of rank (r - t) mod cp; dK/dV: the key tile of rank s meets the query
-// tiles of rank (s + t) mod cp) and counts what they visit.
-ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, int Hkv, int causal, int window,
-                             int sched, int exact, int64_t *stats) {
-    if (!stats) return fail(RA_ERR_INVALID_ARG, "stats is NULL");
-    if (cp < 1 || cp > kMaxMergeParts) return fail(RA_ERR_INVALID_ARG, "cp must be in [1, 64]");
-    if (mode != RA_ZZ_GLOBAL && mode != RA_ZZ_PER_DOC) return fail(RA_ERR_INVALID_ARG, "unknown zigzag mode");
-    if (sched != RA_SCHED_FUSED && sched != RA_SCHED_STEPWISE && sched != RA_SCHED_ALLGATHER)
-        return fail(RA_ERR_INVALID_ARG, "unknown schedule");
-    if (G < 1 || G > kBM || (G & (G - 1)) || Hkv < 1) return fail(RA_ERR_INVALID_ARG, "bad head grouping");
-    ra_status st = validate_cu(cu, B, -1);
-    if (st) return st;
-    const int64_t T = cu[B];
-    if (window >= T) window = -1;
-    if (window < -1) window = -1;
-    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, true,
-                              sched == RA_SCHED_ALLGATHER, &st);
-    if (!plan) return st;
-    const TilePlan &tp = plan->tiles;
-    for (int i = 0; i < RA_PLAN_STATS_N; ++i) stats[i] = 0;
-    stats[0] = (int64_t)tp.qtiles.size();
-    stats[1] = (int64_t)tp.kvtiles.size();
-    stats[2] = (int64_t)tp.items.size();
-    stats[3] = (int64_t)tp.bitems.size();
-    stats[4] = (int64_t)tp.qitems.size();
-    const uint8_t *blob = plan->dev.blob.data();
-    for (int64_t i = 0; i < T; ++i) {
-        stats[7] += blob[plan->dev.o_qmask + i];
-        stats[8] += blob[plan->dev.o_kvmask + i];
-    }
-    auto pos_of = [](const Tile &t, int i) { return i < t.split ? (int64_t)t.pos0 + i : (int64_t)t.pos1 + (i - t.split); };
-    // allowed (query token, key) pairs of one tile pair; `bad` counts the
-    // disallowed ones among the valid rows and keys
-    auto count = [&](const Tile &q, const Tile &k, int64_t *bad) {
-        int64_t ok = 0;
-        for (int i = 0; i < q.len; ++i) {
-            const int64_t qp = pos_of(q, i);
-            for (int j = 0; j < k.len; ++j) {
-                const int64_t kp = pos_of(k, j);
-                const bool allowed = (!causal || kp <= qp) && (window < 0 || kp >= qp - window);
-                if (allowed)
-                    ++ok;
-                else if (bad)
-                    ++*bad;
-            }
-        }
-        return ok;
-    };
-    const int q_tokens = tp.q_tokens;
-    auto seg = [&](int r, int b) { return (size_t)r * (B + 1) + b; };
-    for (const WorkItem &w : tp.items) {
-        if (w.g != 0) continue;
-        for (int t = w.t0; t < w.t1; ++t) {
-            const int s = ((w.r - t) % cp + cp) % cp;
-            for (int j = tp.kv_off[seg(s, w.b)]; j < tp.kv_off[seg(s, w.b) + 1]; ++j) {
-                for (int qt : {w.qt0, w.qt1}) {
-                    if (qt < 0) continue;
-                    const int c = classify(tp.qtiles[qt], tp.kvtiles[j], causal, window);
-                    if (c == kSkip) continue;
-                    ++stats[5];
-                    stats[9] += (int64_t)q_tokens * kBN;
-                    if (c == kFull) ++stats[6];
-                    if (exact) stats[10] += count(tp.qtiles[qt], tp.kvtiles[j], c == kFull ? &stats[11] : nullptr);
-                }
-            }
-        }
-    }
-    for (const WorkItem &w : tp.bitems) {
-        if (w.g != 0) continue;
-        for (int t = w.t0; t < w.t1; ++t) {
-            const int r = (w.r + t) % cp;
-            for (int i = tp.q_off[seg(r, w.b)]; i < tp.q_off[seg(r, w.b) + 1]; ++i) {
-                if (classify(tp.qtiles[i], tp.kvtiles[w.qt0], causal, window) == kSkip) continue;
-                ++stats[14];
-                if (exact) stats[12] += count(tp.qtiles[i], tp.kvtiles[w.qt0], nullptr);
-            }
-        }
-    }
-    for (const WorkItem &w : tp.qitems) {
-        if (w.g != 0) continue;
-        for (int t = w.t0; t < w.t1; ++t) {
-            const int s = ((w.r - t) % cp + cp) % cp;
-            for (int j = tp.kv_off[seg(s, w.b)]; j < tp.kv_off[seg(s, w.b) + 1]; ++j) {
-                if (classify(tp.qtiles[w.qt0], tp.kvtiles[j], causal, window) == kSkip) continue;
-                ++stats[15];
-                if (exact) stats[13] += count(tp.qtiles[w.qt0], tp.kvtiles[j], nullptr);
-            }
-        }
-    }
-    if (!exact) stats[10] = stats[11] = stats[12] = stats[13] = -1;
-    return RA_OK;
-}
-
 ra_status ra_get_device_status(void *stream) {
     RA_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");
     int *p = device_status_ptr();
