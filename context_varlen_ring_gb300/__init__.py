@@ -83,18 +83,20 @@ def ring_rank_pairs(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool 
 
 PLAN_STATS = ("q_tiles", "kv_tiles", "fwd_items", "dkdv_items", "dq_items", "fwd_visited", "fwd_full",
               "two_run_q_rows", "two_run_kv_rows", "fwd_capacity", "fwd_allowed", "full_disallowed",
-              "dkdv_allowed", "dq_allowed", "dkdv_visited", "dq_visited")
+              "dkdv_allowed", "dq_allowed", "dkdv_visited", "dq_visited",
+              "fwd_makespan", "dkdv_makespan", "dq_makespan")
 
 
 def ring_plan_stats(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, G: int = 4, Hkv: int = 8, causal: bool = True,
-                    window: int = -1, sched: str = "fused", exact: bool = False) -> dict:
+                    window: int = -1, sched: str = "fused", exact: bool = False, n_sm: int = 152) -> dict:
     """Host-only counts of what the tensor-core passes visit (tiles, work
     items, visited tile pairs, rows copied into rank order; with exact=True
-    also the allowed pairs inside the visited tile pairs of each pass)."""
+    also the allowed pairs inside the visited tile pairs of each pass) and a
+    scheduling model of each pass over n_sm SMs (makespans in tile visits)."""
     cu = _host_i32(cu_seqlens)
     out = np.zeros(len(PLAN_STATS), dtype=np.int64)
     check(lib().ra_ring_plan_stats(_np_ptr(cu), len(cu) - 1, cp, mode, G, Hkv, int(causal), int(window),
-                                   _SCHED[sched], int(exact), _np_ptr(out)), "ra_ring_plan_stats")
+                                   _SCHED[sched], int(exact), int(n_sm), _np_ptr(out)), "ra_ring_plan_stats")
     return dict(zip(PLAN_STATS, (int(x) for x in out)))
 
 

@@ -66,7 +66,7 @@ def _declare(L):
         "ra_ring_attn_bwd": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, i32, i32, f32, i32,
                                    P, P, P, P, P, P, i32, i32, P, sz, P]),
         "ra_ring_rank_pairs": (i32, [P, i32, i32, i32, i32, i32, P]),
-        "ra_ring_plan_stats": (i32, [P, i32, i32, i32, i32, i32, i32, i32, i32, i32, P]),
+        "ra_ring_plan_stats": (i32, [P, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, P]),
         "ra_get_device_status": (i32, [P]),
         "ra_selftest_wait_timeout": (i32, [i64, P]),
         "ra_status_string": (ctypes.c_char_p, [i32]),

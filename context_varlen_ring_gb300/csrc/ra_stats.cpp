@@ -2,7 +2,11 @@
 // tensor-core passes visit for a packing, for the planner's coverage tests
 // and for reports.  Uses the planner and the tile classifier the drivers
 // and kernels use.
+#include <algorithm>
 #include <cstdint>
+#include <functional>
+#include <queue>
+#include <vector>
 
 #include "ra_internal.h"
 #include "ra_kernels.h"
@@ -16,8 +20,9 @@ extern "C" {
 // of rank (r - t) mod cp; dK/dV: the key tile of rank s meets the query
 // tiles of rank (s + t) mod cp) and counts what they visit.
 ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, int Hkv, int causal, int window,
-                             int sched, int exact, int64_t *stats) {
+                             int sched, int exact, int n_sm, int64_t *stats) {
     if (!stats) return fail(RA_ERR_INVALID_ARG, "stats is NULL");
+    if (n_sm < 1) return fail(RA_ERR_INVALID_ARG, "n_sm must be >= 1");
     if (cp < 1 || cp > kMaxMergeParts) return fail(RA_ERR_INVALID_ARG, "cp must be in [1, 64]");
     if (mode != RA_ZZ_GLOBAL && mode != RA_ZZ_PER_DOC) return fail(RA_ERR_INVALID_ARG, "unknown zigzag mode");
     if (sched != RA_SCHED_FUSED && sched != RA_SCHED_STEPWISE && sched != RA_SCHED_ALLGATHER)
@@ -63,8 +68,13 @@ ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, 
     };
     const int q_tokens = tp.q_tokens;
     auto seg = [&](int r, int b) { return (size_t)r * (B + 1) + b; };
+    // visited tile pairs of each item (its cost in the scheduling model);
+    // the coverage counts come from the items of KV head 0 (the others repeat
+    // them for their own head)
+    std::vector<int64_t> c_fwd, c_kv, c_q;
+    c_fwd.reserve(tp.items.size());
     for (const WorkItem &w : tp.items) {
-        if (w.g != 0) continue;
+        int64_t n = 0;
         for (int t = w.t0; t < w.t1; ++t) {
             const int s = ((w.r - t) % cp + cp) % cp;
             for (int j = tp.kv_off[seg(s, w.b)]; j < tp.kv_off[seg(s, w.b) + 1]; ++j) {
@@ -72,6 +82,8 @@ ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, 
                     if (qt < 0) continue;
                     const int c = classify(tp.qtiles[qt], tp.kvtiles[j], causal, window);
                     if (c == kSkip) continue;
+                    ++n;
+                    if (w.g != 0) continue;
                     ++stats[5];
                     stats[9] += (int64_t)q_tokens * kBN;
                     if (c == kFull) ++stats[6];
@@ -79,30 +91,64 @@ ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, 
                 }
             }
         }
+        c_fwd.push_back(n);
     }
+    c_kv.reserve(tp.bitems.size());
     for (const WorkItem &w : tp.bitems) {
-        if (w.g != 0) continue;
+        int64_t n = 0;
         for (int t = w.t0; t < w.t1; ++t) {
             const int r = (w.r + t) % cp;
             for (int i = tp.q_off[seg(r, w.b)]; i < tp.q_off[seg(r, w.b) + 1]; ++i) {
                 if (classify(tp.qtiles[i], tp.kvtiles[w.qt0], causal, window) == kSkip) continue;
+                ++n;
+                if (w.g != 0) continue;
                 ++stats[14];
                 if (exact) stats[12] += count(tp.qtiles[i], tp.kvtiles[w.qt0], nullptr);
             }
         }
+        c_kv.push_back(n);
     }
+    c_q.reserve(tp.qitems.size());
     for (const WorkItem &w : tp.qitems) {
-        if (w.g != 0) continue;
+        int64_t n = 0;
         for (int t = w.t0; t < w.t1; ++t) {
             const int s = ((w.r - t) % cp + cp) % cp;
             for (int j = tp.kv_off[seg(s, w.b)]; j < tp.kv_off[seg(s, w.b) + 1]; ++j) {
                 if (classify(tp.qtiles[w.qt0], tp.kvtiles[j], causal, window) == kSkip) continue;
+                ++n;
+                if (w.g != 0) continue;
                 ++stats[15];
                 if (exact) stats[13] += count(tp.qtiles[w.qt0], tp.kvtiles[j], nullptr);
             }
         }
+        c_q.push_back(n);
     }
     if (!exact) stats[10] = stats[11] = stats[12] = stats[13] = -1;
+    // Scheduling model, in tile visits: the forward's persistent CTAs claim
+    // items in list order from a counter, and the key-side grid (one CTA per
+    // item) is dispatched in block order as SMs free up -- both greedy list
+    // scheduling over n_sm workers; the dQ grid takes items with a static
+    // stride (CTA c runs items c, c + n_sm, ...).
+    auto greedy = [n_sm](const std::vector<int64_t> &cost) {
+        std::priority_queue<int64_t, std::vector<int64_t>, std::greater<int64_t>> free_at;
+        for (int i = 0; i < n_sm; ++i) free_at.push(0);
+        int64_t end = 0;
+        for (int64_t c : cost) {
+            const int64_t t = free_at.top() + c;
+            free_at.pop();
+            free_at.push(t);
+            end = std::max(end, t);
+        }
+        return end;
+    };
+    auto strided = [n_sm](const std::vector<int64_t> &cost) {
+        std::vector<int64_t> load((size_t)n_sm, 0);
+        for (size_t i = 0; i < cost.size(); ++i) load[i % (size_t)n_sm] += cost[i];
+        return load.empty() ? (int64_t)0 : *std::max_element(load.begin(), load.end());
+    };
+    stats[16] = greedy(c_fwd);
+    stats[17] = greedy(c_kv);
+    stats[18] = strided(c_q);
     return RA_OK;
 }
 

@@ -295,12 +295,17 @@ ra_status ra_ring_rank_pairs(const int32_t *cu_seqlens, int B, int cp, int zz_mo
  *   [12] allowed pairs inside the dK/dV pass's visited pairs
  *   [13] allowed pairs inside the dQ pass's visited pairs
  *   [14] dK/dV visited pairs  [15] dQ visited pairs
+ *   scheduling model over n_sm SMs, in tile-pair visits per SM (all KV
+ *   heads; the ideal is the pass's total visits / n_sm):
+ *   [16] forward (persistent CTAs claiming items in order)
+ *   [17] dK/dV (one CTA per item, dispatched in order as SMs free up)
+ *   [18] dQ (persistent CTAs, static stride over the items)
  * A correct plan covers each allowed pair once in every pass: [10], [12]
  * and [13] equal the sum of ra_ring_rank_pairs, and [11] is 0.
  * ------------------------------------------------------------------------ */
-#define RA_PLAN_STATS_N 16
+#define RA_PLAN_STATS_N 19
 ra_status ra_ring_plan_stats(const int32_t *cu_seqlens, int B, int cp, int zz_mode, int G, int Hkv, int causal,
-                             int window, int sched, int exact, int64_t *stats);
+                             int window, int sched, int exact, int n_sm, int64_t *stats);
 
 /* Reads and clears the device status word of the current device (waits for
  * `stream` first).  Returns RA_OK, RA_ERR_TIMEOUT or RA_ERR_DEVICE_BOUNDS. */

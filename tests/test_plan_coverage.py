@@ -67,16 +67,35 @@ def test_packed_workload_tiling(ra, orc):
     assert ref / ag["fwd_capacity"] > 0.9 > ref / ring["fwd_capacity"] > 0.75
 
 
+def test_scheduling_model_bounds(ra):
+    """The scheduling model: on one SM every pass takes its whole work (all
+    KV heads' visits); on many it takes at least the even share and at most
+    the whole."""
+    rng = np.random.default_rng(5)
+    for _ in range(4):
+        cu = W.cu_seqlens(W.random_doc_lens(rng, int(rng.integers(500, 3000)), 1, 900))
+        for sched in ("fused", "allgather"):
+            one = ra.ring_plan_stats(cu, 4, 1, 4, 2, True, -1, sched, n_sm=1)
+            assert one["fwd_makespan"] == 2 * one["fwd_visited"]
+            assert one["dkdv_makespan"] == 2 * one["dkdv_visited"]
+            assert one["dq_makespan"] == 2 * one["dq_visited"]
+            many = ra.ring_plan_stats(cu, 4, 1, 4, 2, True, -1, sched, n_sm=7)
+            for k, tot in (("fwd_makespan", 2 * many["fwd_visited"]), ("dkdv_makespan", 2 * many["dkdv_visited"]),
+                           ("dq_makespan", 2 * many["dq_visited"])):
+                assert -(-tot // 7) <= many[k] <= tot
+
+
 def test_plan_stats_argument_checks(ra):
     import ctypes
     from context_varlen_ring_gb300 import _lib
     L = _lib.lib()
     cu = np.array([0, 100], np.int32)
-    out = np.zeros(16, np.int64)
+    out = np.zeros(19, np.int64)
     p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
-    assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 7, 0, p(out)) == _lib.RA_ERR_INVALID_ARG  # schedule
-    assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 3, 2, 1, -1, 0, 0, p(out)) == _lib.RA_ERR_INVALID_ARG  # G
-    assert L.ra_ring_plan_stats(p(cu), 1, 0, 0, 4, 2, 1, -1, 0, 0, p(out)) == _lib.RA_ERR_INVALID_ARG  # cp
-    assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 0, 0, None) == _lib.RA_ERR_INVALID_ARG
-    assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 0, 0, p(out)) == 0
+    assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 7, 0, 152, p(out)) == _lib.RA_ERR_INVALID_ARG  # schedule
+    assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 3, 2, 1, -1, 0, 0, 152, p(out)) == _lib.RA_ERR_INVALID_ARG  # G
+    assert L.ra_ring_plan_stats(p(cu), 1, 0, 0, 4, 2, 1, -1, 0, 0, 152, p(out)) == _lib.RA_ERR_INVALID_ARG  # cp
+    assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 0, 0, 152, None) == _lib.RA_ERR_INVALID_ARG
+    assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 0, 0, 0, p(out)) == _lib.RA_ERR_INVALID_ARG  # n_sm
+    assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 0, 0, 152, p(out)) == 0
     assert out[10] == -1 and out[0] > 0
