@@ -105,6 +105,14 @@ def test_invalid_arguments_return_status(ra):
     rc = L.ra_ring_attn_fwd(fake, fake, fake, _lib.RA_BF16, 8, 4, 2, 128, _p(cu), 1, 2, 0, 1, -1, 0.1, 0, fake, fake,
                             ws, 16, None)
     assert rc == _lib.RA_ERR_WORKSPACE
+    # the all-gather schedule is accepted by both ring calls (the check that
+    # stops them here is the workspace size, after the plan is built)
+    rc = L.ra_ring_attn_fwd(fake, fake, fake, _lib.RA_BF16, 8, 4, 2, 128, _p(cu), 1, 2, 0, 1, -1, 0.1,
+                            _lib.RA_SCHED_ALLGATHER, fake, fake, ws, 16, None)
+    assert rc == _lib.RA_ERR_WORKSPACE
+    rc = L.ra_ring_attn_bwd(fake, fake, fake, _lib.RA_BF16, 8, 4, 2, 128, _p(cu), 1, 2, 0, 1, -1, 0.1,
+                            _lib.RA_SCHED_ALLGATHER, fake, fake, fake, fake, fake, fake, _lib.RA_BF16, 0, ws, 16, None)
+    assert rc == _lib.RA_ERR_WORKSPACE
     # merge argument checks
     assert L.ra_lse_merge(0, None, None, 4, 2, 128, fake, 0, fake, None) == _lib.RA_ERR_INVALID_ARG
     assert L.ra_lse_merge(65, None, None, 4, 2, 128, fake, 0, fake, None) == _lib.RA_ERR_INVALID_ARG
