@@ -66,3 +66,31 @@ def test_balance_study_lines():
     c2 = [x for x in lines if x["docs_seed"] == 0 and x["doc_order"] == "drawn" and x["window"] == -1][0]
     assert c2["per_doc_zigzag"] < 1.002
     assert c2["contiguous"] > 1.5 and c2["stream_zigzag"] > 1.5
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """bench.py --impl reference (host only): times the fp64 oracle on a
+    sample of the packed workload and prints one JSON line with the keys the
+    harness reads; here the sample is cut to the smallest document so the
+    test stays short."""
+    import argparse
+    import json
+    monkeypatch.setattr(bench, "cpu_sample_docs", lambda lens: [min(range(len(lens)), key=lambda i: lens[i])])
+    monkeypatch.delenv("RANK", raising=False)
+    bench.reference_arm(argparse.Namespace(gpus=1, steps=1, warmup=3))
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    assert line["metric"] == bench.METRIC and line["value"] > 0 and line["ms_per_step"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert "1 of the 15 documents" in line["cpu_baseline"]["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["dtype"] == "f64" and line["data"] == "synthetic"
+
+
+def test_reference_arm_other_ranks_print_nothing(monkeypatch, capsys):
+    import argparse
+    monkeypatch.setenv("RANK", "1")
+    bench.reference_arm(argparse.Namespace(gpus=2, steps=1, warmup=3))
+    assert capsys.readouterr().out == ""
