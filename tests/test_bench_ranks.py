@@ -94,3 +94,25 @@ def test_reference_arm_other_ranks_print_nothing(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     bench.reference_arm(argparse.Namespace(gpus=2, steps=1, warmup=3))
     assert capsys.readouterr().out == ""
+
+
+def test_flop_count_matches_oracle_pairs(orc):
+    """The allowed-pair count behind every reported TFLOP/s equals the
+    oracle's per-rank counts summed over ranks (any CP size, both zigzag
+    modes, with and without a window), and gives the per-launch FLOPs the
+    roofline uses on the packed 32768-token workload."""
+    import numpy as np
+
+    import workloads as W
+    rng = np.random.default_rng(17)
+    for _ in range(6):
+        cu = W.cu_seqlens(W.random_doc_lens(rng, int(rng.integers(100, 4000)), 1, 1500))
+        for w in (-1, 0, 1, 33, 700, 10**6):
+            ref = int(orc.rank_pairs(cu, int(rng.integers(1, 9)), int(rng.integers(0, 2)), True, window=w).sum())
+            assert bench.pairs_of(cu, w) == ref
+    cu = W.C4.cu_seqlens()
+    assert bench.pairs_of(cu) == 67823768
+    d, hq = 128, 32
+    assert 2 * d * hq * bench.PRODUCTS["ra_tc_fwd"] * 67823768 == pytest.approx(1.111e12, rel=1e-3)
+    assert 2 * d * hq * bench.PRODUCTS["ra_tc_bwd"] * 67823768 == pytest.approx(3.889e12, rel=1e-3)
+    assert bench.PRODUCTS["ra_tc_bwd"] == bench.PRODUCTS["ra_tc_bwd_dkdv"] + bench.PRODUCTS["ra_tc_bwd_dq"]
