@@ -113,29 +113,28 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def cpu_sample_docs(lens):
+def cpu_sample_docs(lens, pair_budget=15_000_000):
     """A bounded sample of the workload for the CPU oracle: the smaller
-    documents up to ~15M causal pairs (about 10-30 s of fp64 work)."""
+    documents up to `pair_budget` causal pairs (15M: about 10-30 s of fp64
+    fwd+bwd work on 16 cores)."""
     order = sorted(range(len(lens)), key=lambda i: lens[i])
     pick, pairs = [], 0
     for i in order:
         p = lens[i] * (lens[i] + 1) // 2
-        if pairs + p > 15_000_000 and pick:
+        if pairs + p > pair_budget and pick:
             break
         pick.append(i)
         pairs += p
     return sorted(pick)
 
 
-def run_cpu_oracle(wl, steps=1, window=-1):
+def run_cpu_oracle(wl, steps=1, window=-1, pair_budget=15_000_000, threads=None):
     """fwd+bwd of the sampled documents with the fp64 oracle; returns
-    (TFLOP/s, seconds per step, cores, sample description)."""
-    import torch
-
+    (TFLOP/s, seconds per step, cores, sample description, sample pairs)."""
     import oracle
     oracle.build()
-    cores = oracle.set_threads(os.cpu_count() or 1)
-    pick = cpu_sample_docs(list(wl.doc_lens))
+    cores = oracle.set_threads(threads or os.cpu_count() or 1)
+    pick = cpu_sample_docs(list(wl.doc_lens), pair_budget)
     lens = [wl.doc_lens[i] for i in pick]
     cu = W.cu_seqlens(lens)
     T = int(cu[-1])
@@ -148,10 +147,13 @@ def run_cpu_oracle(wl, steps=1, window=-1):
         oracle.attn_bwd(q, k, v, o, l, do, cu, True, wl.scale, window=window)
         times.append(time.perf_counter() - t0)
     sec = statistics.median(times)
-    flops = 14 * wl.d * wl.hq * pairs_of(cu, window)
+    if threads:
+        oracle.set_threads(os.cpu_count() or 1)
+    sp = pairs_of(cu, window)
+    flops = 14 * wl.d * wl.hq * sp
     sample = (f"fp64 fwd+bwd of {len(lens)} of the {wl.B} documents ({T} of {wl.T} tokens, "
-              f"{pairs_of(cu, window)} of {pairs_of(wl.cu_seqlens(), window)} allowed pairs), all {wl.hq} heads")
-    return flops / sec / 1e12, sec, cores, sample
+              f"{sp} of {pairs_of(wl.cu_seqlens(), window)} allowed pairs), all {wl.hq} heads")
+    return flops / sec / 1e12, sec, cores, sample, sp
 
 
 def reference_arm(args):
@@ -161,7 +163,11 @@ def reference_arm(args):
     wl = W.C4
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state; warm-up steps are not repeated
-    tf, sec, cores, sample = run_cpu_oracle(wl, steps=max(1, args.steps))
+    # each step a bounded sample sized so that the whole run ends within a
+    # few minutes: about 120 s of fp64 work over the K steps (15M pairs take
+    # about 18 s on 16 host cores)
+    budget = int(min(15_000_000, max(1_000_000, 15_000_000 * 120 / (18 * max(1, args.steps)))))
+    tf, sec, cores, sample, _ = run_cpu_oracle(wl, steps=max(1, args.steps), pair_budget=budget)
     line = {"impl": "reference", "metric": METRIC, "value": tf, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -190,16 +196,16 @@ def job_tflops(world, flops_per_step, steps, max_ms):
     return world * flops_per_step * steps / (max_ms / 1e3) / 1e12
 
 
-# Algorithmic work of what each timed scope computes, per launch (fused
-# schedule: one launch covers all ring steps), in products of 2*d FLOPs per
-# (query head, allowed pair).  ra_tc_bwd is the fused backward: the key-side
-# kernel (S^T, dP^T, dV, dK) and the query-side kernel (S, dP, dQ) running
-# concurrently on two streams under one timing scope.
-PRODUCTS = {"ra_tc_fwd": 2, "ra_simt_fwd": 2,     # S, PV
-            "ra_tc_bwd": 7,                       # both backward kernels
-            "ra_tc_bwd_dkdv": 4,                  # S^T, dP^T, dV, dK
-            "ra_tc_bwd_dq": 3,                    # S, dP, dQ
-            "ra_simt_bwd": 5}
+# Work of each timed scope per launch (fused schedule: one launch covers all
+# ring steps), in products of 2*d FLOPs per (query head, allowed pair).
+# ALGORITHMIC counts what the method needs: the forward's S and PV, the
+# backward's recomputed S, dV, dP, dK and dQ (10*d*Hq per pair).  EXECUTED
+# counts what the kernels form: the backward runs as two concurrent passes
+# (key side: S^T, dP^T, dV, dK; query side: S, dP, dQ), so S and dP are
+# formed twice; the difference is implementation overhead and is reported
+# beside the roofline, never in it.
+ALGORITHMIC_PRODUCTS = {"ra_tc_fwd": 2, "ra_simt_fwd": 2, "ra_tc_bwd": 5, "ra_simt_bwd": 5}
+EXECUTED_PRODUCTS = {"ra_tc_fwd": 2, "ra_tc_bwd": 7, "ra_tc_bwd_dkdv": 4, "ra_tc_bwd_dq": 3}
 KERNELS_PER_SCOPE = {"ra_tc_bwd": 2}
 
 
@@ -226,6 +232,259 @@ def kernel_traffic(name):
         except OSError:
             return None
     return ent["dram_bytes_per_launch"]
+
+
+def tensor_roofline(name, ms_per_launch, d, hq, pairs, peak, peak_src):
+    """Roofline entry of a tensor-core scope: the method's algorithmic FLOPs
+    per launch over the launch's CUDA-event time, against the burst bf16
+    peak (the scopes are timed inside a loop well under a second long).
+    The FLOPs the kernels execute (the backward forms S and dP twice) are
+    reported beside it as executed_*."""
+    sec = ms_per_launch / 1e3
+    n_alg = ALGORITHMIC_PRODUCTS.get(name)
+    if n_alg is None:
+        return {"kernel": name, "bound": "hbm", "achieved": None, "peak": None, "unit": "GB/s", "frac": None,
+                "traffic": kernel_traffic(name)}
+    flops = n_alg * 2 * d * hq * pairs
+    ach = flops / sec / 1e12
+    n_exe = EXECUTED_PRODUCTS.get(name, n_alg)
+    exe = n_exe * 2 * d * hq * pairs / sec / 1e12
+    return {"kernel": name, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+            "frac": ach / peak, "traffic": kernel_traffic(name),
+            "peak_kind": f"{peak_src} dense bf16 burst (the scope is timed inside a loop of well under a second)",
+            "ms_per_launch": ms_per_launch,
+            "algorithmic_per_launch": flops, "algorithmic_unit": "FLOP",
+            "algorithmic_rule": f"{n_alg} products x 2*d FLOPs per (query head, allowed pair)",
+            "executed_tflops": exe, "executed_frac": exe / peak,
+            "executed_rule": f"{n_exe} products formed by the kernels"}
+
+
+def time_calls(fn, steps, warmup, stream, torch):
+    """Milliseconds per call of fn(): `warmup` untimed calls, then `steps`
+    calls between two CUDA events on the launching stream."""
+    for _ in range(max(warmup, 3)):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def bandwidth_kernels(ra, torch, dev, wl, steps, warmup, hbm):
+    """The HBM-bound kernels of the path at full size on the packed
+    32768-token workload, each as algorithmic bytes (every byte the
+    operation must read and write once) over its CUDA-event time:
+      permute   ra_zigzag_permute of Q, K and V into rank order (3 calls a rep)
+      unpermute ra_zigzag_unpermute of O back to original order
+      merge     ra_lse_merge of cp fp32 partials [T, Hq, d] (+ LSEs), bf16 out
+    Each rep moves more than the 129 MB L2 (merge: 4.6 GB, permute 805 MB,
+    unpermute 537 MB), so no flush is needed between reps."""
+    L = ra.lib()
+    cu = wl.cu_seqlens()
+    T, hq, hkv, d = wl.T, wl.hq, wl.hkv, wl.d
+    perm_h, _, _ = ra.zigzag_plan(cu, wl.cp, wl.zz_mode)
+    perm = torch.from_numpy(perm_h.astype(np.int32)).to(dev)
+    q, k, v = (x.to(dev) for x in W.make_qkv(T, hq, hkv, d, wl.dtype))
+    yq, yk, yv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    rb = lambda t: t[0].numel() * t.element_size()
+
+    def permute3():
+        for x, y in ((q, yq), (k, yk), (v, yv)):
+            assert L.ra_zigzag_permute(P(x), P(y), P(perm), T, rb(x), sp) == 0
+
+    def unpermute_o():
+        assert L.ra_zigzag_unpermute(P(yq), P(q), P(perm), T, rb(yq), sp) == 0
+
+    res = {}
+    ms = time_calls(permute3, steps, warmup, stream, torch)
+    nb = 2 * sum(x.numel() * x.element_size() for x in (q, k, v))
+    res["permute_qkv"] = {"ms": ms, "bytes": nb, "gbs": nb / ms / 1e6, "frac": nb / ms / 1e6 / hbm}
+    ms = time_calls(unpermute_o, steps, warmup, stream, torch)
+    nb = 2 * q.numel() * q.element_size()
+    res["unpermute_o"] = {"ms": ms, "bytes": nb, "gbs": nb / ms / 1e6, "frac": nb / ms / 1e6 / hbm}
+    del yk, yv
+    n = wl.cp
+    g = torch.Generator(device=dev).manual_seed(5)
+    parts = [torch.randn((T, hq, d), generator=g, device=dev, dtype=torch.float32) for _ in range(n)]
+    lses = [torch.randn((hq, T), generator=g, device=dev, dtype=torch.float32) * 3 for _ in range(n)]
+    po = (ctypes.c_void_p * n)(*[x.data_ptr() for x in parts])
+    pl = (ctypes.c_void_p * n)(*[x.data_ptr() for x in lses])
+    mo = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+    ml = torch.empty((hq, T), dtype=torch.float32, device=dev)
+
+    def merge():
+        assert L.ra_lse_merge(n, po, pl, T, hq, d, P(mo), 0, P(ml), sp) == 0
+
+    ms = time_calls(merge, steps, warmup, stream, torch)
+    nb = sum(x.numel() * 4 for x in parts + lses) + mo.numel() * 2 + ml.numel() * 4
+    res["lse_merge"] = {"ms": ms, "bytes": nb, "gbs": nb / ms / 1e6, "frac": nb / ms / 1e6 / hbm, "parts": n,
+                        "note": "every partial finite (all parts read)"}
+    assert ra.device_status() == 0
+    del parts, lses, mo, ml, q, k, v, yq
+    torch.cuda.empty_cache()
+    return {"peak_gbs": hbm, "rule": "algorithmic bytes (read once + written once) / CUDA-event time", **res}
+
+
+def fwd_lines(ra, torch, dev, names, steps, warmup, peak, sched="fused"):
+    """Forward-only calls of the named workloads (whole call: table upload,
+    permute of two-run tile rows, fused forward): ms and TFLOP/s."""
+    out = {}
+    for name in names:
+        wl = W.ALL[name]
+        cu = wl.cu_seqlens()
+        T, hq, hkv, d = wl.T, wl.hq, wl.hkv, wl.d
+        pairs = pairs_of(cu)
+        q, k, v = (x.to(dev) for x in W.make_qkv(T, hq, hkv, d, wl.dtype))
+        o = torch.empty_like(q)
+        lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
+        ws = torch.empty(ra.ring_workspace_bytes(T, hq, hkv, d, 0, cu, wl.cp, wl.zz_mode, sched, bwd=False),
+                         dtype=torch.uint8, device=dev)
+        f = lambda: ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, sched, out=o, lse=lse,
+                                     workspace=ws)
+        ms = time_calls(f, steps, warmup, torch.cuda.current_stream(dev), torch)
+        assert ra.device_status() == 0
+        tf = 4 * d * hq * pairs / (ms / 1e3) / 1e12
+        out[name] = {"ms": ms, "tflops": tf, "frac_of_peak": tf / peak, "allowed_pairs_per_head": pairs,
+                     "T": T, "Hq": hq, "Hkv": hkv, "cp": wl.cp, "sched": sched}
+        del q, k, v, o, lse, ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def _numa_node_of(addr):
+    """NUMA node holding the pages of the mapping that contains `addr`
+    (from /proc/self/maps and /proc/self/numa_maps), or None."""
+    try:
+        start = None
+        for line in open("/proc/self/maps"):
+            a, b = line.split()[0].split("-")
+            if int(a, 16) <= addr < int(b, 16):
+                start = a.lstrip("0") or "0"
+                break
+        if start is None:
+            return None
+        for line in open("/proc/self/numa_maps"):
+            f = line.split()
+            if f and (f[0].lstrip("0") or "0") == start:
+                nodes = {int(x[1:x.index("=")]): int(x[x.index("=") + 1:]) for x in f if x.startswith("N")}
+                return max(nodes, key=nodes.get) if nodes else None
+    except (OSError, ValueError):
+        return None
+    return None
+
+
+def host_copy_rates(torch, dev, tensors_in, tensors_out, stream):
+    """Standalone page-locked copies of one step's inputs (host to device)
+    and results (device to host), alone and both directions at once, in
+    GB/s, with where the page-locked buffers and the GPU sit."""
+    h_in = [x.cpu().pin_memory() for x in tensors_in]
+    d_in = [torch.empty_like(x) for x in tensors_in]
+    h_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in tensors_out]
+    nin = sum(x.numel() * x.element_size() for x in h_in)
+    nout = sum(x.numel() * x.element_size() for x in h_out)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn, reps=5):
+        best = None
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            best = dt if best is None else min(best, dt)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            for a, b in zip(d_in, h_in):
+                a.copy_(b, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            for a, b in zip(h_out, tensors_out):
+                a.copy_(b, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_in, t_out, t_both = timed(h2d), timed(d2h), timed(both)
+    info = {"h2d_gbs": nin / t_in / 1e9, "d2h_gbs": nout / t_out / 1e9,
+            "concurrent_gbs_each_way": {"h2d": nin / t_both / 1e9, "d2h": nout / t_both / 1e9},
+            "bytes_each_way": [nin, nout], "rule": "best of 5 wall-clock runs of one step's copies"}
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = f"{props.pci_domain_id:04x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+        info["gpu_pci"] = bus
+        info["gpu_numa_node"] = int(open(f"/sys/bus/pci/devices/{bus}/numa_node").read().strip())
+    except Exception:
+        pass
+    info["pinned_numa_node"] = _numa_node_of(h_in[0].data_ptr())
+    try:
+        cpus = sorted(os.sched_getaffinity(0))
+        info["process_cpus"] = f"{cpus[0]}-{cpus[-1]} ({len(cpus)})" if cpus else None
+    except Exception:
+        pass
+    del h_in, d_in, h_out
+    return info
+
+
+
+def stepwise_lines(ra, torch, dev, wl, steps, warmup, peak, q, k, v, do):
+    """The literal per-step structure (one partial launch per ring step into
+    fp32 partials, the LSE merge, the unpermutes; backward per step with
+    fp32 dK/dV accumulated in global memory) on the same data as the fused
+    step: whole-step and forward times and the per-kernel split."""
+    sched = "stepwise"
+    cu = wl.cu_seqlens()
+    T, hq, hkv, d = wl.T, wl.hq, wl.hkv, wl.d
+    pairs = pairs_of(cu)
+    nb = max(ra.ring_workspace_bytes(T, hq, hkv, d, 0, cu, wl.cp, wl.zz_mode, sched, bwd=b) for b in (False, True))
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out, lse = torch.empty_like(q), torch.empty((hq, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def fwd():
+        ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, sched, out=out, lse=lse, workspace=ws)
+
+    def step():
+        fwd()
+        ra.ring_attn_bwd(q, k, v, out, lse, do, cu, wl.cp, wl.zz_mode, True, wl.scale, sched, dq=dq, dk=dk, dv=dv,
+                         workspace=ws, reuse_fwd_workspace=True)
+
+    stream = torch.cuda.current_stream(dev)
+    ms_step = time_calls(step, steps, warmup, stream, torch)
+    ms_fwd = time_calls(fwd, steps, warmup, stream, torch)
+    L = ra.lib()
+    L.ra_profile_enable(1)
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    names = ctypes.create_string_buffer(64 * 32)
+    kms = (ctypes.c_double * 32)()
+    kn = (ctypes.c_int64 * 32)()
+    nk = L.ra_profile_read(32, names, kms, kn)
+    L.ra_profile_enable(0)
+    per = {}
+    for i in range(max(nk, 0)):
+        nm = names.raw[64 * i:64 * i + 64].split(b"\0")[0].decode()
+        per[nm] = {"ms_per_step": kms[i] / steps, "launches_per_step": int(kn[i]) // steps}
+    assert ra.device_status() == 0
+    del ws, out, lse, dq, dk, dv
+    torch.cuda.empty_cache()
+    tf = 14 * d * hq * pairs / (ms_step / 1e3) / 1e12
+    tff = 4 * d * hq * pairs / (ms_fwd / 1e3) / 1e12
+    return {"ms_per_step": ms_step, "tflops": tf, "frac_of_peak": tf / peak,
+            "fwd": {"ms": ms_fwd, "tflops": tff, "frac_of_peak": tff / peak}, "kernels_per_step": per}
+
 
 
 def fwd_configs(args, ra, torch):
@@ -452,28 +711,21 @@ def main():
     dominant = max(kernels, key=lambda n: kernels[n]["ms_total"]) if kernels else None
     roof = None
     if dominant:
-        per_launch_s = kernels[dominant]["ms_per_launch"] / 1e3
-        # algorithmic work of what each kernel computes, per launch (fused schedule:
-        # one launch covers all ring steps): 2*d FLOPs per (query head, allowed pair)
-        # for each product it forms
-        n_prod = PRODUCTS.get(dominant)
-        if n_prod is not None:
-            flops = n_prod * 2 * d * hq * pairs
-            ach = flops / per_launch_s / 1e12
-            roof = {"kernel": dominant, "bound": "tensor", "achieved": ach, "peak": peak_sust, "unit": "TFLOP/s",
-                    "frac": ach / peak_sust, "traffic": kernel_traffic(dominant),
-                    "peak_kind": f"{peak_src} bf16 sustained (kernel timed inside a multi-step loop)",
-                    "algorithmic_per_launch": flops, "algorithmic_unit": "FLOP",
-                    "algorithmic_rule": f"{n_prod} products x 2*d FLOPs per (query head, allowed pair)"}
-        else:
-            roof = {"kernel": dominant, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s",
-                    "frac": None, "traffic": kernel_traffic(dominant)}
+        roof = tensor_roofline(dominant, kernels[dominant]["ms_per_launch"], d, hq, pairs, peak_burst, peak_src)
     all_roof = {}
     for nm, x in kernels.items():
-        n_prod = PRODUCTS.get(nm)
-        if n_prod and nm.startswith("ra_tc"):
-            tf = n_prod * 2 * d * hq * pairs / (x["ms_per_launch"] / 1e3) / 1e12
-            all_roof[nm] = {"tflops": tf, "frac_of_sustained": tf / peak_sust}
+        if nm in ALGORITHMIC_PRODUCTS:
+            r = tensor_roofline(nm, x["ms_per_launch"], d, hq, pairs, peak_burst, peak_src)
+            all_roof[nm] = {k_: r[k_] for k_ in ("achieved", "frac", "executed_tflops", "executed_frac")}
+
+    extras = {}
+    if not args.probe and args.sched == "fused" and args.window < 0:
+        # the other forward workloads, the per-step schedule on the same data,
+        # and the bandwidth-bound kernels at full size
+        extras["fwd_configs"] = fwd_lines(ra, torch, dev, ["C1", "C3"], args.steps, args.warmup, peak_burst)
+        extras["stepwise"] = stepwise_lines(ra, torch, dev, wl, args.steps, args.warmup, peak_burst, q, k, v, do)
+        extras["bandwidth_kernels"] = bandwidth_kernels(ra, torch, dev, wl, args.steps, args.warmup, hbm)
+        barrier()
 
     # ---- end to end through the public API with host buffers.  Every step
     # copies its inputs (Q, K, V, dO) in from pinned host memory and its
@@ -550,6 +802,7 @@ def main():
     e2e_match = all(torch.equal(h, x.cpu()) for h, x in zip(last, (out, dq, dk, dv)))
     e2e_value = job_tflops(world, step_flops, args.steps, e2e_ms)
     assert ra.device_status() == 0
+    copy_rates = host_copy_rates(torch, dev, (q, k, v, do), (out, dq, dk, dv), stream)
 
     if rank != 0:
         if world > 1:
@@ -558,9 +811,16 @@ def main():
 
     cpu = None
     if world == 1 and not args.no_cpu:
-        tf, sec, cores, sample = run_cpu_oracle(wl, steps=1, window=args.window)
+        tf, sec, cores, sample, sp = run_cpu_oracle(wl, steps=1, window=args.window)
+        tf1, sec1, _, sample1, sp1 = run_cpu_oracle(wl, steps=1, window=args.window, pair_budget=1_000_000,
+                                                     threads=1)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample,
-               "sec_per_sample": sec}
+               "sec_per_sample": sec,
+               "full_workload_s_extrapolated": sec * pairs / sp,
+               "extrapolation": "sample seconds x (allowed pairs of the whole workload / of the sample); labelled "
+                                "extrapolated, not run",
+               "one_core": {"value": tf1, "unit": "TFLOP/s", "cores": 1, "sample": sample1, "sec_per_sample": sec1,
+                            "full_workload_s_extrapolated": sec1 * pairs / sp1}}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -588,9 +848,11 @@ def main():
                 "overlap": "step i+1's input copies and step i-1's result copies run on two copy streams beside "
                            "step i's compute (double-buffered device inputs and results); each step is one CUDA "
                            "graph of the public calls; every step's copies are inside the timed region",
-                "results_match_device_run": e2e_match},
+                "results_match_device_run": e2e_match,
+                "host_copies": copy_rates},
         "cpu_baseline": cpu,
         "clocks": clk,
+        **extras,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -36,7 +36,7 @@ EXPORTS = (
     "ra_ring_workspace_bytes", "ra_ring_attn_fwd", "ra_ring_attn_bwd",
     "ra_ring_rank_pairs", "ra_get_device_status", "ra_selftest_wait_timeout",
     "ra_status_string", "ra_last_error", "ra_version", "ra_profile_enable", "ra_profile_read",
-    "ra_varlen_attn_partial_noalloc", "ra_ring_plan_stats",
+    "ra_varlen_attn_partial_noalloc", "ra_ring_plan_stats", "ra_partial_table_bytes",
 )
 
 _lib = None
@@ -55,6 +55,7 @@ def _declare(L):
         "ra_zigzag_permute": (i32, [P, P, P, i64, i64, P]),
         "ra_zigzag_unpermute": (i32, [P, P, P, i64, i64, P]),
         "ra_partial_workspace_bytes": (sz, [i64, i64, i32, i32, i32, i32, i32]),
+        "ra_partial_table_bytes": (sz, [i64, i64, i32, i32, i32, i32, P, P, i32, P, P, i32, i32]),
         "ra_varlen_attn_partial": (i32, [P, P, P, i32, i64, i64, i32, i32, i32, P, P, i32, P, P, i32, i32, f32,
                                          P, P, P, sz, P]),
         "ra_varlen_attn_partial_noalloc": (i32, [P, P, P, i32, i64, i64, i32, i32, i32, P, P, i32, P, P, i32,

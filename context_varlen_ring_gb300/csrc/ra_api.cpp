@@ -452,16 +452,39 @@ size_t ra_partial_workspace_bytes(int64_t Tq, int64_t Tk, int nseg, int Hq, int 
     (void)d;
     (void)dtype;
     if (Tq < 0 || Tk < 0 || nseg < 1 || Hkv <= 0 || Hq <= 0) return 0;
-    // Upper bound over any positions: every tile holds at least one row.
+    // Upper bound over any positions (a tile holds at least one row, so there
+    // are at most Tq query tiles and Tk KV tiles) of the tables a call
+    // uploads: query and KV tile records, their per-segment offsets, the
+    // forward items (two query tiles of one segment per item and KV head)
+    // and the work counter; the SIMT path's position and offset arrays are
+    // added on top.
     const size_t qt = (size_t)Tq + nseg, kt = (size_t)Tk + nseg;
     size_t s = 0;
     s += align_up(qt * sizeof(Tile), 256) + align_up(kt * sizeof(Tile), 256);
     s += 2 * align_up(((size_t)nseg + 2) * 4, 256);
     s += align_up(((qt + 1) / 2 + nseg) * (size_t)Hkv * sizeof(WorkItem), 256);
-    s += align_up(((size_t)kt) * (size_t)Hkv * sizeof(WorkItem), 256);
     // SIMT path: positions and offsets
     s += align_up((size_t)Tq * 4, 256) + align_up((size_t)Tk * 4, 256) + 4 * align_up(((size_t)nseg + 2) * 4, 256);
     return s + 4096;
+}
+
+size_t ra_partial_table_bytes(int64_t Tq, int64_t Tk, int Hq, int Hkv, int d, int dtype, const int32_t *cu_q,
+                              const int32_t *cu_k, int nseg, const int32_t *q_pos, const int32_t *k_pos, int causal,
+                              int window) {
+    if (check_common(dtype, Hq, Hkv, d) || Tq < 0 || Tk < 0 || Tq > INT32_MAX || Tk > INT32_MAX || nseg < 1)
+        return 0;
+    if (validate_cu(cu_q, nseg, Tq) || validate_cu(cu_k, nseg, Tk)) return 0;
+    if (tc_fwd_supported(dtype, d, Hq, Hkv)) {
+        TilePlan tp;
+        if (build_partial_tiles(cu_q, cu_k, nseg, q_pos, k_pos, Tq, Tk, Hq / Hkv, Hkv, causal, window, tp)) return 0;
+        tp.bitems.clear();
+        tp.qitems.clear();
+        DeviceTables dt;
+        pack_tables(nullptr, &tp, dt);
+        return dt.blob.size();
+    }
+    auto a64 = [](size_t n) { return align_up(n, 64); };
+    return 4 * (a64((size_t)Tq) + a64((size_t)Tk) + 2 * a64(2) + 2 * a64((size_t)nseg + 1));
 }
 
 ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, int dtype, int64_t Tq, int64_t Tk,
@@ -496,14 +519,35 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
     const size_t need = ra_partial_workspace_bytes(Tq, Tk, nseg, Hq, Hkv, d, dtype);
     if (!workspace || ws_bytes < need) return fail(RA_ERR_WORKSPACE, "workspace must be >= " + std::to_string(need));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    {
+        // The segment and position arrays are host arrays: each call plans
+        // on the host and uploads its tables from host memory on `stream`,
+        // which a captured graph could not replay (the host copy is gone
+        // after the call), so a capturing stream is refused before any work.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            cs = cudaStreamCaptureStatusNone;
+        }
+        if (cs != cudaStreamCaptureStatusNone)
+            return fail(RA_ERR_UNSUPPORTED,
+                        "the partial calls upload per-call tables from host memory and cannot be captured");
+    }
     const int G = Hq / Hkv;
     const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
     Carver cv(workspace);
     if (tc) {
         TilePlan tp;
         if ((st = build_partial_tiles(cu_q, cu_k, nseg, q_pos, k_pos, Tq, Tk, G, Hkv, causal, window, tp))) return st;
+        // one forward pass: the backward passes' items are not uploaded (the
+        // same tables ra_partial_table_bytes sizes)
+        tp.bitems.clear();
+        tp.qitems.clear();
         DeviceTables dt;
         pack_tables(nullptr, &tp, dt);
+        if (dt.blob.size() > ws_bytes)
+            return fail(RA_ERR_WORKSPACE, "tile tables need " + std::to_string(dt.blob.size()) +
+                                              " bytes, more than the workspace's " + std::to_string(ws_bytes));
         void *tab = cv.take(dt.blob.size());
         RA_CUDA(cudaMemcpyAsync(tab, dt.blob.data(), dt.blob.size(), cudaMemcpyHostToDevice, s), "table upload");
         const uint8_t *tb = static_cast<const uint8_t *>(tab);
@@ -556,6 +600,9 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
     o_offk = put(offk, 2);
     o_cuq = put(cu_q, (size_t)nseg + 1);
     o_cuk = put(cu_k, (size_t)nseg + 1);
+    if (host.size() * 4 > ws_bytes)
+        return fail(RA_ERR_WORKSPACE, "position tables need " + std::to_string(host.size() * 4) +
+                                          " bytes, more than the workspace's " + std::to_string(ws_bytes));
     int32_t *dh = static_cast<int32_t *>(cv.take(host.size() * 4));
     RA_CUDA(cudaMemcpyAsync(dh, host.data(), host.size() * 4, cudaMemcpyHostToDevice, s), "table upload");
     SimtArgs a{};

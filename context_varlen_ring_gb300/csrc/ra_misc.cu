@@ -146,7 +146,11 @@ struct MergePtrs {
 };
 
 // One warp per (token, head) row.  M = max lse_p, L = M + log sum exp(lse_p - M),
-// out = sum_p exp(lse_p - L) out_p; lanes hold 4 consecutive elements of d.
+// out = sum_p exp(lse_p - L) out_p.  Lane p holds the weight of part p (and
+// p + 32); every lane runs the same loops (the weights are broadcast with
+// full-warp shuffles), and a lane whose 4 elements lie past d only skips its
+// loads and stores.  Parts are read four at a time so that each warp keeps
+// several 16-byte loads in flight.
 template <typename TOut>
 __global__ void __launch_bounds__(256) merge_kernel(MergePtrs P, int n, int64_t Tq, int Hq, int d, TOut *out,
                                                      float *lse_out) {
@@ -171,24 +175,39 @@ __global__ void __launch_bounds__(256) merge_kernel(MergePtrs P, int n, int64_t 
         }
         const float wa = (M == -INFINITY || la == -INFINITY) ? 0.f : expf(la - L);
         const float wb = (M == -INFINITY || lb == -INFINITY) ? 0.f : expf(lb - L);
-        for (int c = lane * 4; c < d; c += 128) {
+        for (int c0 = 0; c0 < d; c0 += 128) {
+            const int c = c0 + lane * 4;
+            const bool act = c < d;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int p = 0; p < n; ++p) {
-                const float wp = __shfl_sync(0xffffffffu, p < 32 ? wa : wb, p & 31);
-                if (wp == 0.f) continue;
-                const float4 x = *reinterpret_cast<const float4 *>(P.o[p] + w * d + c);
-                acc.x += wp * x.x;
-                acc.y += wp * x.y;
-                acc.z += wp * x.z;
-                acc.w += wp * x.w;
+            for (int p0 = 0; p0 < n; p0 += 4) {
+                float wq[4];
+                float4 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int p = p0 + u;
+                    const float src = p < 32 ? wa : wb;
+                    wq[u] = __shfl_sync(0xffffffffu, src, p & 31);
+                    if (p >= n) wq[u] = 0.f;
+                    x[u] = (act && wq[u] != 0.f) ? *reinterpret_cast<const float4 *>(P.o[p] + w * d + c)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    acc.x += wq[u] * x[u].x;
+                    acc.y += wq[u] * x[u].y;
+                    acc.z += wq[u] * x[u].z;
+                    acc.w += wq[u] * x[u].w;
+                }
             }
-            if constexpr (sizeof(TOut) == 4) {
-                *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + w * d + c) = acc;
-            } else {
-                uint2 pk;
-                pk.x = dev::pack_bf16x2(acc.x, acc.y);
-                pk.y = dev::pack_bf16x2(acc.z, acc.w);
-                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + w * d + c) = pk;
+            if (act) {
+                if constexpr (sizeof(TOut) == 4) {
+                    *reinterpret_cast<float4 *>(reinterpret_cast<float *>(out) + w * d + c) = acc;
+                } else {
+                    uint2 pk;
+                    pk.x = dev::pack_bf16x2(acc.x, acc.y);
+                    pk.y = dev::pack_bf16x2(acc.z, acc.w);
+                    *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) + w * d + c) = pk;
+                }
             }
         }
         if (lse_out && lane == 0) lse_out[li] = L;

@@ -12,7 +12,8 @@
 // Host code must not pass the array's name to a kernel: on the host it is
 // only a stand-in symbol, not a device address.  The device address is
 // fetched once per device with cudaGetSymbolAddress (on the first call made
-// while that device is current) and cached.
+// while that device is current) and cached for the life of the device's
+// context (a cudaDeviceReset after that first call is not supported).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -31,11 +32,21 @@ std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of this device's scratch array (set up on first use).
-ra_status scratch_address(void **out) {
+// The kernels run on the current device, so the caller's stream must
+// belong to it: the address handed to them is the current device's copy.
+ra_status scratch_address(void *stream, void **out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(RA_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return fail(RA_ERR_UNSUPPORTED, "device index out of range");
+    if (stream) {
+        int sdev = -1;
+        e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev);
+        if (e != cudaSuccess) return fail(RA_ERR_CUDA, std::string("cudaStreamGetDevice: ") + cudaGetErrorString(e));
+        if (sdev != dev)
+            return fail(RA_ERR_INVALID_ARG, "stream belongs to device " + std::to_string(sdev) + ", but device " +
+                                                std::to_string(dev) + " is current");
+    }
     std::lock_guard<std::mutex> lk(g_scratch_mu);
     if (!g_scratch_addr[dev]) {
         void *p = nullptr;
@@ -65,7 +76,7 @@ extern "C" ra_status ra_varlen_attn_partial_noalloc(const void *q, const void *k
                                           std::to_string((size_t)RA_NOALLOC_SCRATCH_BYTES) +
                                           " bytes; use ra_varlen_attn_partial with a caller workspace");
     void *scratch = nullptr;
-    ra_status st = scratch_address(&scratch);
+    ra_status st = scratch_address(stream, &scratch);
     if (st) return st;
     // Every table the kernel reads is rewritten by this call (uploaded on
     // `stream` before the launch), so nothing in the shared array has to

@@ -122,8 +122,19 @@ ra_status ra_zigzag_unpermute(const void *y, void *x, const int32_t *perm,
  *   workspace DEVICE, >= ra_partial_workspace_bytes(...) bytes
  * bf16 with d = 128 and G a power of two <= 16 runs on the tensor cores
  * (tcgen05, fp32 accumulation); other shapes and fp32 run a SIMT fp32 path.
+ * Host arrays: every call tiles its segments on the host (O(Tq + Tk) work
+ * plus O(query tiles x KV tiles) to classify tile pairs) and copies the
+ * tables into the workspace on `stream` from host memory, so a call on a
+ * capturing stream is refused with RA_ERR_UNSUPPORTED before any work
+ * (the ring calls, which cache their plans, can be captured).
+ * ra_partial_workspace_bytes is a bound over every position pattern;
+ * ra_partial_table_bytes gives the exact bytes the tables of one call take
+ * (HOST, no GPU needed; 0 for invalid arguments) and never exceeds it.
  * ------------------------------------------------------------------------ */
 size_t ra_partial_workspace_bytes(int64_t Tq, int64_t Tk, int nseg, int Hq, int Hkv, int d, int dtype);
+size_t ra_partial_table_bytes(int64_t Tq, int64_t Tk, int Hq, int Hkv, int d, int dtype,
+                              const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int nseg,
+                              const int32_t *q_pos, const int32_t *k_pos, int causal, int window);
 ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, int dtype,
                                  int64_t Tq, int64_t Tk, int Hq, int Hkv, int d,
                                  const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int nseg,
@@ -149,7 +160,10 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
  *    in ra_last_error() names both sizes); nothing is launched.
  *  - Set-up: the first call on a device (with that device current) looks up
  *    the array's device address and caches it.  Make that first call before
- *    any stream capture.
+ *    any stream capture.  `stream` must belong to the current device (a
+ *    stream of another device is rejected with RA_ERR_INVALID_ARG).  The
+ *    cached address lives as long as the device's context: a
+ *    cudaDeviceReset after the first call is not supported.
  *  - Sharing: all calls on a device share the one array, which keeps the
  *    last call's contents.  Each call rewrites every table it reads, so no
  *    state carries over, but calls that overlap on the GPU (different

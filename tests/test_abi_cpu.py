@@ -154,3 +154,39 @@ def test_ring_rank_pairs_window_matches_oracle(orc):
                     for window in (0, 13, 256, 10**6):
                         assert np.array_equal(ra.ring_rank_pairs(cu, cp, mode, causal, window),
                                               orc.rank_pairs(cu, cp, mode, causal, window))
+
+
+@pytest.mark.parametrize("G", [1, 4, 16])
+def test_partial_workspace_bound_covers_tables(ra, G):
+    """ra_partial_workspace_bytes bounds the tables a partial call uploads for
+    every position pattern, including positions that break each tile into
+    the most runs (a stride of 2 leaves two rows per tile, so the tile and
+    item counts are the largest a segment can have)."""
+    L = ra.lib()
+    hkv = 8
+    hq = hkv * G
+    rng = np.random.default_rng(21)
+    cases = []
+    for Tq, Tk, nseg in ((4096, 128, 1), (4096, 4096, 3), (777, 1500, 5), (1, 1, 1), (300, 0, 2)):
+        cuq = np.sort(np.concatenate([[0, Tq], rng.integers(0, Tq + 1, nseg - 1)])).astype(np.int32)
+        cuk = np.sort(np.concatenate([[0, Tk], rng.integers(0, Tk + 1, nseg - 1)])).astype(np.int32)
+        for name in ("contiguous", "stride2", "random"):
+            if name == "contiguous":
+                qp, kp = np.arange(Tq, dtype=np.int32), np.arange(Tk, dtype=np.int32)
+            elif name == "stride2":
+                qp, kp = 2 * np.arange(Tq, dtype=np.int32), 2 * np.arange(Tk, dtype=np.int32)
+            else:
+                qp = rng.integers(0, 10 * Tq + 1, Tq).astype(np.int32)
+                kp = rng.integers(0, 10 * Tk + 1, max(Tk, 0)).astype(np.int32)
+            cases.append((Tq, Tk, nseg, cuq, cuk, qp, kp))
+    for Tq, Tk, nseg, cuq, cuk, qp, kp in cases:
+        bound = L.ra_partial_workspace_bytes(Tq, Tk, nseg, hq, hkv, 128, 0)
+        for causal in (0, 1):
+            exact = L.ra_partial_table_bytes(Tq, Tk, hq, hkv, 128, 0, _p(cuq), _p(cuk), nseg, _p(qp),
+                                             _p(kp) if Tk else None, causal, -1)
+            assert 0 < exact <= bound, (Tq, Tk, nseg, causal, exact, bound)
+    # the case of the finding: 4096 queries at a stride of 2 against 128 keys
+    cu_q, cu_k = np.array([0, 4096], np.int32), np.array([0, 128], np.int32)
+    qp, kp = 2 * np.arange(4096, dtype=np.int32), np.arange(128, dtype=np.int32)
+    exact = L.ra_partial_table_bytes(4096, 128, 32, 8, 128, 0, _p(cu_q), _p(cu_k), 1, _p(qp), _p(kp), 1, -1)
+    assert exact <= L.ra_partial_workspace_bytes(4096, 128, 1, 32, 8, 128, 0)

@@ -75,7 +75,7 @@ def test_reference_arm_line(monkeypatch, capsys):
     test stays short."""
     import argparse
     import json
-    monkeypatch.setattr(bench, "cpu_sample_docs", lambda lens: [min(range(len(lens)), key=lambda i: lens[i])])
+    monkeypatch.setattr(bench, "cpu_sample_docs", lambda lens, *a: [min(range(len(lens)), key=lambda i: lens[i])])
     monkeypatch.delenv("RANK", raising=False)
     bench.reference_arm(argparse.Namespace(gpus=1, steps=1, warmup=3))
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
@@ -113,6 +113,12 @@ def test_flop_count_matches_oracle_pairs(orc):
     cu = W.C4.cu_seqlens()
     assert bench.pairs_of(cu) == 67823768
     d, hq = 128, 32
-    assert 2 * d * hq * bench.PRODUCTS["ra_tc_fwd"] * 67823768 == pytest.approx(1.111e12, rel=1e-3)
-    assert 2 * d * hq * bench.PRODUCTS["ra_tc_bwd"] * 67823768 == pytest.approx(3.889e12, rel=1e-3)
-    assert bench.PRODUCTS["ra_tc_bwd"] == bench.PRODUCTS["ra_tc_bwd_dkdv"] + bench.PRODUCTS["ra_tc_bwd_dq"]
+    # the method's work: 4*d*Hq per pair forward, 10*d*Hq backward
+    assert 2 * d * hq * bench.ALGORITHMIC_PRODUCTS["ra_tc_fwd"] * 67823768 == pytest.approx(1.111e12, rel=1e-3)
+    assert 2 * d * hq * bench.ALGORITHMIC_PRODUCTS["ra_tc_bwd"] * 67823768 == pytest.approx(2.778e12, rel=1e-3)
+    # the two backward passes form S and dP twice: 7 products executed
+    ex = bench.EXECUTED_PRODUCTS
+    assert ex["ra_tc_bwd"] == ex["ra_tc_bwd_dkdv"] + ex["ra_tc_bwd_dq"] == 7
+    r = bench.tensor_roofline("ra_tc_bwd", 3.0, d, hq, 67823768, 1902.4, "measured")
+    assert r["frac"] == pytest.approx(2.778e12 / 3.0e-3 / 1e12 / 1902.4, rel=1e-3)
+    assert r["executed_frac"] == pytest.approx(r["frac"] * 7 / 5)

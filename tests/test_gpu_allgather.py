@@ -27,7 +27,16 @@ def ra():
 
 
 def _err(got, ref):
-    return float(np.abs(np.asarray(got, dtype=np.float64) - ref).max()) / max(1.0, float(np.abs(ref).max()))
+    """Plain max-abs error (outputs)."""
+    return float(np.abs(np.asarray(got, dtype=np.float64) - ref).max())
+
+
+def _gerr(got, ref):
+    """Gradient error: max-abs over max(1, max|ref|).  A gradient of a KV
+    head sums the products of its G query heads, formed from bf16 operands
+    (P, dS) that carry a relative rounding of 2^-9 each, so its error grows
+    with its magnitude, which grows with G and the document length."""
+    return _err(got, ref) / max(1.0, float(np.abs(ref).max()))
 
 
 def _lse_err(got_hq_t, ref_t_hq):
@@ -71,7 +80,7 @@ def test_allgather_fwd_bwd_bf16(ra, orc, mode, G, causal, window):
         for g, r in ((dq, rdq), (dk, rdk), (dv, rdv)):
             a = g.cpu().numpy()
             assert np.isfinite(a).all()
-            assert _err(a, r) <= 2e-2, (docs, cp)
+            assert _gerr(a, r) <= 2e-2, (docs, cp, _err(a, r), float(np.abs(r).max()))
 
 
 def test_allgather_fp32_runs_fused(ra, orc):

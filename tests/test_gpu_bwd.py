@@ -1,6 +1,8 @@
 """GPU parity of the ring backward (dQ, dK, dV from the saved LSE) against the
-fp64 oracle.  bf16 inputs: max-abs error <= 2e-2 * max(1, max|ref|) per
-gradient; fp32 inputs: 1e-5 * max(1, max|ref|)."""
+fp64 oracle.  bf16 inputs: gradients to max-abs 2e-2 * max(1, max|ref|)
+(the gradient rule of _rel), and the full-size packed workload's gradients
+of every document to plain max-abs 2e-2; fp32 inputs: 1e-5 plain.  Each
+failure message carries the plain error and max|ref|."""
 import math
 
 import numpy as np
@@ -24,7 +26,18 @@ def ra():
 
 
 def _err(got, ref):
-    return float(np.abs(np.asarray(got, dtype=np.float64) - ref).max()) / max(1.0, float(np.abs(ref).max()))
+    """Plain max-abs error."""
+    return float(np.abs(np.asarray(got, dtype=np.float64) - ref).max())
+
+
+def _rel(got, ref):
+    """Max-abs error over max(1, max|ref|), the gradient rule: a gradient of
+    a KV head sums the products of its G query heads, formed from bf16
+    operands (P, dS) that carry a relative rounding of 2^-9 each, so its
+    error grows with its magnitude (which grows with G and the document
+    length); a gradient returned in bf16 adds its own rounding of up to
+    m * 2^-9 at magnitude m."""
+    return _err(got, ref) / max(1.0, float(np.abs(ref).max()))
 
 
 def _run(ra, q, k, v, do, cu, cp, mode, causal, sched, grad_dtype=torch.float32):
@@ -68,8 +81,7 @@ def test_bwd_small_bf16(ra, orc, sched, mode, G):
         ro, rl = orc.attn_fwd(q, k, v, cu, causal, scale)
         rdq, rdk, rdv = orc.attn_bwd(q, k, v, ro, rl, do, cu, causal, scale)
         for name, g, r in (("dq", dq, rdq), ("dk", dk, rdk), ("dv", dv, rdv)):
-            e = _err(g, r)
-            assert e <= 2e-2, (name, docs, cp, e)
+            assert _rel(g, r) <= 2e-2, (name, docs, cp, _err(g, r), float(np.abs(r).max()))
 
 
 def test_bwd_bf16_grad_output(ra, orc):
@@ -82,55 +94,51 @@ def test_bwd_bf16_grad_output(ra, orc):
     ro, rl = orc.attn_fwd(q, k, v, cu, True, 1 / math.sqrt(128))
     rdq, rdk, rdv = orc.attn_bwd(q, k, v, ro, rl, do, cu, True, 1 / math.sqrt(128))
     for g, r in ((dq, rdq), (dk, rdk), (dv, rdv)):
-        assert _err(g, r) <= 2e-2
+        mx = float(np.abs(r).max())
+        print(f"bf16 gradient: max-abs {_err(g, r):.4g}, max|ref| {mx:.4g}, relative {_rel(g, r):.4g}")
+        assert _rel(g, r) <= 2e-2, (_err(g, r), mx)
 
 
 def test_bwd_c4_full_size(ra, orc):
-    """The packed 32768-token workload at full size: every gradient row of
-    the documents up to 1300 tokens against the oracle (documents are
-    independent), sampled dQ rows of the long documents, and the two sum
-    identities over all keys."""
+    """The packed 32768-token workload at full size, in the launch
+    configuration the benchmark times (fused ring, CP=8, per-document
+    zigzag): for every document, two KV heads with their G query heads are
+    compared element by element with the oracle -- O and LSE of the forward,
+    dQ, dK and dV of the backward (fp32 gradients) -- at the plain max-abs
+    tolerances (2e-2 on outputs and gradients, 1e-3 on LSE).  Documents do
+    not attend to each other, so each is its own oracle problem.  The KV
+    heads rotate over the documents so that all eight are covered."""
     wl = W.C4
     cu = wl.cu_seqlens()
     T = wl.T
+    G = wl.hq // wl.hkv
     q, k, v = W.make_qkv(T, wl.hq, wl.hkv, wl.d, wl.dtype)
     do = W.make_dout(T, wl.hq, wl.d, wl.dtype)
     out, lse, dq, dk, dv = _run(ra, q, k, v, do, cu, wl.cp, wl.zz_mode, True, "fused")
-    lens = np.diff(cu)
-    for bdoc in np.nonzero(lens <= 1300)[0]:
+    out = out.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    report = []
+    for bdoc in range(len(cu) - 1):
         a, e = int(cu[bdoc]), int(cu[bdoc + 1])
         sub = np.array([0, e - a])
-        qs, ks, vs, ds = q[a:e], k[a:e], v[a:e], do[a:e]
-        ro, rl = orc.attn_fwd(qs, ks, vs, sub, True, wl.scale)
-        rdq, rdk, rdv = orc.attn_bwd(qs, ks, vs, ro, rl, ds, sub, True, wl.scale)
-        for name, g, r in (("dq", dq[a:e], rdq), ("dk", dk[a:e], rdk), ("dv", dv[a:e], rdv)):
-            err = _err(g, r)
-            assert err <= 2e-2, (name, bdoc, err)
-    # sampled dQ rows in the long documents
-    long_docs = np.nonzero(lens > 1300)[0]
-    rows = []
-    rng = np.random.default_rng(7)
-    for bdoc in long_docs:
-        a, e = int(cu[bdoc]), int(cu[bdoc + 1])
-        rows += [a, e - 1] + list(rng.integers(a, e, size=3))
-    rows = np.array(sorted(set(rows)), dtype=np.int64)
-    seg = orc.doc_ids(cu)
-    pos = np.arange(T)
-    ro, rl = orc.partial_fwd(q[torch.from_numpy(rows)], k, v, seg[rows], seg, rows, pos, True, wl.scale)
-    o_full = np.zeros((T, wl.hq, wl.d))
-    l_full = np.zeros((T, wl.hq))
-    o_full[rows] = ro
-    l_full[rows] = rl
-    rdq, _, _ = orc.attn_bwd(q, k, v, o_full, l_full, do, cu, True, wl.scale, dq_rows=rows, dk_rows=np.array([0]))
-    assert _err(dq[rows], rdq) <= 2e-2
-    # sum identities: sum_j dV_j = sum over the group's heads of sum_i dO_i; sum_j dK_j = 0
-    G = wl.hq // wl.hkv
-    dof = do.double().numpy()
-    for g in range(wl.hkv):
-        ref = dof[:, g * G:(g + 1) * G].sum((0, 1))
-        assert np.abs(dv[:, g].astype(np.float64).sum(0) - ref).max() <= 1e-2 * max(1.0, np.abs(ref).max())
-        scale_k = np.abs(dk[:, g]).sum(0).max()
-        assert np.abs(dk[:, g].astype(np.float64).sum(0)).max() <= 1e-3 * scale_k
+        for g in sorted({bdoc % wl.hkv, (bdoc + 3) % wl.hkv}):
+            hs = slice(g * G, (g + 1) * G)
+            qs, ks, vs, ds = (x.contiguous() for x in (q[a:e, hs], k[a:e, g:g + 1], v[a:e, g:g + 1], do[a:e, hs]))
+            ro, rl = orc.attn_fwd(qs, ks, vs, sub, True, wl.scale)
+            rdq, rdk, rdv = orc.attn_bwd(qs, ks, vs, ro, rl, ds, sub, True, wl.scale)
+            _err_lse = np.abs(lse[hs, a:e].T - rl).max()
+            assert _err_lse <= 1e-3, (bdoc, g, _err_lse)
+            for name, got, ref in (("o", out[a:e, hs], ro), ("dq", dq[a:e, hs], rdq), ("dk", dk[a:e, g:g + 1], rdk),
+                                   ("dv", dv[a:e, g:g + 1], rdv)):
+                err = float(np.abs(np.asarray(got, dtype=np.float64) - ref).max())
+                mx = float(np.abs(ref).max())
+                report.append((name, bdoc, e - a, g, err, mx))
+                assert err <= 2e-2, (name, bdoc, e - a, g, err, mx)
+    worst = {}
+    for name, bdoc, L_, g, err, mx in report:
+        if err > worst.get(name, (0.0,))[0]:
+            worst[name] = (err, mx, bdoc, L_, g)
+    print("worst max-abs error (error, max|ref| of that block, doc, length, KV head):", worst)
 
 
 @pytest.mark.parametrize("sched", ["fused", "stepwise"])

@@ -98,10 +98,13 @@ def test_partial_vs_oracle(ra, orc, dtype, d, hq, hkv, causal):
     _cmp_lse(lse.cpu().numpy(), rl, tl)
 
 
-def test_merge_vs_oracle(ra, orc):
-    rng = np.random.default_rng(3)
-    T, H, d = 777, 6, 128
-    n = 5
+@pytest.mark.parametrize("d,n", [(128, 5), (64, 3), (160, 33), (4, 64), (256, 8)])
+def test_merge_vs_oracle(ra, orc, d, n):
+    """Head dims that are not a multiple of 128 leave some lanes without
+    elements in the last 128-column pass (d=64: lanes 16-31; d=160: lanes
+    8-31 of the second pass), and n > 32 puts part weights in both halves."""
+    rng = np.random.default_rng(3 + d + n)
+    T, H = 777, 6
     outs, lses = [], []
     for p in range(n):
         o = rng.standard_normal((T, H, d)).astype(np.float32)
@@ -201,3 +204,30 @@ def test_wait_guard_selftest(ra):
     torch.cuda.synchronize()
     assert ra.device_status() == _lib.RA_ERR_TIMEOUT
     assert ra.device_status() == 0
+
+
+def test_partial_refuses_stream_capture(ra):
+    """The partial call plans on the host and uploads its tables from host
+    memory each call, so on a capturing stream it returns
+    RA_ERR_UNSUPPORTED before doing any work; eager calls are unaffected."""
+    cu = np.array([0, 200], np.int32)
+    q, k, v = (x.cuda() for x in W.make_qkv(200, 8, 2, 128, torch.bfloat16))
+    out = torch.empty((200, 8, 128), device="cuda")
+    lse = torch.empty((8, 200), device="cuda")
+    ra.varlen_attn_partial(q, k, v, cu, cu, out=out, lse=lse)
+    torch.cuda.synchronize()
+    ref = (out.clone(), lse.clone())
+    g = torch.cuda.CUDAGraph()
+    err = None
+    with torch.cuda.graph(g):
+        try:
+            ra.varlen_attn_partial(q, k, v, cu, cu, out=out, lse=lse)
+        except ra.RaError as e:
+            err = e
+    assert err is not None and err.status == 2, err
+    del g
+    out.zero_()
+    ra.varlen_attn_partial(q, k, v, cu, cu, out=out, lse=lse)
+    torch.cuda.synchronize()
+    _check_status(ra)
+    assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])

@@ -32,7 +32,16 @@ def _status(ra):
 
 
 def _err(got, ref):
-    return float(np.abs(np.asarray(got, dtype=np.float64) - ref).max()) / max(1.0, float(np.abs(ref).max()))
+    """Plain max-abs error (outputs)."""
+    return float(np.abs(np.asarray(got, dtype=np.float64) - ref).max())
+
+
+def _gerr(got, ref):
+    """Gradient error: max-abs over max(1, max|ref|).  A gradient of a KV
+    head sums the products of its G query heads, formed from bf16 operands
+    (P, dS) that carry a relative rounding of 2^-9 each, so its error grows
+    with its magnitude, which grows with G and the document length."""
+    return _err(got, ref) / max(1.0, float(np.abs(ref).max()))
 
 
 def _lse_err(got_hq_t, ref_t_hq):
@@ -69,7 +78,7 @@ def test_window_ring_fwd_bwd_bf16(ra, orc, sched, mode, G, causal):
         assert _lse_err(lse.cpu().numpy(), rl) <= 1e-3, window
         rdq, rdk, rdv = orc.attn_bwd(q, k, v, ro, rl, do, cu, causal, scale, window=window)
         for g, r in ((dq, rdq), (dk, rdk), (dv, rdv)):
-            assert _err(g.cpu().numpy(), r) <= 2e-2, (window, docs)
+            assert _gerr(g.cpu().numpy(), r) <= 2e-2, (window, docs, _err(g.cpu().numpy(), r), float(np.abs(r).max()))
 
 
 @pytest.mark.parametrize("sched", ["fused", "stepwise"])
@@ -144,7 +153,7 @@ def test_window_c2_sampled(ra, orc):
     rdq, rdk, rdv = orc.attn_bwd(qs, ks, vs, so, sl, dos, sub_cu, True, wl.scale, window=window)
     sidx = torch.from_numpy(sel).cuda()
     for g, r in ((dq, rdq), (dk, rdk), (dv, rdv)):
-        assert _err(g[sidx].cpu().numpy(), r) <= 2e-2
+        assert _gerr(g[sidx].cpu().numpy(), r) <= 2e-2, (_err(g[sidx].cpu().numpy(), r), float(np.abs(r).max()))
 
 
 def test_noncausal_ring_plan(ra, orc):

@@ -2,7 +2,9 @@
 callers that cannot allocate device memory (its scratch is a static device
 array inside the library).  Called through the C ABI and compared with the
 workspace-taking ra_varlen_attn_partial on the same inputs, on two calls in
-a row (the second call must not see anything left over by the first).
+a row (the second call must not see anything left over by the first); both
+run the same kernel on the same tables, so the results must be
+bit-identical.
 
 This file is named to be collected last, so a run that stops at the first
 failure has already run every other test."""
@@ -76,11 +78,10 @@ def test_noalloc_matches_workspace_entry_point_two_calls(L):
     ]
     for cuq, cuk, qpos, kpos, q, k, v in cases:
         ro, rl, o, l = _run_both(L, cuq, cuk, qpos, kpos, q, k, v)
-        assert np.abs(o - ro).max() <= 2e-2
-        fin = np.isfinite(rl)
-        assert np.array_equal(np.isfinite(l), fin)
-        assert np.all(l[~fin] == -np.inf)
-        assert np.abs(l[fin] - rl[fin]).max() <= 1e-3
+        # the same kernel on the same inputs and tables: bit-identical
+        # (every row is computed by one work item in a fixed order)
+        assert np.array_equal(o, ro)
+        assert np.array_equal(l, rl)
 
 
 def test_noalloc_rejects_oversize_problem(L):
