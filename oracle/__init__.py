@@ -41,11 +41,12 @@ def lib():
         i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
         L.orc_set_threads.argtypes = [i32]
         L.orc_set_threads.restype = i32
-        L.orc_partial_fwd.argtypes = [P, P, P, i64, i64, i32, i32, i32, P, P, P, P, i32, i64, dbl, P, i64, P, P]
+        L.orc_partial_fwd.argtypes = [P, P, P, i64, i64, i32, i32, i32, P, P, P, P, i32, i64, dbl, P, P, P, i64, P, P]
         L.orc_partial_fwd.restype = i32
         L.orc_lse_merge.argtypes = [i32, P, P, i64, i32, i32, P, P]
         L.orc_lse_merge.restype = i32
-        L.orc_attn_bwd.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, P, P, i32, i64, dbl, P, i64, P, i64, P, P, P]
+        L.orc_attn_bwd.argtypes = [P, P, P, P, P, P, i64, i32, i32, i32, P, P, i32, i64, dbl, P, P, P, i64, P, i64, P, P,
+                                   P]
         L.orc_attn_bwd.restype = i32
         L.orc_zigzag_owner.argtypes = [P, i32, i32, i32, P]
         L.orc_zigzag_owner.restype = i32
@@ -93,13 +94,24 @@ def doc_ids(cu) -> np.ndarray:
     return ids
 
 
-def partial_fwd(q, k, v, seg_q, seg_k, q_pos, k_pos, causal: bool, scale: float, rows=None, window: int = -1):
+def _bounds(b, n):
+    if b is None:
+        return None, None
+    a = _i64(b)
+    assert a.shape == (n,)
+    return a, _p(a)
+
+
+def partial_fwd(q, k, v, seg_q, seg_k, q_pos, k_pos, causal: bool, scale: float, rows=None, window: int = -1,
+                q_lo=None, q_hi=None):
     """Attention of queries against keys over the allowed pairs
     {(i,j): seg_k[j]==seg_q[i] and (not causal or k_pos[j] <= q_pos[i])
-    and (window < 0 or k_pos[j] >= q_pos[i] - window)}.
+    and (window < 0 or k_pos[j] >= q_pos[i] - window)
+    and (q_lo is None or k_pos[j] >= q_lo[i]) and (q_hi is None or k_pos[j] <= q_hi[i])}.
 
-    q [Tq,Hq,d], k/v [Tk,Hkv,d].  Returns (out [R,Hq,d], lse [R,Hq]) in fp64,
-    R = len(rows) or Tq.  Empty rows give out = 0 and lse = -inf."""
+    q [Tq,Hq,d], k/v [Tk,Hkv,d]; q_lo / q_hi [Tq] (per query, indexed like
+    q).  Returns (out [R,Hq,d], lse [R,Hq]) in fp64, R = len(rows) or Tq.
+    Empty rows give out = 0 and lse = -inf."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     Tq, Hq, d = q.shape
     Tk, Hkv, _ = k.shape
@@ -111,22 +123,25 @@ def partial_fwd(q, k, v, seg_q, seg_k, q_pos, k_pos, causal: bool, scale: float,
     else:
         rr = _i64(rows)
         R, rp = len(rr), _p(rr)
+    lo_a, lo_p = _bounds(q_lo, Tq)
+    hi_a, hi_p = _bounds(q_hi, Tq)
     out = np.zeros((R, Hq, d), dtype=np.float64)
     lse = np.zeros((R, Hq), dtype=np.float64)
     rc = lib().orc_partial_fwd(_p(q), _p(k), _p(v), Tq, Tk, Hq, Hkv, d, _p(sq), _p(sk), _p(pq), _p(pk),
-                               int(bool(causal)), int(window), float(scale), rp, R, _p(out), _p(lse))
+                               int(bool(causal)), int(window), float(scale), lo_p, hi_p, rp, R, _p(out), _p(lse))
     if rc:
         raise ValueError(f"orc_partial_fwd failed ({rc})")
     return out, lse
 
 
-def attn_fwd(q, k, v, cu, causal: bool, scale: float, rows=None, window: int = -1):
+def attn_fwd(q, k, v, cu, causal: bool, scale: float, rows=None, window: int = -1, q_lo=None, q_hi=None):
     """Full packed (block-diagonal, optionally causal, optionally
-    sliding-window) attention."""
+    sliding-window, optionally interval-masked by per-token key bounds
+    q_lo / q_hi on packed positions) attention."""
     T = int(np.asarray(cu)[-1])
     seg = doc_ids(cu)
     pos = np.arange(T, dtype=np.int64)
-    return partial_fwd(q, k, v, seg, seg, pos, pos, causal, scale, rows, window)
+    return partial_fwd(q, k, v, seg, seg, pos, pos, causal, scale, rows, window, q_lo, q_hi)
 
 
 def lse_merge(outs, lses):
@@ -145,8 +160,10 @@ def lse_merge(outs, lses):
     return out, lse
 
 
-def attn_bwd(q, k, v, o, lse, dout, cu, causal: bool, scale: float, dq_rows=None, dk_rows=None, window: int = -1):
-    """Gradients (dq, dk, dv) in fp64 given the oracle's own forward (o, lse).
+def attn_bwd(q, k, v, o, lse, dout, cu, causal: bool, scale: float, dq_rows=None, dk_rows=None, window: int = -1,
+             q_lo=None, q_hi=None):
+    """Gradients (dq, dk, dv) in fp64 given the oracle's own forward (o, lse)
+    over the allowed set of attn_fwd with the same arguments.
 
     o/lse/dout are [T,Hq,d]/[T,Hq]/[T,Hq,d]; rows that no requested output
     depends on may hold zeros."""
@@ -165,12 +182,14 @@ def attn_bwd(q, k, v, o, lse, dout, cu, causal: bool, scale: float, dq_rows=None
     else:
         ka = _i64(dk_rows)
         nk, kp = len(ka), _p(ka)
+    lo_a, lo_p = _bounds(q_lo, T)
+    hi_a, hi_p = _bounds(q_hi, T)
     dq = np.zeros((nq, Hq, d))
     dk = np.zeros((nk, Hkv, d))
     dv = np.zeros((nk, Hkv, d))
     rc = lib().orc_attn_bwd(_p(q), _p(k), _p(v), _p(o), _p(lse), _p(dout), T, Hq, Hkv, d,
-                            _p(seg), _p(pos), int(bool(causal)), int(window), float(scale), qp, nq, kp, nk,
-                            _p(dq), _p(dk), _p(dv))
+                            _p(seg), _p(pos), int(bool(causal)), int(window), float(scale), lo_p, hi_p, qp, nq,
+                            kp, nk, _p(dq), _p(dk), _p(dv))
     if rc:
         raise ValueError("orc_attn_bwd failed")
     return dq, dk, dv

@@ -56,6 +56,15 @@ int orc_set_threads(int n) {
  * block-diagonal causal attention; with a subset of keys it is one ring
  * step's partial result.
  *
+ * Interval masks (the dynamic, per-token attention masks of "[Train]
+ * Support custom attention with context parallel", FlagScale PR #910,
+ * description: flex attention with context parallelism): with q_lo and
+ * q_hi given (NULL = none), the allowed set is further restricted to
+ *      q_lo[i] <= k_pos[j] <= q_hi[i],
+ * the bounds being positions, like k_pos.  Causal, sliding-window,
+ * chunked-local, prefix-LM and bidirectional document masks are all such
+ * intervals.
+ *
  *   s_ij  = scale * sum_c q[i,h,c] * k[j,g,c],      g = h / (Hq/Hkv)
  *   lse_i = m + log( sum_{j in A(i)} exp(s_ij - m) ),  m = max_{j in A(i)} s_ij
  *   o_i   = sum_{j in A(i)} exp(s_ij - lse_i) * v[j,g,:]
@@ -64,11 +73,23 @@ int orc_set_threads(int n) {
  * rows: the query indices to evaluate (NULL = all Tq rows in order).
  * out [nrows, Hq, d], lse [nrows, Hq] (natural log).
  * ------------------------------------------------------------------------ */
+static int pair_allowed(int32_t sq, int32_t sk, int64_t qp, int64_t kp, int causal, int64_t window,
+                        const int64_t *q_lo, const int64_t *q_hi, int64_t i)
+{
+    if (sk != sq) return 0;
+    if (causal && kp > qp) return 0;
+    if (window >= 0 && kp < qp - window) return 0;
+    if (q_lo && kp < q_lo[i]) return 0;
+    if (q_hi && kp > q_hi[i]) return 0;
+    return 1;
+}
+
 int orc_partial_fwd(const double *q, const double *k, const double *v,
                     int64_t Tq, int64_t Tk, int Hq, int Hkv, int d,
                     const int32_t *seg_q, const int32_t *seg_k,
                     const int64_t *q_pos, const int64_t *k_pos,
                     int causal, int64_t window, double scale,
+                    const int64_t *q_lo, const int64_t *q_hi,
                     const int64_t *rows, int64_t nrows,
                     double *out, double *lse)
 {
@@ -90,8 +111,7 @@ int orc_partial_fwd(const double *q, const double *k, const double *v,
             double m = -INFINITY;
             int any = 0;
             for (int64_t j = 0; j < Tk; ++j) {
-                int allowed = (seg_k[j] == seg_q[i]) && (!causal || k_pos[j] <= q_pos[i]) &&
-                              (window < 0 || k_pos[j] >= q_pos[i] - window);
+                int allowed = pair_allowed(seg_q[i], seg_k[j], q_pos[i], k_pos[j], causal, window, q_lo, q_hi, i);
                 ok[j] = (unsigned char)allowed;
                 if (!allowed) continue;
                 const double *kj = k + (j * Hkv + g) * (int64_t)d;
@@ -170,7 +190,8 @@ int orc_lse_merge(int n, const double *const *outs, const double *const *lses,
  *   dQ_i  = scale * sum_j dS_ij k_j
  *   dK_j  = scale * sum_{h in group(g)} sum_i dS_ij q_i
  *   dV_j  =         sum_{h in group(g)} sum_i P_ij dO_i
- * o, lse are the forward results for the same inputs.
+ * o, lse are the forward results for the same inputs.  The allowed set is
+ * that of orc_partial_fwd (with the same optional q_lo / q_hi bounds).
  * dq_rows / dk_rows: which rows of dQ / dK,dV to evaluate (NULL = all);
  * dq [ndq, Hq, d], dk/dv [ndk, Hkv, d].
  * ------------------------------------------------------------------------ */
@@ -185,6 +206,7 @@ int orc_attn_bwd(const double *q, const double *k, const double *v,
                  const double *o, const double *lse, const double *dout,
                  int64_t T, int Hq, int Hkv, int d,
                  const int32_t *seg, const int64_t *pos, int causal, int64_t window, double scale,
+                 const int64_t *q_lo, const int64_t *q_hi,
                  const int64_t *dq_rows, int64_t ndq,
                  const int64_t *dk_rows, int64_t ndk,
                  double *dq, double *dk, double *dv)
@@ -212,8 +234,7 @@ int orc_attn_bwd(const double *q, const double *k, const double *v,
         for (int c = 0; c < d; ++c) dqi[c] = 0.0;
         double li = lse[i * Hq + h];
         for (int64_t j = 0; j < T; ++j) {
-            if (!(seg[j] == seg[i] && (!causal || pos[j] <= pos[i]) && (window < 0 || pos[j] >= pos[i] - window)))
-                continue;
+            if (!pair_allowed(seg[i], seg[j], pos[i], pos[j], causal, window, q_lo, q_hi, i)) continue;
             const double *kj = k + (j * Hkv + g) * (int64_t)d;
             const double *vj = v + (j * Hkv + g) * (int64_t)d;
             double p = exp(scale * dot(qi, kj, d) - li);
@@ -235,9 +256,7 @@ int orc_attn_bwd(const double *q, const double *k, const double *v,
         for (int c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
         for (int h = g * G; h < (g + 1) * G; ++h) {
             for (int64_t i = 0; i < T; ++i) {
-                if (!(seg[j] == seg[i] && (!causal || pos[j] <= pos[i]) &&
-                      (window < 0 || pos[j] >= pos[i] - window)))
-                    continue;
+                if (!pair_allowed(seg[i], seg[j], pos[i], pos[j], causal, window, q_lo, q_hi, i)) continue;
                 const double *qi = q + (i * Hq + h) * (int64_t)d;
                 const double *doi = dout + (i * Hq + h) * (int64_t)d;
                 double p = exp(scale * dot(qi, kj, d) - lse[i * Hq + h]);

@@ -136,3 +136,59 @@ def sample_rows(T: int, n: int, seed: int, must_include=()) -> np.ndarray:
     while len(rows) < min(n, T):
         rows.add(int(rng.integers(0, T)))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def interval_bounds(cu, kind: str, param: int = 0, seed: int = 0):
+    """Per-token key intervals of a packed batch, on packed positions: query
+    i sees key j of its own document iff lo[i] <= j <= hi[i].  Both arrays
+    are non-decreasing inside every document.  Kinds:
+      causal         lo = document start, hi = i
+      window         lo = max(start, i - param), hi = i  (param = window)
+      chunked        lo = start of i's block of `param` tokens, hi = i
+      prefix         bidirectional over the first `param` tokens of each
+                     document, causal after: lo = start,
+                     hi = max(i, start + param - 1) (capped at the end)
+      bidirectional  lo = start, hi = end - 1
+      random         seeded non-decreasing lo and hi inside each document,
+                     with some rows empty (lo > hi)
+    Returns (lo, hi) as int32 arrays [T]."""
+    cu = np.asarray(cu, dtype=np.int64)
+    T = int(cu[-1])
+    lo = np.zeros(T, dtype=np.int64)
+    hi = np.zeros(T, dtype=np.int64)
+    rng = np.random.default_rng(seed)
+    for b in range(len(cu) - 1):
+        s, e = int(cu[b]), int(cu[b + 1])
+        if e <= s:
+            continue
+        i = np.arange(s, e, dtype=np.int64)
+        if kind == "causal":
+            lo[s:e], hi[s:e] = s, i
+        elif kind == "window":
+            lo[s:e], hi[s:e] = np.maximum(s, i - param), i
+        elif kind == "chunked":
+            lo[s:e], hi[s:e] = s + (i - s) // param * param, i
+        elif kind == "prefix":
+            lo[s:e], hi[s:e] = s, np.minimum(np.maximum(i, s + param - 1), e - 1)
+        elif kind == "bidirectional":
+            lo[s:e], hi[s:e] = s, e - 1
+        elif kind == "random":
+            L = e - s
+            a = np.sort(rng.integers(s, e, L))
+            c = np.sort(rng.integers(s - 2, e + 2, L))
+            lo[s:e], hi[s:e] = a, np.clip(c, s - 1, e - 1)
+        else:
+            raise ValueError(kind)
+    return lo.astype(np.int32), hi.astype(np.int32)
+
+
+def interval_pairs(cu, lo, hi) -> int:
+    """Allowed (query, key) pairs of an interval mask (keys of the query's
+    own document inside [lo, hi])."""
+    cu = np.asarray(cu, dtype=np.int64)
+    T = int(cu[-1])
+    start = np.repeat(cu[:-1], np.diff(cu))
+    end = np.repeat(cu[1:], np.diff(cu)) - 1
+    a = np.maximum(np.asarray(lo, np.int64), start)
+    b = np.minimum(np.asarray(hi, np.int64), end)
+    return int(np.maximum(b - a + 1, 0).sum()) if T else 0
