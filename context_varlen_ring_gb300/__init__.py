@@ -88,13 +88,20 @@ PLAN_STATS = ("q_tiles", "kv_tiles", "fwd_items", "dkdv_items", "dq_items", "fwd
 
 
 def ring_plan_stats(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, G: int = 4, Hkv: int = 8, causal: bool = True,
-                    window: int = -1, sched: str = "fused", exact: bool = False, n_sm: int = 152) -> dict:
+                    window: int = -1, sched: str = "fused", exact: bool = False, n_sm: int = 152, key_lo=None,
+                    key_hi=None) -> dict:
     """Host-only counts of what the tensor-core passes visit (tiles, work
     items, visited tile pairs, rows copied into rank order; with exact=True
     also the allowed pairs inside the visited tile pairs of each pass) and a
     scheduling model of each pass over n_sm SMs (makespans in tile visits)."""
     cu = _host_i32(cu_seqlens)
     out = np.zeros(len(PLAN_STATS), dtype=np.int64)
+    if key_lo is not None or key_hi is not None:
+        lo, hi = _host_i32(key_lo), _host_i32(key_hi)
+        check(lib().ra_ring_plan_stats_masked(_np_ptr(cu), len(cu) - 1, cp, mode, G, Hkv, _np_ptr(lo), _np_ptr(hi),
+                                              _SCHED[sched], int(exact), int(n_sm), _np_ptr(out)),
+              "ra_ring_plan_stats_masked")
+        return dict(zip(PLAN_STATS, (int(x) for x in out)))
     check(lib().ra_ring_plan_stats(_np_ptr(cu), len(cu) - 1, cp, mode, G, Hkv, int(causal), int(window),
                                    _SCHED[sched], int(exact), int(n_sm), _np_ptr(out)), "ra_ring_plan_stats")
     return dict(zip(PLAN_STATS, (int(x) for x in out)))
@@ -189,21 +196,29 @@ class _Workspace:
 _WS = _Workspace()
 
 
-def ring_workspace_bytes(T, Hq, Hkv, d, dtype, cu_seqlens, cp, mode, sched="fused", bwd=False) -> int:
+def ring_workspace_bytes(T, Hq, Hkv, d, dtype, cu_seqlens, cp, mode, sched="fused", bwd=False, key_lo=None,
+                         key_hi=None) -> int:
     cu = _host_i32(cu_seqlens)
+    if key_lo is not None or key_hi is not None:
+        lo, hi = _host_i32(key_lo), _host_i32(key_hi)
+        return int(lib().ra_ring_workspace_bytes_masked(T, Hq, Hkv, d, dtype, _np_ptr(cu), len(cu) - 1, cp, mode,
+                                                        _np_ptr(lo), _np_ptr(hi), _SCHED[sched], int(bwd)))
     return int(lib().ra_ring_workspace_bytes(T, Hq, Hkv, d, dtype, _np_ptr(cu), len(cu) - 1, cp, mode,
                                              _SCHED[sched], int(bwd)))
 
 
 def ring_attn_fwd(q, k, v, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool = True,
                   scale: float | None = None, sched: str = "fused", out=None, lse=None, workspace=None,
-                  window: int = -1):
+                  window: int = -1, key_lo=None, key_hi=None):
     """Simulated zigzag ring attention forward; returns (out [T,Hq,d] in q's
     dtype, lse fp32 [Hq,T]) in the original token order.  window >= 0: a key
     is visible only up to `window` positions behind its query.  sched:
     "fused" (ring steps in one launch), "stepwise" (a launch per ring step,
     then the LSE merge) or "allgather" (each rank's queries over the gathered
-    K/V of all ranks)."""
+    K/V of all ranks).  key_lo / key_hi (int32 [T], host or device, both
+    non-decreasing inside each document): an interval mask instead of
+    causal and window -- query i sees key j of its document iff
+    key_lo[i] <= j <= key_hi[i]."""
     _check_cuda(q, k, v)
     T, Hq, d = q.shape
     Hkv = k.shape[1]
@@ -216,6 +231,15 @@ def ring_attn_fwd(q, k, v, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal
     if lse is None:
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
     L = lib()
+    if key_lo is not None or key_hi is not None:
+        lo, hi = _host_i32(key_lo), _host_i32(key_hi)
+        need = L.ra_ring_workspace_bytes_masked(T, Hq, Hkv, d, dt, _np_ptr(cu), B, cp, mode, _np_ptr(lo), _np_ptr(hi),
+                                                _SCHED[sched], 0)
+        ws = workspace if workspace is not None else _WS.get(q.device, int(need))
+        check(L.ra_ring_attn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), dt, T, Hq, Hkv, d, _np_ptr(cu), B, cp, mode,
+                                        _np_ptr(lo), _np_ptr(hi), scale, _SCHED[sched], _ptr(out), _ptr(lse), _ptr(ws),
+                                        ws.numel(), _stream(q.device)), "ra_ring_attn_fwd_masked")
+        return out, lse
     need = L.ra_ring_workspace_bytes(T, Hq, Hkv, d, dt, _np_ptr(cu), B, cp, mode, _SCHED[sched], 0)
     ws = workspace if workspace is not None else _WS.get(q.device, int(need))
     check(L.ra_ring_attn_fwd(_ptr(q), _ptr(k), _ptr(v), dt, T, Hq, Hkv, d, _np_ptr(cu), B, cp, mode, int(causal),
@@ -226,9 +250,9 @@ def ring_attn_fwd(q, k, v, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal
 
 def ring_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool = True,
                   scale: float | None = None, sched: str = "fused", grad_dtype=None, dq=None, dk=None, dv=None,
-                  workspace=None, reuse_fwd_workspace: bool = False, window: int = -1):
-    """Gradients (dq, dk, dv) in the original token order (window as in
-    ring_attn_fwd; pass the forward's).
+                  workspace=None, reuse_fwd_workspace: bool = False, window: int = -1, key_lo=None, key_hi=None):
+    """Gradients (dq, dk, dv) in the original token order (window, or
+    key_lo / key_hi, as in ring_attn_fwd; pass the forward's).
 
     reuse_fwd_workspace: `workspace` is the one the preceding ring_attn_fwd
     used with these same q, k, v and arguments, untouched since; its
@@ -246,6 +270,17 @@ def ring_attn_bwd(q, k, v, out, lse, dout, cu_seqlens, cp: int, mode: int = RA_Z
     dk = torch.empty((T, Hkv, d), dtype=gd, device=q.device) if dk is None else dk
     dv = torch.empty((T, Hkv, d), dtype=gd, device=q.device) if dv is None else dv
     L = lib()
+    if key_lo is not None or key_hi is not None:
+        lo, hi = _host_i32(key_lo), _host_i32(key_hi)
+        need = L.ra_ring_workspace_bytes_masked(T, Hq, Hkv, d, dt, _np_ptr(cu), B, cp, mode, _np_ptr(lo), _np_ptr(hi),
+                                                _SCHED[sched], 1)
+        ws = workspace if workspace is not None else _WS.get(q.device, int(need))
+        check(L.ra_ring_attn_bwd_masked(_ptr(q), _ptr(k), _ptr(v), dt, T, Hq, Hkv, d, _np_ptr(cu), B, cp, mode,
+                                        _np_ptr(lo), _np_ptr(hi), scale, _SCHED[sched], _ptr(out), _ptr(lse),
+                                        _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _dtype_code(dq),
+                                        RA_BWD_FWD_RESERVE if reuse_fwd_workspace else 0, _ptr(ws), ws.numel(),
+                                        _stream(q.device)), "ra_ring_attn_bwd_masked")
+        return dq, dk, dv
     need = L.ra_ring_workspace_bytes(T, Hq, Hkv, d, dt, _np_ptr(cu), B, cp, mode, _SCHED[sched], 1)
     ws = workspace if workspace is not None else _WS.get(q.device, int(need))
     check(L.ra_ring_attn_bwd(_ptr(q), _ptr(k), _ptr(v), dt, T, Hq, Hkv, d, _np_ptr(cu), B, cp, mode, int(causal),

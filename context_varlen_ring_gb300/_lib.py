@@ -37,6 +37,8 @@ EXPORTS = (
     "ra_ring_rank_pairs", "ra_get_device_status", "ra_selftest_wait_timeout",
     "ra_status_string", "ra_last_error", "ra_version", "ra_profile_enable", "ra_profile_read",
     "ra_varlen_attn_partial_noalloc", "ra_ring_plan_stats", "ra_partial_table_bytes",
+    "ra_ring_workspace_bytes_masked", "ra_ring_attn_fwd_masked", "ra_ring_attn_bwd_masked",
+    "ra_ring_plan_stats_masked",
 )
 
 _lib = None
@@ -66,8 +68,14 @@ def _declare(L):
                                    P, P, P, sz, P]),
         "ra_ring_attn_bwd": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, i32, i32, f32, i32,
                                    P, P, P, P, P, P, i32, i32, P, sz, P]),
+        "ra_ring_workspace_bytes_masked": (sz, [i64, i32, i32, i32, i32, P, i32, i32, i32, P, P, i32, i32]),
+        "ra_ring_attn_fwd_masked": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, P, P, f32, i32,
+                                          P, P, P, sz, P]),
+        "ra_ring_attn_bwd_masked": (i32, [P, P, P, i32, i64, i32, i32, i32, P, i32, i32, i32, P, P, f32, i32,
+                                          P, P, P, P, P, P, i32, i32, P, sz, P]),
         "ra_ring_rank_pairs": (i32, [P, i32, i32, i32, i32, i32, P]),
         "ra_ring_plan_stats": (i32, [P, i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, P]),
+        "ra_ring_plan_stats_masked": (i32, [P, i32, i32, i32, i32, i32, P, P, i32, i32, i32, P]),
         "ra_get_device_status": (i32, [P]),
         "ra_selftest_wait_timeout": (i32, [i64, P]),
         "ra_status_string": (ctypes.c_char_p, [i32]),

@@ -680,6 +680,28 @@ RingLayout ring_layout(const RingPlan &plan, int64_t T, int Hq, int Hkv, int d, 
     return L;
 }
 
+// Interval masks: both bounds or neither; they run on the tensor-core
+// path in the fused and all-gather schedules; each bound must keep the
+// kernels' 32-bit position arithmetic exact.  With bounds the causal flag
+// and the window are not used (the intervals hold them).
+static ra_status bounds_checks(const int32_t *key_lo, const int32_t *key_hi, int64_t T, bool tc, int sched,
+                               int *causal, int *window) {
+    if (!key_lo && !key_hi) return RA_OK;
+    if (!key_lo || !key_hi) return fail(RA_ERR_INVALID_ARG, "key_lo and key_hi go together");
+    if (!tc)
+        return fail(RA_ERR_UNSUPPORTED, "interval masks run on the tensor-core path (bf16, d = 128, Hq / Hkv a "
+                                        "power of two <= 16)");
+    if (sched == RA_SCHED_STEPWISE)
+        return fail(RA_ERR_UNSUPPORTED, "interval masks run in the fused and all-gather schedules");
+    const int32_t lim = 1 << 30;
+    for (int64_t i = 0; i < T; ++i)
+        if (key_lo[i] <= -lim || key_lo[i] >= lim || key_hi[i] <= -lim || key_hi[i] >= lim)
+            return fail(RA_ERR_UNSUPPORTED, "interval bounds must lie in (-2^30, 2^30)");
+    *causal = 0;
+    *window = -1;
+    return RA_OK;
+}
+
 // A window >= T reaches every earlier key of every document: no window.
 // Positions (< T) plus the window must fit the kernels' 32-bit arithmetic.
 static ra_status ring_window(int64_t T, int *window) {
@@ -722,23 +744,40 @@ size_t ra_ring_workspace_bytes(int64_t T, int Hq, int Hkv, int d, int dtype, con
     return ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, bwd).total;
 }
 
-ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
-                           const int32_t *cu, int B, int cp, int mode, int causal, int window, float scale, int sched,
-                           void *out, float *lse, void *workspace, size_t ws_bytes, void *stream) {
+size_t ra_ring_workspace_bytes_masked(int64_t T, int Hq, int Hkv, int d, int dtype, const int32_t *cu, int B, int cp,
+                                      int mode, const int32_t *key_lo, const int32_t *key_hi, int sched, int bwd) {
+    if (check_common(dtype, Hq, Hkv, d) != RA_OK || T < 0 || T > INT32_MAX) return 0;
+    if (sched != RA_SCHED_FUSED && sched != RA_SCHED_ALLGATHER) return 0;
+    if (!tc_fwd_supported(dtype, d, Hq, Hkv) || !key_lo || !key_hi) return 0;
+    if (validate_cu(cu, B, T) != RA_OK) return 0;
+    ra_status st;
+    int causal = 0, window = -1;
+    if (bounds_checks(key_lo, key_hi, T, true, sched, &causal, &window) != RA_OK) return 0;
+    auto plan = get_ring_plan(cu, B, cp, mode, Hq / Hkv, Hkv, 0, -1, true, sched == RA_SCHED_ALLGATHER, &st, key_lo,
+                              key_hi);
+    if (!plan) return 0;
+    return ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, bwd).total;
+}
+
+static ra_status ring_fwd_impl(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv,
+                               int d, const int32_t *cu, int B, int cp, int mode, int causal, int window, float scale,
+                               int sched, void *out, float *lse, void *workspace, size_t ws_bytes, void *stream,
+                               const int32_t *key_lo, const int32_t *key_hi) {
     ra_status st = ring_checks(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, sched, scale);
     if (st) return st;
+    const int G = Hq / Hkv;
+    const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
+    if ((st = bounds_checks(key_lo, key_hi, T, tc, sched, &causal, &window))) return st;
     if (T == 0) return RA_OK;
     if (!out || !lse) return fail(RA_ERR_INVALID_ARG, "out/lse is NULL");
     if (!aligned16(out)) return fail(RA_ERR_UNSUPPORTED, "out must be 16-byte aligned");
-    const int G = Hq / Hkv;
-    const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
     // all-gather: one pass of each rank's queries over every document's K/V
     // in original order (tensor cores); elsewhere the fused ring computes the
     // same attention
     const bool allgather = sched == RA_SCHED_ALLGATHER && tc;
     if (sched == RA_SCHED_ALLGATHER && !tc) sched = RA_SCHED_FUSED;
     if ((st = ring_window(T, &window))) return st;
-    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, allgather, &st);
+    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, allgather, &st, key_lo, key_hi);
     if (!plan) return st;
     const RingLayout L = ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, 0);
     if (!workspace || ws_bytes < L.total)
@@ -797,6 +836,11 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
             a.t1 = t1;
             a.causal = causal;
             a.window = window;
+            if (dt.bounds) {
+                a.qbounds = tab + dt.o_qb;
+                a.key_lo = reinterpret_cast<const int32_t *>(tab + dt.o_klo);
+                a.key_hi = reinterpret_cast<const int32_t *>(tab + dt.o_khi);
+            }
             a.scale = scale;
             a.out_mode = out_mode;
             a.out = o;
@@ -872,23 +916,25 @@ ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtyp
     return RA_OK;
 }
 
-ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
-                           const int32_t *cu, int B, int cp, int mode, int causal, int window, float scale, int sched,
-                           const void *out, const float *lse, const void *dout, void *dq, void *dk, void *dv,
-                           int grad_dtype, int flags, void *workspace, size_t ws_bytes, void *stream) {
+static ra_status ring_bwd_impl(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv,
+                               int d, const int32_t *cu, int B, int cp, int mode, int causal, int window, float scale,
+                               int sched, const void *out, const float *lse, const void *dout, void *dq, void *dk,
+                               void *dv, int grad_dtype, int flags, void *workspace, size_t ws_bytes, void *stream,
+                               const int32_t *key_lo, const int32_t *key_hi) {
     ra_status st = ring_checks(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, sched, scale);
     if (st) return st;
     if (grad_dtype != RA_BF16 && grad_dtype != RA_FP32) return fail(RA_ERR_INVALID_ARG, "bad grad_dtype");
+    const int G = Hq / Hkv;
+    const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
+    if ((st = bounds_checks(key_lo, key_hi, T, tc, sched, &causal, &window))) return st;
     if (T == 0) return RA_OK;
     if (!out || !lse || !dout || !dq || !dk || !dv) return fail(RA_ERR_INVALID_ARG, "NULL tensor");
     if (!aligned16(out) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return fail(RA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned");
-    const int G = Hq / Hkv;
-    const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
     const bool allgather = sched == RA_SCHED_ALLGATHER && tc;
     if (sched == RA_SCHED_ALLGATHER && !tc) sched = RA_SCHED_FUSED;
     if ((st = ring_window(T, &window))) return st;
-    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, allgather, &st);
+    auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, tc, allgather, &st, key_lo, key_hi);
     if (!plan) return st;
     const RingLayout L = ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, 1);
     if (!workspace || ws_bytes < L.total)
@@ -981,6 +1027,11 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         a.window = window;
         a.scale = scale;
         a.tile_ld = tld;
+        if (dt.bounds) {
+            a.qbounds = tab + dt.o_qb;
+            a.key_lo = reinterpret_cast<const int32_t *>(tab + dt.o_klo);
+            a.key_hi = reinterpret_cast<const int32_t *>(tab + dt.o_khi);
+        }
         TcDqArgs qa{};
         qa.q = Qp;
         qa.k = allgather ? k : Kp;
@@ -1003,6 +1054,9 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         qa.B = B;
         qa.causal = causal;
         qa.window = window;
+        qa.qbounds = a.qbounds;
+        qa.key_lo = a.key_lo;
+        qa.key_hi = a.key_hi;
         qa.scale = scale;
         qa.lse = lse;
         qa.D = D;
@@ -1111,6 +1165,40 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
         RA_CUDA(launch_cast_f32(dva, dv, grad_dtype, T * Hkv * d, s), "cast dv");
     }
     return RA_OK;
+}
+
+ra_status ra_ring_attn_fwd(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
+                           const int32_t *cu, int B, int cp, int mode, int causal, int window, float scale, int sched,
+                           void *out, float *lse, void *workspace, size_t ws_bytes, void *stream) {
+    return ring_fwd_impl(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, causal, window, scale, sched, out, lse,
+                         workspace, ws_bytes, stream, nullptr, nullptr);
+}
+
+ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq, int Hkv, int d,
+                           const int32_t *cu, int B, int cp, int mode, int causal, int window, float scale, int sched,
+                           const void *out, const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                           int grad_dtype, int flags, void *workspace, size_t ws_bytes, void *stream) {
+    return ring_bwd_impl(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, causal, window, scale, sched, out, lse, dout,
+                         dq, dk, dv, grad_dtype, flags, workspace, ws_bytes, stream, nullptr, nullptr);
+}
+
+ra_status ra_ring_attn_fwd_masked(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq,
+                                  int Hkv, int d, const int32_t *cu, int B, int cp, int mode, const int32_t *key_lo,
+                                  const int32_t *key_hi, float scale, int sched, void *out, float *lse,
+                                  void *workspace, size_t ws_bytes, void *stream) {
+    if (!key_lo || !key_hi) return fail(RA_ERR_INVALID_ARG, "key_lo / key_hi is NULL");
+    return ring_fwd_impl(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, 0, -1, scale, sched, out, lse, workspace,
+                         ws_bytes, stream, key_lo, key_hi);
+}
+
+ra_status ra_ring_attn_bwd_masked(const void *q, const void *k, const void *v, int dtype, int64_t T, int Hq,
+                                  int Hkv, int d, const int32_t *cu, int B, int cp, int mode, const int32_t *key_lo,
+                                  const int32_t *key_hi, float scale, int sched, const void *out, const float *lse,
+                                  const void *dout, void *dq, void *dk, void *dv, int grad_dtype, int flags,
+                                  void *workspace, size_t ws_bytes, void *stream) {
+    if (!key_lo || !key_hi) return fail(RA_ERR_INVALID_ARG, "key_lo / key_hi is NULL");
+    return ring_bwd_impl(q, k, v, dtype, T, Hq, Hkv, d, cu, B, cp, mode, 0, -1, scale, sched, out, lse, dout, dq, dk,
+                         dv, grad_dtype, flags, workspace, ws_bytes, stream, key_lo, key_hi);
 }
 
 }  // extern "C"

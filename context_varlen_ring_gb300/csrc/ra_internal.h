@@ -56,24 +56,6 @@ struct ZigzagPlan {
 ra_status validate_cu(const int32_t *cu, int B, int64_t T);
 ra_status build_zigzag(const int32_t *cu, int B, int cp, int mode, ZigzagPlan &zp);
 
-// Tile tables for one query side and one key side.  Tiles of segment b of
-// rank r are [q_off[r*(B+1)+b], q_off[r*(B+1)+b+1]) (same for kv_off).
-struct TilePlan {
-    int cp = 1, B = 0;
-    int q_tokens = 0;                    // tokens per query tile (128 / G)
-    std::vector<Tile> qtiles, kvtiles;
-    std::vector<int32_t> q_off, kv_off;  // [cp*(B+1)+1]
-    std::vector<WorkItem> items;         // forward items, LPT order
-    std::vector<WorkItem> bitems;        // backward dK/dV items (one per KV tile x head)
-    std::vector<WorkItem> qitems;        // backward dQ items (one per query tile x head)
-    int64_t fwd_tile_pairs = 0;          // non-skipped (query tile, KV tile) visits
-};
-
-// Builds tiles over rows [lo, hi) with positions pos[row] (at most two
-// consecutive-position runs per tile) and appends them.
-void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_t hi,
-                  int tile_rows, int seg);
-
 // Tile-pair class used by both the host cost model and the kernels: skip
 // when no pair is allowed (every key after every query under the causal
 // mask, or further behind every query than the window), full when every
@@ -88,12 +70,58 @@ inline int classify(const Tile &q, const Tile &k, int causal, int window) {
     return kPartial;
 }
 
+// Interval masks: query token i sees key j of its own document iff
+// lo[i] <= j <= hi[i] (original token indices).  Per query tile the planner
+// keeps the extremes of its rows' bounds, from which a tile pair is
+// classified: skip when every row's interval misses the KV tile's positions
+// (hi_max < kpmin or lo_min > kpmax), full when every row's interval covers
+// a complete KV tile (lo_max <= kpmin and hi_min >= kpmax), else partial.
+struct QBounds {
+    int32_t lo_min, lo_max, hi_min, hi_max;
+};
+static_assert(sizeof(QBounds) == 16, "query tile bounds are one int4");
+inline int classify_bounds(const Tile &q, const QBounds &b, const Tile &k) {
+    if (q.len <= 0 || k.len <= 0) return kSkip;
+    if (b.hi_max < k.pmin || b.lo_min > k.pmax) return kSkip;
+    if (k.len == kBN && b.lo_max <= k.pmin && b.hi_min >= k.pmax) return kFull;
+    return kPartial;
+}
+
+// Tile tables for one query side and one key side.  Tiles of segment b of
+// rank r are [q_off[r*(B+1)+b], q_off[r*(B+1)+b+1]) (same for kv_off).
+struct TilePlan {
+    int cp = 1, B = 0;
+    int q_tokens = 0;                    // tokens per query tile (128 / G)
+    std::vector<Tile> qtiles, kvtiles;
+    std::vector<int32_t> q_off, kv_off;  // [cp*(B+1)+1]
+    std::vector<WorkItem> items;         // forward items, LPT order
+    std::vector<WorkItem> bitems;        // backward dK/dV items (one per KV tile x head)
+    std::vector<WorkItem> qitems;        // backward dQ items (one per query tile x head)
+    int64_t fwd_tile_pairs = 0;          // non-skipped (query tile, KV tile) visits
+    // interval masks only: bounds extremes per query tile, and the per-token
+    // bounds [T] the kernels read at a row's original position
+    std::vector<QBounds> qbounds;
+    std::vector<int32_t> key_lo, key_hi;
+    // tile-pair class under the plan's mask
+    int pair_class(int qi, int kj, int causal, int window) const {
+        return qbounds.empty() ? classify(qtiles[qi], kvtiles[kj], causal, window)
+                               : classify_bounds(qtiles[qi], qbounds[qi], kvtiles[kj]);
+    }
+};
+
+// Builds tiles over rows [lo, hi) with positions pos[row] (at most two
+// consecutive-position runs per tile) and appends them.
+void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_t hi,
+                  int tile_rows, int seg);
+
 // Ring tile plan: query side = key side = the permuted buffer.
 // allgather: the key side is every document's K/V in original order (the
 // all-gather schedule), held as the segments of rank 0; otherwise each
 // rank's zigzag shard, as the ring passes it.
+// key_lo / key_hi (NULL = none): an interval mask (then causal and window
+// are ignored), checked for non-decreasing bounds inside every document.
 ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, bool allgather,
-                           TilePlan &tp);
+                           TilePlan &tp, const int32_t *key_lo = nullptr, const int32_t *key_hi = nullptr);
 
 // Generic partial's tile plan: one "rank", separate Q and K sides.
 ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg,
@@ -113,6 +141,9 @@ struct DeviceTables {
     // Work counters of the persistent kernels (uploaded as zeros; a kernel
     // returns its counter to zero when it finishes): [0, 2) forward.
     size_t o_sched = 0;
+    // interval masks: QBounds per query tile, key_lo and key_hi [T]
+    size_t o_qb = 0, o_klo = 0, o_khi = 0;
+    bool bounds = false;
     int n_items = 0, n_bitems = 0, n_qitems = 0;
 };
 void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt);
@@ -141,9 +172,11 @@ struct RingPlan {
 // `stream` (a cudaStream_t).  Under stream capture the plan must already
 // have its page-locked copy (an earlier call outside capture made it).
 ra_status upload_plan_tables(RingPlan &plan, void *dst, void *stream);
-// Cached plans keyed by content (cu_seqlens, cp, mode, G, Hkv, causal, window).
+// Cached plans keyed by content (cu_seqlens, cp, mode, G, Hkv, causal, window,
+// and the interval bounds when given).
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
-                                        int causal, int window, bool want_tiles, bool allgather, ra_status *st);
+                                        int causal, int window, bool want_tiles, bool allgather, ra_status *st,
+                                        const int32_t *key_lo = nullptr, const int32_t *key_hi = nullptr);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

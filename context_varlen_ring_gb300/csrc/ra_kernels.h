@@ -130,6 +130,8 @@ struct TcFwdArgs {
     int t0, t1;                        // >= 0: override every item's step range
     int causal;
     int window;                        // sliding window (keys at most this far behind), < 0: none
+    const void *qbounds;               // interval masks (else NULL): QBounds per query tile,
+    const int32_t *key_lo, *key_hi;    // and each token's key bounds [Tq] at its original position
     float scale;
     int out_mode;
     void *out;
@@ -156,6 +158,8 @@ struct TcBwdArgs {
     int t0, t1;                        // >= 0: override every item's step range
     int causal;
     int window;                        // sliding window (keys at most this far behind), < 0: none
+    const void *qbounds;               // interval masks (else NULL), as in TcFwdArgs
+    const int32_t *key_lo, *key_hi;
     float scale;
     const float *tile_ld;              // launch_tile_lse_d output for these tiles
     void *dk, *dv;                     // [T, Hkv, d] at original positions
@@ -179,6 +183,8 @@ struct TcDqArgs {
     int t0, t1;
     int causal;
     int window;                        // sliding window (keys at most this far behind), < 0: none
+    const void *qbounds;               // interval masks (else NULL), as in TcFwdArgs
+    const int32_t *key_lo, *key_hi;
     float scale;
     const float *lse, *D;              // [Hq, lse_T] at original positions
     int64_t lse_T;

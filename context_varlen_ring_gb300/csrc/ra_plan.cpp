@@ -139,8 +139,8 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
                     const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
                     int64_t c_t = 0;
                     for (int j = ka; j < ke; ++j) {
-                        c_t += classify(tp.qtiles[i], tp.kvtiles[j], causal, window) != kSkip;
-                        if (q1 >= 0) c_t += classify(tp.qtiles[q1], tp.kvtiles[j], causal, window) != kSkip;
+                        c_t += tp.pair_class(i, j, causal, window) != kSkip;
+                        if (q1 >= 0) c_t += tp.pair_class(q1, j, causal, window) != kSkip;
                     }
                     if (c_t) {
                         tf = std::min(tf, t);
@@ -161,7 +161,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
                         const int s2 = ((r - t) % cp + cp) % cp;
                         const int ka = tp.kv_off[seg_idx(s2, b)], ke = tp.kv_off[seg_idx(s2, b) + 1];
                         int64_t c_t = 0;
-                        for (int j = ka; j < ke; ++j) c_t += classify(tp.qtiles[qi], tp.kvtiles[j], causal, window) != kSkip;
+                        for (int j = ka; j < ke; ++j) c_t += tp.pair_class(qi, j, causal, window) != kSkip;
                         if (c_t) {
                             qf = std::min(qf, t);
                             ql = t + 1;
@@ -188,7 +188,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
                     const int r = (s + t) % cp;
                     const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
                     int64_t c_t = 0;
-                    for (int i = qa; i < qe; ++i) c_t += classify(tp.qtiles[i], tp.kvtiles[j], causal, window) != kSkip;
+                    for (int i = qa; i < qe; ++i) c_t += tp.pair_class(i, j, causal, window) != kSkip;
                     if (c_t) {
                         tf = std::min(tf, t);
                         tl = t + 1;
@@ -231,8 +231,18 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
 }
 
 ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, bool allgather,
-                           TilePlan &tp) {
+                           TilePlan &tp, const int32_t *key_lo, const int32_t *key_hi) {
     if (G < 1 || kBM % G != 0) return fail(RA_ERR_UNSUPPORTED, "GQA group must divide 128");
+    if ((key_lo == nullptr) != (key_hi == nullptr)) return fail(RA_ERR_INVALID_ARG, "key_lo and key_hi go together");
+    if (key_lo) {
+        // the key-side backward inverts each row's interval with a binary
+        // search, which needs bounds that never decrease inside a document
+        for (int b = 0; b < zp.B; ++b)
+            for (int64_t i = (int64_t)zp.cu[b] + 1; i < zp.cu[b + 1]; ++i)
+                if (key_lo[i] < key_lo[i - 1] || key_hi[i] < key_hi[i - 1])
+                    return fail(RA_ERR_INVALID_ARG, "key_lo and key_hi must be non-decreasing inside each document "
+                                                    "(token " + std::to_string(i) + ")");
+    }
     tp = TilePlan();
     tp.cp = zp.cp;
     tp.B = zp.B;
@@ -256,6 +266,24 @@ ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int
     }
     tp.q_off.back() = (int32_t)tp.qtiles.size();
     tp.kv_off.back() = (int32_t)tp.kvtiles.size();
+    if (key_lo) {
+        const int64_t T = (int64_t)zp.perm.size();
+        tp.key_lo.assign(key_lo, key_lo + T);
+        tp.key_hi.assign(key_hi, key_hi + T);
+        tp.qbounds.resize(tp.qtiles.size());
+        for (size_t i = 0; i < tp.qtiles.size(); ++i) {
+            const Tile &t = tp.qtiles[i];
+            QBounds qb{INT32_MAX, INT32_MIN, INT32_MAX, INT32_MIN};
+            for (int c = 0; c < t.len; ++c) {
+                const int64_t pos = c < t.split ? (int64_t)t.pos0 + c : (int64_t)t.pos1 + (c - t.split);
+                qb.lo_min = std::min(qb.lo_min, key_lo[pos]);
+                qb.lo_max = std::max(qb.lo_max, key_lo[pos]);
+                qb.hi_min = std::min(qb.hi_min, key_hi[pos]);
+                qb.hi_max = std::max(qb.hi_max, key_hi[pos]);
+            }
+            tp.qbounds[i] = qb;
+        }
+    }
     build_items(tp, Hkv, causal, window);
     return RA_OK;
 }
@@ -307,6 +335,10 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
     dt.o_sched = take(64);
     dt.o_qmask = take(zp && tp ? zp->perm.size() : 0);
     dt.o_kvmask = take(zp && tp ? zp->perm.size() : 0);
+    dt.bounds = tp && !tp->qbounds.empty();
+    dt.o_qb = take(dt.bounds ? tp->qbounds.size() * sizeof(QBounds) : 0);
+    dt.o_klo = take(dt.bounds ? tp->key_lo.size() * 4 : 0);
+    dt.o_khi = take(dt.bounds ? tp->key_hi.size() * 4 : 0);
     dt.blob.assign(o, 0);
     auto put = [&](size_t at, const void *src, size_t bytes) {
         if (bytes) std::memcpy(dt.blob.data() + at, src, bytes);
@@ -324,6 +356,11 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
         put(dt.o_items, tp->items.data(), tp->items.size() * sizeof(WorkItem));
         put(dt.o_bitems, tp->bitems.data(), tp->bitems.size() * sizeof(WorkItem));
         put(dt.o_qitems, tp->qitems.data(), tp->qitems.size() * sizeof(WorkItem));
+        if (dt.bounds) {
+            put(dt.o_qb, tp->qbounds.data(), tp->qbounds.size() * sizeof(QBounds));
+            put(dt.o_klo, tp->key_lo.data(), tp->key_lo.size() * 4);
+            put(dt.o_khi, tp->key_hi.data(), tp->key_hi.size() * 4);
+        }
         dt.n_items = (int)tp->items.size();
         dt.n_bitems = (int)tp->bitems.size();
         dt.n_qitems = (int)tp->qitems.size();
@@ -346,7 +383,8 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
 }
 
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
-                                        int causal, int window, bool want_tiles, bool allgather, ra_status *st) {
+                                        int causal, int window, bool want_tiles, bool allgather, ra_status *st,
+                                        const int32_t *key_lo, const int32_t *key_hi) {
     static std::mutex mu;
     static std::map<std::string, std::shared_ptr<RingPlan>> cache;
     static std::vector<std::string> order;
@@ -354,8 +392,18 @@ std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mo
     if (*st) return nullptr;
     std::string key;
     key.append(reinterpret_cast<const char *>(cu), sizeof(int32_t) * (size_t)(B + 1));
-    int32_t tail[9] = {B, cp, mode, G, Hkv, causal, window, want_tiles ? 1 : 0, allgather ? 1 : 0};
+    const bool bounds = key_lo != nullptr || key_hi != nullptr;
+    if (bounds && (!key_lo || !key_hi || !want_tiles)) {
+        *st = fail(RA_ERR_INVALID_ARG, "interval masks need both bounds and the tensor-core path");
+        return nullptr;
+    }
+    int32_t tail[10] = {B, cp, mode, G, Hkv, causal, window, want_tiles ? 1 : 0, allgather ? 1 : 0, bounds ? 1 : 0};
     key.append(reinterpret_cast<const char *>(tail), sizeof(tail));
+    if (bounds) {  // the plan depends on every token's bounds
+        const size_t T = (size_t)cu[B];
+        key.append(reinterpret_cast<const char *>(key_lo), T * sizeof(int32_t));
+        key.append(reinterpret_cast<const char *>(key_hi), T * sizeof(int32_t));
+    }
     {
         std::lock_guard<std::mutex> lk(mu);
         auto it = cache.find(key);
@@ -365,7 +413,7 @@ std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mo
     *st = build_zigzag(cu, B, cp, mode, plan->zz);
     if (*st) return nullptr;
     if (want_tiles) {
-        *st = build_ring_tiles(plan->zz, G, Hkv, causal, window, allgather, plan->tiles);
+        *st = build_ring_tiles(plan->zz, G, Hkv, causal, window, allgather, plan->tiles, key_lo, key_hi);
         if (*st) return nullptr;
         plan->has_tiles = true;
     }

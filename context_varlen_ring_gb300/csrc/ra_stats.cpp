@@ -13,14 +13,14 @@
 
 using namespace ra;
 
-extern "C" {
-
 // Walks each tensor-core pass's work items over their ring-step ranges the
 // way the kernels do (forward and dQ: rank r at step t reads the key tiles
 // of rank (r - t) mod cp; dK/dV: the key tile of rank s meets the query
-// tiles of rank (s + t) mod cp) and counts what they visit.
-ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, int Hkv, int causal, int window,
-                             int sched, int exact, int n_sm, int64_t *stats) {
+// tiles of rank (s + t) mod cp) and counts what they visit.  key_lo /
+// key_hi: an interval mask (then causal and window are not used).
+static ra_status plan_stats_impl(const int32_t *cu, int B, int cp, int mode, int G, int Hkv, int causal, int window,
+                                 int sched, int exact, int n_sm, int64_t *stats, const int32_t *key_lo,
+                                 const int32_t *key_hi) {
     if (!stats) return fail(RA_ERR_INVALID_ARG, "stats is NULL");
     if (n_sm < 1) return fail(RA_ERR_INVALID_ARG, "n_sm must be >= 1");
     if (cp < 1 || cp > kMaxMergeParts) return fail(RA_ERR_INVALID_ARG, "cp must be in [1, 64]");
@@ -33,8 +33,12 @@ ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, 
     const int64_t T = cu[B];
     if (window >= T) window = -1;
     if (window < -1) window = -1;
+    if (key_lo || key_hi) {
+        causal = 0;
+        window = -1;
+    }
     auto plan = get_ring_plan(cu, B, cp, mode, G, Hkv, causal ? 1 : 0, window, true,
-                              sched == RA_SCHED_ALLGATHER, &st);
+                              sched == RA_SCHED_ALLGATHER, &st, key_lo, key_hi);
     if (!plan) return st;
     const TilePlan &tp = plan->tiles;
     for (int i = 0; i < RA_PLAN_STATS_N; ++i) stats[i] = 0;
@@ -57,7 +61,8 @@ ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, 
             const int64_t qp = pos_of(q, i);
             for (int j = 0; j < k.len; ++j) {
                 const int64_t kp = pos_of(k, j);
-                const bool allowed = (!causal || kp <= qp) && (window < 0 || kp >= qp - window);
+                const bool allowed = key_lo ? (kp >= key_lo[qp] && kp <= key_hi[qp])
+                                            : (!causal || kp <= qp) && (window < 0 || kp >= qp - window);
                 if (allowed)
                     ++ok;
                 else if (bad)
@@ -80,7 +85,7 @@ ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, 
             for (int j = tp.kv_off[seg(s, w.b)]; j < tp.kv_off[seg(s, w.b) + 1]; ++j) {
                 for (int qt : {w.qt0, w.qt1}) {
                     if (qt < 0) continue;
-                    const int c = classify(tp.qtiles[qt], tp.kvtiles[j], causal, window);
+                    const int c = tp.pair_class(qt, j, causal, window);
                     if (c == kSkip) continue;
                     ++n;
                     if (w.g != 0) continue;
@@ -99,7 +104,7 @@ ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, 
         for (int t = w.t0; t < w.t1; ++t) {
             const int r = (w.r + t) % cp;
             for (int i = tp.q_off[seg(r, w.b)]; i < tp.q_off[seg(r, w.b) + 1]; ++i) {
-                if (classify(tp.qtiles[i], tp.kvtiles[w.qt0], causal, window) == kSkip) continue;
+                if (tp.pair_class(i, w.qt0, causal, window) == kSkip) continue;
                 ++n;
                 if (w.g != 0) continue;
                 ++stats[14];
@@ -114,7 +119,7 @@ ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, 
         for (int t = w.t0; t < w.t1; ++t) {
             const int s = ((w.r - t) % cp + cp) % cp;
             for (int j = tp.kv_off[seg(s, w.b)]; j < tp.kv_off[seg(s, w.b) + 1]; ++j) {
-                if (classify(tp.qtiles[w.qt0], tp.kvtiles[j], causal, window) == kSkip) continue;
+                if (tp.pair_class(w.qt0, j, causal, window) == kSkip) continue;
                 ++n;
                 if (w.g != 0) continue;
                 ++stats[15];
@@ -150,6 +155,21 @@ ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, 
     stats[17] = greedy(c_kv);
     stats[18] = strided(c_q);
     return RA_OK;
+}
+
+extern "C" {
+
+ra_status ra_ring_plan_stats(const int32_t *cu, int B, int cp, int mode, int G, int Hkv, int causal, int window,
+                             int sched, int exact, int n_sm, int64_t *stats) {
+    return plan_stats_impl(cu, B, cp, mode, G, Hkv, causal, window, sched, exact, n_sm, stats, nullptr, nullptr);
+}
+
+ra_status ra_ring_plan_stats_masked(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
+                                    const int32_t *key_lo, const int32_t *key_hi, int sched, int exact, int n_sm,
+                                    int64_t *stats) {
+    if (!key_lo || !key_hi) return fail(RA_ERR_INVALID_ARG, "key_lo / key_hi is NULL");
+    if (sched == RA_SCHED_STEPWISE) return fail(RA_ERR_UNSUPPORTED, "interval masks run in the fused and all-gather schedules");
+    return plan_stats_impl(cu, B, cp, mode, G, Hkv, 0, -1, sched, exact, n_sm, stats, key_lo, key_hi);
 }
 
 }  // extern "C"

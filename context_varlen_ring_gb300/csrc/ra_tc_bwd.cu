@@ -82,6 +82,8 @@ struct BwdParams {
     int kv_direct;   // single-run KV tiles: K and V likewise
     int n_items, cp, B, G, log2G, Hq, Hkv;
     int t0, t1, causal, window, out_mode;          // 0 bf16 store, 1 fp32 store, 2 fp32 +=
+    const int4 *qbounds;         // interval masks: QBounds per query tile
+    const int *key_lo, *key_hi;  // and each token's key bounds at its original position
     float scale, scale_log2;
     const float *tile_ld;
     void *dk, *dv;
@@ -91,7 +93,16 @@ struct BwdParams {
 
 struct QInfo {
     int len, pmin, pmax;
+    int lo_min, lo_max, hi_min, hi_max;  // interval masks only
 };
+
+// The host's classify_bounds (interval masks), on device.
+__device__ __forceinline__ int classify_b(const QInfo &q, int klen, int kpmin, int kpmax) {
+    if (q.len <= 0 || klen <= 0) return kSkip;
+    if (q.hi_max < kpmin || q.lo_min > kpmax) return kSkip;
+    if (klen == kBN && q.lo_max <= kpmin && q.hi_min >= kpmax) return kFull;
+    return kPartial;
+}
 
 __device__ __forceinline__ int classify_pair(const QInfo &q, int klen, int kpmin, int kpmax, int causal,
                                              int window) {
@@ -107,9 +118,11 @@ __device__ __forceinline__ uint32_t range_bits(int a, int b, int base) {
     return (uint32_t)(((1ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
 }
 
-// kWindow: compiled with the sliding-window mask (p.window >= 0).
-template <bool kWindow>
+// kMask: 0 causal (or none), 1 with the sliding-window mask (p.window >= 0),
+// 2 interval masks (per-token key bounds).
+template <int kMask>
 __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_constant__ BwdParams p) {
+    constexpr bool kWindow = kMask == 1, kBounds = kMask == 2;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t base_s = smem_u32(smem);
     if (base_s & 1023u) {  // the layout has no slack for realignment
@@ -231,7 +244,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
                 if (idx < hi) {
                     qa = __ldg(p.qtiles + 2 * idx);
                     qb = __ldg(p.qtiles + 2 * idx + 1);
-                    cls = classify_pair(QInfo{qa.y, qb.y, qb.z}, ka.y, kb.y, kb.z, p.causal, kWindow ? p.window : -1);
+                    if (kBounds) {
+                        const int4 bb = __ldg(p.qbounds + idx);
+                        cls = classify_b(QInfo{qa.y, qb.y, qb.z, bb.x, bb.y, bb.z, bb.w}, ka.y, kb.y, kb.z);
+                    } else {
+                        cls = classify_pair(QInfo{qa.y, qb.y, qb.z, 0, 0, 0, 0}, ka.y, kb.y, kb.z, p.causal,
+                                            kWindow ? p.window : -1);
+                    }
                 }
                 uint32_t vis = __ballot_sync(0xffffffffu, cls != kSkip);
                 while (vis && ok) {
@@ -386,7 +405,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dkdv_kernel(const __grid_const
             uint32_t wm[2] = {~0u, ~0u};
             if (cls == kPartial) {
                 int a1 = 0, e1 = 0, a2 = 0, e2 = 0;
-                if (kvalid) {
+                if (kvalid && kBounds) {
+                    // the tokens t of the query tile whose key interval holds
+                    // kpos, [a1, e1): both bounds are non-decreasing along the
+                    // tile (its two runs lie in one document, in position
+                    // order), so each end is a binary search
+                    const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
+                    int lo_ = 0, hi_ = qlen;
+                    while (lo_ < hi_) {  // first t with key_hi >= kpos
+                        const int mid = (lo_ + hi_) >> 1;
+                        const int pm = mid < split ? pos0 + mid : pos1 + (mid - split);
+                        if (__ldg(p.key_hi + pm) >= kpos) hi_ = mid; else lo_ = mid + 1;
+                    }
+                    a1 = lo_;
+                    lo_ = 0;
+                    hi_ = qlen;
+                    while (lo_ < hi_) {  // first t with key_lo > kpos
+                        const int mid = (lo_ + hi_) >> 1;
+                        const int pm = mid < split ? pos0 + mid : pos1 + (mid - split);
+                        if (__ldg(p.key_lo + pm) > kpos) hi_ = mid; else lo_ = mid + 1;
+                    }
+                    e1 = lo_;
+                } else if (kvalid) {
                     const int qlen = d0.y, split = d0.z, pos0 = d0.w, pos1 = d1.x;
                     if (p.causal) {
                         a1 = min(max(kpos - pos0, 0), split);
@@ -585,6 +625,11 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
     p.t1 = a.t1;
     p.causal = a.causal;
     p.window = a.window;
+    if ((a.qbounds != nullptr) != (a.key_lo != nullptr) || (a.key_lo != nullptr) != (a.key_hi != nullptr))
+        return cudaErrorInvalidValue;
+    p.qbounds = static_cast<const int4 *>(a.qbounds);
+    p.key_lo = a.key_lo;
+    p.key_hi = a.key_hi;
     p.out_mode = a.out_mode;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -597,16 +642,19 @@ cudaError_t launch_tc_bwd(const TcBwdArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-        for (const void *fn : {(const void *)tc_dkdv_kernel<false>, (const void *)tc_dkdv_kernel<true>}) {
+        for (const void *fn : {(const void *)tc_dkdv_kernel<0>, (const void *)tc_dkdv_kernel<1>,
+                               (const void *)tc_dkdv_kernel<2>}) {
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess) return e;
         }
         attr_set[dev] = true;
     }
-    if (p.window >= 0)
-        tc_dkdv_kernel<true><<<a.n_items, kThreads, kSmemBytes, st>>>(p);
+    if (p.qbounds)
+        tc_dkdv_kernel<2><<<a.n_items, kThreads, kSmemBytes, st>>>(p);
+    else if (p.window >= 0)
+        tc_dkdv_kernel<1><<<a.n_items, kThreads, kSmemBytes, st>>>(p);
     else
-        tc_dkdv_kernel<false><<<a.n_items, kThreads, kSmemBytes, st>>>(p);
+        tc_dkdv_kernel<0><<<a.n_items, kThreads, kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -76,6 +76,8 @@ struct DqParams {
     int kv_direct;   // single-run KV tiles: K and V likewise
     int n_items, cp, B, G, log2G, Hq;
     int t0, t1, causal, window, out_mode;  // out_mode: 0 bf16 store, 1 fp32 store, 2 fp32 +=
+    const int4 *qbounds;         // interval masks: QBounds per query tile
+    const int *key_lo, *key_hi;  // and each token's key bounds at its original position
     float scale, scale_log2, log2_scale;
     const float *lse, *D;
     long long lse_T;
@@ -86,6 +88,7 @@ struct DqParams {
 
 struct QInfo {
     int len, pmin, pmax;
+    int lo_min, lo_max, hi_min, hi_max;  // interval masks only
 };
 
 // The host classifier's rule (skip / full / partial), on device.
@@ -97,15 +100,25 @@ __device__ __forceinline__ int classify_q(const QInfo &q, int klen, int kpmin, i
     return kPartial;
 }
 
+// The host's classify_bounds (interval masks), on device.
+__device__ __forceinline__ int classify_b(const QInfo &q, int klen, int kpmin, int kpmax) {
+    if (q.len <= 0 || klen <= 0) return kSkip;
+    if (q.hi_max < kpmin || q.lo_min > kpmax) return kSkip;
+    if (klen == kBN && q.lo_max <= kpmin && q.hi_min >= kpmax) return kFull;
+    return kPartial;
+}
+
 __device__ __forceinline__ uint32_t range_bits(int a, int b, int base) {
     const int lo = min(max(a - base, 0), 32), hi = min(max(b - base, 0), 32);
     return (uint32_t)(((1ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
 }
 
 
-// kWindow: compiled with the sliding-window mask (p.window >= 0).
-template <bool kWindow>
+// kMask: 0 causal (or none), 1 with the sliding-window mask (p.window >= 0),
+// 2 interval masks (per-token key bounds).
+template <int kMask>
 __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constant__ DqParams p) {
+    constexpr bool kWindow = kMask == 1, kBounds = kMask == 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -212,7 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                 const int t0 = p.t0 >= 0 ? p.t0 : ib.y;
                 const int t1 = p.t0 >= 0 ? p.t1 : ib.z;
                 const int4 qa = __ldg(p.qtiles + 2 * qt), qb = __ldg(p.qtiles + 2 * qt + 1);
-                const QInfo q{qa.y, qb.y, qb.z};
+                QInfo q{qa.y, qb.y, qb.z, 0, 0, 0, 0};
+                if (kBounds) {
+                    const int4 bb = __ldg(p.qbounds + qt);
+                    q.lo_min = bb.x;
+                    q.lo_max = bb.y;
+                    q.hi_min = bb.z;
+                    q.hi_max = bb.w;
+                }
                 if (lane == 0) {
                     // Q(k) into the next ring slot, ahead of the item's K/V tiles
                     const uint32_t slot = u % kSlots, ph = (u / kSlots) & 1u;
@@ -243,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                         if (idx < hi) {
                             ka = __ldg(p.kvtiles + 2 * idx);
                             kb = __ldg(p.kvtiles + 2 * idx + 1);
-                            c = classify_q(q, ka.y, kb.y, kb.z, p.causal, kWindow ? p.window : -1);
+                            c = kBounds ? classify_b(q, ka.y, kb.y, kb.z)
+                                        : classify_q(q, ka.y, kb.y, kb.z, p.causal, kWindow ? p.window : -1);
                         }
                         uint32_t vis = __ballot_sync(0xffffffffu, c != kSkip);
                         while (vis && ok) {
@@ -491,20 +512,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
             bool valid;
             int qpos, head;
             float lse, D;
+            int lo, hi;  // interval masks: the row's key bounds
         };
         auto row_info = [&](int k) -> RowInfo {
             const int4 ia = __ldg(p.items + 2 * item_of(k));
             const int4 qa = __ldg(p.qtiles + 2 * ia.x), qb = __ldg(p.qtiles + 2 * ia.x + 1);
             const int tok = m >> p.log2G;
-            RowInfo ri_{tok < qa.y, tok < qa.z ? qa.w + tok : qb.x + (tok - qa.z), ia.z * G + (m & (G - 1)), 0.f, 0.f};
+            RowInfo ri_{tok < qa.y, tok < qa.z ? qa.w + tok : qb.x + (tok - qa.z), ia.z * G + (m & (G - 1)), 0.f, 0.f,
+                        1, 0};
             if (ri_.valid) {
                 ri_.lse = __ldg(p.lse + (long long)ri_.head * p.lse_T + ri_.qpos);
                 ri_.D = __ldg(p.D + (long long)ri_.head * p.lse_T + ri_.qpos);
+                if (kBounds) {
+                    ri_.lo = __ldg(p.key_lo + ri_.qpos);
+                    ri_.hi = __ldg(p.key_hi + ri_.qpos);
+                }
             }
             return ri_;
         };
         bool ok = n_my > 0 ? copy_q(0) : true;
-        RowInfo nxt = n_my > 0 ? row_info(0) : RowInfo{false, 0, 0, 0.f, 0.f};
+        RowInfo nxt = n_my > 0 ? row_info(0) : RowInfo{false, 0, 0, 0.f, 0.f, 1, 0};
         for (int k = 0; k < n_my && ok; ++k) {
             const RowInfo cur = nxt;
             if (k + 1 < n_my) nxt = row_info(k + 1);
@@ -547,16 +574,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_dq_kernel(const __grid_constan
                     // upper limits, window lower limits)
                     const int kt_len = e.y & 0xffff, kt_split = e.y >> 16, kt_pos0 = e.z, kt_pos1 = e.w;
                     int lim1, lim2, lo1 = 0, lo2 = kt_split;
-                    if (p.causal) {
-                        lim1 = min(max(qpos - kt_pos0 + 1, 0), kt_split);
-                        lim2 = min(max(qpos - kt_pos1 + kt_split + 1, kt_split), kt_len);
+                    if (kBounds) {  // keys at positions [cur.lo, cur.hi]
+                        lim1 = min(max(cur.hi - kt_pos0 + 1, 0), kt_split);
+                        lim2 = min(max(cur.hi - kt_pos1 + kt_split + 1, kt_split), kt_len);
+                        lo1 = min(max(cur.lo - kt_pos0, 0), kt_split);
+                        lo2 = min(max(cur.lo - kt_pos1 + kt_split, kt_split), kt_len);
                     } else {
-                        lim1 = kt_split;
-                        lim2 = kt_len;
-                    }
-                    if (kWindow) {
-                        lo1 = min(max(qpos - p.window - kt_pos0, 0), kt_split);
-                        lo2 = min(max(qpos - p.window - kt_pos1 + kt_split, kt_split), kt_len);
+                        if (p.causal) {
+                            lim1 = min(max(qpos - kt_pos0 + 1, 0), kt_split);
+                            lim2 = min(max(qpos - kt_pos1 + kt_split + 1, kt_split), kt_len);
+                        } else {
+                            lim1 = kt_split;
+                            lim2 = kt_len;
+                        }
+                        if (kWindow) {
+                            lo1 = min(max(qpos - p.window - kt_pos0, 0), kt_split);
+                            lo2 = min(max(qpos - p.window - kt_pos1 + kt_split, kt_split), kt_len);
+                        }
                     }
                     uint32_t wm[2];
 #pragma unroll
@@ -716,6 +750,11 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
     p.t1 = a.t1;
     p.causal = a.causal;
     p.window = a.window;
+    if ((a.qbounds != nullptr) != (a.key_lo != nullptr) || (a.key_lo != nullptr) != (a.key_hi != nullptr))
+        return cudaErrorInvalidValue;
+    p.qbounds = static_cast<const int4 *>(a.qbounds);
+    p.key_lo = a.key_lo;
+    p.key_hi = a.key_hi;
     p.out_mode = a.out_mode;
     p.scale = a.scale;
     p.scale_log2 = a.scale * 1.4426950408889634f;
@@ -730,7 +769,8 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-        for (const void *fn : {(const void *)tc_dq_kernel<false>, (const void *)tc_dq_kernel<true>}) {
+        for (const void *fn : {(const void *)tc_dq_kernel<0>, (const void *)tc_dq_kernel<1>,
+                               (const void *)tc_dq_kernel<2>}) {
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess) return e;
             cudaFuncAttributes fa;
@@ -749,10 +789,12 @@ cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st) {
         sm_count[dev] = n > 0 ? n : 1;
     }
     const int grid = std::min(a.n_items, (dev >= 0 && dev < 128) ? sm_count[dev] : 1);
-    if (p.window >= 0)
-        tc_dq_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p);
+    if (p.qbounds)
+        tc_dq_kernel<2><<<grid, kThreads, kSmemBytes, st>>>(p);
+    else if (p.window >= 0)
+        tc_dq_kernel<1><<<grid, kThreads, kSmemBytes, st>>>(p);
     else
-        tc_dq_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p);
+        tc_dq_kernel<0><<<grid, kThreads, kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -85,6 +85,8 @@ struct FwdParams {
     int kv_direct;  // single-run KV tiles likewise from tmKo / tmVo
     int n_items, cp, B, G, log2G, Hq;
     int t0, t1, causal, window, out_mode;
+    const int4 *qbounds;        // interval masks: QBounds per query tile
+    const int *key_lo, *key_hi;  // and each token's key bounds at its original position
     float scale_log2;
     void *out;
     float *lse;
@@ -104,6 +106,7 @@ __device__ __forceinline__ TileD load_tile(const int4 *tab, int idx) {
 
 struct QInfo {
     int len, pmin, pmax;
+    int lo_min, lo_max, hi_min, hi_max;  // interval masks only
 };
 
 // The host classifier's rule (skip / full / partial), on device.
@@ -112,6 +115,14 @@ __device__ __forceinline__ int classify_q(const QInfo &q, int klen, int kpmin, i
     if (causal && q.pmax < kpmin) return kSkip;
     if (window >= 0 && q.pmin - window > kpmax) return kSkip;
     if (klen == kBN && (!causal || q.pmin >= kpmax) && (window < 0 || q.pmax - window <= kpmin)) return kFull;
+    return kPartial;
+}
+
+// The host's classify_bounds (interval masks), on device.
+__device__ __forceinline__ int classify_b(const QInfo &q, int klen, int kpmin, int kpmax) {
+    if (q.len <= 0 || klen <= 0) return kSkip;
+    if (q.hi_max < kpmin || q.lo_min > kpmax) return kSkip;
+    if (klen == kBN && q.lo_max <= kpmin && q.hi_min >= kpmax) return kFull;
     return kPartial;
 }
 
@@ -141,11 +152,13 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     }
 }
 
-// kWindow: compiled with the sliding-window mask (p.window >= 0); the
-// instantiation without it keeps the partial-tile path as short as before
-// (this kernel is sensitive to its instruction footprint).
-template <bool kWindow>
+// kMask: 0 causal (or none), 1 with the sliding-window mask (p.window >= 0),
+// 2 interval masks (per-token key bounds).  Each mask has its own
+// instantiation, so the plain causal one keeps the partial-tile path as
+// short as possible (this kernel is sensitive to its instruction footprint).
+template <int kMask>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ FwdParams p) {
+    constexpr bool kWindow = kMask == 1, kBounds = kMask == 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -261,19 +274,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 const int t1 = p.t0 >= 0 ? p.t1 : ib.z;
                 const bool has1 = qt1 >= 0;
                 const int4 qa0 = __ldg(p.qtiles + 2 * qt0), qb0 = __ldg(p.qtiles + 2 * qt0 + 1);
-                const QInfo q0{qa0.y, qb0.y, qb0.z};
+                QInfo q0{qa0.y, qb0.y, qb0.z, 0, 0, 0, 0};
+                if (kBounds) {
+                    const int4 bb = __ldg(p.qbounds + qt0);
+                    q0.lo_min = bb.x;
+                    q0.lo_max = bb.y;
+                    q0.hi_min = bb.z;
+                    q0.hi_max = bb.w;
+                }
                 // a tile of one position run (split == len) is the original
                 // rows [pos0, pos0 + len): read it there, not from the
                 // rank-ordered copy (which then holds only two-run tiles)
                 const bool dir0 = p.q_direct && qa0.z == qa0.y;
                 const CUtensorMap *mq0 = dir0 ? &p.tmQo : &p.tmQ;
                 const int qrow0 = dir0 ? qa0.w : qa0.x;
-                QInfo q1{0, 0, 0};
+                QInfo q1{0, 0, 0, 0, 0, 0, 0};
                 int qrow1 = 0;
                 const CUtensorMap *mq1 = &p.tmQ;
                 if (has1) {
                     const int4 qa1 = __ldg(p.qtiles + 2 * qt1), qb1 = __ldg(p.qtiles + 2 * qt1 + 1);
-                    q1 = QInfo{qa1.y, qb1.y, qb1.z};
+                    q1 = QInfo{qa1.y, qb1.y, qb1.z, 0, 0, 0, 0};
+                    if (kBounds) {
+                        const int4 bb = __ldg(p.qbounds + qt1);
+                        q1.lo_min = bb.x;
+                        q1.lo_max = bb.y;
+                        q1.hi_min = bb.z;
+                        q1.hi_max = bb.w;
+                    }
                     const bool dir1 = p.q_direct && qa1.z == qa1.y;
                     mq1 = dir1 ? &p.tmQo : &p.tmQ;
                     qrow1 = dir1 ? qa1.w : qa1.x;
@@ -320,9 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         if (idx < hi) {
                             ka = __ldg(p.kvtiles + 2 * idx);
                             kb = __ldg(p.kvtiles + 2 * idx + 1);
-                            const int win = kWindow ? p.window : -1;
-                            c0 = classify_q(q0, ka.y, kb.y, kb.z, p.causal, win);
-                            c1 = has1 ? classify_q(q1, ka.y, kb.y, kb.z, p.causal, win) : kSkip;
+                            if (kBounds) {
+                                c0 = classify_b(q0, ka.y, kb.y, kb.z);
+                                c1 = has1 ? classify_b(q1, ka.y, kb.y, kb.z) : kSkip;
+                            } else {
+                                const int win = kWindow ? p.window : -1;
+                                c0 = classify_q(q0, ka.y, kb.y, kb.z, p.causal, win);
+                                c1 = has1 ? classify_q(q1, ka.y, kb.y, kb.z, p.causal, win) : kSkip;
+                            }
                         }
                         uint32_t vis = __ballot_sync(0xffffffffu, c0 != kSkip || c1 != kSkip);
                         while (vis && ok) {
@@ -526,6 +558,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             if (qt >= 0) q = load_tile(p.qtiles, qt);
             const bool valid = qt >= 0 && tok < q.len;
             const int qpos = tok < q.split ? q.pos0 + tok : q.pos1 + (tok - q.split);
+            // interval masks: this row's key bounds (an empty interval for padding rows)
+            int rlo = 1, rhi = 0;
+            if (kBounds && valid) {
+                rlo = __ldg(p.key_lo + qpos);
+                rhi = __ldg(p.key_hi + qpos);
+            }
             float m_run = -INFINITY, l_run = 0.f;
             uint32_t nd = 0;  // this item's
             for (;;) {
@@ -555,16 +593,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                     // from the window)
                     const int kt_len = e.y & 0xffff, kt_split = e.y >> 16, kt_pos0 = e.z, kt_pos1 = e.w;
                     int lim1, lim2, lo1 = 0, lo2 = kt_split;
-                    if (p.causal) {
-                        lim1 = min(max(qpos - kt_pos0 + 1, 0), kt_split);
-                        lim2 = min(max(qpos - kt_pos1 + kt_split + 1, kt_split), kt_len);
+                    if (kBounds) {  // keys at positions [rlo, rhi]
+                        lim1 = min(max(rhi - kt_pos0 + 1, 0), kt_split);
+                        lim2 = min(max(rhi - kt_pos1 + kt_split + 1, kt_split), kt_len);
+                        lo1 = min(max(rlo - kt_pos0, 0), kt_split);
+                        lo2 = min(max(rlo - kt_pos1 + kt_split, kt_split), kt_len);
                     } else {
-                        lim1 = kt_split;
-                        lim2 = kt_len;
-                    }
-                    if (kWindow) {
-                        lo1 = min(max(qpos - p.window - kt_pos0, 0), kt_split);
-                        lo2 = min(max(qpos - p.window - kt_pos1 + kt_split, kt_split), kt_len);
+                        if (p.causal) {
+                            lim1 = min(max(qpos - kt_pos0 + 1, 0), kt_split);
+                            lim2 = min(max(qpos - kt_pos1 + kt_split + 1, kt_split), kt_len);
+                        } else {
+                            lim1 = kt_split;
+                            lim2 = kt_len;
+                        }
+                        if (kWindow) {
+                            lo1 = min(max(qpos - p.window - kt_pos0, 0), kt_split);
+                            lo2 = min(max(qpos - p.window - kt_pos1 + kt_split, kt_split), kt_len);
+                        }
                     }
 #pragma unroll
                     for (int ch = 0; ch < 4; ++ch) {
@@ -764,6 +809,11 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
     p.t1 = a.t1;
     p.causal = a.causal;
     p.window = a.window;
+    if ((a.qbounds != nullptr) != (a.key_lo != nullptr) || (a.key_lo != nullptr) != (a.key_hi != nullptr))
+        return cudaErrorInvalidValue;
+    p.qbounds = static_cast<const int4 *>(a.qbounds);
+    p.key_lo = a.key_lo;
+    p.key_hi = a.key_hi;
     p.out_mode = a.out_mode;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     p.out = a.out;
@@ -775,7 +825,8 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 128 && !attr_set[dev]) {
-        for (const void *fn : {(const void *)tc_fwd_kernel<false>, (const void *)tc_fwd_kernel<true>}) {
+        for (const void *fn : {(const void *)tc_fwd_kernel<0>, (const void *)tc_fwd_kernel<1>,
+                               (const void *)tc_fwd_kernel<2>}) {
             cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess) return e;
             // The setmaxnreg split (128 x 80 + 256 x 200) needs the CTA to be
@@ -797,10 +848,12 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
         sm_count[dev] = n > 0 ? n : 1;
     }
     const int grid = std::min(a.n_items, (dev >= 0 && dev < 128) ? sm_count[dev] : 1);
-    if (p.window >= 0)
-        tc_fwd_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(p);
+    if (p.qbounds)
+        tc_fwd_kernel<2><<<grid, kThreads, kSmemBytes, st>>>(p);
+    else if (p.window >= 0)
+        tc_fwd_kernel<1><<<grid, kThreads, kSmemBytes, st>>>(p);
     else
-        tc_fwd_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(p);
+        tc_fwd_kernel<0><<<grid, kThreads, kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 

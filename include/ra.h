@@ -276,6 +276,48 @@ ra_status ra_ring_attn_bwd(const void *q, const void *k, const void *v, int dtyp
                            void *workspace, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * ra_ring_attn_fwd_masked / ra_ring_attn_bwd_masked  (DEVICE tensors, HOST
+ * cu_seqlens and bounds)
+ *
+ * The ring of ra_ring_attn_fwd / bwd under an interval mask instead of the
+ * causal flag and the window: the dynamic, per-token attention masks that
+ * "[Train] Support custom attention with context parallel" (FlagScale PR
+ * #910, description) adds to context parallelism through flex attention,
+ * in the form of one key interval per query token:
+ *   query i sees key j  iff  same document  and  key_lo[i] <= j <= key_hi[i]
+ * (original token indices).  This holds causal (lo = document start,
+ * hi = i), sliding-window, chunked-local, prefix-LM (hi = max(i, end of
+ * the prefix)) and bidirectional document masks.
+ *   key_lo, key_hi HOST int32 [T]: both non-decreasing inside every
+ *                  document (else RA_ERR_INVALID_ARG), values in
+ *                  (-2^30, 2^30); a row with no key inside its interval
+ *                  gets output 0 and lse -inf.
+ * Fully masked tile pairs are skipped and fully visible ones run unmasked:
+ * the block map comes from each query tile's bound extremes (the pruning
+ * of the same PR).  Everything else is as in ra_ring_attn_fwd / bwd, with
+ * these limits: the tensor-core path only (bf16, d = 128, Hq / Hkv a power
+ * of two <= 16) and the RA_SCHED_FUSED or RA_SCHED_ALLGATHER schedule
+ * (otherwise RA_ERR_UNSUPPORTED).  The plan (and so the workspace size)
+ * depends on the bounds: size the workspace with
+ * ra_ring_workspace_bytes_masked for the same bounds.
+ * ------------------------------------------------------------------------ */
+size_t ra_ring_workspace_bytes_masked(int64_t T, int Hq, int Hkv, int d, int dtype,
+                                      const int32_t *cu_seqlens, int B, int cp, int zz_mode,
+                                      const int32_t *key_lo, const int32_t *key_hi, int sched, int bwd);
+ra_status ra_ring_attn_fwd_masked(const void *q, const void *k, const void *v, int dtype,
+                                  int64_t T, int Hq, int Hkv, int d,
+                                  const int32_t *cu_seqlens, int B, int cp, int zz_mode,
+                                  const int32_t *key_lo, const int32_t *key_hi, float scale, int sched,
+                                  void *out, float *lse, void *workspace, size_t ws_bytes, void *stream);
+ra_status ra_ring_attn_bwd_masked(const void *q, const void *k, const void *v, int dtype,
+                                  int64_t T, int Hq, int Hkv, int d,
+                                  const int32_t *cu_seqlens, int B, int cp, int zz_mode,
+                                  const int32_t *key_lo, const int32_t *key_hi, float scale, int sched,
+                                  const void *out, const float *lse, const void *dout,
+                                  void *dq, void *dk, void *dv, int grad_dtype, int flags,
+                                  void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * ra_ring_rank_pairs  (HOST, synchronous)
  *
  * Allowed (query, key) pairs each simulated rank computes over the whole
@@ -320,6 +362,11 @@ ra_status ra_ring_rank_pairs(const int32_t *cu_seqlens, int B, int cp, int zz_mo
 #define RA_PLAN_STATS_N 19
 ra_status ra_ring_plan_stats(const int32_t *cu_seqlens, int B, int cp, int zz_mode, int G, int Hkv, int causal,
                              int window, int sched, int exact, int n_sm, int64_t *stats);
+/* The same statistics under an interval mask (key_lo / key_hi as in
+ * ra_ring_attn_fwd_masked; RA_SCHED_FUSED or RA_SCHED_ALLGATHER). */
+ra_status ra_ring_plan_stats_masked(const int32_t *cu_seqlens, int B, int cp, int zz_mode, int G, int Hkv,
+                                    const int32_t *key_lo, const int32_t *key_hi, int sched, int exact, int n_sm,
+                                    int64_t *stats);
 
 /* Reads and clears the device status word of the current device (waits for
  * `stream` first).  Returns RA_OK, RA_ERR_TIMEOUT or RA_ERR_DEVICE_BOUNDS. */

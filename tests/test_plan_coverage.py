@@ -99,3 +99,67 @@ def test_plan_stats_argument_checks(ra):
     assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 0, 0, 0, p(out)) == _lib.RA_ERR_INVALID_ARG  # n_sm
     assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 0, 0, 152, p(out)) == 0
     assert out[10] == -1 and out[0] > 0
+
+
+MASKS = [("causal", 0), ("window", 40), ("chunked", 64), ("prefix", 100), ("bidirectional", 0), ("random", 0)]
+
+
+@pytest.mark.parametrize("sched", ["fused", "allgather"])
+def test_interval_masks_cover_every_allowed_pair_once(ra, sched):
+    """Interval masks (per-token key bounds): every pass's visited tile
+    pairs hold each allowed pair exactly once and no "full" pair holds a
+    masked one.  The totals are the brute-force interval counts
+    (workloads.interval_pairs, pinned against dense masks in
+    test_oracle_bounds.py)."""
+    rng = np.random.default_rng(70 + (sched == "allgather"))
+    n = 0
+    for trial in range(4):
+        cu = W.cu_seqlens(W.random_doc_lens(rng, int(rng.integers(60, 1500)), 1, 500))
+        for kind, par in MASKS:
+            lo, hi = W.interval_bounds(cu, kind, par, seed=trial)
+            ref = W.interval_pairs(cu, lo, hi)
+            for cp, mode in ((1, 0), (3, 1), (8, int(rng.integers(0, 2)))):
+                G = int(rng.choice([1, 2, 4, 8, 16]))
+                st = ra.ring_plan_stats(cu, cp, mode, G, 2, sched=sched, exact=True, key_lo=lo, key_hi=hi)
+                case = (sched, kind, list(np.diff(cu)), cp, mode, G)
+                assert st["fwd_allowed"] == st["dkdv_allowed"] == st["dq_allowed"] == ref, case
+                assert st["full_disallowed"] == 0, case
+                assert st["fwd_visited"] == st["dq_visited"] == st["dkdv_visited"], case
+                n += 1
+    assert n == 4 * len(MASKS) * 3
+
+
+def test_causal_intervals_plan_like_the_causal_mask(ra):
+    """Bounds that spell out the causal mask (document start to the query)
+    give the block map of the causal plan: the same visited, full and
+    capacity counts on the packed workload."""
+    wl = W.C2
+    cu = wl.cu_seqlens()
+    lo, hi = W.interval_bounds(cu, "causal")
+    for sched in ("fused", "allgather"):
+        a = ra.ring_plan_stats(cu, wl.cp, wl.zz_mode, 4, 8, True, -1, sched)
+        b = ra.ring_plan_stats(cu, wl.cp, wl.zz_mode, 4, 8, sched=sched, key_lo=lo, key_hi=hi)
+        for key in ("fwd_visited", "fwd_full", "fwd_capacity", "dkdv_visited", "dq_visited", "fwd_items"):
+            assert a[key] == b[key], (sched, key)
+
+
+def test_interval_mask_argument_checks(ra):
+    """Host-side refusals, before any device work: bounds that decrease
+    inside a document, fp32 (no tensor-core path), the stepwise schedule."""
+    import ctypes
+    L = ra.lib()
+    cu = W.cu_seqlens((50, 30))
+    T = 80
+    lo, hi = W.interval_bounds(cu, "causal")
+    bad = hi.copy()
+    bad[10] = bad[9] - 1
+    P = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    assert L.ra_ring_workspace_bytes_masked(T, 8, 2, 128, 0, P(cu), 2, 2, 1, P(lo), P(hi), 0, 0) > 0
+    assert L.ra_ring_workspace_bytes_masked(T, 8, 2, 128, 0, P(cu), 2, 2, 1, P(lo), P(bad), 0, 0) == 0
+    fake = ctypes.c_void_p(256)
+    args = lambda dt, l, h, sched: (fake, fake, fake, dt, T, 8, 2, 128, P(cu), 2, 2, 1, P(l), P(h), 0.1, sched,
+                                    fake, fake, fake, 1 << 30, None)
+    assert L.ra_ring_attn_fwd_masked(*args(0, lo, bad, 0)) == 1  # RA_ERR_INVALID_ARG
+    assert b"non-decreasing" in L.ra_last_error()
+    assert L.ra_ring_attn_fwd_masked(*args(1, lo, hi, 0)) == 2   # fp32: RA_ERR_UNSUPPORTED
+    assert L.ra_ring_attn_fwd_masked(*args(0, lo, hi, 1)) == 2   # stepwise: RA_ERR_UNSUPPORTED
