@@ -487,6 +487,46 @@ def stepwise_lines(ra, torch, dev, wl, steps, warmup, peak, q, k, v, do):
 
 
 
+def masked_lines(ra, torch, dev, wl, steps, warmup, peak, q, k, v, do, specs):
+    """Interval masks (per-token key bounds, workloads.interval_bounds) on
+    the same data: the fused ring's fwd+bwd step and forward, TFLOP/s over
+    the mask's allowed pairs."""
+    cu = wl.cu_seqlens()
+    T, hq, hkv, d = wl.T, wl.hq, wl.hkv, wl.d
+    res = {}
+    for spec in specs:
+        kind, _, par = spec.partition(":")
+        lo, hi = W.interval_bounds(cu, kind, int(par or 0))
+        pairs = W.interval_pairs(cu, lo, hi)
+        kw = dict(key_lo=lo, key_hi=hi)
+        nb = max(ra.ring_workspace_bytes(T, hq, hkv, d, 0, cu, wl.cp, wl.zz_mode, "fused", bwd=b, **kw)
+                 for b in (False, True))
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        out, lse = torch.empty_like(q), torch.empty((hq, T), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def fwd():
+            ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, scale=wl.scale, out=out, lse=lse, workspace=ws, **kw)
+
+        def step():
+            fwd()
+            ra.ring_attn_bwd(q, k, v, out, lse, do, cu, wl.cp, wl.zz_mode, scale=wl.scale, dq=dq, dk=dk, dv=dv,
+                             workspace=ws, reuse_fwd_workspace=True, **kw)
+
+        stream = torch.cuda.current_stream(dev)
+        ms_step = time_calls(step, steps, warmup, stream, torch)
+        ms_fwd = time_calls(fwd, steps, warmup, stream, torch)
+        assert ra.device_status() == 0
+        tf = 14 * d * hq * pairs / (ms_step / 1e3) / 1e12
+        tff = 4 * d * hq * pairs / (ms_fwd / 1e3) / 1e12
+        res[spec] = {"allowed_pairs_per_head": pairs, "ms_per_step": ms_step, "tflops": tf, "frac_of_peak": tf / peak,
+                     "fwd": {"ms": ms_fwd, "tflops": tff, "frac_of_peak": tff / peak}}
+        del ws, out, lse, dq, dk, dv
+        torch.cuda.empty_cache()
+    return res
+
+
+
 def fwd_configs(args, ra, torch):
     """Forward-only TFLOP/s of the named workloads on one GPU (CUDA events on
     the launching stream, W warm-up calls, K timed calls; every input is far
@@ -725,6 +765,8 @@ def main():
         extras["fwd_configs"] = fwd_lines(ra, torch, dev, ["C1", "C3"], args.steps, args.warmup, peak_burst)
         extras["stepwise"] = stepwise_lines(ra, torch, dev, wl, args.steps, args.warmup, peak_burst, q, k, v, do)
         extras["bandwidth_kernels"] = bandwidth_kernels(ra, torch, dev, wl, args.steps, args.warmup, hbm)
+        extras["interval_masks"] = masked_lines(ra, torch, dev, wl, args.steps, args.warmup, peak_burst, q, k, v, do,
+                                                ["prefix:512", "chunked:1024"])
         barrier()
 
     # ---- end to end through the public API with host buffers.  Every step
