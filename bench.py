@@ -274,7 +274,7 @@ def time_calls(fn, steps, warmup, stream, torch):
     return e0.elapsed_time(e1) / steps
 
 
-def bandwidth_kernels(ra, torch, dev, wl, steps, warmup, hbm):
+def bandwidth_kernels(ra, torch, dev, wl, steps, warmup, hbm, merge_parts=None):
     """The HBM-bound kernels of the path at full size on the packed
     32768-token workload, each as algorithmic bytes (every byte the
     operation must read and write once) over its CUDA-event time:
@@ -310,7 +310,7 @@ def bandwidth_kernels(ra, torch, dev, wl, steps, warmup, hbm):
     nb = 2 * q.numel() * q.element_size()
     res["unpermute_o"] = {"ms": ms, "bytes": nb, "gbs": nb / ms / 1e6, "frac": nb / ms / 1e6 / hbm}
     del yk, yv
-    n = wl.cp
+    n = merge_parts or wl.cp
     g = torch.Generator(device=dev).manual_seed(5)
     parts = [torch.randn((T, hq, d), generator=g, device=dev, dtype=torch.float32) for _ in range(n)]
     lses = [torch.randn((hq, T), generator=g, device=dev, dtype=torch.float32) * 3 for _ in range(n)]
@@ -527,6 +527,82 @@ def masked_lines(ra, torch, dev, wl, steps, warmup, peak, q, k, v, do, specs):
 
 
 
+def cpu_configs(args):
+    """The fp64 oracle on the host cores, per workload: the forward of the
+    8192-token sequence and of the packed 32768-token workload in full, the
+    131072-token sequence on a fixed sample of query rows (every chunk
+    boundary row of its zigzag split plus seeded random rows, all 64 heads;
+    the whole run extrapolated by allowed pairs and labelled so), each on
+    all cores and on one core (one core: a smaller sample, extrapolated).
+    One JSON line per measurement; host only."""
+    import oracle
+    oracle.build()
+    ncores = os.cpu_count() or 1
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    def line(name, threads, sec, flops, sample, full_flops):
+        rate = flops / sec / 1e12
+        print(json.dumps({"cpu_config": name, "cores": threads, "sec": sec, "tflops": rate, "sample": sample,
+                          "full_sec_extrapolated": None if flops == full_flops else sec * full_flops / flops}),
+              flush=True)
+
+    for name, n_all in (("C1", None), ("C2", 2048)):
+        wl = W.ALL[name]
+        cu = wl.cu_seqlens()
+        q, k, v = W.make_qkv(wl.T, wl.hq, wl.hkv, wl.d, wl.dtype)
+        full = 4 * wl.d * wl.hq * pairs_of(cu)
+        seg = oracle.doc_ids(cu)
+        pos = np.arange(wl.T)
+
+        def row_pairs(rows):
+            return int(sum(r - cu[np.searchsorted(cu, r, side="right") - 1] + 1 for r in rows))
+
+        oracle.set_threads(ncores)
+        if n_all is None:
+            sec = timed(lambda: oracle.attn_fwd(q, k, v, cu, True, wl.scale))
+            line(name + " fwd", ncores, sec, full, "whole workload", full)
+        else:
+            rows = W.sample_rows(wl.T, n_all, 4, list(cu[:-1]))
+            sec = timed(lambda: oracle.partial_fwd(q[torch_index(rows)], k, v, seg[rows], seg, rows, pos, True,
+                                                   wl.scale))
+            line(name + " fwd", ncores, sec, 4 * wl.d * wl.hq * row_pairs(rows),
+                 f"{len(rows)} query rows of {wl.T} (document starts and seeded rows, all {wl.hq} heads)", full)
+        # one core: a fixed sample of 64 query rows of all heads
+        rows = W.sample_rows(wl.T, 64, 5, list(cu[:-1]))
+        oracle.set_threads(1)
+        sec1 = timed(lambda: oracle.partial_fwd(q[torch_index(rows)], k, v, seg[rows], seg, rows, pos, True, wl.scale))
+        oracle.set_threads(ncores)
+        line(name + " fwd", 1, sec1, 4 * wl.d * wl.hq * row_pairs(rows),
+             f"{len(rows)} query rows of {wl.T} (all {wl.hq} heads)", full)
+    wl = W.C3
+    cu = wl.cu_seqlens()
+    q, k, v = W.make_qkv(wl.T, wl.hq, wl.hkv, wl.d, wl.dtype)
+    n = 2 * wl.cp
+    bounds = [c * wl.T // n for c in range(1, n)]
+    rows = W.sample_rows(wl.T, 256, 6, bounds + [b - 1 for b in bounds] + [0, wl.T - 1])
+    seg = oracle.doc_ids(cu)
+    pos = np.arange(wl.T)
+    row_pairs = int((rows + 1).sum())
+    full = 4 * wl.d * wl.hq * pairs_of(cu)
+    for threads, rr in ((ncores, rows), (1, rows[::16])):
+        oracle.set_threads(threads)
+        rp = int((rr + 1).sum())
+        sec = timed(lambda: oracle.partial_fwd(q[torch_index(rr)], k, v, seg[rr], seg, rr, pos, True, wl.scale))
+        line("C3 fwd", threads, sec, 4 * wl.d * wl.hq * rp,
+             f"{len(rr)} query rows of {wl.T} (zigzag chunk boundaries and seeded rows, all {wl.hq} heads)", full)
+    oracle.set_threads(ncores)
+
+
+def torch_index(rows):
+    import torch
+    return torch.from_numpy(np.asarray(rows, dtype=np.int64))
+
+
+
 def fwd_configs(args, ra, torch):
     """Forward-only TFLOP/s of the named workloads on one GPU (CUDA events on
     the launching stream, W warm-up calls, K timed calls; every input is far
@@ -622,12 +698,21 @@ def main():
                     help="host-only study of per-rank causal load under CP sharding policies (JSON lines)")
     ap.add_argument("--window", type=int, default=-1,
                     help="sliding window (a key at most this many positions behind its query); -1: none")
+    ap.add_argument("--cpu-configs", action="store_true",
+                    help="host only: the fp64 oracle's time per workload on all cores and on one core (JSON lines)")
+    ap.add_argument("--bandwidth", action="store_true",
+                    help="only the HBM-bound kernels at full size (permute, unpermute, LSE merge): one JSON line")
+    ap.add_argument("--merge-parts", type=int, default=0,
+                    help="partials merged by --bandwidth (default: the workload's CP size)")
     ap.add_argument("--fwd-configs", default="",
                     help="comma list of forward-only workloads (e.g. C1,C2,C3) to time instead of the "
                          "fwd+bwd step; one JSON line each (not the headline line)")
     args = ap.parse_args()
     if args.balance:
         balance_study(args)
+        return
+    if args.cpu_configs:
+        cpu_configs(args)
         return
     if args.impl == "reference":
         reference_arm(args)
@@ -640,6 +725,14 @@ def main():
 
     if args.fwd_configs:
         fwd_configs(args, ra, torch)
+        return
+    if args.bandwidth:
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        res = bandwidth_kernels(ra, torch, dev, W.C2, args.steps, args.warmup, peaks()[2],
+                                merge_parts=args.merge_parts or None)
+        print(json.dumps({"bandwidth_kernels": res, "workload": W.C2.name, "steps": args.steps,
+                          "warmup": args.warmup}), flush=True)
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
