@@ -17,7 +17,8 @@ from ._lib import (RA_BF16, RA_BWD_FWD_RESERVE, RA_FP32, RA_SCHED_ALLGATHER, RA_
                    RA_ZZ_GLOBAL, RA_ZZ_PER_DOC, RaError, check, lib)
 
 __all__ = [
-    "zigzag_plan", "zigzag_permute", "zigzag_unpermute", "varlen_attn_partial", "lse_merge",
+    "zigzag_plan", "zigzag_permute", "zigzag_unpermute", "varlen_attn_partial", "varlen_attn_partial_dev",
+    "lse_merge",
     "ring_attn_fwd", "ring_attn_bwd", "ring_rank_pairs", "ring_plan_stats", "device_status", "selftest_wait_timeout",
     "RA_ZZ_GLOBAL", "RA_ZZ_PER_DOC", "RA_SCHED_FUSED", "RA_SCHED_STEPWISE", "RA_SCHED_ALLGATHER", "RaError",
 ]
@@ -161,6 +162,36 @@ def varlen_attn_partial(q, k, v, cu_seqlens_q, cu_seqlens_k, q_pos=None, k_pos=N
                                    _np_ptr(kp) if kp is not None else None, int(causal), int(window), scale, _ptr(out),
                                    _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device)),
           "ra_varlen_attn_partial")
+    return out, lse
+
+
+def varlen_attn_partial_dev(q, k, v, cu_seqlens_q, cu_seqlens_k, q_pos=None, k_pos=None, causal: bool = True,
+                            scale: float | None = None, out=None, lse=None, window: int = -1, workspace=None):
+    """varlen_attn_partial with the segment boundaries and positions as int32
+    tensors on q's device (no host round trip; capturable).  Tensor-core
+    path only (bf16, d = 128, Hq / Hkv a power of two <= 16)."""
+    _check_cuda(q, k, v, cu_seqlens_q, cu_seqlens_k)
+    for t in (q_pos, k_pos):
+        if t is not None:
+            _check_cuda(t)
+    for t in (cu_seqlens_q, cu_seqlens_k, q_pos, k_pos):
+        if t is not None and t.dtype != torch.int32:
+            raise TypeError("segment boundaries and positions must be int32")
+    Tq, Hq, d = q.shape
+    Tk, Hkv, _ = k.shape
+    nseg = cu_seqlens_q.numel() - 1
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((Tq, Hq, d), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    L = lib()
+    ws_bytes = int(L.ra_partial_workspace_bytes(Tq, Tk, nseg, Hq, Hkv, d, _dtype_code(q)))
+    ws = workspace if workspace is not None else torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    check(L.ra_varlen_attn_partial_dev(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), Tq, Tk, Hq, Hkv, d,
+                                       _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), nseg, _ptr(q_pos), _ptr(k_pos),
+                                       int(causal), int(window), scale, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
+                                       _stream(q.device)), "ra_varlen_attn_partial_dev")
     return out, lse
 
 

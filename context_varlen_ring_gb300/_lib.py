@@ -38,7 +38,7 @@ EXPORTS = (
     "ra_status_string", "ra_last_error", "ra_version", "ra_profile_enable", "ra_profile_read",
     "ra_varlen_attn_partial_noalloc", "ra_ring_plan_stats", "ra_partial_table_bytes",
     "ra_ring_workspace_bytes_masked", "ra_ring_attn_fwd_masked", "ra_ring_attn_bwd_masked",
-    "ra_ring_plan_stats_masked",
+    "ra_ring_plan_stats_masked", "ra_varlen_attn_partial_dev",
 )
 
 _lib = None
@@ -60,6 +60,8 @@ def _declare(L):
         "ra_partial_table_bytes": (sz, [i64, i64, i32, i32, i32, i32, P, P, i32, P, P, i32, i32]),
         "ra_varlen_attn_partial": (i32, [P, P, P, i32, i64, i64, i32, i32, i32, P, P, i32, P, P, i32, i32, f32,
                                          P, P, P, sz, P]),
+        "ra_varlen_attn_partial_dev": (i32, [P, P, P, i32, i64, i64, i32, i32, i32, P, P, i32, P, P, i32, i32, f32,
+                                             P, P, P, sz, P]),
         "ra_varlen_attn_partial_noalloc": (i32, [P, P, P, i32, i64, i64, i32, i32, i32, P, P, i32, P, P, i32,
                                                  i32, f32, P, P, P]),
         "ra_lse_merge": (i32, [i32, P, P, i64, i32, i32, P, i32, P, P]),

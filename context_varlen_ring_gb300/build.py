@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libra.so")
 SOURCES = ["ra_api.cpp", "ra_plan.cpp", "ra_stats.cpp", "ra_misc.cu", "ra_simt.cu", "ra_tc_fwd.cu", "ra_tc_bwd.cu",
-           "ra_tc_dq.cu", "ra_noalloc.cu"]
+           "ra_tc_dq.cu", "ra_noalloc.cu", "ra_tile_build.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
           "-I" + os.path.join(HERE, "..", "include")]

@@ -637,6 +637,89 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
     return RA_OK;
 }
 
+ra_status ra_varlen_attn_partial_dev(const void *q, const void *k, const void *v, int dtype, int64_t Tq, int64_t Tk,
+                                     int Hq, int Hkv, int d, const int32_t *cu_q, const int32_t *cu_k, int nseg,
+                                     const int32_t *q_pos, const int32_t *k_pos, int causal, int window, float scale,
+                                     float *out, float *lse, void *workspace, size_t ws_bytes, void *stream) {
+    ra_status st = check_common(dtype, Hq, Hkv, d);
+    if (st) return st;
+    if (!tc_fwd_supported(dtype, d, Hq, Hkv))
+        return fail(RA_ERR_UNSUPPORTED, "device-array partials run on the tensor-core path (bf16, d = 128, Hq / Hkv "
+                                        "a power of two <= 16); use ra_varlen_attn_partial");
+    if (Tq < 0 || Tk < 0 || Tq > INT32_MAX || Tk > INT32_MAX) return fail(RA_ERR_INVALID_ARG, "bad Tq/Tk");
+    if (nseg < 1) return fail(RA_ERR_INVALID_ARG, "nseg must be >= 1");
+    if (!std::isfinite(scale)) return fail(RA_ERR_INVALID_ARG, "scale must be finite");
+    if (window >= (1 << 30)) window = -1;  // reaches back further than any position
+    if (window >= 0 && (Tq >= (1 << 30) || Tk >= (1 << 30)))
+        return fail(RA_ERR_UNSUPPORTED, "with a window, Tq and Tk must be < 2^30");
+    if (Tq == 0) return RA_OK;
+    if (!q || !out || !lse || !cu_q || !cu_k || (Tk > 0 && (!k || !v))) return fail(RA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned16(q) || !aligned16(out) || (Tk > 0 && (!aligned16(k) || !aligned16(v))))
+        return fail(RA_ERR_UNSUPPORTED, "tensors must be 16-byte aligned");
+    const size_t need = ra_partial_workspace_bytes(Tq, Tk, nseg, Hq, Hkv, d, dtype);
+    if (!workspace || ws_bytes < need) return fail(RA_ERR_WORKSPACE, "workspace must be >= " + std::to_string(need));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int G = Hq / Hkv;
+    const size_t qt = (size_t)Tq + nseg, kt = (size_t)Tk + nseg;
+    Carver cv(workspace);
+    DevTileArgs b{};
+    b.cu_q = cu_q;
+    b.cu_k = cu_k;
+    b.q_pos = q_pos;
+    b.k_pos = k_pos;
+    b.Tq = Tq;
+    b.Tk = Tk;
+    b.nseg = nseg;
+    b.Hkv = Hkv;
+    b.q_rows = kBM / G;
+    b.check_pos = window >= 0;
+    b.qtiles = cv.take(qt * sizeof(Tile));
+    b.kvtiles = cv.take(kt * sizeof(Tile));
+    b.q_off = static_cast<int32_t *>(cv.take(((size_t)nseg + 2) * 4));
+    b.kv_off = static_cast<int32_t *>(cv.take(((size_t)nseg + 2) * 4));
+    b.items = cv.take(((qt + 1) / 2 + nseg) * (size_t)Hkv * sizeof(WorkItem));
+    b.sched = static_cast<int *>(cv.take(64));
+    b.n_items = static_cast<int *>(cv.take(16));
+    b.q_cnt = static_cast<int32_t *>(cv.take((size_t)nseg * 4));
+    b.k_cnt = static_cast<int32_t *>(cv.take((size_t)nseg * 4));
+    b.pair_off = static_cast<int32_t *>(cv.take(((size_t)nseg + 1) * 4));
+    if (cv.used > ws_bytes) return fail(RA_ERR_WORKSPACE, "internal: device tables exceed the workspace bound");
+    {
+        ProfScope ps("ra_tile_build", s);
+        RA_CUDA(launch_tile_build(b, s), "tile build launch");
+    }
+    TcFwdArgs a{};
+    a.q = q;
+    a.k = k ? k : q;
+    a.v = v ? v : q;
+    a.Tq = Tq;
+    a.Tk = Tk;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = G;
+    a.qtiles = b.qtiles;
+    a.kvtiles = b.kvtiles;
+    a.kv_off = b.kv_off;
+    a.items = b.items;
+    a.sched = b.sched;
+    a.n_items = INT32_MAX;  // the count is on the device: one CTA per SM
+    a.n_items_dev = b.n_items;
+    a.cp = 1;
+    a.B = nseg;
+    a.t0 = 0;
+    a.t1 = 1;
+    a.causal = causal;
+    a.window = window;
+    a.scale = scale;
+    a.out_mode = kOutPartial;
+    a.out = out;
+    a.lse = lse;
+    a.lse_T = Tq;
+    ProfScope ps("ra_tc_fwd", s);
+    RA_CUDA(launch_tc_fwd(a, s), "tensor-core partial launch");
+    return RA_OK;
+}
+
 // ---------------------------------------------------------------- ring
 namespace {
 

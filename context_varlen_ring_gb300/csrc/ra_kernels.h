@@ -125,7 +125,8 @@ struct TcFwdArgs {
     const int32_t *kv_off;             // [cp*(B+1)+1]
     const void *items;                 // WorkItem records
     int *sched;                        // [2] work counter, zero before the first launch
-    int n_items;
+    int n_items;                       // item count (an upper bound when n_items_dev is given)
+    const int *n_items_dev;            // nullable: the item count in device memory
     int cp, B;
     int t0, t1;                        // >= 0: override every item's step range
     int causal;
@@ -192,6 +193,26 @@ struct TcDqArgs {
     int out_mode;
 };
 cudaError_t launch_tc_dq(const TcDqArgs &a, cudaStream_t st);
+
+// ------------------------------------------------------------ device tile tables
+// The tile tables of one partial call built on the device (ra_tile_build.cu):
+// query tiles of q_rows rows and KV tiles of 128 rows, at most two position
+// runs each, per segment; forward items (pairs of query tiles x KV heads,
+// head major), their count in *n_items and the work counter zeroed.  Tables
+// sized by the host bound (a tile holds at least one row).  Malformed
+// segment boundaries (or, with check_pos, positions outside [0, 2^30)) are
+// recorded as RA_ERR_DEVICE_BOUNDS and leave *n_items = 0.
+struct DevTileArgs {
+    const int32_t *cu_q, *cu_k;        // DEVICE [nseg + 1]
+    const int32_t *q_pos, *k_pos;      // DEVICE [Tq], [Tk]; NULL = row index
+    int64_t Tq, Tk;
+    int nseg, Hkv, q_rows, check_pos;
+    void *qtiles, *kvtiles, *items;    // Tile [Tq + nseg], Tile [Tk + nseg], WorkItem [pairs x Hkv]
+    int32_t *q_off, *kv_off;           // [nseg + 2]
+    int32_t *q_cnt, *k_cnt, *pair_off; // scratch [nseg], [nseg], [nseg + 1]
+    int *n_items, *sched;              // 1 int, 2 ints
+};
+cudaError_t launch_tile_build(const DevTileArgs &a, cudaStream_t st);
 
 // Device-wait self-test (see ra_selftest_wait_timeout).
 cudaError_t launch_wait_selftest(uint64_t budget_ns, cudaStream_t st);

@@ -81,6 +81,7 @@ struct FwdParams {
     const int4 *qtiles, *kvtiles, *items;
     const int *kv_off;
     int *sched;  // [2]: next item to claim, CTAs finished (zero between launches)
+    const int *n_items_dev;  // the item count in device memory (NULL: n_items)
     int q_direct;   // single-run query tiles are read from tmQo at their first position
     int kv_direct;  // single-run KV tiles likewise from tmKo / tmVo
     int n_items, cp, B, G, log2G, Hq;
@@ -242,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             // K and V through the ring.
             uint32_t u = 0, jt = 0;
             int ok = 1, n_q = 0;
+            const int n_items = p.n_items_dev ? *p.n_items_dev : p.n_items;
             auto publish = [&](int4 v) -> int {  // lane 0
                 const uint32_t e = jt % kRing;
                 if (!mbar_wait(info_empty + e, ((jt / kRing) & 1u) ^ 1u, wc)) return 0;
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 int item = 0;
                 if (lane == 0) item = atomicAdd(p.sched, 1);
                 item = __shfl_sync(0xffffffffu, item, 0);
-                if (item >= p.n_items) {
+                if (item < 0 || item >= n_items) {  // (a claim outside the list ends the walk)
                     if (lane == 0) ok = publish(make_int4(kDone, 0, 0, 0));
                     ++jt;
                     break;
@@ -798,6 +800,7 @@ cudaError_t launch_tc_fwd(const TcFwdArgs &a, cudaStream_t st) {
     p.kv_off = a.kv_off;
     p.sched = a.sched;
     p.n_items = a.n_items;
+    p.n_items_dev = a.n_items_dev;
     p.cp = a.cp;
     p.B = a.B;
     p.G = G;

@@ -144,6 +144,32 @@ ra_status ra_varlen_attn_partial(const void *q, const void *k, const void *v, in
                                  void *workspace, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * ra_varlen_attn_partial_dev  (DEVICE tensors and DEVICE segment/position
+ * arrays)
+ *
+ * ra_varlen_attn_partial with cu_seqlens_q, cu_seqlens_k [nseg+1], q_pos
+ * [Tq] and k_pos [Tk] (NULL = the local row index) in DEVICE memory, as a
+ * ring step holds them: the tile tables are built on the GPU (one small
+ * kernel, the host planner's tiling row for row) ahead of the tensor-core
+ * kernel, so the call makes no host round trip and can be captured in a
+ * CUDA graph.  Same allowed pairs, results and workspace bound
+ * (ra_partial_workspace_bytes) as ra_varlen_attn_partial; with the same
+ * inputs the results are bit-identical to it.  Tensor-core path only
+ * (bf16, d = 128, Hq / Hkv a power of two <= 16; else RA_ERR_UNSUPPORTED).
+ * The device arrays are checked on the device: segment boundaries that do
+ * not start at 0, decrease, or do not end at Tq / Tk (and, with a window,
+ * positions outside [0, 2^30)) are recorded as RA_ERR_DEVICE_BOUNDS in the
+ * status word (ra_get_device_status) and leave out / lse unwritten.
+ * ------------------------------------------------------------------------ */
+ra_status ra_varlen_attn_partial_dev(const void *q, const void *k, const void *v, int dtype,
+                                     int64_t Tq, int64_t Tk, int Hq, int Hkv, int d,
+                                     const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int nseg,
+                                     const int32_t *q_pos, const int32_t *k_pos,
+                                     int causal, int window, float scale,
+                                     float *out, float *lse,
+                                     void *workspace, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * ra_varlen_attn_partial_noalloc  (DEVICE tensors, HOST segment/position
  * arrays) -- the pages have no counterpart; this is a library convenience.
  *
