@@ -623,9 +623,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                 // row max as 8 independent chains of three-input maxima, then a tree
                 float mx8[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+                for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(s[i], s[8 + i]);
 #pragma unroll
-                for (int c = 8; c < 128; c += 16) {
+                for (int c = 16; c < 128; c += 16) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) mx8[i] = max3f(mx8[i], s[c + i], s[c + 8 + i]);
                 }
