@@ -85,7 +85,7 @@ def ring_rank_pairs(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, causal: bool 
 PLAN_STATS = ("q_tiles", "kv_tiles", "fwd_items", "dkdv_items", "dq_items", "fwd_visited", "fwd_full",
               "two_run_q_rows", "two_run_kv_rows", "fwd_capacity", "fwd_allowed", "full_disallowed",
               "dkdv_allowed", "dq_allowed", "dkdv_visited", "dq_visited",
-              "fwd_makespan", "dkdv_makespan", "dq_makespan")
+              "fwd_makespan", "dkdv_makespan", "dq_makespan", "fwd_steps")
 
 
 def ring_plan_stats(cu_seqlens, cp: int, mode: int = RA_ZZ_GLOBAL, G: int = 4, Hkv: int = 8, causal: bool = True,

@@ -116,8 +116,21 @@ void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_
     }
 }
 
-// Forward items: pairs of consecutive query tiles of one (rank, segment),
-// replicated over KV heads; backward items: one per KV tile and KV head.
+// Forward items: pairs of query tiles of one (rank, segment), replicated
+// over KV heads; backward items: one per KV tile and KV head.
+//
+// A forward item walks the union of its two query tiles' KV tiles, and a
+// KV tile that only one of them needs costs the item about as much time as
+// one that both need (the kernel's loop is set by the latency of each query
+// tile's S -> softmax -> PV chain, and the two tiles cover each other's
+// softmax only when both have products).  So the tiles of a segment are
+// paired in order of their visit counts, from the most visits down: tiles
+// with the same KV needs share items, and when the count is odd the tile
+// left alone is the one with the fewest visits.  (Pairing consecutive
+// tiles left the last one alone -- in a zigzag shard the late chunk's last
+// tile, which visits every KV tile of its document.)  A query tile's
+// result does not depend on its partner: it walks its own visited tiles in
+// the same order in any item.
 static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
     const int cp = tp.cp, B = tp.B;
     tp.items.clear();
@@ -125,54 +138,81 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
     tp.qitems.clear();
     tp.fwd_tile_pairs = 0;
     auto seg_idx = [&](int r, int b) { return r * (B + 1) + b; };
+    // visited KV tiles of query tile qi over the ring steps, and the step
+    // range [tf, tl) that holds them
+    auto q_visits = [&](int qi, int r, int b, int *tf, int *tl) {
+        int64_t c = 0;
+        *tf = cp;
+        *tl = 0;
+        for (int t = 0; t < cp; ++t) {
+            const int s = ((r - t) % cp + cp) % cp;
+            const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
+            int64_t c_t = 0;
+            for (int j = ka; j < ke; ++j) c_t += tp.pair_class(qi, j, causal, window) != kSkip;
+            if (c_t) {
+                *tf = std::min(*tf, t);
+                *tl = t + 1;
+            }
+            c += c_t;
+        }
+        if (*tf > *tl) *tf = *tl = 0;
+        return c;
+    };
+    std::vector<int> order;
+    std::vector<int64_t> cnt;
+    std::vector<int> tfs, tls;
     for (int r = 0; r < cp; ++r) {
         for (int b = 0; b < B; ++b) {
             const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
-            for (int i = qa; i < qe; i += 2) {
-                const int q1 = (i + 1 < qe) ? i + 1 : -1;
-                // the ring steps [tf, tl) span every visited KV tile: the
-                // kernels' producers scan no tile records outside them
+            const int n = qe - qa;
+            cnt.assign((size_t)n, 0);
+            tfs.assign((size_t)n, 0);
+            tls.assign((size_t)n, 0);
+            for (int i = 0; i < n; ++i) {
+                const int qi = qa + i;
+                cnt[(size_t)i] = q_visits(qi, r, b, &tfs[(size_t)i], &tls[(size_t)i]);
+                // per-query-tile items of the dQ pass
+                for (int g = 0; g < Hkv; ++g) {
+                    WorkItem w{qi, -1, g, r, b, tfs[(size_t)i], tls[(size_t)i],
+                               (int32_t)std::min<int64_t>(cnt[(size_t)i], INT32_MAX)};
+                    tp.qitems.push_back(w);
+                }
+            }
+            order.resize((size_t)n);
+            for (int i = 0; i < n; ++i) order[(size_t)i] = i;
+            std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+                if (cnt[(size_t)x] != cnt[(size_t)y]) return cnt[(size_t)x] > cnt[(size_t)y];
+                return tp.qtiles[qa + x].pmax > tp.qtiles[qa + y].pmax;
+            });
+            for (int j = 0; j < n; j += 2) {
+                const int x = order[(size_t)j];
+                const int y = j + 1 < n ? order[(size_t)j + 1] : -1;
+                const int i = qa + x, q1 = y >= 0 ? qa + y : -1;
+                // the item's steps span both tiles' visited KV tiles; its cost
+                // is the KV tiles it walks with at least one product
+                int tf = tfs[(size_t)x], tl = tls[(size_t)x];
+                if (y >= 0 && tls[(size_t)y] > tfs[(size_t)y]) {
+                    if (tl <= tf) {
+                        tf = tfs[(size_t)y];
+                        tl = tls[(size_t)y];
+                    } else {
+                        tf = std::min(tf, tfs[(size_t)y]);
+                        tl = std::max(tl, tls[(size_t)y]);
+                    }
+                }
                 int64_t cost = 0;
-                int tf = cp, tl = 0;
-                for (int t = 0; t < cp; ++t) {
+                for (int t = tf; t < tl; ++t) {
                     const int s = ((r - t) % cp + cp) % cp;
                     const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
-                    int64_t c_t = 0;
-                    for (int j = ka; j < ke; ++j) {
-                        c_t += tp.pair_class(i, j, causal, window) != kSkip;
-                        if (q1 >= 0) c_t += tp.pair_class(q1, j, causal, window) != kSkip;
+                    for (int k = ka; k < ke; ++k) {
+                        cost += tp.pair_class(i, k, causal, window) != kSkip;
+                        if (q1 >= 0) cost += tp.pair_class(q1, k, causal, window) != kSkip;
                     }
-                    if (c_t) {
-                        tf = std::min(tf, t);
-                        tl = t + 1;
-                    }
-                    cost += c_t;
                 }
-                if (tf > tl) tf = tl = 0;
+                if (tf >= tl) tf = tl = 0;
                 for (int g = 0; g < Hkv; ++g) {
                     WorkItem w{i, q1, g, r, b, tf, tl, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
                     tp.items.push_back(w);
-                }
-                // per-query-tile items of the dQ pass
-                for (int qi = i; qi <= (q1 >= 0 ? q1 : i); ++qi) {
-                    int64_t qc = 0;
-                    int qf = cp, ql = 0;
-                    for (int t = 0; t < cp; ++t) {
-                        const int s2 = ((r - t) % cp + cp) % cp;
-                        const int ka = tp.kv_off[seg_idx(s2, b)], ke = tp.kv_off[seg_idx(s2, b) + 1];
-                        int64_t c_t = 0;
-                        for (int j = ka; j < ke; ++j) c_t += tp.pair_class(qi, j, causal, window) != kSkip;
-                        if (c_t) {
-                            qf = std::min(qf, t);
-                            ql = t + 1;
-                        }
-                        qc += c_t;
-                    }
-                    if (qf > ql) qf = ql = 0;
-                    for (int g = 0; g < Hkv; ++g) {
-                        WorkItem w{qi, -1, g, r, b, qf, ql, (int32_t)std::min<int64_t>(qc, INT32_MAX)};
-                        tp.qitems.push_back(w);
-                    }
                 }
                 tp.fwd_tile_pairs += cost * Hkv;
             }

@@ -83,6 +83,9 @@ static ra_status plan_stats_impl(const int32_t *cu, int B, int cp, int mode, int
         for (int t = w.t0; t < w.t1; ++t) {
             const int s = ((w.r - t) % cp + cp) % cp;
             for (int j = tp.kv_off[seg(s, w.b)]; j < tp.kv_off[seg(s, w.b) + 1]; ++j) {
+                if (w.g == 0 && (tp.pair_class(w.qt0, j, causal, window) != kSkip ||
+                                 (w.qt1 >= 0 && tp.pair_class(w.qt1, j, causal, window) != kSkip)))
+                    ++stats[19];
                 for (int qt : {w.qt0, w.qt1}) {
                     if (qt < 0) continue;
                     const int c = tp.pair_class(qt, j, causal, window);

@@ -382,10 +382,12 @@ ra_status ra_ring_rank_pairs(const int32_t *cu_seqlens, int B, int cp, int zz_mo
  *   [16] forward (persistent CTAs claiming items in order)
  *   [17] dK/dV (one CTA per item, dispatched in order as SMs free up)
  *   [18] dQ (persistent CTAs, static stride over the items)
+ *   [19] forward KV steps: KV tiles the forward items of one KV head walk
+ *        with a product of either query tile ([5] counts one per query tile)
  * A correct plan covers each allowed pair once in every pass: [10], [12]
  * and [13] equal the sum of ra_ring_rank_pairs, and [11] is 0.
  * ------------------------------------------------------------------------ */
-#define RA_PLAN_STATS_N 19
+#define RA_PLAN_STATS_N 20
 ra_status ra_ring_plan_stats(const int32_t *cu_seqlens, int B, int cp, int zz_mode, int G, int Hkv, int causal,
                              int window, int sched, int exact, int n_sm, int64_t *stats);
 /* The same statistics under an interval mask (key_lo / key_hi as in

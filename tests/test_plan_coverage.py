@@ -63,6 +63,55 @@ def test_packed_workload_tiling(ra, orc):
         assert st["q_tiles"] == 1080 and st["two_run_q_rows"] == 3174
     assert ring["kv_tiles"] == 328 and ag["kv_tiles"] == 265
     assert ring["two_run_kv_rows"] == 10938 and ag["two_run_kv_rows"] == 0
+    # forward items pair the query tiles of a segment by visit count: the
+    # KV steps they walk match a separate restatement of the tiling and the
+    # pairing (11 236 per KV head; consecutive pairs would walk 11 768)
+    assert ring["fwd_steps"] == _ring_fwd_steps(np.diff(cu), wl.cp, 128 // (wl.hq // wl.hkv)) == 11236
+    assert _ring_fwd_steps(np.diff(cu), wl.cp, 128 // (wl.hq // wl.hkv), pair_sorted=False) == 11768
+    for st in (ring, ag):
+        assert 2 * st["fwd_steps"] >= st["fwd_visited"]
+
+
+def _runs_tiles(pos, rows):
+    """Greedy tiles of at most `rows` positions and at most two runs of
+    consecutive positions (the planner's rule), as arrays of positions."""
+    out, i, n = [], 0, len(pos)
+    while i < n:
+        s = i
+        i += 1
+        while i < n and i - s < rows and pos[i] == pos[i - 1] + 1:
+            i += 1
+        if i < n and i - s < rows:
+            i += 1
+            while i < n and i - s < rows and pos[i] == pos[i - 1] + 1:
+                i += 1
+        out.append(np.asarray(pos[s:i]))
+    return out
+
+
+def _ring_fwd_steps(lens, cp, q_tokens, pair_sorted=True):
+    """KV tiles walked by the causal ring forward's items of one KV head:
+    per document and rank, the rank's two zigzag chunks (floor(c*L/2cp)
+    bounds) cut into query tiles of q_tokens and KV tiles of 128; a query
+    tile needs every KV tile of its document (all ranks) starting at or
+    before its last position; tiles of a segment paired by need, largest
+    first (or consecutively); an item walks the union of its pair's needs."""
+    steps = 0
+    for L in (int(x) for x in lens):
+        n = 2 * cp
+        bnd = [c * L // n for c in range(n + 1)]
+        shards = [list(range(bnd[r], bnd[r + 1])) + list(range(bnd[n - 1 - r], bnd[n - r])) for r in range(cp)]
+        kmin = np.array([t.min() for sh in shards for t in _runs_tiles(sh, 128)])
+        for sh in shards:
+            qt = _runs_tiles(sh, q_tokens)
+            need = [kmin <= t.max() for t in qt]
+            idx = list(range(len(qt)))
+            if pair_sorted:
+                idx.sort(key=lambda i: (int(need[i].sum()), int(qt[i].max())), reverse=True)
+            for j in range(0, len(idx), 2):
+                u = need[idx[j]] | (need[idx[j + 1]] if j + 1 < len(idx) else False)
+                steps += int(u.sum())
+    return steps
     assert ag["fwd_capacity"] < ring["fwd_capacity"]
     assert ref / ag["fwd_capacity"] > 0.9 > ref / ring["fwd_capacity"] > 0.75
 
@@ -90,7 +139,7 @@ def test_plan_stats_argument_checks(ra):
     from context_varlen_ring_gb300 import _lib
     L = _lib.lib()
     cu = np.array([0, 100], np.int32)
-    out = np.zeros(19, np.int64)
+    out = np.zeros(20, np.int64)
     p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
     assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 4, 2, 1, -1, 7, 0, 152, p(out)) == _lib.RA_ERR_INVALID_ARG  # schedule
     assert L.ra_ring_plan_stats(p(cu), 1, 2, 0, 3, 2, 1, -1, 0, 0, 152, p(out)) == _lib.RA_ERR_INVALID_ARG  # G
