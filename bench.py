@@ -529,13 +529,14 @@ def masked_lines(ra, torch, dev, wl, steps, warmup, peak, q, k, v, do, specs):
 
 
 def cpu_configs(args):
-    """The fp64 oracle on the host cores, per workload: the forward of the
-    8192-token sequence and of the packed 32768-token workload in full, the
-    131072-token sequence on a fixed sample of query rows (every chunk
-    boundary row of its zigzag split plus seeded random rows, all 64 heads;
-    the whole run extrapolated by allowed pairs and labelled so), each on
-    all cores and on one core (one core: a smaller sample, extrapolated).
-    One JSON line per measurement; host only."""
+    """The fp64 oracle on the host cores, per workload: the 128-token fp32
+    batch, the forward of the 8192-token sequence and of the packed
+    32768-token workload, and the fwd+bwd of the packed workload, in full;
+    the 131072-token sequence on a fixed sample of 2048 query rows (every
+    chunk boundary row of its zigzag split plus seeded random rows, all 64
+    heads; the whole run extrapolated by allowed pairs and labelled so).
+    Each on all cores, and on one core on a smaller sample (extrapolated).
+    One JSON line per measurement; host only (several minutes)."""
     import oracle
     oracle.build()
     ncores = os.cpu_count() or 1
@@ -551,7 +552,13 @@ def cpu_configs(args):
                           "full_sec_extrapolated": None if flops == full_flops else sec * full_flops / flops}),
               flush=True)
 
-    for name, n_all in (("C1", None), ("C2", 2048)):
+    oracle.set_threads(ncores)
+    wl = W.C0
+    cu = wl.cu_seqlens()
+    q, k, v = W.make_qkv(wl.T, wl.hq, wl.hkv, wl.d, wl.dtype)
+    full = 4 * wl.d * wl.hq * pairs_of(cu)
+    line("C0 fwd", ncores, timed(lambda: oracle.attn_fwd(q, k, v, cu, True, wl.scale)), full, "whole workload", full)
+    for name in ("C1", "C2"):
         wl = W.ALL[name]
         cu = wl.cu_seqlens()
         q, k, v = W.make_qkv(wl.T, wl.hq, wl.hkv, wl.d, wl.dtype)
@@ -563,15 +570,8 @@ def cpu_configs(args):
             return int(sum(r - cu[np.searchsorted(cu, r, side="right") - 1] + 1 for r in rows))
 
         oracle.set_threads(ncores)
-        if n_all is None:
-            sec = timed(lambda: oracle.attn_fwd(q, k, v, cu, True, wl.scale))
-            line(name + " fwd", ncores, sec, full, "whole workload", full)
-        else:
-            rows = W.sample_rows(wl.T, n_all, 4, list(cu[:-1]))
-            sec = timed(lambda: oracle.partial_fwd(q[torch_index(rows)], k, v, seg[rows], seg, rows, pos, True,
-                                                   wl.scale))
-            line(name + " fwd", ncores, sec, 4 * wl.d * wl.hq * row_pairs(rows),
-                 f"{len(rows)} query rows of {wl.T} (document starts and seeded rows, all {wl.hq} heads)", full)
+        sec = timed(lambda: oracle.attn_fwd(q, k, v, cu, True, wl.scale))
+        line(name + " fwd", ncores, sec, full, "whole workload", full)
         # one core: a fixed sample of 64 query rows of all heads
         rows = W.sample_rows(wl.T, 64, 5, list(cu[:-1]))
         oracle.set_threads(1)
@@ -579,17 +579,24 @@ def cpu_configs(args):
         oracle.set_threads(ncores)
         line(name + " fwd", 1, sec1, 4 * wl.d * wl.hq * row_pairs(rows),
              f"{len(rows)} query rows of {wl.T} (all {wl.hq} heads)", full)
+    # fwd+bwd of the packed workload: every document on all cores; the
+    # smallest documents up to 1M allowed pairs on one core
+    wl = W.C4
+    full = 14 * wl.d * wl.hq * pairs_of(wl.cu_seqlens())
+    tf, sec, cores, sample, sp = run_cpu_oracle(wl, steps=1, pair_budget=pairs_of(wl.cu_seqlens()))
+    line("C4 fwd+bwd", cores, sec, 14 * wl.d * wl.hq * sp, sample, full)
+    tf, sec, _, sample, sp = run_cpu_oracle(wl, steps=1, pair_budget=1_000_000, threads=1)
+    line("C4 fwd+bwd", 1, sec, 14 * wl.d * wl.hq * sp, sample, full)
     wl = W.C3
     cu = wl.cu_seqlens()
     q, k, v = W.make_qkv(wl.T, wl.hq, wl.hkv, wl.d, wl.dtype)
     n = 2 * wl.cp
     bounds = [c * wl.T // n for c in range(1, n)]
-    rows = W.sample_rows(wl.T, 256, 6, bounds + [b - 1 for b in bounds] + [0, wl.T - 1])
+    rows = W.sample_rows(wl.T, 2048, 6, bounds + [b - 1 for b in bounds] + [0, wl.T - 1])
     seg = oracle.doc_ids(cu)
     pos = np.arange(wl.T)
-    row_pairs = int((rows + 1).sum())
     full = 4 * wl.d * wl.hq * pairs_of(cu)
-    for threads, rr in ((ncores, rows), (1, rows[::16])):
+    for threads, rr in ((ncores, rows), (1, rows[::128])):
         oracle.set_threads(threads)
         rp = int((rr + 1).sum())
         sec = timed(lambda: oracle.partial_fwd(q[torch_index(rr)], k, v, seg[rr], seg, rr, pos, True, wl.scale))

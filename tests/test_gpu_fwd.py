@@ -194,7 +194,24 @@ def test_ring_c2_stepwise_sampled(ra, orc):
 
 
 def test_ring_c3_sampled(ra, orc):
-    _sampled_check(ra, orc, W.C3, 24, 3)
+    """The 131072-token sequence (CP 16): 256 query rows of all 64 heads,
+    every zigzag rank boundary among them."""
+    _sampled_check(ra, orc, W.C3, 256, 3)
+
+
+def test_ring_c2_whole_output(ra, orc):
+    """The packed 32768-token workload in the bench's configuration (fused
+    ring, CP 8, per-document zigzag): every output element and every LSE
+    against the oracle's forward of the whole workload."""
+    wl = W.C2
+    cu = wl.cu_seqlens()
+    q, k, v = W.make_qkv(wl.T, wl.hq, wl.hkv, wl.d, wl.dtype)
+    out, lse = ra.ring_attn_fwd(q.cuda(), k.cuda(), v.cuda(), cu, wl.cp, wl.zz_mode, True, wl.scale)
+    _check_status(ra)
+    ro, rl = orc.attn_fwd(q, k, v, cu, True, wl.scale)
+    err = np.abs(out.float().cpu().numpy() - ro).max()
+    assert err <= 2e-2, err
+    _cmp_lse(lse.cpu().numpy(), rl, 1e-3)
 
 
 def test_wait_guard_selftest(ra):
