@@ -199,11 +199,13 @@ def test_ring_c3_sampled(ra, orc):
     _sampled_check(ra, orc, W.C3, 256, 3)
 
 
-def test_ring_c2_whole_output(ra, orc):
-    """The packed 32768-token workload in the bench's configuration (fused
-    ring, CP 8, per-document zigzag): every output element and every LSE
-    against the oracle's forward of the whole workload."""
-    wl = W.C2
+@pytest.mark.parametrize("name", ["C1", "C2"])
+def test_ring_whole_output(ra, orc, name):
+    """The 8192-token sequence (CP 4, zigzag over the stream) and the packed
+    32768-token workload (CP 8, per-document zigzag) in the bench's
+    configuration (fused ring): every output element and every LSE against
+    the oracle's forward of the whole workload."""
+    wl = W.ALL[name]
     cu = wl.cu_seqlens()
     q, k, v = W.make_qkv(wl.T, wl.hq, wl.hkv, wl.d, wl.dtype)
     out, lse = ra.ring_attn_fwd(q.cuda(), k.cuda(), v.cuda(), cu, wl.cp, wl.zz_mode, True, wl.scale)
