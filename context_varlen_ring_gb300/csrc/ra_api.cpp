@@ -821,10 +821,18 @@ size_t ra_ring_workspace_bytes(int64_t T, int Hq, int Hkv, int d, int dtype, con
     ra_status st;
     const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
     if (sched != RA_SCHED_FUSED && sched != RA_SCHED_STEPWISE && sched != RA_SCHED_ALLGATHER) return 0;
-    // sizes are mask-independent
-    auto plan = get_ring_plan(cu, B, cp, mode, Hq / Hkv, Hkv, 1, -1, tc, tc && sched == RA_SCHED_ALLGATHER, &st);
-    if (!plan) return 0;
-    return ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, bwd).total;
+    // Only the plan's tables depend on the mask: the KV tiles of a ring plan
+    // have at most two position runs or one, whichever the mask visits less
+    // (a sliding window usually takes tiles of one run), so the size covers
+    // both tilings.
+    size_t total = 0;
+    for (int kv_runs : {2, 1}) {
+        auto plan = get_ring_plan(cu, B, cp, mode, Hq / Hkv, Hkv, 1, -1, tc, tc && sched == RA_SCHED_ALLGATHER, &st,
+                                  nullptr, nullptr, kv_runs);
+        if (!plan) return 0;
+        total = std::max(total, ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, bwd).total);
+    }
+    return total;
 }
 
 size_t ra_ring_workspace_bytes_masked(int64_t T, int Hq, int Hkv, int d, int dtype, const int32_t *cu, int B, int cp,

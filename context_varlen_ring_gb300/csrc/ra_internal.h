@@ -109,10 +109,10 @@ struct TilePlan {
     }
 };
 
-// Builds tiles over rows [lo, hi) with positions pos[row] (at most two
-// consecutive-position runs per tile) and appends them.
+// Builds tiles over rows [lo, hi) with positions pos[row] (at most
+// max_runs, 1 or 2, consecutive-position runs per tile) and appends them.
 void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_t hi,
-                  int tile_rows, int seg);
+                  int tile_rows, int seg, int max_runs = 2);
 
 // Ring tile plan: query side = key side = the permuted buffer.
 // allgather: the key side is every document's K/V in original order (the
@@ -120,8 +120,11 @@ void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_
 // rank's zigzag shard, as the ring passes it.
 // key_lo / key_hi (NULL = none): an interval mask (then causal and window
 // are ignored), checked for non-decreasing bounds inside every document.
+// kv_runs: 0 = the KV tiling with fewer forward visits (tiles of at most two
+// position runs, or of one), 1 or 2 = that tiling.
 ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, bool allgather,
-                           TilePlan &tp, const int32_t *key_lo = nullptr, const int32_t *key_hi = nullptr);
+                           TilePlan &tp, const int32_t *key_lo = nullptr, const int32_t *key_hi = nullptr,
+                           int kv_runs = 0);
 
 // Generic partial's tile plan: one "rank", separate Q and K sides.
 ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg,
@@ -176,7 +179,8 @@ ra_status upload_plan_tables(RingPlan &plan, void *dst, void *stream);
 // and the interval bounds when given).
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
                                         int causal, int window, bool want_tiles, bool allgather, ra_status *st,
-                                        const int32_t *key_lo = nullptr, const int32_t *key_hi = nullptr);
+                                        const int32_t *key_lo = nullptr, const int32_t *key_hi = nullptr,
+                                        int kv_runs = 0);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

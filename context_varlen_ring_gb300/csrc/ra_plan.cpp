@@ -85,7 +85,8 @@ ra_status build_zigzag(const int32_t *cu, int B, int cp, int mode, ZigzagPlan &z
     return RA_OK;
 }
 
-void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_t hi, int tile_rows, int seg) {
+void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_t hi, int tile_rows, int seg,
+                  int max_runs) {
     int64_t i = lo;
     while (i < hi) {
         const int64_t start = i;
@@ -96,7 +97,7 @@ void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_
         const int32_t split = (int32_t)(i - start);
         int32_t p1 = p0 + split;
         bool two = false;
-        if (i < hi && i - start < tile_rows) {
+        if (max_runs > 1 && i < hi && i - start < tile_rows) {
             p1 = P(i);
             two = true;
             ++i;
@@ -271,7 +272,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
 }
 
 ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, bool allgather,
-                           TilePlan &tp, const int32_t *key_lo, const int32_t *key_hi) {
+                           TilePlan &tp, const int32_t *key_lo, const int32_t *key_hi, int kv_runs) {
     if (G < 1 || kBM % G != 0) return fail(RA_ERR_UNSUPPORTED, "GQA group must divide 128");
     if ((key_lo == nullptr) != (key_hi == nullptr)) return fail(RA_ERR_INVALID_ARG, "key_lo and key_hi go together");
     if (key_lo) {
@@ -306,7 +307,7 @@ ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int
     }
     tp.q_off.back() = (int32_t)tp.qtiles.size();
     tp.kv_off.back() = (int32_t)tp.kvtiles.size();
-    if (key_lo) {
+    if (key_lo) {  // (the KV tiling choice below classifies with the bounds)
         const int64_t T = (int64_t)zp.perm.size();
         tp.key_lo.assign(key_lo, key_lo + T);
         tp.key_hi.assign(key_hi, key_hi + T);
@@ -322,6 +323,49 @@ ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int
                 qb.hi_max = std::max(qb.hi_max, key_hi[pos]);
             }
             tp.qbounds[i] = qb;
+        }
+    }
+    if (!allgather && kv_runs != 2) {
+        // A ring KV tile may join the tail of a rank's early zigzag chunk and
+        // the head of its late one.  Under the causal mask that saves visits
+        // (one tile instead of two short ones once both runs are needed);
+        // under a sliding window or an interval mask the two runs, far apart,
+        // are rarely both needed, and tiles of one run are visited less.  So
+        // both tilings are counted (forward tile-pair visits of every query
+        // tile over every rank's KV tiles of its segment) and the one with
+        // fewer visits is kept.
+        std::vector<Tile> kv1;
+        std::vector<int32_t> off1((size_t)zp.cp * (B + 1) + 1, 0);
+        for (int r = 0; r < zp.cp; ++r) {
+            for (int b = 0; b <= B; ++b) {
+                const size_t idx = (size_t)r * (B + 1) + b;
+                off1[idx] = (int32_t)kv1.size();
+                if (b == B) break;
+                const int64_t lo = zp.off[r] + zp.cu_local[idx], hi = zp.off[r] + zp.cu_local[idx + 1];
+                append_tiles(kv1, zp.perm.data(), lo, hi, kBN, b, 1);
+            }
+        }
+        off1.back() = (int32_t)kv1.size();
+        auto visits = [&](const std::vector<Tile> &kv, const std::vector<int32_t> &koff) {
+            int64_t n = 0;
+            for (int b = 0; b < B; ++b)
+                for (int r = 0; r < zp.cp; ++r) {
+                    const size_t qi = (size_t)r * (B + 1) + b;
+                    for (int i = tp.q_off[qi]; i < tp.q_off[qi + 1]; ++i)
+                        for (int s = 0; s < zp.cp; ++s) {
+                            const size_t ki = (size_t)s * (B + 1) + b;
+                            for (int j = koff[ki]; j < koff[ki + 1]; ++j)
+                                n += (tp.qbounds.empty() ? classify(tp.qtiles[i], kv[j], causal, window)
+                                                         : classify_bounds(tp.qtiles[i], tp.qbounds[i], kv[j])) !=
+                                     kSkip;
+                        }
+                }
+            return n;
+        };
+        if (kv_runs == 1 ||
+            (kv_runs == 0 && kv1.size() != tp.kvtiles.size() && visits(kv1, off1) < visits(tp.kvtiles, tp.kv_off))) {
+            tp.kvtiles.swap(kv1);
+            tp.kv_off.swap(off1);
         }
     }
     build_items(tp, Hkv, causal, window);
@@ -424,7 +468,7 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
 
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
                                         int causal, int window, bool want_tiles, bool allgather, ra_status *st,
-                                        const int32_t *key_lo, const int32_t *key_hi) {
+                                        const int32_t *key_lo, const int32_t *key_hi, int kv_runs) {
     static std::mutex mu;
     static std::map<std::string, std::shared_ptr<RingPlan>> cache;
     static std::vector<std::string> order;
@@ -437,7 +481,8 @@ std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mo
         *st = fail(RA_ERR_INVALID_ARG, "interval masks need both bounds and the tensor-core path");
         return nullptr;
     }
-    int32_t tail[10] = {B, cp, mode, G, Hkv, causal, window, want_tiles ? 1 : 0, allgather ? 1 : 0, bounds ? 1 : 0};
+    int32_t tail[11] = {B,      cp, mode, G, Hkv, causal, window, want_tiles ? 1 : 0, allgather ? 1 : 0,
+                        bounds ? 1 : 0, kv_runs};
     key.append(reinterpret_cast<const char *>(tail), sizeof(tail));
     if (bounds) {  // the plan depends on every token's bounds
         const size_t T = (size_t)cu[B];
@@ -453,7 +498,7 @@ std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mo
     *st = build_zigzag(cu, B, cp, mode, plan->zz);
     if (*st) return nullptr;
     if (want_tiles) {
-        *st = build_ring_tiles(plan->zz, G, Hkv, causal, window, allgather, plan->tiles, key_lo, key_hi);
+        *st = build_ring_tiles(plan->zz, G, Hkv, causal, window, allgather, plan->tiles, key_lo, key_hi, kv_runs);
         if (*st) return nullptr;
         plan->has_tiles = true;
     }

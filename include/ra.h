@@ -261,7 +261,10 @@ ra_status ra_lse_merge(int n_parts, const float *const *outs, const float *const
  * PR #1133, cudnn_flash_attention diff).  cp >= 1.  window: sliding window
  * as in ra_varlen_attn_partial (-1 = none); positions are the original
  * (unpermuted) token indices, so the zigzag reorder leaves the mask intact.
- * workspace: DEVICE, >= ra_ring_workspace_bytes(...) for the same arguments.
+ * workspace: DEVICE, >= ra_ring_workspace_bytes(...) for the same arguments
+ * (the size holds for every causal and window setting: the planner's KV
+ * tiling, which the mask selects, only changes the size of its tables and
+ * the size covers both tilings).
  * On the tensor-core path (bf16, d = 128) the kernels read every tile whose
  * rows form one position run straight from q, k, v (and dout), and the
  * workspace receives rank-ordered copies of the rows of the other tiles

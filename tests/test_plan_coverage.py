@@ -72,16 +72,16 @@ def test_packed_workload_tiling(ra, orc):
         assert 2 * st["fwd_steps"] >= st["fwd_visited"]
 
 
-def _runs_tiles(pos, rows):
-    """Greedy tiles of at most `rows` positions and at most two runs of
-    consecutive positions (the planner's rule), as arrays of positions."""
+def _runs_tiles(pos, rows, max_runs=2):
+    """Greedy tiles of at most `rows` positions and at most `max_runs` runs
+    of consecutive positions (the planner's rule), as arrays of positions."""
     out, i, n = [], 0, len(pos)
     while i < n:
         s = i
         i += 1
         while i < n and i - s < rows and pos[i] == pos[i - 1] + 1:
             i += 1
-        if i < n and i - s < rows:
+        if max_runs > 1 and i < n and i - s < rows:
             i += 1
             while i < n and i - s < rows and pos[i] == pos[i - 1] + 1:
                 i += 1
@@ -89,22 +89,30 @@ def _runs_tiles(pos, rows):
     return out
 
 
-def _ring_fwd_steps(lens, cp, q_tokens, pair_sorted=True):
+def _ring_fwd_steps(lens, cp, q_tokens, pair_sorted=True, window=-1, kv_runs=2, visits=False):
     """KV tiles walked by the causal ring forward's items of one KV head:
     per document and rank, the rank's two zigzag chunks (floor(c*L/2cp)
-    bounds) cut into query tiles of q_tokens and KV tiles of 128; a query
-    tile needs every KV tile of its document (all ranks) starting at or
-    before its last position; tiles of a segment paired by need, largest
-    first (or consecutively); an item walks the union of its pair's needs."""
+    bounds) cut into query tiles of q_tokens and KV tiles of 128 (of at
+    most kv_runs position runs); a query tile needs every KV tile of its
+    document (all ranks) starting at or before its last position (and, with
+    a window w, ending at or after its first position - w); tiles of a
+    segment paired by need, largest first (or consecutively); an item walks
+    the union of its pair's needs.  visits=True: the query tiles' needs
+    summed instead."""
     steps = 0
     for L in (int(x) for x in lens):
         n = 2 * cp
         bnd = [c * L // n for c in range(n + 1)]
         shards = [list(range(bnd[r], bnd[r + 1])) + list(range(bnd[n - 1 - r], bnd[n - r])) for r in range(cp)]
-        kmin = np.array([t.min() for sh in shards for t in _runs_tiles(sh, 128)])
+        kt = [t for sh in shards for t in _runs_tiles(sh, 128, kv_runs)]
+        kmin = np.array([t.min() for t in kt])
+        kmax = np.array([t.max() for t in kt])
         for sh in shards:
             qt = _runs_tiles(sh, q_tokens)
-            need = [kmin <= t.max() for t in qt]
+            need = [(kmin <= t.max()) & ((kmax >= t.min() - window) if window >= 0 else True) for t in qt]
+            if visits:
+                steps += int(sum(x.sum() for x in need))
+                continue
             idx = list(range(len(qt)))
             if pair_sorted:
                 idx.sort(key=lambda i: (int(need[i].sum()), int(qt[i].max())), reverse=True)
@@ -114,6 +122,22 @@ def _ring_fwd_steps(lens, cp, q_tokens, pair_sorted=True):
     return steps
     assert ag["fwd_capacity"] < ring["fwd_capacity"]
     assert ref / ag["fwd_capacity"] > 0.9 > ref / ring["fwd_capacity"] > 0.75
+
+
+@pytest.mark.parametrize("window", [1024, 256, 64])
+def test_ring_kv_tiling_takes_fewer_visits(ra, window):
+    """Under a sliding window the ring planner keeps whichever KV tiling
+    (tiles of at most two position runs, or of one) visits fewer tile pairs
+    in the forward; its visits and steps match the restatement."""
+    wl = W.C2
+    cu = wl.cu_seqlens()
+    lens, qtok = np.diff(cu), 128 // (wl.hq // wl.hkv)
+    v = {r: _ring_fwd_steps(lens, wl.cp, qtok, window=window, kv_runs=r, visits=True) for r in (1, 2)}
+    st = ra.ring_plan_stats(cu, wl.cp, wl.zz_mode, wl.hq // wl.hkv, wl.hkv, True, window, "fused")
+    runs = 1 if v[1] < v[2] else 2
+    assert st["fwd_visited"] == v[runs] == min(v.values())
+    assert st["fwd_steps"] == _ring_fwd_steps(lens, wl.cp, qtok, window=window, kv_runs=runs)
+    assert (st["two_run_kv_rows"] == 0) == (runs == 1)
 
 
 def test_scheduling_model_bounds(ra):
