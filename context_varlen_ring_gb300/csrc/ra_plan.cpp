@@ -291,23 +291,22 @@ ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int
     const int B = zp.B;
     tp.q_off.assign((size_t)zp.cp * (B + 1) + 1, 0);
     tp.kv_off.assign((size_t)zp.cp * (B + 1) + 1, 0);
+    auto seg_rows = [&](int r, int b, int64_t *lo, int64_t *hi) {
+        const size_t idx = (size_t)r * (B + 1) + b;
+        *lo = zp.off[r] + zp.cu_local[idx];
+        *hi = zp.off[r] + zp.cu_local[idx + 1];
+    };
     for (int r = 0; r < zp.cp; ++r) {
         for (int b = 0; b <= B; ++b) {
-            const size_t idx = (size_t)r * (B + 1) + b;
-            tp.q_off[idx] = (int32_t)tp.qtiles.size();
-            tp.kv_off[idx] = (int32_t)tp.kvtiles.size();
+            tp.q_off[(size_t)r * (B + 1) + b] = (int32_t)tp.qtiles.size();
             if (b == B) break;
-            const int64_t lo = zp.off[r] + zp.cu_local[idx], hi = zp.off[r] + zp.cu_local[idx + 1];
+            int64_t lo, hi;
+            seg_rows(r, b, &lo, &hi);
             append_tiles(tp.qtiles, zp.perm.data(), lo, hi, tp.q_tokens, b);
-            if (!allgather)
-                append_tiles(tp.kvtiles, zp.perm.data(), lo, hi, kBN, b);
-            else if (r == 0)  // the whole document, original rows = positions
-                append_tiles(tp.kvtiles, nullptr, zp.cu[b], zp.cu[b + 1], kBN, b);
         }
     }
     tp.q_off.back() = (int32_t)tp.qtiles.size();
-    tp.kv_off.back() = (int32_t)tp.kvtiles.size();
-    if (key_lo) {  // (the KV tiling choice below classifies with the bounds)
+    if (key_lo) {
         const int64_t T = (int64_t)zp.perm.size();
         tp.key_lo.assign(key_lo, key_lo + T);
         tp.key_hi.assign(key_hi, key_hi + T);
@@ -325,49 +324,50 @@ ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int
             tp.qbounds[i] = qb;
         }
     }
-    if (!allgather && kv_runs != 2) {
-        // A ring KV tile may join the tail of a rank's early zigzag chunk and
-        // the head of its late one.  Under the causal mask that saves visits
-        // (one tile instead of two short ones once both runs are needed);
-        // under a sliding window or an interval mask the two runs, far apart,
-        // are rarely both needed, and tiles of one run are visited less.  So
-        // both tilings are counted (forward tile-pair visits of every query
-        // tile over every rank's KV tiles of its segment) and the one with
-        // fewer visits is kept.
-        std::vector<Tile> kv1;
-        std::vector<int32_t> off1((size_t)zp.cp * (B + 1) + 1, 0);
-        for (int r = 0; r < zp.cp; ++r) {
-            for (int b = 0; b <= B; ++b) {
-                const size_t idx = (size_t)r * (B + 1) + b;
-                off1[idx] = (int32_t)kv1.size();
-                if (b == B) break;
-                const int64_t lo = zp.off[r] + zp.cu_local[idx], hi = zp.off[r] + zp.cu_local[idx + 1];
-                append_tiles(kv1, zp.perm.data(), lo, hi, kBN, b, 1);
+    // KV tiles.  A ring KV tile may join the tail of a rank's early zigzag
+    // chunk and the head of its late one.  Under the causal mask that saves
+    // visits (one tile instead of two short ones once both runs are needed);
+    // under a sliding window or an interval mask the two runs, far apart,
+    // are often not both needed, and tiles of one run are visited less.  So
+    // each rank's KV tiles of a segment are built both ways and the way with
+    // fewer forward visits (tile pairs with any allowed pair, over every
+    // query tile of the segment's document) is kept (kv_runs = 1 or 2 forces
+    // one way).
+    std::vector<Tile> cand[2];
+    for (int r = 0; r < zp.cp; ++r) {
+        for (int b = 0; b <= B; ++b) {
+            tp.kv_off[(size_t)r * (B + 1) + b] = (int32_t)tp.kvtiles.size();
+            if (b == B) break;
+            if (allgather) {
+                if (r == 0)  // the whole document, original rows = positions
+                    append_tiles(tp.kvtiles, nullptr, zp.cu[b], zp.cu[b + 1], kBN, b);
+                continue;
             }
-        }
-        off1.back() = (int32_t)kv1.size();
-        auto visits = [&](const std::vector<Tile> &kv, const std::vector<int32_t> &koff) {
-            int64_t n = 0;
-            for (int b = 0; b < B; ++b)
-                for (int r = 0; r < zp.cp; ++r) {
-                    const size_t qi = (size_t)r * (B + 1) + b;
-                    for (int i = tp.q_off[qi]; i < tp.q_off[qi + 1]; ++i)
-                        for (int s = 0; s < zp.cp; ++s) {
-                            const size_t ki = (size_t)s * (B + 1) + b;
-                            for (int j = koff[ki]; j < koff[ki + 1]; ++j)
-                                n += (tp.qbounds.empty() ? classify(tp.qtiles[i], kv[j], causal, window)
-                                                         : classify_bounds(tp.qtiles[i], tp.qbounds[i], kv[j])) !=
-                                     kSkip;
-                        }
+            int64_t lo, hi;
+            seg_rows(r, b, &lo, &hi);
+            int runs = kv_runs == 1 ? 1 : 2;
+            if (kv_runs == 0) {
+                int64_t vis[2] = {0, 0};
+                for (int w = 0; w < 2; ++w) {
+                    cand[w].clear();
+                    append_tiles(cand[w], zp.perm.data(), lo, hi, kBN, b, w + 1);
                 }
-            return n;
-        };
-        if (kv_runs == 1 ||
-            (kv_runs == 0 && kv1.size() != tp.kvtiles.size() && visits(kv1, off1) < visits(tp.kvtiles, tp.kv_off))) {
-            tp.kvtiles.swap(kv1);
-            tp.kv_off.swap(off1);
+                // (the same number of tiles can still cut the runs differently)
+                for (int w = 0; w < 2; ++w)
+                    for (int rq = 0; rq < zp.cp; ++rq) {
+                        const size_t qi = (size_t)rq * (B + 1) + b;
+                        for (int i = tp.q_off[qi]; i < tp.q_off[qi + 1]; ++i)
+                            for (const Tile &k : cand[w])
+                                vis[w] += (tp.qbounds.empty() ? classify(tp.qtiles[i], k, causal, window)
+                                                              : classify_bounds(tp.qtiles[i], tp.qbounds[i], k)) !=
+                                          kSkip;
+                    }
+                if (vis[0] < vis[1]) runs = 1;
+            }
+            append_tiles(tp.kvtiles, zp.perm.data(), lo, hi, kBN, b, runs);
         }
     }
+    tp.kv_off.back() = (int32_t)tp.kvtiles.size();
     build_items(tp, Hkv, causal, window);
     return RA_OK;
 }
