@@ -117,21 +117,22 @@ void append_tiles(std::vector<Tile> &out, const int32_t *pos, int64_t lo, int64_
     }
 }
 
-// Forward items: pairs of query tiles of one (rank, segment), replicated
-// over KV heads; backward items: one per KV tile and KV head.
+// Forward items: pairs of query tiles of one document, replicated over KV
+// heads; backward items: one per KV tile and KV head.
 //
 // A forward item walks the union of its two query tiles' KV tiles, and a
 // KV tile that only one of them needs costs the item about as much time as
 // one that both need (the kernel's loop is set by the latency of each query
 // tile's S -> softmax -> PV chain, and the two tiles cover each other's
-// softmax only when both have products).  So the tiles of a segment are
-// paired in order of their visit counts, from the most visits down: tiles
-// with the same KV needs share items, and when the count is odd the tile
-// left alone is the one with the fewest visits.  (Pairing consecutive
-// tiles left the last one alone -- in a zigzag shard the late chunk's last
-// tile, which visits every KV tile of its document.)  A query tile's
-// result does not depend on its partner: it walks its own visited tiles in
-// the same order in any item.
+// softmax only when both have products).  So the query tiles of a document
+// are paired in order of their visit counts, from the most visits down,
+// across the simulated ranks: tiles with the same KV needs share items, and
+// when the count is odd the tile left alone is the one with the fewest
+// visits.  An item walks the ring steps of its first tile's rank; the
+// second tile, possibly of another rank, meets its own KV tiles in that
+// order (the same tiles: each rank's steps run over every rank's shard),
+// which changes its result only in the order of the online softmax's
+// floating-point accumulation.
 static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
     const int cp = tp.cp, B = tp.B;
     tp.items.clear();
@@ -159,64 +160,64 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
         if (*tf > *tl) *tf = *tl = 0;
         return c;
     };
-    std::vector<int> order;
-    std::vector<int64_t> cnt;
-    std::vector<int> tfs, tls;
-    for (int r = 0; r < cp; ++r) {
-        for (int b = 0; b < B; ++b) {
-            const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
-            const int n = qe - qa;
-            cnt.assign((size_t)n, 0);
-            tfs.assign((size_t)n, 0);
-            tls.assign((size_t)n, 0);
-            for (int i = 0; i < n; ++i) {
-                const int qi = qa + i;
-                cnt[(size_t)i] = q_visits(qi, r, b, &tfs[(size_t)i], &tls[(size_t)i]);
-                // per-query-tile items of the dQ pass
+    struct QEntry {
+        int qi, r;
+        int64_t cnt;
+    };
+    std::vector<QEntry> qs;
+    for (int b = 0; b < B; ++b) {
+        // the query tiles of document b on every rank, with their visits
+        qs.clear();
+        for (int r = 0; r < cp; ++r) {
+            for (int qi = tp.q_off[seg_idx(r, b)]; qi < tp.q_off[seg_idx(r, b) + 1]; ++qi) {
+                int tf, tl;
+                const int64_t c = q_visits(qi, r, b, &tf, &tl);
+                qs.push_back(QEntry{qi, r, c});
+                // per-query-tile items of the dQ pass (the tile's own ring order)
                 for (int g = 0; g < Hkv; ++g) {
-                    WorkItem w{qi, -1, g, r, b, tfs[(size_t)i], tls[(size_t)i],
-                               (int32_t)std::min<int64_t>(cnt[(size_t)i], INT32_MAX)};
+                    WorkItem w{qi, -1, g, r, b, tf, tl, (int32_t)std::min<int64_t>(c, INT32_MAX)};
                     tp.qitems.push_back(w);
                 }
             }
-            order.resize((size_t)n);
-            for (int i = 0; i < n; ++i) order[(size_t)i] = i;
-            std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
-                if (cnt[(size_t)x] != cnt[(size_t)y]) return cnt[(size_t)x] > cnt[(size_t)y];
-                return tp.qtiles[qa + x].pmax > tp.qtiles[qa + y].pmax;
-            });
-            for (int j = 0; j < n; j += 2) {
-                const int x = order[(size_t)j];
-                const int y = j + 1 < n ? order[(size_t)j + 1] : -1;
-                const int i = qa + x, q1 = y >= 0 ? qa + y : -1;
-                // the item's steps span both tiles' visited KV tiles; its cost
-                // is the KV tiles it walks with at least one product
-                int tf = tfs[(size_t)x], tl = tls[(size_t)x];
-                if (y >= 0 && tls[(size_t)y] > tfs[(size_t)y]) {
-                    if (tl <= tf) {
-                        tf = tfs[(size_t)y];
-                        tl = tls[(size_t)y];
-                    } else {
-                        tf = std::min(tf, tfs[(size_t)y]);
-                        tl = std::max(tl, tls[(size_t)y]);
-                    }
+        }
+        // Forward items pair the document's query tiles in order of their
+        // visits, from the most down, across ranks: the item walks the KV
+        // tiles in the ring order of its first tile's rank (every rank's
+        // shards, so the second tile meets all of its own as well), and two
+        // tiles with the same visits share (nearly) every KV step.
+        std::stable_sort(qs.begin(), qs.end(), [&](const QEntry &x, const QEntry &y) {
+            if (x.cnt != y.cnt) return x.cnt > y.cnt;
+            return tp.qtiles[x.qi].pmax > tp.qtiles[y.qi].pmax;
+        });
+        const int n = (int)qs.size();
+        for (int j = 0; j < n; j += 2) {
+            const QEntry &x = qs[(size_t)j];
+            const int q1 = j + 1 < n ? qs[(size_t)j + 1].qi : -1;
+            const int r = x.r, i = x.qi;
+            // the steps [tf, tl) of rank r's ring order that hold a KV tile
+            // either query tile visits; the cost is their visits
+            int64_t cost = 0;
+            int tf = cp, tl = 0;
+            for (int t = 0; t < cp; ++t) {
+                const int sr = ((r - t) % cp + cp) % cp;
+                const int ka = tp.kv_off[seg_idx(sr, b)], ke = tp.kv_off[seg_idx(sr, b) + 1];
+                int64_t c_t = 0;
+                for (int k = ka; k < ke; ++k) {
+                    c_t += tp.pair_class(i, k, causal, window) != kSkip;
+                    if (q1 >= 0) c_t += tp.pair_class(q1, k, causal, window) != kSkip;
                 }
-                int64_t cost = 0;
-                for (int t = tf; t < tl; ++t) {
-                    const int s = ((r - t) % cp + cp) % cp;
-                    const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
-                    for (int k = ka; k < ke; ++k) {
-                        cost += tp.pair_class(i, k, causal, window) != kSkip;
-                        if (q1 >= 0) cost += tp.pair_class(q1, k, causal, window) != kSkip;
-                    }
+                if (c_t) {
+                    tf = std::min(tf, t);
+                    tl = t + 1;
                 }
-                if (tf >= tl) tf = tl = 0;
-                for (int g = 0; g < Hkv; ++g) {
-                    WorkItem w{i, q1, g, r, b, tf, tl, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
-                    tp.items.push_back(w);
-                }
-                tp.fwd_tile_pairs += cost * Hkv;
+                cost += c_t;
             }
+            if (tf >= tl) tf = tl = 0;
+            for (int g = 0; g < Hkv; ++g) {
+                WorkItem w{i, q1, g, r, b, tf, tl, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
+                tp.items.push_back(w);
+            }
+            tp.fwd_tile_pairs += cost * Hkv;
         }
     }
     for (int s = 0; s < cp; ++s) {

@@ -63,11 +63,15 @@ def test_packed_workload_tiling(ra, orc):
         assert st["q_tiles"] == 1080 and st["two_run_q_rows"] == 3174
     assert ring["kv_tiles"] == 328 and ag["kv_tiles"] == 265
     assert ring["two_run_kv_rows"] == 10938 and ag["two_run_kv_rows"] == 0
-    # forward items pair the query tiles of a segment by visit count: the
-    # KV steps they walk match a separate restatement of the tiling and the
-    # pairing (11 236 per KV head; consecutive pairs would walk 11 768)
-    assert ring["fwd_steps"] == _ring_fwd_steps(np.diff(cu), wl.cp, 128 // (wl.hq // wl.hkv)) == 11236
-    assert _ring_fwd_steps(np.diff(cu), wl.cp, 128 // (wl.hq // wl.hkv), pair_sorted=False) == 11768
+    # forward items pair a document's query tiles across ranks by visit
+    # count: the KV steps they walk match a separate restatement of the
+    # tiling and the pairing (10 700 per KV head, the lower bound of half the
+    # 21 264 visits being 10 632; pairing within each rank's share walks 11 236,
+    # consecutive tiles of a share 11 768)
+    lens, qtok = np.diff(cu), 128 // (wl.hq // wl.hkv)
+    assert ring["fwd_steps"] == _ring_fwd_steps(lens, wl.cp, qtok) == 10700
+    assert _ring_fwd_steps(lens, wl.cp, qtok, cross_rank=False) == 11236
+    assert _ring_fwd_steps(lens, wl.cp, qtok, pair_sorted=False, cross_rank=False) == 11768
     for st in (ring, ag):
         assert 2 * st["fwd_steps"] >= st["fwd_visited"]
 
@@ -89,7 +93,7 @@ def _runs_tiles(pos, rows, max_runs=2):
     return out
 
 
-def _ring_fwd_steps(lens, cp, q_tokens, pair_sorted=True, window=-1, kv_runs=2, visits=False):
+def _ring_fwd_steps(lens, cp, q_tokens, pair_sorted=True, window=-1, kv_runs=2, visits=False, cross_rank=True):
     # kv_runs: 1 or 2 runs per KV tile, or 0: per rank shard, the tiling the
     # forward visits less
     """KV tiles walked by the causal ring forward's items of one KV head:
@@ -98,9 +102,9 @@ def _ring_fwd_steps(lens, cp, q_tokens, pair_sorted=True, window=-1, kv_runs=2, 
     most kv_runs position runs); a query tile needs every KV tile of its
     document (all ranks) starting at or before its last position (and, with
     a window w, ending at or after its first position - w); tiles of a
-    segment paired by need, largest first (or consecutively); an item walks
-    the union of its pair's needs.  visits=True: the query tiles' needs
-    summed instead."""
+    document (across ranks; cross_rank=False: of each rank's share) paired
+    by need, largest first (or consecutively); an item walks the union of
+    its pair's needs.  visits=True: the query tiles' needs summed instead."""
     steps = 0
     for L in (int(x) for x in lens):
         n = 2 * cp
@@ -120,8 +124,9 @@ def _ring_fwd_steps(lens, cp, q_tokens, pair_sorted=True, window=-1, kv_runs=2, 
             kt += pick
         kmin = np.array([t.min() for t in kt])
         kmax = np.array([t.max() for t in kt])
-        for sh in shards:
-            qt = _runs_tiles(sh, q_tokens)
+        # pairing groups: the whole document across ranks, or each rank's share
+        groups = [qall] if cross_rank else [_runs_tiles(sh, q_tokens) for sh in shards]
+        for qt in groups:
             need = [(kmin <= t.max()) & ((kmax >= t.min() - window) if window >= 0 else True) for t in qt]
             if visits:
                 steps += int(sum(x.sum() for x in need))
