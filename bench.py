@@ -528,6 +528,43 @@ def masked_lines(ra, torch, dev, wl, steps, warmup, peak, q, k, v, do, specs):
 
 
 
+def schedule_lines(ra, torch, dev, wl, steps, warmup, peak, q, k, v, do):
+    """The same data under the all-gather KV schedule and, on the fused ring,
+    with a 1024-token sliding window: fwd+bwd step and forward, TFLOP/s over
+    each case's allowed pairs."""
+    cu = wl.cu_seqlens()
+    T, hq, hkv, d = wl.T, wl.hq, wl.hkv, wl.d
+    res = {}
+    for name, sched, window in (("allgather", "allgather", -1), ("window:1024", "fused", 1024)):
+        pairs = pairs_of(cu, window)
+        nb = max(ra.ring_workspace_bytes(T, hq, hkv, d, 0, cu, wl.cp, wl.zz_mode, sched, bwd=b) for b in (False, True))
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        out, lse = torch.empty_like(q), torch.empty((hq, T), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def fwd():
+            ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, sched, out=out, lse=lse, workspace=ws,
+                             window=window)
+
+        def step():
+            fwd()
+            ra.ring_attn_bwd(q, k, v, out, lse, do, cu, wl.cp, wl.zz_mode, True, wl.scale, sched, dq=dq, dk=dk,
+                             dv=dv, workspace=ws, reuse_fwd_workspace=True, window=window)
+
+        stream = torch.cuda.current_stream(dev)
+        ms_step = time_calls(step, steps, warmup, stream, torch)
+        ms_fwd = time_calls(fwd, steps, warmup, stream, torch)
+        assert ra.device_status() == 0
+        tf = 14 * d * hq * pairs / (ms_step / 1e3) / 1e12
+        tff = 4 * d * hq * pairs / (ms_fwd / 1e3) / 1e12
+        res[name] = {"sched": sched, "window": window, "allowed_pairs_per_head": pairs, "ms_per_step": ms_step,
+                     "tflops": tf, "frac_of_peak": tf / peak,
+                     "fwd": {"ms": ms_fwd, "tflops": tff, "frac_of_peak": tff / peak}}
+        del ws, out, lse, dq, dk, dv
+        torch.cuda.empty_cache()
+    return res
+
+
 def cpu_configs(args):
     """The fp64 oracle on the host cores, per workload: the 128-token fp32
     batch, the forward of the 8192-token sequence and of the packed
@@ -868,6 +905,8 @@ def main():
         extras["bandwidth_kernels"] = bandwidth_kernels(ra, torch, dev, wl, args.steps, args.warmup, hbm)
         extras["interval_masks"] = masked_lines(ra, torch, dev, wl, args.steps, args.warmup, peak_burst, q, k, v, do,
                                                 ["prefix:512", "chunked:1024"])
+        extras["other_schedules"] = schedule_lines(ra, torch, dev, wl, args.steps, args.warmup, peak_burst,
+                                                   q, k, v, do)
         barrier()
 
     # ---- end to end through the public API with host buffers.  Every step

@@ -26,7 +26,7 @@ def test_every_allowed_pair_once(ra, orc, sched, causal):
     n = 0
     for trial in range(6):
         cu = W.cu_seqlens(W.random_doc_lens(rng, int(rng.integers(60, 1500)), 1, 500))
-        for cp in (1, 2, 3, 8):
+        for cp in (1, 2, 3, 8, 16):
             for mode in (0, 1):
                 G = int(rng.choice([1, 2, 4, 8, 16]))
                 window = int(rng.choice([-1, -1, 0, 5, 130]))
@@ -43,7 +43,7 @@ def test_every_allowed_pair_once(ra, orc, sched, causal):
                 if sched == "allgather":
                     assert st["two_run_kv_rows"] == 0, case
                 n += 1
-    assert n == 48
+    assert n == 60
 
 
 def test_packed_workload_tiling(ra, orc):
