@@ -96,7 +96,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
     }
 }
 
-// The same wait run by every lane of a converged warp; the verdict is made
+// The same wait run by every lane of a converged warp; the result is made
 // warp-uniform so the warp stays converged for elect.sync issue below.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, const WaitCtl &w) {
     const bool r = mbar_wait(bar, parity, w);
