@@ -732,7 +732,10 @@ struct RingLayout {
     size_t dop = 0, Dv = 0, dq = 0, dk = 0, dv = 0, tile_ld = 0;
 };
 
-RingLayout ring_layout(const RingPlan &plan, int64_t T, int Hq, int Hkv, int d, int dtype, int cp, int sched, int bwd) {
+// The workspace regions of a ring call whose tables take blob_bytes and
+// whose plan has n_qtiles query tiles.
+static RingLayout ring_layout_sized(size_t blob_bytes, size_t n_qtiles, int64_t T, int Hq, int Hkv, int d, int dtype,
+                                    int cp, int sched, int bwd) {
     RingLayout L;
     Carver c(nullptr);
     auto at = [&](size_t bytes) {
@@ -741,7 +744,7 @@ RingLayout ring_layout(const RingPlan &plan, int64_t T, int Hq, int Hkv, int d, 
         return o;
     };
     const size_t es = esize(dtype);
-    L.tables = at(plan.dev.blob.size());
+    L.tables = at(blob_bytes);
     L.qp = at((size_t)T * Hq * d * es);
     L.kp = at((size_t)T * Hkv * d * es);
     L.vp = at((size_t)T * Hkv * d * es);
@@ -757,10 +760,14 @@ RingLayout ring_layout(const RingPlan &plan, int64_t T, int Hq, int Hkv, int d, 
         L.dq = at((size_t)T * Hq * d * 4);
         L.dk = at((size_t)T * Hkv * d * 4);
         L.dv = at((size_t)T * Hkv * d * 4);
-        L.tile_ld = at(plan.tiles.qtiles.size() * (size_t)Hkv * 1024);
+        L.tile_ld = at(n_qtiles * (size_t)Hkv * 1024);
     }
     L.total = c.used + 256;
     return L;
+}
+
+RingLayout ring_layout(const RingPlan &plan, int64_t T, int Hq, int Hkv, int d, int dtype, int cp, int sched, int bwd) {
+    return ring_layout_sized(plan.dev.blob.size(), plan.tiles.qtiles.size(), T, Hq, Hkv, d, dtype, cp, sched, bwd);
 }
 
 // Interval masks: both bounds or neither; they run on the tensor-core
@@ -821,18 +828,15 @@ size_t ra_ring_workspace_bytes(int64_t T, int Hq, int Hkv, int d, int dtype, con
     ra_status st;
     const bool tc = tc_fwd_supported(dtype, d, Hq, Hkv);
     if (sched != RA_SCHED_FUSED && sched != RA_SCHED_STEPWISE && sched != RA_SCHED_ALLGATHER) return 0;
-    // Only the plan's tables depend on the mask: the KV tiles of a ring plan
-    // have at most two position runs or one, whichever the mask visits less
-    // (a sliding window usually takes tiles of one run), so the size covers
-    // both tilings.
-    size_t total = 0;
-    for (int kv_runs : {2, 1}) {
-        auto plan = get_ring_plan(cu, B, cp, mode, Hq / Hkv, Hkv, 1, -1, tc, tc && sched == RA_SCHED_ALLGATHER, &st,
-                                  nullptr, nullptr, kv_runs);
-        if (!plan) return 0;
-        total = std::max(total, ring_layout(*plan, T, Hq, Hkv, d, dtype, cp, sched, bwd).total);
-    }
-    return total;
+    // Only the plan's tables depend on the mask: each rank's KV tiles of a
+    // document have at most two position runs or one, whichever the mask
+    // visits less (a sliding window usually takes tiles of one run), so the
+    // size is that of the tables with every KV tile of one run, the most
+    // tiles; counted from the tiles alone (no plan is built or cached).
+    size_t blob = 0, nq = 0;
+    st = ring_tables_bound(cu, B, cp, mode, Hq / Hkv, Hkv, tc, tc && sched == RA_SCHED_ALLGATHER, &blob, &nq);
+    if (st) return 0;
+    return ring_layout_sized(blob, nq, T, Hq, Hkv, d, dtype, cp, sched, bwd).total;
 }
 
 size_t ra_ring_workspace_bytes_masked(int64_t T, int Hq, int Hkv, int d, int dtype, const int32_t *cu, int B, int cp,

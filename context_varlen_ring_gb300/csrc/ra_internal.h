@@ -2,6 +2,7 @@
 // units (planner, drivers, kernel launchers).  Not part of the public ABI.
 #pragma once
 
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
 #include <memory>
@@ -87,6 +88,52 @@ inline int classify_bounds(const Tile &q, const QBounds &b, const Tile &k) {
     return kPartial;
 }
 
+// Counting visits without walking every tile pair.  The tiles of one
+// segment cover consecutive rows whose positions increase, so along them
+// both pmin and pmax increase, and under the interval masks (bounds that
+// never decrease inside a document) so do a query tile's lo_min and hi_max.
+// A tile pair is skipped above exactly when one of two monotone tests
+// fails, so the tiles of a segment that a fixed partner visits form one
+// index range, found by two binary searches.
+//
+// KV tiles k[0, n) of one segment that query tile q visits (classify or
+// classify_bounds other than kSkip; qb is q's bounds under interval masks,
+// else null).
+inline int64_t kv_tiles_visited(const Tile &q, const QBounds *qb, const Tile *k, int n, int causal, int window) {
+    if (q.len <= 0 || n <= 0) return 0;
+    // visited iff k.pmin <= hi and k.pmax >= lo
+    int64_t hi = INT64_MAX, lo = INT64_MIN;
+    if (qb) {
+        hi = qb->hi_max;
+        lo = qb->lo_min;
+    } else {
+        if (causal) hi = q.pmax;
+        if (window >= 0) lo = (int64_t)q.pmin - window;
+    }
+    const Tile *e = std::upper_bound(k, k + n, hi, [](int64_t v, const Tile &t) { return v < (int64_t)t.pmin; });
+    const Tile *b = std::lower_bound(k, k + n, lo, [](const Tile &t, int64_t v) { return (int64_t)t.pmax < v; });
+    return e > b ? (int64_t)(e - b) : 0;
+}
+
+// Query tiles q[0, n) of one segment (with their bounds qb[0, n) under
+// interval masks, else null) that visit KV tile k.
+inline int64_t q_tiles_visiting(const Tile *q, const QBounds *qb, int n, const Tile &k, int causal, int window) {
+    if (k.len <= 0 || n <= 0) return 0;
+    int b = 0, e = n;
+    if (qb) {  // visited iff hi_max >= k.pmin and lo_min <= k.pmax
+        b = (int)(std::lower_bound(qb, qb + n, k.pmin, [](const QBounds &x, int32_t v) { return x.hi_max < v; }) - qb);
+        e = (int)(std::upper_bound(qb, qb + n, k.pmax, [](int32_t v, const QBounds &x) { return v < x.lo_min; }) - qb);
+    } else {  // visited iff q.pmax >= k.pmin (causal) and q.pmin - window <= k.pmax (window)
+        if (causal)
+            b = (int)(std::lower_bound(q, q + n, k.pmin, [](const Tile &t, int32_t v) { return t.pmax < v; }) - q);
+        if (window >= 0) {
+            const int64_t lim = (int64_t)k.pmax + window;
+            e = (int)(std::upper_bound(q, q + n, lim, [](int64_t v, const Tile &t) { return v < (int64_t)t.pmin; }) - q);
+        }
+    }
+    return e > b ? e - b : 0;
+}
+
 // Tile tables for one query side and one key side.  Tiles of segment b of
 // rank r are [q_off[r*(B+1)+b], q_off[r*(B+1)+b+1]) (same for kv_off).
 struct TilePlan {
@@ -150,6 +197,24 @@ struct DeviceTables {
     int n_items = 0, n_bitems = 0, n_qitems = 0;
 };
 void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt);
+
+// Record counts that fix the size and the offsets of the device tables.
+struct TableCounts {
+    size_t T = 0, cul = 0, off = 0;  // zigzag: perm [T], cu_local, off (all 0 without a zigzag plan)
+    bool tiles = false;              // tile tables present (with the two-run row masks [T] each)
+    size_t qt = 0, kt = 0, qoff = 0, kvoff = 0, items = 0, bitems = 0, qitems = 0;
+    size_t qb = 0, klo = 0, khi = 0;  // interval masks: bounds per query tile, key_lo and key_hi
+};
+// Sets dt's offsets for tables with these counts; returns their total bytes.
+size_t layout_tables(const TableCounts &n, DeviceTables &dt);
+
+// Table bytes and query-tile count of the ring plan with the most KV tiles
+// for this packing (every KV tile of one position run; a rank's share of a
+// document cut at its chunk boundary never has fewer tiles than joined across
+// it), found from the tiles alone, without work items.  No mask or per-share
+// tiling choice gives a plan with larger tables.
+ra_status ring_tables_bound(const int32_t *cu, int B, int cp, int mode, int G, int Hkv, bool want_tiles,
+                            bool allgather, size_t *blob_bytes, size_t *n_qtiles);
 
 struct RingPlan {
     ZigzagPlan zz;

@@ -140,6 +140,12 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
     tp.qitems.clear();
     tp.fwd_tile_pairs = 0;
     auto seg_idx = [&](int r, int b) { return r * (B + 1) + b; };
+    const bool bounds = !tp.qbounds.empty();
+    // KV tiles [ka, ke) that query tile qi visits
+    auto kv_visits = [&](int qi, int ka, int ke) -> int64_t {
+        return kv_tiles_visited(tp.qtiles[(size_t)qi], bounds ? &tp.qbounds[(size_t)qi] : nullptr,
+                                tp.kvtiles.data() + ka, ke - ka, causal, window);
+    };
     // visited KV tiles of query tile qi over the ring steps, and the step
     // range [tf, tl) that holds them
     auto q_visits = [&](int qi, int r, int b, int *tf, int *tl) {
@@ -149,8 +155,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
         for (int t = 0; t < cp; ++t) {
             const int s = ((r - t) % cp + cp) % cp;
             const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
-            int64_t c_t = 0;
-            for (int j = ka; j < ke; ++j) c_t += tp.pair_class(qi, j, causal, window) != kSkip;
+            const int64_t c_t = kv_visits(qi, ka, ke);
             if (c_t) {
                 *tf = std::min(*tf, t);
                 *tl = t + 1;
@@ -165,6 +170,9 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
         int64_t cnt;
     };
     std::vector<QEntry> qs;
+    tp.qitems.reserve(tp.qtiles.size() * (size_t)Hkv);
+    tp.items.reserve((tp.qtiles.size() + (size_t)B) / 2 * (size_t)Hkv + (size_t)Hkv);
+    tp.bitems.reserve(tp.kvtiles.size() * (size_t)Hkv);
     for (int b = 0; b < B; ++b) {
         // the query tiles of document b on every rank, with their visits
         qs.clear();
@@ -201,11 +209,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
             for (int t = 0; t < cp; ++t) {
                 const int sr = ((r - t) % cp + cp) % cp;
                 const int ka = tp.kv_off[seg_idx(sr, b)], ke = tp.kv_off[seg_idx(sr, b) + 1];
-                int64_t c_t = 0;
-                for (int k = ka; k < ke; ++k) {
-                    c_t += tp.pair_class(i, k, causal, window) != kSkip;
-                    if (q1 >= 0) c_t += tp.pair_class(q1, k, causal, window) != kSkip;
-                }
+                const int64_t c_t = kv_visits(i, ka, ke) + (q1 >= 0 ? kv_visits(q1, ka, ke) : 0);
                 if (c_t) {
                     tf = std::min(tf, t);
                     tl = t + 1;
@@ -229,8 +233,8 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
                 for (int t = 0; t < cp; ++t) {
                     const int r = (s + t) % cp;
                     const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
-                    int64_t c_t = 0;
-                    for (int i = qa; i < qe; ++i) c_t += tp.pair_class(i, j, causal, window) != kSkip;
+                    const int64_t c_t = q_tiles_visiting(tp.qtiles.data() + qa, bounds ? tp.qbounds.data() + qa : nullptr,
+                                                         qe - qa, tp.kvtiles[(size_t)j], causal, window);
                     if (c_t) {
                         tf = std::min(tf, t);
                         tl = t + 1;
@@ -358,10 +362,9 @@ ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int
                     for (int rq = 0; rq < zp.cp; ++rq) {
                         const size_t qi = (size_t)rq * (B + 1) + b;
                         for (int i = tp.q_off[qi]; i < tp.q_off[qi + 1]; ++i)
-                            for (const Tile &k : cand[w])
-                                vis[w] += (tp.qbounds.empty() ? classify(tp.qtiles[i], k, causal, window)
-                                                              : classify_bounds(tp.qtiles[i], tp.qbounds[i], k)) !=
-                                          kSkip;
+                            vis[w] += kv_tiles_visited(tp.qtiles[(size_t)i],
+                                                       tp.qbounds.empty() ? nullptr : &tp.qbounds[(size_t)i],
+                                                       cand[w].data(), (int)cand[w].size(), causal, window);
                     }
                 if (vis[0] < vis[1]) runs = 1;
             }
@@ -400,31 +403,56 @@ ra_status build_partial_tiles(const int32_t *cu_q, const int32_t *cu_k, int nseg
     return RA_OK;
 }
 
-void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
+size_t layout_tables(const TableCounts &n, DeviceTables &dt) {
     size_t o = 0;
     auto take = [&](size_t bytes) {
         size_t at = o;
         o = align_up(o + bytes, 256);
         return at;
     };
-    dt.o_perm = take(zp ? zp->perm.size() * 4 : 0);
-    dt.o_qt = take(tp ? tp->qtiles.size() * sizeof(Tile) : 0);
-    dt.o_kt = take(tp ? tp->kvtiles.size() * sizeof(Tile) : 0);
-    dt.o_qoff = take(tp ? tp->q_off.size() * 4 : 0);
-    dt.o_kvoff = take(tp ? tp->kv_off.size() * 4 : 0);
-    dt.o_items = take(tp ? tp->items.size() * sizeof(WorkItem) : 0);
-    dt.o_bitems = take(tp ? tp->bitems.size() * sizeof(WorkItem) : 0);
-    dt.o_qitems = take(tp ? tp->qitems.size() * sizeof(WorkItem) : 0);
-    dt.o_cul = take(zp ? zp->cu_local.size() * 4 : 0);
-    dt.o_off = take(zp ? zp->off.size() * 4 : 0);
+    dt.o_perm = take(n.T * 4);
+    dt.o_qt = take(n.qt * sizeof(Tile));
+    dt.o_kt = take(n.kt * sizeof(Tile));
+    dt.o_qoff = take(n.qoff * 4);
+    dt.o_kvoff = take(n.kvoff * 4);
+    dt.o_items = take(n.items * sizeof(WorkItem));
+    dt.o_bitems = take(n.bitems * sizeof(WorkItem));
+    dt.o_qitems = take(n.qitems * sizeof(WorkItem));
+    dt.o_cul = take(n.cul * 4);
+    dt.o_off = take(n.off * 4);
     dt.o_sched = take(64);
-    dt.o_qmask = take(zp && tp ? zp->perm.size() : 0);
-    dt.o_kvmask = take(zp && tp ? zp->perm.size() : 0);
-    dt.bounds = tp && !tp->qbounds.empty();
-    dt.o_qb = take(dt.bounds ? tp->qbounds.size() * sizeof(QBounds) : 0);
-    dt.o_klo = take(dt.bounds ? tp->key_lo.size() * 4 : 0);
-    dt.o_khi = take(dt.bounds ? tp->key_hi.size() * 4 : 0);
-    dt.blob.assign(o, 0);
+    dt.o_qmask = take(n.tiles ? n.T : 0);
+    dt.o_kvmask = take(n.tiles ? n.T : 0);
+    dt.bounds = n.qb > 0;
+    dt.o_qb = take(n.qb * sizeof(QBounds));
+    dt.o_klo = take(n.klo * 4);
+    dt.o_khi = take(n.khi * 4);
+    return o;
+}
+
+void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
+    TableCounts n;
+    if (zp) {
+        n.T = zp->perm.size();
+        n.cul = zp->cu_local.size();
+        n.off = zp->off.size();
+    }
+    if (tp) {
+        n.tiles = zp != nullptr;
+        n.qt = tp->qtiles.size();
+        n.kt = tp->kvtiles.size();
+        n.qoff = tp->q_off.size();
+        n.kvoff = tp->kv_off.size();
+        n.items = tp->items.size();
+        n.bitems = tp->bitems.size();
+        n.qitems = tp->qitems.size();
+        if (!tp->qbounds.empty()) {
+            n.qb = tp->qbounds.size();
+            n.klo = tp->key_lo.size();
+            n.khi = tp->key_hi.size();
+        }
+    }
+    dt.blob.assign(layout_tables(n, dt), 0);
     auto put = [&](size_t at, const void *src, size_t bytes) {
         if (bytes) std::memcpy(dt.blob.data() + at, src, bytes);
     };
@@ -465,6 +493,51 @@ void pack_tables(const ZigzagPlan *zp, const TilePlan *tp, DeviceTables &dt) {
         mark(dt.o_qmask, tp->qtiles, tp->q_tokens);
         mark(dt.o_kvmask, tp->kvtiles, kBN);
     }
+}
+
+ra_status ring_tables_bound(const int32_t *cu, int B, int cp, int mode, int G, int Hkv, bool want_tiles,
+                            bool allgather, size_t *blob_bytes, size_t *n_qtiles) {
+    ra_status st = validate_cu(cu, B, -1);
+    if (st) return st;
+    ZigzagPlan zp;
+    if ((st = build_zigzag(cu, B, cp, mode, zp))) return st;
+    TableCounts n;
+    n.T = zp.perm.size();
+    n.cul = zp.cu_local.size();
+    n.off = zp.off.size();
+    *n_qtiles = 0;
+    if (want_tiles) {
+        if (G < 1 || kBM % G != 0) return fail(RA_ERR_UNSUPPORTED, "GQA group must divide 128");
+        std::vector<Tile> scratch;
+        std::vector<size_t> q_doc((size_t)B, 0);
+        for (int r = 0; r < cp; ++r) {
+            for (int b = 0; b < B; ++b) {
+                const size_t idx = (size_t)r * (B + 1) + b;
+                const int64_t lo = zp.off[r] + zp.cu_local[idx], hi = zp.off[r] + zp.cu_local[idx + 1];
+                scratch.clear();
+                append_tiles(scratch, zp.perm.data(), lo, hi, kBM / G, b);
+                n.qt += scratch.size();
+                q_doc[(size_t)b] += scratch.size();
+                scratch.clear();
+                if (allgather) {
+                    if (r == 0) append_tiles(scratch, nullptr, zp.cu[b], zp.cu[b + 1], kBN, b);
+                } else {
+                    append_tiles(scratch, zp.perm.data(), lo, hi, kBN, b, 1);
+                }
+                n.kt += scratch.size();
+            }
+        }
+        n.tiles = true;
+        n.qoff = n.kvoff = (size_t)cp * (B + 1) + 1;
+        for (size_t q : q_doc) n.items += (q + 1) / 2;  // pairs of a document's query tiles
+        n.items *= (size_t)Hkv;
+        n.bitems = n.kt * (size_t)Hkv;
+        n.qitems = n.qt * (size_t)Hkv;
+        *n_qtiles = n.qt;
+    }
+    DeviceTables dt;
+    *blob_bytes = layout_tables(n, dt);
+    return RA_OK;
 }
 
 std::shared_ptr<RingPlan> get_ring_plan(const int32_t *cu, int B, int cp, int mode, int G, int Hkv,
