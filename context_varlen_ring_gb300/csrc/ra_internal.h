@@ -94,25 +94,36 @@ inline int classify_bounds(const Tile &q, const QBounds &b, const Tile &k) {
 // never decrease inside a document) so do a query tile's lo_min and hi_max.
 // A tile pair is skipped above exactly when one of two monotone tests
 // fails, so the tiles of a segment that a fixed partner visits form one
-// index range, found by two binary searches.
+// index range: two binary searches find it, and for a whole segment of
+// partners in order two pointers that only move forward.
 //
-// KV tiles k[0, n) of one segment that query tile q visits (classify or
-// classify_bounds other than kSkip; qb is q's bounds under interval masks,
-// else null).
-inline int64_t kv_tiles_visited(const Tile &q, const QBounds *qb, const Tile *k, int n, int causal, int window) {
-    if (q.len <= 0 || n <= 0) return 0;
-    // visited iff k.pmin <= hi and k.pmax >= lo
-    int64_t hi = INT64_MAX, lo = INT64_MIN;
-    if (qb) {
-        hi = qb->hi_max;
-        lo = qb->lo_min;
-    } else {
-        if (causal) hi = q.pmax;
-        if (window >= 0) lo = (int64_t)q.pmin - window;
+// For every query tile q[0, nq) of one segment (bounds qb[0, nq) under
+// interval masks, else null), the KV tiles of k[0, nk) (one segment) that
+// it visits (classify or classify_bounds other than kSkip): a tile pair is
+// visited iff k.pmin <= hi and k.pmax >= lo, with hi and lo from the query
+// tile, and along the query tiles both move forward, so two pointers walk
+// each list once.  Writes the counts to out[i * stride] when out is not
+// null; returns their sum.
+inline int64_t kv_tiles_visited_each(const Tile *q, const QBounds *qb, int nq, const Tile *k, int nk, int causal,
+                                     int window, int32_t *out, int stride) {
+    int64_t sum = 0;
+    int b = 0, e = 0;
+    for (int i = 0; i < nq; ++i) {
+        int64_t hi = INT64_MAX, lo = INT64_MIN;
+        if (qb) {
+            hi = qb[i].hi_max;
+            lo = qb[i].lo_min;
+        } else {
+            if (causal) hi = q[i].pmax;
+            if (window >= 0) lo = (int64_t)q[i].pmin - window;
+        }
+        while (e < nk && (int64_t)k[e].pmin <= hi) ++e;
+        while (b < nk && (int64_t)k[b].pmax < lo) ++b;
+        const int c = (q[i].len > 0 && e > b) ? e - b : 0;
+        if (out) out[(size_t)i * stride] = c;
+        sum += c;
     }
-    const Tile *e = std::upper_bound(k, k + n, hi, [](int64_t v, const Tile &t) { return v < (int64_t)t.pmin; });
-    const Tile *b = std::lower_bound(k, k + n, lo, [](const Tile &t, int64_t v) { return (int64_t)t.pmax < v; });
-    return e > b ? (int64_t)(e - b) : 0;
+    return sum;
 }
 
 // Query tiles q[0, n) of one segment (with their bounds qb[0, n) under

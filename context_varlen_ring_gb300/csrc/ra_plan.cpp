@@ -141,21 +141,30 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
     tp.fwd_tile_pairs = 0;
     auto seg_idx = [&](int r, int b) { return r * (B + 1) + b; };
     const bool bounds = !tp.qbounds.empty();
-    // KV tiles [ka, ke) that query tile qi visits
-    auto kv_visits = [&](int qi, int ka, int ke) -> int64_t {
-        return kv_tiles_visited(tp.qtiles[(size_t)qi], bounds ? &tp.qbounds[(size_t)qi] : nullptr,
-                                tp.kvtiles.data() + ka, ke - ka, causal, window);
-    };
+    // vis[qi * cp + s]: the KV tiles of rank s's share of query tile qi's
+    // document that qi visits
+    std::vector<int32_t> vis(tp.qtiles.size() * (size_t)cp, 0);
+    for (int b = 0; b < B; ++b)
+        for (int r = 0; r < cp; ++r) {
+            const int qa = tp.q_off[seg_idx(r, b)], qe = tp.q_off[seg_idx(r, b) + 1];
+            for (int s = 0; s < cp && qe > qa; ++s) {
+                const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
+                kv_tiles_visited_each(tp.qtiles.data() + qa, bounds ? tp.qbounds.data() + qa : nullptr, qe - qa,
+                                      tp.kvtiles.data() + ka, ke - ka, causal, window, vis.data() + (size_t)qa * cp + s,
+                                      cp);
+            }
+        }
+    auto kv_visits = [&](int qi, int s) -> int64_t { return vis[(size_t)qi * cp + s]; };
     // visited KV tiles of query tile qi over the ring steps, and the step
     // range [tf, tl) that holds them
     auto q_visits = [&](int qi, int r, int b, int *tf, int *tl) {
+        (void)b;
         int64_t c = 0;
         *tf = cp;
         *tl = 0;
         for (int t = 0; t < cp; ++t) {
             const int s = ((r - t) % cp + cp) % cp;
-            const int ka = tp.kv_off[seg_idx(s, b)], ke = tp.kv_off[seg_idx(s, b) + 1];
-            const int64_t c_t = kv_visits(qi, ka, ke);
+            const int64_t c_t = kv_visits(qi, s);
             if (c_t) {
                 *tf = std::min(*tf, t);
                 *tl = t + 1;
@@ -170,9 +179,13 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
         int64_t cnt;
     };
     std::vector<QEntry> qs;
-    tp.qitems.reserve(tp.qtiles.size() * (size_t)Hkv);
-    tp.items.reserve((tp.qtiles.size() + (size_t)B) / 2 * (size_t)Hkv + (size_t)Hkv);
-    tp.bitems.reserve(tp.kvtiles.size() * (size_t)Hkv);
+    // One record per tile or tile pair (KV head 0); each pass's item list is
+    // its records sorted and then repeated for every KV head (no cost
+    // depends on the head).
+    std::vector<WorkItem> fwd1, dq1, kv1;
+    fwd1.reserve((tp.qtiles.size() + (size_t)B) / 2 + 1);
+    dq1.reserve(tp.qtiles.size());
+    kv1.reserve(tp.kvtiles.size());
     for (int b = 0; b < B; ++b) {
         // the query tiles of document b on every rank, with their visits
         qs.clear();
@@ -182,10 +195,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
                 const int64_t c = q_visits(qi, r, b, &tf, &tl);
                 qs.push_back(QEntry{qi, r, c});
                 // per-query-tile items of the dQ pass (the tile's own ring order)
-                for (int g = 0; g < Hkv; ++g) {
-                    WorkItem w{qi, -1, g, r, b, tf, tl, (int32_t)std::min<int64_t>(c, INT32_MAX)};
-                    tp.qitems.push_back(w);
-                }
+                dq1.push_back(WorkItem{qi, -1, 0, r, b, tf, tl, (int32_t)std::min<int64_t>(c, INT32_MAX)});
             }
         }
         // Forward items pair the document's query tiles in order of their
@@ -208,8 +218,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
             int tf = cp, tl = 0;
             for (int t = 0; t < cp; ++t) {
                 const int sr = ((r - t) % cp + cp) % cp;
-                const int ka = tp.kv_off[seg_idx(sr, b)], ke = tp.kv_off[seg_idx(sr, b) + 1];
-                const int64_t c_t = kv_visits(i, ka, ke) + (q1 >= 0 ? kv_visits(q1, ka, ke) : 0);
+                const int64_t c_t = kv_visits(i, sr) + (q1 >= 0 ? kv_visits(q1, sr) : 0);
                 if (c_t) {
                     tf = std::min(tf, t);
                     tl = t + 1;
@@ -217,10 +226,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
                 cost += c_t;
             }
             if (tf >= tl) tf = tl = 0;
-            for (int g = 0; g < Hkv; ++g) {
-                WorkItem w{i, q1, g, r, b, tf, tl, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
-                tp.items.push_back(w);
-            }
+            fwd1.push_back(WorkItem{i, q1, 0, r, b, tf, tl, (int32_t)std::min<int64_t>(cost, INT32_MAX)});
             tp.fwd_tile_pairs += cost * Hkv;
         }
     }
@@ -242,22 +248,24 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
                     cost += c_t;
                 }
                 if (tf > tl) tf = tl = 0;
-                for (int g = 0; g < Hkv; ++g) {
-                    WorkItem w{j, -1, g, s, b, tf, tl, (int32_t)std::min<int64_t>(cost, INT32_MAX)};
-                    tp.bitems.push_back(w);
-                }
+                kv1.push_back(WorkItem{j, -1, 0, s, b, tf, tl, (int32_t)std::min<int64_t>(cost, INT32_MAX)});
             }
         }
     }
     // KV head major, then longest-processing-time first within a head: the
     // CTAs resident at any moment read the K/V of one or two heads (tens of
     // MB), which stays in L2, and the launch ends on short items.
-    auto by_cost = [](const WorkItem &a, const WorkItem &b) {
-        if (a.g != b.g) return a.g < b.g;
-        return a.cost > b.cost;
+    auto per_head = [&](std::vector<WorkItem> &one, std::vector<WorkItem> &all) {
+        std::stable_sort(one.begin(), one.end(), [](const WorkItem &a, const WorkItem &b) { return a.cost > b.cost; });
+        all.reserve(one.size() * (size_t)Hkv);
+        for (int g = 0; g < Hkv; ++g)
+            for (WorkItem w : one) {
+                w.g = g;
+                all.push_back(w);
+            }
     };
-    std::stable_sort(tp.items.begin(), tp.items.end(), by_cost);
-    std::stable_sort(tp.qitems.begin(), tp.qitems.end(), by_cost);
+    per_head(fwd1, tp.items);
+    per_head(dq1, tp.qitems);
     // Key-side items: document major (heaviest document first), then KV
     // head, then longest first.  A long document's first KV tile sees every
     // query tile of the document, more work than one head's share of an SM,
@@ -267,13 +275,24 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
     // resident at once read the Q and dO of one or two (document, head)
     // pairs, a smaller set than one head of every document.
     std::vector<int32_t> doc_max(B, 0);
-    for (const WorkItem &w : tp.bitems) doc_max[w.b] = std::max(doc_max[w.b], w.cost);
-    std::stable_sort(tp.bitems.begin(), tp.bitems.end(), [&](const WorkItem &a, const WorkItem &b) {
+    for (const WorkItem &w : kv1) doc_max[w.b] = std::max(doc_max[w.b], w.cost);
+    std::stable_sort(kv1.begin(), kv1.end(), [&](const WorkItem &a, const WorkItem &b) {
         if (doc_max[a.b] != doc_max[b.b]) return doc_max[a.b] > doc_max[b.b];
         if (a.b != b.b) return a.b < b.b;
-        if (a.g != b.g) return a.g < b.g;
         return a.cost > b.cost;
     });
+    tp.bitems.reserve(kv1.size() * (size_t)Hkv);
+    for (size_t a = 0; a < kv1.size();) {
+        size_t e = a;
+        while (e < kv1.size() && kv1[e].b == kv1[a].b) ++e;
+        for (int g = 0; g < Hkv; ++g)
+            for (size_t i = a; i < e; ++i) {
+                WorkItem w = kv1[i];
+                w.g = g;
+                tp.bitems.push_back(w);
+            }
+        a = e;
+    }
 }
 
 ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int window, bool allgather,
@@ -361,10 +380,10 @@ ra_status build_ring_tiles(const ZigzagPlan &zp, int G, int Hkv, int causal, int
                 for (int w = 0; w < 2; ++w)
                     for (int rq = 0; rq < zp.cp; ++rq) {
                         const size_t qi = (size_t)rq * (B + 1) + b;
-                        for (int i = tp.q_off[qi]; i < tp.q_off[qi + 1]; ++i)
-                            vis[w] += kv_tiles_visited(tp.qtiles[(size_t)i],
-                                                       tp.qbounds.empty() ? nullptr : &tp.qbounds[(size_t)i],
-                                                       cand[w].data(), (int)cand[w].size(), causal, window);
+                        const int qa = tp.q_off[qi], qe = tp.q_off[qi + 1];
+                        vis[w] += kv_tiles_visited_each(tp.qtiles.data() + qa,
+                                                        tp.qbounds.empty() ? nullptr : tp.qbounds.data() + qa, qe - qa,
+                                                        cand[w].data(), (int)cand[w].size(), causal, window, nullptr, 1);
                     }
                 if (vis[0] < vis[1]) runs = 1;
             }
