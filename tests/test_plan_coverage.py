@@ -74,6 +74,33 @@ def test_packed_workload_tiling(ra, orc):
     assert _ring_fwd_steps(lens, wl.cp, qtok, pair_sorted=False, cross_rank=False) == 11768
     for st in (ring, ag):
         assert 2 * st["fwd_steps"] >= st["fwd_visited"]
+    assert ag["fwd_capacity"] < ring["fwd_capacity"]
+    assert ref / ag["fwd_capacity"] > 0.9 > ref / ring["fwd_capacity"] > 0.75
+
+
+def test_one_run_tiling_has_the_most_kv_tiles(ra):
+    """The workspace size query counts the KV tiles of the tiling that cuts
+    every rank's share at its chunk boundary (one position run per tile).
+    Whatever a mask or window makes the planner choose per share, its plan
+    has no more KV tiles than that (per-document zigzag, restated here)."""
+    rng = np.random.default_rng(23)
+    for trial in range(12):
+        lens = W.random_doc_lens(rng, int(rng.integers(300, 6000)), 1, 2500)
+        cu = W.cu_seqlens(lens)
+        for cp in (2, 4, 8):
+            one_run = 0
+            for L in (int(x) for x in lens):
+                bnd = [c * L // (2 * cp) for c in range(2 * cp + 1)]
+                for r in range(cp):
+                    sh = list(range(bnd[r], bnd[r + 1])) + list(range(bnd[2 * cp - 1 - r], bnd[2 * cp - r]))
+                    one_run += len(_runs_tiles(sh, 128, 1))
+            cases = [dict(window=w) for w in (-1, 0, 64, 1024)]
+            for kind, par in (("chunked", 200), ("random", 0), ("window", 100)):
+                lo, hi = W.interval_bounds(cu, kind, par, seed=trial)
+                cases.append(dict(key_lo=lo, key_hi=hi))
+            for kw in cases:
+                st = ra.ring_plan_stats(cu, cp, 1, 4, 2, True, sched="fused", **kw)
+                assert st["kv_tiles"] <= one_run, (trial, cp, kw.keys())
 
 
 def _runs_tiles(pos, rows, max_runs=2):
@@ -138,8 +165,6 @@ def _ring_fwd_steps(lens, cp, q_tokens, pair_sorted=True, window=-1, kv_runs=2, 
                 u = need[idx[j]] | (need[idx[j + 1]] if j + 1 < len(idx) else False)
                 steps += int(u.sum())
     return steps
-    assert ag["fwd_capacity"] < ring["fwd_capacity"]
-    assert ref / ag["fwd_capacity"] > 0.9 > ref / ring["fwd_capacity"] > 0.75
 
 
 @pytest.mark.parametrize("window", [-1, 1024, 256, 64])
