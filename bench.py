@@ -565,6 +565,32 @@ def schedule_lines(ra, torch, dev, wl, steps, warmup, peak, q, k, v, do):
     return res
 
 
+def host_planning(ra, torch, dev, wl, q, k, v, n=8):
+    """Host cost of a ring forward on a packing the library has not seen (as
+    in training on a new varlen batch every step): the wall time of the
+    workspace size query plus the forward call, which plans (zigzag split,
+    tiles, work items, table image) and enqueues its kernels; packings of
+    the same total drawn with the same length distribution (seeds 1..n),
+    the device synchronised between calls, outside the timed span."""
+    T, hq, hkv, d = wl.T, wl.hq, wl.hkv, wl.d
+    out = torch.empty_like(q)
+    lse = torch.empty((hq, T), dtype=torch.float32, device=dev)
+    ms = []
+    for seed in range(1, n + 1):
+        cu = W.cu_seqlens(W.loguniform_doc_lens(T, 128, 8192, seed))
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        nb = ra.ring_workspace_bytes(T, hq, hkv, d, 0, cu, wl.cp, wl.zz_mode, "fused", bwd=False)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        ra.ring_attn_fwd(q, k, v, cu, wl.cp, wl.zz_mode, True, wl.scale, "fused", out=out, lse=lse, workspace=ws)
+        ms.append((time.perf_counter() - t0) * 1e3)
+        torch.cuda.synchronize()
+        del ws
+    assert ra.device_status() == 0
+    return {"ms_median": float(np.median(ms)), "ms": ms, "packings": n,
+            "rule": "size query + forward call on a new packing (planning and kernel enqueue), host wall time"}
+
+
 def cpu_configs(args):
     """The fp64 oracle on the host cores, per workload: the 128-token fp32
     batch, the forward of the 8192-token sequence and of the packed
@@ -907,6 +933,7 @@ def main():
                                                 ["prefix:512", "chunked:1024"])
         extras["other_schedules"] = schedule_lines(ra, torch, dev, wl, args.steps, args.warmup, peak_burst,
                                                    q, k, v, do)
+        extras["host_planning"] = host_planning(ra, torch, dev, wl, q, k, v)
         barrier()
 
     # ---- end to end through the public API with host buffers.  Every step
