@@ -157,8 +157,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
     auto kv_visits = [&](int qi, int s) -> int64_t { return vis[(size_t)qi * cp + s]; };
     // visited KV tiles of query tile qi over the ring steps, and the step
     // range [tf, tl) that holds them
-    auto q_visits = [&](int qi, int r, int b, int *tf, int *tl) {
-        (void)b;
+    auto q_visits = [&](int qi, int r, int *tf, int *tl) {
         int64_t c = 0;
         *tf = cp;
         *tl = 0;
@@ -192,7 +191,7 @@ static void build_items(TilePlan &tp, int Hkv, int causal, int window) {
         for (int r = 0; r < cp; ++r) {
             for (int qi = tp.q_off[seg_idx(r, b)]; qi < tp.q_off[seg_idx(r, b) + 1]; ++qi) {
                 int tf, tl;
-                const int64_t c = q_visits(qi, r, b, &tf, &tl);
+                const int64_t c = q_visits(qi, r, &tf, &tl);
                 qs.push_back(QEntry{qi, r, c});
                 // per-query-tile items of the dQ pass (the tile's own ring order)
                 dq1.push_back(WorkItem{qi, -1, 0, r, b, tf, tl, (int32_t)std::min<int64_t>(c, INT32_MAX)});
