@@ -250,3 +250,27 @@ def test_partial_refuses_stream_capture(ra):
     torch.cuda.synchronize()
     _check_status(ra)
     assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])
+
+
+def test_readme_usage_example(ra):
+    """The README's Python example runs as written: the whole ring (8 ranks,
+    per-document zigzag) and one partial over the whole packed buffer (local
+    row index as position, so each document's causal attention) merged alone
+    give the same attention, within the bf16 output tolerance, and the
+    backward returns finite gradients of the inputs' shapes."""
+    cu = [0, 1809, 2202, 2353]
+    g = torch.Generator(device="cuda").manual_seed(3)
+    q = torch.randn(2353, 32, 128, device="cuda", dtype=torch.bfloat16, generator=g)
+    k = torch.randn(2353, 8, 128, device="cuda", dtype=torch.bfloat16, generator=g)
+    v = torch.randn(2353, 8, 128, device="cuda", dtype=torch.bfloat16, generator=g)
+    out, lse = ra.ring_attn_fwd(q, k, v, cu, 8, ra.RA_ZZ_PER_DOC)
+    do = torch.randn(2353, 32, 128, device="cuda", dtype=torch.bfloat16, generator=g)
+    dq, dk, dv = ra.ring_attn_bwd(q, k, v, out, lse, do, cu, 8, ra.RA_ZZ_PER_DOC)
+    o1, l1 = ra.varlen_attn_partial(q, k, v, cu, cu)
+    o, l = ra.lse_merge([o1], [l1], out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert ra.device_status() == 0
+    assert (out.float() - o.float()).abs().max().item() <= TOL[torch.bfloat16][0]
+    assert (lse - l).abs().max().item() <= TOL[torch.bfloat16][1]
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+    assert all(torch.isfinite(t.float()).all().item() for t in (dq, dk, dv))
