@@ -104,8 +104,9 @@ def test_bwd_c4_full_size(ra, orc):
     configuration the benchmark times (fused ring, CP=8, per-document
     zigzag): for every document, two KV heads with their G query heads are
     compared element by element with the oracle -- O and LSE of the forward,
-    dQ, dK and dV of the backward (fp32 gradients) -- at the plain max-abs
-    tolerances (2e-2 on outputs and gradients, 1e-3 on LSE).  Documents do
+    dQ, dK and dV of the backward (fp32 gradients; the bf16 gradients the
+    benchmark writes are checked to be exactly those rounded) -- at the
+    plain max-abs tolerances (2e-2 on outputs and gradients, 1e-3 on LSE).  Documents do
     not attend to each other, so each is its own oracle problem.  The KV
     heads rotate over the documents so that all eight are covered."""
     wl = W.C4
@@ -117,6 +118,13 @@ def test_bwd_c4_full_size(ra, orc):
     out, lse, dq, dk, dv = _run(ra, q, k, v, do, cu, wl.cp, wl.zz_mode, True, "fused")
     out = out.float().cpu().numpy()
     lse = lse.cpu().numpy()
+    # the benchmark's launch writes bf16 gradients: the same kernels with the
+    # bf16 epilogue give exactly the fp32 gradients rounded to bf16 (round to
+    # nearest even), so the parity below holds for that launch as well
+    _, _, dq16, dk16, dv16 = _run(ra, q, k, v, do, cu, wl.cp, wl.zz_mode, True, "fused", grad_dtype=torch.bfloat16)
+    for name, got, f32 in (("dq", dq16, dq), ("dk", dk16, dk), ("dv", dv16, dv)):
+        ref16 = torch.from_numpy(np.ascontiguousarray(f32)).to(torch.bfloat16).float().numpy()
+        assert np.array_equal(got, ref16), name
     report = []
     for bdoc in range(len(cu) - 1):
         a, e = int(cu[bdoc]), int(cu[bdoc + 1])
