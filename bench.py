@@ -235,6 +235,60 @@ def kernel_traffic(name):
     return ent["dram_bytes_per_launch"]
 
 
+# Timing scope -> (kernels whose DRAM bytes it sums, source files it depends on).
+TRAFFIC_SCOPES = {
+    "ra_tc_fwd": (["tc_fwd_kernel"], ["ra_tc_fwd.cu", "ra_dev.cuh", "ra_plan.cpp", "ra_api.cpp"]),
+    "ra_tc_bwd": (["tc_dq_kernel", "tc_dkdv_kernel"], ["ra_tc_bwd.cu", "ra_tc_dq.cu", "ra_api.cpp", "ra_dev.cuh",
+                                                       "ra_plan.cpp"]),
+    "ra_tc_bwd_dkdv": (["tc_dkdv_kernel"], ["ra_tc_bwd.cu", "ra_dev.cuh", "ra_plan.cpp"]),
+    "ra_tc_bwd_dq": (["tc_dq_kernel"], ["ra_tc_dq.cu", "ra_dev.cuh", "ra_plan.cpp"]),
+    "ra_permute_fwd": (["permute_kernel"], ["ra_misc.cu", "ra_dev.cuh", "ra_plan.cpp", "ra_api.cpp"]),
+    "ra_permute_rowdot": (["permute_rowdot_kernel"], ["ra_misc.cu", "ra_dev.cuh", "ra_plan.cpp", "ra_api.cpp"]),
+}
+
+
+def traffic_table(source, profile="profiles/launches_c4_fwd_bwd.md"):
+    """The per-scope DRAM bytes table (profiles/traffic.json) from an ncu
+    launch list of one fwd+bwd step in CSV form (--metrics
+    dram__bytes_read.sum,dram__bytes_write.sum,... --csv; a path, or its
+    lines): per scope, the
+    read + write bytes of its kernels' launches in the list, with the
+    sha256 of every source file the scope depends on at the time of the
+    call.  A launch's kernel is the identifier that its argument list (and
+    template arguments) follow in the demangled name ncu prints."""
+    import csv
+    import hashlib
+    import re
+    src_lines = open(source).read().splitlines() if isinstance(source, str) else list(source)
+    lines = [ln for ln in src_lines if not ln.startswith("==")]
+    rows = list(csv.reader(lines))
+    hdr = rows[0]
+    ident = re.compile(r"([A-Za-z_]\w*)\s*(?:<[^()]*>)?\s*\(")
+    per = {}
+    for r in rows[1:]:
+        d = dict(zip(hdr, r))
+        m = ident.search(d["Kernel Name"])
+        key = (d.get("ID", ""), m.group(1) if m else d["Kernel Name"])
+        per.setdefault(key, {})[d["Metric Name"]] = float(d["Metric Value"].replace(",", ""))
+
+    def bytes_of(kernel):
+        hits = [m for (i, n), m in per.items() if n == kernel]
+        if len(hits) != 1:
+            raise ValueError(f"{kernel}: {len(hits)} launches in the list, expected one")
+        return int(hits[0]["dram__bytes_read.sum"] + hits[0]["dram__bytes_write.sum"])
+
+    csrc = os.path.join(ROOT, "context_varlen_ring_gb300", "csrc")
+    tab = {}
+    for scope, (kernels, files) in TRAFFIC_SCOPES.items():
+        srcs = {}
+        for f in files:
+            with open(os.path.join(csrc, f), "rb") as fh:
+                srcs[f] = hashlib.sha256(fh.read()).hexdigest()
+        tab[scope] = {"sources": srcs, "dram_bytes_per_launch": sum(bytes_of(k) for k in kernels),
+                      "profile": profile}
+    return tab
+
+
 def tensor_roofline(name, ms_per_launch, d, hq, pairs, peak, peak_src):
     """Roofline entry of a tensor-core scope: the method's algorithmic FLOPs
     per launch over the launch's CUDA-event time, against the burst bf16
@@ -775,10 +829,19 @@ def main():
                     help="only the HBM-bound kernels at full size (permute, unpermute, LSE merge): one JSON line")
     ap.add_argument("--merge-parts", type=int, default=0,
                     help="partials merged by --bandwidth (default: the workload's CP size)")
+    ap.add_argument("--traffic-from", default="", metavar="CSV",
+                    help="write profiles/traffic.json from an ncu launch list of one fwd+bwd step (CSV) and "
+                         "exit (host only)")
     ap.add_argument("--fwd-configs", default="",
                     help="comma list of forward-only workloads (e.g. C1,C2,C3) to time instead of the "
                          "fwd+bwd step; one JSON line each (not the headline line)")
     args = ap.parse_args()
+    if args.traffic_from:
+        tab = traffic_table(args.traffic_from)
+        with open(os.path.join(ROOT, "profiles", "traffic.json"), "w") as f:
+            json.dump(tab, f, indent=1)
+        print(json.dumps({k: v["dram_bytes_per_launch"] for k, v in tab.items()}))
+        return
     if args.balance:
         balance_study(args)
         return

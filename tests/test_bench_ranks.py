@@ -122,3 +122,34 @@ def test_flop_count_matches_oracle_pairs(orc):
     r = bench.tensor_roofline("ra_tc_bwd", 3.0, d, hq, 67823768, 1902.4, "measured")
     assert r["frac"] == pytest.approx(2.778e12 / 3.0e-3 / 1e12 / 1902.4, rel=1e-3)
     assert r["executed_frac"] == pytest.approx(r["frac"] * 7 / 5)
+
+
+def test_traffic_table_from_a_launch_list():
+    """bench.py --traffic-from: per timing scope, the DRAM read + write bytes
+    of its kernels' launches in an ncu CSV launch list (the backward pair
+    sums both kernels), with the sha256 of each source file the scope
+    depends on, which kernel_traffic checks before reporting the bytes."""
+    import hashlib
+    hdr = '"ID","Kernel Name","Metric Name","Metric Unit","Metric Value"'
+    kern = {"copy_from_host_kernel(const uint4 *, uint4 *, long, const uint8_t *, uint8_t *, int)": (1, 0),
+            "void ra::permute_kernel<uint4>(ra::PermJobs, const int *, long, int, int *)": (70, 20),
+            "void ra::(anonymous namespace)::tc_fwd_kernel<0>(ra::(anonymous namespace)::FwdParams)": (400, 200),
+            "void ra::permute_rowdot_kernel(ra::PermJobs, const void *, void *, const void *, float *)": (500, 30),
+            "void unnamed>::tc_dq_kernel<0>(unnamed>::DqParams)": (700, 250),
+            "void unnamed>::tc_dkdv_kernel<0>(unnamed>::BwdParams)": (800, 120)}
+    lines = ["==PROF== Connected to process 1", hdr]
+    for i, (name, (rd, wr)) in enumerate(kern.items()):
+        lines.append(f'"{i}","{name}","dram__bytes_read.sum","byte","{rd * 1_000_000:,}"')
+        lines.append(f'"{i}","{name}","dram__bytes_write.sum","byte","{wr * 1_000_000}"')
+        lines.append(f'"{i}","{name}","gpu__time_duration.sum","us","12.5"')
+    tab = bench.traffic_table(lines)
+    mb = {k: v["dram_bytes_per_launch"] // 1_000_000 for k, v in tab.items()}
+    assert mb == {"ra_tc_fwd": 600, "ra_tc_bwd": 950 + 920, "ra_tc_bwd_dkdv": 920, "ra_tc_bwd_dq": 950,
+                  "ra_permute_fwd": 90, "ra_permute_rowdot": 530}
+    csrc = os.path.join(bench.ROOT, "context_varlen_ring_gb300", "csrc")
+    for ent in tab.values():
+        for f, h in ent["sources"].items():
+            assert h == hashlib.sha256(open(os.path.join(csrc, f), "rb").read()).hexdigest()
+    # a kernel missing from the list is an error, not a silent zero
+    with pytest.raises(ValueError):
+        bench.traffic_table([ln for ln in lines if "tc_dq_kernel" not in ln])
