@@ -264,7 +264,9 @@ ra_status ra_lse_merge(int n_parts, const float *const *outs, const float *const
  * workspace: DEVICE, >= ra_ring_workspace_bytes(...) for the same arguments
  * (the size holds for every causal and window setting: the planner's KV
  * tiling, which the mask selects, only changes the size of its tables and
- * the size covers both tilings).
+ * the size covers every tiling).  ra_ring_workspace_bytes counts tiles on
+ * the host (well under a millisecond for 32768 tokens) and keeps no state;
+ * it returns 0 for invalid arguments.
  * On the tensor-core path (bf16, d = 128) the kernels read every tile whose
  * rows form one position run straight from q, k, v (and dout), and the
  * workspace receives rank-ordered copies of the rows of the other tiles
